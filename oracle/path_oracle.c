@@ -1,0 +1,281 @@
+/*
+ * PaTH attention oracle: plain fp64 CPU code, written straight from the
+ * definition of the method.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only tests/, the package's smoke() check and the
+ * CPU-baseline leg of bench.py may load this library. The CUDA product path
+ * shares no code with it and never calls it.
+ *
+ * Sources (web pages on PaTH attention):
+ *  [KO] "거리에서 경로로, PaTH Attention" (iplexlaw.co.kr review),
+ *       §3 핵심 원리 (per-token H = I - beta w w^T; logit k_j^T(H_{j+1}...H_i)q_i,
+ *       order matters), §4 (softmax over the logits, weighted sum of V,
+ *       PaTH-FoX adds a forget gate), §9 (decode updates the cached keys in place).
+ *  [JA] "技術要約: PaTH Attention" (gist.science), §2 手法 "コアメカニズム"
+ *       (logit formula, product s = j+1..i, H_s = I - beta_s w_s w_s^T),
+ *       §2 "拡張: PaTH-FoX" (additive data-dependent forget gate),
+ *       §3 "推論" (in-place key update with the current transition).
+ *
+ * Readings where the pages are silent (same list as the design notes):
+ *  - softmax scale sigma multiplies the whole PaTH logit; the FoX bias
+ *    sum_{s=j+1..i} log f_s is added after scaling, unscaled;
+ *  - the product covers s = j+1..i: H_i is applied to q_i first, H_j is not
+ *    applied; j = i uses the identity; the attention is causal (j <= i);
+ *  - decode step t with N cached keys: first k_j <- H_t k_j for every j < N,
+ *    then append (k_t, v_t) untransformed, then attend with q_t over N+1 keys.
+ *
+ * Every function computes the definition directly: no blocking, no UT
+ * transform, no fusion. Cost O(L^2 d) per head.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* x <- H x with H = I - beta w w^T  ([KO] §3, [JA] §2 "データ依存の遷移行列"). */
+static void apply_transition(double *x, const double *w, double beta, int d)
+{
+    double dot = 0.0;
+    for (int c = 0; c < d; ++c)
+        dot += w[c] * x[c];
+    const double a = beta * dot;
+    for (int c = 0; c < d; ++c)
+        x[c] -= a * w[c];
+}
+
+/*
+ * Logits of query row i against keys j = i, i-1, ..., 0 of one head:
+ *   logit[j] = scale * k_j^T (H_{j+1} ... H_i) q_i  [+ sum_{s=j+1..i} log f_s]
+ * The running vector x starts at q_i; once key j is scored, H_j is applied so
+ * that x = H_j ... H_i q_i when key j-1 is scored ([JA] §2 formula; [KO] §3).
+ */
+static void row_logits(const double *q_i, const double *K, const double *W,
+                       const double *beta, const double *log_f, int i, int d,
+                       double scale, double *logit, double *x)
+{
+    memcpy(x, q_i, (size_t)d * sizeof(double));
+    double bias = 0.0;
+    for (int j = i; j >= 0; --j) {
+        const double *k_j = K + (size_t)j * d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += k_j[c] * x[c];
+        logit[j] = scale * dot + bias;
+        apply_transition(x, W + (size_t)j * d, beta[j], d);
+        if (log_f)
+            bias += log_f[j];
+    }
+}
+
+/* Causal softmax over logit[0..n-1] and the weighted sum of V rows ([KO] §4). */
+static void softmax_combine(const double *logit, const double *V, int n, int d,
+                            double *p, double *out, double *lse)
+{
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j)
+        if (logit[j] > m)
+            m = logit[j];
+    double z = 0.0;
+    for (int j = 0; j < n; ++j) {
+        p[j] = exp(logit[j] - m);
+        z += p[j];
+    }
+    for (int c = 0; c < d; ++c)
+        out[c] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        const double pj = p[j] / z;
+        const double *v_j = V + (size_t)j * d;
+        for (int c = 0; c < d; ++c)
+            out[c] += pj * v_j[c];
+    }
+    if (lse)
+        *lse = m + log(z);
+}
+
+/* ---------------------------------------------------------------- threads */
+
+typedef struct {
+    const double *q, *k, *v, *w, *beta, *log_f;
+    int L, d;
+    double scale;
+    const int64_t *rows; /* (head, i) pairs, or NULL for every row */
+    int64_t nrows;
+    double *out, *lse;
+    int64_t next; /* shared work counter */
+    pthread_mutex_t mu;
+} fwd_job;
+
+static int64_t take(fwd_job *job, int64_t chunk)
+{
+    pthread_mutex_lock(&job->mu);
+    int64_t r = job->next;
+    job->next += chunk;
+    pthread_mutex_unlock(&job->mu);
+    return r;
+}
+
+static void *fwd_worker(void *arg)
+{
+    fwd_job *job = (fwd_job *)arg;
+    const int L = job->L, d = job->d;
+    double *logit = (double *)malloc((size_t)L * sizeof(double));
+    double *p = (double *)malloc((size_t)L * sizeof(double));
+    double *x = (double *)malloc((size_t)d * sizeof(double));
+    for (;;) {
+        const int64_t start = take(job, 16);
+        if (start >= job->nrows)
+            break;
+        const int64_t stop = start + 16 < job->nrows ? start + 16 : job->nrows;
+        for (int64_t r = start; r < stop; ++r) {
+            int64_t head, i;
+            if (job->rows) {
+                head = job->rows[2 * r];
+                i = job->rows[2 * r + 1];
+            } else {
+                head = r / L;
+                i = r % L;
+            }
+            const size_t hb = (size_t)head * L;
+            row_logits(job->q + (hb + i) * d, job->k + hb * d, job->w + hb * d,
+                       job->beta + hb, job->log_f ? job->log_f + hb : NULL,
+                       (int)i, d, job->scale, logit, x);
+            softmax_combine(logit, job->v + hb * d, (int)i + 1, d, p,
+                            job->out + (size_t)r * d,
+                            job->lse ? job->lse + r : NULL);
+        }
+    }
+    free(logit);
+    free(p);
+    free(x);
+    return NULL;
+}
+
+static int resolve_threads(int nthreads)
+{
+    if (nthreads > 0)
+        return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static void run_job(fwd_job *job, int nthreads)
+{
+    nthreads = resolve_threads(nthreads);
+    pthread_mutex_init(&job->mu, NULL);
+    job->next = 0;
+    pthread_t *tid = (pthread_t *)malloc((size_t)nthreads * sizeof(pthread_t));
+    for (int t = 0; t < nthreads; ++t)
+        pthread_create(&tid[t], NULL, fwd_worker, job);
+    for (int t = 0; t < nthreads; ++t)
+        pthread_join(tid[t], NULL);
+    free(tid);
+    pthread_mutex_destroy(&job->mu);
+}
+
+/* ---------------------------------------------------------------- exports */
+
+/*
+ * Full forward. Tensors are contiguous (nh, L, d) with nh = B*H heads;
+ * beta and log_f are (nh, L); log_f may be NULL (plain PaTH) or the per-token
+ * log forget gate (PaTH-FoX). out is (nh, L, d); lse (nh, L) may be NULL.
+ * nthreads <= 0 uses every online core. Returns the thread count used.
+ */
+int oracle_path_fwd(const double *q, const double *k, const double *v,
+                    const double *w, const double *beta, const double *log_f,
+                    int nh, int L, int d, double scale, double *out, double *lse,
+                    int nthreads)
+{
+    fwd_job job = {q, k, v, w, beta, log_f, L, d, scale, NULL,
+                   (int64_t)nh * L, out, lse, 0};
+    run_job(&job, nthreads);
+    return resolve_threads(nthreads);
+}
+
+/*
+ * The same forward for a list of sampled rows: rows holds nrows pairs
+ * (head, i); out is (nrows, d), lse (nrows). Costs O(i d) per row, so it can
+ * check sampled outputs of workloads too large for the full forward.
+ */
+int oracle_path_rows(const double *q, const double *k, const double *v,
+                     const double *w, const double *beta, const double *log_f,
+                     int nh, int L, int d, double scale, const int64_t *rows,
+                     int64_t nrows, double *out, double *lse, int nthreads)
+{
+    (void)nh;
+    fwd_job job = {q, k, v, w, beta, log_f, L, d, scale, rows, nrows, out, lse, 0};
+    run_job(&job, nthreads);
+    return resolve_threads(nthreads);
+}
+
+/* Full logit matrix of one head: logits[i*L + j] for j <= i, -inf above. */
+void oracle_path_logits(const double *q, const double *k, const double *w,
+                        const double *beta, const double *log_f, int L, int d,
+                        double scale, double *logits)
+{
+    double *x = (double *)malloc((size_t)d * sizeof(double));
+    for (int i = 0; i < L; ++i) {
+        double *row = logits + (size_t)i * L;
+        row_logits(q + (size_t)i * d, k, w, beta, log_f, i, d, scale, row, x);
+        for (int j = i + 1; j < L; ++j)
+            row[j] = -INFINITY;
+    }
+    free(x);
+}
+
+/*
+ * The transport used for every logit: x = H_{j+1} ... H_i q for one head,
+ * applying H_i first. Exposed so that tests can pin its invariants.
+ */
+void oracle_path_transport(const double *q, const double *w, const double *beta,
+                           int i, int j, int d, double *x)
+{
+    memcpy(x, q, (size_t)d * sizeof(double));
+    for (int s = i; s > j; --s)
+        apply_transition(x, w + (size_t)s * d, beta[s], d);
+}
+
+/*
+ * One decode step for nh independent heads ([KO] §9, [JA] §3 "推論"):
+ *   k_j <- H_t k_j for every cached j < len (in place in the fp64 cache),
+ *   append k_t, v_t at index len, then attend with q_t over len+1 keys.
+ * Kc, Vc are (nh, cap, d); q, k, v, w are (nh, d); beta (nh); out (nh, d).
+ * log_f (nh) may be NULL; with it the cache keeps per-key running biases in
+ * cbias (nh, cap): cbias_j <- cbias_j + log f_t for j < len, cbias_len = 0,
+ * so that key j carries sum_{s=j+1..t} log f_s.
+ */
+void oracle_path_decode_step(const double *q, const double *k, const double *v,
+                             const double *w, const double *beta,
+                             const double *log_f, double *Kc, double *Vc,
+                             double *cbias, int nh, int len, int cap, int d,
+                             double scale, double *out)
+{
+    double *logit = (double *)malloc((size_t)(len + 1) * sizeof(double));
+    double *p = (double *)malloc((size_t)(len + 1) * sizeof(double));
+    for (int h = 0; h < nh; ++h) {
+        double *K = Kc + (size_t)h * cap * d;
+        double *V = Vc + (size_t)h * cap * d;
+        const double *w_t = w + (size_t)h * d;
+        for (int j = 0; j < len; ++j)
+            apply_transition(K + (size_t)j * d, w_t, beta[h], d);
+        memcpy(K + (size_t)len * d, k + (size_t)h * d, (size_t)d * sizeof(double));
+        memcpy(V + (size_t)len * d, v + (size_t)h * d, (size_t)d * sizeof(double));
+        if (log_f) {
+            double *cb = cbias + (size_t)h * cap;
+            for (int j = 0; j < len; ++j)
+                cb[j] += log_f[h];
+            cb[len] = 0.0;
+        }
+        const double *q_t = q + (size_t)h * d;
+        for (int j = 0; j <= len; ++j) {
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c)
+                dot += q_t[c] * K[(size_t)j * d + c];
+            logit[j] = scale * dot + (log_f ? cbias[(size_t)h * cap + j] : 0.0);
+        }
+        softmax_combine(logit, V, len + 1, d, p, out + (size_t)h * d, NULL);
+    }
+    free(logit);
+    free(p);
+}

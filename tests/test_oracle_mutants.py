@@ -1,0 +1,98 @@
+"""Plants plausible mistakes in copies of the oracle and checks that the pins catch them.
+
+Each mutant is path_oracle.c with one textual change (a dropped term, a wrong sign, a
+shifted index, a step in the wrong order), compiled on the CPU into a temporary
+library. The pins of test_oracle_pins.py then run against it, and at least one must
+fail. The real oracle is restored afterwards.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import build as oracle_build
+from tests import test_oracle_pins as pins
+
+SRC = oracle_build.SRC
+
+MUTANTS = {
+    "transition_sign": ("x[c] -= a * w[c];", "x[c] += a * w[c];"),
+    "beta_dropped": ("const double a = beta * dot;", "const double a = dot;"),
+    "transition_index_shifted": (
+        "apply_transition(x, W + (size_t)j * d, beta[j], d);",
+        "apply_transition(x, W + (size_t)(j > 0 ? j - 1 : 0) * d, beta[j > 0 ? j - 1 : 0], d);"),
+    "transition_before_score": (
+        "        logit[j] = scale * dot + bias;\n        apply_transition(x, W + (size_t)j * d, beta[j], d);",
+        "        apply_transition(x, W + (size_t)j * d, beta[j], d);\n"
+        "        dot = 0.0;\n        for (int c = 0; c < d; ++c)\n            dot += k_j[c] * x[c];\n"
+        "        logit[j] = scale * dot + bias;"),
+    "scale_dropped": ("logit[j] = scale * dot + bias;", "logit[j] = dot + bias;"),
+    "gate_scaled": ("logit[j] = scale * dot + bias;", "logit[j] = scale * (dot + bias);"),
+    "gate_range_includes_j": ("logit[j] = scale * dot + bias;",
+                              "logit[j] = scale * dot + bias + (log_f ? log_f[j] : 0.0);"),
+    "lse_without_max": ("*lse = m + log(z);", "*lse = log(z);"),
+    "softmax_not_normalised": ("const double pj = p[j] / z;", "const double pj = p[j];"),
+    "decode_skips_last_key": ("for (int j = 0; j < len; ++j)\n            apply_transition(K",
+                              "for (int j = 0; j + 1 < len; ++j)\n            apply_transition(K"),
+    "decode_transforms_new_key": (
+        "        for (int j = 0; j < len; ++j)\n            apply_transition(K + (size_t)j * d, w_t, beta[h], d);\n"
+        "        memcpy(K + (size_t)len * d, k + (size_t)h * d, (size_t)d * sizeof(double));",
+        "        memcpy(K + (size_t)len * d, k + (size_t)h * d, (size_t)d * sizeof(double));\n"
+        "        for (int j = 0; j <= len; ++j)\n            apply_transition(K + (size_t)j * d, w_t, beta[h], d);"),
+    "decode_gate_on_new_key": ("cb[len] = 0.0;", "cb[len] = log_f[h];"),
+}
+
+
+def run_all_pins():
+    """Runs every pin; returns the names of those that failed."""
+    failed = []
+    checks = [
+        ("hand", pins.test_hand_example_logits_outputs_and_fox, ()),
+        ("beta0", pins.test_beta_zero_is_causal_softmax_attention, (37, 8)),
+        ("diag", pins.test_diagonal_logit_is_plain_dot_product, ()),
+        ("brute", pins.test_brute_force_explicit_matrices, (9, 8)),
+        ("repeat", pins.test_repeated_transition_closed_form, ()),
+        ("norm", pins.test_reflections_preserve_norm_and_general_beta_contracts, ()),
+        ("order", pins.test_order_of_transitions_matters, ()),
+        ("fox", pins.test_fox_reductions, ()),
+        ("decode", pins.test_decode_from_empty_cache_matches_prefill, (False,)),
+        ("decode_fox", pins.test_decode_from_empty_cache_matches_prefill, (True,)),
+        ("rows", pins.test_sampled_rows_match_full_forward, ()),
+    ]
+    for name, fn, args in checks:
+        try:
+            with np.errstate(all="ignore"):
+                fn(*args)
+        except AssertionError:
+            failed.append(name)
+    return failed
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, mutant_dir):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, "mutation site not found exactly once"
+    src = os.path.join(mutant_dir, name + ".c")
+    lib = os.path.join(mutant_dir, "lib" + name + ".so")
+    with open(src, "w") as f:
+        f.write(text.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread", src, "-o", lib,
+                    "-lm"], check=True)
+    prev = oracle.swap_library(lib)
+    try:
+        failed = run_all_pins()
+    finally:
+        oracle.restore_library(prev)
+    assert failed, "no pin caught mutant %s" % name
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert run_all_pins() == []
