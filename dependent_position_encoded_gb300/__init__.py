@@ -1,0 +1,266 @@
+"""GB300 (sm_103a) PaTH attention.
+
+A thin Python binding over ``libpath_attn.so``, whose C ABI is declared in
+``include/path_attn.h``. Every step of the computation runs in the library's
+CUDA kernels; this module only checks tensor arguments, allocates outputs and
+workspaces with PyTorch (device memory and streams are PyTorch's job here) and
+passes raw pointers. There is no CPU fallback: without the built library or a
+CUDA device every call raises.
+
+Entry points keep the C names: ``path_attn_fwd``, ``path_fox_fwd``,
+``path_fwd_prepare``, ``path_fwd_scan``, ``path_decode_step``,
+``path_workspace_bytes``, ``path_check_workspace``, ``path_status_string``.
+"""
+import ctypes
+import math
+import os
+
+from . import build as _build
+
+# status codes and enums, mirroring include/path_attn.h
+OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CAPACITY, ERR_TIMEOUT, \
+    ERR_CUDA, ERR_ARG = range(10)
+F32, BF16 = 0, 1
+OP_FWD, OP_FOX_FWD, OP_DECODE = 0, 1, 2
+HEAD_DIM = 64
+
+EXPORTED = ("path_workspace_bytes", "path_attn_fwd", "path_fox_fwd", "path_fwd_prepare",
+            "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string")
+
+_lib = None
+
+
+class PathError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s" % (where, path_status_string(code)))
+
+
+def library_path():
+    return _build.LIB
+
+
+def ensure_built():
+    """Builds libpath_attn.so if it is missing or older than its sources."""
+    if not _build.up_to_date():
+        _build.build()
+    return _build.LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libpath_attn.so is not built; run dependent_position_encoded_gb300."
+                           "build.build() (or __graft_entry__.build())")
+    lib = ctypes.CDLL(_build.LIB)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.path_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.path_workspace_bytes.restype = S
+    lib.path_attn_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P, S, P]
+    lib.path_attn_fwd.restype = I
+    lib.path_fox_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, S, P]
+    lib.path_fox_fwd.restype = I
+    lib.path_fwd_prepare.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, S, P]
+    lib.path_fwd_prepare.restype = I
+    lib.path_fwd_scan.argtypes = [P, P, P, I, I, I, I, I, I, F, P, S, P]
+    lib.path_fwd_scan.restype = I
+    lib.path_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, S, P]
+    lib.path_decode_step.restype = I
+    lib.path_check_workspace.argtypes = [P, P]
+    lib.path_check_workspace.restype = I
+    lib.path_status_string.argtypes = [I]
+    lib.path_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def path_status_string(code):
+    return _load().path_status_string(int(code)).decode()
+
+
+def _check(code, where):
+    if code != OK:
+        raise PathError(code, where)
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("unsupported dtype %s (bfloat16 or float32)" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda_tensor(t, name, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def path_workspace_bytes(op, B, H, L, d=HEAD_DIM, dtype=BF16):
+    return int(_load().path_workspace_bytes(int(op), int(B), int(H), int(L), int(d), int(dtype)))
+
+
+def new_workspace(op, B, H, L, dtype, device):
+    """A device workspace sized by path_workspace_bytes (256-byte aligned by PyTorch)."""
+    torch = _torch()
+    n = path_workspace_bytes(op, B, H, L, HEAD_DIM, dtype)
+    if n == 0:
+        raise PathError(ERR_SHAPE, "path_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _fwd_args(q, k, v, w, beta):
+    torch = _torch()
+    _cuda_tensor(q, "q")
+    dt = q.dtype
+    for t, n in ((k, "k"), (v, "v"), (w, "w")):
+        _cuda_tensor(t, n, dt)
+        if t.shape != q.shape:
+            raise ValueError("%s has shape %s, expected %s" % (n, tuple(t.shape), tuple(q.shape)))
+    if q.dim() != 4:
+        raise ValueError("q must be (B, H, L, d)")
+    B, H, L, d = q.shape
+    _cuda_tensor(beta, "beta", torch.float32)
+    if beta.shape != (B, H, L):
+        raise ValueError("beta must be (B, H, L) float32")
+    return B, H, L, d, _dtype_code(q)
+
+
+def _outputs(q, out, lse, B, H, L):
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_tensor(out, "out", q.dtype)
+    if lse is True:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    elif lse is not None and lse is not False:
+        _cuda_tensor(lse, "lse", torch.float32)
+    else:
+        lse = None
+    return out, lse
+
+
+def path_attn_fwd(q, k, v, w, beta, out=None, lse=True, scale=None, workspace=None, stream=None):
+    """PaTH forward; returns (out, lse or None). lse=True allocates it, None skips it."""
+    B, H, L, d, dt = _fwd_args(q, k, v, w, beta)
+    out, lse = _outputs(q, out, lse, B, H, L)
+    if workspace is None:
+        workspace = new_workspace(OP_FWD, B, H, L, dt, q.device)
+    _check(_load().path_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(out),
+                                 _ptr(lse), B, H, L, d, dt, _scale(scale, d), _ptr(workspace),
+                                 workspace.numel(), _stream(stream, q.device)), "path_attn_fwd")
+    return out, lse
+
+
+def path_fox_fwd(q, k, v, w, beta, log_f, out=None, lse=True, scale=None, workspace=None,
+                 stream=None):
+    """PaTH-FoX forward; returns (out, lse or None)."""
+    torch = _torch()
+    B, H, L, d, dt = _fwd_args(q, k, v, w, beta)
+    _cuda_tensor(log_f, "log_f", torch.float32)
+    if log_f.shape != (B, H, L):
+        raise ValueError("log_f must be (B, H, L) float32")
+    out, lse = _outputs(q, out, lse, B, H, L)
+    if workspace is None:
+        workspace = new_workspace(OP_FOX_FWD, B, H, L, dt, q.device)
+    _check(_load().path_fox_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
+                                _ptr(out), _ptr(lse), B, H, L, d, dt, _scale(scale, d),
+                                _ptr(workspace), workspace.numel(), _stream(stream, q.device)),
+           "path_fox_fwd")
+    return out, lse
+
+
+def path_fwd_prepare(q, k, w, beta, workspace, log_f=None, scale=None, stream=None):
+    """First stage (UT preprocessing) into `workspace`."""
+    torch = _torch()
+    B, H, L, d, dt = _fwd_args(q, k, q, w, beta)
+    if log_f is not None:
+        _cuda_tensor(log_f, "log_f", torch.float32)
+    _check(_load().path_fwd_prepare(_ptr(q), _ptr(k), _ptr(w), _ptr(beta), _ptr(log_f), B, H, L,
+                                    d, dt, _scale(scale, d), _ptr(workspace), workspace.numel(),
+                                    _stream(stream, q.device)), "path_fwd_prepare")
+
+
+def path_fwd_scan(v, workspace, out=None, lse=True, fox=False, scale=None, stream=None):
+    """Second stage (block scan) from `workspace`; returns (out, lse or None)."""
+    _cuda_tensor(v, "v")
+    B, H, L, d = v.shape
+    dt = _dtype_code(v)
+    out, lse = _outputs(v, out, lse, B, H, L)
+    _check(_load().path_fwd_scan(_ptr(v), _ptr(out), _ptr(lse), int(bool(fox)), B, H, L, d, dt,
+                                 _scale(scale, d), _ptr(workspace), workspace.numel(),
+                                 _stream(stream, v.device)), "path_fwd_scan")
+    return out, lse
+
+
+def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, out=None,
+                     workspace=None, stream=None):
+    """One decode step: updates k_cache in place, appends (k, v) at cache_len and returns
+    the attention output (B, H, d). q, k, v, w: (B, H, d) (a trailing length-1 axis is
+    accepted); beta: (B, H); caches: (B, H, cap, d)."""
+    torch = _torch()
+    _cuda_tensor(k_cache, "k_cache")
+    dt_t = k_cache.dtype
+    B, H, cap, d = k_cache.shape
+    _cuda_tensor(v_cache, "v_cache", dt_t)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("v_cache must match k_cache")
+    ins = []
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (w, "w")):
+        _cuda_tensor(t, n, dt_t)
+        if t.numel() != B * H * d:
+            raise ValueError("%s must hold (B, H, d) values" % n)
+        ins.append(t)
+    _cuda_tensor(beta, "beta", torch.float32)
+    if beta.numel() != B * H:
+        raise ValueError("beta must hold (B, H) values")
+    if out is None:
+        out = torch.empty((B, H, d), dtype=dt_t, device=k_cache.device)
+    else:
+        _cuda_tensor(out, "out", dt_t)
+    if workspace is None:
+        workspace = new_workspace(OP_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device)
+    _check(_load().path_decode_step(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]), _ptr(ins[3]),
+                                    _ptr(beta), _ptr(k_cache), _ptr(v_cache), B, H,
+                                    int(cache_len), cap, d, _dtype_code(k_cache),
+                                    _scale(scale, d), _ptr(out), _ptr(workspace),
+                                    workspace.numel(), _stream(stream, k_cache.device)),
+           "path_decode_step")
+    return out
+
+
+def path_check_workspace(workspace, stream=None):
+    """Synchronises the stream and returns the status code left by kernels in `workspace`."""
+    return int(_load().path_check_workspace(_ptr(workspace), _stream(stream, workspace.device)))

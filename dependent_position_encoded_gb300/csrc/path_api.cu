@@ -1,0 +1,216 @@
+// Host side of the C ABI declared in include/path_attn.h: argument checks (synchronous,
+// before any launch), workspace sizing and kernel dispatch on the caller's stream.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "path_attn.h"
+
+namespace path {
+size_t ut_prepare_smem_bytes();
+template <typename T>
+cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const float *beta,
+                              const float *log_f, int BH, int L, float scale, void *ws,
+                              cudaStream_t stream);
+cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int BH, int L,
+                           float scale, void *ws, uint64_t limit_ns, int force_timeout,
+                           cudaStream_t stream);
+cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int BH, int L,
+                            float scale, void *ws, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *w,
+                          const float *beta, void *k_cache, void *v_cache, int BH, int cache_len,
+                          int cap, float scale, void *out, void *ws, cudaStream_t stream);
+}  // namespace path
+
+namespace {
+
+using namespace path;
+
+// Bounded waits inside the tensor-core scan give up after this long.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Test hook: PATH_ATTN_DEBUG_FORCE_TIMEOUT=1 makes the scan's MMA lane wait on a barrier
+// that nothing arrives at, with a 2 ms limit, to exercise the timeout path without a fault.
+constexpr uint64_t kDebugWaitLimitNs = 2000000ull;
+
+bool debug_force_timeout() {
+    const char *e = std::getenv("PATH_ATTN_DEBUG_FORCE_TIMEOUT");
+    return e != nullptr && e[0] == '1';
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elt_bytes(int dtype) { return dtype == PATH_BF16 ? 2 : 4; }
+
+path_status check_sizes(int B, int H, int L, int d, int dtype) {
+    if (B < 0 || H < 0 || L < 0) return PATH_ERR_SHAPE;
+    if (d != kD) return PATH_ERR_SHAPE;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_DTYPE;
+    if ((long long)B * H > PATH_MAX_HEADS || L > PATH_MAX_LEN) return PATH_ERR_SHAPE;
+    return PATH_OK;
+}
+
+path_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA; }
+
+path_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+    if (ws == nullptr) return PATH_ERR_NULL;
+    if (!aligned(ws, 256)) return PATH_ERR_ALIGN;
+    if (ws_bytes < need) return PATH_ERR_WORKSPACE;
+    return PATH_OK;
+}
+
+path_status prepare_impl(const void *q, const void *k, const void *w, const float *beta,
+                         const float *log_f, bool fox, int B, int H, int L, int d, int dtype,
+                         float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if (!std::isfinite(scale)) return PATH_ERR_ARG;
+    if ((long long)B * H * L == 0) return PATH_OK;
+    if (!q || !k || !w || !beta || (fox && !log_f)) return PATH_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 16) || !aligned(beta, 16) ||
+        (fox && !aligned(log_f, 16)))
+        return PATH_ERR_ALIGN;
+    const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
+    if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
+    const float *lf = fox ? log_f : nullptr;
+    if (dtype == PATH_BF16)
+        return from_cuda(launch_ut_prepare<__nv_bfloat16>(q, k, w, beta, lf, B * H, L, scale, ws,
+                                                          stream));
+    return from_cuda(launch_ut_prepare<float>(q, k, w, beta, lf, B * H, L, scale, ws, stream));
+}
+
+path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int H, int L, int d,
+                      int dtype, float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if (!std::isfinite(scale)) return PATH_ERR_ARG;
+    if ((long long)B * H * L == 0) return PATH_OK;
+    if (!v || !out) return PATH_ERR_NULL;
+    if (!aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16))) return PATH_ERR_ALIGN;
+    const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
+    if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
+    if (dtype == PATH_BF16) {
+        const bool force = debug_force_timeout();
+        cudaError_t e = launch_scan_tc(v, out, lse, fox, B * H, L, scale, ws,
+                                       force ? kDebugWaitLimitNs : kWaitLimitNs, force ? 1 : 0,
+                                       stream);
+        return from_cuda(e);
+    }
+    return from_cuda(launch_scan_f32(v, out, lse, fox, B * H, L, scale, ws, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
+    if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+    switch (op) {
+        case PATH_OP_FWD: return fwd_layout(B, H, L, elt_bytes(dtype), false).total;
+        case PATH_OP_FOX_FWD: return fwd_layout(B, H, L, elt_bytes(dtype), true).total;
+        case PATH_OP_DECODE: return decode_ws_bytes(B, H, L);
+        default: return 0;
+    }
+}
+
+path_status path_fwd_prepare(const void *q, const void *k, const void *w, const float *beta,
+                             const float *log_f, int B, int H, int L, int d, int dtype,
+                             float scale, void *ws, size_t ws_bytes, void *stream) {
+    return prepare_impl(q, k, w, beta, log_f, log_f != nullptr, B, H, L, d, dtype, scale, ws,
+                        ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, int H, int L,
+                          int d, int dtype, float scale, void *ws, size_t ws_bytes,
+                          void *stream) {
+    return scan_impl(v, out, lse, fox != 0, B, H, L, d, dtype, scale, ws, ws_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+path_status path_attn_fwd(const void *q, const void *k, const void *v, const void *w,
+                          const float *beta, void *out, float *lse, int B, int H, int L, int d,
+                          int dtype, float scale, void *ws, size_t ws_bytes, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every argument of both stages is checked before the first launch
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if ((long long)B * H * L > 0) {
+        if (!v || !out) return PATH_ERR_NULL;
+        if (!aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16)))
+            return PATH_ERR_ALIGN;
+    }
+    st = prepare_impl(q, k, w, beta, nullptr, false, B, H, L, d, dtype, scale, ws, ws_bytes, s);
+    if (st != PATH_OK) return st;
+    return scan_impl(v, out, lse, false, B, H, L, d, dtype, scale, ws, ws_bytes, s);
+}
+
+path_status path_fox_fwd(const void *q, const void *k, const void *v, const void *w,
+                         const float *beta, const float *log_f, void *out, float *lse, int B,
+                         int H, int L, int d, int dtype, float scale, void *ws, size_t ws_bytes,
+                         void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if ((long long)B * H * L > 0) {
+        if (!v || !out || !log_f) return PATH_ERR_NULL;
+        if (!aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16)))
+            return PATH_ERR_ALIGN;
+    }
+    st = prepare_impl(q, k, w, beta, log_f, true, B, H, L, d, dtype, scale, ws, ws_bytes, s);
+    if (st != PATH_OK) return st;
+    return scan_impl(v, out, lse, true, B, H, L, d, dtype, scale, ws, ws_bytes, s);
+}
+
+path_status path_decode_step(const void *q, const void *k, const void *v, const void *w,
+                             const float *beta, void *k_cache, void *v_cache, int B, int H,
+                             int cache_len, int cache_cap, int d, int dtype, float scale,
+                             void *out, void *ws, size_t ws_bytes, void *stream) {
+    path_status st = check_sizes(B, H, cache_cap, d, dtype);
+    if (st != PATH_OK) return st;
+    if (cache_len < 0) return PATH_ERR_SHAPE;
+    if (!std::isfinite(scale)) return PATH_ERR_ARG;
+    if ((long long)B * H == 0) return PATH_OK;
+    if (cache_len + 1 > cache_cap) return PATH_ERR_CAPACITY;
+    if (!q || !k || !v || !w || !beta || !k_cache || !v_cache || !out) return PATH_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(w, 16) ||
+        !aligned(beta, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return PATH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, H, cache_cap))) != PATH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == PATH_BF16)
+        return from_cuda(launch_decode<__nv_bfloat16>(q, k, v, w, beta, k_cache, v_cache, B * H,
+                                                      cache_len, cache_cap, scale, out, ws, s));
+    return from_cuda(launch_decode<float>(q, k, v, w, beta, k_cache, v_cache, B * H, cache_len,
+                                          cache_cap, scale, out, ws, s));
+}
+
+path_status path_check_workspace(void *ws, void *stream) {
+    if (ws == nullptr) return PATH_ERR_NULL;
+    if (!aligned(ws, 256)) return PATH_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PATH_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PATH_ERR_CUDA;
+    if (word != 0 && cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return PATH_ERR_CUDA;
+    return word == 0 ? PATH_OK : (word == kStatusTimeout ? PATH_ERR_TIMEOUT : PATH_ERR_CUDA);
+}
+
+const char *path_status_string(int status) {
+    switch (status) {
+        case PATH_OK: return "PATH_OK";
+        case PATH_ERR_NULL: return "PATH_ERR_NULL: a required pointer is NULL";
+        case PATH_ERR_SHAPE: return "PATH_ERR_SHAPE: unsupported or negative size";
+        case PATH_ERR_DTYPE: return "PATH_ERR_DTYPE: unsupported dtype";
+        case PATH_ERR_ALIGN: return "PATH_ERR_ALIGN: misaligned pointer";
+        case PATH_ERR_WORKSPACE: return "PATH_ERR_WORKSPACE: workspace too small";
+        case PATH_ERR_CAPACITY: return "PATH_ERR_CAPACITY: decode cache is full";
+        case PATH_ERR_TIMEOUT: return "PATH_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        case PATH_ERR_CUDA: return "PATH_ERR_CUDA: a CUDA call failed";
+        case PATH_ERR_ARG: return "PATH_ERR_ARG: scalar argument out of range";
+        default: return "PATH_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

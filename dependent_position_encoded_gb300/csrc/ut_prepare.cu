@@ -1,0 +1,356 @@
+// K1: per-block UT preprocessing of PaTH attention.
+//
+// For every block of C = 64 tokens of one head (technical summary "技術要約: PaTH
+// Attention" §3 "UT変換による表現" and the block-wise algorithm below it; review
+// "거리에서 경로로, PaTH Attention" §9) this kernel forms, in fp32:
+//   G  = W W^T, N = strictly-upper(G), D = diag(beta)
+//   A  = (I + D N)^{-1} D            so that H_0 ... H_63 = I - W^T A W  (UT form)
+//   q~_i = (H_0 ... H_i) q_i         = q_i - sum_s (Lq A^T)[i, s] w_s,  Lq[i,u] = (q_i.w_u)[u<=i]
+//   k~_j = (H_{j+1} ... H_63)^T k_j  = k_j - sum_u (Rk A)[j, u] w_u,    Rk[j,s] = (k_j.w_s)[s>j]
+//   P_b  = H_0 ... H_63              = I - W^T (A W)   (dense 64 x 64 block transition)
+//   diagonal-block logits, j <= i:  scale * (q_i.k_j - sum_s (Lq A^T)[i,s] Rk[j,s])
+//                                    [+ sum_{s=j+1..i} log f_s]   stored in log2 units.
+// Leading and trailing partial products use the matching sub-blocks of A, since
+// the inverse of a triangular matrix restricted to a contiguous diagonal range
+// is the inverse of that range's sub-block.
+//
+// One CTA of 256 threads per (block, head). Every product is a 64 x 64 x 64
+// contraction over shared memory with both operands stored k-major, each thread
+// owning a 4 x 4 output tile.
+#include "common.cuh"
+
+namespace path {
+
+namespace {
+
+constexpr int LD = 68;                 // padded row stride (floats), rows 16-byte aligned
+constexpr int BUF = kC * LD;           // floats per 64 x 64 buffer
+constexpr int kPrepThreads = 256;
+
+// acc[i][j] += sum_{k in [k0, k1)} X[k][m0 + i] * Y[k][n0 + j]
+__device__ __forceinline__ void mm_acc(const float *__restrict__ X, const float *__restrict__ Y,
+                                       int m0, int n0, float (&acc)[4][4], int k0 = 0,
+                                       int k1 = kC) {
+#pragma unroll 4
+    for (int k = k0; k < k1; ++k) {
+        const float4 a = *reinterpret_cast<const float4 *>(X + k * LD + m0);
+        const float4 b = *reinterpret_cast<const float4 *>(Y + k * LD + n0);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+}
+
+// Writes acc (rows m0.., cols n0..) into buffer Z as Z[m][n].
+__device__ __forceinline__ void store_rm(float *Z, int m0, int n0, const float (&acc)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(Z + (m0 + i) * LD + n0) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row4(T *dst, const float *v);
+template <>
+__device__ __forceinline__ void store_row4<float>(float *dst, const float *v) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store_row4<__nv_bfloat16>(__nv_bfloat16 *dst, const float *v) {
+    uint2 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    *reinterpret_cast<uint2 *>(dst) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPrepThreads)
+ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
+                  const float *__restrict__ beta, const float *__restrict__ log_f, int L,
+                  int Lp, int nblk, float scale_log2, T *__restrict__ qt, T *__restrict__ kp,
+                  float *__restrict__ dg, uint32_t *status) {
+    extern __shared__ __align__(16) float sm[];
+    float *Wr = sm;            // W[s][c]
+    float *Wt = Wr + BUF;      // W[c][s]
+    float *Qt = Wt + BUF;      // Q[c][i]
+    float *Kt = Qt + BUF;      // K[c][j]
+    float *Ar = Kt + BUF;      // A[s][u]
+    float *At = Ar + BUF;      // A[u][s]
+    float *X = At + BUF;       // scratch
+    float *Y = X + BUF;        // scratch
+    float *bs = Y + BUF;       // beta[64]
+    float *lc = bs + kC;       // block-local inclusive cumsum of log f [64]
+
+    const int tid = threadIdx.x;
+    const int blk = blockIdx.x;
+    const int bh = blockIdx.y;
+    const int t0 = blk * kC;
+    const size_t head = (size_t)bh * L;
+    if (blk == 0 && bh == 0 && tid == 0 && status) *status = 0u;
+
+    // ---- load W, Q, K (fp32, both layouts for W), beta; padded tokens are zero
+    for (int e = tid; e < kC * kD; e += kPrepThreads) {
+        const int s = e / kD, c = e % kD;
+        const int t = t0 + s;
+        float wv = 0.f, qv = 0.f, kv = 0.f;
+        if (t < L) {
+            const size_t g = (head + t) * kD + c;
+            wv = Elt<T>::to_f(w[g]);
+            qv = Elt<T>::to_f(q[g]);
+            kv = Elt<T>::to_f(k[g]);
+        }
+        Wr[s * LD + c] = wv;
+        Wt[c * LD + s] = wv;
+        Qt[c * LD + s] = qv;
+        Kt[c * LD + s] = kv;
+        Ar[s * LD + c] = 0.f;
+    }
+    if (tid < kC) {
+        const int t = t0 + tid;
+        bs[tid] = (t < L) ? beta[head + t] : 0.f;
+    }
+    if (log_f != nullptr && tid < 32) {
+        // inclusive scan of the block's log f values (two per lane)
+        const int t_a = t0 + 2 * tid, t_b = t_a + 1;
+        float a = (t_a < L) ? log_f[head + t_a] : 0.f;
+        float b = (t_b < L) ? log_f[head + t_b] : 0.f;
+        b += a;
+        float run = b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float n = __shfl_up_sync(0xffffffffu, run, o);
+            if (tid >= o) run += n;
+        }
+        const float excl = run - b;
+        lc[2 * tid] = excl + a;
+        lc[2 * tid + 1] = excl + b;
+    }
+    __syncthreads();
+
+    const int ty = tid / 16, tx = tid % 16;
+    const int m0 = ty * 4, n0 = tx * 4;
+    float acc[4][4];
+
+    // ---- G = W W^T -> X (row-major G[s][u])
+    zero(acc);
+    mm_acc(Wt, Wt, m0, n0, acc);
+    store_rm(X, m0, n0, acc);
+    __syncthreads();
+
+    // ---- A = (I + D N)^{-1} D, one column per group of 4 threads.
+    // Column u: A[u][u] = beta_u; for s < u, A[s][u] = -beta_s sum_{v=s+1..u} G[s][v] A[v][u].
+    {
+        const int u = tid >> 2, part = tid & 3;
+        for (int s = kC - 1; s >= 0; --s) {
+            float sum = 0.f;
+            for (int v = s + 1 + part; v < kC; v += 4) sum = fmaf(X[s * LD + v], Ar[v * LD + u], sum);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (part == 0) {
+                float a = 0.f;
+                if (s == u) a = bs[u];
+                else if (s < u) a = -bs[s] * sum;
+                Ar[s * LD + u] = a;
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < kC * kC; e += kPrepThreads) {
+        const int s = e / kC, u = e % kC;
+        At[u * LD + s] = Ar[s * LD + u];
+    }
+    __syncthreads();
+
+    // ---- Lq^T -> X ([u][i], u <= i), Rk^T -> Y ([s][j], s > j)
+    zero(acc);
+    mm_acc(Wt, Qt, m0, n0, acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (m0 + i > n0 + j) acc[i][j] = 0.f;
+    store_rm(X, m0, n0, acc);
+    zero(acc);
+    mm_acc(Wt, Kt, m0, n0, acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (m0 + i <= n0 + j) acc[i][j] = 0.f;
+    store_rm(Y, m0, n0, acc);
+    __syncthreads();
+
+    // ---- Qhat^T[s][i] = sum_u A[s][u] Lq^T[u][i]  (in place in X)
+    zero(acc);
+    mm_acc(At, X, m0, n0, acc);
+    __syncthreads();
+    store_rm(X, m0, n0, acc);
+    __syncthreads();
+
+    const size_t blk_base = (size_t)bh * nblk + blk;
+
+    // ---- diagonal-block logits: Dg[i][j] = scale_log2 * (q_i.k_j - sum_s Qhat[i][s] Rk[j][s])
+    {
+        float qk[4][4], corr[4][4];
+        zero(qk);
+        zero(corr);
+        mm_acc(Qt, Kt, m0, n0, qk);
+        mm_acc(X, Y, m0, n0, corr);
+        float *out = dg + blk_base * kC * kC;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+            const int ii = m0 + i;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int jj = n0 + j;
+                float x = scale_log2 * (qk[i][j] - corr[i][j]);
+                if (log_f != nullptr) x += kLog2e * (lc[ii] - lc[jj]);
+                v[j] = (jj <= ii && t0 + jj < L) ? x : -INFINITY;
+            }
+            store_row4<float>(out + ii * kC + n0, v);
+        }
+    }
+
+    // ---- q~[i][c] = q[i][c] - sum_s Qhat[i][s] W[s][c]
+    {
+        zero(acc);
+        mm_acc(X, Wr, m0, n0, acc);
+        T *out = qt + ((size_t)bh * Lp + t0) * kD;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = Qt[(n0 + j) * LD + m0 + i] - acc[i][j];
+            store_row4<T>(out + (m0 + i) * kD + n0, v);
+        }
+    }
+    __syncthreads();
+
+    // ---- Khat^T[u][j] = sum_s A[s][u] Rk^T[s][j]  (in place in Y)
+    zero(acc);
+    mm_acc(Ar, Y, m0, n0, acc);
+    __syncthreads();
+    store_rm(Y, m0, n0, acc);
+    __syncthreads();
+
+    // ---- k~[j][c] = k[j][c] - sum_u Khat[j][u] W[u][c];  AW = A W -> X
+    T *kp_blk = kp + blk_base * (2 * kC) * kD;
+    {
+        zero(acc);
+        mm_acc(Y, Wr, m0, n0, acc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = Kt[(n0 + j) * LD + m0 + i] - acc[i][j];
+            store_row4<T>(kp_blk + (m0 + i) * kD + n0, v);
+        }
+        zero(acc);
+        mm_acc(At, Wr, m0, n0, acc);
+        store_rm(X, m0, n0, acc);
+    }
+    __syncthreads();
+
+    // ---- P_b[n][c] = delta(n, c) - sum_s W[s][n] (A W)[s][c]
+    {
+        zero(acc);
+        mm_acc(Wr, X, m0, n0, acc);
+        T *out = kp_blk + kC * kD;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = ((m0 + i) == (n0 + j) ? 1.f : 0.f) - acc[i][j];
+            store_row4<T>(out + (m0 + i) * kD + n0, v);
+        }
+    }
+}
+
+// Inclusive prefix sum of log f over each head, scaled by log2(e): c2[bh][t].
+// One CTA of 1024 threads per head; padded positions repeat the last value.
+__global__ void __launch_bounds__(1024)
+fox_cumsum_kernel(const float *__restrict__ log_f, int L, int Lp, float *__restrict__ c2) {
+    __shared__ float warp_tot[32];
+    __shared__ float carry_s;
+    const int bh = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const float *src = log_f + (size_t)bh * L;
+    float *dst = c2 + (size_t)bh * Lp;
+    if (tid == 0) carry_s = 0.f;
+    __syncthreads();
+    for (int base = 0; base < Lp; base += 1024) {
+        const int t = base + tid;
+        float x = (t < L) ? src[t] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += n;
+        }
+        if (lane == 31) warp_tot[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            float y = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                float n = __shfl_up_sync(0xffffffffu, y, o);
+                if (lane >= o) y += n;
+            }
+            warp_tot[lane] = y;
+        }
+        __syncthreads();
+        const float carry = carry_s;
+        const float v = carry + x + (wid > 0 ? warp_tot[wid - 1] : 0.f);
+        if (t < Lp) dst[t] = kLog2e * v;
+        __syncthreads();
+        if (tid == 1023) carry_s = v;
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+size_t ut_prepare_smem_bytes() { return (size_t)(8 * BUF + 2 * kC) * sizeof(float); }
+
+template <typename T>
+cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const float *beta,
+                              const float *log_f, int BH, int L, float scale, void *ws,
+                              cudaStream_t stream) {
+    const FwdLayout lay = fwd_layout(1, BH, L, (int)sizeof(T), log_f != nullptr);
+    char *base = static_cast<char *>(ws);
+    const size_t smem = ut_prepare_smem_bytes();
+    cudaError_t err = cudaFuncSetAttribute(ut_prepare_kernel<T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(lay.nblk, BH);
+    ut_prepare_kernel<T><<<grid, kPrepThreads, smem, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
+        log_f, L, lay.Lp, lay.nblk, scale * kLog2e, reinterpret_cast<T *>(base + lay.off_qt),
+        reinterpret_cast<T *>(base + lay.off_kp), reinterpret_cast<float *>(base + lay.off_dg),
+        reinterpret_cast<uint32_t *>(base));
+    err = cudaGetLastError();
+    if (err != cudaSuccess || log_f == nullptr) return err;
+    fox_cumsum_kernel<<<BH, 1024, 0, stream>>>(log_f, L, lay.Lp,
+                                               reinterpret_cast<float *>(base + lay.off_c2));
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_ut_prepare<float>(const void *, const void *, const void *,
+                                              const float *, const float *, int, int, float,
+                                              void *, cudaStream_t);
+template cudaError_t launch_ut_prepare<__nv_bfloat16>(const void *, const void *, const void *,
+                                                      const float *, const float *, int, int,
+                                                      float, void *, cudaStream_t);
+
+}  // namespace path

@@ -1,0 +1,153 @@
+/*
+ * path_attn.h - C ABI of the GB300 PaTH attention library (libpath_attn.so).
+ *
+ * PaTH attention ("PaTH Attention: Position Encoding via Accumulating Householder
+ * Transformations", summarised on the review page "거리에서 경로로, PaTH Attention"
+ * §3-§4 and §9, and on the technical summary "技術要約: PaTH Attention" §2-§3):
+ * per token s and head, a transition H_s = I - beta_s w_s w_s^T (w_s unit-norm,
+ * beta_s in (0, 2)); query i attends causally to key j with logit
+ *     scale * k_j^T (H_{j+1} ... H_i) q_i                      (PaTH)
+ *     scale * k_j^T (H_{j+1} ... H_i) q_i + sum_{s=j+1..i} log f_s   (PaTH-FoX)
+ * followed by softmax over j <= i and the weighted sum of v_j.
+ *
+ * Conventions shared by every entry point
+ *  - Device pointers, contiguous row-major: q, k, v, w, out are (B, H, L, d);
+ *    beta, log_f, lse are (B, H, L) fp32. Element type of q, k, v, w, out and of
+ *    the decode caches is given by `dtype` (PATH_F32 or PATH_BF16).
+ *  - d must be 64 (the head size the pages benchmark). Anything else returns
+ *    PATH_ERR_SHAPE.
+ *  - Every tensor pointer and the workspace must be 16-byte aligned
+ *    (PATH_ERR_ALIGN); the workspace must be 256-byte aligned.
+ *  - The caller owns every buffer, the workspace included. The library
+ *    allocates no device memory and keeps no state between calls.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Every call is
+ *    asynchronous on it; argument checks are synchronous and run before any
+ *    launch: on an error nothing is launched and nothing is written.
+ *  - Errors detected after launch: PATH_ERR_CUDA (a launch failed; returned by
+ *    the call) and PATH_ERR_TIMEOUT (a kernel gave up a bounded wait; read it
+ *    with path_check_workspace after the stream has reached the call).
+ *  - Empty problems (B, H or L equal to 0; decode with B or H equal to 0) are
+ *    valid and launch nothing.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef PATH_ATTN_H
+#define PATH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PATH_OK = 0,
+    PATH_ERR_NULL = 1,      /* a required pointer is NULL */
+    PATH_ERR_SHAPE = 2,     /* negative size, d != 64, or a size above the limits */
+    PATH_ERR_DTYPE = 3,     /* dtype is not PATH_F32 or PATH_BF16 */
+    PATH_ERR_ALIGN = 4,     /* a pointer is not 16-byte (workspace: 256-byte) aligned */
+    PATH_ERR_WORKSPACE = 5, /* ws_bytes below path_workspace_bytes() */
+    PATH_ERR_CAPACITY = 6,  /* decode: cache_len + 1 > cache_cap */
+    PATH_ERR_TIMEOUT = 7,   /* a kernel gave up a bounded wait (see path_check_workspace) */
+    PATH_ERR_CUDA = 8,      /* a CUDA call failed */
+    PATH_ERR_ARG = 9        /* a scalar argument is out of range (e.g. non-finite scale) */
+} path_status;
+
+typedef enum { PATH_F32 = 0, PATH_BF16 = 1 } path_dtype;
+
+typedef enum { PATH_OP_FWD = 0, PATH_OP_FOX_FWD = 1, PATH_OP_DECODE = 2 } path_op;
+
+/* Largest sizes accepted: B*H <= PATH_MAX_HEADS, L <= PATH_MAX_LEN. */
+#define PATH_MAX_HEADS 65535
+#define PATH_MAX_LEN (1 << 22)
+
+/*
+ * Workspace bytes that `op` needs for the given sizes (L = cache capacity for
+ * PATH_OP_DECODE). Returns 0 for invalid arguments. The workspace holds the
+ * per-block factors of the forward (boundary-adjusted queries and keys, the
+ * dense block transitions, the diagonal-block logits, the FoX prefix sums)
+ * or the split partial results of decode, plus a 256-byte status header.
+ */
+size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype);
+
+/*
+ * PaTH forward: out = softmax_j(scale * k_j^T (H_{j+1}...H_i) q_i) v, causal.
+ *   q, k, v, w : (B, H, L, d) dtype      beta : (B, H, L) fp32
+ *   out        : (B, H, L, d) dtype      lse  : (B, H, L) fp32, natural-log
+ *                                               log-sum-exp of the logits; may be NULL
+ *   scale      : softmax scale, any finite value (1/sqrt(d) is the usual one)
+ *   ws         : workspace of ws_bytes >= path_workspace_bytes(PATH_OP_FWD, ...)
+ * Equivalent to path_fwd_prepare followed by path_fwd_scan on the same stream.
+ */
+path_status path_attn_fwd(const void *q, const void *k, const void *v, const void *w,
+                          const float *beta, void *out, float *lse, int B, int H, int L,
+                          int d, int dtype, float scale, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/*
+ * PaTH-FoX forward: as path_attn_fwd with the additive forget-gate bias
+ * sum_{s=j+1..i} log f_s (added after scaling) on every logit.
+ *   log_f : (B, H, L) fp32 per-token log forget gate (<= 0 in practice; any finite value)
+ * ws must hold path_workspace_bytes(PATH_OP_FOX_FWD, ...).
+ */
+path_status path_fox_fwd(const void *q, const void *k, const void *v, const void *w,
+                         const float *beta, const float *log_f, void *out, float *lse,
+                         int B, int H, int L, int d, int dtype, float scale, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/*
+ * First stage of the forward (the per-block UT preprocessing): for every block
+ * of 64 tokens it forms the block's compact Householder-product factors and
+ * writes into ws the boundary-adjusted queries and keys, the dense block
+ * transition and the diagonal-block logits; with log_f (PaTH-FoX; NULL for
+ * PaTH) also the prefix sums of log f. Reads q, k, w, beta[, log_f].
+ */
+path_status path_fwd_prepare(const void *q, const void *k, const void *w, const float *beta,
+                             const float *log_f, int B, int H, int L, int d, int dtype,
+                             float scale, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Second stage of the forward: the right-to-left scan over key blocks with
+ * online softmax. Reads v and the factors path_fwd_prepare left in ws (which
+ * must come from a prepare call with the same sizes, dtype, scale and log_f
+ * presence); writes out and lse (may be NULL).
+ */
+path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, int H, int L,
+                          int d, int dtype, float scale, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/*
+ * One PaTH decode step (the pages' inference scheme: the new token's
+ * transition updates the cached keys in place, no w/beta cache is kept):
+ *   1. k_j <- H_t k_j = k_j - beta_t (w_t . k_j) w_t for every cached j < cache_len,
+ *      written back into k_cache (rounded to dtype);
+ *   2. k_t, v_t are appended untransformed at index cache_len;
+ *   3. out = softmax_j(scale * q_t . k_j) v_j over j <= cache_len.
+ *   q, k, v, w : (B, H, d) dtype         beta : (B, H) fp32
+ *   k_cache, v_cache : (B, H, cache_cap, d) dtype, updated in place
+ *   out : (B, H, d) dtype
+ * On return the caches hold cache_len + 1 valid entries; the caller advances its
+ * length. Requires cache_len >= 0 and cache_len + 1 <= cache_cap
+ * (PATH_ERR_CAPACITY otherwise). Calls on the same caches must be ordered on
+ * one stream: each step rewrites every cached key.
+ */
+path_status path_decode_step(const void *q, const void *k, const void *v, const void *w,
+                             const float *beta, void *k_cache, void *v_cache, int B, int H,
+                             int cache_len, int cache_cap, int d, int dtype, float scale,
+                             void *out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Waits for `stream`, then reads and clears the status word that kernels of
+ * earlier calls on this workspace wrote. Returns PATH_OK, PATH_ERR_TIMEOUT or
+ * PATH_ERR_CUDA (if the synchronisation or the read failed).
+ */
+path_status path_check_workspace(void *ws, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *path_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PATH_ATTN_H */

@@ -1,0 +1,110 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/path_attn.h declares, sizes workspaces, and rejects bad arguments
+synchronously, before any CUDA call (fake device pointers are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "path_attn.h")
+
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(path_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("path_attn_fwd", "path_fox_fwd", "path_decode_step", "path_workspace_bytes",
+              "path_status_string", "path_fwd_prepare", "path_fwd_scan", "path_check_workspace"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.library_path())
+    for n in declared_functions():
+        assert hasattr(so, n), n
+    assert set(lib.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = lib.path_status_string(code)
+        assert s.startswith("PATH_")
+    assert "UNKNOWN" in lib.path_status_string(99)
+
+
+def test_workspace_sizes(lib):
+    # header 256 B; bf16 B1 H1 L128: qt 128*64*2, kp 2*128*64*2, dg 2*64*64*4
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) == \
+        256 + 128 * 64 * 2 + 2 * 128 * 64 * 2 + 2 * 64 * 64 * 4
+    fox = lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 64, lib.BF16)
+    assert fox == lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) + 512
+    # ragged L rounds up to an even number of 64-token blocks
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 65, 64, lib.BF16) == \
+        lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16)
+    part = 4 * 2 * 66 * 4  # heads x splits x (m, l, o[64]) fp32, rounded up to 256 B
+    assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 64, lib.BF16) == \
+        256 + (part + 255) // 256 * 256
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 32, lib.BF16) == 0
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, 7) == 0
+    assert lib.path_workspace_bytes(9, 1, 1, 128, 64, lib.BF16) == 0
+
+
+def _fwd(so, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, w=FAKE, beta=FAKE, out=FAKE, lse=None, B=1, H=1, L=128,
+             d=64, dtype=1, scale=0.125, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return so.path_attn_fwd(a["q"], a["k"], a["v"], a["w"], a["beta"], a["out"], a["lse"],
+                            a["B"], a["H"], a["L"], a["d"], a["dtype"],
+                            ctypes.c_float(a["scale"]), a["ws"], ctypes.c_size_t(a["ws_bytes"]),
+                            a["stream"])
+
+
+@pytest.fixture(scope="module")
+def so(lib):
+    return lib._load()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(v=None), 1), (dict(ws=None), 1), (dict(beta=None), 1),
+    (dict(d=32), 2), (dict(L=-1), 2), (dict(B=70000), 2), (dict(dtype=3), 3),
+    (dict(q=FAKE + 8), 4), (dict(out=FAKE + 4), 4), (dict(ws=FAKE + 16), 4),
+    (dict(ws_bytes=1000), 5), (dict(scale=float("inf")), 9), (dict(scale=float("nan")), 9),
+])
+def test_fwd_rejects_bad_arguments_before_launch(so, kw, code):
+    assert _fwd(so, **kw) == code
+
+
+def test_empty_problems_launch_nothing(so):
+    assert _fwd(so, L=0, q=None, k=None, v=None, w=None, beta=None, out=None, ws=None) == 0
+    assert _fwd(so, B=0) == 0
+
+
+def test_fox_needs_log_f(so):
+    r = so.path_fox_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 1, 128, 64, 1,
+                        ctypes.c_float(0.125), FAKE, ctypes.c_size_t(1 << 30), None)
+    assert r == 1
+
+
+def test_decode_argument_checks(so):
+    def call(**kw):
+        a = dict(B=1, H=1, cache_len=10, cap=16, d=64, dtype=1, ws_bytes=1 << 20, kc=FAKE)
+        a.update(kw)
+        return so.path_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, a["kc"], FAKE, a["B"], a["H"],
+                                   a["cache_len"], a["cap"], a["d"], a["dtype"],
+                                   ctypes.c_float(0.125), FAKE, FAKE,
+                                   ctypes.c_size_t(a["ws_bytes"]), None)
+    assert call(cache_len=16) == 6
+    assert call(cache_len=-1) == 2
+    assert call(d=128) == 2
+    assert call(kc=None) == 1
+    assert call(kc=FAKE + 2) == 4
+    assert call(ws_bytes=8) == 5
+    assert call(B=0) == 0

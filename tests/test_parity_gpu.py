@@ -1,0 +1,257 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances: fp32 inputs, max normwise relative error <= 1e-4 (max|o - o*| / max|o*|);
+bf16 inputs, max absolute error <= 2e-2 on every output element, plus a mean absolute
+error bound (2e-3) that catches systematic drift which the max bound would miss, and
+LSE within 2e-2 absolute. The oracle sees exactly the rounded tensors the GPU sees.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import path_inputs as pi
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX_ABS = 2e-2
+BF16_MEAN_ABS = 2e-3
+F32_MAX_REL = 1e-4
+
+
+def run_fwd(pa, x, fox=False, scale=None):
+    if fox:
+        return pa.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], scale=scale)
+    return pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=scale)
+
+
+def check_bf16(got, ref, lse=None, ref_lse=None):
+    got = got.double().cpu().numpy() if hasattr(got, "cpu") else got
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    assert err.max() <= BF16_MAX_ABS, "max abs err %g" % err.max()
+    assert err.mean() <= BF16_MEAN_ABS, "mean abs err %g" % err.mean()
+    if lse is not None:
+        le = np.abs(lse.double().cpu().numpy() - ref_lse)
+        assert le.max() <= BF16_MAX_ABS, "lse err %g" % le.max()
+
+
+# ---------------------------------------------------------------- fp32
+
+def test_tiny_fp32_workload(lib):
+    x = pi.workload_inputs(pi.TINY_FP32, device="cuda")
+    out, lse = run_fwd(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert rel <= F32_MAX_REL, rel
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
+
+
+@pytest.mark.parametrize("L", [1, 50, 64, 65, 130, 257])
+@pytest.mark.parametrize("fox", [False, True])
+def test_fp32_ragged(lib, L, fox):
+    x = pi.make_fwd_inputs(2, 2, L, dtype=torch.float32, seed=L, clip=0.0, fox=fox, device="cuda")
+    out, lse = run_fwd(lib, x, fox)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x.get("log_f"))
+    rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert rel <= F32_MAX_REL, rel
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
+
+
+# ---------------------------------------------------------------- bf16, full oracle
+
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 127, 128, 129, 200, 384, 515])
+def test_bf16_ragged_lengths(lib, L):
+    x = pi.make_fwd_inputs(2, 3, L, seed=100 + L, device="cuda")
+    out, lse = run_fwd(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_bf16_workload_L2048(lib):
+    x = pi.workload_inputs(pi.BF16_L2048, device="cuda")
+    out, lse = run_fwd(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+@pytest.mark.parametrize("L", [64, 200, 640])
+def test_fox_bf16_full(lib, L):
+    x = pi.make_fwd_inputs(2, 2, L, seed=300 + L, fox=True, device="cuda")
+    out, lse = run_fwd(lib, x, fox=True)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_beta_extremes_bf16(lib):
+    # beta = 0 everywhere is plain causal attention; beta near 2 is the reflection regime
+    for lo, hi in ((0.0, 0.0), (1.98, 1.99)):
+        x = pi.make_fwd_inputs(1, 2, 333, seed=7, device="cuda")
+        x["beta"] = torch.empty_like(x["beta"]).uniform_(lo, hi) if hi > 0 else \
+            torch.zeros_like(x["beta"])
+        out, lse = run_fwd(lib, x)
+        ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+        check_bf16(out, ref, lse, ref_lse)
+
+
+def test_custom_scale(lib):
+    x = pi.make_fwd_inputs(1, 2, 150, seed=9, device="cuda")
+    out, lse = run_fwd(lib, x, scale=0.3)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=0.3)
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_prepare_then_scan_equals_fused(lib):
+    x = pi.make_fwd_inputs(2, 2, 300, seed=11, device="cuda")
+    out, lse = run_fwd(lib, x)
+    ws = lib.new_workspace(lib.OP_FWD, 2, 2, 300, lib.BF16, "cuda")
+    lib.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws)
+    out2, lse2 = lib.path_fwd_scan(x["v"], ws)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_deterministic(lib):
+    x = pi.make_fwd_inputs(2, 4, 700, seed=12, device="cuda")
+    a, _ = run_fwd(lib, x)
+    b, _ = run_fwd(lib, x)
+    assert torch.equal(a, b)
+
+
+def test_empty_problem_is_a_no_op(lib):
+    z = torch.empty((1, 2, 0, 64), dtype=torch.bfloat16, device="cuda")
+    beta = torch.empty((1, 2, 0), dtype=torch.float32, device="cuda")
+    out, lse = lib.path_attn_fwd(z, z, z, z, beta)
+    assert out.shape == (1, 2, 0, 64)
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled rows
+
+def _sampled_parity(lib, wl, n_heads=12, n_rows=600, seed=0):
+    x = pi.workload_inputs(wl, device="cuda")
+    out, lse = run_fwd(lib, x, fox=wl.fox)
+    torch.cuda.synchronize()
+    B, H, L = wl.B, wl.H, wl.L
+    g = torch.Generator().manual_seed(seed)
+    heads = torch.randperm(B * H, generator=g)[:n_heads]
+    sel = {k: v.reshape(B * H, *v.shape[2:])[heads.to(v.device)].cpu() for k, v in x.items()}
+    rows = pi.sample_rows(n_heads, L, n_rows, seed=seed)
+    ref, ref_lse = oracle.path_rows(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"], rows,
+                                    log_f=sel.get("log_f"))
+    flat = out.reshape(B * H, L, 64)
+    flat_lse = lse.reshape(B * H, L)
+    hsel = heads[rows[:, 0]].to(out.device)
+    ridx = torch.as_tensor(rows[:, 1], device=out.device)
+    got = flat[hsel, ridx].double().cpu().numpy()
+    got_lse = flat_lse[hsel, ridx].double().cpu().numpy()
+    check_bf16(got, ref)
+    assert np.abs(got_lse - ref_lse).max() <= BF16_MAX_ABS
+    assert torch.isfinite(out).all()
+
+
+def test_speed_workload_sampled(lib):
+    _sampled_parity(lib, pi.BF16_L4096)
+
+
+def test_fox_long_workload_sampled(lib):
+    _sampled_parity(lib, pi.FOX_L16384, n_heads=8, n_rows=300)
+
+
+# ---------------------------------------------------------------- decode
+
+def _decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None):
+    wl = pi.DecodeWorkload("t", B, H, n0, steps, 64, dtype, seed, 1000 + seed)
+    cap = n0 + steps
+    kc, vc = pi.make_decode_prefix(wl, cap, device="cuda")
+    heads = list(range(B * H)) if check_heads is None else check_heads
+    hk = kc.reshape(B * H, cap, 64)[heads, :n0].cpu()
+    hv = vc.reshape(B * H, cap, 64)[heads, :n0].cpu()
+    ocache = oracle.DecodeCache(hk, hv, cap)
+    ws = lib.new_workspace(lib.OP_DECODE, B, H, cap, lib.BF16 if dtype == torch.bfloat16 else lib.F32,
+                           "cuda")
+    worst = 0.0
+    for t in range(steps):
+        s = pi.make_decode_step(wl, t, device="cuda")
+        pre = kc.reshape(B * H, cap, 64)[heads[:2], :n0 + t].double().cpu().numpy()
+        o = lib.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc, n0 + t,
+                                 workspace=ws)
+        sel = {k: v.reshape(B * H, -1)[heads].cpu() for k, v in s.items()}
+        ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
+        got = o.reshape(B * H, 64)[heads].double().cpu().numpy()
+        worst = max(worst, np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+        if dtype == torch.bfloat16:
+            assert np.abs(got - ref).max() <= BF16_MAX_ABS
+        # the updated keys equal H_t applied to the pre-step keys, rounded once
+        post = kc.reshape(B * H, cap, 64)[heads[:2], :n0 + t + 1].double().cpu().numpy()
+        w = sel["w"][:2].double().numpy()
+        b = sel["beta"][:2].double().numpy().reshape(2, 1)
+        expect = pre - b[:, :, None] * np.einsum("hjc,hc->hj", pre, w)[:, :, None] * w[:, None, :]
+        expect = torch.from_numpy(expect).to(dtype).double().numpy()
+        # fp32 arithmetic then one rounding: within 2 ulps of the fp64 result rounded once
+        ulp = np.abs(expect) * (2.0 ** -6 if dtype == torch.bfloat16 else 2.0 ** -21)
+        assert np.all(np.abs(post[:, :n0 + t] - expect) <= ulp + 1e-5)
+        assert np.array_equal(post[:, n0 + t], sel["k"][:2].double().numpy())
+    return worst
+
+
+def test_decode_small_fp32(lib):
+    worst = _decode_run(lib, 2, 3, 200, 12, torch.float32, seed=1)
+    assert worst <= F32_MAX_REL
+
+
+def test_decode_small_bf16_from_empty_and_ragged(lib):
+    # empty prefix, then lengths crossing the split boundary (1024 keys per split)
+    _decode_run(lib, 1, 2, 0, 5, torch.bfloat16, seed=2)
+    worst = _decode_run(lib, 2, 2, 1020, 8, torch.bfloat16, seed=3)
+    assert worst <= 5e-2
+
+
+def test_decode_workload_sampled_heads(lib):
+    wl = pi.DECODE_32K
+    cap = wl.n_prefix + wl.steps
+    kc, vc = pi.make_decode_prefix(wl, cap, device="cuda")
+    heads = [0, 77, 513, 1023]
+    nh = wl.B * wl.H
+    ocache = oracle.DecodeCache(kc.reshape(nh, cap, 64)[heads, :wl.n_prefix].cpu(),
+                                vc.reshape(nh, cap, 64)[heads, :wl.n_prefix].cpu(), cap)
+    ws = lib.new_workspace(lib.OP_DECODE, wl.B, wl.H, cap, lib.BF16, "cuda")
+    rel = []
+    for t in range(wl.steps):
+        s = pi.make_decode_step(wl, t, device="cuda")
+        o = lib.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
+                                 wl.n_prefix + t, workspace=ws)
+        if t % 8 == 7 or t == 0:
+            sel = {k: v.reshape(nh, -1)[heads].cpu() for k, v in s.items()}
+            # the oracle steps every time; compare on a subset of steps
+            ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
+            got = o.reshape(nh, 64)[heads].double().cpu().numpy()
+            assert np.abs(got - ref).max() <= BF16_MAX_ABS
+            rel.append(np.abs(got - ref).max() / np.abs(ref).max())
+        else:
+            sel = {k: v.reshape(nh, -1)[heads].cpu() for k, v in s.items()}
+            ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
+    assert max(rel) <= 5e-2, rel
+
+
+def test_decode_capacity_error(lib):
+    kc = torch.zeros((1, 1, 4, 64), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    s = pi.make_fwd_inputs(1, 1, 1, seed=0, device="cuda")
+    with pytest.raises(lib.PathError) as e:
+        lib.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc, 4)
+    assert e.value.code == lib.ERR_CAPACITY
+    assert torch.count_nonzero(kc) == 0
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_forced_timeout_reports_status_and_context_survives(lib, monkeypatch):
+    x = pi.make_fwd_inputs(1, 1, 256, seed=5, device="cuda")
+    ws = lib.new_workspace(lib.OP_FWD, 1, 1, 256, lib.BF16, "cuda")
+    monkeypatch.setenv("PATH_ATTN_DEBUG_FORCE_TIMEOUT", "1")
+    lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], workspace=ws)
+    assert lib.path_check_workspace(ws) == lib.ERR_TIMEOUT
+    monkeypatch.delenv("PATH_ATTN_DEBUG_FORCE_TIMEOUT")
+    out, _ = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], workspace=ws)
+    assert lib.path_check_workspace(ws) == lib.OK
+    ref, _ = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    check_bf16(out, ref)
