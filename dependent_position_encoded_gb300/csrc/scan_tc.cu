@@ -24,6 +24,10 @@
 // online softmax with lazy rescaling, fp32 -> bf16 conversion of the new state into the
 // swizzled A-operand tile. Warp 4 allocates TMEM and one lane issues every MMA. Warp 5
 // (one lane) streams K~|P_b and V_b tiles by TMA through an NS-stage ring.
+// The bf16 state tile is double-buffered (step s reads buffer s & 1 while the new state
+// of step s + 1 is written into the other one: the S MMA of step s may still be reading
+// its operand when the state MMA that precedes it has completed). The probability tile
+// is single-buffered: it is rewritten only after the previous P.V MMA has completed.
 // TMEM columns: [0,64) new state, [64,128) and [128,192) S (double buffer), [192,256) O.
 #include "common.cuh"
 
@@ -40,15 +44,15 @@ constexpr float kRescaleThreshold = 8.f;    // lazy rescale: keep the old max wi
 
 struct ScanSmem {
     // byte offsets from the 1024-aligned base
-    static constexpr uint32_t q_st = 0;
-    static constexpr uint32_t p_buf = kTileBytes;               // two 16 KB tiles
-    static constexpr uint32_t stage = p_buf + 2 * kTileBytes;   // NS stages
+    static constexpr uint32_t q_st = 0;                         // two 16 KB state tiles
+    static constexpr uint32_t p_buf = 2 * kTileBytes;           // one 16 KB tile
+    static constexpr uint32_t stage = p_buf + kTileBytes;       // NS stages
     static constexpr uint32_t bars = stage + NS * kStageBytes;
     // barrier indices
     static constexpr int FULL = 0, EMPTY = NS, QFULL = 2 * NS, BAR_QN = 2 * NS + 1,
-                         BAR_S = 2 * NS + 2, BAR_O = 2 * NS + 3 /* 2 */, QREADY = 2 * NS + 5,
-                         PREADY = 2 * NS + 6 /* 2 */, FINAL = 2 * NS + 8, NEVER = 2 * NS + 9,
-                         NBARS = 2 * NS + 10;
+                         BAR_S = 2 * NS + 2, BAR_O = 2 * NS + 3, QREADY = 2 * NS + 4,
+                         PREADY = 2 * NS + 5, FINAL = 2 * NS + 6, NEVER = 2 * NS + 7,
+                         NBARS = 2 * NS + 8;
     static constexpr uint32_t tmem_slot = bars + NBARS * 8;
     static constexpr uint32_t abort_flag = tmem_slot + 4;
     static constexpr uint32_t bytes = abort_flag + 4;
@@ -81,7 +85,8 @@ template <bool FOX>
 __global__ void __launch_bounds__(kScanThreads, 2)
 path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_kp,
-                    const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ dg,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __nv_bfloat16 *__restrict__ qt, const float *__restrict__ dg,
                     const float *__restrict__ c2, __nv_bfloat16 *__restrict__ out,
                     float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
                     uint32_t *status, uint64_t limit_ns, int force_timeout) {
@@ -111,10 +116,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         mbar_init(bar(ScanSmem::BAR_QN), 1);
         mbar_init(bar(ScanSmem::BAR_S), 1);
         mbar_init(bar(ScanSmem::BAR_O), 1);
-        mbar_init(bar(ScanSmem::BAR_O + 1), 1);
         mbar_init(bar(ScanSmem::QREADY), 128);
         mbar_init(bar(ScanSmem::PREADY), 128);
-        mbar_init(bar(ScanSmem::PREADY + 1), 128);
         mbar_init(bar(ScanSmem::FINAL), 1);
         mbar_init(bar(ScanSmem::NEVER), 1);
         *abort_flag = 0u;
@@ -131,8 +134,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const uint32_t tmem = *tmem_slot;
     const uint32_t T_QN = tmem + 0, T_S0 = tmem + 64, T_O = tmem + 192;
 
-    const uint32_t q_st = base + ScanSmem::q_st;
-    auto p_buf = [&](int i) { return base + ScanSmem::p_buf + (uint32_t)i * kTileBytes; };
+    auto q_st = [&](int i) { return base + ScanSmem::q_st + (uint32_t)i * kTileBytes; };
+    const uint32_t p_buf = base + ScanSmem::p_buf;
     auto stage_kp = [&](int i) { return base + ScanSmem::stage + (uint32_t)i * kStageBytes; };
     auto stage_v = [&](int i) { return stage_kp(i) + kTileBytes; };
 
@@ -143,7 +146,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             tma_prefetch_desc(&tm_kp);
             tma_prefetch_desc(&tm_v);
             mbar_arrive_expect_tx(bar(ScanSmem::QFULL), kTileBytes);
-            tma_load_3d(q_st, &tm_qt, bar(ScanSmem::QFULL), 0, tile * kTile, bh);
+            tma_load_3d(q_st(1), &tm_qt, bar(ScanSmem::QFULL), 0, tile * kTile, bh);
             int issued = 0;
             for (int s = 0; s < nsteps; ++s) {
                 const int st = s % NS;
@@ -174,7 +177,6 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         if (lane == 0) {
             constexpr uint32_t ID_KMAJ = idesc_bf16(128, 64, false);
             constexpr uint32_t ID_PV = idesc_bf16(128, 64, true);
-            const uint64_t a_q = sdesc_sw128(q_st, 16, 1024);
             bool ok = true;
             if (force_timeout) ok = wait(bar(ScanSmem::NEVER), 0);  // nothing arrives here
             auto issue_sq = [&](int s) -> bool {
@@ -182,6 +184,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (!wait(bar(ScanSmem::FULL + st), (s / NS) & 1)) return false;
                 if (s >= 2 && !wait(bar(ScanSmem::QREADY), (s - 2) & 1)) return false;
                 tc_fence_after();
+                const uint64_t a_q = sdesc_sw128(q_st(s & 1), 16, 1024);
                 const uint64_t b_k = sdesc_sw128(stage_kp(st), 16, 1024);
                 const uint64_t b_p = sdesc_sw128(stage_kp(st) + 64 * 128, 16, 1024);
                 if (s < nsteps - 1) {
@@ -203,14 +206,14 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (s + 1 >= 2 && s + 1 <= nsteps - 1 && !(ok = issue_sq(s + 1))) break;
                 const int st = s % NS;
                 if (s == 0 && !(ok = wait(bar(ScanSmem::FULL + st), 0))) break;
-                if (!(ok = wait(bar(ScanSmem::PREADY + (s & 1)), (s >> 1) & 1))) break;
+                if (!(ok = wait(bar(ScanSmem::PREADY), s & 1))) break;
                 tc_fence_after();
-                const uint64_t a_p = sdesc_sw128(p_buf(s & 1), 16, 1024);
+                const uint64_t a_p = sdesc_sw128(p_buf, 16, 1024);
                 const uint64_t b_v = sdesc_sw128(stage_v(st), 1024, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     umma_bf16(T_O, a_p + 2 * kk, b_v + 128 * kk, ID_PV, (s > 0 || kk > 0));
-                umma_commit(bar(ScanSmem::BAR_O + (s & 1)));
+                umma_commit(bar(ScanSmem::BAR_O));
                 umma_commit(bar(ScanSmem::EMPTY + st));
             }
             // every MMA issued above has completed before TMEM is released
@@ -246,12 +249,13 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (s < nsteps - 1) {
                     if (!(ok = wwait(bar(ScanSmem::BAR_QN), (s - 1) & 1))) break;
                     tc_fence_after();
+                    // the state of step s + 1 goes to buffer (s + 1) & 1
+                    uint8_t *row = gbase + ScanSmem::q_st + (uint32_t)((s + 1) & 1) * kTileBytes;
                     if (s >= 2 || warp >= 2) {
                         uint32_t qa[32], qb[32];
                         tmem_ld32(T_QN + lane_base, qa);
                         tmem_ld32(T_QN + lane_base + 32, qb);
                         tmem_ld_wait();
-                        uint8_t *row = gbase + ScanSmem::q_st;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             const uint32_t *src = (c < 4) ? &qa[8 * c] : &qb[8 * (c - 4)];
@@ -262,6 +266,13 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                             u.w = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
                             *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = u;
                         }
+                    } else {
+                        // rows of block ib0 keep q~ through step 1: copy it from the workspace
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            qt + (head * Lp + (size_t)tile * kTile + r) * kD);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = __ldg(src + c);
                     }
                     fence_proxy_async_smem();
                     tc_fence_before();
@@ -331,7 +342,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
             if (s >= 1 && __any_sync(0xffffffffu, rescale)) {
                 // O must be complete up to step s - 1 before it is rewritten
-                if (!(ok = wwait(bar(ScanSmem::BAR_O + ((s - 1) & 1)), ((s - 1) >> 1) & 1))) break;
+                if (!(ok = wwait(bar(ScanSmem::BAR_O), (s - 1) & 1))) break;
                 tc_fence_after();
                 uint32_t oa[32], ob[32];
                 tmem_ld32(T_O + lane_base, oa);
@@ -357,9 +368,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 pk[j] = pack_bf16x2(p0, p1);
             }
             l_run += lsum;
-            // the P buffer of step s was last read by the MMA of step s - 2
-            if (s >= 2 && !(ok = wwait(bar(ScanSmem::BAR_O + (s & 1)), ((s - 2) >> 1) & 1))) break;
-            uint8_t *prow = gbase + ScanSmem::p_buf + (uint32_t)(s & 1) * kTileBytes;
+            // the P tile was last read by the P.V MMA of step s - 1
+            if (s >= 1 && !(ok = wwait(bar(ScanSmem::BAR_O), (s - 1) & 1))) break;
+            uint8_t *prow = gbase + ScanSmem::p_buf;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint4 u = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
@@ -367,11 +378,11 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(ScanSmem::PREADY + (s & 1)));
+            mbar_arrive(bar(ScanSmem::PREADY));
         }
 
         // ---- epilogue: O / l, LSE
-        if (ok) ok = wwait(bar(ScanSmem::BAR_O + ((nsteps - 1) & 1)), ((nsteps - 1) >> 1) & 1);
+        if (ok) ok = wwait(bar(ScanSmem::BAR_O), (nsteps - 1) & 1);
         if (ok) {
             tc_fence_after();
             uint32_t oa[32], ob[32];
@@ -457,7 +468,8 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
     if (err != cudaSuccess) return err;
     dim3 grid(lay.nblk / 2, BH);
     kern<<<grid, kScanThreads, kScanSmemBytes, stream>>>(
-        tm_qt, tm_kp, tm_v, reinterpret_cast<const float *>(basep + lay.off_dg),
+        tm_qt, tm_kp, tm_v, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
+        reinterpret_cast<const float *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e,
         reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout);
