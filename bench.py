@@ -1,0 +1,501 @@
+"""Benchmark of the PaTH attention hot path on GB300.
+
+One step = one PaTH forward (UT preprocessing + block scan) over the bf16 speed
+workload B=32, H=32, L=4096, d=64, inputs resident in HBM (2.1 GB of inputs per
+step, larger than the 129 MB L2, so no flush is needed between steps). Timed
+with CUDA events on the launching stream. The line also carries the PaTH-FoX
+forward (B=8, H=16, L=16384) and the decode step (B=32, H=32, 32K-token cache,
+64 steps) as sub-objects, an end-to-end figure through the C ABI from pinned
+host buffers, the roofline of the dominant kernel and the fp64 oracle timed on
+the host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank runs
+its own batch of the workload (weak scaling, no collective on the data path).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import path_inputs as pi  # noqa: E402
+
+C = 64
+METRIC = "PaTH attn fwd tokens/s & TFLOP/s (B32 H32 d64 L4096 bf16), % roofline; decode GB/s"
+
+
+def fwd_flops(B, H, L, d=64):
+    """Algorithmic FLOPs of one forward: causal QK^T + PV, the rank-C state updates of
+    the block scan, and the per-block UT preprocessing."""
+    f_attn = 2.0 * B * H * L * L * d
+    f_corr = 2.0 * B * H * d * L * (L - C)
+    f_pre = B * H * L * (12.0 * C * d + 2.0 / 3.0 * C * C)
+    return f_attn, f_corr, f_pre
+
+
+def scan_executed_flops(B, H, L):
+    """Tensor-core FLOPs the block-scan kernel actually issues (128-row tiles; per
+    visited key block S = X K~^T and, except at the last block, X P_b^T; P V every block)."""
+    nblk = (L + C - 1) // C
+    nblk += nblk & 1
+    mm = 2.0 * 128 * 64 * 64
+    total = 0.0
+    for t in range(nblk // 2):
+        steps = 2 * t + 2
+        total += (steps - 1) * mm + (steps - 2) * mm + steps * mm
+    return B * H * total
+
+
+def decode_bytes(B, H, n, d=64):
+    """HBM bytes of one decode step over n cached keys: key read + key write + value
+    read (2 bytes each) plus the new token's q, k, v, w, o."""
+    return B * H * (6.0 * n * d + 12.0 * d)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash(name):
+    src = os.path.join(ROOT, "dependent_position_encoded_gb300", "csrc", name)
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_hash(e["source"]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    t = [x.strip() for x in line.split(",")]
+                    if len(t) >= 9:
+                        rows.append(t)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def time_forward(pa, x, steps, warmup, fox=False):
+    """Times `steps` forwards (prepare + scan); returns (total_ms, scan_ms_list, prep_ms_list)."""
+    B, H, L, _ = x["q"].shape
+    op = pa.OP_FOX_FWD if fox else pa.OP_FWD
+    ws = pa.new_workspace(op, B, H, L, pa.BF16, x["q"].device)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=x["q"].device)
+    log_f = x.get("log_f") if fox else None
+    stream = torch.cuda.current_stream()
+
+    def one(evs=None):
+        if evs:
+            evs[0].record(stream)
+        pa.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws, log_f=log_f)
+        if evs:
+            evs[1].record(stream)
+        pa.path_fwd_scan(x["v"], ws, out=out, lse=lse, fox=fox)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        one(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    status = pa.path_check_workspace(ws)
+    if status != pa.OK:
+        raise RuntimeError("kernel status " + pa.path_status_string(status))
+    total = start.elapsed_time(end)
+    prep = [e[0].elapsed_time(e[1]) for e in evs]
+    scan = [e[1].elapsed_time(e[2]) for e in evs]
+    return total, scan, prep
+
+
+def time_e2e(pa, x, steps, warmup):
+    """The same forward through the C ABI, with every step copying its inputs from pinned
+    host memory and reading the output back."""
+    host = {k: v.cpu().pin_memory() for k, v in x.items()}
+    dev = {k: torch.empty_like(v) for k, v in x.items()}
+    B, H, L, _ = x["q"].shape
+    ws = pa.new_workspace(pa.OP_FWD, B, H, L, pa.BF16, x["q"].device)
+    out = torch.empty_like(x["q"])
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k in ("q", "k", "v", "w", "beta"):
+            dev[k].copy_(host[k], non_blocking=True)
+        pa.path_attn_fwd(dev["q"], dev["k"], dev["v"], dev["w"], dev["beta"], out=out, lse=None,
+                         workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "w", "beta"))
+    d2h = out_h.numel() * out_h.element_size()
+    return start.elapsed_time(end), h2d, d2h
+
+
+def time_decode(pa, wl, reps=2):
+    """Times the 64-step decode sequence (cache reset to the prefix length each repetition;
+    the cache content drifts across repetitions, which does not change the work)."""
+    dev = torch.device("cuda")
+    cap = wl.n_prefix + wl.steps
+    kc, vc = pi.make_decode_prefix(wl, cap, device=dev)
+    steps = [pi.make_decode_step(wl, t, device=dev) for t in range(wl.steps)]
+    ws = pa.new_workspace(pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16, dev)
+    out = torch.empty((wl.B, wl.H, 64), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    per_step = []
+    for r in range(reps + 1):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(wl.steps + 1)]
+        evs[0].record(stream)
+        for t, s in enumerate(steps):
+            pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
+                                wl.n_prefix + t, out=out, workspace=ws)
+            evs[t + 1].record(stream)
+        torch.cuda.synchronize()
+        if r > 0:  # the first pass is the warm-up
+            per_step.append([evs[t].elapsed_time(evs[t + 1]) for t in range(wl.steps)])
+    ms = [statistics.mean(col) for col in zip(*per_step)]
+    nbytes = [decode_bytes(wl.B, wl.H, wl.n_prefix + t) for t in range(wl.steps)]
+    gbs = sum(nbytes) / (sum(ms) * 1e-3) / 1e9
+    return {"ms_per_step": sum(ms) / len(ms), "gbs": gbs,
+            "tokens_per_s": wl.B / (sum(ms) / len(ms) * 1e-3),
+            "bytes_per_step": sum(nbytes) / len(nbytes), "launches_per_step": 2}
+
+
+def cpu_baseline(x_cpu, wl, target_s=12.0):
+    """The fp64 oracle on whole heads of the workload, timed on the host cores."""
+    import oracle
+    B, H, L = wl.B, wl.H, wl.L
+    nh_total = B * H
+    # x_cpu holds a subset of heads drawn in the workload's distribution
+    sel = {k: v.reshape(-1, *v.shape[2:]) for k, v in x_cpu.items()}
+    nh_avail = sel["q"].shape[0]
+
+    def run(n):
+        t0 = time.perf_counter()
+        oracle.path_fwd(sel["q"][:n], sel["k"][:n], sel["v"][:n], sel["w"][:n],
+                        sel["beta"][:n], log_f=sel.get("log_f", None) if wl.fox else None)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    n = max(1, min(nh_avail, int(target_s / max(t1, 1e-3))))
+    t = run(n) if n > 1 else t1
+    cores = os.cpu_count()
+    t_full = t * nh_total / n
+    return {"value": B * L / t_full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of %d heads of the workload, every query row (%.1f s); full-workload "
+                      "time extrapolated by head count" % (n, nh_total, t)}
+
+
+PROFILE_CASES = {
+    # a quarter of the speed workload: 1.3 GB on the device, inputs larger than L2
+    "fwd": pi.FwdWorkload("path_fwd_bf16_B8H32L4096", 8, 32, 4096, 64, torch.bfloat16, 3,
+                          pi.BETA_CLIP, False),
+    "fox": pi.FwdWorkload("path_fox_fwd_bf16_B2H16L16384", 2, 16, 16384, 64, torch.bfloat16, 4,
+                          pi.BETA_CLIP, True),
+    "decode": pi.DecodeWorkload("path_decode_bf16_B8H32N32768x4", 8, 32, 32768, 4, 64,
+                                torch.bfloat16, 5, 1000),
+}
+
+
+def run_profile_case(args):
+    """Runs one operation on its reduced case: warm-up launches, then `steps` launches."""
+    import dependent_position_encoded_gb300 as pa
+    pa.ensure_built()
+    dev = torch.device("cuda")
+    wl = PROFILE_CASES[args.profile]
+    if args.profile == "decode":
+        cap = wl.n_prefix + args.warmup + args.steps
+        kc, vc = pi.make_decode_prefix(wl, cap, device=dev)
+        ws = pa.new_workspace(pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16, dev)
+        s = pi.make_decode_step(wl, 0, device=dev)
+        for t in range(args.warmup + args.steps):
+            pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
+                                wl.n_prefix + t, workspace=ws)
+    else:
+        x = pi.workload_inputs(wl, device=dev)
+        total, scan, prep = time_forward(pa, x, args.steps, args.warmup, fox=wl.fox)
+        print(json.dumps({"profile": wl.name, "scan_ms": scan, "prepare_ms": prep}))
+    torch.cuda.synchronize()
+
+
+def dist_setup(n_gpus):
+    if n_gpus <= 1 and "WORLD_SIZE" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle as the reference arm, on rank 0 only."""
+    if rank != 0:
+        return
+    wl = pi.BF16_L4096
+    # one head per step: the oracle on the full workload would take hours
+    import oracle
+    g = pi.make_fwd_inputs(1, 2, wl.L, seed=wl.seed, device="cpu")
+    sel = {k: v.reshape(2, *v.shape[2:]) for k, v in g.items()}
+
+    def step():
+        t0 = time.perf_counter()
+        oracle.path_fwd(sel["q"][:1], sel["k"][:1], sel["v"][:1], sel["w"][:1], sel["beta"][:1])
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    t_head = statistics.mean(times)
+    t_full = t_head * wl.B * wl.H
+    value = wl.B * wl.L / t_full
+    cores = os.cpu_count()
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_full * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "L": wl.L, "d": 64},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "one head (all %d query rows) per step; full-workload "
+                                       "time = per-head time x %d heads" % (wl.L, wl.B * wl.H)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
+    ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
+    ap.add_argument("--profile", choices=["fwd", "fox", "decode"],
+                    help="run only that operation on a reduced case (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.profile:
+        run_profile_case(args)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import dependent_position_encoded_gb300 as pa
+    pa.ensure_built() if rank == 0 else None
+    barrier(world)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    wl = pi.BF16_L4096
+    x = pi.workload_inputs(wl, device=dev)
+    B, H, L = wl.B, wl.H, wl.L
+    f_attn, f_corr, f_pre = fwd_flops(B, H, L)
+    F = f_attn + f_corr + f_pre
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total_ms, scan_ms, prep_ms = time_forward(pa, x, args.steps, args.warmup)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = clk.summary()
+    t_max = max_over_ranks(total_ms, world)
+    ms_step = t_max / args.steps
+    value = world * B * L * args.steps / (t_max * 1e-3)
+
+    scan_avg = statistics.mean(scan_ms)
+    prep_avg = statistics.mean(prep_ms)
+    achieved = (f_attn + f_corr) / (scan_avg * 1e-3) / 1e12
+    roofline = {"kernel": "path_scan_tc_kernel", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "traffic": ncu_traffic("path_scan_tc_kernel"),
+                "peak_source": "%s bf16 dense (burst)" % peaks["source"],
+                "algorithmic_flops_per_launch": f_attn + f_corr,
+                "executed_tensor_tflops": scan_executed_flops(B, H, L) / (scan_avg * 1e-3) / 1e12,
+                "ms_per_launch": scan_avg}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "H": H, "L": L, "d": 64,
+                       "per_rank_batch": B, "l2": "inputs 2.1 GB per step (> L2), no flush",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "tflops": F / (ms_step * 1e-3) / 1e12 * world,
+            "fa_equiv_tflops": f_attn / (ms_step * 1e-3) / 1e12 * world,
+            "fwd_roofline_frac": F / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "prepare_ms": prep_avg, "scan_ms": scan_avg,
+            "roofline": roofline, "clocks": clocks,
+            "gpu_launches": 2 * args.steps}
+
+    if not args.no_extras:
+        e2e_ms, h2d, d2h = time_e2e(pa, x, max(2, args.steps // 2), 3)
+        e2e_max = max_over_ranks(e2e_ms, world)
+        n_e2e = max(2, args.steps // 2)
+        line["e2e"] = {"value": world * B * L * n_e2e / (e2e_max * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del x
+        torch.cuda.empty_cache()
+        fw = pi.FOX_L16384
+        xf = pi.workload_inputs(fw, device=dev)
+        fox_total, fox_scan, fox_prep = time_forward(pa, xf, 3, 3, fox=True)
+        fa, fc, fp = fwd_flops(fw.B, fw.H, fw.L)
+        fox_ms = fox_total / 3
+        line["fox"] = {"workload": fw.name, "ms_per_step": fox_ms,
+                       "tokens_per_s": fw.B * fw.L / (fox_ms * 1e-3),
+                       "tflops": (fa + fc + fp) / (fox_ms * 1e-3) / 1e12,
+                       "scan_ms": statistics.mean(fox_scan), "prepare_ms": statistics.mean(fox_prep)}
+        del xf
+        torch.cuda.empty_cache()
+        dec = time_decode(pa, pi.DECODE_32K)
+        dec["workload"] = pi.DECODE_32K.name
+        dec["roofline"] = {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": dec["gbs"],
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": dec["gbs"] / peaks["hbm_gbs"],
+                           "traffic": ncu_traffic("decode_split_kernel"),
+                           "peak_source": "%s HBM copy" % peaks["source"]}
+        line["decode"] = dec
+
+    if args.sweep and rank == 0:
+        sweep = {}
+        for Ls in pi.SPEED_SWEEP_L:
+            xs = pi.workload_inputs(pi.speed_shape(Ls), device=dev)
+            tot, sc, pr = time_forward(pa, xs, 3, 3)
+            a, c, p = fwd_flops(32, 32, Ls)
+            sweep[str(Ls)] = {"ms": tot / 3, "tflops": (a + c + p) / (tot / 3 * 1e-3) / 1e12,
+                              "tokens_per_s": 32 * Ls / (tot / 3 * 1e-3)}
+            del xs
+            torch.cuda.empty_cache()
+        line["sweep_L"] = sweep
+
+    if rank == 0 and not args.no_cpu_baseline:
+        xc = pi.make_fwd_inputs(1, 64, wl.L, seed=wl.seed, device="cpu")
+        line["cpu_baseline"] = cpu_baseline(xc, pi.FwdWorkload(wl.name, wl.B, wl.H, wl.L, 64,
+                                                               wl.dtype, wl.seed, wl.clip, False))
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
