@@ -25,7 +25,8 @@ OP_FWD, OP_FOX_FWD, OP_DECODE = 0, 1, 2
 HEAD_DIM = 64
 
 EXPORTED = ("path_workspace_bytes", "path_attn_fwd", "path_fox_fwd", "path_fwd_prepare",
-            "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string")
+            "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string",
+            "path_decode_step_noalloc")
 
 _lib = None
 
@@ -68,6 +69,8 @@ def _load():
     lib.path_fwd_scan.restype = I
     lib.path_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, S, P]
     lib.path_decode_step.restype = I
+    lib.path_decode_step_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    lib.path_decode_step_noalloc.restype = I
     lib.path_check_workspace.argtypes = [P, P]
     lib.path_check_workspace.restype = I
     lib.path_status_string.argtypes = [I]
@@ -264,3 +267,26 @@ def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, 
 def path_check_workspace(workspace, stream=None):
     """Synchronises the stream and returns the status code left by kernels in `workspace`."""
     return int(_load().path_check_workspace(_ptr(workspace), _stream(stream, workspace.device)))
+
+
+def path_decode_step_noalloc(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, out=None,
+                             stream=None):
+    """path_decode_step without a workspace, for callers that may not allocate device memory
+    for the library on the call path. The split partials live in a fixed 16 MiB array inside
+    the library; calls that overlap on one GPU share it and must be serialised. Raises
+    PathError(ERR_WORKSPACE) when B * H * ceil(cache_len / 1024) partials do not fit."""
+    torch = _torch()
+    _cuda_tensor(k_cache, "k_cache")
+    B, H, cap, d = k_cache.shape
+    _cuda_tensor(v_cache, "v_cache", k_cache.dtype)
+    ins = [_cuda_tensor(t, n, k_cache.dtype) for t, n in ((q, "q"), (k, "k"), (v, "v"), (w, "w"))]
+    _cuda_tensor(beta, "beta", torch.float32)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=k_cache.dtype, device=k_cache.device)
+    _check(_load().path_decode_step_noalloc(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]),
+                                            _ptr(ins[3]), _ptr(beta), _ptr(k_cache),
+                                            _ptr(v_cache), B, H, int(cache_len), cap, d,
+                                            _dtype_code(k_cache), _scale(scale, d), _ptr(out),
+                                            _stream(stream, k_cache.device)),
+           "path_decode_step_noalloc")
+    return out

@@ -13,6 +13,8 @@
 // online softmax and o += p v in registers. The CTA merges its warps' partial softmax
 // states and writes (m, l, o) of the split. A second kernel (one CTA per head) appends
 // the new key/value, scores it and merges the splits.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace path {
@@ -208,6 +210,86 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const voi
         static_cast<T *>(out));
     return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------- no-allocation variant
+// Callers that cannot give this library any device memory of their own (a plugin inside
+// an engine whose allocator is not exposed to it, or a real-time loop that may not call
+// cudaMalloc because the call can synchronise the device) use this variant: its split
+// partials live in a fixed array compiled into the library. Every GPU that loads the
+// library holds these 16 MiB until the process exits. All calls on a device share the
+// array, so calls that overlap on that GPU (other streams, other host threads) race and
+// must be serialised by the caller. Nothing in the array has to start at zero: each call
+// writes every partial entry it later reads.
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the static scratch on the current device. The first call on a
+// device looks it up (host code only holds a stand-in for the symbol, never its device
+// address) and caches it; later calls reuse the cached pointer.
+static cudaError_t static_scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+size_t decode_static_scratch_bytes() { return kStaticScratchBytes; }
+
+size_t decode_static_scratch_needed(int BH, int cache_len) {
+    const size_t used = (size_t)((cache_len + kDecodeChunk - 1) / kDecodeChunk);
+    return (size_t)BH * used * (kD + 2) * sizeof(float);
+}
+
+// Same kernels as launch_decode, with the partials in the static scratch. The caller
+// has checked decode_static_scratch_needed() <= decode_static_scratch_bytes().
+template <typename T>
+cudaError_t launch_decode_static(const void *q, const void *k, const void *v, const void *w,
+                                 const float *beta, void *k_cache, void *v_cache, int BH,
+                                 int cache_len, int cap, float scale, void *out,
+                                 cudaStream_t stream) {
+    void *scratch = nullptr;
+    cudaError_t err = static_scratch_address(&scratch);
+    if (err != cudaSuccess) return err;
+    float *part = static_cast<float *>(scratch);
+    const float sl2 = scale * kLog2e;
+    const int used = (cache_len + kDecodeChunk - 1) / kDecodeChunk;
+    if (used > 0) {
+        dim3 grid(used, BH);
+        decode_split_kernel<T><<<grid, kThreads, 0, stream>>>(
+            static_cast<const T *>(q), static_cast<const T *>(w), beta, static_cast<T *>(k_cache),
+            static_cast<const T *>(v_cache), cache_len, cap, used, sl2, part);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    decode_merge_kernel<T><<<BH, kD, 0, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
+        static_cast<T *>(k_cache), static_cast<T *>(v_cache), cache_len, cap, used, sl2, part,
+        static_cast<T *>(out));
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_decode_static<float>(const void *, const void *, const void *,
+                                                 const void *, const float *, void *, void *,
+                                                 int, int, int, float, void *, cudaStream_t);
+template cudaError_t launch_decode_static<__nv_bfloat16>(const void *, const void *,
+                                                         const void *, const void *,
+                                                         const float *, void *, void *, int, int,
+                                                         int, float, void *, cudaStream_t);
 
 template cudaError_t launch_decode<float>(const void *, const void *, const void *, const void *,
                                           const float *, void *, void *, int, int, int, float,

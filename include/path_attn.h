@@ -137,6 +137,29 @@ path_status path_decode_step(const void *q, const void *k, const void *v, const 
                              void *out, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * path_decode_step without a workspace, for callers that cannot allocate device memory
+ * for this library: for instance a plugin inside an inference engine that owns all
+ * device memory through an allocator the plugin cannot reach, or a latency-bound loop
+ * that must not call cudaMalloc because it can synchronise the device. The paper has no
+ * counterpart; this is an interface convenience only.
+ * Same arguments and results as path_decode_step, minus ws/ws_bytes. The split partial
+ * results go to a fixed PATH_NOALLOC_SCRATCH_BYTES array compiled into the library, held
+ * by every GPU that loads the library until the process exits. Limit:
+ * B * H * ceil(cache_len / 1024) * 264 bytes <= PATH_NOALLOC_SCRATCH_BYTES (for example
+ * B*H = 1024 heads with up to 63488 cached keys); larger problems return
+ * PATH_ERR_WORKSPACE before any launch. The call allocates nothing. The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call outside any stream capture. All calls on a device share
+ * the array: calls that may overlap on the GPU (different streams or host threads) race
+ * and must be serialised by the caller. No part of the array needs to start at zero.
+ */
+#define PATH_NOALLOC_SCRATCH_BYTES (16u << 20)
+path_status path_decode_step_noalloc(const void *q, const void *k, const void *v, const void *w,
+                                     const float *beta, void *k_cache, void *v_cache, int B,
+                                     int H, int cache_len, int cache_cap, int d, int dtype,
+                                     float scale, void *out, void *stream);
+
+/*
  * Waits for `stream`, then reads and clears the status word that kernels of
  * earlier calls on this workspace wrote. Returns PATH_OK, PATH_ERR_TIMEOUT or
  * PATH_ERR_CUDA (if the synchronisation or the read failed).

@@ -108,3 +108,15 @@ def test_decode_argument_checks(so):
     assert call(kc=FAKE + 2) == 4
     assert call(ws_bytes=8) == 5
     assert call(B=0) == 0
+
+
+def test_noalloc_decode_rejects_problems_beyond_the_fixed_scratch(so):
+    # 4096 heads x 17 splits of 1024 keys x 264 B = 18.4 MB > 16 MiB: refused before any
+    # launch. The size is checked here first so that these never-dereferenced pointers
+    # cannot reach a kernel even if the numbers above were wrong.
+    B, H, n = 64, 64, 16 * 1024 + 1
+    need = B * H * (-(-n // 1024)) * 66 * 4
+    assert need > 16 << 20
+    rc = so.path_decode_step_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, n, n + 1,
+                                     64, 1, ctypes.c_float(0.125), FAKE, None)
+    assert rc == 5
