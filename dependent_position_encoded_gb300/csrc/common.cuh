@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,7 +23,8 @@ constexpr uint32_t kStatusTimeout = 7u;
 //   qt  : (BH, Lp, 64)        boundary-adjusted queries  q~_i = (H_start ... H_i) q_i
 //   kp  : (BH, nblk, 128, 64) rows 0-63 keys k~_j = H_end ... H_{j+1} k_j,
 //                             rows 64-127 the dense block transition P_b (row-major)
-//   dg  : (BH, nblk, 64, 64)  fp32 diagonal-block logits in log2 units (masked -inf)
+//   dg  : (BH, nblk, 64, 64)  diagonal-block logits in log2 units (masked -inf): fp16 for
+//                             bf16 inputs, fp32 for fp32 inputs
 //   c2  : (BH, Lp)            fp32 log2(e) * cumsum(log f) (PaTH-FoX only)
 // nblk is rounded up to an even count so that 128-row tiles are complete;
 // padded tokens carry identity transitions and zero queries and keys.
@@ -48,7 +50,7 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     lay.off_kp = off;
     off = align256(off + bh * lay.nblk * 2 * kC * kD * elt_bytes);
     lay.off_dg = off;
-    off = align256(off + bh * lay.nblk * kC * kC * sizeof(float));
+    off = align256(off + bh * lay.nblk * kC * kC * (elt_bytes == 2 ? 2 : 4));
     lay.off_c2 = off;
     if (fox) off = align256(off + bh * lay.Lp * sizeof(float));
     lay.total = off;

@@ -13,6 +13,11 @@ template <typename T>
 cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const float *beta,
                               const float *log_f, int BH, int L, float scale, void *ws,
                               cudaStream_t stream);
+cudaError_t launch_fox_cumsum(const float *log_f, int BH, int L, int elt_bytes, void *ws,
+                              cudaStream_t stream);
+cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, const float *beta,
+                                 const float *log_f, int BH, int L, float scale, void *ws,
+                                 uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int BH, int L,
                            float scale, void *ws, uint64_t limit_ns, int force_timeout,
                            cudaStream_t stream);
@@ -81,10 +86,12 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
     const float *lf = fox ? log_f : nullptr;
-    if (dtype == PATH_BF16)
-        return from_cuda(launch_ut_prepare<__nv_bfloat16>(q, k, w, beta, lf, B * H, L, scale, ws,
-                                                          stream));
-    return from_cuda(launch_ut_prepare<float>(q, k, w, beta, lf, B * H, L, scale, ws, stream));
+    cudaError_t e = (dtype == PATH_BF16)
+                        ? launch_ut_prepare_tc(q, k, w, beta, lf, B * H, L, scale, ws,
+                                               kWaitLimitNs, stream)
+                        : launch_ut_prepare<float>(q, k, w, beta, lf, B * H, L, scale, ws, stream);
+    if (e == cudaSuccess && fox) e = launch_fox_cumsum(lf, B * H, L, elt_bytes(dtype), ws, stream);
+    return from_cuda(e);
 }
 
 path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int H, int L, int d,

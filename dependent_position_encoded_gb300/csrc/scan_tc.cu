@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kScanThreads, 2)
 path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_kp,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __nv_bfloat16 *__restrict__ qt, const float *__restrict__ dg,
+                    const __nv_bfloat16 *__restrict__ qt, const __half *__restrict__ dg,
                     const float *__restrict__ c2, __nv_bfloat16 *__restrict__ out,
                     float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
                     uint32_t *status, uint64_t limit_ns, int force_timeout) {
@@ -310,15 +310,19 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
             if (from_diag) {
                 if (diag_row >= 0) {
-                    const float4 *src = reinterpret_cast<const float4 *>(
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
                         dg + (((head * nblk + diag_blk) * kC) + diag_row) * kC);
 #pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4) {
-                        const float4 c = __ldg(src + q4);
-                        x[4 * q4 + 0] = c.x;
-                        x[4 * q4 + 1] = c.y;
-                        x[4 * q4 + 2] = c.z;
-                        x[4 * q4 + 3] = c.w;
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const uint4 c = __ldg(src + q8);
+                        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f =
+                                __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
+                            x[8 * q8 + 2 * e] = f.x;
+                            x[8 * q8 + 2 * e + 1] = f.y;
+                        }
                     }
                 } else {
 #pragma unroll
@@ -469,7 +473,7 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
     dim3 grid(lay.nblk / 2, BH);
     kern<<<grid, kScanThreads, kScanSmemBytes, stream>>>(
         tm_qt, tm_kp, tm_v, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
-        reinterpret_cast<const float *>(basep + lay.off_dg),
+        reinterpret_cast<const __half *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e,
         reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout);

@@ -1,4 +1,6 @@
-// K1: per-block UT preprocessing of PaTH attention.
+// K1 (fp32 dtype): per-block UT preprocessing of PaTH attention in fp32 FFMA. bf16 inputs
+// use the tensor-core version (ut_prepare_tc.cu); the fp32 workload's 1e-4 tolerance
+// rules out 16-bit operands, so this kernel keeps every product in fp32.
 //
 // For every block of C = 64 tokens of one head (technical summary "技術要約: PaTH
 // Attention" §3 "UT変換による表現" and the block-wise algorithm below it; review
@@ -339,18 +341,20 @@ cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const
         log_f, L, lay.Lp, lay.nblk, scale * kLog2e, reinterpret_cast<T *>(base + lay.off_qt),
         reinterpret_cast<T *>(base + lay.off_kp), reinterpret_cast<float *>(base + lay.off_dg),
         reinterpret_cast<uint32_t *>(base));
-    err = cudaGetLastError();
-    if (err != cudaSuccess || log_f == nullptr) return err;
-    fox_cumsum_kernel<<<BH, 1024, 0, stream>>>(log_f, L, lay.Lp,
-                                               reinterpret_cast<float *>(base + lay.off_c2));
+    return cudaGetLastError();
+}
+
+// PaTH-FoX: log2(e) * inclusive prefix sums of log f per head into the workspace.
+cudaError_t launch_fox_cumsum(const float *log_f, int BH, int L, int elt_bytes, void *ws,
+                              cudaStream_t stream) {
+    const FwdLayout lay = fwd_layout(1, BH, L, elt_bytes, true);
+    fox_cumsum_kernel<<<BH, 1024, 0, stream>>>(
+        log_f, L, lay.Lp, reinterpret_cast<float *>(static_cast<char *>(ws) + lay.off_c2));
     return cudaGetLastError();
 }
 
 template cudaError_t launch_ut_prepare<float>(const void *, const void *, const void *,
                                               const float *, const float *, int, int, float,
                                               void *, cudaStream_t);
-template cudaError_t launch_ut_prepare<__nv_bfloat16>(const void *, const void *, const void *,
-                                                      const float *, const float *, int, int,
-                                                      float, void *, cudaStream_t);
 
 }  // namespace path

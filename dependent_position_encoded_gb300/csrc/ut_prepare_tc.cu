@@ -1,0 +1,450 @@
+// K1 (bf16): per-block UT preprocessing of PaTH attention on tcgen05 tensor cores.
+//
+// Technical summary "技術要約: PaTH Attention" §3 ("UT変換による表現": the product of a
+// block's transitions is I - W^T T^{-1} W with T triangular and built from beta; the
+// block-wise algorithm precomputes boundary-adjusted queries and keys per block). For one
+// block of 64 tokens of one head (W, Q, K rows = w_s, q_i, k_j; D = diag(beta)):
+//   G  = W W^T,  A = (I + D strictly-upper(G))^{-1} D        (fp32 triangular solve)
+//   Lq = lower-incl(Q W^T),  Rk = strictly-upper(K W^T)
+//   U  = A^T W,  V' = A W,  Khat = Rk A
+//   q~ = Q - Lq U            (rows: (H_0 ... H_i) q_i)
+//   k~ = K - Rk V'           (rows: (H_{j+1} ... H_63)^T k_j)
+//   P_b = I - W^T V'         (H_0 ... H_63, dense)
+//   diag logits (j <= i) = scale * (Q K^T - Lq Khat^T) [+ sum_{s=j+1..i} log f_s]
+// Lq U equals (Lq A^T) W and Lq Khat^T equals Lq A^T Rk^T, the leading/trailing partial
+// products of the UT form (sub-blocks of A invert the matching sub-blocks of T).
+//
+// Four tcgen05.mma groups, all M = 128 (operand tiles are stacked so that one MMA serves
+// two products), with 64x64 16-bit tiles in 128-byte-swizzled shared memory:
+//   MMA1 (bf16): [Q; W] x [W; K]^T         -> Q W^T | Q K^T  /  W W^T | W K^T
+//   MMA3 (fp16): [A^T; A] x [W | Rk^T]     -> U | Khat^T     /  V' | (unused)
+//   MMA4 (fp16): Lq x [U | Khat^T]          -> Lq U | Lq Khat^T
+//                [W^T; Rk] x V'             -> W^T V'         /  Rk V'
+// The second-level operands (A, Lq, Rk, U, V', Khat, W) are rounded to fp16 (11-bit
+// significand; every one of them is bounded: |A_su| <= beta_s beta_u <= 4), fp32
+// accumulation throughout. One CTA of 128 threads per (block, head): thread r owns TMEM
+// lane r; thread 0 issues the TMA loads and the MMAs. 256 TMEM columns.
+#include "common.cuh"
+
+namespace path {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr uint32_t kT = 8192;  // one 64 x 64 16-bit tile
+
+// Shared-memory tile offsets (from the 1024-aligned base). Adjacent pairs are required
+// by the stacked operands: [Q; W] and [W; K] (MMA1), [W16 | RkT] and [W16; RkT] (MMA3 B
+// and MMA4 A, atom stride 8 KB), [AT; A] (MMA3 A), [U | KhT] (MMA4 B).
+constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_W16 = 3 * kT, T_RKT = 4 * kT,
+                   T_LQ = 5 * kT, T_AT = 6 * kT, T_A = 7 * kT, T_U = 8 * kT, T_KHT = 9 * kT,
+                   T_V = 10 * kT;
+constexpr uint32_t G_OFF = T_U;            // fp32 G (64 x 68) overlays T_U.. during the solve
+constexpr int GLD = 68;
+constexpr uint32_t BAR_OFF = 11 * kT;      // 2 mbarriers
+constexpr uint32_t SLOT_OFF = BAR_OFF + 16;
+constexpr uint32_t BETA_OFF = SLOT_OFF + 16;
+constexpr uint32_t LC_OFF = BETA_OFF + 256;
+constexpr uint32_t kSmemBytes = LC_OFF + 256 + 1024;
+
+static_assert(G_OFF + kC * GLD * 4 <= T_V + kT, "G overlay stays inside the scratch tiles");
+
+// idesc for kind::f16 with both operands bf16 (fmt 1) or fp16 (fmt 0)
+__host__ __device__ constexpr uint32_t idesc16(int M, int N, uint32_t fmt, bool a_mn, bool b_mn,
+                                               bool neg_a = false) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((neg_a ? 1u : 0u) << 13) |
+           ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Writes 64 fp32 values as one 16-bit row (fp16 or bf16) of a swizzled tile.
+template <bool HALF>
+__device__ __forceinline__ void store_row16(uint8_t *tile, int row, const float *x) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 u;
+        const float *s = x + 8 * c;
+        if (HALF) {
+            u.x = pack_h2(s[0], s[1]); u.y = pack_h2(s[2], s[3]);
+            u.z = pack_h2(s[4], s[5]); u.w = pack_h2(s[6], s[7]);
+        } else {
+            u.x = pack_bf16x2(s[0], s[1]); u.y = pack_bf16x2(s[2], s[3]);
+            u.z = pack_bf16x2(s[4], s[5]); u.w = pack_bf16x2(s[6], s[7]);
+        }
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c)) = u;
+    }
+}
+
+// Reads one bf16 row of a swizzled tile as 64 fp32 values.
+__device__ __forceinline__ void load_row_bf16(const uint8_t *tile, int row, float *x) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_offset(row, c));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            x[8 * c + 2 * e] = f.x;
+            x[8 * c + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+// 64 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_row64(uint32_t taddr, float *x) {
+    uint32_t a[32], b[32];
+    tmem_ld32(taddr, a);
+    tmem_ld32(taddr + 32, b);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        x[j] = __uint_as_float(a[j]);
+        x[32 + j] = __uint_as_float(b[j]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ beta,
+                     const float *__restrict__ log_f, int L, int Lp, int nblk, float scale_log2,
+                     __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ kp,
+                     __half *__restrict__ dg, uint32_t *status, uint64_t limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const sm = smem_raw + (base - raw);
+    float *const Gs = reinterpret_cast<float *>(sm + G_OFF);
+    float *const bs = reinterpret_cast<float *>(sm + BETA_OFF);
+    float *const lc = reinterpret_cast<float *>(sm + LC_OFF);
+    uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + SLOT_OFF);
+    const uint32_t bar_tma = base + BAR_OFF, bar_mma = base + BAR_OFF + 8;
+
+    const int r = threadIdx.x, warp = r >> 5;
+    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = blk * kC;
+    const size_t head = (size_t)bh * L;
+    if (blk == 0 && bh == 0 && r == 0 && status) *status = 0u;
+
+    __shared__ uint32_t abort_s;
+    if (r == 0) {
+        abort_s = 0u;
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_w);
+        mbar_arrive_expect_tx(bar_tma, 3 * kT);
+        tma_load_3d(base + T_Q, &tm_q, bar_tma, 0, t0, bh);
+        tma_load_3d(base + T_W, &tm_w, bar_tma, 0, t0, bh);
+        tma_load_3d(base + T_K, &tm_k, bar_tma, 0, t0, bh);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    if (r < kC) {
+        const int t = t0 + r;
+        bs[r] = (t < L) ? beta[head + t] : 0.f;
+    }
+    if (log_f != nullptr && warp == 1) {
+        const int ln = r - 32;
+        const int ta = t0 + 2 * ln, tb = ta + 1;
+        const float a = (ta < L) ? log_f[head + ta] : 0.f;
+        const float b = ((tb < L) ? log_f[head + tb] : 0.f) + a;
+        float run = b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, run, o);
+            if (ln >= o) run += n;
+        }
+        lc[2 * ln] = run - b + a;
+        lc[2 * ln + 1] = run;
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+
+    // bounded wait used by every thread; a timeout skips the remaining work
+    auto wait_all = [&](uint32_t bar, uint32_t par) {
+        bool ok = mbar_try_wait(bar, par);
+        if (!ok) {
+            const uint64_t tstart = globaltimer_ns();
+            while (!(ok = mbar_try_wait(bar, par)) && globaltimer_ns() - tstart < limit_ns) {
+            }
+        }
+        if (!ok) {
+            report_status(status, kStatusTimeout);
+            abort_s = 1u;
+        }
+        __syncthreads();
+        return abort_s == 0u;
+    };
+
+    // ---- MMA1: [Q; W] x [W; K]^T (bf16)
+    if (r == 0) {
+        const uint64_t t0s = globaltimer_ns();
+        bool ok = mbar_try_wait(bar_tma, 0);
+        while (!ok && globaltimer_ns() - t0s < limit_ns) ok = mbar_try_wait(bar_tma, 0);
+        if (ok) {
+            tc_fence_after();
+            const uint64_t a = sdesc_sw128(base + T_Q, 16, 1024);
+            const uint64_t b = sdesc_sw128(base + T_W, 16, 1024);
+            constexpr uint32_t ID = idesc16(128, 128, 1, false, false);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 2 * kk, b + 2 * kk, ID, kk > 0);
+        } else {
+            report_status(status, kStatusTimeout);
+        }
+        umma_commit(bar_mma);
+    }
+    bool ok = wait_all(bar_mma, 0);
+    if (ok) {
+        tc_fence_after();
+        float x[64];
+        if (r < kC) {
+            // row i of Q W^T -> Lq (u <= i), fp16
+            tmem_row64(tmem + lane_off, x);
+#pragma unroll
+            for (int u = 0; u < 64; ++u)
+                if (u > r) x[u] = 0.f;
+            store_row16<true>(sm + T_LQ, r, x);
+        } else {
+            const int s = r - kC;
+            // row s of W W^T -> G (fp32), row s of W K^T -> Rk^T (s > j), fp16
+            tmem_row64(tmem + lane_off, x);
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4)
+                *reinterpret_cast<float4 *>(Gs + s * GLD + 4 * q4) =
+                    make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+            tmem_row64(tmem + lane_off + 64, x);
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                if (s <= j) x[j] = 0.f;
+            store_row16<true>(sm + T_RKT, s, x);
+            // fp16 copy of W (MMA3 and MMA4 take fp16 operands only)
+            load_row_bf16(sm + T_W, s, x);
+            store_row16<true>(sm + T_W16, s, x);
+        }
+    }
+    __syncthreads();
+
+    // ---- A = (I + D N)^{-1} D, column u per thread (threads 0-63), fp32:
+    //      A[u][u] = beta_u;  A[s][u] = -beta_s sum_{v=s+1..63} G[s][v] A[v][u]  (s < u)
+    if (ok && r < kC) {
+        const int u = r;
+        float a[64];
+#pragma unroll
+        for (int s = 63; s >= 0; --s) {
+            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+            for (int v = s + 1; v < 64; ++v) {
+                const float g = Gs[s * GLD + v];
+                switch ((v - s - 1) & 3) {
+                    case 0: acc0 = fmaf(g, a[v], acc0); break;
+                    case 1: acc1 = fmaf(g, a[v], acc1); break;
+                    case 2: acc2 = fmaf(g, a[v], acc2); break;
+                    default: acc3 = fmaf(g, a[v], acc3); break;
+                }
+            }
+            const float sum = (acc0 + acc1) + (acc2 + acc3);
+            a[s] = (s == u) ? bs[s] : ((s < u) ? -bs[s] * sum : 0.f);
+        }
+        // A^T row u (contiguous over s) and column u of A
+        store_row16<true>(sm + T_AT, u, a);
+        uint8_t *ta = sm + T_A;
+#pragma unroll
+        for (int s = 0; s < 64; ++s) {
+            const uint32_t off = sw128_offset(s, u >> 3) + 2 * (u & 7);
+            *reinterpret_cast<__half *>(ta + off) = __float2half_rn(a[s]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA3: [A^T; A] x [W | Rk^T] (fp16, B MN-major, N = 128)
+    if (r == 0 && ok) {
+        tc_fence_after();
+        const uint64_t a = sdesc_sw128(base + T_AT, 16, 1024);
+        const uint64_t b = sdesc_sw128(base + T_W16, kT, 1024);
+        constexpr uint32_t ID = idesc16(128, 128, 0, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 128, a + 2 * kk, b + 128 * kk, ID, kk > 0);
+    }
+    if (r == 0) umma_commit(bar_mma);
+    if (ok) ok = wait_all(bar_mma, 1);
+    if (ok) {
+        tc_fence_after();
+        float x[64];
+        if (r < kC) {
+            tmem_row64(tmem + lane_off + 128, x);  // U row u
+            store_row16<true>(sm + T_U, r, x);
+            tmem_row64(tmem + lane_off + 192, x);  // Khat^T row u
+            store_row16<true>(sm + T_KHT, r, x);
+        } else {
+            tmem_row64(tmem + lane_off + 128, x);  // V' row s
+            store_row16<true>(sm + T_V, r - kC, x);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA4: Lq x [U | Khat^T] -> cols 128..255;  [W^T; Rk] x V' -> cols 0..63
+    if (r == 0 && ok) {
+        tc_fence_after();
+        const uint64_t a1 = sdesc_sw128(base + T_LQ, 16, 1024);
+        const uint64_t b1 = sdesc_sw128(base + T_U, kT, 1024);
+        constexpr uint32_t ID1 = idesc16(128, 128, 0, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 128, a1 + 2 * kk, b1 + 128 * kk, ID1, kk > 0);
+        const uint64_t a2 = sdesc_sw128(base + T_W16, kT, 1024);
+        const uint64_t b2 = sdesc_sw128(base + T_V, 1024, 1024);
+        constexpr uint32_t ID2 = idesc16(128, 64, 0, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a2 + 128 * kk, b2 + 128 * kk, ID2, kk > 0);
+    }
+    if (r == 0) umma_commit(bar_mma);
+    if (ok) ok = wait_all(bar_mma, 0);
+
+    // ---- epilogue
+    if (ok) {
+        tc_fence_after();
+        const size_t blk_base = (size_t)bh * nblk + blk;
+        __nv_bfloat16 *kp_blk = kp + blk_base * (2 * kC) * kD;
+        float x[64], y[64];
+        if (r < kC) {
+            const int i = r;
+            // q~_i = q_i - (Lq U)_i
+            load_row_bf16(sm + T_Q, i, y);
+            tmem_row64(tmem + lane_off + 128, x);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) y[c] -= x[c];
+            uint4 *dq = reinterpret_cast<uint4 *>(qt + ((size_t)bh * Lp + t0 + i) * kD);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                dq[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]),
+                                   pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
+                                   pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
+                                   pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
+            // diagonal logits, log2 units: scale (q_i.k_j - (Lq Khat^T)_ij) [+ FoX], j <= i
+            tmem_row64(tmem + lane_off + 64, y);    // Q K^T row i (from MMA1)
+            tmem_row64(tmem + lane_off + 192, x);   // Lq Khat^T row i
+            const float lci = (log_f != nullptr) ? lc[i] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                float v = scale_log2 * (y[j] - x[j]);
+                if (log_f != nullptr) v += kLog2e * (lci - lc[j]);
+                y[j] = (j <= i && t0 + j < L) ? v : -INFINITY;
+            }
+            uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                dd[c] = make_uint4(pack_h2(y[8 * c], y[8 * c + 1]), pack_h2(y[8 * c + 2], y[8 * c + 3]),
+                                   pack_h2(y[8 * c + 4], y[8 * c + 5]), pack_h2(y[8 * c + 6], y[8 * c + 7]));
+            // P_b row n = i: delta - (W^T V')_n
+            tmem_row64(tmem + lane_off, x);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) x[c] = (c == i ? 1.f : 0.f) - x[c];
+            uint4 *dp = reinterpret_cast<uint4 *>(kp_blk + (kC + i) * kD);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                dp[c] = make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]),
+                                   pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                                   pack_bf16x2(x[8 * c + 4], x[8 * c + 5]),
+                                   pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+        } else {
+            const int j = r - kC;
+            // k~_j = k_j - (Rk V')_j
+            load_row_bf16(sm + T_K, j, y);
+            tmem_row64(tmem + lane_off, x);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) y[c] -= x[c];
+            uint4 *dk = reinterpret_cast<uint4 *>(kp_blk + j * kD);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                dk[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]),
+                                   pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
+                                   pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
+                                   pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// (heads, L rows, 64 columns) bf16 input, 64-row boxes, 128-byte swizzle; rows past L
+// read as zero.
+bool make_input_map(CUtensorMap *m, const void *ptr, int L, int heads) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)L * kD * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)kC, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, const float *beta,
+                                 const float *log_f, int BH, int L, float scale, void *ws,
+                                 uint64_t limit_ns, cudaStream_t stream) {
+    const FwdLayout lay = fwd_layout(1, BH, L, 2, log_f != nullptr);
+    char *basep = static_cast<char *>(ws);
+    CUtensorMap tq, tk, tw;
+    if (!make_input_map(&tq, q, L, BH) || !make_input_map(&tk, k, L, BH) ||
+        !make_input_map(&tw, w, L, BH))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(ut_prepare_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    dim3 grid(lay.nblk, BH);
+    ut_prepare_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
+        tq, tk, tw, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
+        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_qt),
+        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_kp),
+        reinterpret_cast<__half *>(basep + lay.off_dg), reinterpret_cast<uint32_t *>(basep),
+        limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace path

@@ -124,6 +124,85 @@ def test_empty_problem_is_a_no_op(lib):
     assert out.shape == (1, 2, 0, 64)
 
 
+# ---------------------------------------------------------------- preprocessing factors
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+def _block_reference(q, k, w, beta, log_f, t0, L, scale):
+    """fp64 boundary-adjusted rows, dense block transition and diagonal logits (log2
+    units) of the 64-token block starting at t0, by explicit Householder products."""
+    d = q.shape[1]
+    H = [np.eye(d) - beta[t] * np.outer(w[t], w[t]) if t < L else np.eye(d)
+         for t in range(t0, t0 + 64)]
+    qt = np.zeros((64, d)); kt = np.zeros((64, d)); D = np.full((64, 64), -np.inf)
+    P = np.eye(d)
+    for m in H:
+        P = P @ m
+    for i in range(64):
+        if t0 + i >= L:
+            continue
+        x = q[t0 + i].copy()
+        for s in range(i, -1, -1):      # (H_0 ... H_i) q_i: H_i first
+            x = H[s] @ x
+        qt[i] = x
+        y = k[t0 + i].copy()
+        for s in range(i + 1, 64):      # H_63 ... H_{i+1} k_i: H_{i+1} first
+            y = H[s] @ y
+        kt[i] = y
+    for i in range(64):
+        if t0 + i >= L:
+            continue
+        x = q[t0 + i].copy()
+        bias = 0.0
+        for j in range(i, -1, -1):
+            D[i, j] = scale * (k[t0 + j] @ x) * 1.4426950408889634
+            if log_f is not None:
+                D[i, j] += bias * 1.4426950408889634
+                bias += log_f[t0 + j]
+            x = H[j] @ x
+    return qt, kt, P, D
+
+
+@pytest.mark.parametrize("L,fox", [(64, False), (200, False), (130, True)])
+def test_prepare_factors_match_explicit_products(lib, L, fox):
+    B, H = 1, 2
+    x = pi.make_fwd_inputs(B, H, L, seed=50 + L, fox=fox, device="cuda")
+    ws = lib.new_workspace(lib.OP_FOX_FWD if fox else lib.OP_FWD, B, H, L, lib.BF16, "cuda")
+    ws.zero_()
+    lib.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws, log_f=x.get("log_f"))
+    torch.cuda.synchronize()
+    nb = (L + 63) // 64
+    nblk = nb + (nb & 1)
+    Lp = nblk * 64
+    BH = B * H
+    off_qt = 256
+    off_kp = _align256(off_qt + BH * Lp * 64 * 2)
+    off_dg = _align256(off_kp + BH * nblk * 128 * 64 * 2)
+    qt = ws[off_qt:off_qt + BH * Lp * 64 * 2].view(torch.bfloat16).reshape(BH, Lp, 64)
+    kp = ws[off_kp:off_kp + BH * nblk * 128 * 64 * 2].view(torch.bfloat16).reshape(
+        BH, nblk, 128, 64)
+    dg = ws[off_dg:off_dg + BH * nblk * 64 * 64 * 2].view(torch.float16).reshape(
+        BH, nblk, 64, 64)
+    h = {k_: v.reshape(BH, L, *v.shape[3:]).double().cpu().numpy() for k_, v in x.items()}
+    for bh in range(BH):
+        for b in range(nb):
+            rq, rk, rP, rD = _block_reference(h["q"][bh], h["k"][bh], h["w"][bh], h["beta"][bh],
+                                              h["log_f"][bh] if fox else None, 64 * b, L, 0.125)
+            n = min(64, L - 64 * b)
+            gq = qt[bh, 64 * b:64 * b + n].double().cpu().numpy()
+            gk = kp[bh, b, :n].double().cpu().numpy()
+            gP = kp[bh, b, 64:].double().cpu().numpy()
+            gD = dg[bh, b, :n].double().cpu().numpy()
+            assert np.abs(gq - rq[:n]).max() <= 2e-2
+            assert np.abs(gk - rk[:n]).max() <= 2e-2
+            assert np.abs(gP - rP).max() <= 1e-2
+            fin = np.isfinite(rD[:n])
+            assert np.array_equal(fin, np.isfinite(gD))
+            assert np.abs(gD[fin] - rD[:n][fin]).max() <= 2e-2
+
+
 # ---------------------------------------------------------------- full-size workloads, sampled rows
 
 def _sampled_parity(lib, wl, n_heads=12, n_rows=600, seed=0):
