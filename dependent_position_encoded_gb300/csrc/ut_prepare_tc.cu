@@ -4,7 +4,7 @@
 // block's transitions is I - W^T T^{-1} W with T triangular and built from beta; the
 // block-wise algorithm precomputes boundary-adjusted queries and keys per block). For one
 // block of 64 tokens of one head (W, Q, K rows = w_s, q_i, k_j; D = diag(beta)):
-//   G  = W W^T,  A = (I + D strictly-upper(G))^{-1} D        (fp32 triangular solve)
+//   G  = W W^T,  E = D strictly-upper(G),  A = (I + E)^{-1} D      (fp32)
 //   Lq = lower-incl(Q W^T),  Rk = strictly-upper(K W^T)
 //   U  = A^T W,  V' = A W,  Khat = Rk A
 //   q~ = Q - Lq U            (rows: (H_0 ... H_i) q_i)
@@ -14,16 +14,21 @@
 // Lq U equals (Lq A^T) W and Lq Khat^T equals Lq A^T Rk^T, the leading/trailing partial
 // products of the UT form (sub-blocks of A invert the matching sub-blocks of T).
 //
-// Four tcgen05.mma groups, all M = 128 (operand tiles are stacked so that one MMA serves
-// two products), with 64x64 16-bit tiles in 128-byte-swizzled shared memory:
-//   MMA1 (bf16): [Q; W] x [W; K]^T         -> Q W^T | Q K^T  /  W W^T | W K^T
-//   MMA3 (fp16): [A^T; A] x [W | Rk^T]     -> U | Khat^T     /  V' | (unused)
-//   MMA4 (fp16): Lq x [U | Khat^T]          -> Lq U | Lq Khat^T
-//                [W^T; Rk] x V'             -> W^T V'         /  Rk V'
-// The second-level operands (A, Lq, Rk, U, V', Khat, W) are rounded to fp16 (11-bit
-// significand; every one of them is bounded: |A_su| <= beta_s beta_u <= 4), fp32
-// accumulation throughout. One CTA of 128 threads per (block, head): thread r owns TMEM
-// lane r; thread 0 issues the TMA loads and the MMAs. 256 TMEM columns.
+// (I + E)^{-1} is formed blockwise: the four 16 x 16 diagonal blocks by back-substitution,
+// then X12 = -X11 E12 X22 for the 16-blocks and for the 32-blocks (fp32). Every factor is
+// bounded (X_su = A_su / beta_u), so no intermediate grows.
+//
+// tcgen05.mma groups, all M = 128, with 64x64 16-bit tiles in 128-byte-swizzled shared
+// memory (K-major tiles stacked in M must be adjacent; MN-major atoms use the LBO stride):
+//   MMA1 (bf16):  [Q; W] x [W; K]^T          -> Q W^T | (Q K^T)  /  W W^T | W K^T
+//   MMA3 (fp16):  [A^T; A] x [W | Rk^T]      -> U | Khat^T       /  V' | (unused)
+//   MMA4x:        Lq x U (fp16)              -> Lq U
+//                 Q x K^T (bf16) - Lq x Khat^T (fp16), one accumulator -> diag logits
+//   MMA4y (fp16): [W^T; Rk] x V'             -> W^T V'          /  Rk V'
+// Second-level operands are fp16 (11-bit significand; all bounded, |A_su| <= 4), fp32
+// accumulation. One CTA of 128 threads per (block, head), thread r owns TMEM lane r,
+// thread 0 issues the TMA loads and the MMAs. 128 TMEM columns and 64 KB of tiles, so
+// three CTAs share an SM.
 #include "common.cuh"
 
 namespace path {
@@ -33,21 +38,22 @@ namespace {
 constexpr int kThreads = 128;
 constexpr uint32_t kT = 8192;  // one 64 x 64 16-bit tile
 
-// Shared-memory tile offsets (from the 1024-aligned base). Adjacent pairs are required
-// by the stacked operands: [Q; W] and [W; K] (MMA1), [W16 | RkT] and [W16; RkT] (MMA3 B
-// and MMA4 A, atom stride 8 KB), [AT; A] (MMA3 A), [U | KhT] (MMA4 B).
-constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_W16 = 3 * kT, T_RKT = 4 * kT,
-                   T_LQ = 5 * kT, T_AT = 6 * kT, T_A = 7 * kT, T_U = 8 * kT, T_KHT = 9 * kT,
-                   T_V = 10 * kT;
-constexpr uint32_t G_OFF = T_U;            // fp32 G (64 x 68) overlays T_U.. during the solve
-constexpr int GLD = 68;
-constexpr uint32_t BAR_OFF = 11 * kT;      // 2 mbarriers
+// Tile slots (from the 1024-aligned base). Q, W, K adjacent (MMA1 A = [Q; W], B = [W; K]);
+// AT, A adjacent (MMA3 A). U, KhT, V reuse the slots of AT, A and the solve scratch.
+constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_RKT = 3 * kT, T_LQ = 4 * kT,
+                   T_AT = 5 * kT, T_A = 6 * kT, T_U = 5 * kT, T_KHT = 6 * kT, T_V = 7 * kT;
+constexpr uint32_t SCR = 5 * kT;           // solve scratch (E/X fp32 + Y) overlays slots 5-7
+constexpr int XLD = 68;
+constexpr uint32_t Y_OFF = SCR + 64 * XLD * 4;
+constexpr int YLD = 36;
+constexpr uint32_t BAR_OFF = 8 * kT;       // 2 mbarriers
 constexpr uint32_t SLOT_OFF = BAR_OFF + 16;
 constexpr uint32_t BETA_OFF = SLOT_OFF + 16;
 constexpr uint32_t LC_OFF = BETA_OFF + 256;
 constexpr uint32_t kSmemBytes = LC_OFF + 256 + 1024;
+constexpr uint32_t kTmemCols = 128;
 
-static_assert(G_OFF + kC * GLD * 4 <= T_V + kT, "G overlay stays inside the scratch tiles");
+static_assert(Y_OFF + 32 * YLD * 4 <= 8 * kT, "solve scratch fits in slots 5-7");
 
 // idesc for kind::f16 with both operands bf16 (fmt 1) or fp16 (fmt 0)
 __host__ __device__ constexpr uint32_t idesc16(int M, int N, uint32_t fmt, bool a_mn, bool b_mn,
@@ -108,7 +114,100 @@ __device__ __forceinline__ void tmem_row64(uint32_t taddr, float *x) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void store_global_row(__nv_bfloat16 *dst, const float *y) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        d[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]), pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
+                          pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
+                          pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
+}
+
+// (I + E)^{-1} in place over E (upper triangle; E is zero on and below the diagonal),
+// all 128 threads. On return X[s][u] (s <= u) holds the inverse.
+__device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, int r) {
+    // level 0: the four 16 x 16 diagonal blocks, one column per thread
+    float x[16];
+    const int u = r & 63, b0 = (u >> 4) << 4, lu = u & 15;
+    if (r < 64) {
+#pragma unroll
+        for (int l = 15; l >= 0; --l) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = l + 1; m < 16; ++m) acc = fmaf(X[(b0 + l) * XLD + b0 + m], x[m], acc);
+            x[l] = (l == lu) ? 1.f : ((l < lu) ? -acc : 0.f);
+        }
+    }
+    __syncthreads();
+    if (r < 64) {
+#pragma unroll
+        for (int l = 0; l < 16; ++l) X[(b0 + l) * XLD + u] = x[l];
+    }
+    __syncthreads();
+    // level 1: X[16p', 16p'+16..] = -X11 E12 X22 for the two 32-blocks p
+    {
+        const int p = r >> 6, q = r & 63, i = q >> 2, c0 = (q & 3) * 4;
+        const int o = 32 * p;
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float e = X[(o + i) * XLD + o + 16 + m];
+            const float4 xr = *reinterpret_cast<const float4 *>(X + (o + 16 + m) * XLD + o + 16 + c0);
+            y[0] = fmaf(e, xr.x, y[0]); y[1] = fmaf(e, xr.y, y[1]);
+            y[2] = fmaf(e, xr.z, y[2]); y[3] = fmaf(e, xr.w, y[3]);
+        }
+        *reinterpret_cast<float4 *>(Y + (16 * p + i) * YLD + c0) = make_float4(y[0], y[1], y[2], y[3]);
+        __syncthreads();
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float xv = X[(o + i) * XLD + o + m];
+            const float4 yr = *reinterpret_cast<const float4 *>(Y + (16 * p + m) * YLD + c0);
+            z[0] = fmaf(xv, yr.x, z[0]); z[1] = fmaf(xv, yr.y, z[1]);
+            z[2] = fmaf(xv, yr.z, z[2]); z[3] = fmaf(xv, yr.w, z[3]);
+        }
+        *reinterpret_cast<float4 *>(X + (o + i) * XLD + o + 16 + c0) =
+            make_float4(-z[0], -z[1], -z[2], -z[3]);
+    }
+    __syncthreads();
+    // level 2: X[0:32, 32:64] = -X[0:32, 0:32] E[0:32, 32:64] X[32:64, 32:64]
+    {
+        const int i = r >> 2, c0 = (r & 3) * 8;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 32; ++m) {
+            const float e = X[i * XLD + 32 + m];
+            const float4 a = *reinterpret_cast<const float4 *>(X + (32 + m) * XLD + 32 + c0);
+            const float4 b = *reinterpret_cast<const float4 *>(X + (32 + m) * XLD + 36 + c0);
+            y[0] = fmaf(e, a.x, y[0]); y[1] = fmaf(e, a.y, y[1]);
+            y[2] = fmaf(e, a.z, y[2]); y[3] = fmaf(e, a.w, y[3]);
+            y[4] = fmaf(e, b.x, y[4]); y[5] = fmaf(e, b.y, y[5]);
+            y[6] = fmaf(e, b.z, y[6]); y[7] = fmaf(e, b.w, y[7]);
+        }
+        *reinterpret_cast<float4 *>(Y + i * YLD + c0) = make_float4(y[0], y[1], y[2], y[3]);
+        *reinterpret_cast<float4 *>(Y + i * YLD + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 32; ++m) {
+            const float xv = X[i * XLD + m];
+            const float4 a = *reinterpret_cast<const float4 *>(Y + m * YLD + c0);
+            const float4 b = *reinterpret_cast<const float4 *>(Y + m * YLD + c0 + 4);
+            y[0] = fmaf(xv, a.x, y[0]); y[1] = fmaf(xv, a.y, y[1]);
+            y[2] = fmaf(xv, a.z, y[2]); y[3] = fmaf(xv, a.w, y[3]);
+            y[4] = fmaf(xv, b.x, y[4]); y[5] = fmaf(xv, b.y, y[5]);
+            y[6] = fmaf(xv, b.z, y[6]); y[7] = fmaf(xv, b.w, y[7]);
+        }
+        *reinterpret_cast<float4 *>(X + i * XLD + 32 + c0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+        *reinterpret_cast<float4 *>(X + i * XLD + 36 + c0) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 3)
 ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ beta,
@@ -119,7 +218,8 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const sm = smem_raw + (base - raw);
-    float *const Gs = reinterpret_cast<float *>(sm + G_OFF);
+    float *const X = reinterpret_cast<float *>(sm + SCR);
+    float *const Y = reinterpret_cast<float *>(sm + Y_OFF);
     float *const bs = reinterpret_cast<float *>(sm + BETA_OFF);
     float *const lc = reinterpret_cast<float *>(sm + LC_OFF);
     uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + SLOT_OFF);
@@ -147,7 +247,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tma_load_3d(base + T_K, &tm_k, bar_tma, 0, t0, bh);
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(slot), 256);
+        tmem_alloc(smem_u32(slot), kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -190,7 +290,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         return abort_s == 0u;
     };
 
-    // ---- MMA1: [Q; W] x [W; K]^T (bf16)
+    // ---- MMA1: [Q; W] x [W; K]^T (bf16) -> cols 0..127
     if (r == 0) {
         const uint64_t t0s = globaltimer_ns();
         bool ok = mbar_try_wait(bar_tma, 0);
@@ -220,66 +320,62 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             store_row16<true>(sm + T_LQ, r, x);
         } else {
             const int s = r - kC;
-            // row s of W W^T -> G (fp32), row s of W K^T -> Rk^T (s > j), fp16
+            // row s of W W^T -> E = beta_s G[s][v] for v > s (fp32 scratch)
             tmem_row64(tmem + lane_off, x);
+            const float bsv = bs[s];
 #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4)
-                *reinterpret_cast<float4 *>(Gs + s * GLD + 4 * q4) =
-                    make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+            for (int q4 = 0; q4 < 16; ++q4) {
+                float e[4];
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int v = 4 * q4 + e4;
+                    e[e4] = (v > s) ? bsv * x[v] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(X + s * XLD + 4 * q4) = make_float4(e[0], e[1], e[2], e[3]);
+            }
+            // row s of W K^T -> Rk^T (s > j), fp16
             tmem_row64(tmem + lane_off + 64, x);
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 if (s <= j) x[j] = 0.f;
             store_row16<true>(sm + T_RKT, s, x);
-            // fp16 copy of W (MMA3 and MMA4 take fp16 operands only)
+            // W to fp16 in place (MMA1 has completed; later MMAs take fp16 operands)
             load_row_bf16(sm + T_W, s, x);
-            store_row16<true>(sm + T_W16, s, x);
+            store_row16<true>(sm + T_W, s, x);
         }
     }
     __syncthreads();
 
-    // ---- A = (I + D N)^{-1} D, column u per thread (threads 0-63), fp32:
-    //      A[u][u] = beta_u;  A[s][u] = -beta_s sum_{v=s+1..63} G[s][v] A[v][u]  (s < u)
-    if (ok && r < kC) {
-        const int u = r;
+    // ---- A = (I + E)^{-1} D, then A (rows s) and A^T (rows u) as fp16 tiles
+    if (ok) {
+        blocked_unit_upper_inverse(X, Y, r);
         float a[64];
+        if (r < kC) {
+            const int s = r;   // row s: A[s][u] = X[s][u] beta_u, u >= s
 #pragma unroll
-        for (int s = 63; s >= 0; --s) {
-            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+            for (int u = 0; u < 64; ++u) a[u] = (u >= s) ? X[s * XLD + u] * bs[u] : 0.f;
+        } else {
+            const int u = r - kC;  // column u: A[s][u], s <= u
+            const float bu = bs[u];
 #pragma unroll
-            for (int v = s + 1; v < 64; ++v) {
-                const float g = Gs[s * GLD + v];
-                switch ((v - s - 1) & 3) {
-                    case 0: acc0 = fmaf(g, a[v], acc0); break;
-                    case 1: acc1 = fmaf(g, a[v], acc1); break;
-                    case 2: acc2 = fmaf(g, a[v], acc2); break;
-                    default: acc3 = fmaf(g, a[v], acc3); break;
-                }
-            }
-            const float sum = (acc0 + acc1) + (acc2 + acc3);
-            a[s] = (s == u) ? bs[s] : ((s < u) ? -bs[s] * sum : 0.f);
+            for (int s2 = 0; s2 < 64; ++s2) a[s2] = (s2 <= u) ? X[s2 * XLD + u] * bu : 0.f;
         }
-        // A^T row u (contiguous over s) and column u of A
-        store_row16<true>(sm + T_AT, u, a);
-        uint8_t *ta = sm + T_A;
-#pragma unroll
-        for (int s = 0; s < 64; ++s) {
-            const uint32_t off = sw128_offset(s, u >> 3) + 2 * (u & 7);
-            *reinterpret_cast<__half *>(ta + off) = __float2half_rn(a[s]);
-        }
+        __syncthreads();  // the scratch overlays the A tiles
+        if (r < kC) store_row16<true>(sm + T_A, r, a);
+        else store_row16<true>(sm + T_AT, r - kC, a);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA3: [A^T; A] x [W | Rk^T] (fp16, B MN-major, N = 128)
+    // ---- MMA3: [A^T; A] x [W | Rk^T] (fp16, B MN-major, N = 128) -> cols 0..127
     if (r == 0 && ok) {
         tc_fence_after();
         const uint64_t a = sdesc_sw128(base + T_AT, 16, 1024);
-        const uint64_t b = sdesc_sw128(base + T_W16, kT, 1024);
+        const uint64_t b = sdesc_sw128(base + T_W, T_RKT - T_W, 1024);
         constexpr uint32_t ID = idesc16(128, 128, 0, false, true);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 128, a + 2 * kk, b + 128 * kk, ID, kk > 0);
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 2 * kk, b + 128 * kk, ID, kk > 0);
     }
     if (r == 0) umma_commit(bar_mma);
     if (ok) ok = wait_all(bar_mma, 1);
@@ -287,12 +383,12 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
         float x[64];
         if (r < kC) {
-            tmem_row64(tmem + lane_off + 128, x);  // U row u
+            tmem_row64(tmem + lane_off, x);       // U row u
             store_row16<true>(sm + T_U, r, x);
-            tmem_row64(tmem + lane_off + 192, x);  // Khat^T row u
+            tmem_row64(tmem + lane_off + 64, x);  // Khat^T row u
             store_row16<true>(sm + T_KHT, r, x);
         } else {
-            tmem_row64(tmem + lane_off + 128, x);  // V' row s
+            tmem_row64(tmem + lane_off, x);       // V' row s
             store_row16<true>(sm + T_V, r - kC, x);
         }
     }
@@ -300,90 +396,94 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA4: Lq x [U | Khat^T] -> cols 128..255;  [W^T; Rk] x V' -> cols 0..63
+    // ---- MMA4x: Lq U -> cols 0..63;  Q K^T - Lq Khat^T -> cols 64..127
     if (r == 0 && ok) {
         tc_fence_after();
         const uint64_t a1 = sdesc_sw128(base + T_LQ, 16, 1024);
-        const uint64_t b1 = sdesc_sw128(base + T_U, kT, 1024);
-        constexpr uint32_t ID1 = idesc16(128, 128, 0, false, true);
+        const uint64_t b1 = sdesc_sw128(base + T_U, 1024, 1024);
+        constexpr uint32_t ID1 = idesc16(128, 64, 0, false, true);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 128, a1 + 2 * kk, b1 + 128 * kk, ID1, kk > 0);
-        const uint64_t a2 = sdesc_sw128(base + T_W16, kT, 1024);
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a1 + 2 * kk, b1 + 128 * kk, ID1, kk > 0);
+        const uint64_t aq = sdesc_sw128(base + T_Q, 16, 1024);
+        const uint64_t bk = sdesc_sw128(base + T_K, 16, 1024);
+        constexpr uint32_t IDQK = idesc16(128, 64, 1, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 64, aq + 2 * kk, bk + 2 * kk, IDQK, kk > 0);
+        const uint64_t bh2 = sdesc_sw128(base + T_KHT, 1024, 1024);
+        constexpr uint32_t IDC = idesc16(128, 64, 0, false, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 64, a1 + 2 * kk, bh2 + 128 * kk, IDC, 1);
+    }
+    if (r == 0) umma_commit(bar_mma);
+    if (ok) ok = wait_all(bar_mma, 0);
+
+    const size_t blk_base = (size_t)bh * nblk + blk;
+    __nv_bfloat16 *kp_blk = kp + blk_base * (2 * kC) * kD;
+    if (ok && r < kC) {
+        tc_fence_after();
+        const int i = r;
+        float x[64], y[64];
+        // q~_i = q_i - (Lq U)_i
+        load_row_bf16(sm + T_Q, i, y);
+        tmem_row64(tmem + lane_off, x);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) y[c] -= x[c];
+        store_global_row(qt + ((size_t)bh * Lp + t0 + i) * kD, y);
+        // diagonal logits, log2 units, j <= i
+        tmem_row64(tmem + lane_off + 64, x);
+        const float lci = (log_f != nullptr) ? lc[i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            float v = scale_log2 * x[j];
+            if (log_f != nullptr) v += kLog2e * (lci - lc[j]);
+            x[j] = (j <= i && t0 + j < L) ? v : -INFINITY;
+        }
+        uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
+                               pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+    } else if (ok && warp >= 2) {
+        // warps 2-3: the lanes of MMA4x rows 64..127 hold nothing; keep the warp collective
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA4y: [W^T; Rk] x V' (fp16, A and B MN-major) -> cols 0..63
+    if (r == 0 && ok) {
+        tc_fence_after();
+        const uint64_t a2 = sdesc_sw128(base + T_W, T_RKT - T_W, 1024);
         const uint64_t b2 = sdesc_sw128(base + T_V, 1024, 1024);
         constexpr uint32_t ID2 = idesc16(128, 64, 0, true, true);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a2 + 128 * kk, b2 + 128 * kk, ID2, kk > 0);
     }
     if (r == 0) umma_commit(bar_mma);
-    if (ok) ok = wait_all(bar_mma, 0);
-
-    // ---- epilogue
+    if (ok) ok = wait_all(bar_mma, 1);
     if (ok) {
         tc_fence_after();
-        const size_t blk_base = (size_t)bh * nblk + blk;
-        __nv_bfloat16 *kp_blk = kp + blk_base * (2 * kC) * kD;
-        float x[64], y[64];
+        float x[64];
+        tmem_row64(tmem + lane_off, x);
         if (r < kC) {
-            const int i = r;
-            // q~_i = q_i - (Lq U)_i
-            load_row_bf16(sm + T_Q, i, y);
-            tmem_row64(tmem + lane_off + 128, x);
+            // P_b row n = r: delta - (W^T V')_n
 #pragma unroll
-            for (int c = 0; c < 64; ++c) y[c] -= x[c];
-            uint4 *dq = reinterpret_cast<uint4 *>(qt + ((size_t)bh * Lp + t0 + i) * kD);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                dq[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]),
-                                   pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
-                                   pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
-                                   pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
-            // diagonal logits, log2 units: scale (q_i.k_j - (Lq Khat^T)_ij) [+ FoX], j <= i
-            tmem_row64(tmem + lane_off + 64, y);    // Q K^T row i (from MMA1)
-            tmem_row64(tmem + lane_off + 192, x);   // Lq Khat^T row i
-            const float lci = (log_f != nullptr) ? lc[i] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float v = scale_log2 * (y[j] - x[j]);
-                if (log_f != nullptr) v += kLog2e * (lci - lc[j]);
-                y[j] = (j <= i && t0 + j < L) ? v : -INFINITY;
-            }
-            uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                dd[c] = make_uint4(pack_h2(y[8 * c], y[8 * c + 1]), pack_h2(y[8 * c + 2], y[8 * c + 3]),
-                                   pack_h2(y[8 * c + 4], y[8 * c + 5]), pack_h2(y[8 * c + 6], y[8 * c + 7]));
-            // P_b row n = i: delta - (W^T V')_n
-            tmem_row64(tmem + lane_off, x);
-#pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = (c == i ? 1.f : 0.f) - x[c];
-            uint4 *dp = reinterpret_cast<uint4 *>(kp_blk + (kC + i) * kD);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                dp[c] = make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]),
-                                   pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
-                                   pack_bf16x2(x[8 * c + 4], x[8 * c + 5]),
-                                   pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+            for (int c = 0; c < 64; ++c) x[c] = (c == r ? 1.f : 0.f) - x[c];
+            store_global_row(kp_blk + (kC + r) * kD, x);
         } else {
-            const int j = r - kC;
             // k~_j = k_j - (Rk V')_j
+            const int j = r - kC;
+            float y[64];
             load_row_bf16(sm + T_K, j, y);
-            tmem_row64(tmem + lane_off, x);
 #pragma unroll
             for (int c = 0; c < 64; ++c) y[c] -= x[c];
-            uint4 *dk = reinterpret_cast<uint4 *>(kp_blk + j * kD);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                dk[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]),
-                                   pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
-                                   pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
-                                   pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
+            store_global_row(kp_blk + j * kD, y);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
