@@ -89,11 +89,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
+// SM cycle counter: cheap enough to read inside polling loops. Wait limits are given
+// in nanoseconds and converted at 2 cycles per ns, so at clocks up to 2 GHz a limit never
+// expires early (it may expire somewhat later at lower clocks).
+__device__ __forceinline__ uint64_t cycles_now() { return (uint64_t)clock64(); }
+__host__ __device__ constexpr uint64_t ns_to_cycles(uint64_t ns) { return 2 * ns; }
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -121,15 +121,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: returns false after `limit_ns` nanoseconds without completion.
+// Non-blocking test of a phase (for polling loops that watch several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: returns false after about `limit_ns` nanoseconds without completion.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = cycles_now(), lim = ns_to_cycles(limit_ns);
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (cycles_now() - t0 > lim) return false;
     }
+}
+
+// 2^x on the SFU (approximate, subnormal results flushed to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // ---------------------------------------------------------------- fences

@@ -6,53 +6,67 @@
 // "거리에서 경로로, PaTH Attention" §9 (the same scheme, blockwise preprocessing and
 // blockwise updates of the accumulated transform and softmax statistics).
 //
-// One CTA owns a tile of 128 query rows = two 64-token blocks ib0 = 2t, ib1 = 2t + 1 of
-// one head. With q~ the boundary-adjusted queries, k~ the boundary-adjusted keys and
-// P_b = H_start(b) ... H_end(b) the dense block transition (all from the preprocessing
-// kernel), the logit of row i against key j of an earlier block b is
+// A tile is 128 query rows = two 64-token blocks ib0 = 2t, ib1 = 2t + 1 of one head. With
+// q~ the boundary-adjusted queries, k~ the boundary-adjusted keys and P_b = H_start(b) ...
+// H_end(b) the dense block transition (all from the preprocessing kernel), the logit of
+// row i against key j of an earlier block b is
 //     scale * k~_j^T P_{b+1} ... P_{ib-1} q~_i,
-// so a state row x_i = q~_i is scored against block ib-1, then x_i <- P_{ib-1} x_i, and
-// so on down to block 0. In row form the whole tile advances as X <- X P_b^T, one
-// 128 x 64 x 64 MMA per block, next to S = X K~_b^T and O += P V_b.
-// Steps s = 0 .. ib1 visit key block b = ib1 - s:
+// so a state row x_i = q~_i is scored against block ib-1, then x_i <- P_{ib-1} x_i, and so
+// on down to block 0. In row form a tile advances as X <- X P_b^T, one 128 x 64 x 64 MMA
+// per block, next to S = X K~_b^T and O += P V_b. Steps s = 0 .. ib1 visit block ib1 - s:
 //   s = 0 : block ib1; rows 64-127 take their diagonal-block logits, rows 0-63 are masked.
 //   s = 1 : block ib0; rows 0-63 take their diagonal-block logits, rows 64-127 the MMA
 //           logits of block ib0, and only rows 64-127 advance their state by P_{ib0}.
 //   s >= 2: block ib1 - s for every row.
 //
-// Warp roles (192 threads): warps 0-3 own one query row per thread (TMEM lane = row):
-// online softmax with lazy rescaling, fp32 -> bf16 conversion of the new state into the
-// swizzled A-operand tile. Warp 4 allocates TMEM and one lane issues every MMA. Warp 5
-// (one lane) streams K~|P_b and V_b tiles by TMA through an NS-stage ring.
-// The bf16 state tile is double-buffered (step s reads buffer s & 1 while the new state
-// of step s + 1 is written into the other one: the S MMA of step s may still be reading
-// its operand when the state MMA that precedes it has completed). The probability tile
-// is single-buffered: it is rewritten only after the previous P.V MMA has completed.
-// TMEM columns: [0,64) new state, [64,128) and [128,192) S (double buffer), [192,256) O.
+// One CTA owns a pair of tiles of one head, A = 2p and B = 2p + 1, and streams the key
+// blocks 4p+3, 4p+2, ..., 0 once through an NS-stage TMA ring: B consumes every block,
+// A every block from 4p+1 down, so each stage is loaded once for both tiles. A stage holds
+// [K~_b; P_b; K~_b] (K~_b loaded twice) and V_b. Per tile and step, S = X K~_b^T and the
+// new state X P_b^T come from ONE MMA with N = 128: B = [K~_b; P_b] on even steps (S lands
+// in TMEM columns [0,64), the state in [64,128)) and B = [P_b; K~_b] on odd steps (state in
+// [64,128), S in [128,192)), so S is double-buffered while the state accumulator is not.
+// O += P V_b follows (N = 64, columns [192,256)). Tile B's columns are at +256.
+// Warp roles (512 threads):
+//   warps 0-3 / 4-7  softmax of tile A / B, one row per thread (= TMEM lane): load S,
+//                    release its buffer, online softmax with lazy rescaling, P tile;
+//   warps 8-11       the state recurrence of both tiles (one per TMEM lane quadrant):
+//                    fp32 -> bf16 conversion of each new state into a swizzled A tile;
+//   warps 12 / 13    issue tile A's / B's S|state MMAs (the recurrence: needs the
+//                    converted state and a free S buffer, never the softmax of this step);
+//   warps 14 / 15    issue tile A's / B's P.V MMAs and release the stages; warp 14
+//                    also feeds the TMA ring (both duties poll, neither blocks the other);
+//   warp 12 also owns TMEM.
+// Each issuing thread is its own in-order MMA stream: one thread issuing back to back
+// cannot keep the tensor core busy with N <= 128 instructions, four can.
+// The bf16 state tile is double-buffered, the P tile single-buffered (rewritten after the
+// tile's previous P.V has completed).
 #include "common.cuh"
 
 namespace path {
 
 namespace {
 
-constexpr int kScanThreads = 192;
-constexpr int NS = 2;                       // TMA stages (K~|P and V of one block each)
+constexpr int kScanThreads = 512;
+constexpr int NS = 4;                       // TMA stages ([K~|P|K~] and V of one block each)
 constexpr uint32_t kTileBytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr uint32_t kVBytes = 64 * 128;      // 64 rows x 64 bf16
-constexpr uint32_t kStageBytes = kTileBytes + kVBytes;
+constexpr uint32_t kKdupBytes = 64 * 128;   // second copy of K~_b after P_b
+constexpr uint32_t kStageBytes = kTileBytes + kKdupBytes + kVBytes;
 constexpr float kRescaleThreshold = 8.f;    // lazy rescale: keep the old max within 2^8
 
 struct ScanSmem {
     // byte offsets from the 1024-aligned base
-    static constexpr uint32_t q_st = 0;                         // two 16 KB state tiles
-    static constexpr uint32_t p_buf = 2 * kTileBytes;           // one 16 KB tile
-    static constexpr uint32_t stage = p_buf + kTileBytes;       // NS stages
+    __host__ __device__ static constexpr uint32_t q_st(int t, int i) { return (uint32_t)(2 * t + i) * kTileBytes; }
+    __host__ __device__ static constexpr uint32_t p_buf(int t) { return (uint32_t)(4 + t) * kTileBytes; }
+    static constexpr uint32_t stage = 6 * kTileBytes;
     static constexpr uint32_t bars = stage + NS * kStageBytes;
-    // barrier indices
-    static constexpr int FULL = 0, EMPTY = NS, QFULL = 2 * NS, BAR_QN = 2 * NS + 1,
-                         BAR_S = 2 * NS + 2, BAR_O = 2 * NS + 3, QREADY = 2 * NS + 4,
-                         PREADY = 2 * NS + 5, FINAL = 2 * NS + 6, NEVER = 2 * NS + 7,
-                         NBARS = 2 * NS + 8;
+    // barrier indices: the ring, then ten per tile (S buffers have their own), then one
+    static constexpr int FULL = 0, EMPTY = NS, TILE0 = 2 * NS;
+    static constexpr int QFULL = 0, BAR_SX = 1 /* 2 */, BAR_O = 3, QREADY = 4,
+                         SFREE = 5 /* 2 */, PREADY = 7, FINAL_SX = 8, FINAL_PV = 9;
+    __host__ __device__ static constexpr int per_tile(int t, int which) { return TILE0 + 10 * t + which; }
+    static constexpr int NEVER = TILE0 + 20, NBARS = TILE0 + 21;
     static constexpr uint32_t tmem_slot = bars + NBARS * 8;
     static constexpr uint32_t abort_flag = tmem_slot + 4;
     static constexpr uint32_t bytes = abort_flag + 4;
@@ -67,12 +81,11 @@ struct Waiter {
     // Bounded wait; on timeout records the status and raises the CTA abort flag.
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
         if (mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = globaltimer_ns();
+        const uint64_t t0 = cycles_now(), lim = ns_to_cycles(limit_ns);
         for (;;) {
-            for (int i = 0; i < 32; ++i)
-                if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait(bar, parity)) return true;
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
+            if (cycles_now() - t0 > lim) {
                 report_status(status, kStatusTimeout);
                 *abort = 1u;
                 return false;
@@ -81,10 +94,12 @@ struct Waiter {
     }
 };
 
-template <bool FOX>
-__global__ void __launch_bounds__(kScanThreads, 2)
+// RAW: no bias and a positive scale, so the scale is applied inside the exponent's FFMA.
+template <bool FOX, bool RAW>
+__global__ void __launch_bounds__(kScanThreads, 1)
 path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_kp,
+                    const __grid_constant__ CUtensorMap tm_k64,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __nv_bfloat16 *__restrict__ qt, const __half *__restrict__ dg,
                     const float *__restrict__ c2, __nv_bfloat16 *__restrict__ out,
@@ -97,136 +112,246 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntile = nblk >> 1;
-    const int tile = ntile - 1 - (int)blockIdx.x;  // longest tiles first
+    const int npair = (ntile + 1) >> 1;
+    const int pair = npair - 1 - (int)blockIdx.x;  // heaviest pairs first
     const int bh = blockIdx.y;
-    const int ib0 = 2 * tile, ib1 = 2 * tile + 1;
-    const int nsteps = ib1 + 1;
+    const bool hasB = 2 * pair + 1 < ntile;
+    const int top = hasB ? 4 * pair + 3 : 4 * pair + 1;  // first key block of the stream
+    const int nstream = top + 1;
+    // tile t (0 = A, 1 = B): tile index, its step count, and stream position of its step 0
+    auto tile_of = [&](int t) { return 2 * pair + t; };
+    auto nsteps_of = [&](int t) { return 2 * tile_of(t) + 2; };
+    auto off_of = [&](int t) { return top - (2 * tile_of(t) + 1); };
 
     auto bar = [&](int i) { return base + ScanSmem::bars + 8u * (uint32_t)i; };
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + ScanSmem::abort_flag);
+    auto tbar = [&](int t, int which) { return bar(ScanSmem::per_tile(t, which)); };
+    volatile uint32_t *abort_flag =
+        reinterpret_cast<volatile uint32_t *>(gbase + ScanSmem::abort_flag);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + ScanSmem::tmem_slot);
     const Waiter wait{abort_flag, status, limit_ns};
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(bar(ScanSmem::FULL + i), 1);
-            mbar_init(bar(ScanSmem::EMPTY + i), 1);
+            mbar_init(bar(ScanSmem::EMPTY + i), 2);  // two arrivals per use (see issuers)
         }
-        mbar_init(bar(ScanSmem::QFULL), 1);
-        mbar_init(bar(ScanSmem::BAR_QN), 1);
-        mbar_init(bar(ScanSmem::BAR_S), 1);
-        mbar_init(bar(ScanSmem::BAR_O), 1);
-        mbar_init(bar(ScanSmem::QREADY), 128);
-        mbar_init(bar(ScanSmem::PREADY), 128);
-        mbar_init(bar(ScanSmem::FINAL), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(tbar(t, ScanSmem::QFULL), 1);
+            mbar_init(tbar(t, ScanSmem::BAR_SX), 1);
+            mbar_init(tbar(t, ScanSmem::BAR_SX + 1), 1);
+            mbar_init(tbar(t, ScanSmem::BAR_O), 1);
+            mbar_init(tbar(t, ScanSmem::QREADY), 128);
+            mbar_init(tbar(t, ScanSmem::SFREE), 128);
+            mbar_init(tbar(t, ScanSmem::SFREE + 1), 128);
+            mbar_init(tbar(t, ScanSmem::PREADY), 128);
+            mbar_init(tbar(t, ScanSmem::FINAL_SX), 1);
+            mbar_init(tbar(t, ScanSmem::FINAL_PV), 1);
+        }
         mbar_init(bar(ScanSmem::NEVER), 1);
         *abort_flag = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == 4) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+    if (warp == 12) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t T_QN = tmem + 0, T_S0 = tmem + 64, T_O = tmem + 192;
-
-    auto q_st = [&](int i) { return base + ScanSmem::q_st + (uint32_t)i * kTileBytes; };
-    const uint32_t p_buf = base + ScanSmem::p_buf;
+    // per tile: S of even steps [0,64), new state [64,128), S of odd steps [128,192), O
+    auto t_state = [&](int t) { return tmem + 256u * (uint32_t)t + 64u; };
+    auto t_s = [&](int t, int s) { return tmem + 256u * (uint32_t)t + ((s & 1) ? 128u : 0u); };
+    auto t_sxd = [&](int t, int s) { return tmem + 256u * (uint32_t)t + ((s & 1) ? 64u : 0u); };
+    auto t_o = [&](int t) { return tmem + 256u * (uint32_t)t + 192u; };
     auto stage_kp = [&](int i) { return base + ScanSmem::stage + (uint32_t)i * kStageBytes; };
-    auto stage_v = [&](int i) { return stage_kp(i) + kTileBytes; };
+    auto stage_v = [&](int i) { return stage_kp(i) + kTileBytes + kKdupBytes; };
 
-    if (warp == 5) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_qt);
-            tma_prefetch_desc(&tm_kp);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(bar(ScanSmem::QFULL), kTileBytes);
-            tma_load_3d(q_st(1), &tm_qt, bar(ScanSmem::QFULL), 0, tile * kTile, bh);
-            int issued = 0;
-            for (int s = 0; s < nsteps; ++s) {
-                const int st = s % NS;
-                if (s >= NS && !wait(bar(ScanSmem::EMPTY + st), ((s / NS) - 1) & 1)) break;
-                const int b = ib1 - s;
-                if (s == 0) {
-                    mbar_arrive_expect_tx(bar(ScanSmem::FULL + st), kVBytes);
-                } else {
-                    mbar_arrive_expect_tx(bar(ScanSmem::FULL + st), kStageBytes);
-                    tma_load_3d(stage_kp(st), &tm_kp, bar(ScanSmem::FULL + st), 0, b * 2 * kC, bh);
-                }
-                tma_load_3d(stage_v(st), &tm_v, bar(ScanSmem::FULL + st), 0, b * kC, bh);
-                issued = s + 1;
-            }
-            // drain: every issued copy has landed before the CTA may exit
-            for (int s = (issued > NS ? issued - NS : 0); s < issued; ++s) {
-                const uint32_t bfull = bar(ScanSmem::FULL + s % NS);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(bfull, (s / NS) & 1) && globaltimer_ns() - t0 < limit_ns) {
-                }
-            }
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(ScanSmem::QFULL), 0) && globaltimer_ns() - t0 < limit_ns) {
-            }
-        }
-    } else if (warp == 4) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t ID_KMAJ = idesc_bf16(128, 64, false);
-            constexpr uint32_t ID_PV = idesc_bf16(128, 64, true);
+    if (warp >= 12 && warp <= 13) {
+        // ------------------------------------------------------------ S|state issuers
+        const int t = warp - 12;
+        if (lane == 0 && (t == 0 || hasB)) {
+            constexpr uint32_t ID_SX = idesc_bf16(128, 128, false);
+            const int nst = nsteps_of(t), off = off_of(t);
             bool ok = true;
-            if (force_timeout) ok = wait(bar(ScanSmem::NEVER), 0);  // nothing arrives here
-            auto issue_sq = [&](int s) -> bool {
-                const int st = s % NS;
-                if (!wait(bar(ScanSmem::FULL + st), (s / NS) & 1)) return false;
-                if (s >= 2 && !wait(bar(ScanSmem::QREADY), (s - 2) & 1)) return false;
-                tc_fence_after();
-                const uint64_t a_q = sdesc_sw128(q_st(s & 1), 16, 1024);
-                const uint64_t b_k = sdesc_sw128(stage_kp(st), 16, 1024);
-                const uint64_t b_p = sdesc_sw128(stage_kp(st) + 64 * 128, 16, 1024);
-                if (s < nsteps - 1) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(T_QN, a_q + 2 * kk, b_p + 2 * kk, ID_KMAJ, kk > 0);
-                    umma_commit(bar(ScanSmem::BAR_QN));
+            if (force_timeout && t == 0) ok = wait(bar(ScanSmem::NEVER), 0);  // nothing arrives here
+            for (int s = 1; ok && s < nst; ++s) {
+                const int n = s + off, st = n % NS;
+                if (!(ok = wait(bar(ScanSmem::FULL + st), (n / NS) & 1))) break;
+                // the state of step s: q~ (step 1) or the converted new state of step s - 1
+                if (s == 1) {
+                    if (!(ok = wait(tbar(t, ScanSmem::QFULL), 0))) break;
+                } else if (!(ok = wait(tbar(t, ScanSmem::QREADY), (s - 2) & 1))) {
+                    break;
                 }
-                const uint32_t t_s = T_S0 + 64u * (uint32_t)(s & 1);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(t_s, a_q + 2 * kk, b_k + 2 * kk, ID_KMAJ, kk > 0);
-                umma_commit(bar(ScanSmem::BAR_S));
-                return true;
-            };
-            if (ok) ok = wait(bar(ScanSmem::QFULL), 0);
-            if (ok && nsteps >= 2) ok = issue_sq(1);
-            for (int s = 0; ok && s < nsteps; ++s) {
-                if (s + 1 >= 2 && s + 1 <= nsteps - 1 && !(ok = issue_sq(s + 1))) break;
-                const int st = s % NS;
-                if (s == 0 && !(ok = wait(bar(ScanSmem::FULL + st), 0))) break;
-                if (!(ok = wait(bar(ScanSmem::PREADY), s & 1))) break;
+                // S buffer s & 1 was last read by the softmax of step s - 2
+                if (s >= 3 && !(ok = wait(tbar(t, ScanSmem::SFREE + (s & 1)), ((s - 3) >> 1) & 1)))
+                    break;
                 tc_fence_after();
-                const uint64_t a_p = sdesc_sw128(p_buf, 16, 1024);
-                const uint64_t b_v = sdesc_sw128(stage_v(st), 1024, 1024);
+                const uint64_t a_q = sdesc_sw128(base + ScanSmem::q_st(t, s & 1), 16, 1024);
+                const uint64_t b_kp =
+                    sdesc_sw128(stage_kp(st) + ((s & 1) ? 64u * 128u : 0u), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(T_O, a_p + 2 * kk, b_v + 128 * kk, ID_PV, (s > 0 || kk > 0));
-                umma_commit(bar(ScanSmem::BAR_O));
-                umma_commit(bar(ScanSmem::EMPTY + st));
+                    umma_bf16(t_sxd(t, s), a_q + 2 * kk, b_kp + 2 * kk, ID_SX, kk > 0);
+                umma_commit(tbar(t, ScanSmem::BAR_SX + (s & 1)));
             }
-            // every MMA issued above has completed before TMEM is released
-            umma_commit(bar(ScanSmem::FINAL));
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(ScanSmem::FINAL), 0) && globaltimer_ns() - t0 < limit_ns) {
+            umma_commit(tbar(t, ScanSmem::FINAL_SX));
+            const uint64_t t0 = cycles_now();
+            while (!mbar_try_wait(tbar(t, ScanSmem::FINAL_SX), 0) &&
+                   cycles_now() - t0 < ns_to_cycles(limit_ns)) {
             }
         }
-    } else {
+    } else if (warp >= 14 && warp <= 15) {
+        // ------------------------------------------------------------ P.V issuers (+ TMA)
+        // Tile A's thread also feeds the TMA ring; both duties poll without blocking.
+        const int t = warp - 14;
+        const bool producer = (t == 0);
+        if (lane == 0 && (t == 0 || hasB)) {
+            constexpr uint32_t ID_PV = idesc_bf16(128, 64, true);
+            const int nst = nsteps_of(t), off = off_of(t);
+            if (producer) {
+                tma_prefetch_desc(&tm_qt);
+                tma_prefetch_desc(&tm_kp);
+                tma_prefetch_desc(&tm_k64);
+                tma_prefetch_desc(&tm_v);
+                for (int tt = 0; tt < (hasB ? 2 : 1); ++tt) {
+                    mbar_arrive_expect_tx(tbar(tt, ScanSmem::QFULL), kTileBytes);
+                    tma_load_3d(base + ScanSmem::q_st(tt, 1), &tm_qt, tbar(tt, ScanSmem::QFULL), 0,
+                                tile_of(tt) * kTile, bh);
+                }
+            }
+            int n_fill = producer ? 0 : nstream;  // next stream position to load
+            int s = 0;                            // next P.V step
+            bool ok = true;
+            uint64_t t_last = cycles_now();
+            while (ok && (s < nst || n_fill < nstream)) {
+                bool progress = false;
+                if (n_fill < nstream &&
+                    (n_fill < NS ||
+                     mbar_test_wait(bar(ScanSmem::EMPTY + n_fill % NS), ((n_fill / NS) - 1) & 1))) {
+                    const int st = n_fill % NS, b = top - n_fill;
+                    if (n_fill == 0) {  // the top tile's own diagonal block: values only
+                        mbar_arrive_expect_tx(bar(ScanSmem::FULL + st), kVBytes);
+                    } else {
+                        mbar_arrive_expect_tx(bar(ScanSmem::FULL + st), kStageBytes);
+                        tma_load_3d(stage_kp(st), &tm_kp, bar(ScanSmem::FULL + st), 0, b * 2 * kC, bh);
+                        tma_load_3d(stage_kp(st) + kTileBytes, &tm_k64, bar(ScanSmem::FULL + st), 0,
+                                    b * 2 * kC, bh);
+                    }
+                    tma_load_3d(stage_v(st), &tm_v, bar(ScanSmem::FULL + st), 0, b * kC, bh);
+                    ++n_fill;
+                    progress = true;
+                }
+                if (s < nst) {
+                    const int n = s + off, st = n % NS;
+                    const bool in_ready = (s > 0) || mbar_test_wait(bar(ScanSmem::FULL + st), (n / NS) & 1);
+                    if (in_ready && mbar_test_wait(tbar(t, ScanSmem::PREADY), s & 1)) {
+                        tc_fence_after();
+                        const uint64_t a_p = sdesc_sw128(base + ScanSmem::p_buf(t), 16, 1024);
+                        const uint64_t b_v = sdesc_sw128(stage_v(st), 1024, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_bf16(t_o(t), a_p + 2 * kk, b_v + 128 * kk, ID_PV, (s > 0 || kk > 0));
+                        umma_commit(tbar(t, ScanSmem::BAR_O));
+                        // this step's S|state MMA completed before its softmax finished, so
+                        // this commit covers every read of the stage by tile t; two arrivals
+                        // per stage (a stage read by one tile only gets both from that tile)
+                        umma_commit(bar(ScanSmem::EMPTY + st));
+                        if (!(hasB && n >= off_of(0))) umma_commit(bar(ScanSmem::EMPTY + st));
+                        ++s;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    t_last = cycles_now();
+                } else if (*abort_flag) {
+                    ok = false;
+                } else if (cycles_now() - t_last > ns_to_cycles(limit_ns)) {
+                    report_status(status, kStatusTimeout);
+                    *abort_flag = 1u;
+                    ok = false;
+                }
+            }
+            if (producer) {
+                // drain: every issued copy has landed before the CTA may exit
+                for (int n = (n_fill > NS ? n_fill - NS : 0); n < n_fill; ++n) {
+                    const uint32_t bfull = bar(ScanSmem::FULL + n % NS);
+                    const uint64_t t0 = cycles_now();
+                    while (!mbar_try_wait(bfull, (n / NS) & 1) &&
+                           cycles_now() - t0 < ns_to_cycles(limit_ns)) {
+                    }
+                }
+                for (int tt = 0; tt < (hasB ? 2 : 1); ++tt) {
+                    const uint64_t t0 = cycles_now();
+                    while (!mbar_try_wait(tbar(tt, ScanSmem::QFULL), 0) &&
+                           cycles_now() - t0 < ns_to_cycles(limit_ns)) {
+                    }
+                }
+            }
+            umma_commit(tbar(t, ScanSmem::FINAL_PV));
+            const uint64_t t0 = cycles_now();
+            while (!mbar_try_wait(tbar(t, ScanSmem::FINAL_PV), 0) &&
+                   cycles_now() - t0 < ns_to_cycles(limit_ns)) {
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ state warps
+        const int quad = warp - 8;
+        const int r = quad * 32 + lane;          // row of both tiles = TMEM lane
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const size_t head = (size_t)bh;
+        bool ok = true;
+        auto wwait = [&](uint32_t b_, uint32_t par) {
+            return __all_sync(0xffffffffu, wait(b_, par)) != 0;
+        };
+        const int smax = nsteps_of(hasB ? 1 : 0);
+        for (int s = 1; s < smax && ok; ++s) {
+            for (int t = hasB ? 1 : 0; t >= 0; --t) {
+                if (s >= nsteps_of(t) - 1) continue;  // the last step needs no new state
+                if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX + (s & 1)), ((s - 1) >> 1) & 1))) break;
+                tc_fence_after();
+                // the state of step s + 1 goes to buffer (s + 1) & 1
+                uint8_t *row = gbase + ScanSmem::q_st(t, (s + 1) & 1);
+                if (s >= 2 || quad >= 2) {
+                    uint32_t qa[32], qb[32];
+                    tmem_ld32(t_state(t) + lane_base, qa);
+                    tmem_ld32(t_state(t) + 32 + lane_base, qb);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t *src = (c < 4) ? &qa[8 * c] : &qb[8 * (c - 4)];
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
+                        u.y = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
+                        u.z = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
+                        u.w = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
+                        *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = u;
+                    }
+                } else {
+                    // rows of block ib0 keep q~ through step 1: copy it from the workspace
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        qt + (head * Lp + (size_t)tile_of(t) * kTile + r) * kD);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = __ldg(src + c);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(tbar(t, ScanSmem::QREADY));
+            }
+        }
+        tc_fence_before();
+    } else if (warp < 4 || hasB) {
         // ------------------------------------------------------------ softmax warps
-        const int r = threadIdx.x;             // tile row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const int i = tile * kTile + r;        // query index
+        const int t = warp >> 2;                 // 0 = tile A, 1 = tile B
+        const int r = threadIdx.x - 128 * t;     // tile row = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int tile = tile_of(t);
+        const int ib0 = 2 * tile, ib1 = 2 * tile + 1;
+        const int nsteps = ib1 + 1;
+        const int i = tile * kTile + r;          // query index
         const size_t head = (size_t)bh;
         float m_run = -INFINITY, l_run = 0.f;
         const float c2_i = FOX ? c2[head * Lp + i] : 0.f;
@@ -235,10 +360,13 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         auto wwait = [&](uint32_t b_, uint32_t par) {
             return __all_sync(0xffffffffu, wait(b_, par)) != 0;
         };
+        const uint32_t T_O = t_o(t);
 
         for (int s = 0; s < nsteps && ok; ++s) {
             const int b = ib1 - s;
-            float x[64];
+            // logits of this row come from the diagonal-block table (step 0, and step 1 for
+            // rows 0-63) or from S in TMEM; they are read twice, in 32-column chunks (row
+            // max, then exponentials), which keeps the live register set small
             bool from_diag = false;
             int diag_blk = 0, diag_row = 0;
             if (s == 0) {
@@ -246,147 +374,140 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 diag_blk = ib1;
                 diag_row = r - 64;
             } else {
-                if (s < nsteps - 1) {
-                    if (!(ok = wwait(bar(ScanSmem::BAR_QN), (s - 1) & 1))) break;
-                    tc_fence_after();
-                    // the state of step s + 1 goes to buffer (s + 1) & 1
-                    uint8_t *row = gbase + ScanSmem::q_st + (uint32_t)((s + 1) & 1) * kTileBytes;
-                    if (s >= 2 || warp >= 2) {
-                        uint32_t qa[32], qb[32];
-                        tmem_ld32(T_QN + lane_base, qa);
-                        tmem_ld32(T_QN + lane_base + 32, qb);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint32_t *src = (c < 4) ? &qa[8 * c] : &qb[8 * (c - 4)];
-                            uint4 u;
-                            u.x = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
-                            u.y = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
-                            u.z = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
-                            u.w = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
-                            *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = u;
-                        }
-                    } else {
-                        // rows of block ib0 keep q~ through step 1: copy it from the workspace
-                        const uint4 *src = reinterpret_cast<const uint4 *>(
-                            qt + (head * Lp + (size_t)tile * kTile + r) * kD);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = __ldg(src + c);
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(bar(ScanSmem::QREADY));
-                }
-                if (!(ok = wwait(bar(ScanSmem::BAR_S), (s - 1) & 1))) break;
+                if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX + (s & 1)), ((s - 1) >> 1) & 1))) break;
                 tc_fence_after();
-                if (s == 1 && warp < 2) {
+                if (s == 1 && (warp & 3) < 2) {
                     from_diag = true;
                     diag_blk = ib0;
                     diag_row = r;
+                }
+            }
+            const uint32_t ts = t_s(t, s) + lane_base;
+            const __half *drow = dg + (((head * nblk + diag_blk) * kC) + (diag_row < 0 ? 0 : diag_row)) * kC;
+            const bool raw_s = RAW && !from_diag;
+            // 32 logits of chunk h (log2 units, or raw scores when raw_s)
+            auto load_chunk = [&](int h, float (&v)[32]) {
+                if (from_diag) {
+                    if (diag_row >= 0) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(drow + 32 * h);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint4 c = __ldg(src + q8);
+                            const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f =
+                                    __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
+                                v[8 * q8 + 2 * e] = f.x;
+                                v[8 * q8 + 2 * e + 1] = f.y;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+                    }
                 } else {
-                    uint32_t sa[32], sb[32];
-                    const uint32_t t_s = T_S0 + 64u * (uint32_t)(s & 1) + lane_base;
-                    tmem_ld32(t_s, sa);
-                    tmem_ld32(t_s + 32, sb);
+                    uint32_t u[32];
+                    tmem_ld32(ts + 32 * h, u);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        x[j] = __uint_as_float(sa[j]) * scale_log2;
-                        x[j + 32] = __uint_as_float(sb[j]) * scale_log2;
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = RAW ? __uint_as_float(u[j]) : __uint_as_float(u[j]) * scale_log2;
                     if (FOX) {
-                        const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + b * kC);
+                        const float4 *cj =
+                            reinterpret_cast<const float4 *>(c2 + head * Lp + b * kC + 32 * h);
 #pragma unroll
-                        for (int q4 = 0; q4 < 16; ++q4) {
+                        for (int q4 = 0; q4 < 8; ++q4) {
                             const float4 c = __ldg(cj + q4);
-                            x[4 * q4 + 0] += c2_i - c.x;
-                            x[4 * q4 + 1] += c2_i - c.y;
-                            x[4 * q4 + 2] += c2_i - c.z;
-                            x[4 * q4 + 3] += c2_i - c.w;
+                            v[4 * q4 + 0] += c2_i - c.x;
+                            v[4 * q4 + 1] += c2_i - c.y;
+                            v[4 * q4 + 2] += c2_i - c.z;
+                            v[4 * q4 + 3] += c2_i - c.w;
                         }
                     }
                 }
-            }
-            if (from_diag) {
-                if (diag_row >= 0) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        dg + (((head * nblk + diag_blk) * kC) + diag_row) * kC);
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        const uint4 c = __ldg(src + q8);
-                        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f =
-                                __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
-                            x[8 * q8 + 2 * e] = f.x;
-                            x[8 * q8 + 2 * e + 1] = f.y;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) x[j] = -INFINITY;
-                }
-            }
+            };
 
-            // ---- online softmax (base 2), lazy rescaling of O
-            float mx = x[0];
+            // ---- pass 1: row max
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int j = 1; j < 64; ++j) mx = fmaxf(mx, x[j]);
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                load_chunk(h, v);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    m4[0] = fmaxf(m4[0], v[j]);
+                    m4[1] = fmaxf(m4[1], v[j + 1]);
+                    m4[2] = fmaxf(m4[2], v[j + 2]);
+                    m4[3] = fmaxf(m4[3], v[j + 3]);
+                }
+            }
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            if (raw_s) mx *= scale_log2;
+            // lazy rescaling: keep the old max unless the new one exceeds it by 2^8
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m_run + kRescaleThreshold) {
                 if (m_run != -INFINITY) {
-                    alpha = exp2f(m_run - mx);
+                    alpha = ex2_approx(m_run - mx);
                     rescale = true;
                 }
                 m_run = mx;
                 l_run *= alpha;
             }
-            if (s >= 1 && __any_sync(0xffffffffu, rescale)) {
-                // O must be complete up to step s - 1 before it is rewritten
-                if (!(ok = wwait(bar(ScanSmem::BAR_O), (s - 1) & 1))) break;
-                tc_fence_after();
-                uint32_t oa[32], ob[32];
-                tmem_ld32(T_O + lane_base, oa);
-                tmem_ld32(T_O + lane_base + 32, ob);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    oa[j] = __float_as_uint(__uint_as_float(oa[j]) * alpha);
-                    ob[j] = __float_as_uint(__uint_as_float(ob[j]) * alpha);
-                }
-                tmem_st32(T_O + lane_base, oa);
-                tmem_st32(T_O + lane_base + 32, ob);
-                tmem_st_wait();
-            }
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            float lsum = 0.f;
-            uint32_t pk[32];
+            const float cs = raw_s ? scale_log2 : 1.f;
+            const float neg_m = -m_use;
+            // the P tile was last read by this tile's P.V MMA of step s - 1, which also has
+            // to be complete before O is rescaled
+            if (s >= 1 && !(ok = wwait(tbar(t, ScanSmem::BAR_O), (s - 1) & 1))) break;
+            // ---- pass 2: exponentials, row sum, bf16 P tile
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint8_t *prow = gbase + ScanSmem::p_buf(t);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = exp2f(x[2 * j] - m_use);
-                const float p1 = exp2f(x[2 * j + 1] - m_use);
-                lsum += p0 + p1;
-                pk[j] = pack_bf16x2(p0, p1);
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                load_chunk(h, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = ex2_approx(fmaf(v[2 * j], cs, neg_m));
+                    const float p1 = ex2_approx(fmaf(v[2 * j + 1], cs, neg_m));
+                    ls[(2 * j) & 3] += p0;
+                    ls[(2 * j + 1) & 3] += p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(prow + sw128_offset(r, 4 * h + c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
-            l_run += lsum;
-            // the P tile was last read by the P.V MMA of step s - 1
-            if (s >= 1 && !(ok = wwait(bar(ScanSmem::BAR_O), (s - 1) & 1))) break;
-            uint8_t *prow = gbase + ScanSmem::p_buf;
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            if (s >= 1) {
+                // S has been read for the last time: its buffer may be rewritten
+                tc_fence_before();
+                mbar_arrive(tbar(t, ScanSmem::SFREE + (s & 1)));
+            }
+            if (s >= 1 && __any_sync(0xffffffffu, rescale)) {
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 u = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                *reinterpret_cast<uint4 *>(prow + sw128_offset(r, c)) = u;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t oa[32];
+                    tmem_ld32(T_O + lane_base + 32 * h, oa);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) oa[j] = __float_as_uint(__uint_as_float(oa[j]) * alpha);
+                    tmem_st32(T_O + lane_base + 32 * h, oa);
+                }
+                tmem_st_wait();
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(ScanSmem::PREADY));
+            mbar_arrive(tbar(t, ScanSmem::PREADY));
         }
 
         // ---- epilogue: O / l, LSE
-        if (ok) ok = wwait(bar(ScanSmem::BAR_O), (nsteps - 1) & 1);
+        if (ok) ok = wwait(tbar(t, ScanSmem::BAR_O), (nsteps - 1) & 1);
         if (ok) {
             tc_fence_after();
             uint32_t oa[32], ob[32];
@@ -413,9 +534,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     }
 
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 12) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -462,17 +583,22 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
     const FwdLayout lay = fwd_layout(1, BH, L, 2, fox);
     char *basep = static_cast<char *>(ws);
     CUtensorMap tm_qt, tm_kp, tm_v;
+    CUtensorMap tm_k64;
     if (!make_map(&tm_qt, basep + lay.off_qt, lay.Lp, BH, kTile) ||
         !make_map(&tm_kp, basep + lay.off_kp, lay.nblk * 2 * kC, BH, kTile) ||
+        !make_map(&tm_k64, basep + lay.off_kp, lay.nblk * 2 * kC, BH, kC) ||
         !make_map(&tm_v, v, L, BH, kC))
         return cudaErrorInvalidValue;
-    auto kern = fox ? path_scan_tc_kernel<true> : path_scan_tc_kernel<false>;
+    auto kern = fox ? path_scan_tc_kernel<true, false>
+                    : (scale > 0.f ? path_scan_tc_kernel<false, true>
+                                   : path_scan_tc_kernel<false, false>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kScanSmemBytes);
     if (err != cudaSuccess) return err;
-    dim3 grid(lay.nblk / 2, BH);
+    const int ntile = lay.nblk / 2;
+    dim3 grid((ntile + 1) / 2, BH);
     kern<<<grid, kScanThreads, kScanSmemBytes, stream>>>(
-        tm_qt, tm_kp, tm_v, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
+        tm_qt, tm_kp, tm_k64, tm_v, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
         reinterpret_cast<const __half *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e,

@@ -278,8 +278,8 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto wait_all = [&](uint32_t bar, uint32_t par) {
         bool ok = mbar_try_wait(bar, par);
         if (!ok) {
-            const uint64_t tstart = globaltimer_ns();
-            while (!(ok = mbar_try_wait(bar, par)) && globaltimer_ns() - tstart < limit_ns) {
+            const uint64_t tstart = cycles_now();
+            while (!(ok = mbar_try_wait(bar, par)) && cycles_now() - tstart < ns_to_cycles(limit_ns)) {
             }
         }
         if (!ok) {
@@ -292,9 +292,9 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- MMA1: [Q; W] x [W; K]^T (bf16) -> cols 0..127
     if (r == 0) {
-        const uint64_t t0s = globaltimer_ns();
+        const uint64_t t0s = cycles_now();
         bool ok = mbar_try_wait(bar_tma, 0);
-        while (!ok && globaltimer_ns() - t0s < limit_ns) ok = mbar_try_wait(bar_tma, 0);
+        while (!ok && cycles_now() - t0s < ns_to_cycles(limit_ns)) ok = mbar_try_wait(bar_tma, 0);
         if (ok) {
             tc_fence_after();
             const uint64_t a = sdesc_sw128(base + T_Q, 16, 1024);
