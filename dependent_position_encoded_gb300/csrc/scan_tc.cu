@@ -428,61 +428,65 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 }
             };
 
-            // ---- pass 1: row max
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            // ---- one pass over two 32-column chunks: online max with lazy rescaling (a
+            // chunk raises the running max only if it exceeds it by more than 2^8; then the
+            // row sum, O and the chunk already packed are rescaled), exponentials, row sum
+            float alpha = 1.f;   // accumulated rescale factor of O for this step
+            bool rescale = false;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[32];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float v[32];
                 load_chunk(h, v);
+                float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
+                for (int j = 4; j < 32; j += 4) {
                     m4[0] = fmaxf(m4[0], v[j]);
                     m4[1] = fmaxf(m4[1], v[j + 1]);
                     m4[2] = fmaxf(m4[2], v[j + 2]);
                     m4[3] = fmaxf(m4[3], v[j + 3]);
                 }
-            }
-            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            if (raw_s) mx *= scale_log2;
-            // lazy rescaling: keep the old max unless the new one exceeds it by 2^8
-            float alpha = 1.f;
-            bool rescale = false;
-            if (mx > m_run + kRescaleThreshold) {
-                if (m_run != -INFINITY) {
-                    alpha = ex2_approx(m_run - mx);
-                    rescale = true;
-                }
-                m_run = mx;
-                l_run *= alpha;
-            }
-            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            const float cs = raw_s ? scale_log2 : 1.f;
-            const float neg_m = -m_use;
-            // the P tile was last read by this tile's P.V MMA of step s - 1, which also has
-            // to be complete before O is rescaled
-            if (s >= 1 && !(ok = wwait(tbar(t, ScanSmem::BAR_O), (s - 1) & 1))) break;
-            // ---- pass 2: exponentials, row sum, bf16 P tile
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint8_t *prow = gbase + ScanSmem::p_buf(t);
+                float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                if (raw_s) mx *= scale_log2;
+                if (mx > m_run + kRescaleThreshold) {
+                    if (m_run != -INFINITY) {
+                        const float a = ex2_approx(m_run - mx);
+                        alpha *= a;
+                        rescale = true;
+                        l_run *= a;
+                        ls[0] *= a; ls[1] *= a; ls[2] *= a; ls[3] *= a;
+                        if (h == 1) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v[32];
-                load_chunk(h, v);
-                uint32_t pk[16];
+                            for (int j = 0; j < 16; ++j) {
+                                const float2 f = unpack_bf16x2(pk[j]);
+                                pk[j] = pack_bf16x2(f.x * a, f.y * a);
+                            }
+                        }
+                    }
+                    m_run = mx;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                const float cs = raw_s ? scale_log2 : 1.f;
+                const float neg_m = -m_use;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const float p0 = ex2_approx(fmaf(v[2 * j], cs, neg_m));
                     const float p1 = ex2_approx(fmaf(v[2 * j + 1], cs, neg_m));
                     ls[(2 * j) & 3] += p0;
                     ls[(2 * j + 1) & 3] += p1;
-                    pk[j] = pack_bf16x2(p0, p1);
+                    pk[16 * h + j] = pack_bf16x2(p0, p1);
                 }
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(prow + sw128_offset(r, 4 * h + c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // the P tile was last read by this tile's P.V MMA of step s - 1, which also has
+            // to be complete before O is rescaled
+            if (s >= 1 && !(ok = wwait(tbar(t, ScanSmem::BAR_O), (s - 1) & 1))) break;
+            uint8_t *prow = gbase + ScanSmem::p_buf(t);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(prow + sw128_offset(r, c)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             if (s >= 1) {
                 // S has been read for the last time: its buffer may be rewritten
                 tc_fence_before();
