@@ -311,7 +311,7 @@ def run_profile_case(args):
     torch.cuda.synchronize()
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend=None):
     if n_gpus <= 1 and "WORLD_SIZE" not in os.environ:
         return 0, 1, 0
     import torch.distributed as dist
@@ -319,11 +319,27 @@ def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", 1))
     local = int(os.environ.get("LOCAL_RANK", 0))
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
     if backend == "nccl":
         torch.cuda.set_device(local)
     dist.init_process_group(backend=backend)
     return rank, world, local
+
+
+def shard_workload(wl, rank):
+    """The rank's shard of the global batch: its own B rows, drawn from their own seed.
+
+    Batch rows are independent problems, so ranks share nothing on the data path; rank 0's
+    shard is the single-GPU workload itself.
+    """
+    import dataclasses
+    return wl if rank == 0 else dataclasses.replace(wl, seed=wl.seed + 7919 * rank)
+
+
+def aggregate(local_ms, world, rows_per_rank, L, steps):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    t_max = max_over_ranks(local_ms, world)
+    return t_max, t_max / steps, world * rows_per_rank * L * steps / (t_max * 1e-3)
 
 
 def barrier(world):
@@ -336,7 +352,8 @@ def max_over_ranks(x, world):
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -404,7 +421,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = load_peaks()
-    wl = pi.BF16_L4096
+    wl = shard_workload(pi.BF16_L4096, rank)
     x = pi.workload_inputs(wl, device=dev)
     B, H, L = wl.B, wl.H, wl.L
     f_attn, f_corr, f_pre = fwd_flops(B, H, L)
@@ -417,9 +434,7 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     clocks = clk.summary()
-    t_max = max_over_ranks(total_ms, world)
-    ms_step = t_max / args.steps
-    value = world * B * L * args.steps / (t_max * 1e-3)
+    t_max, ms_step, value = aggregate(total_ms, world, B, L, args.steps)
 
     scan_avg = statistics.mean(scan_ms)
     prep_avg = statistics.mean(prep_ms)
@@ -437,8 +452,9 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": wl.name, "B": B, "H": H, "L": L, "d": 64,
-                       "per_rank_batch": B, "l2": "inputs 2.1 GB per step (> L2), no flush",
-                       "parallelism": "replicas" if world > 1 else "single"},
+                       "per_rank_batch": B, "global_batch": world * B,
+                       "l2": "inputs 2.1 GB per step (> L2), no flush",
+                       "parallelism": "dp%d (batch shards)" % world if world > 1 else "single"},
             "tflops": F / (ms_step * 1e-3) / 1e12 * world,
             "fa_equiv_tflops": f_attn / (ms_step * 1e-3) / 1e12 * world,
             "fwd_roofline_frac": F / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"],
@@ -448,13 +464,12 @@ def main():
 
     if not args.no_extras:
         e2e_ms, h2d, d2h = time_e2e(pa, x, max(2, args.steps // 2), 3)
-        e2e_max = max_over_ranks(e2e_ms, world)
         n_e2e = max(2, args.steps // 2)
-        line["e2e"] = {"value": world * B * L * n_e2e / (e2e_max * 1e-3), "unit": "tokens/s",
+        line["e2e"] = {"value": aggregate(e2e_ms, world, B, L, n_e2e)[2], "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del x
         torch.cuda.empty_cache()
-        fw = pi.FOX_L16384
+        fw = shard_workload(pi.FOX_L16384, rank)
         xf = pi.workload_inputs(fw, device=dev)
         fox_total, fox_scan, fox_prep = time_forward(pa, xf, 3, 3, fox=True)
         fa, fc, fp = fwd_flops(fw.B, fw.H, fw.L)

@@ -39,8 +39,8 @@
 //   warp 12 also owns TMEM.
 // Each issuing thread is its own in-order MMA stream: one thread issuing back to back
 // cannot keep the tensor core busy with N <= 128 instructions, four can.
-// The bf16 state tile is double-buffered, the P tile single-buffered (rewritten after the
-// tile's previous P.V has completed).
+// The bf16 state tile and the P tile are single-buffered: the state is rewritten once the
+// S|state MMA that read it has completed, P once the tile's previous P.V has completed.
 #include "common.cuh"
 
 namespace path {
@@ -48,7 +48,7 @@ namespace path {
 namespace {
 
 constexpr int kScanThreads = 512;
-constexpr int NS = 4;                       // TMA stages ([K~|P|K~] and V of one block each)
+constexpr int NS = 5;                       // TMA stages ([K~|P|K~] and V of one block each)
 constexpr uint32_t kTileBytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr uint32_t kVBytes = 64 * 128;      // 64 rows x 64 bf16
 constexpr uint32_t kKdupBytes = 64 * 128;   // second copy of K~_b after P_b
@@ -57,9 +57,9 @@ constexpr float kRescaleThreshold = 8.f;    // lazy rescale: keep the old max wi
 
 struct ScanSmem {
     // byte offsets from the 1024-aligned base
-    __host__ __device__ static constexpr uint32_t q_st(int t, int i) { return (uint32_t)(2 * t + i) * kTileBytes; }
-    __host__ __device__ static constexpr uint32_t p_buf(int t) { return (uint32_t)(4 + t) * kTileBytes; }
-    static constexpr uint32_t stage = 6 * kTileBytes;
+    __host__ __device__ static constexpr uint32_t q_st(int t) { return (uint32_t)t * kTileBytes; }
+    __host__ __device__ static constexpr uint32_t p_buf(int t) { return (uint32_t)(2 + t) * kTileBytes; }
+    static constexpr uint32_t stage = 4 * kTileBytes;
     static constexpr uint32_t bars = stage + NS * kStageBytes;
     // barrier indices: the ring, then ten per tile (S buffers have their own), then one
     static constexpr int FULL = 0, EMPTY = NS, TILE0 = 2 * NS;
@@ -73,6 +73,7 @@ struct ScanSmem {
 };
 
 constexpr uint32_t kScanSmemBytes = ScanSmem::bytes + 1024;  // + alignment slack
+static_assert(kScanSmemBytes <= 227u * 1024u, "scan shared memory exceeds the per-CTA limit");
 
 struct Waiter {
     volatile uint32_t *abort;
@@ -140,10 +141,10 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             mbar_init(tbar(t, ScanSmem::BAR_SX), 1);
             mbar_init(tbar(t, ScanSmem::BAR_SX + 1), 1);
             mbar_init(tbar(t, ScanSmem::BAR_O), 1);
-            mbar_init(tbar(t, ScanSmem::QREADY), 128);
-            mbar_init(tbar(t, ScanSmem::SFREE), 128);
-            mbar_init(tbar(t, ScanSmem::SFREE + 1), 128);
-            mbar_init(tbar(t, ScanSmem::PREADY), 128);
+            mbar_init(tbar(t, ScanSmem::QREADY), 4);  // one arrival per warp
+            mbar_init(tbar(t, ScanSmem::SFREE), 4);
+            mbar_init(tbar(t, ScanSmem::SFREE + 1), 4);
+            mbar_init(tbar(t, ScanSmem::PREADY), 4);
             mbar_init(tbar(t, ScanSmem::FINAL_SX), 1);
             mbar_init(tbar(t, ScanSmem::FINAL_PV), 1);
         }
@@ -189,7 +190,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (s >= 3 && !(ok = wait(tbar(t, ScanSmem::SFREE + (s & 1)), ((s - 3) >> 1) & 1)))
                     break;
                 tc_fence_after();
-                const uint64_t a_q = sdesc_sw128(base + ScanSmem::q_st(t, s & 1), 16, 1024);
+                const uint64_t a_q = sdesc_sw128(base + ScanSmem::q_st(t), 16, 1024);
                 const uint64_t b_kp =
                     sdesc_sw128(stage_kp(st) + ((s & 1) ? 64u * 128u : 0u), 16, 1024);
 #pragma unroll
@@ -218,7 +219,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 tma_prefetch_desc(&tm_v);
                 for (int tt = 0; tt < (hasB ? 2 : 1); ++tt) {
                     mbar_arrive_expect_tx(tbar(tt, ScanSmem::QFULL), kTileBytes);
-                    tma_load_3d(base + ScanSmem::q_st(tt, 1), &tm_qt, tbar(tt, ScanSmem::QFULL), 0,
+                    tma_load_3d(base + ScanSmem::q_st(tt), &tm_qt, tbar(tt, ScanSmem::QFULL), 0,
                                 tile_of(tt) * kTile, bh);
                 }
             }
@@ -312,8 +313,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (s >= nsteps_of(t) - 1) continue;  // the last step needs no new state
                 if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX + (s & 1)), ((s - 1) >> 1) & 1))) break;
                 tc_fence_after();
-                // the state of step s + 1 goes to buffer (s + 1) & 1
-                uint8_t *row = gbase + ScanSmem::q_st(t, (s + 1) & 1);
+                // the state of step s + 1 replaces that of step s, whose only reader (the
+                // S|state MMA of step s) has completed
+                uint8_t *row = gbase + ScanSmem::q_st(t);
                 if (s >= 2 || quad >= 2) {
                     uint32_t qa[32], qb[32];
                     tmem_ld32(t_state(t) + lane_base, qa);
@@ -339,7 +341,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(tbar(t, ScanSmem::QREADY));
+                mbar_arrive_warp(tbar(t, ScanSmem::QREADY));
             }
         }
         tc_fence_before();
@@ -490,7 +492,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             if (s >= 1) {
                 // S has been read for the last time: its buffer may be rewritten
                 tc_fence_before();
-                mbar_arrive(tbar(t, ScanSmem::SFREE + (s & 1)));
+                mbar_arrive_warp(tbar(t, ScanSmem::SFREE + (s & 1)));
             }
             if (s >= 1 && __any_sync(0xffffffffu, rescale)) {
                 tc_fence_after();
@@ -507,7 +509,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(tbar(t, ScanSmem::PREADY));
+            mbar_arrive_warp(tbar(t, ScanSmem::PREADY));
         }
 
         // ---- epilogue: O / l, LSE
