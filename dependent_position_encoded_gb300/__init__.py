@@ -26,7 +26,7 @@ HEAD_DIM = 64
 
 EXPORTED = ("path_workspace_bytes", "path_attn_fwd", "path_fox_fwd", "path_fwd_prepare",
             "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string",
-            "path_decode_step_noalloc")
+            "path_decode_step_noalloc", "path_fox_first_blocks")
 
 _lib = None
 
@@ -71,6 +71,8 @@ def _load():
     lib.path_decode_step.restype = I
     lib.path_decode_step_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.path_decode_step_noalloc.restype = I
+    lib.path_fox_first_blocks.argtypes = [P, S, I, I, I, I, I, P, P]
+    lib.path_fox_first_blocks.restype = I
     lib.path_check_workspace.argtypes = [P, P]
     lib.path_check_workspace.restype = I
     lib.path_status_string.argtypes = [I]
@@ -95,13 +97,17 @@ def _torch():
     return torch
 
 
-def _dtype_code(t):
+def _dtype_code_of(dtype):
     torch = _torch()
-    if t.dtype == torch.bfloat16:
+    if dtype == torch.bfloat16:
         return BF16
-    if t.dtype == torch.float32:
+    if dtype == torch.float32:
         return F32
-    raise TypeError("unsupported dtype %s (bfloat16 or float32)" % t.dtype)
+    raise TypeError("unsupported dtype %s (bfloat16 or float32)" % dtype)
+
+
+def _dtype_code(t):
+    return _dtype_code_of(t.dtype)
 
 
 def _ptr(t):
@@ -226,6 +232,19 @@ def path_fwd_scan(v, workspace, out=None, lse=True, fox=False, scale=None, strea
                                  _scale(scale, d), _ptr(workspace), workspace.numel(),
                                  _stream(stream, v.device)), "path_fwd_scan")
     return out, lse
+
+
+def path_fox_first_blocks(workspace, B, H, L, dtype, stream=None):
+    """PaTH-FoX early-exit extents left in `workspace` by path_fwd_prepare(..., log_f):
+    an int32 tensor (B, H, ceil(L / 64)) of the lowest key block each query block needs."""
+    torch = _torch()
+    nq = (L + 63) // 64
+    first = torch.empty((B, H, nq), dtype=torch.int32, device=workspace.device)
+    _check(_load().path_fox_first_blocks(_ptr(workspace), workspace.numel(), B, H, L, 64,
+                                         _dtype_code_of(dtype), _ptr(first),
+                                         _stream(stream, workspace.device)),
+           "path_fox_first_blocks")
+    return first
 
 
 def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, out=None,

@@ -30,7 +30,7 @@ constexpr uint32_t kStatusTimeout = 7u;
 // padded tokens carry identity transitions and zero queries and keys.
 struct FwdLayout {
     int BH, L, nblk, Lp, elt;
-    size_t off_qt, off_kp, off_dg, off_c2, total;
+    size_t off_qt, off_kp, off_dg, off_c2, off_mpre, off_kpre, off_fb, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -51,8 +51,19 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     off = align256(off + bh * lay.nblk * 2 * kC * kD * elt_bytes);
     lay.off_dg = off;
     off = align256(off + bh * lay.nblk * kC * kC * (elt_bytes == 2 ? 2 : 4));
-    lay.off_c2 = off;
-    if (fox) off = align256(off + bh * lay.Lp * sizeof(float));
+    // PaTH-FoX only: c2 = log2(e) * cumsum(log f) (BH, Lp); per key block the prefix
+    // minimum of c2 and prefix maximum of |k~| (BH, nblk); per query block the first key
+    // block the scan visits (BH, nblk) int32
+    lay.off_c2 = lay.off_mpre = lay.off_kpre = lay.off_fb = off;
+    if (fox) {
+        off = align256(off + bh * lay.Lp * sizeof(float));
+        lay.off_mpre = off;
+        off = align256(off + bh * lay.nblk * sizeof(float));
+        lay.off_kpre = off;
+        off = align256(off + bh * lay.nblk * sizeof(float));
+        lay.off_fb = off;
+        off = align256(off + bh * lay.nblk * sizeof(int));
+    }
     lay.total = off;
     return lay;
 }

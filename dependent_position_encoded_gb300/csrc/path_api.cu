@@ -13,8 +13,8 @@ template <typename T>
 cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const float *beta,
                               const float *log_f, int BH, int L, float scale, void *ws,
                               cudaStream_t stream);
-cudaError_t launch_fox_cumsum(const float *log_f, int BH, int L, int elt_bytes, void *ws,
-                              cudaStream_t stream);
+cudaError_t launch_fox_prepare(const float *log_f, int BH, int L, int elt_bytes, float scale,
+                               void *ws, cudaStream_t stream);
 cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, const float *beta,
                                  const float *log_f, int BH, int L, float scale, void *ws,
                                  uint64_t limit_ns, cudaStream_t stream);
@@ -90,7 +90,9 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
                         ? launch_ut_prepare_tc(q, k, w, beta, lf, B * H, L, scale, ws,
                                                kWaitLimitNs, stream)
                         : launch_ut_prepare<float>(q, k, w, beta, lf, B * H, L, scale, ws, stream);
-    if (e == cudaSuccess && fox) e = launch_fox_cumsum(lf, B * H, L, elt_bytes(dtype), ws, stream);
+    // FoX: gate prefix sums and the scan's early-exit extents (reads K1's q~, k~ and table)
+    if (e == cudaSuccess && fox)
+        e = launch_fox_prepare(lf, B * H, L, elt_bytes(dtype), scale, ws, stream);
     return from_cuda(e);
 }
 
@@ -133,6 +135,23 @@ path_status path_fwd_prepare(const void *q, const void *k, const void *w, const 
                              float scale, void *ws, size_t ws_bytes, void *stream) {
     return prepare_impl(q, k, w, beta, log_f, log_f != nullptr, B, H, L, d, dtype, scale, ws,
                         ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H, int L,
+                                  int d, int dtype, int *first_block, void *stream) {
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if ((long long)B * H * L == 0) return PATH_OK;
+    if (!first_block) return PATH_ERR_NULL;
+    if (!aligned(first_block, 4)) return PATH_ERR_ALIGN;
+    const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), true);
+    if ((st = check_ws(const_cast<void *>(ws), ws_bytes, lay.total)) != PATH_OK) return st;
+    const int nq = (L + kC - 1) / kC;
+    return from_cuda(cudaMemcpy2DAsync(first_block, (size_t)nq * sizeof(int),
+                                       static_cast<const char *>(ws) + lay.off_fb,
+                                       (size_t)lay.nblk * sizeof(int), (size_t)nq * sizeof(int),
+                                       (size_t)B * H, cudaMemcpyDeviceToDevice,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, int H, int L,

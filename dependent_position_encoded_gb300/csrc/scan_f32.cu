@@ -35,8 +35,9 @@ template <bool FOX>
 __global__ void __launch_bounds__(kThreads)
 path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
                      const float *__restrict__ kp, const float *__restrict__ dg,
-                     const float *__restrict__ c2, float *__restrict__ out,
-                     float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2) {
+                     const float *__restrict__ c2, const int *__restrict__ first_blk,
+                     float *__restrict__ out, float *__restrict__ lse, int L, int Lp, int nblk,
+                     float scale_log2) {
     extern __shared__ __align__(16) float sm[];
     float *XT = sm;          // state, transposed: XT[c][i]
     float *KT = XT + BUF;    // k~_b transposed: KT[c][j]
@@ -67,7 +68,9 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
-    for (int b = ib; b >= 0; --b) {
+    // PaTH-FoX stops above the blocks whose keys all weigh below e^-40 (see fox_exit.cu)
+    const int b_last = FOX ? first_blk[head * nblk + ib] : 0;
+    for (int b = ib; b >= b_last; --b) {
         __syncthreads();
         for (int e = tid; e < kC * kD; e += kThreads) {
             const int j = e / kD, c = e % kD;
@@ -176,6 +179,7 @@ cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int 
         reinterpret_cast<const float *>(basep + lay.off_kp),
         reinterpret_cast<const float *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
+        fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,
         static_cast<float *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e);
     return cudaGetLastError();
 }

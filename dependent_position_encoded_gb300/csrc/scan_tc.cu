@@ -20,7 +20,8 @@
 //   s >= 2: block ib1 - s for every row.
 //
 // One CTA owns a pair of tiles of one head, A = 2p and B = 2p + 1, and streams the key
-// blocks 4p+3, 4p+2, ..., 0 once through an NS-stage TMA ring: B consumes every block,
+// blocks 4p+3, 4p+2, ..., 0 (PaTH-FoX: down to the lower of the two tiles' early-exit
+// extents from fox_exit.cu) once through an NS-stage TMA ring: B consumes every block,
 // A every block from 4p+1 down, so each stage is loaded once for both tiles. A stage holds
 // [K~_b; P_b; K~_b] (K~_b loaded twice) and V_b. Per tile and step, S = X K~_b^T and the
 // new state X P_b^T come from ONE MMA with N = 128: B = [K~_b; P_b] on even steps (S lands
@@ -103,7 +104,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_k64,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __nv_bfloat16 *__restrict__ qt, const __half *__restrict__ dg,
-                    const float *__restrict__ c2, __nv_bfloat16 *__restrict__ out,
+                    const float *__restrict__ c2, const int *__restrict__ first_blk,
+                    __nv_bfloat16 *__restrict__ out,
                     float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
                     uint32_t *status, uint64_t limit_ns, int force_timeout) {
     extern __shared__ uint8_t smem_raw[];
@@ -118,11 +120,24 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const int bh = blockIdx.y;
     const bool hasB = 2 * pair + 1 < ntile;
     const int top = hasB ? 4 * pair + 3 : 4 * pair + 1;  // first key block of the stream
-    const int nstream = top + 1;
+    // lowest key block each tile visits: 0, or for PaTH-FoX the early-exit extent of its
+    // two query blocks (never above the tile's own first block)
+    int fb[2] = {0, 0};
+    if (FOX) {
+        for (int t = 0; t < (hasB ? 2 : 1); ++t) {
+            const int *f = first_blk + (size_t)blockIdx.y * nblk + 4 * pair + 2 * t;
+            fb[t] = min(min(__ldg(f), __ldg(f + 1)), 4 * pair + 2 * t);
+        }
+    }
+    const int nstream = top + 1 - (hasB ? min(fb[0], fb[1]) : fb[0]);
     // tile t (0 = A, 1 = B): tile index, its step count, and stream position of its step 0
     auto tile_of = [&](int t) { return 2 * pair + t; };
-    auto nsteps_of = [&](int t) { return 2 * tile_of(t) + 2; };
+    auto nsteps_of = [&](int t) { return 2 * tile_of(t) + 2 - fb[t]; };
     auto off_of = [&](int t) { return top - (2 * tile_of(t) + 1); };
+    // whether tile t reads stream position n
+    auto reads = [&](int t, int n) {
+        return (t == 0 || hasB) && n >= off_of(t) && n < off_of(t) + nsteps_of(t);
+    };
 
     auto bar = [&](int i) { return base + ScanSmem::bars + 8u * (uint32_t)i; };
     auto tbar = [&](int t, int which) { return bar(ScanSmem::per_tile(t, which)); };
@@ -260,7 +275,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         // this commit covers every read of the stage by tile t; two arrivals
                         // per stage (a stage read by one tile only gets both from that tile)
                         umma_commit(bar(ScanSmem::EMPTY + st));
-                        if (!(hasB && n >= off_of(0))) umma_commit(bar(ScanSmem::EMPTY + st));
+                        if (!reads(1 - t, n)) umma_commit(bar(ScanSmem::EMPTY + st));
                         ++s;
                         progress = true;
                     }
@@ -307,7 +322,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         auto wwait = [&](uint32_t b_, uint32_t par) {
             return __all_sync(0xffffffffu, wait(b_, par)) != 0;
         };
-        const int smax = nsteps_of(hasB ? 1 : 0);
+        const int smax = hasB ? max(nsteps_of(0), nsteps_of(1)) : nsteps_of(0);
         for (int s = 1; s < smax && ok; ++s) {
             for (int t = hasB ? 1 : 0; t >= 0; --t) {
                 if (s >= nsteps_of(t) - 1) continue;  // the last step needs no new state
@@ -352,7 +367,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int tile = tile_of(t);
         const int ib0 = 2 * tile, ib1 = 2 * tile + 1;
-        const int nsteps = ib1 + 1;
+        const int nsteps = nsteps_of(t);
         const int i = tile * kTile + r;          // query index
         const size_t head = (size_t)bh;
         float m_run = -INFINITY, l_run = 0.f;
@@ -607,6 +622,7 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
         tm_qt, tm_kp, tm_k64, tm_v, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
         reinterpret_cast<const __half *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
+        fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e,
         reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout);
     return cudaGetLastError();

@@ -280,47 +280,6 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     }
 }
 
-// Inclusive prefix sum of log f over each head, scaled by log2(e): c2[bh][t].
-// One CTA of 1024 threads per head; padded positions repeat the last value.
-__global__ void __launch_bounds__(1024)
-fox_cumsum_kernel(const float *__restrict__ log_f, int L, int Lp, float *__restrict__ c2) {
-    __shared__ float warp_tot[32];
-    __shared__ float carry_s;
-    const int bh = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const float *src = log_f + (size_t)bh * L;
-    float *dst = c2 + (size_t)bh * Lp;
-    if (tid == 0) carry_s = 0.f;
-    __syncthreads();
-    for (int base = 0; base < Lp; base += 1024) {
-        const int t = base + tid;
-        float x = (t < L) ? src[t] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            float n = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += n;
-        }
-        if (lane == 31) warp_tot[wid] = x;
-        __syncthreads();
-        if (wid == 0) {
-            float y = warp_tot[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                float n = __shfl_up_sync(0xffffffffu, y, o);
-                if (lane >= o) y += n;
-            }
-            warp_tot[lane] = y;
-        }
-        __syncthreads();
-        const float carry = carry_s;
-        const float v = carry + x + (wid > 0 ? warp_tot[wid - 1] : 0.f);
-        if (t < Lp) dst[t] = kLog2e * v;
-        __syncthreads();
-        if (tid == 1023) carry_s = v;
-        __syncthreads();
-    }
-}
-
 }  // namespace
 
 size_t ut_prepare_smem_bytes() { return (size_t)(8 * BUF + 2 * kC) * sizeof(float); }
@@ -345,14 +304,6 @@ cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const
 }
 
 // PaTH-FoX: log2(e) * inclusive prefix sums of log f per head into the workspace.
-cudaError_t launch_fox_cumsum(const float *log_f, int BH, int L, int elt_bytes, void *ws,
-                              cudaStream_t stream) {
-    const FwdLayout lay = fwd_layout(1, BH, L, elt_bytes, true);
-    fox_cumsum_kernel<<<BH, 1024, 0, stream>>>(
-        log_f, L, lay.Lp, reinterpret_cast<float *>(static_cast<char *>(ws) + lay.off_c2));
-    return cudaGetLastError();
-}
-
 template cudaError_t launch_ut_prepare<float>(const void *, const void *, const void *,
                                               const float *, const float *, int, int, float,
                                               void *, cudaStream_t);

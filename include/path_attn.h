@@ -89,6 +89,11 @@ path_status path_attn_fwd(const void *q, const void *k, const void *v, const voi
  * sum_{s=j+1..i} log f_s (added after scaling) on every logit.
  *   log_f : (B, H, L) fp32 per-token log forget gate (<= 0 in practice; any finite value)
  * ws must hold path_workspace_bytes(PATH_OP_FOX_FWD, ...).
+ * Early exit (exact within rounding): since every H_s is a contraction, a PaTH logit
+ * is at most |scale| |q~_i| |k~_j|; the scan of a 128-row tile stops above the key
+ * blocks whose every key, bias included, weighs below e^-40 relative to the largest
+ * logit of the row's own block (with the bound doubled for rounding). See
+ * path_fox_first_blocks.
  */
 path_status path_fox_fwd(const void *q, const void *k, const void *v, const void *w,
                          const float *beta, const float *log_f, void *out, float *lse,
@@ -115,6 +120,20 @@ path_status path_fwd_prepare(const void *q, const void *k, const void *w, const 
 path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, int H, int L,
                           int d, int dtype, float scale, void *ws, size_t ws_bytes,
                           void *stream);
+
+/*
+ * PaTH-FoX early-exit extents, for inspection. After path_fwd_prepare with log_f on ws
+ * (and until ws is reused), copies asynchronously on `stream`, into the device buffer
+ * first_block (B * H * ceil(L / 64) int32, row-major (B, H, L / 64)), for every query
+ * block of 64 rows the lowest 64-token key block any of its rows needs; the scan visits
+ * key blocks from the tile's own down to the lower of its two query blocks' values.
+ * Values lie in [0, query block]. Returns PATH_ERR_WORKSPACE if ws_bytes is below
+ * path_workspace_bytes(PATH_OP_FOX_FWD, ...). The pages give no such call: it exposes
+ * the rule of review "거리에서 경로로, PaTH Attention" §4 / technical summary
+ * "技術要約: PaTH Attention" §2 (the gate makes distant keys vanish) for testing.
+ */
+path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H, int L,
+                                  int d, int dtype, int *first_block, void *stream);
 
 /*
  * One PaTH decode step (the pages' inference scheme: the new token's

@@ -47,8 +47,10 @@ def test_workspace_sizes(lib):
     # fp32: every region fp32
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.F32) == \
         256 + 128 * 64 * 4 + 2 * 128 * 64 * 4 + 2 * 64 * 64 * 4
+    # FoX adds c2 (Lp fp32) and, per key block, two fp32 bounds and one int32 extent,
+    # each region rounded up to 256 B
     fox = lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 64, lib.BF16)
-    assert fox == lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) + 512
+    assert fox == lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) + 512 + 3 * 256
     # ragged L rounds up to an even number of 64-token blocks
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 65, 64, lib.BF16) == \
         lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16)
@@ -123,3 +125,18 @@ def test_noalloc_decode_rejects_problems_beyond_the_fixed_scratch(so):
     rc = so.path_decode_step_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, n, n + 1,
                                      64, 1, ctypes.c_float(0.125), FAKE, None)
     assert rc == 5
+
+
+def test_fox_first_blocks_argument_checks(so):
+    def call(**kw):
+        a = dict(ws=FAKE, ws_bytes=1 << 30, B=1, H=1, L=128, d=64, dtype=1, first=FAKE)
+        a.update(kw)
+        return so.path_fox_first_blocks(a["ws"], ctypes.c_size_t(a["ws_bytes"]), a["B"], a["H"],
+                                        a["L"], a["d"], a["dtype"], a["first"], None)
+    assert call(first=None) == 1
+    assert call(ws=None) == 1
+    assert call(d=32) == 2
+    assert call(first=FAKE + 2) == 4
+    assert call(ws=FAKE + 8) == 4
+    assert call(ws_bytes=1024) == 5
+    assert call(L=0) == 0

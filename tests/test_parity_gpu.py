@@ -235,6 +235,92 @@ def test_fox_long_workload_sampled(lib):
     _sampled_parity(lib, pi.FOX_L16384, n_heads=8, n_rows=300)
 
 
+# ---------------------------------------------------------------- FoX early exit
+
+def _fox_with_extents(lib, x, scale=None):
+    """Prepare + scan through the two-stage ABI; returns (extents, out, lse)."""
+    B, H, L, _ = x["q"].shape
+    code = lib.BF16 if x["q"].dtype == torch.bfloat16 else lib.F32
+    ws = lib.new_workspace(lib.OP_FOX_FWD, B, H, L, code, "cuda")
+    lib.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws, log_f=x["log_f"], scale=scale)
+    first = lib.path_fox_first_blocks(ws, B, H, L, x["q"].dtype)
+    out, lse = lib.path_fwd_scan(x["v"], ws, fox=True, scale=scale)
+    return first.cpu().numpy(), out, lse
+
+
+def _check_extents_safe(x, first, scale=None):
+    """Every key a query block skips weighs below e^-40 relative to its row's largest
+    logit, by the oracle's fp64 logits; returns the fraction of key blocks skipped."""
+    B, H, L, _ = x["q"].shape
+    skipped = total = 0
+    for b in range(B):
+        for h in range(H):
+            lg = oracle.path_logits(x["q"][b, h].cpu(), x["k"][b, h].cpu(), x["w"][b, h].cpu(),
+                                    x["beta"][b, h].cpu(), x["log_f"][b, h].cpu(), scale)
+            m = lg.max(axis=1)
+            for qb in range(first.shape[2]):
+                f = int(first[b, h, qb])
+                assert 0 <= f <= qb
+                skipped += f
+                total += qb
+                if f:
+                    rows = slice(64 * qb, min(64 * qb + 64, L))
+                    assert (lg[rows, :64 * f] < m[rows, None] - 40.0).all()
+    return skipped / max(total, 1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_fox_early_exit_strong_gate(lib, dtype):
+    # log f ~ logsigmoid(N(-1, 1)): about -80 nats per 64-token block, so every tile
+    # stops within a block or two of its own; the output must still match the oracle's
+    # full sum
+    x = pi.make_fwd_inputs(1, 2, 1000, dtype=dtype, seed=41, clip=0.0 if dtype == torch.float32
+                           else pi.BETA_CLIP, fox=True, device="cuda")
+    x["log_f"] = torch.nn.functional.logsigmoid(torch.randn_like(x["log_f"]) - 1.0).contiguous()
+    first, out, lse = _fox_with_extents(lib, x)
+    frac = _check_extents_safe(x, first)
+    assert frac > 0.8, frac
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    if dtype == torch.float32:
+        rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+        assert rel <= F32_MAX_REL, rel
+        assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
+    else:
+        check_bf16(out, ref, lse, ref_lse)
+
+
+def test_fox_early_exit_workload_gate(lib):
+    # the FoX workload's gate, logsigmoid(N(2, 1)): the exit is active from a few blocks on
+    x = pi.make_fwd_inputs(1, 2, 2048, seed=42, fox=True, device="cuda")
+    first, out, lse = _fox_with_extents(lib, x)
+    frac = _check_extents_safe(x, first)
+    assert frac > 0.3, frac
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_fox_early_exit_mixed_sign_gate(lib):
+    # log f of both signs: the prefix sums are not monotone; the bound uses prefix minima
+    x = pi.make_fwd_inputs(2, 2, 640, seed=43, fox=True, device="cuda")
+    x["log_f"] = (0.5 * torch.randn_like(x["log_f"]) - 0.3).contiguous()
+    first, out, lse = _fox_with_extents(lib, x, scale=0.2)
+    _check_extents_safe(x, first, scale=0.2)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"],
+                                   scale=0.2)
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_fox_zero_gate_has_no_exit(lib):
+    # log f = 0: no bias, nothing can be skipped, and FoX equals PaTH (up to rounding:
+    # the FoX scan applies the scale in another order than the PaTH scan)
+    x = pi.make_fwd_inputs(1, 2, 700, seed=44, fox=True, device="cuda")
+    x["log_f"] = torch.zeros_like(x["log_f"])
+    first, out, lse = _fox_with_extents(lib, x)
+    assert (first == 0).all()
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
 # ---------------------------------------------------------------- decode
 
 def _decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None):
