@@ -25,12 +25,15 @@ constexpr uint32_t kStatusTimeout = 7u;
 //                             rows 64-127 the dense block transition P_b (row-major)
 //   dg  : (BH, nblk, 64, 64)  diagonal-block logits in log2 units (masked -inf): fp16 for
 //                             bf16 inputs, fp32 for fp32 inputs
+//   pr  : (BH, nblk/2, 128, 64) bf16 inputs only: per pair of blocks u = (2u, 2u+1),
+//                             rows 0-63 K^_j = P_{2u+1}^T k~_j (keys of block 2u carried
+//                             through block 2u+1), rows 64-127 Pi_u = P_{2u} P_{2u+1}
 //   c2  : (BH, Lp)            fp32 log2(e) * cumsum(log f) (PaTH-FoX only)
 // nblk is rounded up to an even count so that 128-row tiles are complete;
 // padded tokens carry identity transitions and zero queries and keys.
 struct FwdLayout {
     int BH, L, nblk, Lp, elt;
-    size_t off_qt, off_kp, off_dg, off_c2, off_mpre, off_kpre, off_fb, total;
+    size_t off_qt, off_kp, off_dg, off_pr, off_c2, off_mpre, off_kpre, off_fb, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -51,6 +54,8 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     off = align256(off + bh * lay.nblk * 2 * kC * kD * elt_bytes);
     lay.off_dg = off;
     off = align256(off + bh * lay.nblk * kC * kC * (elt_bytes == 2 ? 2 : 4));
+    lay.off_pr = off;
+    if (elt_bytes == 2) off = align256(off + bh * (lay.nblk / 2) * 2 * kC * kD * 2);
     // PaTH-FoX only: c2 = log2(e) * cumsum(log f) (BH, Lp); per key block the prefix
     // minimum of c2 and prefix maximum of |k~| (BH, nblk); per query block the first key
     // block the scan visits (BH, nblk) int32
@@ -289,6 +294,42 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
 // Records the first error code in the workspace status word.
 __device__ __forceinline__ void report_status(uint32_t *status, uint32_t code) {
     if (status) atomicCAS(status, 0u, code);
+}
+
+// ---------------------------------------------------------------- host: TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 map over (heads, rows, 64 columns) with a (1, box_rows, 64) box and 128-byte
+// swizzle (the layout every tcgen05 operand tile here uses). Rows beyond `rows` read 0.
+inline bool make_map_bf16(CUtensorMap *m, const void *ptr, int rows, int heads, int box_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)rows * kD * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace path

@@ -59,8 +59,33 @@ __device__ __forceinline__ float row_norm2(const float *row) {
     return s;
 }
 
-__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
-__device__ __forceinline__ float to_float(float x) { return x; }
+// Largest entry of one 64-element row of the diagonal-block table (entries above the
+// diagonal and beyond L hold -inf).
+__device__ __forceinline__ float row_max(const __half *row) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(row);
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 u = __ldg(p + c);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
+            m = fmaxf(m, fmaxf(f.x, f.y));
+        }
+    }
+    return m;
+}
+__device__ __forceinline__ float row_max(const float *row) {
+    const float4 *p = reinterpret_cast<const float4 *>(row);
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const float4 f = __ldg(p + c);
+        m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+    }
+    return m;
+}
 
 // Per head (one CTA of 1024 threads, 16 blocks of 64 tokens per pass):
 //   c2[t]   = log2(e) * sum_{s<=t} log f_s   (padded positions repeat the last value)
@@ -155,9 +180,7 @@ fox_exit_kernel(const T *__restrict__ qt, const D *__restrict__ dg,
     int lo = qb;
     if (i < L && qb > 0) {
         const float qn = sqrtf(row_norm2(qt + ((size_t)bh * Lp + i) * kD));
-        const D *drow = dg + (((size_t)bh * nblk + qb) * kC + r) * kC;
-        float dmax = -INFINITY;
-        for (int j = 0; j <= r; ++j) dmax = fmaxf(dmax, to_float(drow[j]));
+        const float dmax = row_max(dg + (((size_t)bh * nblk + qb) * kC + r) * kC);
         const float rhs = dmax - kExitLog2;
         const float ci = c2[(size_t)bh * Lp + i];
         const float qk = 2.f * abs_scale_log2 * qn;

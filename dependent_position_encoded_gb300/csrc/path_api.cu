@@ -18,6 +18,7 @@ cudaError_t launch_fox_prepare(const float *log_f, int BH, int L, int elt_bytes,
 cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, const float *beta,
                                  const float *log_f, int BH, int L, float scale, void *ws,
                                  uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_pair_combine(int BH, int L, void *ws, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int BH, int L,
                            float scale, void *ws, uint64_t limit_ns, int force_timeout,
                            cudaStream_t stream);
@@ -90,6 +91,8 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
                         ? launch_ut_prepare_tc(q, k, w, beta, lf, B * H, L, scale, ws,
                                                kWaitLimitNs, stream)
                         : launch_ut_prepare<float>(q, k, w, beta, lf, B * H, L, scale, ws, stream);
+    // bf16: the block-pair products the two-block scan steps use
+    if (e == cudaSuccess && dtype == PATH_BF16) e = launch_pair_combine(B * H, L, ws, kWaitLimitNs, stream);
     // FoX: gate prefix sums and the scan's early-exit extents (reads K1's q~, k~ and table)
     if (e == cudaSuccess && fox)
         e = launch_fox_prepare(lf, B * H, L, elt_bytes(dtype), scale, ws, stream);

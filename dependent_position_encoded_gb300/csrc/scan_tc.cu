@@ -1,4 +1,5 @@
-// K2 (bf16): the right-to-left block scan of PaTH attention on tcgen05 tensor cores.
+// K2 (bf16): the right-to-left block scan of PaTH attention on tcgen05 tensor cores,
+// two key blocks per step.
 //
 // Technical summary "技術要約: PaTH Attention" §3 (FlashAttention-style algorithm: per-block
 // boundary-adjusted queries and keys, a right-to-left scan over key/value blocks that
@@ -6,42 +7,42 @@
 // "거리에서 경로로, PaTH Attention" §9 (the same scheme, blockwise preprocessing and
 // blockwise updates of the accumulated transform and softmax statistics).
 //
-// A tile is 128 query rows = two 64-token blocks ib0 = 2t, ib1 = 2t + 1 of one head. With
-// q~ the boundary-adjusted queries, k~ the boundary-adjusted keys and P_b = H_start(b) ...
-// H_end(b) the dense block transition (all from the preprocessing kernel), the logit of
-// row i against key j of an earlier block b is
-//     scale * k~_j^T P_{b+1} ... P_{ib-1} q~_i,
-// so a state row x_i = q~_i is scored against block ib-1, then x_i <- P_{ib-1} x_i, and so
-// on down to block 0. In row form a tile advances as X <- X P_b^T, one 128 x 64 x 64 MMA
-// per block, next to S = X K~_b^T and O += P V_b. Steps s = 0 .. ib1 visit block ib1 - s:
-//   s = 0 : block ib1; rows 64-127 take their diagonal-block logits, rows 0-63 are masked.
-//   s = 1 : block ib0; rows 0-63 take their diagonal-block logits, rows 64-127 the MMA
-//           logits of block ib0, and only rows 64-127 advance their state by P_{ib0}.
-//   s >= 2: block ib1 - s for every row.
+// A tile is 128 query rows = the pair of 64-token blocks (2t, 2t+1) of one head. With q~
+// the boundary-adjusted queries, k~ the boundary-adjusted keys and P_b the dense block
+// transition, a state row x_i starts as q~_i and the tile visits key-block pairs
+// u = t, t-1, ..., 0 (step s visits pair t - s). For an earlier pair the row scores block
+// 2u+1 as x . k~_j and block 2u as x . K^_j with K^_j = P_{2u+1}^T k~_j, then leaves as
+// Pi_u x with Pi_u = P_{2u} P_{2u+1} (the pair products come from pair_combine.cu). In
+// row form one MMA with N = 192 gives both logit blocks and the new state:
+//     [S_lo | S_hi | X'] = X [K^_{2u}; K~_{2u+1}; Pi_u]^T,
+// followed by O += P [V_{2u}; V_{2u+1}] (K = 128). Step 0 is the tile's own pair: rows of
+// block 2t take the diagonal-block table for block 2t and nothing of block 2t+1; rows of
+// block 2t+1 take the table for block 2t+1 and the MMA logits x . k~_j against block 2t
+// from X [K~_{2t}; P_{2t}]^T (N = 128), which also gives their new state P_{2t} q~_i;
+// rows of block 2t keep q~_i.
 //
-// One CTA owns a pair of tiles of one head, A = 2p and B = 2p + 1, and streams the key
-// blocks 4p+3, 4p+2, ..., 0 (PaTH-FoX: down to the lower of the two tiles' early-exit
-// extents from fox_exit.cu) once through an NS-stage TMA ring: B consumes every block,
-// A every block from 4p+1 down, so each stage is loaded once for both tiles. A stage holds
-// [K~_b; P_b; K~_b] (K~_b loaded twice) and V_b. Per tile and step, S = X K~_b^T and the
-// new state X P_b^T come from ONE MMA with N = 128: B = [K~_b; P_b] on even steps (S lands
-// in TMEM columns [0,64), the state in [64,128)) and B = [P_b; K~_b] on odd steps (state in
-// [64,128), S in [128,192)), so S is double-buffered while the state accumulator is not.
-// O += P V_b follows (N = 64, columns [192,256)). Tile B's columns are at +256.
-// Warp roles (512 threads):
-//   warps 0-3 / 4-7  softmax of tile A / B, one row per thread (= TMEM lane): load S,
-//                    release its buffer, online softmax with lazy rescaling, P tile;
+// One CTA owns the tiles A = 2p and B = 2p + 1 of one head and streams the key-block pairs
+// 2p+1, 2p, ..., 0 (PaTH-FoX: down to the lower of the two tiles' early-exit extents from
+// fox_exit.cu) once through an NS-stage TMA ring, so each stage serves both tiles. A stage
+// holds [K^_{2u}; K~_{2u+1}; Pi_u] and [V_{2u}; V_{2u+1}]; step 0's operand [K~_{2t}; P_{2t}]
+// is staged in the tile's P buffer, which the softmax overwrites only after that MMA.
+// TMEM per tile (256 columns): S [0,128) (block 2u in [0,64), 2u+1 in [64,128)), the new
+// state [128,192) (at [64,128) on step 0), O [192,256); tile B's columns at +256.
+// Warp roles (512 threads; registers moved to the softmax warpgroups with setmaxnreg):
+//   warps 0-3 / 4-7  softmax of tile A / B, one row per thread (= TMEM lane): load all
+//                    128 logits of the step at once and release S, online softmax with
+//                    lazy rescaling, P tile;
 //   warps 8-11       the state recurrence of both tiles (one per TMEM lane quadrant):
 //                    fp32 -> bf16 conversion of each new state into a swizzled A tile;
-//   warps 12 / 13    issue tile A's / B's S|state MMAs (the recurrence: needs the
-//                    converted state and a free S buffer, never the softmax of this step);
-//   warps 14 / 15    issue tile A's / B's P.V MMAs and release the stages; warp 14
-//                    also feeds the TMA ring (both duties poll, neither blocks the other);
+//   warps 12 / 13    issue tile A's / B's S|state MMAs (they need the converted state and
+//                    the released S of the previous step);
+//   warps 14 / 15    issue tile A's / B's P.V MMAs and release the stages; warp 14 also
+//                    feeds the TMA ring (both duties poll, neither blocks the other);
 //   warp 12 also owns TMEM.
-// Each issuing thread is its own in-order MMA stream: one thread issuing back to back
-// cannot keep the tensor core busy with N <= 128 instructions, four can.
-// The bf16 state tile and the P tile are single-buffered: the state is rewritten once the
-// S|state MMA that read it has completed, P once the tile's previous P.V has completed.
+// One issuing thread sustains one M = 128, K = 16 MMA per ~150 cycles whatever N is, so
+// each MMA stream has its own thread. The state tile and the P tile are single-buffered:
+// the state is rewritten once the S|state MMA that read it has completed, P once the
+// tile's previous P.V has completed.
 #include "common.cuh"
 
 namespace path {
@@ -49,25 +50,31 @@ namespace path {
 namespace {
 
 constexpr int kScanThreads = 512;
-constexpr int NS = 5;                       // TMA stages ([K~|P|K~] and V of one block each)
-constexpr uint32_t kTileBytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr uint32_t kVBytes = 64 * 128;      // 64 rows x 64 bf16
-constexpr uint32_t kKdupBytes = 64 * 128;   // second copy of K~_b after P_b
-constexpr uint32_t kStageBytes = kTileBytes + kKdupBytes + kVBytes;
-constexpr float kRescaleThreshold = 8.f;    // lazy rescale: keep the old max within 2^8
+constexpr int NS = 3;                          // TMA stages (one key-block pair each)
+constexpr uint32_t kQBytes = 128 * 128;        // 128 rows x 64 bf16
+constexpr uint32_t kRBytes = 192 * 128;        // [K^_{2u}; K~_{2u+1}; Pi_u]
+constexpr uint32_t kV2Bytes = 128 * 128;       // [V_{2u}; V_{2u+1}]
+constexpr uint32_t kStageBytes = kRBytes + kV2Bytes;
+constexpr uint32_t kPBytes = 2 * 128 * 128;    // P: 128 x 128 bf16 as two 64-column halves
+constexpr float kRescaleThreshold = 8.f;       // lazy rescale: keep the old max within 2^8
+
+// Registers per thread after the split (launch: 128 for all 512 threads).
+constexpr int kRegSoftmax = 184, kRegState = 88, kRegIssue = 56;
+constexpr int kRegTotal = 256 * kRegSoftmax + 128 * kRegState + 128 * kRegIssue;
+static_assert(kRegTotal <= 65536, "register split exceeds the register file");
 
 struct ScanSmem {
     // byte offsets from the 1024-aligned base
-    __host__ __device__ static constexpr uint32_t q_st(int t) { return (uint32_t)t * kTileBytes; }
-    __host__ __device__ static constexpr uint32_t p_buf(int t) { return (uint32_t)(2 + t) * kTileBytes; }
-    static constexpr uint32_t stage = 4 * kTileBytes;
+    __host__ __device__ static constexpr uint32_t q_st(int t) { return (uint32_t)t * kQBytes; }
+    __host__ __device__ static constexpr uint32_t p_buf(int t) { return 2 * kQBytes + (uint32_t)t * kPBytes; }
+    static constexpr uint32_t stage = 2 * kQBytes + 2 * kPBytes;
     static constexpr uint32_t bars = stage + NS * kStageBytes;
-    // barrier indices: the ring, then ten per tile (S buffers have their own), then one
+    // barrier indices: the ring, then eight per tile, then one
     static constexpr int FULL = 0, EMPTY = NS, TILE0 = 2 * NS;
-    static constexpr int QFULL = 0, BAR_SX = 1 /* 2 */, BAR_O = 3, QREADY = 4,
-                         SFREE = 5 /* 2 */, PREADY = 7, FINAL_SX = 8, FINAL_PV = 9;
-    __host__ __device__ static constexpr int per_tile(int t, int which) { return TILE0 + 10 * t + which; }
-    static constexpr int NEVER = TILE0 + 20, NBARS = TILE0 + 21;
+    static constexpr int QFULL = 0, BAR_SX = 1, BAR_O = 2, QREADY = 3, SFREE = 4, PREADY = 5,
+                         FINAL_SX = 6, FINAL_PV = 7;
+    __host__ __device__ static constexpr int per_tile(int t, int which) { return TILE0 + 8 * t + which; }
+    static constexpr int NEVER = TILE0 + 16, NBARS = TILE0 + 17;
     static constexpr uint32_t tmem_slot = bars + NBARS * 8;
     static constexpr uint32_t abort_flag = tmem_slot + 4;
     static constexpr uint32_t bytes = abort_flag + 4;
@@ -96,16 +103,41 @@ struct Waiter {
     }
 };
 
+template <int N>
+__device__ __forceinline__ void reg_alloc_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
+// 64 fp16 entries of a diagonal-block table row, in log2 units.
+__device__ __forceinline__ void load_diag_row(const __half *row, float *v) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(row);
+#pragma unroll
+    for (int q8 = 0; q8 < 8; ++q8) {
+        const uint4 c = __ldg(src + q8);
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
+            v[8 * q8 + 2 * e] = f.x;
+            v[8 * q8 + 2 * e + 1] = f.y;
+        }
+    }
+}
+
 // RAW: no bias and a positive scale, so the scale is applied inside the exponent's FFMA.
 template <bool FOX, bool RAW>
 __global__ void __launch_bounds__(kScanThreads, 1)
 path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
-                    const __grid_constant__ CUtensorMap tm_kp,
-                    const __grid_constant__ CUtensorMap tm_k64,
-                    const __grid_constant__ CUtensorMap tm_v,
-                    const __nv_bfloat16 *__restrict__ qt, const __half *__restrict__ dg,
-                    const float *__restrict__ c2, const int *__restrict__ first_blk,
-                    __nv_bfloat16 *__restrict__ out,
+                    const __grid_constant__ CUtensorMap tm_kp128,
+                    const __grid_constant__ CUtensorMap tm_kp64,
+                    const __grid_constant__ CUtensorMap tm_pr64,
+                    const __grid_constant__ CUtensorMap tm_v128,
+                    const __half *__restrict__ dg, const float *__restrict__ c2,
+                    const int *__restrict__ first_blk, __nv_bfloat16 *__restrict__ out,
                     float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
                     uint32_t *status, uint64_t limit_ns, int force_timeout) {
     extern __shared__ uint8_t smem_raw[];
@@ -114,26 +146,27 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     uint8_t *const gbase = smem_raw + (base - raw);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntile = nblk >> 1;
-    const int npair = (ntile + 1) >> 1;
-    const int pair = npair - 1 - (int)blockIdx.x;  // heaviest pairs first
+    const int ntile = nblk >> 1;                   // tiles = key-block pairs
+    const int ncta = (ntile + 1) >> 1;
+    const int pair = ncta - 1 - (int)blockIdx.x;   // heaviest tile pairs first
     const int bh = blockIdx.y;
     const bool hasB = 2 * pair + 1 < ntile;
-    const int top = hasB ? 4 * pair + 3 : 4 * pair + 1;  // first key block of the stream
-    // lowest key block each tile visits: 0, or for PaTH-FoX the early-exit extent of its
-    // two query blocks (never above the tile's own first block)
-    int fb[2] = {0, 0};
+    const int top = hasB ? 2 * pair + 1 : 2 * pair;  // first key-block pair of the stream
+    // lowest key-block pair each tile visits: 0, or for PaTH-FoX the pair holding the lower
+    // early-exit extent of its two query blocks (never above the tile's own pair)
+    int fp[2] = {0, 0};
     if (FOX) {
         for (int t = 0; t < (hasB ? 2 : 1); ++t) {
-            const int *f = first_blk + (size_t)blockIdx.y * nblk + 4 * pair + 2 * t;
-            fb[t] = min(min(__ldg(f), __ldg(f + 1)), 4 * pair + 2 * t);
+            const int tile = 2 * pair + t;
+            const int *f = first_blk + (size_t)bh * nblk + 2 * tile;
+            fp[t] = min(min(__ldg(f), __ldg(f + 1)) >> 1, tile);
         }
     }
-    const int nstream = top + 1 - (hasB ? min(fb[0], fb[1]) : fb[0]);
+    const int nstream = top + 1 - (hasB ? min(fp[0], fp[1]) : fp[0]);
     // tile t (0 = A, 1 = B): tile index, its step count, and stream position of its step 0
     auto tile_of = [&](int t) { return 2 * pair + t; };
-    auto nsteps_of = [&](int t) { return 2 * tile_of(t) + 2 - fb[t]; };
-    auto off_of = [&](int t) { return top - (2 * tile_of(t) + 1); };
+    auto nsteps_of = [&](int t) { return tile_of(t) + 1 - fp[t]; };
+    auto off_of = [&](int t) { return top - tile_of(t); };
     // whether tile t reads stream position n
     auto reads = [&](int t, int n) {
         return (t == 0 || hasB) && n >= off_of(t) && n < off_of(t) + nsteps_of(t);
@@ -154,11 +187,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         for (int t = 0; t < 2; ++t) {
             mbar_init(tbar(t, ScanSmem::QFULL), 1);
             mbar_init(tbar(t, ScanSmem::BAR_SX), 1);
-            mbar_init(tbar(t, ScanSmem::BAR_SX + 1), 1);
             mbar_init(tbar(t, ScanSmem::BAR_O), 1);
             mbar_init(tbar(t, ScanSmem::QREADY), 4);  // one arrival per warp
             mbar_init(tbar(t, ScanSmem::SFREE), 4);
-            mbar_init(tbar(t, ScanSmem::SFREE + 1), 4);
             mbar_init(tbar(t, ScanSmem::PREADY), 4);
             mbar_init(tbar(t, ScanSmem::FINAL_SX), 1);
             mbar_init(tbar(t, ScanSmem::FINAL_PV), 1);
@@ -176,42 +207,49 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // per tile: S of even steps [0,64), new state [64,128), S of odd steps [128,192), O
-    auto t_state = [&](int t) { return tmem + 256u * (uint32_t)t + 64u; };
-    auto t_s = [&](int t, int s) { return tmem + 256u * (uint32_t)t + ((s & 1) ? 128u : 0u); };
-    auto t_sxd = [&](int t, int s) { return tmem + 256u * (uint32_t)t + ((s & 1) ? 64u : 0u); };
-    auto t_o = [&](int t) { return tmem + 256u * (uint32_t)t + 192u; };
-    auto stage_kp = [&](int i) { return base + ScanSmem::stage + (uint32_t)i * kStageBytes; };
-    auto stage_v = [&](int i) { return stage_kp(i) + kTileBytes + kKdupBytes; };
+    // per tile: S [0,128), new state [128,192) ([64,128) on step 0), O [192,256)
+    auto t_base = [&](int t) { return tmem + 256u * (uint32_t)t; };
+    auto t_o = [&](int t) { return t_base(t) + 192u; };
+    auto stage_r = [&](int i) { return base + ScanSmem::stage + (uint32_t)i * kStageBytes; };
+    auto stage_v = [&](int i) { return stage_r(i) + kRBytes; };
 
-    if (warp >= 12 && warp <= 13) {
+    // Registers move to the softmax warpgroups (a step's 128 logits per thread); each
+    // warpgroup executes its setmaxnreg once, at the head of its role.
+    if (warp >= 12) {
+      reg_alloc_dec<kRegIssue>();
+      if (warp <= 13) {
         // ------------------------------------------------------------ S|state issuers
         const int t = warp - 12;
         if (lane == 0 && (t == 0 || hasB)) {
-            constexpr uint32_t ID_SX = idesc_bf16(128, 128, false);
+            constexpr uint32_t ID_DIAG = idesc_bf16(128, 128, false);
+            constexpr uint32_t ID_SX = idesc_bf16(128, 192, false);
             const int nst = nsteps_of(t), off = off_of(t);
             bool ok = true;
             if (force_timeout && t == 0) ok = wait(bar(ScanSmem::NEVER), 0);  // nothing arrives here
-            for (int s = 1; ok && s < nst; ++s) {
-                const int n = s + off, st = n % NS;
-                if (!(ok = wait(bar(ScanSmem::FULL + st), (n / NS) & 1))) break;
-                // the state of step s: q~ (step 1) or the converted new state of step s - 1
-                if (s == 1) {
+            const uint64_t a_q = sdesc_sw128(base + ScanSmem::q_st(t), 16, 1024);
+            for (int s = 0; ok && s < nst; ++s) {
+                if (s == 0) {
+                    // q~ and [K~_{2t}; P_{2t}] of the tile's own pair
                     if (!(ok = wait(tbar(t, ScanSmem::QFULL), 0))) break;
-                } else if (!(ok = wait(tbar(t, ScanSmem::QREADY), (s - 2) & 1))) {
-                    break;
-                }
-                // S buffer s & 1 was last read by the softmax of step s - 2
-                if (s >= 3 && !(ok = wait(tbar(t, ScanSmem::SFREE + (s & 1)), ((s - 3) >> 1) & 1)))
-                    break;
-                tc_fence_after();
-                const uint64_t a_q = sdesc_sw128(base + ScanSmem::q_st(t), 16, 1024);
-                const uint64_t b_kp =
-                    sdesc_sw128(stage_kp(st) + ((s & 1) ? 64u * 128u : 0u), 16, 1024);
+                    tc_fence_after();
+                    const uint64_t b = sdesc_sw128(base + ScanSmem::p_buf(t), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(t_sxd(t, s), a_q + 2 * kk, b_kp + 2 * kk, ID_SX, kk > 0);
-                umma_commit(tbar(t, ScanSmem::BAR_SX + (s & 1)));
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(t_base(t), a_q + 2 * kk, b + 2 * kk, ID_DIAG, kk > 0);
+                } else {
+                    const int n = s + off, st = n % NS;
+                    if (!(ok = wait(bar(ScanSmem::FULL + st), (n / NS) & 1))) break;
+                    // the state of step s, converted after the MMA of step s - 1
+                    if (!(ok = wait(tbar(t, ScanSmem::QREADY), (s - 1) & 1))) break;
+                    // S of step s - 1 has been read by the softmax
+                    if (!(ok = wait(tbar(t, ScanSmem::SFREE), (s - 1) & 1))) break;
+                    tc_fence_after();
+                    const uint64_t b = sdesc_sw128(stage_r(st), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(t_base(t), a_q + 2 * kk, b + 2 * kk, ID_SX, kk > 0);
+                }
+                umma_commit(tbar(t, ScanSmem::BAR_SX));
             }
             umma_commit(tbar(t, ScanSmem::FINAL_SX));
             const uint64_t t0 = cycles_now();
@@ -219,9 +257,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                    cycles_now() - t0 < ns_to_cycles(limit_ns)) {
             }
         }
-    } else if (warp >= 14 && warp <= 15) {
+      } else {
         // ------------------------------------------------------------ P.V issuers (+ TMA)
-        // Tile A's thread also feeds the TMA ring; both duties poll without blocking.
+        // Tile A's thread also feeds the TMA ring; both duties poll, neither blocks the other.
         const int t = warp - 14;
         const bool producer = (t == 0);
         if (lane == 0 && (t == 0 || hasB)) {
@@ -229,15 +267,20 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             const int nst = nsteps_of(t), off = off_of(t);
             if (producer) {
                 tma_prefetch_desc(&tm_qt);
-                tma_prefetch_desc(&tm_kp);
-                tma_prefetch_desc(&tm_k64);
-                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_kp128);
+                tma_prefetch_desc(&tm_kp64);
+                tma_prefetch_desc(&tm_pr64);
+                tma_prefetch_desc(&tm_v128);
                 for (int tt = 0; tt < (hasB ? 2 : 1); ++tt) {
-                    mbar_arrive_expect_tx(tbar(tt, ScanSmem::QFULL), kTileBytes);
+                    const int tile = tile_of(tt);
+                    mbar_arrive_expect_tx(tbar(tt, ScanSmem::QFULL), 2 * kQBytes);
                     tma_load_3d(base + ScanSmem::q_st(tt), &tm_qt, tbar(tt, ScanSmem::QFULL), 0,
-                                tile_of(tt) * kTile, bh);
+                                tile * kTile, bh);
+                    tma_load_3d(base + ScanSmem::p_buf(tt), &tm_kp128, tbar(tt, ScanSmem::QFULL), 0,
+                                2 * tile * 2 * kC, bh);
                 }
             }
+            const uint64_t a_p = sdesc_sw128(base + ScanSmem::p_buf(t), 16, 1024);
             int n_fill = producer ? 0 : nstream;  // next stream position to load
             int s = 0;                            // next P.V step
             bool ok = true;
@@ -247,29 +290,32 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (n_fill < nstream &&
                     (n_fill < NS ||
                      mbar_test_wait(bar(ScanSmem::EMPTY + n_fill % NS), ((n_fill / NS) - 1) & 1))) {
-                    const int st = n_fill % NS, b = top - n_fill;
-                    if (n_fill == 0) {  // the top tile's own diagonal block: values only
-                        mbar_arrive_expect_tx(bar(ScanSmem::FULL + st), kVBytes);
+                    const int st = n_fill % NS, u = top - n_fill;
+                    const uint32_t full = bar(ScanSmem::FULL + st);
+                    if (n_fill == 0) {  // the top tile's own pair: values only
+                        mbar_arrive_expect_tx(full, kV2Bytes);
                     } else {
-                        mbar_arrive_expect_tx(bar(ScanSmem::FULL + st), kStageBytes);
-                        tma_load_3d(stage_kp(st), &tm_kp, bar(ScanSmem::FULL + st), 0, b * 2 * kC, bh);
-                        tma_load_3d(stage_kp(st) + kTileBytes, &tm_k64, bar(ScanSmem::FULL + st), 0,
-                                    b * 2 * kC, bh);
+                        mbar_arrive_expect_tx(full, kStageBytes);
+                        tma_load_3d(stage_r(st), &tm_pr64, full, 0, u * 2 * kC, bh);
+                        tma_load_3d(stage_r(st) + 64 * 128, &tm_kp64, full, 0,
+                                    (2 * u + 1) * 2 * kC, bh);
+                        tma_load_3d(stage_r(st) + 128 * 128, &tm_pr64, full, 0, u * 2 * kC + kC, bh);
                     }
-                    tma_load_3d(stage_v(st), &tm_v, bar(ScanSmem::FULL + st), 0, b * kC, bh);
+                    tma_load_3d(stage_v(st), &tm_v128, full, 0, u * kTile, bh);
                     ++n_fill;
                     progress = true;
                 }
                 if (s < nst) {
                     const int n = s + off, st = n % NS;
+                    // steps >= 1 follow an S|state MMA that waited for this stage
                     const bool in_ready = (s > 0) || mbar_test_wait(bar(ScanSmem::FULL + st), (n / NS) & 1);
                     if (in_ready && mbar_test_wait(tbar(t, ScanSmem::PREADY), s & 1)) {
                         tc_fence_after();
-                        const uint64_t a_p = sdesc_sw128(base + ScanSmem::p_buf(t), 16, 1024);
                         const uint64_t b_v = sdesc_sw128(stage_v(st), 1024, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16(t_o(t), a_p + 2 * kk, b_v + 128 * kk, ID_PV, (s > 0 || kk > 0));
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_bf16(t_o(t), a_p + (uint64_t)((kk >> 2) * (kQBytes >> 4) + 2 * (kk & 3)),
+                                      b_v + 128 * kk, ID_PV, (s > 0 || kk > 0));
                         umma_commit(tbar(t, ScanSmem::BAR_O));
                         // this step's S|state MMA completed before its softmax finished, so
                         // this commit covers every read of the stage by tile t; two arrivals
@@ -312,47 +358,43 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                    cycles_now() - t0 < ns_to_cycles(limit_ns)) {
             }
         }
+      }
     } else if (warp >= 8) {
+        reg_alloc_dec<kRegState>();
         // ------------------------------------------------------------ state warps
         const int quad = warp - 8;
         const int r = quad * 32 + lane;          // row of both tiles = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const size_t head = (size_t)bh;
         bool ok = true;
         auto wwait = [&](uint32_t b_, uint32_t par) {
             return __all_sync(0xffffffffu, wait(b_, par)) != 0;
         };
         const int smax = hasB ? max(nsteps_of(0), nsteps_of(1)) : nsteps_of(0);
-        for (int s = 1; s < smax && ok; ++s) {
+        for (int s = 0; s < smax - 1 && ok; ++s) {
             for (int t = hasB ? 1 : 0; t >= 0; --t) {
                 if (s >= nsteps_of(t) - 1) continue;  // the last step needs no new state
-                if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX + (s & 1)), ((s - 1) >> 1) & 1))) break;
+                if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX), s & 1))) break;
                 tc_fence_after();
                 // the state of step s + 1 replaces that of step s, whose only reader (the
-                // S|state MMA of step s) has completed
-                uint8_t *row = gbase + ScanSmem::q_st(t);
-                if (s >= 2 || quad >= 2) {
-                    uint32_t qa[32], qb[32];
-                    tmem_ld32(t_state(t) + lane_base, qa);
-                    tmem_ld32(t_state(t) + 32 + lane_base, qb);
-                    tmem_ld_wait();
+                // S|state MMA of step s) has completed; rows of block 2t keep q~ after step 0
+                if (s >= 1 || quad >= 2) {
+                    uint8_t *row = gbase + ScanSmem::q_st(t);
+                    const uint32_t src = t_base(t) + (s == 0 ? 64u : 128u) + lane_base;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t *src = (c < 4) ? &qa[8 * c] : &qb[8 * (c - 4)];
-                        uint4 u;
-                        u.x = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
-                        u.y = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
-                        u.z = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
-                        u.w = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
-                        *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = u;
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t x[32];
+                        tmem_ld32(src + 32 * h, x);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t *e = &x[8 * c];
+                            *reinterpret_cast<uint4 *>(row + sw128_offset(r, 4 * h + c)) =
+                                make_uint4(pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1])),
+                                           pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3])),
+                                           pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5])),
+                                           pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7])));
+                        }
                     }
-                } else {
-                    // rows of block ib0 keep q~ through step 1: copy it from the workspace
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        qt + (head * Lp + (size_t)tile_of(t) * kTile + r) * kD);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(row + sw128_offset(r, c)) = __ldg(src + c);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -360,13 +402,15 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
         }
         tc_fence_before();
-    } else if (warp < 4 || hasB) {
+    } else {
+      reg_alloc_inc<kRegSoftmax>();
+      if (warp < 4 || hasB) {
         // ------------------------------------------------------------ softmax warps
         const int t = warp >> 2;                 // 0 = tile A, 1 = tile B
         const int r = threadIdx.x - 128 * t;     // tile row = TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int q = warp & 3;                  // lane quadrant
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int tile = tile_of(t);
-        const int ib0 = 2 * tile, ib1 = 2 * tile + 1;
         const int nsteps = nsteps_of(t);
         const int i = tile * kTile + r;          // query index
         const size_t head = (size_t)bh;
@@ -377,64 +421,39 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         auto wwait = [&](uint32_t b_, uint32_t par) {
             return __all_sync(0xffffffffu, wait(b_, par)) != 0;
         };
-        const uint32_t T_O = t_o(t);
+        const uint32_t T_S = t_base(t) + lane_base;
+        const uint32_t T_O = t_o(t) + lane_base;
 
         for (int s = 0; s < nsteps && ok; ++s) {
-            const int b = ib1 - s;
-            // logits of this row come from the diagonal-block table (step 0, and step 1 for
-            // rows 0-63) or from S in TMEM; they are read twice, in 32-column chunks (row
-            // max, then exponentials), which keeps the live register set small
-            bool from_diag = false;
-            int diag_blk = 0, diag_row = 0;
+            const int u = tile - s;              // key-block pair of this step
+            if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX), s & 1))) break;
+            tc_fence_after();
+            // the step's 128 logits: column c is key 128 u + c (block 2u, then 2u+1)
+            float v[128];
+            bool raw_s = RAW;
             if (s == 0) {
-                from_diag = true;
-                diag_blk = ib1;
-                diag_row = r - 64;
-            } else {
-                if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX + (s & 1)), ((s - 1) >> 1) & 1))) break;
-                tc_fence_after();
-                if (s == 1 && (warp & 3) < 2) {
-                    from_diag = true;
-                    diag_blk = ib0;
-                    diag_row = r;
-                }
-            }
-            const uint32_t ts = t_s(t, s) + lane_base;
-            const __half *drow = dg + (((head * nblk + diag_blk) * kC) + (diag_row < 0 ? 0 : diag_row)) * kC;
-            const bool raw_s = RAW && !from_diag;
-            // 32 logits of chunk h (log2 units, or raw scores when raw_s)
-            auto load_chunk = [&](int h, float (&v)[32]) {
-                if (from_diag) {
-                    if (diag_row >= 0) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(drow + 32 * h);
+                // own pair: table rows for the diagonal blocks, MMA logits of block 2t for the
+                // rows of block 2t+1, block 2t+1 masked for the rows of block 2t; all in log2
+                // units
+                raw_s = false;
+                if (q < 2) {
+                    load_diag_row(dg + ((head * nblk + 2 * tile) * kC + r) * kC, v);
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            const uint4 c = __ldg(src + q8);
-                            const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f =
-                                    __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
-                                v[8 * q8 + 2 * e] = f.x;
-                                v[8 * q8 + 2 * e + 1] = f.y;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
-                    }
+                    for (int j = 64; j < 128; ++j) v[j] = -INFINITY;
                 } else {
-                    uint32_t u[32];
-                    tmem_ld32(ts + 32 * h, u);
+                    uint32_t a[32], b[32];
+                    tmem_ld32(T_S, a);
+                    tmem_ld32(T_S + 32, b);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = RAW ? __uint_as_float(u[j]) : __uint_as_float(u[j]) * scale_log2;
+                    for (int j = 0; j < 32; ++j) {
+                        v[j] = __uint_as_float(a[j]) * scale_log2;
+                        v[32 + j] = __uint_as_float(b[j]) * scale_log2;
+                    }
                     if (FOX) {
-                        const float4 *cj =
-                            reinterpret_cast<const float4 *>(c2 + head * Lp + b * kC + 32 * h);
+                        const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
+                        for (int q4 = 0; q4 < 16; ++q4) {
                             const float4 c = __ldg(cj + q4);
                             v[4 * q4 + 0] += c2_i - c.x;
                             v[4 * q4 + 1] += c2_i - c.y;
@@ -442,83 +461,95 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                             v[4 * q4 + 3] += c2_i - c.w;
                         }
                     }
+                    load_diag_row(dg + ((head * nblk + 2 * tile + 1) * kC + (r - 64)) * kC, v + 64);
                 }
-            };
-
-            // ---- one pass over two 32-column chunks: online max with lazy rescaling (a
-            // chunk raises the running max only if it exceeds it by more than 2^8; then the
-            // row sum, O and the chunk already packed are rescaled), exponentials, row sum
-            float alpha = 1.f;   // accumulated rescale factor of O for this step
-            bool rescale = false;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[32];
+            } else {
+                uint32_t a[32], b[32], c[32], d[32];
+                tmem_ld32(T_S, a);
+                tmem_ld32(T_S + 32, b);
+                tmem_ld32(T_S + 64, c);
+                tmem_ld32(T_S + 96, d);
+                tmem_ld_wait();
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v[32];
-                load_chunk(h, v);
-                float m4[4] = {v[0], v[1], v[2], v[3]};
-#pragma unroll
-                for (int j = 4; j < 32; j += 4) {
-                    m4[0] = fmaxf(m4[0], v[j]);
-                    m4[1] = fmaxf(m4[1], v[j + 1]);
-                    m4[2] = fmaxf(m4[2], v[j + 2]);
-                    m4[3] = fmaxf(m4[3], v[j + 3]);
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = RAW ? __uint_as_float(a[j]) : __uint_as_float(a[j]) * scale_log2;
+                    v[32 + j] = RAW ? __uint_as_float(b[j]) : __uint_as_float(b[j]) * scale_log2;
+                    v[64 + j] = RAW ? __uint_as_float(c[j]) : __uint_as_float(c[j]) * scale_log2;
+                    v[96 + j] = RAW ? __uint_as_float(d[j]) : __uint_as_float(d[j]) * scale_log2;
                 }
-                float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                if (raw_s) mx *= scale_log2;
-                if (mx > m_run + kRescaleThreshold) {
-                    if (m_run != -INFINITY) {
-                        const float a = ex2_approx(m_run - mx);
-                        alpha *= a;
-                        rescale = true;
-                        l_run *= a;
-                        ls[0] *= a; ls[1] *= a; ls[2] *= a; ls[3] *= a;
-                        if (h == 1) {
+                if (FOX) {
+                    const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float2 f = unpack_bf16x2(pk[j]);
-                                pk[j] = pack_bf16x2(f.x * a, f.y * a);
-                            }
-                        }
+                    for (int q4 = 0; q4 < 32; ++q4) {
+                        const float4 cc = __ldg(cj + q4);
+                        v[4 * q4 + 0] += c2_i - cc.x;
+                        v[4 * q4 + 1] += c2_i - cc.y;
+                        v[4 * q4 + 2] += c2_i - cc.z;
+                        v[4 * q4 + 3] += c2_i - cc.w;
                     }
-                    m_run = mx;
-                }
-                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                const float cs = raw_s ? scale_log2 : 1.f;
-                const float neg_m = -m_use;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float p0 = ex2_approx(fmaf(v[2 * j], cs, neg_m));
-                    const float p1 = ex2_approx(fmaf(v[2 * j + 1], cs, neg_m));
-                    ls[(2 * j) & 3] += p0;
-                    ls[(2 * j + 1) & 3] += p1;
-                    pk[16 * h + j] = pack_bf16x2(p0, p1);
                 }
             }
+            // S is in registers: its TMEM columns may be rewritten by the next step's MMA
+            tc_fence_before();
+            if (s + 1 < nsteps) mbar_arrive_warp(tbar(t, ScanSmem::SFREE));
+
+            // ---- online softmax with lazy rescaling: the running max is raised only when
+            // the step's max exceeds it by more than 2^8; then the row sum and O are rescaled
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = v[e];
+#pragma unroll
+            for (int j = 8; j < 128; j += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], v[j + e]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            if (raw_s) mx *= scale_log2;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m_run + kRescaleThreshold) {
+                if (m_run != -INFINITY) {
+                    alpha = ex2_approx(m_run - mx);
+                    rescale = true;
+                    l_run *= alpha;
+                }
+                m_run = mx;
+            }
+            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+            const float cs = raw_s ? scale_log2 : 1.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float p0 = ex2_approx(fmaf(v[2 * j], cs, neg_m));
+                const float p1 = ex2_approx(fmaf(v[2 * j + 1], cs, neg_m));
+                ls[(2 * j) & 3] += p0;
+                ls[(2 * j + 1) & 3] += p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // the P tile was last read by this tile's P.V MMA of step s - 1, which also has
-            // to be complete before O is rescaled
+            // the P tile was last read by this tile's P.V MMA of step s - 1 (on step 0 it held
+            // [K~_{2t}; P_{2t}], read by the MMA that produced this step's S); that P.V also
+            // has to be complete before O is rescaled
             if (s >= 1 && !(ok = wwait(tbar(t, ScanSmem::BAR_O), (s - 1) & 1))) break;
             uint8_t *prow = gbase + ScanSmem::p_buf(t);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(prow + sw128_offset(r, c)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            if (s >= 1) {
-                // S has been read for the last time: its buffer may be rewritten
-                tc_fence_before();
-                mbar_arrive_warp(tbar(t, ScanSmem::SFREE + (s & 1)));
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(prow + h * kQBytes + sw128_offset(r, c)) =
+                        make_uint4(pk[32 * h + 4 * c], pk[32 * h + 4 * c + 1],
+                                   pk[32 * h + 4 * c + 2], pk[32 * h + 4 * c + 3]);
             if (s >= 1 && __any_sync(0xffffffffu, rescale)) {
                 tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t oa[32];
-                    tmem_ld32(T_O + lane_base + 32 * h, oa);
+                    tmem_ld32(T_O + 32 * h, oa);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) oa[j] = __float_as_uint(__uint_as_float(oa[j]) * alpha);
-                    tmem_st32(T_O + lane_base + 32 * h, oa);
+                    tmem_st32(T_O + 32 * h, oa);
                 }
                 tmem_st_wait();
             }
@@ -532,8 +563,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         if (ok) {
             tc_fence_after();
             uint32_t oa[32], ob[32];
-            tmem_ld32(T_O + lane_base, oa);
-            tmem_ld32(T_O + lane_base + 32, ob);
+            tmem_ld32(T_O, oa);
+            tmem_ld32(T_O + 32, ob);
             tmem_ld_wait();
             if (i < L) {
                 const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -541,17 +572,18 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint32_t *src = (c < 4) ? &oa[8 * c] : &ob[8 * (c - 4)];
-                    uint4 u;
-                    u.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
-                    u.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
-                    u.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
-                    u.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
-                    dst[c] = u;
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+                    dst[c] = w;
                 }
                 if (lse != nullptr) lse[head * L + i] = (m_run + log2f(l_run)) * 0.69314718055994531f;
             }
         }
         tc_fence_before();
+      }
     }
 
     __syncthreads();
@@ -563,63 +595,36 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 
 }  // namespace
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiled get_encode_tiled() {
-    static EncodeTiled fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    }
-    return fn;
-}
-
-// 3-D bf16 map over (heads, rows, 64 columns) with a (1, box_rows, 64) box, 128-byte swizzle.
-static bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads, int box_rows) {
-    EncodeTiled enc = get_encode_tiled();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)rows, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)rows * kD * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Returns cudaErrorInvalidValue if the tensor maps cannot be encoded.
+// Returns cudaErrorInvalidValue if the tensor maps cannot be encoded, and
+// cudaErrorInvalidConfiguration if the compiled kernel was given fewer registers than the
+// warpgroup split redistributes (its setmaxnreg.inc could then never be satisfied).
 cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int BH, int L,
                            float scale, void *ws, uint64_t limit_ns, int force_timeout,
                            cudaStream_t stream) {
     const FwdLayout lay = fwd_layout(1, BH, L, 2, fox);
     char *basep = static_cast<char *>(ws);
-    CUtensorMap tm_qt, tm_kp, tm_v;
-    CUtensorMap tm_k64;
-    if (!make_map(&tm_qt, basep + lay.off_qt, lay.Lp, BH, kTile) ||
-        !make_map(&tm_kp, basep + lay.off_kp, lay.nblk * 2 * kC, BH, kTile) ||
-        !make_map(&tm_k64, basep + lay.off_kp, lay.nblk * 2 * kC, BH, kC) ||
-        !make_map(&tm_v, v, L, BH, kC))
+    CUtensorMap tm_qt, tm_kp128, tm_kp64, tm_pr64, tm_v128;
+    const int nrows_kp = lay.nblk * 2 * kC, nrows_pr = (lay.nblk / 2) * 2 * kC;
+    if (!make_map_bf16(&tm_qt, basep + lay.off_qt, lay.Lp, BH, kTile) ||
+        !make_map_bf16(&tm_kp128, basep + lay.off_kp, nrows_kp, BH, 2 * kC) ||
+        !make_map_bf16(&tm_kp64, basep + lay.off_kp, nrows_kp, BH, kC) ||
+        !make_map_bf16(&tm_pr64, basep + lay.off_pr, nrows_pr, BH, kC) ||
+        !make_map_bf16(&tm_v128, v, L, BH, kTile))
         return cudaErrorInvalidValue;
     auto kern = fox ? path_scan_tc_kernel<true, false>
                     : (scale > 0.f ? path_scan_tc_kernel<false, true>
                                    : path_scan_tc_kernel<false, false>);
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kScanSmemBytes);
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs * kScanThreads < kRegTotal) return cudaErrorInvalidConfiguration;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kScanSmemBytes);
     if (err != cudaSuccess) return err;
     const int ntile = lay.nblk / 2;
     dim3 grid((ntile + 1) / 2, BH);
     kern<<<grid, kScanThreads, kScanSmemBytes, stream>>>(
-        tm_qt, tm_kp, tm_k64, tm_v, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
+        tm_qt, tm_kp128, tm_kp64, tm_pr64, tm_v128,
         reinterpret_cast<const __half *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
         fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,

@@ -41,9 +41,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # header 256 B; bf16 B1 H1 L128: qt 128*64*2, kp 2*128*64*2, dg 2*64*64*2 (fp16)
+    # header 256 B; bf16 B1 H1 L128: qt 128*64*2, kp 2*128*64*2, dg 2*64*64*2 (fp16), and
+    # the block-pair products 1*128*64*2
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) == \
-        256 + 128 * 64 * 2 + 2 * 128 * 64 * 2 + 2 * 64 * 64 * 2
+        256 + 128 * 64 * 2 + 2 * 128 * 64 * 2 + 2 * 64 * 64 * 2 + 128 * 64 * 2
     # fp32: every region fp32
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.F32) == \
         256 + 128 * 64 * 4 + 2 * 128 * 64 * 4 + 2 * 64 * 64 * 4
