@@ -23,9 +23,11 @@
 //
 // One CTA owns the tiles A = 2p and B = 2p + 1 of one head and streams the key-block pairs
 // 2p+1, 2p, ..., 0 (PaTH-FoX: down to the lower of the two tiles' early-exit extents from
-// fox_exit.cu) once through an NS-stage TMA ring, so each stage serves both tiles. A stage
-// holds [K^_{2u}; K~_{2u+1}; Pi_u] and [V_{2u}; V_{2u+1}]; step 0's operand [K~_{2t}; P_{2t}]
-// is staged in the tile's P buffer, which the softmax overwrites only after that MMA.
+// fox_exit.cu) once, so each pair serves both tiles, through two TMA rings: one of
+// [K^_{2u}; K~_{2u+1}; Pi_u] (released as soon as both S|state MMAs on it have completed)
+// and one of [V_{2u}; V_{2u+1}] (released after the P.V MMAs, which run a softmax later).
+// Step 0's operand [K~_{2t}; P_{2t}] is staged in the tile's P buffer, which the softmax
+// overwrites only after that MMA.
 // TMEM per tile (256 columns): S [0,128) (block 2u in [0,64), 2u+1 in [64,128)), the new
 // state [128,192) (at [64,128) on step 0), O [192,256); tile B's columns at +256.
 // Warp roles (512 threads; registers moved to the softmax warpgroups with setmaxnreg):
@@ -50,11 +52,11 @@ namespace path {
 namespace {
 
 constexpr int kScanThreads = 512;
-constexpr int NS = 3;                          // TMA stages (one key-block pair each)
+constexpr int NR = 3;                          // TMA stages of [K^; K~; Pi] (S|state operand)
+constexpr int NV = 3;                          // TMA stages of [V; V] (P.V operand)
 constexpr uint32_t kQBytes = 128 * 128;        // 128 rows x 64 bf16
 constexpr uint32_t kRBytes = 192 * 128;        // [K^_{2u}; K~_{2u+1}; Pi_u]
 constexpr uint32_t kV2Bytes = 128 * 128;       // [V_{2u}; V_{2u+1}]
-constexpr uint32_t kStageBytes = kRBytes + kV2Bytes;
 constexpr uint32_t kPBytes = 2 * 128 * 128;    // P: 128 x 128 bf16 as two 64-column halves
 constexpr float kRescaleThreshold = 8.f;       // lazy rescale: keep the old max within 2^8
 
@@ -67,10 +69,12 @@ struct ScanSmem {
     // byte offsets from the 1024-aligned base
     __host__ __device__ static constexpr uint32_t q_st(int t) { return (uint32_t)t * kQBytes; }
     __host__ __device__ static constexpr uint32_t p_buf(int t) { return 2 * kQBytes + (uint32_t)t * kPBytes; }
-    static constexpr uint32_t stage = 2 * kQBytes + 2 * kPBytes;
-    static constexpr uint32_t bars = stage + NS * kStageBytes;
-    // barrier indices: the ring, then eight per tile, then one
-    static constexpr int FULL = 0, EMPTY = NS, TILE0 = 2 * NS;
+    static constexpr uint32_t stage_r = 2 * kQBytes + 2 * kPBytes;
+    static constexpr uint32_t stage_v = stage_r + NR * kRBytes;
+    static constexpr uint32_t bars = stage_v + NV * kV2Bytes;
+    // barrier indices: the two rings, then eight per tile, then one
+    static constexpr int FULL_R = 0, EMPTY_R = NR, FULL_V = 2 * NR, EMPTY_V = 2 * NR + NV,
+                         TILE0 = 2 * NR + 2 * NV;
     static constexpr int QFULL = 0, BAR_SX = 1, BAR_O = 2, QREADY = 3, SFREE = 4, PREADY = 5,
                          FINAL_SX = 6, FINAL_PV = 7;
     __host__ __device__ static constexpr int per_tile(int t, int which) { return TILE0 + 8 * t + which; }
@@ -167,10 +171,13 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     auto tile_of = [&](int t) { return 2 * pair + t; };
     auto nsteps_of = [&](int t) { return tile_of(t) + 1 - fp[t]; };
     auto off_of = [&](int t) { return top - tile_of(t); };
-    // whether tile t reads stream position n
+    // whether tile t reads stream position n (its values), and the S|state operand of
+    // position n (every step but the tile's first); the operand ring skips position 0,
+    // which only the top tile's own pair occupies
     auto reads = [&](int t, int n) {
         return (t == 0 || hasB) && n >= off_of(t) && n < off_of(t) + nsteps_of(t);
     };
+    auto reads_r = [&](int t, int n) { return reads(t, n) && n > off_of(t); };
 
     auto bar = [&](int i) { return base + ScanSmem::bars + 8u * (uint32_t)i; };
     auto tbar = [&](int t, int which) { return bar(ScanSmem::per_tile(t, which)); };
@@ -180,9 +187,13 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const Waiter wait{abort_flag, status, limit_ns};
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(bar(ScanSmem::FULL + i), 1);
-            mbar_init(bar(ScanSmem::EMPTY + i), 2);  // two arrivals per use (see issuers)
+        for (int i = 0; i < NR; ++i) {
+            mbar_init(bar(ScanSmem::FULL_R + i), 1);
+            mbar_init(bar(ScanSmem::EMPTY_R + i), 2);  // two arrivals per use (see issuers)
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(bar(ScanSmem::FULL_V + i), 1);
+            mbar_init(bar(ScanSmem::EMPTY_V + i), 2);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(tbar(t, ScanSmem::QFULL), 1);
@@ -210,8 +221,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     // per tile: S [0,128), new state [128,192) ([64,128) on step 0), O [192,256)
     auto t_base = [&](int t) { return tmem + 256u * (uint32_t)t; };
     auto t_o = [&](int t) { return t_base(t) + 192u; };
-    auto stage_r = [&](int i) { return base + ScanSmem::stage + (uint32_t)i * kStageBytes; };
-    auto stage_v = [&](int i) { return stage_r(i) + kRBytes; };
+    auto stage_r = [&](int i) { return base + ScanSmem::stage_r + (uint32_t)i * kRBytes; };
+    auto stage_v = [&](int i) { return base + ScanSmem::stage_v + (uint32_t)i * kV2Bytes; };
 
     // Registers move to the softmax warpgroups (a step's 128 logits per thread); each
     // warpgroup executes its setmaxnreg once, at the head of its role.
@@ -237,8 +248,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(t_base(t), a_q + 2 * kk, b + 2 * kk, ID_DIAG, kk > 0);
                 } else {
-                    const int n = s + off, st = n % NS;
-                    if (!(ok = wait(bar(ScanSmem::FULL + st), (n / NS) & 1))) break;
+                    const int n = s + off, m = n - 1, st = m % NR;  // operand ring index m
+                    if (!(ok = wait(bar(ScanSmem::FULL_R + st), (m / NR) & 1))) break;
                     // the state of step s, converted after the MMA of step s - 1
                     if (!(ok = wait(tbar(t, ScanSmem::QREADY), (s - 1) & 1))) break;
                     // S of step s - 1 has been read by the softmax
@@ -248,6 +259,10 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(t_base(t), a_q + 2 * kk, b + 2 * kk, ID_SX, kk > 0);
+                    // the operand stage is free once both tiles' MMAs on it have completed
+                    // (a stage read by one tile only gets both arrivals from that tile)
+                    umma_commit(bar(ScanSmem::EMPTY_R + st));
+                    if (!reads_r(1 - t, n)) umma_commit(bar(ScanSmem::EMPTY_R + st));
                 }
                 umma_commit(tbar(t, ScanSmem::BAR_SX));
             }
@@ -281,34 +296,40 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 }
             }
             const uint64_t a_p = sdesc_sw128(base + ScanSmem::p_buf(t), 16, 1024);
-            int n_fill = producer ? 0 : nstream;  // next stream position to load
+            // next stream position to load into the value ring / operand ring index (the
+            // operand of position n goes to index n - 1)
+            const int nr_total = nstream - 1;
+            int nv_fill = producer ? 0 : nstream, nr_fill = producer ? 0 : nr_total;
             int s = 0;                            // next P.V step
             bool ok = true;
             uint64_t t_last = cycles_now();
-            while (ok && (s < nst || n_fill < nstream)) {
+            while (ok && (s < nst || nv_fill < nstream || nr_fill < nr_total)) {
                 bool progress = false;
-                if (n_fill < nstream &&
-                    (n_fill < NS ||
-                     mbar_test_wait(bar(ScanSmem::EMPTY + n_fill % NS), ((n_fill / NS) - 1) & 1))) {
-                    const int st = n_fill % NS, u = top - n_fill;
-                    const uint32_t full = bar(ScanSmem::FULL + st);
-                    if (n_fill == 0) {  // the top tile's own pair: values only
-                        mbar_arrive_expect_tx(full, kV2Bytes);
-                    } else {
-                        mbar_arrive_expect_tx(full, kStageBytes);
-                        tma_load_3d(stage_r(st), &tm_pr64, full, 0, u * 2 * kC, bh);
-                        tma_load_3d(stage_r(st) + 64 * 128, &tm_kp64, full, 0,
-                                    (2 * u + 1) * 2 * kC, bh);
-                        tma_load_3d(stage_r(st) + 128 * 128, &tm_pr64, full, 0, u * 2 * kC + kC, bh);
-                    }
+                if (nr_fill < nr_total &&
+                    (nr_fill < NR ||
+                     mbar_test_wait(bar(ScanSmem::EMPTY_R + nr_fill % NR), ((nr_fill / NR) - 1) & 1))) {
+                    const int st = nr_fill % NR, u = top - (nr_fill + 1);
+                    const uint32_t full = bar(ScanSmem::FULL_R + st);
+                    mbar_arrive_expect_tx(full, kRBytes);
+                    tma_load_3d(stage_r(st), &tm_pr64, full, 0, u * 2 * kC, bh);
+                    tma_load_3d(stage_r(st) + 64 * 128, &tm_kp64, full, 0, (2 * u + 1) * 2 * kC, bh);
+                    tma_load_3d(stage_r(st) + 128 * 128, &tm_pr64, full, 0, u * 2 * kC + kC, bh);
+                    ++nr_fill;
+                    progress = true;
+                }
+                if (nv_fill < nstream &&
+                    (nv_fill < NV ||
+                     mbar_test_wait(bar(ScanSmem::EMPTY_V + nv_fill % NV), ((nv_fill / NV) - 1) & 1))) {
+                    const int st = nv_fill % NV, u = top - nv_fill;
+                    const uint32_t full = bar(ScanSmem::FULL_V + st);
+                    mbar_arrive_expect_tx(full, kV2Bytes);
                     tma_load_3d(stage_v(st), &tm_v128, full, 0, u * kTile, bh);
-                    ++n_fill;
+                    ++nv_fill;
                     progress = true;
                 }
                 if (s < nst) {
-                    const int n = s + off, st = n % NS;
-                    // steps >= 1 follow an S|state MMA that waited for this stage
-                    const bool in_ready = (s > 0) || mbar_test_wait(bar(ScanSmem::FULL + st), (n / NS) & 1);
+                    const int n = s + off, st = n % NV;
+                    const bool in_ready = mbar_test_wait(bar(ScanSmem::FULL_V + st), (n / NV) & 1);
                     if (in_ready && mbar_test_wait(tbar(t, ScanSmem::PREADY), s & 1)) {
                         tc_fence_after();
                         const uint64_t b_v = sdesc_sw128(stage_v(st), 1024, 1024);
@@ -317,11 +338,10 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                             umma_bf16(t_o(t), a_p + (uint64_t)((kk >> 2) * (kQBytes >> 4) + 2 * (kk & 3)),
                                       b_v + 128 * kk, ID_PV, (s > 0 || kk > 0));
                         umma_commit(tbar(t, ScanSmem::BAR_O));
-                        // this step's S|state MMA completed before its softmax finished, so
-                        // this commit covers every read of the stage by tile t; two arrivals
-                        // per stage (a stage read by one tile only gets both from that tile)
-                        umma_commit(bar(ScanSmem::EMPTY + st));
-                        if (!reads(1 - t, n)) umma_commit(bar(ScanSmem::EMPTY + st));
+                        // two arrivals per value stage (a stage read by one tile only gets
+                        // both from that tile)
+                        umma_commit(bar(ScanSmem::EMPTY_V + st));
+                        if (!reads(1 - t, n)) umma_commit(bar(ScanSmem::EMPTY_V + st));
                         ++s;
                         progress = true;
                     }
@@ -338,10 +358,17 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
             if (producer) {
                 // drain: every issued copy has landed before the CTA may exit
-                for (int n = (n_fill > NS ? n_fill - NS : 0); n < n_fill; ++n) {
-                    const uint32_t bfull = bar(ScanSmem::FULL + n % NS);
+                for (int n = (nv_fill > NV ? nv_fill - NV : 0); n < nv_fill; ++n) {
+                    const uint32_t bfull = bar(ScanSmem::FULL_V + n % NV);
                     const uint64_t t0 = cycles_now();
-                    while (!mbar_try_wait(bfull, (n / NS) & 1) &&
+                    while (!mbar_try_wait(bfull, (n / NV) & 1) &&
+                           cycles_now() - t0 < ns_to_cycles(limit_ns)) {
+                    }
+                }
+                for (int m = (nr_fill > NR ? nr_fill - NR : 0); m < nr_fill; ++m) {
+                    const uint32_t bfull = bar(ScanSmem::FULL_R + m % NR);
+                    const uint64_t t0 = cycles_now();
+                    while (!mbar_try_wait(bfull, (m / NR) & 1) &&
                            cycles_now() - t0 < ns_to_cycles(limit_ns)) {
                     }
                 }
@@ -472,20 +499,35 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    v[j] = RAW ? __uint_as_float(a[j]) : __uint_as_float(a[j]) * scale_log2;
-                    v[32 + j] = RAW ? __uint_as_float(b[j]) : __uint_as_float(b[j]) * scale_log2;
-                    v[64 + j] = RAW ? __uint_as_float(c[j]) : __uint_as_float(c[j]) * scale_log2;
-                    v[96 + j] = RAW ? __uint_as_float(d[j]) : __uint_as_float(d[j]) * scale_log2;
+                    v[j] = __uint_as_float(a[j]);
+                    v[32 + j] = __uint_as_float(b[j]);
+                    v[64 + j] = __uint_as_float(c[j]);
+                    v[96 + j] = __uint_as_float(d[j]);
                 }
                 if (FOX) {
+                    // v = scale log2(e) S + c2_i - c2_j, two columns per instruction
                     const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
+                    const float2 sl2 = make_float2(scale_log2, scale_log2);
+                    const float2 ci2 = make_float2(c2_i, c2_i);
+                    const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
                     for (int q4 = 0; q4 < 32; ++q4) {
                         const float4 cc = __ldg(cj + q4);
-                        v[4 * q4 + 0] += c2_i - cc.x;
-                        v[4 * q4 + 1] += c2_i - cc.y;
-                        v[4 * q4 + 2] += c2_i - cc.z;
-                        v[4 * q4 + 3] += c2_i - cc.w;
+                        const float2 b0 = ffma2(make_float2(cc.x, cc.y), neg1, ci2);
+                        const float2 b1 = ffma2(make_float2(cc.z, cc.w), neg1, ci2);
+                        const float2 w0 = ffma2(make_float2(v[4 * q4], v[4 * q4 + 1]), sl2, b0);
+                        const float2 w1 = ffma2(make_float2(v[4 * q4 + 2], v[4 * q4 + 3]), sl2, b1);
+                        v[4 * q4] = w0.x; v[4 * q4 + 1] = w0.y;
+                        v[4 * q4 + 2] = w1.x; v[4 * q4 + 3] = w1.y;
+                    }
+                } else if (!RAW) {
+                    const float2 sl2 = make_float2(scale_log2, scale_log2);
+                    const float2 z2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const float2 w = ffma2(make_float2(v[2 * j], v[2 * j + 1]), sl2, z2);
+                        v[2 * j] = w.x;
+                        v[2 * j + 1] = w.y;
                     }
                 }
             }
@@ -495,15 +537,13 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 
             // ---- online softmax with lazy rescaling: the running max is raised only when
             // the step's max exceeds it by more than 2^8; then the row sum and O are rescaled
-            float m8[8];
+            float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = v[e];
+            for (int j = 4; j < 124; j += 8)
 #pragma unroll
-            for (int j = 8; j < 128; j += 8)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], v[j + e]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                for (int e = 0; e < 4; ++e) m4[e] = fmax3(m4[e], v[j + 2 * e], v[j + 2 * e + 1]);
+            float mx = fmax3(fmax3(m4[0], m4[1], v[124]), fmax3(m4[2], m4[3], v[125]),
+                             fmaxf(v[126], v[127]));
             if (raw_s) mx *= scale_log2;
             float alpha = 1.f;
             bool rescale = false;
@@ -517,17 +557,20 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             const float cs = raw_s ? scale_log2 : 1.f;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(neg_m, neg_m);
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
             uint32_t pk[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float p0 = ex2_approx(fmaf(v[2 * j], cs, neg_m));
-                const float p1 = ex2_approx(fmaf(v[2 * j + 1], cs, neg_m));
-                ls[(2 * j) & 3] += p0;
-                ls[(2 * j + 1) & 3] += p1;
-                pk[j] = pack_bf16x2(p0, p1);
+                const float2 x = ffma2(make_float2(v[2 * j], v[2 * j + 1]), cs2, nm2);
+                const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                ls[j & 3] = fadd2(ls[j & 3], p);
+                pk[j] = pack_bf16x2(p.x, p.y);
             }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            const float2 l01 = fadd2(ls[0], ls[1]), l23 = fadd2(ls[2], ls[3]);
+            const float2 l4 = fadd2(l01, l23);
+            l_run += l4.x + l4.y;
             // the P tile was last read by this tile's P.V MMA of step s - 1 (on step 0 it held
             // [K~_{2t}; P_{2t}], read by the MMA that produced this step's S); that P.V also
             // has to be complete before O is rescaled
