@@ -393,40 +393,61 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         const int r = quad * 32 + lane;          // row of both tiles = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         bool ok = true;
-        auto wwait = [&](uint32_t b_, uint32_t par) {
-            return __all_sync(0xffffffffu, wait(b_, par)) != 0;
-        };
-        const int smax = hasB ? max(nsteps_of(0), nsteps_of(1)) : nsteps_of(0);
-        for (int s = 0; s < smax - 1 && ok; ++s) {
-            for (int t = hasB ? 1 : 0; t >= 0; --t) {
-                if (s >= nsteps_of(t) - 1) continue;  // the last step needs no new state
-                if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX), s & 1))) break;
-                tc_fence_after();
-                // the state of step s + 1 replaces that of step s, whose only reader (the
-                // S|state MMA of step s) has completed; rows of block 2t keep q~ after step 0
-                if (s >= 1 || quad >= 2) {
-                    uint8_t *row = gbase + ScanSmem::q_st(t);
-                    const uint32_t src = t_base(t) + (s == 0 ? 64u : 128u) + lane_base;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t x[32];
-                        tmem_ld32(src + 32 * h, x);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t *e = &x[8 * c];
-                            *reinterpret_cast<uint4 *>(row + sw128_offset(r, 4 * h + c)) =
-                                make_uint4(pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1])),
-                                           pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3])),
-                                           pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5])),
-                                           pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7])));
-                        }
+        // each tile needs a new state after every step but its last; convert whichever tile's
+        // S|state MMA completes first (the two tiles' recurrences are independent)
+        int next[2] = {0, 0};
+        const int need[2] = {nsteps_of(0) - 1, hasB ? nsteps_of(1) - 1 : 0};
+        uint64_t t_last = cycles_now();
+        while (ok && (next[0] < need[0] || next[1] < need[1])) {
+            int t = -1;
+            if (lane == 0) {
+                for (int c = 1; c >= 0 && t < 0; --c)
+                    if (next[c] < need[c] && mbar_test_wait(tbar(c, ScanSmem::BAR_SX), next[c] & 1)) t = c;
+            }
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t < 0) {
+                // nothing ready: back off briefly so the softmax warps keep the issue slots
+                int stop = 0;
+                if (lane == 0) {
+                    if (*abort_flag) {
+                        stop = 1;
+                    } else if (cycles_now() - t_last > ns_to_cycles(limit_ns)) {
+                        report_status(status, kStatusTimeout);
+                        *abort_flag = 1u;
+                        stop = 1;
                     }
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive_warp(tbar(t, ScanSmem::QREADY));
+                if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
+                else __nanosleep(32);
+                continue;
             }
+            const int s = next[t]++;
+            t_last = cycles_now();
+            tc_fence_after();
+            // the state of step s + 1 replaces that of step s, whose only reader (the
+            // S|state MMA of step s) has completed; rows of block 2t keep q~ after step 0
+            if (s >= 1 || quad >= 2) {
+                uint8_t *row = gbase + ScanSmem::q_st(t);
+                const uint32_t src = t_base(t) + (s == 0 ? 64u : 128u) + lane_base;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t x[32];
+                    tmem_ld32(src + 32 * h, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t *e = &x[8 * c];
+                        *reinterpret_cast<uint4 *>(row + sw128_offset(r, 4 * h + c)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1])),
+                                       pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3])),
+                                       pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5])),
+                                       pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7])));
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive_warp(tbar(t, ScanSmem::QREADY));
         }
         tc_fence_before();
     } else {
