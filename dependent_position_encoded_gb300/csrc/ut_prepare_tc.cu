@@ -251,10 +251,8 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_relinquish();
         tc_fence_before();
     }
-    if (r < kC) {
-        const int t = t0 + r;
-        bs[r] = (t < L) ? beta[head + t] : 0.f;
-    }
+    // beta is first needed after MMA1: its load overlaps the TMA loads and MMA1
+    const float beta_r = (r < kC && t0 + r < L) ? beta[head + t0 + r] : 0.f;
     if (log_f != nullptr && warp == 1) {
         const int ln = r - 32;
         const int ta = t0 + 2 * ln, tb = ta + 1;
@@ -307,7 +305,8 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         umma_commit(bar_mma);
     }
-    bool ok = wait_all(bar_mma, 0);
+    if (r < kC) bs[r] = beta_r;
+    bool ok = wait_all(bar_mma, 0);  // (its barrier also publishes bs)
     if (ok) {
         tc_fence_after();
         float x[64];
@@ -353,7 +352,15 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (r < kC) {
             const int s = r;   // row s: A[s][u] = X[s][u] beta_u, u >= s
 #pragma unroll
-            for (int u = 0; u < 64; ++u) a[u] = (u >= s) ? X[s * XLD + u] * bs[u] : 0.f;
+            for (int u4 = 0; u4 < 16; ++u4) {
+                const float4 xv = *reinterpret_cast<const float4 *>(X + s * XLD + 4 * u4);
+                const float4 bv = *reinterpret_cast<const float4 *>(bs + 4 * u4);
+                const int u = 4 * u4;
+                a[u] = (u >= s) ? xv.x * bv.x : 0.f;
+                a[u + 1] = (u + 1 >= s) ? xv.y * bv.y : 0.f;
+                a[u + 2] = (u + 2 >= s) ? xv.z * bv.z : 0.f;
+                a[u + 3] = (u + 3 >= s) ? xv.w * bv.w : 0.f;
+            }
         } else {
             const int u = r - kC;  // column u: A[s][u], s <= u
             const float bu = bs[u];
