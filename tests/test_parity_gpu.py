@@ -185,11 +185,26 @@ def test_prepare_factors_match_explicit_products(lib, L, fox):
         BH, nblk, 128, 64)
     dg = ws[off_dg:off_dg + BH * nblk * 64 * 64 * 2].view(torch.float16).reshape(
         BH, nblk, 64, 64)
+    off_pr = _align256(off_dg + BH * nblk * 64 * 64 * 2)
+    pr = ws[off_pr:off_pr + BH * (nblk // 2) * 128 * 64 * 2].view(torch.bfloat16).reshape(
+        BH, nblk // 2, 128, 64)
     h = {k_: v.reshape(BH, L, *v.shape[3:]).double().cpu().numpy() for k_, v in x.items()}
     for bh in range(BH):
+        refs = [_block_reference(h["q"][bh], h["k"][bh], h["w"][bh], h["beta"][bh],
+                                 h["log_f"][bh] if fox else None, 64 * b, L, 0.125)
+                for b in range(nb)]
+        # block-pair products for the two-block scan steps: K^ = K~_{2u} P_{2u+1},
+        # Pi = P_{2u} P_{2u+1} (a block past the end is the identity transition)
+        for u in range(nblk // 2):
+            k_lo, p_lo = refs[2 * u][1], refs[2 * u][2]
+            p_hi = refs[2 * u + 1][2] if 2 * u + 1 < nb else np.eye(64)
+            n = min(64, L - 128 * u)
+            g_kh = pr[bh, u, :64].double().cpu().numpy()
+            g_pi = pr[bh, u, 64:].double().cpu().numpy()
+            assert np.abs(g_kh[:n] - (k_lo @ p_hi)[:n]).max() <= 3e-2
+            assert np.abs(g_pi - p_lo @ p_hi).max() <= 1.5e-2
         for b in range(nb):
-            rq, rk, rP, rD = _block_reference(h["q"][bh], h["k"][bh], h["w"][bh], h["beta"][bh],
-                                              h["log_f"][bh] if fox else None, 64 * b, L, 0.125)
+            rq, rk, rP, rD = refs[b]
             n = min(64, L - 64 * b)
             gq = qt[bh, 64 * b:64 * b + n].double().cpu().numpy()
             gk = kp[bh, b, :n].double().cpu().numpy()
