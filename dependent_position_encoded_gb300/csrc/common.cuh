@@ -28,12 +28,15 @@ constexpr uint32_t kStatusTimeout = 7u;
 //   pr  : (BH, nblk/2, 128, 64) bf16 inputs only: per pair of blocks u = (2u, 2u+1),
 //                             rows 0-63 K^_j = P_{2u+1}^T k~_j (keys of block 2u carried
 //                             through block 2u+1), rows 64-127 Pi_u = P_{2u} P_{2u+1}
-//   c2  : (BH, Lp)            fp32 log2(e) * cumsum(log f) (PaTH-FoX only)
+//   c2  : (BH, Lp)            fp32 log2(e) * cumsum(log f) relative to the base of the
+//                             token's pair of blocks, with the pair bases as fp32 pairs
+//                             (PaTH-FoX only)
 // nblk is rounded up to an even count so that 128-row tiles are complete;
 // padded tokens carry identity transitions and zero queries and keys.
 struct FwdLayout {
     int BH, L, nblk, Lp, elt;
-    size_t off_qt, off_kp, off_dg, off_pr, off_c2, off_mpre, off_kpre, off_fb, total;
+    size_t off_qt, off_kp, off_dg, off_pr, off_c2, off_pbase, off_mpre, off_kpre, off_fb;
+    size_t off_btot, off_bmin, off_boff, off_bkmax, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -56,18 +59,33 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     off = align256(off + bh * lay.nblk * kC * kC * (elt_bytes == 2 ? 2 : 4));
     lay.off_pr = off;
     if (elt_bytes == 2) off = align256(off + bh * (lay.nblk / 2) * 2 * kC * kD * 2);
-    // PaTH-FoX only: c2 = log2(e) * cumsum(log f) (BH, Lp); per key block the prefix
-    // minimum of c2 and prefix maximum of |k~| (BH, nblk); per query block the first key
-    // block the scan visits (BH, nblk) int32
-    lay.off_c2 = lay.off_mpre = lay.off_kpre = lay.off_fb = off;
+    // PaTH-FoX only, with c2 = log2(e) * cumsum(log f): c2 relative to the base of its
+    // pair of blocks, c2_t - c2_base(t / 128) (BH, Lp) fp32, and the pair bases as fp32 pairs
+    // hi + lo (BH, nblk / 2, 2); per key block the prefix minimum of c2 and prefix maximum
+    // of |k~| (BH, nblk) fp32; per query block the first key block the scan visits
+    // (BH, nblk) int32; and the per-block fp64 totals, in-block minima, offsets and fp32
+    // key-norm maxima they come from
+    lay.off_c2 = lay.off_pbase = lay.off_mpre = lay.off_kpre = lay.off_fb = off;
+    lay.off_btot = lay.off_bmin = lay.off_boff = lay.off_bkmax = off;
     if (fox) {
+        const size_t nb = bh * lay.nblk;
         off = align256(off + bh * lay.Lp * sizeof(float));
+        lay.off_pbase = off;
+        off = align256(off + nb * sizeof(float));  // (nblk / 2) pairs x (hi, lo)
         lay.off_mpre = off;
-        off = align256(off + bh * lay.nblk * sizeof(float));
+        off = align256(off + nb * sizeof(float));
         lay.off_kpre = off;
-        off = align256(off + bh * lay.nblk * sizeof(float));
+        off = align256(off + nb * sizeof(float));
         lay.off_fb = off;
-        off = align256(off + bh * lay.nblk * sizeof(int));
+        off = align256(off + nb * sizeof(int));
+        lay.off_btot = off;
+        off = align256(off + nb * sizeof(double));
+        lay.off_bmin = off;
+        off = align256(off + nb * sizeof(double));
+        lay.off_boff = off;
+        off = align256(off + nb * sizeof(double));
+        lay.off_bkmax = off;
+        off = align256(off + nb * sizeof(float));
     }
     lay.total = off;
     return lay;

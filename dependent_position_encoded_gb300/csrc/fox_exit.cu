@@ -4,7 +4,16 @@
 // Attention" §2 ("拡張: PaTH-FoX"): the FoX logit of row i against key j adds the data-
 // dependent forget-gate bias sum_{s=j+1..i} log f_s = c_i - c_j with c the inclusive
 // prefix sum of log f. Everything here is in log2 units (c2 = log2(e) * c), like the
-// scan's logits.
+// scan's logits. The sums are accumulated in fp64 (per block, then over block totals): c_i
+// itself can reach thousands over a long sequence, and one fp32 difference c_i - c_j would
+// carry an error of about ulp(|c_i|) even for neighbouring tokens. So each token stores
+// c2 relative to the base of its pair of 64-token blocks (small, fp32), and each pair its
+// base as an fp32 pair hi + lo; the scan forms c2_i - c2_j as
+//     [(hi_P(i) - hi_u) + (lo_P(i) - lo_u) + rel_i] - rel_j      (j in pair u),
+// the bracket once per row and step, accurate to the size of the bias.
+// Three passes: per key block (fp64 total, in-block minimum, key-norm maximum), per head
+// over the block totals (offsets and prefix bounds), per query block (its c2 values and
+// its early-exit extent).
 //
 // Early exit. Every H_s = I - beta_s w_s w_s^T with beta_s in [0, 2] and unit w_s is a
 // contraction, so the state a row carries down the scan, x = P_{b+1} ... q~_i, has
@@ -87,102 +96,165 @@ __device__ __forceinline__ float row_max(const float *row) {
     return m;
 }
 
-// Per head (one CTA of 1024 threads, 16 blocks of 64 tokens per pass):
-//   c2[t]   = log2(e) * sum_{s<=t} log f_s   (padded positions repeat the last value)
-//   mpre[b] = min of c2 over blocks 0..b,  kpre[b] = max of |k~_j| over real tokens of
-//   blocks 0..b (k~ from the preprocessing workspace, which must already be written).
+// Inclusive prefix sum of log f within one 64-token block, in fp64 (64 threads, one token
+// each; tokens at or beyond L contribute 0).
+__device__ __forceinline__ double block_prefix(const float *__restrict__ log_f, int L, int bh,
+                                               int blk, double *warp_tot) {
+    const int r = threadIdx.x, lane = r & 31, wid = r >> 5;
+    const int t = blk * kC + r;
+    double x = (t < L) ? (double)log_f[(size_t)bh * L + t] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += n;
+    }
+    if (lane == 31) warp_tot[wid] = x;
+    __syncthreads();
+    if (wid == 1) x += warp_tot[0];
+    return x;
+}
+
+// Per key block (64 threads): its total of log f, the minimum of its in-block prefix sums
+// (both fp64) and the largest |k~_j| over its real tokens (k~ from the preprocessing
+// workspace, which must already be written).
 template <typename T>
-__global__ void __launch_bounds__(1024)
-fox_bounds_kernel(const float *__restrict__ log_f, const T *__restrict__ kp, int L, int Lp,
-                  int nblk, float *__restrict__ c2, float *__restrict__ mpre,
-                  float *__restrict__ kpre) {
-    __shared__ float warp_tot[32], warp_min[32], warp_max[32];
-    __shared__ float carry_s, cmin_s, kmax_s;
-    const int bh = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const float *src = log_f + (size_t)bh * L;
-    float *dst = c2 + (size_t)bh * Lp;
-    if (tid == 0) {
-        carry_s = 0.f;
-        cmin_s = INFINITY;
-        kmax_s = 0.f;
+__global__ void __launch_bounds__(64)
+fox_block_kernel(const float *__restrict__ log_f, const T *__restrict__ kp, int L, int nblk,
+                 double *__restrict__ btot, double *__restrict__ bmin, float *__restrict__ bkmax) {
+    __shared__ double warp_tot[2], warp_min[2];
+    __shared__ float warp_kmax[2];
+    const int b = blockIdx.x, bh = blockIdx.y, r = threadIdx.x, lane = r & 31, wid = r >> 5;
+    const double loc = block_prefix(log_f, L, bh, b, warp_tot);
+    const int t = b * kC + r;
+    float kn = 0.f;
+    if (t < L) kn = sqrtf(row_norm2(kp + (((size_t)bh * nblk + b) * (2 * kC) + r) * kD));
+    double m = loc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        m = fmin(m, __shfl_xor_sync(0xffffffffu, m, o));
+        kn = fmaxf(kn, __shfl_xor_sync(0xffffffffu, kn, o));
+    }
+    __syncthreads();  // warp_tot was read by block_prefix
+    if (lane == 0) {
+        warp_min[wid] = m;
+        warp_kmax[wid] = kn;
     }
     __syncthreads();
-    for (int base = 0; base < Lp; base += 1024) {
-        const int t = base + tid;
-        float x = (t < L) ? src[t] : 0.f;
+    if (r == kC - 1) btot[(size_t)bh * nblk + b] = loc;
+    if (r == 0) {
+        bmin[(size_t)bh * nblk + b] = fmin(warp_min[0], warp_min[1]);
+        bkmax[(size_t)bh * nblk + b] = fmaxf(warp_kmax[0], warp_kmax[1]);
+    }
+}
+
+// Per head (256 threads over its key blocks): the fp64 offset of every block (the sum of
+// log f over all earlier blocks), and in log2 units the prefix bounds
+//   mpre[b] = min of c2 over blocks 0..b,   kpre[b] = max of |k~_j| over blocks 0..b.
+__global__ void __launch_bounds__(256)
+fox_prefix_kernel(const double *__restrict__ btot, const double *__restrict__ bmin,
+                  const float *__restrict__ bkmax, int nblk, double *__restrict__ boff,
+                  float *__restrict__ mpre, float *__restrict__ kpre) {
+    __shared__ double w_sum[8], w_min[8];
+    __shared__ float w_max[8];
+    __shared__ double c_off, c_min;
+    __shared__ float c_max;
+    const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) {
+        c_off = 0.0;
+        c_min = INFINITY;
+        c_max = 0.f;
+    }
+    __syncthreads();
+    for (int base = 0; base < nblk; base += 256) {
+        const int b = base + tid;
+        const size_t g = (size_t)bh * nblk + b;
+        const double tot = (b < nblk) ? btot[g] : 0.0;
+        // exclusive prefix of the block totals
+        double x = tot;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, x, o);
+            const double n = __shfl_up_sync(0xffffffffu, x, o);
             if (lane >= o) x += n;
         }
-        if (lane == 31) warp_tot[wid] = x;
+        if (lane == 31) w_sum[wid] = x;
         __syncthreads();
-        if (wid == 0) {
-            float y = warp_tot[lane];
+        double before = c_off;
+        for (int w = 0; w < wid; ++w) before += w_sum[w];
+        const double off = before + x - tot;
+        // prefix minimum of the block minima of c, prefix maximum of |k~|
+        double m = (b < nblk) ? off + bmin[g] : INFINITY;
+        float k = (b < nblk) ? bkmax[g] : 0.f;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, y, o);
-                if (lane >= o) y += n;
+        for (int o = 1; o < 32; o <<= 1) {
+            const double nm = __shfl_up_sync(0xffffffffu, m, o);
+            const float nk = __shfl_up_sync(0xffffffffu, k, o);
+            if (lane >= o) {
+                m = fmin(m, nm);
+                k = fmaxf(k, nk);
             }
-            warp_tot[lane] = y;
+        }
+        if (lane == 31) {
+            w_min[wid] = m;
+            w_max[wid] = k;
         }
         __syncthreads();
-        const float v = carry_s + x + (wid > 0 ? warp_tot[wid - 1] : 0.f);
-        const float cv = kLog2e * v;
-        if (t < Lp) dst[t] = cv;
-        float kn = 0.f;
-        if (t < L) {
-            const T *row = kp + (((size_t)bh * nblk + (t >> 6)) * (2 * kC) + (t & 63)) * kD;
-            kn = sqrtf(row_norm2(row));
+        double pm = c_min;
+        float pk = c_max;
+        for (int w = 0; w < wid; ++w) {
+            pm = fmin(pm, w_min[w]);
+            pk = fmaxf(pk, w_max[w]);
         }
-        float cm = (t < Lp) ? cv : INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            cm = fminf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-            kn = fmaxf(kn, __shfl_xor_sync(0xffffffffu, kn, o));
-        }
-        if (lane == 0) {
-            warp_min[wid] = cm;
-            warp_max[wid] = kn;
+        pm = fmin(pm, m);
+        pk = fmaxf(pk, k);
+        if (b < nblk) {
+            boff[g] = off;
+            mpre[g] = (float)(pm * (double)kLog2e);
+            kpre[g] = pk;
         }
         __syncthreads();
-        if (tid == 1023) carry_s = v;
-        if (tid == 0) {
-            // blocks of 64 tokens = warp pairs; running minimum / maximum across blocks
-            float cmin = cmin_s, kmax = kmax_s;
-            for (int k = 0; k < 16; ++k) {
-                const int b = (base >> 6) + k;
-                if (b >= nblk) break;
-                cmin = fminf(cmin, fminf(warp_min[2 * k], warp_min[2 * k + 1]));
-                kmax = fmaxf(kmax, fmaxf(warp_max[2 * k], warp_max[2 * k + 1]));
-                mpre[(size_t)bh * nblk + b] = cmin;
-                kpre[(size_t)bh * nblk + b] = kmax;
-            }
-            cmin_s = cmin;
-            kmax_s = kmax;
+        if (tid == 255) {
+            c_off = off + tot;
+            c_min = pm;
+            c_max = pk;
         }
         __syncthreads();
     }
 }
 
-// first[bh][qb]: the lowest key block any row of query block qb needs (qb itself when no
-// earlier block is needed). One CTA of 64 threads (one row each) per query block.
+// Per query block (64 threads, one row each): first writes c2 of its 64 positions,
+// c2_i = log2(e) (offset of the block + in-block prefix), as an fp32 pair hi + lo (so that
+// differences c2_i - c2_j stay accurate to their own size however large the sums grow);
+// then first[bh][qb], the lowest key block any of its rows needs (qb itself when no
+// earlier block is needed).
 template <typename T, typename D>
 __global__ void __launch_bounds__(64)
-fox_exit_kernel(const T *__restrict__ qt, const D *__restrict__ dg,
-                const float *__restrict__ c2, const float *__restrict__ mpre,
+fox_exit_kernel(const float *__restrict__ log_f, const double *__restrict__ boff,
+                const T *__restrict__ qt, const D *__restrict__ dg, float *__restrict__ c2,
+                float *__restrict__ pbase, const float *__restrict__ mpre,
                 const float *__restrict__ kpre, int L, int Lp, int nblk, float abs_scale_log2,
                 int *__restrict__ first) {
     __shared__ int warp_first[2];
+    __shared__ double warp_tot[2];
     const int qb = blockIdx.x, bh = blockIdx.y, r = threadIdx.x;
     const int i = qb * kC + r;
+    const double loc = block_prefix(log_f, L, bh, qb, warp_tot);
+    const double own = boff[(size_t)bh * nblk + qb], base = boff[(size_t)bh * nblk + (qb & ~1)];
+    const double cd = (own + loc) * (double)kLog2e;
+    const float c_hi = (float)cd;
+    c2[(size_t)bh * Lp + i] = (float)((own - base + loc) * (double)kLog2e);
+    if (r == 0 && (qb & 1) == 0) {
+        const double bd = base * (double)kLog2e;
+        const float bh_hi = (float)bd;
+        float *pb = pbase + ((size_t)bh * (nblk >> 1) + (qb >> 1)) * 2;
+        pb[0] = bh_hi;
+        pb[1] = (float)(bd - (double)bh_hi);
+    }
     int lo = qb;
     if (i < L && qb > 0) {
         const float qn = sqrtf(row_norm2(qt + ((size_t)bh * Lp + i) * kD));
         const float dmax = row_max(dg + (((size_t)bh * nblk + qb) * kC + r) * kC);
         const float rhs = dmax - kExitLog2;
-        const float ci = c2[(size_t)bh * Lp + i];
+        const float ci = c_hi;
         const float qk = 2.f * abs_scale_log2 * qn;
         const float *mp = mpre + (size_t)bh * nblk;
         const float *kq = kpre + (size_t)bh * nblk;
@@ -211,28 +283,35 @@ cudaError_t launch_fox_prepare(const float *log_f, int BH, int L, int elt_bytes,
     const FwdLayout lay = fwd_layout(1, BH, L, elt_bytes, true);
     char *basep = static_cast<char *>(ws);
     float *c2 = reinterpret_cast<float *>(basep + lay.off_c2);
+    float *pbase = reinterpret_cast<float *>(basep + lay.off_pbase);
     float *mpre = reinterpret_cast<float *>(basep + lay.off_mpre);
     float *kpre = reinterpret_cast<float *>(basep + lay.off_kpre);
     int *first = reinterpret_cast<int *>(basep + lay.off_fb);
+    double *btot = reinterpret_cast<double *>(basep + lay.off_btot);
+    double *bmin = reinterpret_cast<double *>(basep + lay.off_bmin);
+    double *boff = reinterpret_cast<double *>(basep + lay.off_boff);
+    float *bkmax = reinterpret_cast<float *>(basep + lay.off_bkmax);
     const float s = fabsf(scale) * kLog2e;
     const dim3 grid(lay.nblk, BH);
-    if (elt_bytes == 2) {
-        fox_bounds_kernel<__nv_bfloat16><<<BH, 1024, 0, stream>>>(
-            log_f, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_kp), L, lay.Lp,
-            lay.nblk, c2, mpre, kpre);
+    if (elt_bytes == 2)
+        fox_block_kernel<__nv_bfloat16><<<grid, 64, 0, stream>>>(
+            log_f, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_kp), L, lay.nblk, btot,
+            bmin, bkmax);
+    else
+        fox_block_kernel<float><<<grid, 64, 0, stream>>>(
+            log_f, reinterpret_cast<const float *>(basep + lay.off_kp), L, lay.nblk, btot, bmin,
+            bkmax);
+    fox_prefix_kernel<<<BH, 256, 0, stream>>>(btot, bmin, bkmax, lay.nblk, boff, mpre, kpre);
+    if (elt_bytes == 2)
         fox_exit_kernel<__nv_bfloat16, __half><<<grid, 64, 0, stream>>>(
-            reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
-            reinterpret_cast<const __half *>(basep + lay.off_dg), c2, mpre, kpre, L, lay.Lp,
+            log_f, boff, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
+            reinterpret_cast<const __half *>(basep + lay.off_dg), c2, pbase, mpre, kpre, L, lay.Lp,
             lay.nblk, s, first);
-    } else {
-        fox_bounds_kernel<float><<<BH, 1024, 0, stream>>>(
-            log_f, reinterpret_cast<const float *>(basep + lay.off_kp), L, lay.Lp, lay.nblk, c2,
-            mpre, kpre);
+    else
         fox_exit_kernel<float, float><<<grid, 64, 0, stream>>>(
-            reinterpret_cast<const float *>(basep + lay.off_qt),
-            reinterpret_cast<const float *>(basep + lay.off_dg), c2, mpre, kpre, L, lay.Lp,
+            log_f, boff, reinterpret_cast<const float *>(basep + lay.off_qt),
+            reinterpret_cast<const float *>(basep + lay.off_dg), c2, pbase, mpre, kpre, L, lay.Lp,
             lay.nblk, s, first);
-    }
     return cudaGetLastError();
 }
 

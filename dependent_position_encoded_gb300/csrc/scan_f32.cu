@@ -35,7 +35,8 @@ template <bool FOX>
 __global__ void __launch_bounds__(kThreads)
 path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
                      const float *__restrict__ kp, const float *__restrict__ dg,
-                     const float *__restrict__ c2, const int *__restrict__ first_blk,
+                     const float *__restrict__ c2, const float *__restrict__ pbase,
+                     const int *__restrict__ first_blk,
                      float *__restrict__ out, float *__restrict__ lse, int L, int Lp, int nblk,
                      float scale_log2) {
     extern __shared__ __align__(16) float sm[];
@@ -56,7 +57,12 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
     const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
     const int row = tid >> 2, part = tid & 3;  // softmax: 4 threads per row
     float m_run = -INFINITY, l_run = 0.f;
-    const float c2_row = FOX ? c2[head * Lp + ib * kC + row] : 0.f;
+    // gate sums relative to the base of their pair of blocks; per key block the row's
+    // offset against pair b / 2 is (base_own - base) in fp32-pair arithmetic + rel_row
+    const float rel_row = FOX ? c2[head * Lp + ib * kC + row] : 0.f;
+    const int npair = nblk >> 1;
+    const float2 base_own = FOX ? *reinterpret_cast<const float2 *>(pbase + (head * npair + (ib >> 1)) * 2)
+                                : make_float2(0.f, 0.f);
 
     for (int e = tid; e < kC * kD; e += kThreads) {
         const int i = e / kD, c = e % kD;
@@ -85,6 +91,11 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
             }
         }
         if (FOX && b < ib && tid < kC) c2k[tid] = c2[head * Lp + b * kC + tid];
+        float c2_row = 0.f;
+        if (FOX && b < ib) {
+            const float2 bb = *reinterpret_cast<const float2 *>(pbase + (head * npair + (b >> 1)) * 2);
+            c2_row = ((base_own.x - bb.x) + (base_own.y - bb.y)) + rel_row;
+        }
         __syncthreads();
         if (b < ib) {
             float s[4][4], xn[4][4];
@@ -179,6 +190,7 @@ cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int 
         reinterpret_cast<const float *>(basep + lay.off_kp),
         reinterpret_cast<const float *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
+        fox ? reinterpret_cast<const float *>(basep + lay.off_pbase) : nullptr,
         fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,
         static_cast<float *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e);
     return cudaGetLastError();

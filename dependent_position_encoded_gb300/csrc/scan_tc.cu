@@ -141,6 +141,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_pr64,
                     const __grid_constant__ CUtensorMap tm_v128,
                     const __half *__restrict__ dg, const float *__restrict__ c2,
+                    const float *__restrict__ pbase,
                     const int *__restrict__ first_blk, __nv_bfloat16 *__restrict__ out,
                     float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
                     uint32_t *status, uint64_t limit_ns, int force_timeout) {
@@ -463,7 +464,15 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         const int i = tile * kTile + r;          // query index
         const size_t head = (size_t)bh;
         float m_run = -INFINITY, l_run = 0.f;
-        const float c2_i = FOX ? c2[head * Lp + i] : 0.f;
+        // gate sums relative to the base of their pair of blocks; per step the row's offset
+        // against pair u is (base_tile - base_u) in fp32-pair arithmetic + rel_i
+        const float rel_i = FOX ? c2[head * Lp + i] : 0.f;
+        const float2 base_own = FOX ? *reinterpret_cast<const float2 *>(pbase + (head * ntile + tile) * 2)
+                                    : make_float2(0.f, 0.f);
+        auto row_offset = [&](int u) {
+            const float2 bu = *reinterpret_cast<const float2 *>(pbase + (head * ntile + u) * 2);
+            return ((base_own.x - bu.x) + (base_own.y - bu.y)) + rel_i;
+        };
         bool ok = true;
         // every lane of a warp leaves together: tcgen05.ld/st are warp-collective
         auto wwait = [&](uint32_t b_, uint32_t par) {
@@ -500,13 +509,14 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     }
                     if (FOX) {
                         const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
+                        const float ci = row_offset(u);
 #pragma unroll
                         for (int q4 = 0; q4 < 16; ++q4) {
                             const float4 c = __ldg(cj + q4);
-                            v[4 * q4 + 0] += c2_i - c.x;
-                            v[4 * q4 + 1] += c2_i - c.y;
-                            v[4 * q4 + 2] += c2_i - c.z;
-                            v[4 * q4 + 3] += c2_i - c.w;
+                            v[4 * q4 + 0] += ci - c.x;
+                            v[4 * q4 + 1] += ci - c.y;
+                            v[4 * q4 + 2] += ci - c.z;
+                            v[4 * q4 + 3] += ci - c.w;
                         }
                     }
                     load_diag_row(dg + ((head * nblk + 2 * tile + 1) * kC + (r - 64)) * kC, v + 64);
@@ -529,7 +539,8 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     // v = scale log2(e) S + c2_i - c2_j, two columns per instruction
                     const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
                     const float2 sl2 = make_float2(scale_log2, scale_log2);
-                    const float2 ci2 = make_float2(c2_i, c2_i);
+                    const float ci = row_offset(u);
+                    const float2 ci2 = make_float2(ci, ci);
                     const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
                     for (int q4 = 0; q4 < 32; ++q4) {
@@ -691,6 +702,7 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
         tm_qt, tm_kp128, tm_kp64, tm_pr64, tm_v128,
         reinterpret_cast<const __half *>(basep + lay.off_dg),
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
+        fox ? reinterpret_cast<const float *>(basep + lay.off_pbase) : nullptr,
         fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e,
         reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout);

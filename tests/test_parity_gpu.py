@@ -328,6 +328,25 @@ def test_fox_early_exit_mixed_sign_gate(lib):
     check_bf16(out, ref, lse, ref_lse)
 
 
+def test_fox_long_gate_sums_fp32(lib):
+    # 8192 tokens at log f ~ -1.3: the gate prefix sums reach about -10^4; the bias
+    # c_i - c_j must still be accurate to its own size (fp32 pairs), so that fp32 outputs
+    # and LSE stay within 1e-4 of the oracle
+    x = pi.make_fwd_inputs(1, 1, 8192, dtype=torch.float32, seed=45, clip=0.0, fox=True,
+                           device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(145)
+    x["log_f"] = torch.nn.functional.logsigmoid(
+        torch.randn(x["log_f"].shape, generator=g) - 1.0).to("cuda").contiguous()
+    out, lse = run_fwd(lib, x, fox=True)
+    rows = np.arange(0, 8192, 61)
+    pairs = np.stack([np.zeros_like(rows), rows], axis=1)   # (head, query) pairs
+    h = {k: v[0].cpu() for k, v in x.items()}                # (H = 1, L, ...)
+    ref, ref_lse = oracle.path_rows(h["q"], h["k"], h["v"], h["w"], h["beta"], pairs, h["log_f"])
+    got = out[0, 0].double().cpu().numpy()[rows]
+    assert np.abs(got - ref).max() / np.abs(ref).max() <= F32_MAX_REL
+    assert np.abs(lse[0, 0].double().cpu().numpy()[rows] - ref_lse).max() <= 1e-4
+
+
 def test_fox_zero_gate_has_no_exit(lib):
     # log f = 0: no bias, nothing can be skipped, and FoX equals PaTH (up to rounding:
     # the FoX scan applies the scale in another order than the PaTH scan)
