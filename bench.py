@@ -63,6 +63,15 @@ def decode_bytes(B, H, n, d=64):
     return B * H * (6.0 * n * d + 12.0 * d)
 
 
+def fox_decode_bytes(B, H, n, d=64):
+    """HBM bytes every PaTH-FoX decode step must move over n cached keys: key read + key
+    write (2 bytes each) and the per-key gate sum (4 bytes read, 4 written), plus the new
+    token's q, k, v, w, o, log f and appended gate sum. Value rows of keys whose weight
+    vanishes under the gate are not read, so they are not counted: a lower bound of the
+    traffic, and GB/s on this basis never overstates the achieved bandwidth."""
+    return B * H * (4.0 * n * d + 8.0 * n + 12.0 * d + 8.0)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -225,14 +234,19 @@ def time_e2e(pa, x, steps, warmup):
     return start.elapsed_time(end), h2d, d2h
 
 
-def time_decode(pa, wl, reps=2):
+def time_decode(pa, wl, reps=2, fox=False):
     """Times the 64-step decode sequence (cache reset to the prefix length each repetition;
-    the cache content drifts across repetitions, which does not change the work)."""
+    the cache content drifts across repetitions, which does not change the work). With
+    fox, the PaTH-FoX step over the same cache plus its gate sums."""
     dev = torch.device("cuda")
     cap = wl.n_prefix + wl.steps
-    kc, vc = pi.make_decode_prefix(wl, cap, device=dev)
-    steps = [pi.make_decode_step(wl, t, device=dev) for t in range(wl.steps)]
-    ws = pa.new_workspace(pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16, dev)
+    if fox:
+        kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device=dev)
+    else:
+        kc, vc = pi.make_decode_prefix(wl, cap, device=dev)
+    steps = [pi.make_decode_step(wl, t, device=dev, fox=fox) for t in range(wl.steps)]
+    ws = pa.new_workspace(pa.OP_FOX_DECODE if fox else pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16,
+                          dev)
     out = torch.empty((wl.B, wl.H, 64), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     per_step = []
@@ -240,14 +254,19 @@ def time_decode(pa, wl, reps=2):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(wl.steps + 1)]
         evs[0].record(stream)
         for t, s in enumerate(steps):
-            pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
-                                wl.n_prefix + t, out=out, workspace=ws)
+            if fox:
+                pa.path_fox_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"],
+                                        kc, vc, gc, wl.n_prefix + t, out=out, workspace=ws)
+            else:
+                pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
+                                    wl.n_prefix + t, out=out, workspace=ws)
             evs[t + 1].record(stream)
         torch.cuda.synchronize()
         if r > 0:  # the first pass is the warm-up
             per_step.append([evs[t].elapsed_time(evs[t + 1]) for t in range(wl.steps)])
     ms = [statistics.mean(col) for col in zip(*per_step)]
-    nbytes = [decode_bytes(wl.B, wl.H, wl.n_prefix + t) for t in range(wl.steps)]
+    bytes_fn = fox_decode_bytes if fox else decode_bytes
+    nbytes = [bytes_fn(wl.B, wl.H, wl.n_prefix + t) for t in range(wl.steps)]
     gbs = sum(nbytes) / (sum(ms) * 1e-3) / 1e9
     return {"ms_per_step": sum(ms) / len(ms), "gbs": gbs,
             "tokens_per_s": wl.B / (sum(ms) / len(ms) * 1e-3),
@@ -287,6 +306,8 @@ PROFILE_CASES = {
                           pi.BETA_CLIP, True),
     "decode": pi.DecodeWorkload("path_decode_bf16_B8H32N32768x4", 8, 32, 32768, 4, 64,
                                 torch.bfloat16, 5, 1000),
+    "fox_decode": pi.DecodeWorkload("path_fox_decode_bf16_B8H32N32768x4", 8, 32, 32768, 4, 64,
+                                    torch.bfloat16, 5, 1000),
 }
 
 
@@ -304,6 +325,14 @@ def run_profile_case(args):
         for t in range(args.warmup + args.steps):
             pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
                                 wl.n_prefix + t, workspace=ws)
+    elif args.profile == "fox_decode":
+        cap = wl.n_prefix + args.warmup + args.steps
+        kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device=dev)
+        ws = pa.new_workspace(pa.OP_FOX_DECODE, wl.B, wl.H, cap, pa.BF16, dev)
+        s = pi.make_decode_step(wl, 0, device=dev, fox=True)
+        for t in range(args.warmup + args.steps):
+            pa.path_fox_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"], kc,
+                                    vc, gc, wl.n_prefix + t, workspace=ws)
     else:
         x = pi.workload_inputs(wl, device=dev)
         total, scan, prep = time_forward(pa, x, args.steps, args.warmup, fox=wl.fox)
@@ -402,7 +431,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
-    ap.add_argument("--profile", choices=["fwd", "fox", "decode"],
+    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -460,7 +489,8 @@ def main():
             "fwd_roofline_frac": F / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"],
             "prepare_ms": prep_avg, "scan_ms": scan_avg,
             "roofline": roofline, "clocks": clocks,
-            "gpu_launches": 2 * args.steps}
+            # per step: UT preprocessing, block-pair products, block scan
+            "gpu_launches": 3 * args.steps}
 
     if not args.no_extras:
         e2e_ms, h2d, d2h = time_e2e(pa, x, max(2, args.steps // 2), 3)
@@ -488,6 +518,14 @@ def main():
                            "traffic": ncu_traffic("decode_split_kernel"),
                            "peak_source": "%s HBM copy" % peaks["source"]}
         line["decode"] = dec
+        fdec = time_decode(pa, pi.FOX_DECODE_32K, fox=True)
+        fdec["workload"] = pi.FOX_DECODE_32K.name
+        fdec["roofline"] = {"kernel": "decode_split_kernel<FOX>", "bound": "hbm",
+                            "achieved": fdec["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": fdec["gbs"] / peaks["hbm_gbs"],
+                            "traffic": ncu_traffic("decode_split_kernel_fox"),
+                            "peak_source": "%s HBM copy" % peaks["source"]}
+        line["fox_decode"] = fdec
 
     if args.sweep and rank == 0:
         sweep = {}

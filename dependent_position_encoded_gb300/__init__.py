@@ -8,7 +8,7 @@ passes raw pointers. There is no CPU fallback: without the built library or a
 CUDA device every call raises.
 
 Entry points keep the C names: ``path_attn_fwd``, ``path_fox_fwd``,
-``path_fwd_prepare``, ``path_fwd_scan``, ``path_decode_step``,
+``path_fwd_prepare``, ``path_fwd_scan``, ``path_decode_step``, ``path_fox_decode_step``,
 ``path_workspace_bytes``, ``path_check_workspace``, ``path_status_string``.
 """
 import ctypes
@@ -21,12 +21,12 @@ from . import build as _build
 OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CAPACITY, ERR_TIMEOUT, \
     ERR_CUDA, ERR_ARG = range(10)
 F32, BF16 = 0, 1
-OP_FWD, OP_FOX_FWD, OP_DECODE = 0, 1, 2
+OP_FWD, OP_FOX_FWD, OP_DECODE, OP_FOX_DECODE = 0, 1, 2, 3
 HEAD_DIM = 64
 
 EXPORTED = ("path_workspace_bytes", "path_attn_fwd", "path_fox_fwd", "path_fwd_prepare",
             "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string",
-            "path_decode_step_noalloc", "path_fox_first_blocks")
+            "path_decode_step_noalloc", "path_fox_first_blocks", "path_fox_decode_step")
 
 _lib = None
 
@@ -69,6 +69,9 @@ def _load():
     lib.path_fwd_scan.restype = I
     lib.path_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, S, P]
     lib.path_decode_step.restype = I
+    lib.path_fox_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, S,
+                                         P]
+    lib.path_fox_decode_step.restype = I
     lib.path_decode_step_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.path_decode_step_noalloc.restype = I
     lib.path_fox_first_blocks.argtypes = [P, S, I, I, I, I, I, P, P]
@@ -247,11 +250,7 @@ def path_fox_first_blocks(workspace, B, H, L, dtype, stream=None):
     return first
 
 
-def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, out=None,
-                     workspace=None, stream=None):
-    """One decode step: updates k_cache in place, appends (k, v) at cache_len and returns
-    the attention output (B, H, d). q, k, v, w: (B, H, d) (a trailing length-1 axis is
-    accepted); beta: (B, H); caches: (B, H, cap, d)."""
+def _decode_args(q, k, v, w, beta, k_cache, v_cache, out):
     torch = _torch()
     _cuda_tensor(k_cache, "k_cache")
     dt_t = k_cache.dtype
@@ -272,6 +271,15 @@ def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, 
         out = torch.empty((B, H, d), dtype=dt_t, device=k_cache.device)
     else:
         _cuda_tensor(out, "out", dt_t)
+    return ins, out, (B, H, cap, d)
+
+
+def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, out=None,
+                     workspace=None, stream=None):
+    """One decode step: updates k_cache in place, appends (k, v) at cache_len and returns
+    the attention output (B, H, d). q, k, v, w: (B, H, d) (a trailing length-1 axis is
+    accepted); beta: (B, H); caches: (B, H, cap, d)."""
+    ins, out, (B, H, cap, d) = _decode_args(q, k, v, w, beta, k_cache, v_cache, out)
     if workspace is None:
         workspace = new_workspace(OP_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device)
     _check(_load().path_decode_step(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]), _ptr(ins[3]),
@@ -280,6 +288,31 @@ def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, 
                                     _scale(scale, d), _ptr(out), _ptr(workspace),
                                     workspace.numel(), _stream(stream, k_cache.device)),
            "path_decode_step")
+    return out
+
+
+def path_fox_decode_step(q, k, v, w, beta, log_f, k_cache, v_cache, g_cache, cache_len,
+                         scale=None, out=None, workspace=None, stream=None):
+    """One PaTH-FoX decode step: as path_decode_step, plus the per-key gate sums g_cache
+    (B, H, cap) fp32, updated in place (g_j += log_f for j < cache_len, g = 0 appended), and
+    the bias g_j on every logit. log_f: (B, H) fp32, the new token's log forget gate."""
+    torch = _torch()
+    ins, out, (B, H, cap, d) = _decode_args(q, k, v, w, beta, k_cache, v_cache, out)
+    _cuda_tensor(log_f, "log_f", torch.float32)
+    if log_f.numel() != B * H:
+        raise ValueError("log_f must hold (B, H) values")
+    _cuda_tensor(g_cache, "g_cache", torch.float32)
+    if tuple(g_cache.shape) != (B, H, cap):
+        raise ValueError("g_cache must have shape (B, H, cap)")
+    if workspace is None:
+        workspace = new_workspace(OP_FOX_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device)
+    _check(_load().path_fox_decode_step(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]), _ptr(ins[3]),
+                                        _ptr(beta), _ptr(log_f), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(g_cache), B, H, int(cache_len), cap, d,
+                                        _dtype_code(k_cache), _scale(scale, d), _ptr(out),
+                                        _ptr(workspace), workspace.numel(),
+                                        _stream(stream, k_cache.device)),
+           "path_fox_decode_step")
     return out
 
 

@@ -13,6 +13,17 @@
 // online softmax and o += p v in registers. The CTA merges its warps' partial softmax
 // states and writes (m, l, o) of the split. A second kernel (one CTA per head) appends
 // the new key/value, scores it and merges the splits.
+//
+// PaTH-FoX decode (review §4 and technical summary §2 "拡張: PaTH-FoX": the forget gate
+// adds sum_{s=j+1..t} log f_s to the logit of key j): the cache keeps, per cached key, its
+// running gate sum g_j = sum_{s=j+1..N-1} log f_s up to the last cached token, updated in
+// place like the keys: g_j <- g_j + log f_t for j < N, and the new key enters with g = 0.
+// Recent keys, the ones whose weight matters, hold small sums, so fp32 keeps them exact to
+// within a few ulps however long the cache grows. The gate makes old keys vanish: a key
+// whose logit lies more than 64 (log2 units) below the new token's own logit, itself a
+// lower bound of the row's largest logit, weighs below 2^-64 of the largest weight, so its
+// value row is not read (the key is still updated in place). Even 2^22 such keys move the
+// softmax sum by less than 2^-42 of itself: exact within fp32 rounding.
 #include <mutex>
 
 #include "common.cuh"
@@ -37,6 +48,18 @@ template <> struct Vec<__nv_bfloat16> {
             x[2 * i + 1] = f.y;
         }
     }
+    static __device__ __forceinline__ uint4 load_raw(const __nv_bfloat16 *p) {
+        return *reinterpret_cast<const uint4 *>(p);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &u, float (&x)[8]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack_bf16x2(w[i]);
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
+        }
+    }
     static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float (&x)[8]) {
         uint4 u;
         u.x = pack_bf16x2(x[0], x[1]);
@@ -52,16 +75,25 @@ template <> struct Vec<float> {
         const float4 u = *reinterpret_cast<const float4 *>(p);
         x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
     }
+    static __device__ __forceinline__ uint4 load_raw(const float *p) {
+        return *reinterpret_cast<const uint4 *>(p);
+    }
+    static __device__ __forceinline__ void unpack(const uint4 &u, float (&x)[4]) {
+        x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+    }
     static __device__ __forceinline__ void store(float *p, const float (&x)[4]) {
         *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
     }
 };
 
-template <typename T>
+template <typename T, bool FOX>
 __global__ void __launch_bounds__(kThreads)
 decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                     const float *__restrict__ beta, T *__restrict__ kc, const T *__restrict__ vc,
-                    int cache_len, int cap, int nsplit, float scale_log2, float *__restrict__ part) {
+                    int cache_len, int cap, int nsplit, float scale_log2, float *__restrict__ part,
+                    const T *__restrict__ k_new, const float *__restrict__ log_f,
+                    float *__restrict__ gc) {
     constexpr int E = Vec<T>::E;
     constexpr int TPK = kD / E;   // lanes per key
     constexpr int KPW = 32 / TPK; // keys per warp pass
@@ -77,6 +109,18 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
     Vec<T>::load(q + head * kD + e0, qv);
     Vec<T>::load(w + head * kD + e0, wv);
     const float bt = beta[head];
+    const float lf = FOX ? log_f[head] : 0.f;
+    float *const grow = FOX ? gc + head * cap : nullptr;
+    float thr = -INFINITY;  // FoX: keys scoring below it skip their value row
+    if (FOX) {
+        float kn[E], dn = 0.f;
+        Vec<T>::load(k_new + head * kD + e0, kn);
+#pragma unroll
+        for (int e = 0; e < E; ++e) dn = fmaf(qv[e], kn[e], dn);
+#pragma unroll
+        for (int off = 1; off < TPK; off <<= 1) dn += __shfl_xor_sync(0xffffffffu, dn, off);
+        thr = dn * scale_log2 - 64.f;
+    }
 
     const int j0 = sp * kDecodeChunk;
     const int j1 = min(j0 + kDecodeChunk, cache_len);
@@ -86,18 +130,14 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
 
     T *krow = kc + head * cap * kD + e0;
     const T *vrow = vc + head * cap * kD + e0;
-    // warp-uniform trip count: every lane joins the shuffles, lanes past the end idle
-    for (int jb = j0 + warp * KPW; jb < j1; jb += kWarps * KPW) {
-        const int j = jb + g;
-        const bool valid = j < j1;
-        float kv[E], vv[E];
-        if (valid) {
-            Vec<T>::load(krow + (size_t)j * kD, kv);
-            Vec<T>::load(vrow + (size_t)j * kD, vv);
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) kv[e] = vv[e] = 0.f;
-        }
+    // One cached key: update it in place, score it (bias gj, log2 units) and fold it into
+    // the lane's online softmax. Every lane calls it (the shuffles are warp-wide); lanes
+    // whose key is past the end load nothing and store nothing.
+    // The arithmetic of one cached key whose row kv is in registers: update it in place,
+    // score it (bias gj, log2 units) and fold it into the lane's online softmax. Every lane
+    // calls it (the shuffles are warp-wide); lanes whose key is past the end store nothing.
+    // vv holds the value row, or for FoX is loaded here once the key is known to matter.
+    auto key_math = [&](int j, bool valid, float gj, float (&kv)[E], float (&vv)[E]) {
         float dw = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) dw = fmaf(wv[e], kv[e], dw);
@@ -113,8 +153,12 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
         if (valid) Vec<T>::store(krow + (size_t)j * kD, kv);
 #pragma unroll
         for (int off = 1; off < TPK; off <<= 1) dq += __shfl_xor_sync(0xffffffffu, dq, off);
-        if (!valid) continue;
-        const float xl = dq * scale_log2;
+        if (!valid) return;
+        const float xl = FOX ? fmaf(gj, kLog2e, dq * scale_log2) : dq * scale_log2;
+        if (FOX) {
+            if (xl < thr) return;  // uniform over the key's lanes (they share dq and gj)
+            Vec<T>::load(vrow + (size_t)j * kD, vv);
+        }
         const float m_new = fmaxf(m, xl);
         const float sc = exp2f(m - m_new);  // 0 while m is -inf
         const float p = exp2f(xl - m_new);
@@ -122,6 +166,57 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = fmaf(p, vv[e], o[e] * sc);
         m = m_new;
+    };
+    if (!FOX) {
+        // warp-uniform trip count: every lane joins the shuffles, lanes past the end idle
+        for (int jb = j0 + warp * KPW; jb < j1; jb += kWarps * KPW) {
+            const int j = jb + g;
+            const bool valid = j < j1;
+            float kv[E], vv[E];
+            if (valid) {
+                Vec<T>::load(krow + (size_t)j * kD, kv);
+                Vec<T>::load(vrow + (size_t)j * kD, vv);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) kv[e] = vv[e] = 0.f;
+            }
+            key_math(j, valid, 0.f, kv, vv);
+        }
+    } else {
+        // Each warp owns runs of 32 consecutive keys: lane i reads, advances and writes
+        // back the gate sum of key run + i (one coalesced 128-byte load and store per
+        // run), and the key's lanes fetch it by shuffle. Most value rows are skipped, so
+        // the key rows of a batch of passes are loaded up front (raw, 16 bytes per lane
+        // and pass) to keep enough bytes in flight.
+        constexpr int kPasses = 32 / KPW;
+        constexpr int kBatch = kPasses < 8 ? kPasses : 8;
+        for (int rb = j0 + warp * 32; rb < j1; rb += kWarps * 32) {
+            const int jl = rb + lane;
+            float gl = 0.f;
+            if (jl < j1) {
+                gl = grow[jl] + lf;
+                grow[jl] = gl;
+            }
+#pragma unroll
+            for (int b0 = 0; b0 < kPasses; b0 += kBatch) {
+                uint4 kraw[kBatch];
+#pragma unroll
+                for (int pb = 0; pb < kBatch; ++pb) {
+                    const int j = rb + (b0 + pb) * KPW + g;
+                    kraw[pb] = (j < j1) ? Vec<T>::load_raw(krow + (size_t)j * kD)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int pb = 0; pb < kBatch; ++pb) {
+                    const int src = (b0 + pb) * KPW + g;
+                    const float gj = __shfl_sync(0xffffffffu, gl, src);
+                    const int j = rb + src;
+                    float kv[E], vv[E];
+                    Vec<T>::unpack(kraw[pb], kv);
+                    key_math(j, j < j1, gj, kv, vv);
+                }
+            }
+        }
     }
     // ---- merge the kWarps * KPW partial states of this split
     const int slot = warp * KPW + g;
@@ -153,18 +248,21 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
     }
 }
 
-// One CTA of 64 threads per head: append (k_t, v_t), score the new key and merge splits.
-template <typename T>
+// One CTA of 64 threads per head: append (k_t, v_t) (and, for PaTH-FoX, the new key's
+// gate sum 0: its logit has no bias), score the new key and merge splits.
+template <typename T, bool FOX>
 __global__ void __launch_bounds__(kD)
 decode_merge_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                     T *__restrict__ kc, T *__restrict__ vc, int cache_len, int cap, int nsplit,
-                    float scale_log2, const float *__restrict__ part, T *__restrict__ out) {
+                    float scale_log2, const float *__restrict__ part, T *__restrict__ out,
+                    float *__restrict__ gc) {
     __shared__ float red[2];
     const int bh = blockIdx.x, c = threadIdx.x;
     const size_t head = (size_t)bh;
     const T kt = k[head * kD + c], vt = v[head * kD + c];
     kc[(head * cap + cache_len) * kD + c] = kt;
     vc[(head * cap + cache_len) * kD + c] = vt;
+    if (FOX && c == 0) gc[head * cap + cache_len] = 0.f;
     float d = Elt<T>::to_f(q[head * kD + c]) * Elt<T>::to_f(kt);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
@@ -186,29 +284,52 @@ decode_merge_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     out[head * kD + c] = Elt<T>::from_f(Oc / Ls);
 }
 
+// Both kernels of one step with the split partials at `part`; log_f and gc are used only
+// when FOX is set.
+template <typename T, bool FOX>
+cudaError_t launch_decode_kernels(const void *q, const void *k, const void *v, const void *w,
+                                  const float *beta, const float *log_f, void *k_cache,
+                                  void *v_cache, float *gc, int BH, int cache_len, int cap,
+                                  float scale, void *out, float *part, cudaStream_t stream) {
+    const float sl2 = scale * kLog2e;
+    const int used = (cache_len + kDecodeChunk - 1) / kDecodeChunk;
+    if (used > 0) {
+        dim3 grid(used, BH);
+        decode_split_kernel<T, FOX><<<grid, kThreads, 0, stream>>>(
+            static_cast<const T *>(q), static_cast<const T *>(w), beta, static_cast<T *>(k_cache),
+            static_cast<const T *>(v_cache), cache_len, cap, used, sl2, part,
+            static_cast<const T *>(k), log_f, gc);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    decode_merge_kernel<T, FOX><<<BH, kD, 0, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
+        static_cast<T *>(k_cache), static_cast<T *>(v_cache), cache_len, cap, used, sl2, part,
+        static_cast<T *>(out), gc);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 template <typename T>
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *w,
                           const float *beta, void *k_cache, void *v_cache, int BH, int cache_len,
                           int cap, float scale, void *out, void *ws, cudaStream_t stream) {
-    const int nsplit = decode_splits(cap);
     float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
-    const float sl2 = scale * kLog2e;
-    const int used = (cache_len + kDecodeChunk - 1) / kDecodeChunk;
-    if (used > 0) {
-        dim3 grid(used, BH);
-        decode_split_kernel<T><<<grid, kThreads, 0, stream>>>(
-            static_cast<const T *>(q), static_cast<const T *>(w), beta, static_cast<T *>(k_cache),
-            static_cast<const T *>(v_cache), cache_len, cap, used, sl2, part);
-        cudaError_t err = cudaGetLastError();
-        if (err != cudaSuccess) return err;
-    }
-    decode_merge_kernel<T><<<BH, kD, 0, stream>>>(
-        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
-        static_cast<T *>(k_cache), static_cast<T *>(v_cache), cache_len, cap, used, sl2, part,
-        static_cast<T *>(out));
-    return cudaGetLastError();
+    return launch_decode_kernels<T, false>(q, k, v, w, beta, nullptr, k_cache, v_cache, nullptr,
+                                           BH, cache_len, cap, scale, out, part, stream);
+}
+
+// PaTH-FoX decode: as launch_decode, plus the in-place gate sums gc (BH, cap) fp32 and the
+// new token's log forget gate log_f (BH).
+template <typename T>
+cudaError_t launch_fox_decode(const void *q, const void *k, const void *v, const void *w,
+                              const float *beta, const float *log_f, void *k_cache,
+                              void *v_cache, float *gc, int BH, int cache_len, int cap,
+                              float scale, void *out, void *ws, cudaStream_t stream) {
+    float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
+    return launch_decode_kernels<T, true>(q, k, v, w, beta, log_f, k_cache, v_cache, gc, BH,
+                                          cache_len, cap, scale, out, part, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -266,21 +387,8 @@ cudaError_t launch_decode_static(const void *q, const void *k, const void *v, co
     cudaError_t err = static_scratch_address(&scratch);
     if (err != cudaSuccess) return err;
     float *part = static_cast<float *>(scratch);
-    const float sl2 = scale * kLog2e;
-    const int used = (cache_len + kDecodeChunk - 1) / kDecodeChunk;
-    if (used > 0) {
-        dim3 grid(used, BH);
-        decode_split_kernel<T><<<grid, kThreads, 0, stream>>>(
-            static_cast<const T *>(q), static_cast<const T *>(w), beta, static_cast<T *>(k_cache),
-            static_cast<const T *>(v_cache), cache_len, cap, used, sl2, part);
-        err = cudaGetLastError();
-        if (err != cudaSuccess) return err;
-    }
-    decode_merge_kernel<T><<<BH, kD, 0, stream>>>(
-        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
-        static_cast<T *>(k_cache), static_cast<T *>(v_cache), cache_len, cap, used, sl2, part,
-        static_cast<T *>(out));
-    return cudaGetLastError();
+    return launch_decode_kernels<T, false>(q, k, v, w, beta, nullptr, k_cache, v_cache, nullptr,
+                                           BH, cache_len, cap, scale, out, part, stream);
 }
 
 template cudaError_t launch_decode_static<float>(const void *, const void *, const void *,
@@ -298,5 +406,13 @@ template cudaError_t launch_decode<__nv_bfloat16>(const void *, const void *, co
                                                   const void *, const float *, void *, void *,
                                                   int, int, int, float, void *, void *,
                                                   cudaStream_t);
+template cudaError_t launch_fox_decode<float>(const void *, const void *, const void *,
+                                              const void *, const float *, const float *, void *,
+                                              void *, float *, int, int, int, float, void *,
+                                              void *, cudaStream_t);
+template cudaError_t launch_fox_decode<__nv_bfloat16>(const void *, const void *, const void *,
+                                                      const void *, const float *, const float *,
+                                                      void *, void *, float *, int, int, int,
+                                                      float, void *, void *, cudaStream_t);
 
 }  // namespace path

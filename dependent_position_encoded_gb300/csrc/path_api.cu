@@ -28,6 +28,11 @@ template <typename T>
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *w,
                           const float *beta, void *k_cache, void *v_cache, int BH, int cache_len,
                           int cap, float scale, void *out, void *ws, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_fox_decode(const void *q, const void *k, const void *v, const void *w,
+                              const float *beta, const float *log_f, void *k_cache,
+                              void *v_cache, float *gc, int BH, int cache_len, int cap,
+                              float scale, void *out, void *ws, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len);
 template <typename T>
@@ -129,6 +134,7 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
         case PATH_OP_FWD: return fwd_layout(B, H, L, elt_bytes(dtype), false).total;
         case PATH_OP_FOX_FWD: return fwd_layout(B, H, L, elt_bytes(dtype), true).total;
         case PATH_OP_DECODE: return decode_ws_bytes(B, H, L);
+        case PATH_OP_FOX_DECODE: return decode_ws_bytes(B, H, L);
         default: return 0;
     }
 }
@@ -219,6 +225,33 @@ path_status path_decode_step(const void *q, const void *k, const void *v, const 
                                                       cache_len, cache_cap, scale, out, ws, s));
     return from_cuda(launch_decode<float>(q, k, v, w, beta, k_cache, v_cache, B * H, cache_len,
                                           cache_cap, scale, out, ws, s));
+}
+
+path_status path_fox_decode_step(const void *q, const void *k, const void *v, const void *w,
+                                 const float *beta, const float *log_f, void *k_cache,
+                                 void *v_cache, float *g_cache, int B, int H, int cache_len,
+                                 int cache_cap, int d, int dtype, float scale, void *out,
+                                 void *ws, size_t ws_bytes, void *stream) {
+    path_status st = check_sizes(B, H, cache_cap, d, dtype);
+    if (st != PATH_OK) return st;
+    if (cache_len < 0) return PATH_ERR_SHAPE;
+    if (!std::isfinite(scale)) return PATH_ERR_ARG;
+    if ((long long)B * H == 0) return PATH_OK;
+    if (cache_len + 1 > cache_cap) return PATH_ERR_CAPACITY;
+    if (!q || !k || !v || !w || !beta || !log_f || !k_cache || !v_cache || !g_cache || !out)
+        return PATH_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(w, 16) ||
+        !aligned(beta, 4) || !aligned(log_f, 4) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(g_cache, 16) || !aligned(out, 16))
+        return PATH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, H, cache_cap))) != PATH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == PATH_BF16)
+        return from_cuda(launch_fox_decode<__nv_bfloat16>(q, k, v, w, beta, log_f, k_cache,
+                                                          v_cache, g_cache, B * H, cache_len,
+                                                          cache_cap, scale, out, ws, s));
+    return from_cuda(launch_fox_decode<float>(q, k, v, w, beta, log_f, k_cache, v_cache, g_cache,
+                                              B * H, cache_len, cache_cap, scale, out, ws, s));
 }
 
 path_status path_decode_step_noalloc(const void *q, const void *k, const void *v, const void *w,

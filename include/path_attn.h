@@ -55,7 +55,12 @@ typedef enum {
 
 typedef enum { PATH_F32 = 0, PATH_BF16 = 1 } path_dtype;
 
-typedef enum { PATH_OP_FWD = 0, PATH_OP_FOX_FWD = 1, PATH_OP_DECODE = 2 } path_op;
+typedef enum {
+    PATH_OP_FWD = 0,
+    PATH_OP_FOX_FWD = 1,
+    PATH_OP_DECODE = 2,
+    PATH_OP_FOX_DECODE = 3
+} path_op;
 
 /* Largest sizes accepted: B*H <= PATH_MAX_HEADS, L <= PATH_MAX_LEN. */
 #define PATH_MAX_HEADS 65535
@@ -154,6 +159,29 @@ path_status path_decode_step(const void *q, const void *k, const void *v, const 
                              const float *beta, void *k_cache, void *v_cache, int B, int H,
                              int cache_len, int cache_cap, int d, int dtype, float scale,
                              void *out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * One PaTH-FoX decode step: path_decode_step with the forget-gate bias of PaTH-FoX
+ * (review "거리에서 경로로, PaTH Attention" §4; technical summary "技術要約: PaTH
+ * Attention" §2 "拡張: PaTH-FoX"): the logit of cached key j gains
+ * sum_{s=j+1..t} log f_s. The cache keeps that sum per key, updated in place like the
+ * keys (review §9; technical summary §3 "推論"):
+ *   g_cache : (B, H, cache_cap) fp32. On entry g_cache[j] (j < cache_len) holds
+ *             sum_{s=j+1..cache_len-1} log f_s, the gate sum from key j to the last
+ *             cached token (0 for the last one).
+ *   log_f   : (B, H) fp32, the new token's log forget gate (any finite value).
+ *   1. k_j <- H_t k_j and g_j <- g_j + log f_t for every cached j < cache_len;
+ *   2. k_t, v_t are appended untransformed at index cache_len with g = 0;
+ *   3. out = softmax_j(scale * q_t . k_j + g_j) v_j over j <= cache_len.
+ * Other arguments, the results and the error behaviour as path_decode_step; ws must
+ * hold path_workspace_bytes(PATH_OP_FOX_DECODE, B, H, cache_cap, d, dtype) bytes and
+ * g_cache must be 16-byte aligned.
+ */
+path_status path_fox_decode_step(const void *q, const void *k, const void *v, const void *w,
+                                 const float *beta, const float *log_f, void *k_cache,
+                                 void *v_cache, float *g_cache, int B, int H, int cache_len,
+                                 int cache_cap, int d, int dtype, float scale, void *out,
+                                 void *ws, size_t ws_bytes, void *stream);
 
 /*
  * path_decode_step without a workspace, for callers that cannot allocate device memory

@@ -168,7 +168,9 @@ class DecodeCache:
     Kc, Vc: (nh, cap, d) float64; length: number of valid entries.
     """
 
-    def __init__(self, k_prefix, v_prefix, cap, fox=False):
+    def __init__(self, k_prefix, v_prefix, cap, fox=False, g_prefix=None):
+        """g_prefix (nh or (..., n0)): for a PaTH-FoX cache, the per-key gate sums of the
+        prefix keys (sum of log f over positions j+1 .. n0-1); zeros when omitted."""
         k_prefix, v_prefix = _f64(k_prefix), _f64(v_prefix)
         nh = int(np.prod(k_prefix.shape[:-2]))
         n0, d = k_prefix.shape[-2], k_prefix.shape[-1]
@@ -178,6 +180,10 @@ class DecodeCache:
         self.Kc[:, :n0] = k_prefix.reshape(nh, n0, d)
         self.Vc[:, :n0] = v_prefix.reshape(nh, n0, d)
         self.cbias = np.zeros((nh, cap)) if fox else None
+        if g_prefix is not None:
+            if not fox:
+                raise ValueError("g_prefix needs fox=True")
+            self.cbias[:, :n0] = _f64(g_prefix).reshape(nh, n0)
 
     def step(self, q, k, v, w, beta, log_f=None, scale=None):
         """Applies one decode step in place; returns o_t of shape (nh, d)."""

@@ -12,6 +12,13 @@ Recipe (draw order q, k, v, g, z[, u] from one generator per seed):
 q, k, v, w are rounded once to the workload dtype; beta and log f stay fp32
 (bf16 would round a 1.99 clip up to 1.9921875). Consumers use the rounded
 tensors as given; w is not renormalised after rounding.
+
+Decode caches are synthetic cache contents: prefix keys and values ~ N(0, 1)
+(the keys stand for already-transformed cache entries). A PaTH-FoX cache also
+holds per-key gate sums; the synthetic ones are those a gate log f =
+logsigmoid(u), u ~ N(2, 1), at every prefix position leaves behind: the entry of
+key j is the sum of the draws at positions j+1 .. n-1 (fp64, stored fp32), so
+the last key holds 0.
 """
 from dataclasses import dataclass
 
@@ -54,6 +61,8 @@ BF16_L2048 = FwdWorkload("path_fwd_bf16_B4H16L2048", 4, 16, 2048, D, torch.bfloa
 BF16_L4096 = FwdWorkload("path_fwd_bf16_B32H32L4096", 32, 32, 4096, D, torch.bfloat16, 3, BETA_CLIP, False)
 FOX_L16384 = FwdWorkload("path_fox_fwd_bf16_B8H16L16384", 8, 16, 16384, D, torch.bfloat16, 4, BETA_CLIP, True)
 DECODE_32K = DecodeWorkload("path_decode_bf16_B32H32N32768x64", 32, 32, 32768, 64, D, torch.bfloat16, 5, 1000)
+# PaTH-FoX decode: the same cache and steps plus forget gates (prefix gate sums, log f per step).
+FOX_DECODE_32K = DecodeWorkload("path_fox_decode_bf16_B32H32N32768x64", 32, 32, 32768, 64, D, torch.bfloat16, 5, 1000)
 
 SPEED_SWEEP_L = (1024, 2048, 4096, 8192, 16384)
 
@@ -108,6 +117,25 @@ def make_decode_prefix(wl, cap, device="cpu"):
     kc[:, :, :wl.n_prefix] = torch.randn(shape, generator=g, device=device).to(wl.dtype)
     vc[:, :, :wl.n_prefix] = torch.randn(shape, generator=g, device=device).to(wl.dtype)
     return kc, vc
+
+
+def make_fox_decode_prefix(wl, cap, device="cpu"):
+    """(k_cache, v_cache, g_cache): make_decode_prefix's caches (same draws) plus the gate
+    sums (B, H, cap) fp32 of the n_prefix cached keys (see the module recipe)."""
+    g = _gen(wl.seed, device)
+    shape = (wl.B, wl.H, wl.n_prefix, wl.d)
+    kc = torch.zeros((wl.B, wl.H, cap, wl.d), device=device, dtype=wl.dtype)
+    vc = torch.zeros_like(kc)
+    kc[:, :, :wl.n_prefix] = torch.randn(shape, generator=g, device=device).to(wl.dtype)
+    vc[:, :, :wl.n_prefix] = torch.randn(shape, generator=g, device=device).to(wl.dtype)
+    u = torch.randn((wl.B, wl.H, wl.n_prefix), generator=g, device=device) + 2.0
+    draws = torch.nn.functional.logsigmoid(u).double()
+    gc = torch.zeros((wl.B, wl.H, cap), device=device, dtype=torch.float32)
+    if wl.n_prefix > 0:
+        # entry j: draws at positions j+1 .. n-1 (a suffix sum shifted by one)
+        tail = torch.flip(torch.cumsum(torch.flip(draws, [-1]), -1), [-1])
+        gc[:, :, :wl.n_prefix - 1] = tail[:, :, 1:].float()
+    return kc, vc, gc
 
 
 def make_decode_step(wl, t, device="cpu", fox=False, B=None, H=None):

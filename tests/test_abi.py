@@ -117,6 +117,30 @@ def test_decode_argument_checks(so):
     assert call(B=0) == 0
 
 
+def test_fox_decode_argument_checks(so, lib):
+    # every case below is rejected before any launch (fake pointers are never used)
+    def call(**kw):
+        a = dict(B=1, H=1, cache_len=10, cap=16, d=64, dtype=1, ws_bytes=1 << 20, kc=FAKE,
+                 lf=FAKE, gc=FAKE)
+        a.update(kw)
+        return so.path_fox_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, a["lf"], a["kc"], FAKE,
+                                       a["gc"], a["B"], a["H"], a["cache_len"], a["cap"], a["d"],
+                                       a["dtype"], ctypes.c_float(0.125), FAKE, FAKE,
+                                       ctypes.c_size_t(a["ws_bytes"]), None)
+    assert call(cache_len=16) == 6
+    assert call(cache_len=-1) == 2
+    assert call(d=128) == 2
+    assert call(dtype=5) == 3
+    assert call(lf=None) == 1
+    assert call(gc=None) == 1
+    assert call(gc=FAKE + 4) == 4
+    assert call(lf=FAKE + 2) == 4
+    assert call(ws_bytes=8) == 5
+    assert call(B=0) == 0
+    assert lib.path_workspace_bytes(lib.OP_FOX_DECODE, 2, 2, 2048, 64, lib.BF16) == \
+        lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 64, lib.BF16)
+
+
 def test_noalloc_decode_rejects_problems_beyond_the_fixed_scratch(so):
     # 4096 heads x 17 splits of 1024 keys x 264 B = 18.4 MB > 16 MiB: refused before any
     # launch. The size is checked here first so that these never-dereferenced pointers

@@ -47,3 +47,17 @@ def test_sample_rows_in_range():
     r = pi.sample_rows(10, 300, 50, seed=3)
     assert r.shape[1] == 2 and r[:, 0].max() < 10 and r[:, 1].max() < 300
     assert 0 in r[:, 1] and 299 in r[:, 1]
+
+
+def test_fox_decode_prefix_gate_sums():
+    wl = pi.DecodeWorkload("t", 2, 3, 50, 1, 64, torch.bfloat16, 7, 100)
+    kc, vc = pi.make_decode_prefix(wl, 60)
+    kf, vf, gc = pi.make_fox_decode_prefix(wl, 60)
+    # same key/value draws as the plain decode cache
+    assert torch.equal(kc, kf) and torch.equal(vc, vf)
+    assert gc.dtype == torch.float32 and gc.shape == (2, 3, 60)
+    # the last cached key carries no gate, earlier keys ever more negative sums, and the
+    # slots past the prefix are zero
+    assert torch.all(gc[:, :, 49:] == 0)
+    step = gc[:, :, :48] - gc[:, :, 1:49]
+    assert torch.all(step < 0) and torch.all(step > -10)

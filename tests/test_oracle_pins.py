@@ -277,6 +277,33 @@ def test_decode_from_empty_cache_matches_prefill(fox):
     np.testing.assert_allclose(cache.Kc[1, j], P.T @ k[1, j], atol=1e-12)
 
 
+def test_fox_decode_from_prefill_state_matches_prefill():
+    # A PaTH-FoX cache built from a prefix of n0 tokens holds the keys transported to the
+    # prefix's last position and, per key j, the gate sum over positions j+1 .. n0-1.
+    # Built here from explicit d x d products and plain sums, then stepped by the oracle,
+    # it must give the prefill rows n0 .. T-1.
+    rng = np.random.default_rng(29)
+    nh, T, n0, d = 2, 30, 17, 8
+    q, k, v, g = (rng.standard_normal((nh, T, d)) for _ in range(4))
+    w = g / np.linalg.norm(g, axis=-1, keepdims=True)
+    beta = rng.uniform(0, 2, size=(nh, T))
+    log_f = np.log(rng.uniform(0.2, 1.0, size=(nh, T)))
+    ref, _ = oracle.path_fwd(q, k, v, w, beta, log_f=log_f)
+    kp = np.empty((nh, n0, d))
+    gp = np.empty((nh, n0))
+    for h in range(nh):
+        for j in range(n0):
+            P = np.eye(d)
+            for s in range(j + 1, n0):
+                P = P @ householder(w[h, s], beta[h, s])
+            kp[h, j] = P.T @ k[h, j]
+            gp[h, j] = sum(log_f[h, s] for s in range(j + 1, n0))
+    cache = oracle.DecodeCache(kp, v[:, :n0], cap=T, fox=True, g_prefix=gp)
+    for t in range(n0, T):
+        o = cache.step(q[:, t], k[:, t], v[:, t], w[:, t], beta[:, t], log_f=log_f[:, t])
+        np.testing.assert_allclose(o, ref[:, t], atol=1e-12, rtol=0)
+
+
 def test_sampled_rows_match_full_forward():
     rng = np.random.default_rng(23)
     B, H, L, d = 2, 3, 70, 8

@@ -434,6 +434,125 @@ def test_decode_workload_sampled_heads(lib):
     assert max(rel) <= 5e-2, rel
 
 
+# ---------------------------------------------------------------- PaTH-FoX decode
+
+def _fox_decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None):
+    wl = pi.DecodeWorkload("t", B, H, n0, steps, 64, dtype, seed, 1000 + seed)
+    cap = n0 + steps
+    kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device="cuda")
+    heads = list(range(B * H)) if check_heads is None else check_heads
+    ocache = oracle.DecodeCache(kc.reshape(B * H, cap, 64)[heads, :n0].cpu(),
+                                vc.reshape(B * H, cap, 64)[heads, :n0].cpu(), cap, fox=True,
+                                g_prefix=gc.reshape(B * H, cap)[heads, :n0].cpu())
+    ws = lib.new_workspace(lib.OP_FOX_DECODE, B, H, cap,
+                           lib.BF16 if dtype == torch.bfloat16 else lib.F32, "cuda")
+    worst = 0.0
+    for t in range(steps):
+        s = pi.make_decode_step(wl, t, device="cuda", fox=True)
+        pre_g = gc.reshape(B * H, cap)[heads, :n0 + t].double().cpu().numpy()
+        o = lib.path_fox_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"],
+                                     kc, vc, gc, n0 + t, workspace=ws)
+        sel = {k: v.reshape(B * H, -1)[heads].cpu() for k, v in s.items()}
+        ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          log_f=sel["log_f"])
+        got = o.reshape(B * H, 64)[heads].double().cpu().numpy()
+        worst = max(worst, np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+        if dtype == torch.bfloat16:
+            assert np.abs(got - ref).max() <= BF16_MAX_ABS
+        # gate sums: one fp32 addition of log f_t to the stored value, and 0 appended
+        post_g = gc.reshape(B * H, cap)[heads, :n0 + t + 1].double().cpu().numpy()
+        lf = sel["log_f"].double().numpy().reshape(-1, 1)
+        expect = (pre_g + lf).astype(np.float32).astype(np.float64)
+        assert np.all(np.abs(post_g[:, :n0 + t] - expect) <= np.abs(expect) * 2.0 ** -23 + 1e-30)
+        assert np.all(post_g[:, n0 + t] == 0)
+        # and they stay within fp32 rounding of the oracle's fp64 sums
+        assert np.allclose(post_g, ocache.cbias[:, :n0 + t + 1], rtol=1e-5, atol=1e-5)
+    return worst
+
+
+def test_fox_decode_small_fp32(lib):
+    worst = _fox_decode_run(lib, 2, 3, 200, 12, torch.float32, seed=11)
+    assert worst <= F32_MAX_REL
+
+
+def test_fox_decode_bf16_from_empty_and_across_splits(lib):
+    _fox_decode_run(lib, 1, 2, 0, 5, torch.bfloat16, seed=12)
+    worst = _fox_decode_run(lib, 2, 2, 1021, 6, torch.bfloat16, seed=13)
+    assert worst <= 5e-2
+
+
+def test_fox_decode_zero_gate_equals_path_decode(lib):
+    # log f = 0 leaves every gate sum at 0 and adds nothing to a logit: the PaTH step, with
+    # the same keys bit for bit (the softmax partial sums run in another order, so the
+    # outputs agree to rounding)
+    wl = pi.DecodeWorkload("t", 2, 2, 1500, 3, 64, torch.bfloat16, 14, 1014)
+    cap = wl.n_prefix + wl.steps
+    kc, vc = pi.make_decode_prefix(wl, cap, device="cuda")
+    kf, vf = kc.clone(), vc.clone()
+    gc = torch.zeros((2, 2, cap), dtype=torch.float32, device="cuda")
+    for t in range(wl.steps):
+        s = pi.make_decode_step(wl, t, device="cuda")
+        zero = torch.zeros_like(s["beta"])
+        a = lib.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
+                                 wl.n_prefix + t)
+        b = lib.path_fox_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], zero, kf, vf,
+                                     gc, wl.n_prefix + t)
+        assert (a.float() - b.float()).abs().max().item() <= 2.0 ** -7 * a.float().abs().max().item()
+    assert torch.equal(kc, kf) and torch.equal(vc, vf)
+    assert torch.count_nonzero(gc) == 0
+
+
+@pytest.mark.parametrize("kind", ["strong", "mixed_sign"])
+def test_fox_decode_vanishing_keys(lib, kind):
+    # strong gates: all but the last few dozen keys weigh below 2^-64 and skip their value
+    # rows; mixed-sign gates (log f ~ N(0, 2), so older keys can gain weight): the skip rule
+    # still holds because the new key's own logit bounds the row maximum from below
+    B, H, n0, steps = 1, 3, 3000, 4
+    wl = pi.DecodeWorkload("t", B, H, n0, steps, 64, torch.bfloat16, 15, 1015)
+    cap = n0 + steps
+    kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(99)
+    if kind == "strong":
+        gc[:, :, :n0] *= 20.0
+        lf_scale, lf_shift = 1.0, -3.0
+    else:
+        gc[:, :, :n0] = torch.cumsum(2.0 * torch.randn((B, H, n0), generator=g, device="cuda"), -1)
+        gc[:, :, :n0] -= gc[:, :, n0 - 1:n0].clone()
+        lf_scale, lf_shift = 2.0, 0.0
+    ocache = oracle.DecodeCache(kc[:, :, :n0].cpu(), vc[:, :, :n0].cpu(), cap, fox=True,
+                                g_prefix=gc[:, :, :n0].cpu())
+    for t in range(steps):
+        s = pi.make_decode_step(wl, t, device="cuda", fox=True)
+        s["log_f"] = (lf_scale * torch.randn((B, H, 1), generator=g, device="cuda") + lf_shift)
+        o = lib.path_fox_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"],
+                                     s["log_f"].contiguous(), kc, vc, gc, n0 + t)
+        ref = ocache.step(s["q"].cpu(), s["k"].cpu(), s["v"].cpu(), s["w"].cpu(),
+                          s["beta"].cpu(), log_f=s["log_f"].cpu())
+        check_bf16(o.reshape(B * H, 64), ref)
+
+
+def test_fox_decode_workload_sampled_heads(lib):
+    wl = pi.FOX_DECODE_32K
+    cap = wl.n_prefix + wl.steps
+    kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device="cuda")
+    heads = [0, 301, 1023]
+    nh = wl.B * wl.H
+    ocache = oracle.DecodeCache(kc.reshape(nh, cap, 64)[heads, :wl.n_prefix].cpu(),
+                                vc.reshape(nh, cap, 64)[heads, :wl.n_prefix].cpu(), cap,
+                                fox=True, g_prefix=gc.reshape(nh, cap)[heads, :wl.n_prefix].cpu())
+    ws = lib.new_workspace(lib.OP_FOX_DECODE, wl.B, wl.H, cap, lib.BF16, "cuda")
+    for t in range(wl.steps):
+        s = pi.make_decode_step(wl, t, device="cuda", fox=True)
+        o = lib.path_fox_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"],
+                                     kc, vc, gc, wl.n_prefix + t, workspace=ws)
+        sel = {k: v.reshape(nh, -1)[heads].cpu() for k, v in s.items()}
+        ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          log_f=sel["log_f"])
+        if t % 8 == 7 or t == 0:
+            got = o.reshape(nh, 64)[heads].double().cpu().numpy()
+            assert np.abs(got - ref).max() <= BF16_MAX_ABS
+
+
 def test_decode_capacity_error(lib):
     kc = torch.zeros((1, 1, 4, 64), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
