@@ -15,8 +15,10 @@
 // products of the UT form (sub-blocks of A invert the matching sub-blocks of T).
 //
 // (I + E)^{-1} is formed blockwise: the four 16 x 16 diagonal blocks by back-substitution,
-// then X12 = -X11 E12 X22 for the 16-blocks and for the 32-blocks (fp32). Every factor is
-// bounded (X_su = A_su / beta_u), so no intermediate grows.
+// then X12 = -X11 E12 X22 for the 16-blocks and for the 32-blocks, each 16 x 8 output tile
+// one warp's mma.sync over tf32 head/tail splits (fp32 accuracy; these products are too
+// small for tcgen05, and the fragment loads keep shared-memory traffic low). Every factor
+// is bounded (X_su = A_su / beta_u), so no intermediate grows.
 //
 // tcgen05.mma groups, all M = 128, with 64x64 16-bit tiles in 128-byte-swizzled shared
 // memory (K-major tiles stacked in M must be adjacent; MN-major atoms use the LBO stride):
@@ -26,16 +28,17 @@
 //                 Q x K^T (bf16) - Lq x Khat^T (fp16), one accumulator -> diag logits
 //   MMA4y (fp16): [W^T; Rk] x V'             -> W^T V'          /  Rk V'
 // Second-level operands are fp16 (11-bit significand; all bounded, |A_su| <= 4), fp32
-// accumulation. One CTA of 128 threads per (block, head), thread r owns TMEM lane r,
-// thread 0 issues the TMA loads and the MMAs. 128 TMEM columns and 64 KB of tiles, so
-// three CTAs share an SM.
+// accumulation. One CTA of 256 threads per (block, head): warps w and w + 4 read the same
+// 32 TMEM lanes (rows) and split every 64-column epilogue into halves, thread 0 issues
+// the TMA loads and the MMAs. 128 TMEM columns, 64 KB of tiles and 80 registers per
+// thread, so three CTAs (24 warps) share an SM.
 #include "common.cuh"
 
 namespace path {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr uint32_t kT = 8192;  // one 64 x 64 16-bit tile
 
 // Tile slots (from the 1024-aligned base). Q, W, K adjacent (MMA1 A = [Q; W], B = [W; K]);
@@ -45,7 +48,7 @@ constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_RKT = 3 * kT, T_L
 constexpr uint32_t SCR = 5 * kT;           // solve scratch (E/X fp32 + Y) overlays slots 5-7
 constexpr int XLD = 68;
 constexpr uint32_t Y_OFF = SCR + 64 * XLD * 4;
-constexpr int YLD = 36;
+constexpr int YLD = 40;  // B-fragment loads of Y (rows t, columns g) hit 32 banks
 constexpr uint32_t BAR_OFF = 8 * kT;       // 2 mbarriers
 constexpr uint32_t SLOT_OFF = BAR_OFF + 16;
 constexpr uint32_t BETA_OFF = SLOT_OFF + 16;
@@ -68,11 +71,12 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Writes 64 fp32 values as one 16-bit row (fp16 or bf16) of a swizzled tile.
+// Writes 32 fp32 values as half `hf` (16-bit columns 32hf .. 32hf+31, fp16 or bf16) of
+// row `row` of a swizzled tile.
 template <bool HALF>
-__device__ __forceinline__ void store_row16(uint8_t *tile, int row, const float *x) {
+__device__ __forceinline__ void store_half16(uint8_t *tile, int row, int hf, const float *x) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
         uint4 u;
         const float *s = x + 8 * c;
         if (HALF) {
@@ -82,15 +86,15 @@ __device__ __forceinline__ void store_row16(uint8_t *tile, int row, const float 
             u.x = pack_bf16x2(s[0], s[1]); u.y = pack_bf16x2(s[2], s[3]);
             u.z = pack_bf16x2(s[4], s[5]); u.w = pack_bf16x2(s[6], s[7]);
         }
-        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c)) = u;
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, 4 * hf + c)) = u;
     }
 }
 
-// Reads one bf16 row of a swizzled tile as 64 fp32 values.
-__device__ __forceinline__ void load_row_bf16(const uint8_t *tile, int row, float *x) {
+// Reads half `hf` of one bf16 row of a swizzled tile as 32 fp32 values.
+__device__ __forceinline__ void load_half_bf16(const uint8_t *tile, int row, int hf, float *x) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_offset(row, c));
+    for (int c = 0; c < 4; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_offset(row, 4 * hf + c));
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -101,32 +105,70 @@ __device__ __forceinline__ void load_row_bf16(const uint8_t *tile, int row, floa
     }
 }
 
-// 64 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_row64(uint32_t taddr, float *x) {
-    uint32_t a[32], b[32];
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_row32(uint32_t taddr, float *x) {
+    uint32_t a[32];
     tmem_ld32(taddr, a);
-    tmem_ld32(taddr + 32, b);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        x[j] = __uint_as_float(a[j]);
-        x[32 + j] = __uint_as_float(b[j]);
-    }
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(a[j]);
 }
 
-__device__ __forceinline__ void store_global_row(__nv_bfloat16 *dst, const float *y) {
+// 32 fp32 values as 64 contiguous bytes of bf16 in global memory.
+__device__ __forceinline__ void store_global_half(__nv_bfloat16 *dst, const float *y) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
+    for (int c = 0; c < 4; ++c)
         d[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]), pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
                           pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
                           pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
 }
 
+// fp32 split into a tf32 head and a tf32 tail: head + tail carries about 21 significant
+// bits, so the three products head*head + head*tail + tail*head keep fp32-level accuracy.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float rest = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(rest));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// One warp: the 16 x 8 tile acc = A (16 x K, row-major, stride lda) x B (K x 8, row-major,
+// stride ldb) in fp32 accuracy on the tensor cores (three tf32 products per k-step).
+// Fragment layout of m16n8k8: g = lane / 4, t = lane % 4; A rows g, g + 8 and columns
+// t, t + 4; B rows t, t + 4 and column g; acc rows g (0, 1), g + 8 (2, 3), columns 2t, 2t + 1.
+template <int K>
+__device__ __forceinline__ void warp_tile_16x8(const float *A, int lda, const float *B, int ldb,
+                                               int lane, float (&acc)[4]) {
+    const int g = lane >> 2, t = lane & 3;
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(A[g * lda + k0 + t], ah[0], al[0]);
+        split_tf32(A[(g + 8) * lda + k0 + t], ah[1], al[1]);
+        split_tf32(A[g * lda + k0 + t + 4], ah[2], al[2]);
+        split_tf32(A[(g + 8) * lda + k0 + t + 4], ah[3], al[3]);
+        split_tf32(B[(k0 + t) * ldb + g], bh[0], bl[0]);
+        split_tf32(B[(k0 + t + 4) * ldb + g], bh[1], bl[1]);
+        mma_tf32(acc, al, bh);
+        mma_tf32(acc, ah, bl);
+        mma_tf32(acc, ah, bh);
+    }
+}
+
 // (I + E)^{-1} in place over E (upper triangle; E is zero on and below the diagonal),
-// all 128 threads. On return X[s][u] (s <= u) holds the inverse.
+// all 256 threads. On return X[s][u] (s <= u) holds the inverse.
 __device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, int r) {
-    // level 0: the four 16 x 16 diagonal blocks, one column per thread
+    // level 0: the four 16 x 16 diagonal blocks, one column per thread (threads 0-63)
     float x[16];
     const int u = r & 63, b0 = (u >> 4) << 4, lu = u & 15;
     if (r < 64) {
@@ -144,69 +186,47 @@ __device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, i
         for (int l = 0; l < 16; ++l) X[(b0 + l) * XLD + u] = x[l];
     }
     __syncthreads();
-    // level 1: X[16p', 16p'+16..] = -X11 E12 X22 for the two 32-blocks p
-    {
-        const int p = r >> 6, q = r & 63, i = q >> 2, c0 = (q & 3) * 4;
-        const int o = 32 * p;
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float e = X[(o + i) * XLD + o + 16 + m];
-            const float4 xr = *reinterpret_cast<const float4 *>(X + (o + 16 + m) * XLD + o + 16 + c0);
-            y[0] = fmaf(e, xr.x, y[0]); y[1] = fmaf(e, xr.y, y[1]);
-            y[2] = fmaf(e, xr.z, y[2]); y[3] = fmaf(e, xr.w, y[3]);
-        }
-        *reinterpret_cast<float4 *>(Y + (16 * p + i) * YLD + c0) = make_float4(y[0], y[1], y[2], y[3]);
-        __syncthreads();
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float xv = X[(o + i) * XLD + o + m];
-            const float4 yr = *reinterpret_cast<const float4 *>(Y + (16 * p + m) * YLD + c0);
-            z[0] = fmaf(xv, yr.x, z[0]); z[1] = fmaf(xv, yr.y, z[1]);
-            z[2] = fmaf(xv, yr.z, z[2]); z[3] = fmaf(xv, yr.w, z[3]);
-        }
-        *reinterpret_cast<float4 *>(X + (o + i) * XLD + o + 16 + c0) =
-            make_float4(-z[0], -z[1], -z[2], -z[3]);
+    const int warp = r >> 5, lane = r & 31, g = lane >> 2, t = lane & 3;
+    float acc[4];
+    // level 1: X[o:o+16, o+16:o+32] = -X11 E12 X22 for the two 32-blocks (o = 0, 32);
+    // warps 0-3, warp = (block p, 8-column tile n)
+    if (warp < 4) {
+        const int o = 32 * (warp >> 1), n0 = 8 * (warp & 1);
+        warp_tile_16x8<16>(X + o * XLD + o + 16, XLD, X + (o + 16) * XLD + o + 16 + n0, XLD,
+                           lane, acc);
+        float *y = Y + (o >> 1) * YLD + n0;  // rows 16 p .. 16 p + 15 of Y
+        *reinterpret_cast<float2 *>(y + g * YLD + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2 *>(y + (g + 8) * YLD + 2 * t) = make_float2(acc[2], acc[3]);
     }
     __syncthreads();
-    // level 2: X[0:32, 32:64] = -X[0:32, 0:32] E[0:32, 32:64] X[32:64, 32:64]
+    if (warp < 4) {
+        const int o = 32 * (warp >> 1), n0 = 8 * (warp & 1);
+        warp_tile_16x8<16>(X + o * XLD + o, XLD, Y + (o >> 1) * YLD + n0, YLD, lane, acc);
+        float *x12 = X + o * XLD + o + 16 + n0;
+        *reinterpret_cast<float2 *>(x12 + g * XLD + 2 * t) = make_float2(-acc[0], -acc[1]);
+        *reinterpret_cast<float2 *>(x12 + (g + 8) * XLD + 2 * t) = make_float2(-acc[2], -acc[3]);
+    }
+    __syncthreads();
+    // level 2: X[0:32, 32:64] = -X[0:32, 0:32] E[0:32, 32:64] X[32:64, 32:64];
+    // warp = (16-row tile m, 8-column tile n)
     {
-        const int i = r >> 2, c0 = (r & 3) * 8;
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < 32; ++m) {
-            const float e = X[i * XLD + 32 + m];
-            const float4 a = *reinterpret_cast<const float4 *>(X + (32 + m) * XLD + 32 + c0);
-            const float4 b = *reinterpret_cast<const float4 *>(X + (32 + m) * XLD + 36 + c0);
-            y[0] = fmaf(e, a.x, y[0]); y[1] = fmaf(e, a.y, y[1]);
-            y[2] = fmaf(e, a.z, y[2]); y[3] = fmaf(e, a.w, y[3]);
-            y[4] = fmaf(e, b.x, y[4]); y[5] = fmaf(e, b.y, y[5]);
-            y[6] = fmaf(e, b.z, y[6]); y[7] = fmaf(e, b.w, y[7]);
-        }
-        *reinterpret_cast<float4 *>(Y + i * YLD + c0) = make_float4(y[0], y[1], y[2], y[3]);
-        *reinterpret_cast<float4 *>(Y + i * YLD + c0 + 4) = make_float4(y[4], y[5], y[6], y[7]);
+        const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
+        warp_tile_16x8<32>(X + m0 * XLD + 32, XLD, X + 32 * XLD + 32 + n0, XLD, lane, acc);
+        float *y = Y + m0 * YLD + n0;
+        *reinterpret_cast<float2 *>(y + g * YLD + 2 * t) = make_float2(acc[0], acc[1]);
+        *reinterpret_cast<float2 *>(y + (g + 8) * YLD + 2 * t) = make_float2(acc[2], acc[3]);
         __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < 32; ++m) {
-            const float xv = X[i * XLD + m];
-            const float4 a = *reinterpret_cast<const float4 *>(Y + m * YLD + c0);
-            const float4 b = *reinterpret_cast<const float4 *>(Y + m * YLD + c0 + 4);
-            y[0] = fmaf(xv, a.x, y[0]); y[1] = fmaf(xv, a.y, y[1]);
-            y[2] = fmaf(xv, a.z, y[2]); y[3] = fmaf(xv, a.w, y[3]);
-            y[4] = fmaf(xv, b.x, y[4]); y[5] = fmaf(xv, b.y, y[5]);
-            y[6] = fmaf(xv, b.z, y[6]); y[7] = fmaf(xv, b.w, y[7]);
-        }
-        *reinterpret_cast<float4 *>(X + i * XLD + 32 + c0) = make_float4(-y[0], -y[1], -y[2], -y[3]);
-        *reinterpret_cast<float4 *>(X + i * XLD + 36 + c0) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+        warp_tile_16x8<32>(X + m0 * XLD, XLD, Y + n0, YLD, lane, acc);
+        float *x12 = X + m0 * XLD + 32 + n0;
+        *reinterpret_cast<float2 *>(x12 + g * XLD + 2 * t) = make_float2(-acc[0], -acc[1]);
+        *reinterpret_cast<float2 *>(x12 + (g + 8) * XLD + 2 * t) = make_float2(-acc[2], -acc[3]);
     }
     __syncthreads();
 }
 
+// Thread layout: warp w reads TMEM lanes 32 (w mod 4) .. +31 (the accumulator rows lr) and
+// handles the 32-column half hf = w / 4 of every 64-column block of its row, so each row's
+// epilogue is split between two warps.
 __global__ void __launch_bounds__(kThreads, 3)
 ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -225,7 +245,10 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + SLOT_OFF);
     const uint32_t bar_tma = base + BAR_OFF, bar_mma = base + BAR_OFF + 8;
 
-    const int r = threadIdx.x, warp = r >> 5;
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int qd = warp & 3, hf = warp >> 2;
+    const int lr = 32 * qd + lane;  // accumulator row (TMEM lane) of this thread
+    const int c0 = 32 * hf;         // first column of this thread's half
     const int blk = blockIdx.x, bh = blockIdx.y;
     const int t0 = blk * kC;
     const size_t head = (size_t)bh * L;
@@ -270,19 +293,24 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
 
-    // bounded wait used by every thread; a timeout skips the remaining work
+    // bounded wait of the whole CTA: thread 0 polls the barrier and the others wait at
+    // __syncthreads (polling by every thread would load the shared-memory pipe that the
+    // other CTAs on the SM are using); a timeout skips the remaining work
     auto wait_all = [&](uint32_t bar, uint32_t par) {
-        bool ok = mbar_try_wait(bar, par);
-        if (!ok) {
-            const uint64_t tstart = cycles_now();
-            while (!(ok = mbar_try_wait(bar, par)) && cycles_now() - tstart < ns_to_cycles(limit_ns)) {
+        if (r == 0) {
+            bool ok = mbar_try_wait(bar, par);
+            if (!ok) {
+                const uint64_t tstart = cycles_now();
+                while (!(ok = mbar_try_wait(bar, par)) &&
+                       cycles_now() - tstart < ns_to_cycles(limit_ns)) {
+                }
             }
-        }
-        if (!ok) {
-            report_status(status, kStatusTimeout);
-            abort_s = 1u;
+            if (!ok) {
+                report_status(status, kStatusTimeout);
+                abort_s = 1u;
+            }
         }
         __syncthreads();
         return abort_s == 0u;
@@ -309,38 +337,40 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = wait_all(bar_mma, 0);  // (its barrier also publishes bs)
     if (ok) {
         tc_fence_after();
-        float x[64];
-        if (r < kC) {
+        float x[32];
+        if (lr < kC) {
+            const int i = lr;
             // row i of Q W^T -> Lq (u <= i), fp16
-            tmem_row64(tmem + lane_off, x);
+            tmem_row32(tmem + lane_off + c0, x);
 #pragma unroll
-            for (int u = 0; u < 64; ++u)
-                if (u > r) x[u] = 0.f;
-            store_row16<true>(sm + T_LQ, r, x);
+            for (int u = 0; u < 32; ++u)
+                if (c0 + u > i) x[u] = 0.f;
+            store_half16<true>(sm + T_LQ, i, hf, x);
+            // W to fp16 in place (MMA1 has completed; later MMAs take fp16 operands)
+            load_half_bf16(sm + T_W, i, hf, x);
+            store_half16<true>(sm + T_W, i, hf, x);
         } else {
-            const int s = r - kC;
+            const int s = lr - kC;
             // row s of W W^T -> E = beta_s G[s][v] for v > s (fp32 scratch)
-            tmem_row64(tmem + lane_off, x);
+            tmem_row32(tmem + lane_off + c0, x);
             const float bsv = bs[s];
 #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4) {
+            for (int q4 = 0; q4 < 8; ++q4) {
                 float e[4];
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4) {
-                    const int v = 4 * q4 + e4;
-                    e[e4] = (v > s) ? bsv * x[v] : 0.f;
+                    const int v = c0 + 4 * q4 + e4;
+                    e[e4] = (v > s) ? bsv * x[4 * q4 + e4] : 0.f;
                 }
-                *reinterpret_cast<float4 *>(X + s * XLD + 4 * q4) = make_float4(e[0], e[1], e[2], e[3]);
+                *reinterpret_cast<float4 *>(X + s * XLD + c0 + 4 * q4) =
+                    make_float4(e[0], e[1], e[2], e[3]);
             }
             // row s of W K^T -> Rk^T (s > j), fp16
-            tmem_row64(tmem + lane_off + 64, x);
+            tmem_row32(tmem + lane_off + 64 + c0, x);
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                if (s <= j) x[j] = 0.f;
-            store_row16<true>(sm + T_RKT, s, x);
-            // W to fp16 in place (MMA1 has completed; later MMAs take fp16 operands)
-            load_row_bf16(sm + T_W, s, x);
-            store_row16<true>(sm + T_W, s, x);
+            for (int j = 0; j < 32; ++j)
+                if (s <= c0 + j) x[j] = 0.f;
+            store_half16<true>(sm + T_RKT, s, hf, x);
         }
     }
     __syncthreads();
@@ -348,28 +378,29 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---- A = (I + E)^{-1} D, then A (rows s) and A^T (rows u) as fp16 tiles
     if (ok) {
         blocked_unit_upper_inverse(X, Y, r);
-        float a[64];
-        if (r < kC) {
-            const int s = r;   // row s: A[s][u] = X[s][u] beta_u, u >= s
+        float a[32];
+        if (lr < kC) {
+            const int s = lr;  // row s: A[s][u] = X[s][u] beta_u, u >= s
 #pragma unroll
-            for (int u4 = 0; u4 < 16; ++u4) {
-                const float4 xv = *reinterpret_cast<const float4 *>(X + s * XLD + 4 * u4);
-                const float4 bv = *reinterpret_cast<const float4 *>(bs + 4 * u4);
-                const int u = 4 * u4;
-                a[u] = (u >= s) ? xv.x * bv.x : 0.f;
-                a[u + 1] = (u + 1 >= s) ? xv.y * bv.y : 0.f;
-                a[u + 2] = (u + 2 >= s) ? xv.z * bv.z : 0.f;
-                a[u + 3] = (u + 3 >= s) ? xv.w * bv.w : 0.f;
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const int u = c0 + 4 * u4;
+                const float4 xv = *reinterpret_cast<const float4 *>(X + s * XLD + u);
+                const float4 bv = *reinterpret_cast<const float4 *>(bs + u);
+                a[4 * u4] = (u >= s) ? xv.x * bv.x : 0.f;
+                a[4 * u4 + 1] = (u + 1 >= s) ? xv.y * bv.y : 0.f;
+                a[4 * u4 + 2] = (u + 2 >= s) ? xv.z * bv.z : 0.f;
+                a[4 * u4 + 3] = (u + 3 >= s) ? xv.w * bv.w : 0.f;
             }
         } else {
-            const int u = r - kC;  // column u: A[s][u], s <= u
+            const int u = lr - kC;  // column u: A[s][u], s <= u
             const float bu = bs[u];
 #pragma unroll
-            for (int s2 = 0; s2 < 64; ++s2) a[s2] = (s2 <= u) ? X[s2 * XLD + u] * bu : 0.f;
+            for (int s2 = 0; s2 < 32; ++s2)
+                a[s2] = (c0 + s2 <= u) ? X[(c0 + s2) * XLD + u] * bu : 0.f;
         }
         __syncthreads();  // the scratch overlays the A tiles
-        if (r < kC) store_row16<true>(sm + T_A, r, a);
-        else store_row16<true>(sm + T_AT, r - kC, a);
+        if (lr < kC) store_half16<true>(sm + T_A, lr, hf, a);
+        else store_half16<true>(sm + T_AT, lr - kC, hf, a);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -388,15 +419,15 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) ok = wait_all(bar_mma, 1);
     if (ok) {
         tc_fence_after();
-        float x[64];
-        if (r < kC) {
-            tmem_row64(tmem + lane_off, x);       // U row u
-            store_row16<true>(sm + T_U, r, x);
-            tmem_row64(tmem + lane_off + 64, x);  // Khat^T row u
-            store_row16<true>(sm + T_KHT, r, x);
+        float x[32];
+        if (lr < kC) {
+            tmem_row32(tmem + lane_off + c0, x);       // U row u
+            store_half16<true>(sm + T_U, lr, hf, x);
+            tmem_row32(tmem + lane_off + 64 + c0, x);  // Khat^T row u
+            store_half16<true>(sm + T_KHT, lr, hf, x);
         } else {
-            tmem_row64(tmem + lane_off, x);       // V' row s
-            store_row16<true>(sm + T_V, r - kC, x);
+            tmem_row32(tmem + lane_off + c0, x);       // V' row s
+            store_half16<true>(sm + T_V, lr - kC, hf, x);
         }
     }
     fence_proxy_async_smem();
@@ -426,32 +457,31 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     const size_t blk_base = (size_t)bh * nblk + blk;
     __nv_bfloat16 *kp_blk = kp + blk_base * (2 * kC) * kD;
-    if (ok && r < kC) {
+    if (ok && lr < kC) {  // warps whose lanes hold rows 0-63; the others have nothing here
         tc_fence_after();
-        const int i = r;
-        float x[64], y[64];
+        const int i = lr;
+        float x[32], y[32];
         // q~_i = q_i - (Lq U)_i
-        load_row_bf16(sm + T_Q, i, y);
-        tmem_row64(tmem + lane_off, x);
+        load_half_bf16(sm + T_Q, i, hf, y);
+        tmem_row32(tmem + lane_off + c0, x);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) y[c] -= x[c];
-        store_global_row(qt + ((size_t)bh * Lp + t0 + i) * kD, y);
+        for (int c = 0; c < 32; ++c) y[c] -= x[c];
+        store_global_half(qt + ((size_t)bh * Lp + t0 + i) * kD + c0, y);
         // diagonal logits, log2 units, j <= i
-        tmem_row64(tmem + lane_off + 64, x);
+        tmem_row32(tmem + lane_off + 64 + c0, x);
         const float lci = (log_f != nullptr) ? lc[i] : 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < 32; ++j) {
+            const int jj = c0 + j;
             float v = scale_log2 * x[j];
-            if (log_f != nullptr) v += kLog2e * (lci - lc[j]);
-            x[j] = (j <= i && t0 + j < L) ? v : -INFINITY;
+            if (log_f != nullptr) v += kLog2e * (lci - lc[jj]);
+            x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
         }
-        uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC);
+        uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < 4; ++c)
             dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
                                pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
-    } else if (ok && warp >= 2) {
-        // warps 2-3: the lanes of MMA4x rows 64..127 hold nothing; keep the warp collective
     }
     tc_fence_before();
     __syncthreads();
@@ -469,21 +499,21 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) ok = wait_all(bar_mma, 1);
     if (ok) {
         tc_fence_after();
-        float x[64];
-        tmem_row64(tmem + lane_off, x);
-        if (r < kC) {
-            // P_b row n = r: delta - (W^T V')_n
+        float x[32];
+        tmem_row32(tmem + lane_off + c0, x);
+        if (lr < kC) {
+            // P_b row n = lr: delta - (W^T V')_n
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = (c == r ? 1.f : 0.f) - x[c];
-            store_global_row(kp_blk + (kC + r) * kD, x);
+            for (int c = 0; c < 32; ++c) x[c] = (c0 + c == lr ? 1.f : 0.f) - x[c];
+            store_global_half(kp_blk + (kC + lr) * kD + c0, x);
         } else {
             // k~_j = k_j - (Rk V')_j
-            const int j = r - kC;
-            float y[64];
-            load_row_bf16(sm + T_K, j, y);
+            const int j = lr - kC;
+            float y[32];
+            load_half_bf16(sm + T_K, j, hf, y);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) y[c] -= x[c];
-            store_global_row(kp_blk + j * kD, y);
+            for (int c = 0; c < 32; ++c) y[c] -= x[c];
+            store_global_half(kp_blk + j * kD + c0, y);
         }
     }
     tc_fence_before();
