@@ -87,8 +87,10 @@ template <> struct Vec<float> {
     }
 };
 
+// FoX holds a batch of key rows in registers; three CTAs per SM keep enough of them in
+// flight (the bound caps it at 80 registers).
 template <typename T, bool FOX>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, FOX ? 3 : 4)
 decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                     const float *__restrict__ beta, T *__restrict__ kc, const T *__restrict__ vc,
                     int cache_len, int cap, int nsplit, float scale_log2, float *__restrict__ part,
@@ -189,7 +191,7 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
         // the key rows of a batch of passes are loaded up front (raw, 16 bytes per lane
         // and pass) to keep enough bytes in flight.
         constexpr int kPasses = 32 / KPW;
-        constexpr int kBatch = kPasses < 8 ? kPasses : 8;
+        constexpr int kBatch = kPasses < 4 ? kPasses : 4;
         for (int rb = j0 + warp * 32; rb < j1; rb += kWarps * 32) {
             const int jl = rb + lane;
             float gl = 0.f;

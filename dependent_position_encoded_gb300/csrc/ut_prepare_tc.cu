@@ -168,16 +168,20 @@ __device__ __forceinline__ void warp_tile_16x8(const float *A, int lda, const fl
 // (I + E)^{-1} in place over E (upper triangle; E is zero on and below the diagonal),
 // all 256 threads. On return X[s][u] (s <= u) holds the inverse.
 __device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, int r) {
-    // level 0: the four 16 x 16 diagonal blocks, one column per thread (threads 0-63)
+    // level 0: the four 16 x 16 diagonal blocks, one column per thread (threads 0-63).
+    // Column u of the inverse solves x_l = -sum_{m>l} E_lm x_m (x_lu = 1, x_l = 0 below);
+    // right-looking: once x_m is final it is folded into the partial sums of every row
+    // above, so the dependent chain is one FMA per row instead of a whole dot product.
     float x[16];
     const int u = r & 63, b0 = (u >> 4) << 4, lu = u & 15;
     if (r < 64) {
 #pragma unroll
-        for (int l = 15; l >= 0; --l) {
-            float acc = 0.f;
+        for (int l = 0; l < 16; ++l) x[l] = 0.f;
 #pragma unroll
-            for (int m = l + 1; m < 16; ++m) acc = fmaf(X[(b0 + l) * XLD + b0 + m], x[m], acc);
-            x[l] = (l == lu) ? 1.f : ((l < lu) ? -acc : 0.f);
+        for (int m = 15; m >= 0; --m) {
+            x[m] = (m == lu) ? 1.f : ((m < lu) ? -x[m] : 0.f);
+#pragma unroll
+            for (int l = 0; l < m; ++l) x[l] = fmaf(X[(b0 + l) * XLD + b0 + m], x[m], x[l]);
         }
     }
     __syncthreads();
