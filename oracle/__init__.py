@@ -47,6 +47,9 @@ def _configure(lib):
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_double, dp]
     lib.oracle_path_decode_step.restype = None
+    lib.oracle_wbeta_produce.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_double] + \
+        [ctypes.c_int] * 6 + [ctypes.c_double, dp, dp]
+    lib.oracle_wbeta_produce.restype = None
     return lib
 
 
@@ -204,3 +207,23 @@ class DecodeCache:
                                         nh, self.length, self.cap, d, float(scale), _ptr(out))
         self.length += 1
         return out
+
+
+def wbeta_produce(x, w_down, w_up, conv, u, bias, beta_max=2.0, eps=1e-12):
+    """The w/beta producer (see path_oracle.c): x (B, L, D), w_down (R, D), w_up (H*d, R),
+    conv (H*d, 3), u (H, D), bias (H,). Returns (w (B, H, L, d), beta (B, H, L)) float64;
+    d is w_up's rows divided by u's rows."""
+    x, w_down, w_up, conv, u, bias = map(_f64, (x, w_down, w_up, conv, u, bias))
+    B, L, D = x.shape
+    R = w_down.shape[0]
+    H = u.shape[0]
+    d = w_up.shape[0] // H
+    if w_down.shape != (R, D) or w_up.shape != (H * d, R) or conv.shape != (H * d, 3) \
+            or u.shape != (H, D) or bias.shape != (H,):
+        raise ValueError("inconsistent producer shapes")
+    w = np.empty((B, H, L, d))
+    beta = np.empty((B, H, L))
+    _load().oracle_wbeta_produce(_ptr(x), _ptr(w_down), _ptr(w_up), _ptr(conv), _ptr(u),
+                                 _ptr(bias), float(beta_max), B, L, D, R, H, d, float(eps),
+                                 _ptr(w), _ptr(beta))
+    return w, beta

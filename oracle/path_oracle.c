@@ -279,3 +279,74 @@ void oracle_path_decode_step(const double *q, const double *k, const double *v,
     free(logit);
     free(p);
 }
+
+/*
+ * Producer of w and beta from the token activations ([KO] §3: a low-dimensional linear
+ * projection and a short convolution of size 3 give w, which is then L2-normalised, and
+ * beta is 2 sigmoid; [JA] §2: beta_s = 2 sigmoid(u^T x_s + b); [JA] §6: beta needs
+ * clipping in bf16).
+ *   x (B, L, D) activations; w_down (R, D) and w_up (H*d, R): the projection
+ *   x -> w_up (w_down x); conv (H*d, 3) depthwise causal taps, conv[c][2] on token t,
+ *   conv[c][1] on t-1, conv[c][0] on t-2 (zero before the first token);
+ *   u (H, D), bias (H): beta_t,h = min(2 sigmoid(u_h . x_t + bias_h), beta_max).
+ *   w_out (B, H, L, d): per head, the convolved projection divided by max(norm, eps);
+ *   beta_out (B, H, L).
+ * Computed directly: projection of every token, then the convolution, then the norm.
+ */
+void oracle_wbeta_produce(const double *x, const double *w_down, const double *w_up,
+                          const double *conv, const double *u, const double *bias,
+                          double beta_max, int B, int L, int D, int R, int H, int d,
+                          double eps, double *w_out, double *beta_out)
+{
+    const int C = H * d;
+    double *z = (double *)malloc((size_t)L * R * sizeof(double));
+    double *y = (double *)malloc((size_t)L * C * sizeof(double));
+    double *yc = (double *)malloc((size_t)C * sizeof(double));
+    for (int b = 0; b < B; ++b) {
+        const double *xb = x + (size_t)b * L * D;
+        for (int t = 0; t < L; ++t) {
+            for (int r = 0; r < R; ++r) {
+                double acc = 0.0;
+                for (int c = 0; c < D; ++c)
+                    acc += w_down[(size_t)r * D + c] * xb[(size_t)t * D + c];
+                z[(size_t)t * R + r] = acc;
+            }
+            for (int ch = 0; ch < C; ++ch) {
+                double acc = 0.0;
+                for (int r = 0; r < R; ++r)
+                    acc += w_up[(size_t)ch * R + r] * z[(size_t)t * R + r];
+                y[(size_t)t * C + ch] = acc;
+            }
+        }
+        for (int t = 0; t < L; ++t) {
+            for (int ch = 0; ch < C; ++ch) {
+                double acc = conv[(size_t)ch * 3 + 2] * y[(size_t)t * C + ch];
+                if (t >= 1)
+                    acc += conv[(size_t)ch * 3 + 1] * y[(size_t)(t - 1) * C + ch];
+                if (t >= 2)
+                    acc += conv[(size_t)ch * 3 + 0] * y[(size_t)(t - 2) * C + ch];
+                yc[ch] = acc;
+            }
+            for (int h = 0; h < H; ++h) {
+                double ss = 0.0;
+                for (int c = 0; c < d; ++c)
+                    ss += yc[h * d + c] * yc[h * d + c];
+                const double n = sqrt(ss);
+                const double den = n > eps ? n : eps;
+                double *wo = w_out + (((size_t)b * H + h) * L + t) * d;
+                for (int c = 0; c < d; ++c)
+                    wo[c] = yc[h * d + c] / den;
+                double a = bias[h];
+                for (int c = 0; c < D; ++c)
+                    a += u[(size_t)h * D + c] * xb[(size_t)t * D + c];
+                double be = 2.0 / (1.0 + exp(-a));
+                if (be > beta_max)
+                    be = beta_max;
+                beta_out[((size_t)b * H + h) * L + t] = be;
+            }
+        }
+    }
+    free(z);
+    free(y);
+    free(yc);
+}

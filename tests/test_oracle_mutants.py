@@ -14,6 +14,7 @@ import pytest
 import oracle
 from oracle import build as oracle_build
 from tests import test_oracle_pins as pins
+from tests import test_producer_oracle as ppins
 
 SRC = oracle_build.SRC
 
@@ -42,6 +43,23 @@ MUTANTS = {
         "        memcpy(K + (size_t)len * d, k + (size_t)h * d, (size_t)d * sizeof(double));\n"
         "        for (int j = 0; j <= len; ++j)\n            apply_transition(K + (size_t)j * d, w_t, beta[h], d);"),
     "decode_gate_on_new_key": ("cb[len] = 0.0;", "cb[len] = log_f[h];"),
+    # w / beta producer
+    "producer_conv_forward_in_time": (
+        "acc += conv[(size_t)ch * 3 + 1] * y[(size_t)(t - 1) * C + ch];",
+        "acc += conv[(size_t)ch * 3 + 1] * y[(size_t)(t + 1 < L ? t + 1 : t) * C + ch];"),
+    "producer_taps_reversed": (
+        "double acc = conv[(size_t)ch * 3 + 2] * y[(size_t)t * C + ch];",
+        "double acc = conv[(size_t)ch * 3 + 0] * y[(size_t)t * C + ch];"),
+    "producer_norm_over_all_heads": (
+        "for (int c = 0; c < d; ++c)\n                    ss += yc[h * d + c] * yc[h * d + c];",
+        "for (int c = 0; c < C; ++c)\n                    ss += yc[c] * yc[c];"),
+    "producer_beta_without_factor_2": ("double be = 2.0 / (1.0 + exp(-a));",
+                                       "double be = 1.0 / (1.0 + exp(-a));"),
+    "producer_beta_not_clipped": ("if (be > beta_max)\n                    be = beta_max;",
+                                  "(void)beta_max;"),
+    "producer_projects_previous_token": (
+        "acc += w_down[(size_t)r * D + c] * xb[(size_t)t * D + c];",
+        "acc += w_down[(size_t)r * D + c] * xb[(size_t)(t > 0 ? t - 1 : 0) * D + c];"),
 }
 
 
@@ -60,6 +78,12 @@ def run_all_pins():
         ("decode", pins.test_decode_from_empty_cache_matches_prefill, (False,)),
         ("decode_fox", pins.test_decode_from_empty_cache_matches_prefill, (True,)),
         ("rows", pins.test_sampled_rows_match_full_forward, ()),
+        ("p_hand", ppins.test_hand_example, ()),
+        ("p_rank1", ppins.test_rank_one_equal_taps_closed_form, ()),
+        ("p_reach", ppins.test_convolution_reaches_two_tokens_back_and_no_further, ()),
+        ("p_shift", ppins.test_lag_one_tap_shifts_the_output_by_one_token, ()),
+        ("p_norm", ppins.test_unit_norm_scale_invariance_and_heads_independent, ()),
+        ("p_beta", ppins.test_beta_limits, ()),
     ]
     for name, fn, args in checks:
         try:
