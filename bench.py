@@ -72,6 +72,16 @@ def fox_decode_bytes(B, H, n, d=64):
     return B * H * (4.0 * n * d + 8.0 * n + 12.0 * d + 8.0)
 
 
+def producer_bytes(wl, d=64):
+    """HBM bytes of one w / beta production: x read, w and beta written, the bf16
+    intermediate z written and read back, and the weights read (w_up once to form the three
+    tap-scaled copies, written once and read once each)."""
+    B, L, D, R, H = wl.B, wl.L, wl.D, wl.R, wl.H
+    per_token = 2.0 * D + 2.0 * H * d + 4.0 * H + 2.0 * 2 * R
+    weights = 2.0 * (R * D + H * D) + 2.0 * H * d * R * (1 + 3 + 3) + 4.0 * H * d * 3
+    return B * L * per_token + weights
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -273,6 +283,38 @@ def time_decode(pa, wl, reps=2, fox=False):
             "bytes_per_step": sum(nbytes) / len(nbytes), "launches_per_step": 2}
 
 
+def time_producer(pa, wl, steps=5, warmup=3):
+    """Times the w / beta producer (its three launches) on the workload, inputs resident."""
+    dev = torch.device("cuda")
+    p = pi.make_producer_inputs(wl.B, wl.L, wl.D, wl.R, wl.H, seed=wl.seed, device=dev)
+    n = pa.path_wbeta_workspace_bytes(wl.B, wl.L, wl.D, wl.R, wl.H)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    w = torch.empty((wl.B, wl.H, wl.L, 64), dtype=torch.bfloat16, device=dev)
+    beta = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        pa.path_wbeta_produce(p["x"], p["w_down"], p["w_up"], p["conv"], p["u"], p["bias"],
+                              beta_max=pi.BETA_CLIP, w_out=w, beta_out=beta, workspace=ws)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pa.path_check_workspace(ws) != pa.OK:
+        raise RuntimeError("producer kernel status")
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = producer_bytes(wl)
+    return {"workload": wl.name, "ms_per_step": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "tokens_per_s": wl.B * wl.L / (ms * 1e-3), "bytes_per_step": nbytes,
+            "launches_per_step": 3}
+
+
 def cpu_baseline(x_cpu, wl, target_s=12.0):
     """The fp64 oracle on whole heads of the workload, timed on the host cores."""
     import oracle
@@ -308,6 +350,8 @@ PROFILE_CASES = {
                                 torch.bfloat16, 5, 1000),
     "fox_decode": pi.DecodeWorkload("path_fox_decode_bf16_B8H32N32768x4", 8, 32, 32768, 4, 64,
                                     torch.bfloat16, 5, 1000),
+    # a quarter of the producer workload: x 134 MB, w 134 MB (both larger than L2)
+    "producer": pi.ProducerWorkload("path_wbeta_bf16_B8L4096D2048R64H32", 8, 4096, 2048, 64, 32, 6),
 }
 
 
@@ -325,6 +369,9 @@ def run_profile_case(args):
         for t in range(args.warmup + args.steps):
             pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
                                 wl.n_prefix + t, workspace=ws)
+    elif args.profile == "producer":
+        r = time_producer(pa, wl, steps=args.steps, warmup=args.warmup)
+        print(json.dumps(r))
     elif args.profile == "fox_decode":
         cap = wl.n_prefix + args.warmup + args.steps
         kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device=dev)
@@ -431,7 +478,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
-    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode"],
+    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -526,6 +573,14 @@ def main():
                             "traffic": ncu_traffic("decode_split_kernel_fox"),
                             "peak_source": "%s HBM copy" % peaks["source"]}
         line["fox_decode"] = fdec
+        del fdec
+        torch.cuda.empty_cache()
+        prod = time_producer(pa, pi.PRODUCER_L4096)
+        prod["roofline"] = {"kernels": "producer_down_kernel + producer_up_kernel (+ scale)",
+                            "bound": "hbm", "achieved": prod["gbs"], "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": prod["gbs"] / peaks["hbm_gbs"],
+                            "traffic": None, "peak_source": "%s HBM copy" % peaks["source"]}
+        line["producer"] = prod
 
     if args.sweep and rank == 0:
         sweep = {}

@@ -9,6 +9,7 @@ CUDA device every call raises.
 
 Entry points keep the C names: ``path_attn_fwd``, ``path_fox_fwd``,
 ``path_fwd_prepare``, ``path_fwd_scan``, ``path_decode_step``, ``path_fox_decode_step``,
+``path_wbeta_produce``,
 ``path_workspace_bytes``, ``path_check_workspace``, ``path_status_string``.
 """
 import ctypes
@@ -26,7 +27,8 @@ HEAD_DIM = 64
 
 EXPORTED = ("path_workspace_bytes", "path_attn_fwd", "path_fox_fwd", "path_fwd_prepare",
             "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string",
-            "path_decode_step_noalloc", "path_fox_first_blocks", "path_fox_decode_step")
+            "path_decode_step_noalloc", "path_fox_first_blocks", "path_fox_decode_step",
+            "path_wbeta_workspace_bytes", "path_wbeta_produce")
 
 _lib = None
 
@@ -72,6 +74,10 @@ def _load():
     lib.path_fox_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, S,
                                          P]
     lib.path_fox_decode_step.restype = I
+    lib.path_wbeta_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.path_wbeta_workspace_bytes.restype = S
+    lib.path_wbeta_produce.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, P, S, P]
+    lib.path_wbeta_produce.restype = I
     lib.path_decode_step_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.path_decode_step_noalloc.restype = I
     lib.path_fox_first_blocks.argtypes = [P, S, I, I, I, I, I, P, P]
@@ -342,3 +348,44 @@ def path_decode_step_noalloc(q, k, v, w, beta, k_cache, v_cache, cache_len, scal
                                             _stream(stream, k_cache.device)),
            "path_decode_step_noalloc")
     return out
+
+
+def path_wbeta_workspace_bytes(B, L, D, R, H, d=HEAD_DIM, dtype=BF16):
+    return int(_load().path_wbeta_workspace_bytes(int(B), int(L), int(D), int(R), int(H), int(d),
+                                                  int(dtype)))
+
+
+def path_wbeta_produce(x, w_down, w_up, conv, u, bias, beta_max=2.0, w_out=None, beta_out=None,
+                       workspace=None, stream=None):
+    """The w / beta producer: x (B, L, D) bf16; w_down (R, D), w_up (H*d, R), u (H, D) bf16;
+    conv (H*d, 3) and bias (H,) fp32. Returns (w (B, H, L, d) bf16, beta (B, H, L) fp32),
+    the layouts path_attn_fwd takes."""
+    torch = _torch()
+    _cuda_tensor(x, "x", torch.bfloat16)
+    B, L, D = x.shape
+    _cuda_tensor(w_down, "w_down", torch.bfloat16)
+    _cuda_tensor(w_up, "w_up", torch.bfloat16)
+    _cuda_tensor(u, "u", torch.bfloat16)
+    _cuda_tensor(conv, "conv", torch.float32)
+    _cuda_tensor(bias, "bias", torch.float32)
+    R, H = w_down.shape[0], u.shape[0]
+    d = w_up.shape[0] // H
+    if (tuple(w_down.shape) != (R, D) or tuple(w_up.shape) != (H * d, R)
+            or tuple(u.shape) != (H, D) or tuple(conv.shape) != (H * d, 3)
+            or tuple(bias.shape) != (H,)):
+        raise ValueError("inconsistent producer shapes")
+    if w_out is None:
+        w_out = torch.empty((B, H, L, d), dtype=torch.bfloat16, device=x.device)
+    if beta_out is None:
+        beta_out = torch.empty((B, H, L), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        n = path_wbeta_workspace_bytes(B, L, D, R, H, d, BF16)
+        if n == 0:
+            raise PathError(ERR_SHAPE, "path_wbeta_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    _check(_load().path_wbeta_produce(_ptr(x), _ptr(w_down), _ptr(w_up), _ptr(conv), _ptr(u),
+                                      _ptr(bias), float(beta_max), _ptr(w_out), _ptr(beta_out), B,
+                                      L, D, R, H, d, BF16, _ptr(workspace), workspace.numel(),
+                                      _stream(stream, x.device)),
+           "path_wbeta_produce")
+    return w_out, beta_out

@@ -33,6 +33,11 @@ cudaError_t launch_fox_decode(const void *q, const void *k, const void *v, const
                               const float *beta, const float *log_f, void *k_cache,
                               void *v_cache, float *gc, int BH, int cache_len, int cap,
                               float scale, void *out, void *ws, cudaStream_t stream);
+size_t producer_ws_bytes(int B, int L, int R, int H);
+cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up, const float *conv,
+                            const void *u, const float *bias, float beta_max, void *w_out,
+                            float *beta_out, int B, int L, int D, int R, int H, void *ws,
+                            uint64_t limit_ns, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len);
 template <typename T>
@@ -277,6 +282,42 @@ path_status path_decode_step_noalloc(const void *q, const void *k, const void *v
                                                              out, s));
     return from_cuda(launch_decode_static<float>(q, k, v, w, beta, k_cache, v_cache, B * H,
                                                  cache_len, cache_cap, scale, out, s));
+}
+
+namespace {
+path_status check_producer_sizes(int B, int L, int D, int R, int H, int d, int dtype) {
+    if (B < 0 || L < 0 || D <= 0 || R <= 0 || H <= 0) return PATH_ERR_SHAPE;
+    if (dtype != PATH_BF16) return PATH_ERR_DTYPE;
+    if (d != kD || D % 64 != 0 || R % 64 != 0 || R + ((H + 15) & ~15) > 256) return PATH_ERR_SHAPE;
+    if ((long long)B * H > PATH_MAX_HEADS || L > PATH_MAX_LEN || D > (1 << 16) ||
+        (long long)B * L > (1LL << 30))
+        return PATH_ERR_SHAPE;
+    return PATH_OK;
+}
+}  // namespace
+
+size_t path_wbeta_workspace_bytes(int B, int L, int D, int R, int H, int d, int dtype) {
+    if (check_producer_sizes(B, L, D, R, H, d, dtype) != PATH_OK) return 0;
+    return producer_ws_bytes(B, L, R, H);
+}
+
+path_status path_wbeta_produce(const void *x, const void *w_down, const void *w_up,
+                               const float *conv, const void *u, const float *bias,
+                               float beta_max, void *w_out, float *beta_out, int B, int L,
+                               int D, int R, int H, int d, int dtype, void *ws, size_t ws_bytes,
+                               void *stream) {
+    path_status st = check_producer_sizes(B, L, D, R, H, d, dtype);
+    if (st != PATH_OK) return st;
+    if (!std::isfinite(beta_max) || !(beta_max > 0.f)) return PATH_ERR_ARG;
+    if ((long long)B * L == 0) return PATH_OK;
+    if (!x || !w_down || !w_up || !conv || !u || !bias || !w_out || !beta_out) return PATH_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(w_down, 16) || !aligned(w_up, 16) || !aligned(u, 16) ||
+        !aligned(conv, 4) || !aligned(bias, 4) || !aligned(w_out, 16) || !aligned(beta_out, 4))
+        return PATH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, producer_ws_bytes(B, L, R, H))) != PATH_OK) return st;
+    return from_cuda(launch_producer(x, w_down, w_up, conv, u, bias, beta_max, w_out, beta_out, B,
+                                     L, D, R, H, ws, kWaitLimitNs,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 path_status path_check_workspace(void *ws, void *stream) {

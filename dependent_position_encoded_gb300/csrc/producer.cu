@@ -1,0 +1,488 @@
+// The w / beta producer: per token, the Householder direction w and strength beta that
+// PaTH attention consumes.
+//
+// Review "거리에서 경로로, PaTH Attention" §3: w comes from a low-dimensional linear
+// projection and a short convolution of size 3 and is then L2-normalised; beta is twice a
+// sigmoid. Technical summary "技術要約: PaTH Attention" §2: beta_s = 2 sigmoid(u^T x_s + b);
+// §6: beta is clipped for bf16. Per token t of sequence b and head h:
+//   z_t   = W_down x_t                                    (R)
+//   y_t   = W_up z_t                                      (H*d)
+//   y'_t  = conv[:,2] * y_t + conv[:,1] * y_{t-1} + conv[:,0] * y_{t-2}   (zero before t = 0)
+//   w_t,h = y'_t,h / max(|y'_t,h|, 1e-12),   beta_t,h = min(2 sigmoid(u_h . x_t + b_h), beta_max)
+//
+// Three launches:
+//   P0 forms the tap-scaled up-projections W'_k = diag(conv[:,k]) W_up (bf16), so that the
+//      convolution becomes part of the second contraction: y'_t = sum_k W'_k z_{t-2+k};
+//   P1 (tcgen05): [z | beta logits] = x [W_down; u]^T for 128-token tiles, streaming x
+//      through a four-stage TMA ring; the epilogue writes z (bf16) and beta;
+//   P2 (tcgen05): for 128-token tiles of one sequence, three accumulating contractions of
+//      z tiles loaded at rows t0, t0-1, t0-2 (a negative start row reads zeros: the causal
+//      zero history) with W'_2, W'_1, W'_0, two heads (N = 128) per TMEM buffer, double
+//      buffered; the epilogue normalises each head row into a 128-byte-swizzled shared tile
+//      that one TMA tensor store writes to w in the (B, H, L, d) layout the attention
+//      takes (rows past L are clipped by the store).
+// x is read once and w written once: the pair is bound by HBM bandwidth.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace path {
+
+namespace {
+
+constexpr uint32_t kRowTile = 128 * 128;  // 128 rows x 64 bf16, 128-byte swizzled
+
+__host__ __device__ constexpr uint32_t idesc_bf16_kk(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                            int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Tensor store of a 128-byte-swizzled shared tile (box of the map) at (c0, c1, c2); one
+// bulk group per store.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1,
+                                             int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Named barrier over the four epilogue warps (ids 1..; 0 is __syncthreads).
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Bounded wait by one thread; false (and the status word set) after limit_ns.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t par, uint64_t limit_ns,
+                                             uint32_t *status) {
+    if (mbar_wait(bar, par, limit_ns)) return true;
+    report_status(status, kStatusTimeout);
+    return false;
+}
+
+// ---------------------------------------------------------------- P0: tap-scaled W_up
+__global__ void producer_scale_kernel(const __nv_bfloat16 *__restrict__ w_up,
+                                      const float *__restrict__ conv, int C, int R,
+                                      __nv_bfloat16 *__restrict__ wk) {
+    const size_t n = (size_t)C * R;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i / R);
+        const float v = __bfloat162float(w_up[i]);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) wk[(size_t)k * n + i] = __float2bfloat16_rn(conv[c * 3 + k] * v);
+    }
+}
+
+// ---------------------------------------------------------------- P1: z and beta
+constexpr int kP1Stages = 4;
+constexpr int kP1Threads = 192;  // warps 0-3: epilogue (TMEM lanes 0-127); 4: TMA; 5: MMA
+
+__global__ void __launch_bounds__(kP1Threads, 1)
+producer_down_kernel(const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_wd,
+                     const __grid_constant__ CUtensorMap tm_u, const float *__restrict__ bias,
+                     float beta_max, int BL, int L, int D, int R, int H, int Hp, int tmem_cols,
+                     __nv_bfloat16 *__restrict__ z, float *__restrict__ beta_out,
+                     uint32_t *status, uint64_t limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const sm = smem_raw + (base - raw);
+    const int NB = R + Hp;
+    const uint32_t stage_bytes = kRowTile + (uint32_t)NB * 128;
+    const uint32_t bar0 = base + kP1Stages * stage_bytes;  // full[s], empty[s], done
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (kP1Stages + s); };
+    const uint32_t done = bar0 + 8u * (2 * kP1Stages);
+    uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + (bar0 - base) + 8 * (2 * kP1Stages + 1));
+    __shared__ uint32_t abort_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * 128;
+    const int nk = D / 64;
+    if (threadIdx.x == 0) {
+        abort_s = 0u;
+        for (int s = 0; s < kP1Stages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), (uint32_t)tmem_cols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+
+    if (warp == 4 && lane == 0) {
+        // ---- TMA producer: x chunk (128 tokens x 64) and [W_down; u] chunk (NB x 64)
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_wd);
+        tma_prefetch_desc(&tm_u);
+        int issued = 0;
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % kP1Stages;
+            if (kc >= kP1Stages &&
+                !wait_bounded(empty(s), ((kc / kP1Stages) - 1) & 1, limit_ns, status)) {
+                abort_s = 1u;
+                break;
+            }
+            const uint32_t a = base + s * stage_bytes, b = a + kRowTile;
+            mbar_arrive_expect_tx(full(s), stage_bytes);
+            tma_load_2d(a, &tm_x, full(s), kc * 64, row0);
+            tma_load_2d(b, &tm_wd, full(s), kc * 64, 0);
+            tma_load_2d(b + (uint32_t)R * 128, &tm_u, full(s), kc * 64, 0);
+            issued = kc + 1;
+        }
+        // drain: every issued copy has landed before the CTA may exit
+        for (int j = (issued > kP1Stages ? issued - kP1Stages : 0); j < issued; ++j)
+            mbar_wait(full(j % kP1Stages), (j / kP1Stages) & 1, limit_ns);
+    } else if (warp == 5 && lane == 0) {
+        // ---- MMA issuer: D (128 x NB) += x_chunk [W_down; u]_chunk^T
+        const uint32_t idesc = idesc_bf16_kk(128, NB);
+        bool ok = true;
+        for (int kc = 0; kc < nk && ok; ++kc) {
+            const int s = kc % kP1Stages;
+            if (!wait_bounded(full(s), (kc / kP1Stages) & 1, limit_ns, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad = sdesc_sw128(base + s * stage_bytes, 16, 1024);
+            const uint64_t bd = sdesc_sw128(base + s * stage_bytes + kRowTile, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(empty(s));
+        }
+        if (!ok) abort_s = 1u;
+        umma_commit(done);  // (also when aborted: the epilogue must not wait forever)
+    } else if (warp < 4) {
+        // ---- epilogue: row = token row0 + 32 warp + lane
+        if (threadIdx.x == 0 && !wait_bounded(done, 0, limit_ns, status)) abort_s = 1u;
+        epi_sync();
+        if (abort_s == 0u) {
+            tc_fence_after();
+            const int tok = row0 + 32 * warp + lane;
+            const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+            uint32_t v[32];
+            for (int c0 = 0; c0 < R; c0 += 32) {
+                tmem_ld32(tl + c0, v);
+                tmem_ld_wait();
+                if (tok < BL) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(z + (size_t)tok * R + c0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                }
+            }
+            const int bq = tok / L, t = tok - bq * L;
+            for (int h0 = 0; h0 < H; h0 += 32) {
+                tmem_ld32(tl + R + h0, v);
+                tmem_ld_wait();
+                if (tok < BL) {
+#pragma unroll 4
+                    for (int j = 0; j < 32; ++j) {
+                        const int h = h0 + j;
+                        if (h >= H) break;
+                        const float a = __uint_as_float(v[j]) + bias[h];
+                        const float be = 2.f / (1.f + expf(-a));
+                        beta_out[((size_t)bq * H + h) * L + t] = fminf(be, beta_max);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------- P2: w
+constexpr int kP2Stages = 2;
+constexpr int kP2Threads = 192;  // warps 0-3: epilogue; 4: TMA; 5: MMA
+constexpr int kP2Cols = 256;     // two 128-column (two-head) accumulators
+
+__global__ void __launch_bounds__(kP2Threads, 1)
+producer_up_kernel(const __grid_constant__ CUtensorMap tm_z,
+                   const __grid_constant__ CUtensorMap tm_wk,
+                   const __grid_constant__ CUtensorMap tm_w, int L, int R, int H,
+                   uint32_t *status, uint64_t limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const sm = smem_raw + (base - raw);
+    const int nkc = R / 64;                       // 64-wide K chunks of z
+    const uint32_t a_base = base;                 // z tiles: [tap][kc], 128 rows each
+    const uint32_t b_base = base + 3u * nkc * kRowTile;  // W' ring
+    const uint32_t c_base = b_base + kP2Stages * kRowTile;  // staging of one head's w tile
+    const uint32_t bar0 = c_base + kRowTile;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (kP2Stages + s); };
+    const uint32_t a_full = bar0 + 8u * (2 * kP2Stages);
+    auto acc_full = [&](int i) { return bar0 + 8u * (2 * kP2Stages + 1 + i); };
+    auto acc_empty = [&](int i) { return bar0 + 8u * (2 * kP2Stages + 3 + i); };
+    uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + (bar0 - base) + 8 * (2 * kP2Stages + 5));
+    __shared__ uint32_t abort_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * 128, bq = blockIdx.y;
+    const int nchunk = (H + 1) / 2;                // two heads per accumulator
+    const int nsteps = nchunk * 3 * nkc;          // B tiles consumed, in order (chunk, tap, kc)
+    if (threadIdx.x == 0) {
+        abort_s = 0u;
+        for (int s = 0; s < kP2Stages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(a_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full(i), 1);
+            mbar_init(acc_empty(i), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), kP2Cols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+
+    if (warp == 4 && lane == 0) {
+        // ---- TMA: the three shifted z tiles once, then W'_tap chunks in consumption order
+        tma_prefetch_desc(&tm_z);
+        tma_prefetch_desc(&tm_wk);
+        mbar_arrive_expect_tx(a_full, 3u * nkc * kRowTile);
+        for (int tap = 0; tap < 3; ++tap)
+            for (int kc = 0; kc < nkc; ++kc)
+                tma_load_3d(a_base + (uint32_t)(tap * nkc + kc) * kRowTile, &tm_z, a_full, kc * 64,
+                            t0 - (2 - tap), bq);
+        int i = 0;
+        for (; i < nsteps; ++i) {
+            const int s = i % kP2Stages;
+            if (i >= kP2Stages &&
+                !wait_bounded(empty(s), ((i / kP2Stages) - 1) & 1, limit_ns, status)) {
+                abort_s = 1u;
+                break;
+            }
+            const int kc = i % nkc, tap = (i / nkc) % 3, chunk = i / (3 * nkc);
+            mbar_arrive_expect_tx(full(s), kRowTile);
+            tma_load_3d(b_base + (uint32_t)s * kRowTile, &tm_wk, full(s), kc * 64, 128 * chunk, tap);
+        }
+        // drain: every issued copy has landed before the CTA may exit
+        for (int j = (i > kP2Stages ? i - kP2Stages : 0); j < i; ++j)
+            mbar_wait(full(j % kP2Stages), (j / kP2Stages) & 1, limit_ns);
+        mbar_wait(a_full, 0, limit_ns);
+    } else if (warp == 5 && lane == 0) {
+        // ---- MMA: acc[chunk & 1] = sum over taps and K chunks of z_tap W'_tap^T (N = 128)
+        const uint32_t idesc = idesc_bf16_kk(128, 128);
+        bool ok = wait_bounded(a_full, 0, limit_ns, status);
+        int i = 0;
+        for (int chunk = 0; chunk < nchunk && ok; ++chunk) {
+            const int buf = chunk & 1;
+            if (chunk >= 2 && !wait_bounded(acc_empty(buf), ((chunk >> 1) - 1) & 1, limit_ns, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int tap = 0; tap < 3 && ok; ++tap) {
+                for (int kc = 0; kc < nkc; ++kc, ++i) {
+                    const int s = i % kP2Stages;
+                    if (!wait_bounded(full(s), (i / kP2Stages) & 1, limit_ns, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(a_base + (uint32_t)(tap * nkc + kc) * kRowTile, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(b_base + (uint32_t)s * kRowTile, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + 128u * buf, ad + 2 * kk, bd + 2 * kk, idesc,
+                                  (tap > 0 || kc > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(empty(s));
+                }
+            }
+            umma_commit(acc_full(buf));
+        }
+        if (!ok) {
+            abort_s = 1u;
+            // release the epilogue: it waits on the accumulators it has not yet seen
+            for (int i2 = 0; i2 < 2; ++i2) umma_commit(acc_full(i2));
+        }
+    } else if (warp < 4) {
+        // ---- epilogue: row = token t0 + 32 warp + lane; two heads per accumulator
+        const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+        for (int chunk = 0; chunk < nchunk; ++chunk) {
+            const int buf = chunk & 1;
+            if (threadIdx.x == 0 &&
+                !wait_bounded(acc_full(buf), (chunk >> 1) & 1, limit_ns, status))
+                abort_s = 1u;
+            epi_sync();
+            if (abort_s != 0u) break;
+            tc_fence_after();
+            for (int hh = 0; hh < 2; ++hh) {
+                const int h = 2 * chunk + hh;
+                if (h >= H) break;
+                uint32_t a[32], b[32];
+                tmem_ld32(tl + 128u * buf + 64u * hh, a);
+                tmem_ld32(tl + 128u * buf + 64u * hh + 32u, b);
+                tmem_ld_wait();
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p = __uint_as_float(a[j]), q = __uint_as_float(b[j]);
+                    ss = fmaf(p, p, fmaf(q, q, ss));
+                }
+                const float inv = rsqrtf(fmaxf(ss, 1e-24f));  // 1 / max(|y'|, 1e-12)
+                // the previous head's tile has left the staging buffer
+                if (threadIdx.x == 0) bulk_wait_read();
+                epi_sync();
+                // row r of the tile, 128-byte swizzled (conflict-free: the eight lanes of a
+                // store phase hold eight consecutive rows and land in eight distinct chunks)
+                uint8_t *const tile = sm + (c_base - base);
+                const int r = 32 * warp + lane;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(tile + sw128_offset(r, q4)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(a[8 * q4]) * inv, __uint_as_float(a[8 * q4 + 1]) * inv),
+                        pack_bf16x2(__uint_as_float(a[8 * q4 + 2]) * inv, __uint_as_float(a[8 * q4 + 3]) * inv),
+                        pack_bf16x2(__uint_as_float(a[8 * q4 + 4]) * inv, __uint_as_float(a[8 * q4 + 5]) * inv),
+                        pack_bf16x2(__uint_as_float(a[8 * q4 + 6]) * inv, __uint_as_float(a[8 * q4 + 7]) * inv));
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 4 + q4)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(b[8 * q4]) * inv, __uint_as_float(b[8 * q4 + 1]) * inv),
+                        pack_bf16x2(__uint_as_float(b[8 * q4 + 2]) * inv, __uint_as_float(b[8 * q4 + 3]) * inv),
+                        pack_bf16x2(__uint_as_float(b[8 * q4 + 4]) * inv, __uint_as_float(b[8 * q4 + 5]) * inv),
+                        pack_bf16x2(__uint_as_float(b[8 * q4 + 6]) * inv, __uint_as_float(b[8 * q4 + 7]) * inv));
+                fence_proxy_async_smem();
+                epi_sync();
+                // rows past L are clipped by the tensor store
+                if (threadIdx.x == 0) tma_store_3d(&tm_w, c_base, 0, t0, bq * H + h);
+            }
+            tc_fence_before();
+            epi_sync();
+            if (threadIdx.x == 0) mbar_arrive(acc_empty(buf));
+        }
+    }
+    if (threadIdx.x == 0) bulk_wait_all();  // the last tiles have been written
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kP2Cols);
+    }
+}
+
+// 2-D bf16 map (rows x cols, cols contiguous), box (64 cols, box_rows), 128-byte swizzle.
+bool map2d(CUtensorMap *m, const void *ptr, int cols, long long rows, int box_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map (d2, d1, d0 = cols contiguous), box (64, 128, 1), 128-byte swizzle.
+bool map3d(CUtensorMap *m, const void *ptr, int cols, int d1, int d2) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d1, (cuuint64_t)d2};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * d1};
+    cuuint32_t box[3] = {64u, 128u, 1u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Workspace of the producer: 256-byte status header, z (B*L, R) bf16, W'_0..2 (3, H*d, R) bf16.
+size_t producer_ws_bytes(int B, int L, int R, int H) {
+    return 256 + align256((size_t)B * L * R * 2) + align256((size_t)3 * H * kD * R * 2);
+}
+
+size_t producer_down_smem(int R, int Hp) {
+    return (size_t)kP1Stages * (kRowTile + (size_t)(R + Hp) * 128) + 8 * (2 * kP1Stages + 2) + 1024;
+}
+size_t producer_up_smem(int R) {
+    return (size_t)3 * (R / 64) * kRowTile + (size_t)(kP2Stages + 1) * kRowTile +
+           8 * (2 * kP2Stages + 6) + 1024;
+}
+
+// The caller has checked the sizes (d = 64, D and R multiples of 64, R + round16(H) <= 256).
+cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up, const float *conv,
+                            const void *u, const float *bias, float beta_max, void *w_out,
+                            float *beta_out, int B, int L, int D, int R, int H, void *ws,
+                            uint64_t limit_ns, cudaStream_t stream) {
+    char *wsb = static_cast<char *>(ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(wsb);
+    __nv_bfloat16 *z = reinterpret_cast<__nv_bfloat16 *>(wsb + 256);
+    __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(wsb + 256 + align256((size_t)B * L * R * 2));
+    const int C = H * kD;
+    const long long BL = (long long)B * L;
+    const int Hp = (H + 15) & ~15;
+    const int tcols = (R + Hp) <= 128 ? 128 : 256;
+    cudaError_t err = cudaMemsetAsync(status, 0, 4, stream);
+    if (err != cudaSuccess) return err;
+    producer_scale_kernel<<<(unsigned)std::min<size_t>(((size_t)C * R + 255) / 256, 4096), 256, 0,
+                            stream>>>(static_cast<const __nv_bfloat16 *>(w_up), conv, C, R, wk);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    CUtensorMap tx, twd, tu, tz, twk, tw;
+    if (!map2d(&tx, x, D, BL, 128) || !map2d(&twd, w_down, D, R, R) || !map2d(&tu, u, D, H, Hp) ||
+        !map3d(&tz, z, R, L, B) || !map3d(&twk, wk, R, C, 3) || !map3d(&tw, w_out, kD, L, B * H))
+        return cudaErrorInvalidValue;
+    const size_t s1 = producer_down_smem(R, Hp), s2 = producer_up_smem(R);
+    if ((err = cudaFuncSetAttribute(producer_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)s1)) != cudaSuccess)
+        return err;
+    if ((err = cudaFuncSetAttribute(producer_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)s2)) != cudaSuccess)
+        return err;
+    producer_down_kernel<<<(unsigned)((BL + 127) / 128), kP1Threads, s1, stream>>>(
+        tx, twd, tu, bias, beta_max, (int)BL, L, D, R, H, Hp, tcols, z, beta_out, status, limit_ns);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    producer_up_kernel<<<dim3((L + 127) / 128, B), kP2Threads, s2, stream>>>(
+        tz, twk, tw, L, R, H, status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace path

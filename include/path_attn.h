@@ -207,6 +207,35 @@ path_status path_decode_step_noalloc(const void *q, const void *k, const void *v
                                      float scale, void *out, void *stream);
 
 /*
+ * Producer of the per-token Householder directions w and strengths beta (review
+ * "거리에서 경로로, PaTH Attention" §3: a low-dimensional linear projection and a short
+ * convolution of size 3 give w, which is L2-normalised, and beta is twice a sigmoid;
+ * technical summary "技術要約: PaTH Attention" §2: beta_s = 2 sigmoid(u^T x_s + b), §6: beta
+ * is clipped for bf16). For every token t of sequence b and head h:
+ *   y_t   = w_up (w_down x_t)                             (H*d channels)
+ *   y'_t  = conv[:,2] y_t + conv[:,1] y_{t-1} + conv[:,0] y_{t-2}  (depthwise, causal,
+ *           zero before the first token of each sequence)
+ *   w_out[b,h,t,:] = y'_t,h / max(|y'_t,h|, 1e-12)        (per head of d channels)
+ *   beta_out[b,h,t] = min(2 sigmoid(u_h . x_t + bias_h), beta_max)
+ *   x      : (B, L, D) bf16 activations
+ *   w_down : (R, D) bf16, w_up : (H*d, R) bf16, u : (H, D) bf16 (rows = output features)
+ *   conv   : (H*d, 3) fp32 taps; bias : (H) fp32; beta_max: clip (2 or more: none)
+ *   w_out  : (B, H, L, d) bf16, beta_out : (B, H, L) fp32 -- the layouts path_attn_fwd takes
+ *   ws     : path_wbeta_workspace_bytes(B, L, D, R, H, d, dtype) bytes (intermediate
+ *            z = w_down x and the tap-scaled w_up, bf16)
+ * Supported: dtype PATH_BF16 (else PATH_ERR_DTYPE); d = 64; D a positive multiple of 64;
+ * R a multiple of 64 with R + (H rounded up to 16) <= 256; H >= 1 (else PATH_ERR_SHAPE).
+ * beta_max must be positive and finite (PATH_ERR_ARG). Contractions use bf16 operands with
+ * fp32 accumulation; z and the tap-scaled w_up are rounded to bf16.
+ */
+size_t path_wbeta_workspace_bytes(int B, int L, int D, int R, int H, int d, int dtype);
+path_status path_wbeta_produce(const void *x, const void *w_down, const void *w_up,
+                               const float *conv, const void *u, const float *bias,
+                               float beta_max, void *w_out, float *beta_out, int B, int L,
+                               int D, int R, int H, int d, int dtype, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/*
  * Waits for `stream`, then reads and clears the status word that kernels of
  * earlier calls on this workspace wrote. Returns PATH_OK, PATH_ERR_TIMEOUT or
  * PATH_ERR_CUDA (if the synchronisation or the read failed).

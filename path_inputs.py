@@ -138,6 +138,40 @@ def make_fox_decode_prefix(wl, cap, device="cpu"):
     return kc, vc, gc
 
 
+@dataclass(frozen=True)
+class ProducerWorkload:
+    name: str
+    B: int
+    L: int
+    D: int
+    R: int
+    H: int
+    seed: int
+
+
+# The w / beta producer at the speed shape: B=32 sequences of L=4096 tokens, model width
+# D = H*d = 2048, a rank-64 projection, 32 heads.
+PRODUCER_L4096 = ProducerWorkload("path_wbeta_bf16_B32L4096D2048R64H32", 32, 4096, 2048, 64, 32, 6)
+
+
+def make_producer_inputs(B, L, D, R, H, d=D, seed=0, device="cpu"):
+    """Seeded producer inputs (draw order x, w_down, w_up, conv, u, bias): activations
+    x ~ N(0, 1); projection weights ~ N(0, 1 / fan_in) (rows = output features), so that
+    every intermediate is of unit scale; conv taps ~ N(0, 1/3); u ~ N(0, 1 / D);
+    bias ~ N(0, 1). x and the weight matrices bf16, conv and bias fp32."""
+    g = _gen(seed, device)
+    f32 = torch.float32
+    x = torch.randn((B, L, D), generator=g, device=device, dtype=f32)
+    w_down = torch.randn((R, D), generator=g, device=device, dtype=f32) * D ** -0.5
+    w_up = torch.randn((H * d, R), generator=g, device=device, dtype=f32) * R ** -0.5
+    conv = torch.randn((H * d, 3), generator=g, device=device, dtype=f32) * 3 ** -0.5
+    u = torch.randn((H, D), generator=g, device=device, dtype=f32) * D ** -0.5
+    bias = torch.randn((H,), generator=g, device=device, dtype=f32)
+    bf = torch.bfloat16
+    return {"x": x.to(bf), "w_down": w_down.to(bf).contiguous(), "w_up": w_up.to(bf).contiguous(),
+            "conv": conv.contiguous(), "u": u.to(bf).contiguous(), "bias": bias}
+
+
 def make_decode_step(wl, t, device="cpu", fox=False, B=None, H=None):
     """Inputs of decode step t: q, k, v, w (B, H, d) and beta (B, H), seed step_seed + t."""
     B = wl.B if B is None else B

@@ -141,6 +141,34 @@ def test_fox_decode_argument_checks(so, lib):
         lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 64, lib.BF16)
 
 
+def test_producer_argument_checks(so, lib):
+    # every case below is rejected before any launch (fake pointers are never used)
+    def call(**kw):
+        a = dict(B=1, L=128, D=128, R=64, H=2, d=64, dtype=1, ws_bytes=1 << 30, x=FAKE,
+                 out=FAKE, bmax=1.99)
+        a.update(kw)
+        return so.path_wbeta_produce(a["x"], FAKE, FAKE, FAKE, FAKE, FAKE,
+                                     ctypes.c_float(a["bmax"]), a["out"], FAKE, a["B"], a["L"],
+                                     a["D"], a["R"], a["H"], a["d"], a["dtype"], FAKE,
+                                     ctypes.c_size_t(a["ws_bytes"]), None)
+    assert call(dtype=0) == 3          # bf16 only
+    assert call(d=32) == 2
+    assert call(D=100) == 2            # D a multiple of 64
+    assert call(R=48) == 2             # R a multiple of 64
+    assert call(R=192, H=65) == 2      # R + round16(H) > 256
+    assert call(H=0) == 2
+    assert call(x=None) == 1
+    assert call(out=FAKE + 8) == 4
+    assert call(ws_bytes=64) == 5
+    assert call(bmax=float("nan")) == 9
+    assert call(bmax=0.0) == 9
+    assert call(L=0) == 0 and call(B=0) == 0
+    # workspace: header, z (B*L, R) bf16, three tap-scaled (H*d, R) bf16 matrices
+    assert lib.path_wbeta_workspace_bytes(2, 100, 128, 64, 3) == \
+        256 + (2 * 100 * 64 * 2 + 255) // 256 * 256 + (3 * 3 * 64 * 64 * 2 + 255) // 256 * 256
+    assert lib.path_wbeta_workspace_bytes(2, 100, 128, 64, 3, 64, lib.F32) == 0
+
+
 def test_noalloc_decode_rejects_problems_beyond_the_fixed_scratch(so):
     # 4096 heads x 17 splits of 1024 keys x 264 B = 18.4 MB > 16 MiB: refused before any
     # launch. The size is checked here first so that these never-dereferenced pointers
