@@ -576,10 +576,12 @@ def main():
         del fdec
         torch.cuda.empty_cache()
         prod = time_producer(pa, pi.PRODUCER_L4096)
+        t_down, t_up = ncu_traffic("producer_down_kernel"), ncu_traffic("producer_up_kernel")
         prod["roofline"] = {"kernels": "producer_down_kernel + producer_up_kernel (+ scale)",
                             "bound": "hbm", "achieved": prod["gbs"], "peak": peaks["hbm_gbs"],
                             "unit": "GB/s", "frac": prod["gbs"] / peaks["hbm_gbs"],
-                            "traffic": None, "peak_source": "%s HBM copy" % peaks["source"]}
+                            "traffic": (t_down + t_up) if (t_down and t_up) else None,
+                            "peak_source": "%s HBM copy" % peaks["source"]}
         line["producer"] = prod
 
     if args.sweep and rank == 0:
