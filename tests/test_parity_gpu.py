@@ -246,6 +246,14 @@ def test_speed_workload_sampled(lib):
     _sampled_parity(lib, pi.BF16_L4096)
 
 
+@pytest.mark.parametrize("L", [L for L in pi.SPEED_SWEEP_L if L != 4096])
+def test_speed_shape_sweep_sampled(lib, L):
+    # the B32 H32 speed shape at the other sequence lengths of the throughput curve, in the
+    # launch configuration the sweep times; 300 sampled rows on 8 heads (heads are
+    # independent, so the sample is exact for them)
+    _sampled_parity(lib, pi.speed_shape(L), n_heads=8, n_rows=300, seed=L)
+
+
 def test_fox_long_workload_sampled(lib):
     _sampled_parity(lib, pi.FOX_L16384, n_heads=8, n_rows=300)
 
