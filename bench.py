@@ -280,8 +280,8 @@ def time_decode(pa, wl, reps=2, fox=False):
         kc, vc = pi.make_decode_prefix(wl, cap, device=dev)
     steps = [pi.make_decode_step(wl, t, device=dev, fox=fox) for t in range(wl.steps)]
     ws = pa.new_workspace(pa.OP_FOX_DECODE if fox else pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16,
-                          dev)
-    out = torch.empty((wl.B, wl.H, 64), dtype=torch.bfloat16, device=dev)
+                          dev, wl.d)
+    out = torch.empty((wl.B, wl.H, wl.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     per_step = []
     for r in range(reps + 1):
@@ -300,7 +300,7 @@ def time_decode(pa, wl, reps=2, fox=False):
             per_step.append([evs[t].elapsed_time(evs[t + 1]) for t in range(wl.steps)])
     ms = [statistics.mean(col) for col in zip(*per_step)]
     bytes_fn = fox_decode_bytes if fox else decode_bytes
-    nbytes = [bytes_fn(wl.B, wl.H, wl.n_prefix + t) for t in range(wl.steps)]
+    nbytes = [bytes_fn(wl.B, wl.H, wl.n_prefix + t, wl.d) for t in range(wl.steps)]
     gbs = sum(nbytes) / (sum(ms) * 1e-3) / 1e9
     return {"ms_per_step": sum(ms) / len(ms), "gbs": gbs,
             "tokens_per_s": wl.B / (sum(ms) / len(ms) * 1e-3),
@@ -599,6 +599,13 @@ def main():
                             "traffic": ncu_traffic("decode_split_kernel_fox"),
                             "peak_source": "%s HBM copy" % peaks["source"]}
         line["fox_decode"] = fdec
+        d128 = time_decode(pa, pi.DECODE_32K_D128)
+        d128["workload"] = pi.DECODE_32K_D128.name
+        d128["roofline"] = {"kernel": "decode_split_kernel<d=128>", "bound": "hbm",
+                            "achieved": d128["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": d128["gbs"] / peaks["hbm_gbs"], "traffic": None,
+                            "peak_source": "%s HBM copy" % peaks["source"]}
+        line["decode_d128"] = d128
         del fdec
         torch.cuda.empty_cache()
         prod = time_producer(pa, pi.PRODUCER_L4096)

@@ -149,10 +149,10 @@ def path_workspace_bytes(op, B, H, L, d=HEAD_DIM, dtype=BF16):
     return int(_load().path_workspace_bytes(int(op), int(B), int(H), int(L), int(d), int(dtype)))
 
 
-def new_workspace(op, B, H, L, dtype, device):
+def new_workspace(op, B, H, L, dtype, device, d=HEAD_DIM):
     """A device workspace sized by path_workspace_bytes (256-byte aligned by PyTorch)."""
     torch = _torch()
-    n = path_workspace_bytes(op, B, H, L, HEAD_DIM, dtype)
+    n = path_workspace_bytes(op, B, H, L, d, dtype)
     if n == 0:
         raise PathError(ERR_SHAPE, "path_workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -287,7 +287,7 @@ def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, 
     accepted); beta: (B, H); caches: (B, H, cap, d)."""
     ins, out, (B, H, cap, d) = _decode_args(q, k, v, w, beta, k_cache, v_cache, out)
     if workspace is None:
-        workspace = new_workspace(OP_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device)
+        workspace = new_workspace(OP_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device, d)
     _check(_load().path_decode_step(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]), _ptr(ins[3]),
                                     _ptr(beta), _ptr(k_cache), _ptr(v_cache), B, H,
                                     int(cache_len), cap, d, _dtype_code(k_cache),
@@ -311,7 +311,8 @@ def path_fox_decode_step(q, k, v, w, beta, log_f, k_cache, v_cache, g_cache, cac
     if tuple(g_cache.shape) != (B, H, cap):
         raise ValueError("g_cache must have shape (B, H, cap)")
     if workspace is None:
-        workspace = new_workspace(OP_FOX_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device)
+        workspace = new_workspace(OP_FOX_DECODE, B, H, cap, _dtype_code(k_cache), k_cache.device,
+                                  d)
     _check(_load().path_fox_decode_step(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]), _ptr(ins[3]),
                                         _ptr(beta), _ptr(log_f), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(g_cache), B, H, int(cache_len), cap, d,

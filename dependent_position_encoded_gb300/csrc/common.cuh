@@ -91,11 +91,11 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     return lay;
 }
 
-// Decode: per head and split, (m, l, o[64]) partial results.
+// Decode: per head and split, (m, l, o[d]) partial results (d = 64 or 128).
 constexpr int kDecodeChunk = 1024;  // cached keys per split
 inline int decode_splits(int cap) { return (cap + kDecodeChunk - 1) / kDecodeChunk; }
-inline size_t decode_ws_bytes(int B, int H, int cap) {
-    return 256 + align256((size_t)B * H * decode_splits(cap) * (kD + 2) * sizeof(float));
+inline size_t decode_ws_bytes(int B, int H, int cap, int d = kD) {
+    return 256 + align256((size_t)B * H * decode_splits(cap) * (d + 2) * sizeof(float));
 }
 
 // ---------------------------------------------------------------- conversions

@@ -89,7 +89,7 @@ template <> struct Vec<float> {
 
 // FoX holds a batch of key rows in registers; three CTAs per SM keep enough of them in
 // flight (the bound caps it at 80 registers).
-template <typename T, bool FOX>
+template <typename T, bool FOX, int D>
 __global__ void __launch_bounds__(kThreads, FOX ? 3 : 4)
 decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                     const float *__restrict__ beta, T *__restrict__ kc, const T *__restrict__ vc,
@@ -97,10 +97,10 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                     const T *__restrict__ k_new, const float *__restrict__ log_f,
                     float *__restrict__ gc) {
     constexpr int E = Vec<T>::E;
-    constexpr int TPK = kD / E;   // lanes per key
+    constexpr int TPK = D / E;    // lanes per key (16 B each)
     constexpr int KPW = 32 / TPK; // keys per warp pass
     __shared__ float sm_m[kWarps * KPW], sm_l[kWarps * KPW];
-    __shared__ float sm_o[kWarps * KPW][kD];
+    __shared__ float sm_o[kWarps * KPW][D];
 
     const int sp = blockIdx.x, bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,15 +108,15 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
     const size_t head = (size_t)bh;
 
     float qv[E], wv[E];
-    Vec<T>::load(q + head * kD + e0, qv);
-    Vec<T>::load(w + head * kD + e0, wv);
+    Vec<T>::load(q + head * D + e0, qv);
+    Vec<T>::load(w + head * D + e0, wv);
     const float bt = beta[head];
     const float lf = FOX ? log_f[head] : 0.f;
     float *const grow = FOX ? gc + head * cap : nullptr;
     float thr = -INFINITY;  // FoX: keys scoring below it skip their value row
     if (FOX) {
         float kn[E], dn = 0.f;
-        Vec<T>::load(k_new + head * kD + e0, kn);
+        Vec<T>::load(k_new + head * D + e0, kn);
 #pragma unroll
         for (int e = 0; e < E; ++e) dn = fmaf(qv[e], kn[e], dn);
 #pragma unroll
@@ -130,8 +130,8 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.f;
 
-    T *krow = kc + head * cap * kD + e0;
-    const T *vrow = vc + head * cap * kD + e0;
+    T *krow = kc + head * cap * D + e0;
+    const T *vrow = vc + head * cap * D + e0;
     // One cached key: update it in place, score it (bias gj, log2 units) and fold it into
     // the lane's online softmax. Every lane calls it (the shuffles are warp-wide); lanes
     // whose key is past the end load nothing and store nothing.
@@ -152,14 +152,14 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
             kv[e] = fmaf(-a, wv[e], kv[e]);
             dq = fmaf(qv[e], kv[e], dq);
         }
-        if (valid) Vec<T>::store(krow + (size_t)j * kD, kv);
+        if (valid) Vec<T>::store(krow + (size_t)j * D, kv);
 #pragma unroll
         for (int off = 1; off < TPK; off <<= 1) dq += __shfl_xor_sync(0xffffffffu, dq, off);
         if (!valid) return;
         const float xl = FOX ? fmaf(gj, kLog2e, dq * scale_log2) : dq * scale_log2;
         if (FOX) {
             if (xl < thr) return;  // uniform over the key's lanes (they share dq and gj)
-            Vec<T>::load(vrow + (size_t)j * kD, vv);
+            Vec<T>::load(vrow + (size_t)j * D, vv);
         }
         const float m_new = fmaxf(m, xl);
         const float sc = exp2f(m - m_new);  // 0 while m is -inf
@@ -176,8 +176,8 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
             const bool valid = j < j1;
             float kv[E], vv[E];
             if (valid) {
-                Vec<T>::load(krow + (size_t)j * kD, kv);
-                Vec<T>::load(vrow + (size_t)j * kD, vv);
+                Vec<T>::load(krow + (size_t)j * D, kv);
+                Vec<T>::load(vrow + (size_t)j * D, vv);
             } else {
 #pragma unroll
                 for (int e = 0; e < E; ++e) kv[e] = vv[e] = 0.f;
@@ -205,7 +205,7 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
 #pragma unroll
                 for (int pb = 0; pb < kBatch; ++pb) {
                     const int j = rb + (b0 + pb) * KPW + g;
-                    kraw[pb] = (j < j1) ? Vec<T>::load_raw(krow + (size_t)j * kD)
+                    kraw[pb] = (j < j1) ? Vec<T>::load_raw(krow + (size_t)j * D)
                                         : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
@@ -229,7 +229,7 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
 #pragma unroll
     for (int e = 0; e < E; ++e) sm_o[slot][e0 + e] = o[e];
     __syncthreads();
-    if (threadIdx.x < kD) {
+    if (threadIdx.x < D) {
         const int c = threadIdx.x;
         float M = -INFINITY;
         for (int s = 0; s < kWarps * KPW; ++s) M = fmaxf(M, sm_m[s]);
@@ -241,7 +241,7 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                 Oc += sm_o[s][c] * f;
             }
         }
-        float *dst = part + (head * nsplit + sp) * (kD + 2);
+        float *dst = part + (head * nsplit + sp) * (D + 2);
         dst[2 + c] = Oc;
         if (c == 0) {
             dst[0] = M;
@@ -250,45 +250,48 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
     }
 }
 
-// One CTA of 64 threads per head: append (k_t, v_t) (and, for PaTH-FoX, the new key's
+// One CTA of D threads per head: append (k_t, v_t) (and, for PaTH-FoX, the new key's
 // gate sum 0: its logit has no bias), score the new key and merge splits.
-template <typename T, bool FOX>
-__global__ void __launch_bounds__(kD)
+template <typename T, bool FOX, int D>
+__global__ void __launch_bounds__(D)
 decode_merge_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                     T *__restrict__ kc, T *__restrict__ vc, int cache_len, int cap, int nsplit,
                     float scale_log2, const float *__restrict__ part, T *__restrict__ out,
                     float *__restrict__ gc) {
-    __shared__ float red[2];
+    __shared__ float red[D / 32];
     const int bh = blockIdx.x, c = threadIdx.x;
     const size_t head = (size_t)bh;
-    const T kt = k[head * kD + c], vt = v[head * kD + c];
-    kc[(head * cap + cache_len) * kD + c] = kt;
-    vc[(head * cap + cache_len) * kD + c] = vt;
+    const T kt = k[head * D + c], vt = v[head * D + c];
+    kc[(head * cap + cache_len) * D + c] = kt;
+    vc[(head * cap + cache_len) * D + c] = vt;
     if (FOX && c == 0) gc[head * cap + cache_len] = 0.f;
-    float d = Elt<T>::to_f(q[head * kD + c]) * Elt<T>::to_f(kt);
+    float d = Elt<T>::to_f(q[head * D + c]) * Elt<T>::to_f(kt);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
     if ((c & 31) == 0) red[c >> 5] = d;
     __syncthreads();
-    const float x_new = (red[0] + red[1]) * scale_log2;
-    const float *pp = part + head * nsplit * (kD + 2);
+    float dsum = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < D / 32; ++w2) dsum += red[w2];
+    const float x_new = dsum * scale_log2;
+    const float *pp = part + head * nsplit * (D + 2);
     float M = x_new;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pp[s * (kD + 2)]);
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pp[s * (D + 2)]);
     const float f_new = exp2f(x_new - M);
     float Ls = f_new, Oc = f_new * Elt<T>::to_f(vt);
     for (int s = 0; s < nsplit; ++s) {
-        const float ms = pp[s * (kD + 2)];
+        const float ms = pp[s * (D + 2)];
         if (ms == -INFINITY) continue;
         const float f = exp2f(ms - M);
-        Ls += pp[s * (kD + 2) + 1] * f;
-        Oc += pp[s * (kD + 2) + 2 + c] * f;
+        Ls += pp[s * (D + 2) + 1] * f;
+        Oc += pp[s * (D + 2) + 2 + c] * f;
     }
-    out[head * kD + c] = Elt<T>::from_f(Oc / Ls);
+    out[head * D + c] = Elt<T>::from_f(Oc / Ls);
 }
 
 // Both kernels of one step with the split partials at `part`; log_f and gc are used only
 // when FOX is set.
-template <typename T, bool FOX>
+template <typename T, bool FOX, int D>
 cudaError_t launch_decode_kernels(const void *q, const void *k, const void *v, const void *w,
                                   const float *beta, const float *log_f, void *k_cache,
                                   void *v_cache, float *gc, int BH, int cache_len, int cap,
@@ -297,18 +300,30 @@ cudaError_t launch_decode_kernels(const void *q, const void *k, const void *v, c
     const int used = (cache_len + kDecodeChunk - 1) / kDecodeChunk;
     if (used > 0) {
         dim3 grid(used, BH);
-        decode_split_kernel<T, FOX><<<grid, kThreads, 0, stream>>>(
+        decode_split_kernel<T, FOX, D><<<grid, kThreads, 0, stream>>>(
             static_cast<const T *>(q), static_cast<const T *>(w), beta, static_cast<T *>(k_cache),
             static_cast<const T *>(v_cache), cache_len, cap, used, sl2, part,
             static_cast<const T *>(k), log_f, gc);
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
-    decode_merge_kernel<T, FOX><<<BH, kD, 0, stream>>>(
+    decode_merge_kernel<T, FOX, D><<<BH, D, 0, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
         static_cast<T *>(k_cache), static_cast<T *>(v_cache), cache_len, cap, used, sl2, part,
         static_cast<T *>(out), gc);
     return cudaGetLastError();
+}
+
+template <typename T, bool FOX>
+cudaError_t launch_decode_d(int d, const void *q, const void *k, const void *v, const void *w,
+                            const float *beta, const float *log_f, void *k_cache, void *v_cache,
+                            float *gc, int BH, int cache_len, int cap, float scale, void *out,
+                            float *part, cudaStream_t stream) {
+    if (d == 128)
+        return launch_decode_kernels<T, FOX, 128>(q, k, v, w, beta, log_f, k_cache, v_cache, gc,
+                                                  BH, cache_len, cap, scale, out, part, stream);
+    return launch_decode_kernels<T, FOX, 64>(q, k, v, w, beta, log_f, k_cache, v_cache, gc, BH,
+                                             cache_len, cap, scale, out, part, stream);
 }
 
 }  // namespace
@@ -316,10 +331,10 @@ cudaError_t launch_decode_kernels(const void *q, const void *k, const void *v, c
 template <typename T>
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *w,
                           const float *beta, void *k_cache, void *v_cache, int BH, int cache_len,
-                          int cap, float scale, void *out, void *ws, cudaStream_t stream) {
+                          int cap, int d, float scale, void *out, void *ws, cudaStream_t stream) {
     float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
-    return launch_decode_kernels<T, false>(q, k, v, w, beta, nullptr, k_cache, v_cache, nullptr,
-                                           BH, cache_len, cap, scale, out, part, stream);
+    return launch_decode_d<T, false>(d, q, k, v, w, beta, nullptr, k_cache, v_cache, nullptr, BH,
+                                     cache_len, cap, scale, out, part, stream);
 }
 
 // PaTH-FoX decode: as launch_decode, plus the in-place gate sums gc (BH, cap) fp32 and the
@@ -327,11 +342,11 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const voi
 template <typename T>
 cudaError_t launch_fox_decode(const void *q, const void *k, const void *v, const void *w,
                               const float *beta, const float *log_f, void *k_cache,
-                              void *v_cache, float *gc, int BH, int cache_len, int cap,
+                              void *v_cache, float *gc, int BH, int cache_len, int cap, int d,
                               float scale, void *out, void *ws, cudaStream_t stream) {
     float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
-    return launch_decode_kernels<T, true>(q, k, v, w, beta, log_f, k_cache, v_cache, gc, BH,
-                                          cache_len, cap, scale, out, part, stream);
+    return launch_decode_d<T, true>(d, q, k, v, w, beta, log_f, k_cache, v_cache, gc, BH,
+                                    cache_len, cap, scale, out, part, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -373,9 +388,9 @@ static cudaError_t static_scratch_address(void **out) {
 
 size_t decode_static_scratch_bytes() { return kStaticScratchBytes; }
 
-size_t decode_static_scratch_needed(int BH, int cache_len) {
+size_t decode_static_scratch_needed(int BH, int cache_len, int d) {
     const size_t used = (size_t)((cache_len + kDecodeChunk - 1) / kDecodeChunk);
-    return (size_t)BH * used * (kD + 2) * sizeof(float);
+    return (size_t)BH * used * (d + 2) * sizeof(float);
 }
 
 // Same kernels as launch_decode, with the partials in the static scratch. The caller
@@ -383,38 +398,38 @@ size_t decode_static_scratch_needed(int BH, int cache_len) {
 template <typename T>
 cudaError_t launch_decode_static(const void *q, const void *k, const void *v, const void *w,
                                  const float *beta, void *k_cache, void *v_cache, int BH,
-                                 int cache_len, int cap, float scale, void *out,
+                                 int cache_len, int cap, int d, float scale, void *out,
                                  cudaStream_t stream) {
     void *scratch = nullptr;
     cudaError_t err = static_scratch_address(&scratch);
     if (err != cudaSuccess) return err;
     float *part = static_cast<float *>(scratch);
-    return launch_decode_kernels<T, false>(q, k, v, w, beta, nullptr, k_cache, v_cache, nullptr,
-                                           BH, cache_len, cap, scale, out, part, stream);
+    return launch_decode_d<T, false>(d, q, k, v, w, beta, nullptr, k_cache, v_cache, nullptr, BH,
+                                     cache_len, cap, scale, out, part, stream);
 }
 
 template cudaError_t launch_decode_static<float>(const void *, const void *, const void *,
                                                  const void *, const float *, void *, void *,
-                                                 int, int, int, float, void *, cudaStream_t);
+                                                 int, int, int, int, float, void *, cudaStream_t);
 template cudaError_t launch_decode_static<__nv_bfloat16>(const void *, const void *,
                                                          const void *, const void *,
                                                          const float *, void *, void *, int, int,
-                                                         int, float, void *, cudaStream_t);
+                                                         int, int, float, void *, cudaStream_t);
 
 template cudaError_t launch_decode<float>(const void *, const void *, const void *, const void *,
-                                          const float *, void *, void *, int, int, int, float,
-                                          void *, void *, cudaStream_t);
+                                          const float *, void *, void *, int, int, int, int,
+                                          float, void *, void *, cudaStream_t);
 template cudaError_t launch_decode<__nv_bfloat16>(const void *, const void *, const void *,
                                                   const void *, const float *, void *, void *,
-                                                  int, int, int, float, void *, void *,
+                                                  int, int, int, int, float, void *, void *,
                                                   cudaStream_t);
 template cudaError_t launch_fox_decode<float>(const void *, const void *, const void *,
                                               const void *, const float *, const float *, void *,
-                                              void *, float *, int, int, int, float, void *,
+                                              void *, float *, int, int, int, int, float, void *,
                                               void *, cudaStream_t);
 template cudaError_t launch_fox_decode<__nv_bfloat16>(const void *, const void *, const void *,
                                                       const void *, const float *, const float *,
-                                                      void *, void *, float *, int, int, int,
+                                                      void *, void *, float *, int, int, int, int,
                                                       float, void *, void *, cudaStream_t);
 
 }  // namespace path

@@ -27,11 +27,11 @@ cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int 
 template <typename T>
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *w,
                           const float *beta, void *k_cache, void *v_cache, int BH, int cache_len,
-                          int cap, float scale, void *out, void *ws, cudaStream_t stream);
+                          int cap, int d, float scale, void *out, void *ws, cudaStream_t stream);
 template <typename T>
 cudaError_t launch_fox_decode(const void *q, const void *k, const void *v, const void *w,
                               const float *beta, const float *log_f, void *k_cache,
-                              void *v_cache, float *gc, int BH, int cache_len, int cap,
+                              void *v_cache, float *gc, int BH, int cache_len, int cap, int d,
                               float scale, void *out, void *ws, cudaStream_t stream);
 size_t producer_ws_bytes(int B, int L, int R, int H);
 cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up, const float *conv,
@@ -39,11 +39,11 @@ cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up,
                             float *beta_out, int B, int L, int D, int R, int H, void *ws,
                             uint64_t limit_ns, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
-size_t decode_static_scratch_needed(int BH, int cache_len);
+size_t decode_static_scratch_needed(int BH, int cache_len, int d);
 template <typename T>
 cudaError_t launch_decode_static(const void *q, const void *k, const void *v, const void *w,
                                  const float *beta, void *k_cache, void *v_cache, int BH,
-                                 int cache_len, int cap, float scale, void *out,
+                                 int cache_len, int cap, int d, float scale, void *out,
                                  cudaStream_t stream);
 }  // namespace path
 
@@ -72,6 +72,11 @@ path_status check_sizes(int B, int H, int L, int d, int dtype) {
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_DTYPE;
     if ((long long)B * H > PATH_MAX_HEADS || L > PATH_MAX_LEN) return PATH_ERR_SHAPE;
     return PATH_OK;
+}
+
+// Decode works on head sizes 64 and 128 (the forward on 64 only).
+path_status check_decode_sizes(int B, int H, int cap, int d, int dtype) {
+    return check_sizes(B, H, cap, d == 128 ? kD : (d == kD ? kD : -1), dtype);
 }
 
 path_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA; }
@@ -134,12 +139,17 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
 extern "C" {
 
 size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
-    if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
     switch (op) {
-        case PATH_OP_FWD: return fwd_layout(B, H, L, elt_bytes(dtype), false).total;
-        case PATH_OP_FOX_FWD: return fwd_layout(B, H, L, elt_bytes(dtype), true).total;
-        case PATH_OP_DECODE: return decode_ws_bytes(B, H, L);
-        case PATH_OP_FOX_DECODE: return decode_ws_bytes(B, H, L);
+        case PATH_OP_FWD:
+        case PATH_OP_FOX_FWD:
+            if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+            return fwd_layout(B, H, L, elt_bytes(dtype), op == PATH_OP_FOX_FWD).total;
+        default: break;
+    }
+    if (check_decode_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+    switch (op) {
+        case PATH_OP_DECODE: return decode_ws_bytes(B, H, L, d);
+        case PATH_OP_FOX_DECODE: return decode_ws_bytes(B, H, L, d);
         default: return 0;
     }
 }
@@ -213,7 +223,7 @@ path_status path_decode_step(const void *q, const void *k, const void *v, const 
                              const float *beta, void *k_cache, void *v_cache, int B, int H,
                              int cache_len, int cache_cap, int d, int dtype, float scale,
                              void *out, void *ws, size_t ws_bytes, void *stream) {
-    path_status st = check_sizes(B, H, cache_cap, d, dtype);
+    path_status st = check_decode_sizes(B, H, cache_cap, d, dtype);
     if (st != PATH_OK) return st;
     if (cache_len < 0) return PATH_ERR_SHAPE;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
@@ -223,13 +233,13 @@ path_status path_decode_step(const void *q, const void *k, const void *v, const 
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(w, 16) ||
         !aligned(beta, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return PATH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, H, cache_cap))) != PATH_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, H, cache_cap, d))) != PATH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == PATH_BF16)
         return from_cuda(launch_decode<__nv_bfloat16>(q, k, v, w, beta, k_cache, v_cache, B * H,
-                                                      cache_len, cache_cap, scale, out, ws, s));
+                                                      cache_len, cache_cap, d, scale, out, ws, s));
     return from_cuda(launch_decode<float>(q, k, v, w, beta, k_cache, v_cache, B * H, cache_len,
-                                          cache_cap, scale, out, ws, s));
+                                          cache_cap, d, scale, out, ws, s));
 }
 
 path_status path_fox_decode_step(const void *q, const void *k, const void *v, const void *w,
@@ -237,7 +247,7 @@ path_status path_fox_decode_step(const void *q, const void *k, const void *v, co
                                  void *v_cache, float *g_cache, int B, int H, int cache_len,
                                  int cache_cap, int d, int dtype, float scale, void *out,
                                  void *ws, size_t ws_bytes, void *stream) {
-    path_status st = check_sizes(B, H, cache_cap, d, dtype);
+    path_status st = check_decode_sizes(B, H, cache_cap, d, dtype);
     if (st != PATH_OK) return st;
     if (cache_len < 0) return PATH_ERR_SHAPE;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
@@ -249,21 +259,21 @@ path_status path_fox_decode_step(const void *q, const void *k, const void *v, co
         !aligned(beta, 4) || !aligned(log_f, 4) || !aligned(k_cache, 16) ||
         !aligned(v_cache, 16) || !aligned(g_cache, 16) || !aligned(out, 16))
         return PATH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, H, cache_cap))) != PATH_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, H, cache_cap, d))) != PATH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == PATH_BF16)
         return from_cuda(launch_fox_decode<__nv_bfloat16>(q, k, v, w, beta, log_f, k_cache,
                                                           v_cache, g_cache, B * H, cache_len,
-                                                          cache_cap, scale, out, ws, s));
+                                                          cache_cap, d, scale, out, ws, s));
     return from_cuda(launch_fox_decode<float>(q, k, v, w, beta, log_f, k_cache, v_cache, g_cache,
-                                              B * H, cache_len, cache_cap, scale, out, ws, s));
+                                              B * H, cache_len, cache_cap, d, scale, out, ws, s));
 }
 
 path_status path_decode_step_noalloc(const void *q, const void *k, const void *v, const void *w,
                                      const float *beta, void *k_cache, void *v_cache, int B,
                                      int H, int cache_len, int cache_cap, int d, int dtype,
                                      float scale, void *out, void *stream) {
-    path_status st = check_sizes(B, H, cache_cap, d, dtype);
+    path_status st = check_decode_sizes(B, H, cache_cap, d, dtype);
     if (st != PATH_OK) return st;
     if (cache_len < 0) return PATH_ERR_SHAPE;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
@@ -273,15 +283,15 @@ path_status path_decode_step_noalloc(const void *q, const void *k, const void *v
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(w, 16) ||
         !aligned(beta, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return PATH_ERR_ALIGN;
-    if (decode_static_scratch_needed(B * H, cache_len) > decode_static_scratch_bytes())
+    if (decode_static_scratch_needed(B * H, cache_len, d) > decode_static_scratch_bytes())
         return PATH_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == PATH_BF16)
         return from_cuda(launch_decode_static<__nv_bfloat16>(q, k, v, w, beta, k_cache, v_cache,
-                                                             B * H, cache_len, cache_cap, scale,
-                                                             out, s));
+                                                             B * H, cache_len, cache_cap, d,
+                                                             scale, out, s));
     return from_cuda(launch_decode_static<float>(q, k, v, w, beta, k_cache, v_cache, B * H,
-                                                 cache_len, cache_cap, scale, out, s));
+                                                 cache_len, cache_cap, d, scale, out, s));
 }
 
 namespace {

@@ -14,8 +14,8 @@
  *  - Device pointers, contiguous row-major: q, k, v, w, out are (B, H, L, d);
  *    beta, log_f, lse are (B, H, L) fp32. Element type of q, k, v, w, out and of
  *    the decode caches is given by `dtype` (PATH_F32 or PATH_BF16).
- *  - d must be 64 (the head size the pages benchmark). Anything else returns
- *    PATH_ERR_SHAPE.
+ *  - d must be 64 (the head size the pages benchmark); the decode steps also take
+ *    d = 128 (the larger head the pages mention). Anything else returns PATH_ERR_SHAPE.
  *  - Every tensor pointer and the workspace must be 16-byte aligned
  *    (PATH_ERR_ALIGN); the workspace must be 256-byte aligned.
  *  - The caller owns every buffer, the workspace included. The library
@@ -67,8 +67,8 @@ typedef enum {
 #define PATH_MAX_LEN (1 << 22)
 
 /*
- * Workspace bytes that `op` needs for the given sizes (L = cache capacity for
- * PATH_OP_DECODE). Returns 0 for invalid arguments. The workspace holds the
+ * Workspace bytes that `op` needs for the given sizes (L = cache capacity and d = 64 or
+ * 128 for PATH_OP_DECODE and PATH_OP_FOX_DECODE). Returns 0 for invalid arguments. The workspace holds the
  * per-block factors of the forward (boundary-adjusted queries and keys, the
  * dense block transitions, the diagonal-block logits, the FoX prefix sums)
  * or the split partial results of decode, plus a 256-byte status header.
@@ -147,7 +147,7 @@ path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H,
  *      written back into k_cache (rounded to dtype);
  *   2. k_t, v_t are appended untransformed at index cache_len;
  *   3. out = softmax_j(scale * q_t . k_j) v_j over j <= cache_len.
- *   q, k, v, w : (B, H, d) dtype         beta : (B, H) fp32
+ *   q, k, v, w : (B, H, d) dtype         beta : (B, H) fp32      d = 64 or 128
  *   k_cache, v_cache : (B, H, cache_cap, d) dtype, updated in place
  *   out : (B, H, d) dtype
  * On return the caches hold cache_len + 1 valid entries; the caller advances its
@@ -192,7 +192,7 @@ path_status path_fox_decode_step(const void *q, const void *k, const void *v, co
  * Same arguments and results as path_decode_step, minus ws/ws_bytes. The split partial
  * results go to a fixed PATH_NOALLOC_SCRATCH_BYTES array compiled into the library, held
  * by every GPU that loads the library until the process exits. Limit:
- * B * H * ceil(cache_len / 1024) * 264 bytes <= PATH_NOALLOC_SCRATCH_BYTES (for example
+ * B * H * ceil(cache_len / 1024) * (d + 2) * 4 bytes <= PATH_NOALLOC_SCRATCH_BYTES (for example
  * B*H = 1024 heads with up to 63488 cached keys); larger problems return
  * PATH_ERR_WORKSPACE before any launch. The call allocates nothing. The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that device

@@ -61,6 +61,8 @@ BF16_L2048 = FwdWorkload("path_fwd_bf16_B4H16L2048", 4, 16, 2048, D, torch.bfloa
 BF16_L4096 = FwdWorkload("path_fwd_bf16_B32H32L4096", 32, 32, 4096, D, torch.bfloat16, 3, BETA_CLIP, False)
 FOX_L16384 = FwdWorkload("path_fox_fwd_bf16_B8H16L16384", 8, 16, 16384, D, torch.bfloat16, 4, BETA_CLIP, True)
 DECODE_32K = DecodeWorkload("path_decode_bf16_B32H32N32768x64", 32, 32, 32768, 64, D, torch.bfloat16, 5, 1000)
+# Head size 128 at the same model width (H*d = 2048): 16 heads of 128.
+DECODE_32K_D128 = DecodeWorkload("path_decode_bf16_B32H16d128N32768x64", 32, 16, 32768, 64, 128, torch.bfloat16, 5, 1000)
 # PaTH-FoX decode: the same cache and steps plus forget gates (prefix gate sums, log f per step).
 FOX_DECODE_32K = DecodeWorkload("path_fox_decode_bf16_B32H32N32768x64", 32, 32, 32768, 64, D, torch.bfloat16, 5, 1000)
 

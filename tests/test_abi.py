@@ -60,6 +60,15 @@ def test_workspace_sizes(lib):
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 64, lib.BF16) == \
         256 + (part + 255) // 256 * 256
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 32, lib.BF16) == 0
+    # head size 128: decode only; partials (m, l, o[128])
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, lib.BF16) == 0
+    assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, lib.BF16) == 0
+    part128 = 4 * 2 * 130 * 4
+    assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 128, lib.BF16) == \
+        256 + (part128 + 255) // 256 * 256
+    assert lib.path_workspace_bytes(lib.OP_FOX_DECODE, 2, 2, 2048, 128, lib.F32) == \
+        256 + (part128 + 255) // 256 * 256
+    assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 96, lib.BF16) == 0
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, 7) == 0
     assert lib.path_workspace_bytes(9, 1, 1, 128, 64, lib.BF16) == 0
 
@@ -110,7 +119,8 @@ def test_decode_argument_checks(so):
                                    ctypes.c_size_t(a["ws_bytes"]), None)
     assert call(cache_len=16) == 6
     assert call(cache_len=-1) == 2
-    assert call(d=128) == 2
+    assert call(d=96) == 2
+    assert call(d=128, ws_bytes=8) == 5  # head size 128 is accepted by decode
     assert call(kc=None) == 1
     assert call(kc=FAKE + 2) == 4
     assert call(ws_bytes=8) == 5
@@ -129,7 +139,8 @@ def test_fox_decode_argument_checks(so, lib):
                                        ctypes.c_size_t(a["ws_bytes"]), None)
     assert call(cache_len=16) == 6
     assert call(cache_len=-1) == 2
-    assert call(d=128) == 2
+    assert call(d=96) == 2
+    assert call(d=128, ws_bytes=8) == 5  # head size 128 accepted, workspace too small
     assert call(dtype=5) == 3
     assert call(lf=None) == 1
     assert call(gc=None) == 1

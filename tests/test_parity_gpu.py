@@ -368,30 +368,30 @@ def test_fox_zero_gate_has_no_exit(lib):
 
 # ---------------------------------------------------------------- decode
 
-def _decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None):
-    wl = pi.DecodeWorkload("t", B, H, n0, steps, 64, dtype, seed, 1000 + seed)
+def _decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None, d=64):
+    wl = pi.DecodeWorkload("t", B, H, n0, steps, d, dtype, seed, 1000 + seed)
     cap = n0 + steps
     kc, vc = pi.make_decode_prefix(wl, cap, device="cuda")
     heads = list(range(B * H)) if check_heads is None else check_heads
-    hk = kc.reshape(B * H, cap, 64)[heads, :n0].cpu()
-    hv = vc.reshape(B * H, cap, 64)[heads, :n0].cpu()
+    hk = kc.reshape(B * H, cap, d)[heads, :n0].cpu()
+    hv = vc.reshape(B * H, cap, d)[heads, :n0].cpu()
     ocache = oracle.DecodeCache(hk, hv, cap)
     ws = lib.new_workspace(lib.OP_DECODE, B, H, cap, lib.BF16 if dtype == torch.bfloat16 else lib.F32,
-                           "cuda")
+                           "cuda", d)
     worst = 0.0
     for t in range(steps):
         s = pi.make_decode_step(wl, t, device="cuda")
-        pre = kc.reshape(B * H, cap, 64)[heads[:2], :n0 + t].double().cpu().numpy()
+        pre = kc.reshape(B * H, cap, d)[heads[:2], :n0 + t].double().cpu().numpy()
         o = lib.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc, n0 + t,
                                  workspace=ws)
         sel = {k: v.reshape(B * H, -1)[heads].cpu() for k, v in s.items()}
         ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
-        got = o.reshape(B * H, 64)[heads].double().cpu().numpy()
+        got = o.reshape(B * H, d)[heads].double().cpu().numpy()
         worst = max(worst, np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
         if dtype == torch.bfloat16:
             assert np.abs(got - ref).max() <= BF16_MAX_ABS
         # the updated keys equal H_t applied to the pre-step keys, rounded once
-        post = kc.reshape(B * H, cap, 64)[heads[:2], :n0 + t + 1].double().cpu().numpy()
+        post = kc.reshape(B * H, cap, d)[heads[:2], :n0 + t + 1].double().cpu().numpy()
         w = sel["w"][:2].double().numpy()
         b = sel["beta"][:2].double().numpy().reshape(2, 1)
         expect = pre - b[:, :, None] * np.einsum("hjc,hc->hj", pre, w)[:, :, None] * w[:, None, :]
@@ -413,6 +413,15 @@ def test_decode_small_bf16_from_empty_and_ragged(lib):
     _decode_run(lib, 1, 2, 0, 5, torch.bfloat16, seed=2)
     worst = _decode_run(lib, 2, 2, 1020, 8, torch.bfloat16, seed=3)
     assert worst <= 5e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_decode_head_dim_128(lib, dtype):
+    # head size 128: 16 lanes per bf16 key row (32 per fp32 row); empty prefix, then lengths
+    # crossing a split boundary
+    _decode_run(lib, 1, 2, 0, 3, dtype, seed=31, d=128)
+    worst = _decode_run(lib, 2, 2, 1021, 5, dtype, seed=32, d=128)
+    assert worst <= (F32_MAX_REL if dtype == torch.float32 else 5e-2)
 
 
 def test_decode_workload_sampled_heads(lib):
@@ -444,16 +453,16 @@ def test_decode_workload_sampled_heads(lib):
 
 # ---------------------------------------------------------------- PaTH-FoX decode
 
-def _fox_decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None):
-    wl = pi.DecodeWorkload("t", B, H, n0, steps, 64, dtype, seed, 1000 + seed)
+def _fox_decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None, d=64):
+    wl = pi.DecodeWorkload("t", B, H, n0, steps, d, dtype, seed, 1000 + seed)
     cap = n0 + steps
     kc, vc, gc = pi.make_fox_decode_prefix(wl, cap, device="cuda")
     heads = list(range(B * H)) if check_heads is None else check_heads
-    ocache = oracle.DecodeCache(kc.reshape(B * H, cap, 64)[heads, :n0].cpu(),
-                                vc.reshape(B * H, cap, 64)[heads, :n0].cpu(), cap, fox=True,
+    ocache = oracle.DecodeCache(kc.reshape(B * H, cap, d)[heads, :n0].cpu(),
+                                vc.reshape(B * H, cap, d)[heads, :n0].cpu(), cap, fox=True,
                                 g_prefix=gc.reshape(B * H, cap)[heads, :n0].cpu())
     ws = lib.new_workspace(lib.OP_FOX_DECODE, B, H, cap,
-                           lib.BF16 if dtype == torch.bfloat16 else lib.F32, "cuda")
+                           lib.BF16 if dtype == torch.bfloat16 else lib.F32, "cuda", d)
     worst = 0.0
     for t in range(steps):
         s = pi.make_decode_step(wl, t, device="cuda", fox=True)
@@ -463,7 +472,7 @@ def _fox_decode_run(lib, B, H, n0, steps, dtype, seed, check_heads=None):
         sel = {k: v.reshape(B * H, -1)[heads].cpu() for k, v in s.items()}
         ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
                           log_f=sel["log_f"])
-        got = o.reshape(B * H, 64)[heads].double().cpu().numpy()
+        got = o.reshape(B * H, d)[heads].double().cpu().numpy()
         worst = max(worst, np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
         if dtype == torch.bfloat16:
             assert np.abs(got - ref).max() <= BF16_MAX_ABS
@@ -487,6 +496,12 @@ def test_fox_decode_bf16_from_empty_and_across_splits(lib):
     _fox_decode_run(lib, 1, 2, 0, 5, torch.bfloat16, seed=12)
     worst = _fox_decode_run(lib, 2, 2, 1021, 6, torch.bfloat16, seed=13)
     assert worst <= 5e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fox_decode_head_dim_128(lib, dtype):
+    worst = _fox_decode_run(lib, 2, 2, 1500, 4, dtype, seed=33, d=128)
+    assert worst <= (F32_MAX_REL if dtype == torch.float32 else 5e-2)
 
 
 def test_fox_decode_zero_gate_equals_path_decode(lib):
