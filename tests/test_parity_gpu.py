@@ -94,6 +94,61 @@ def test_beta_extremes_bf16(lib):
         check_bf16(out, ref, lse, ref_lse)
 
 
+def test_zero_directions_are_plain_attention(lib):
+    # w = 0 makes every transition the identity whatever beta is: plain causal softmax
+    # attention, which the oracle computes with beta = 0
+    for dtype in (torch.float32, torch.bfloat16):
+        x = pi.make_fwd_inputs(2, 2, 300, dtype=dtype, seed=71, device="cuda")
+        x["w"] = torch.zeros_like(x["w"])
+        out, lse = run_fwd(lib, x)
+        ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"],
+                                       torch.zeros_like(x["beta"]))
+        if dtype == torch.float32:
+            rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+            assert rel <= F32_MAX_REL, rel
+        else:
+            check_bf16(out, ref, lse, ref_lse)
+
+
+def test_exact_reflections_fp32(lib):
+    # beta = 2: every transition is a Householder reflection (orthogonal)
+    x = pi.make_fwd_inputs(1, 2, 257, dtype=torch.float32, seed=72, clip=0.0, device="cuda")
+    x["beta"] = torch.full_like(x["beta"], 2.0)
+    out, lse = run_fwd(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert rel <= F32_MAX_REL, rel
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
+
+
+def test_maximum_head_count(lib):
+    # B * H at the accepted maximum (65535 heads, the grid's y limit): spot-check heads
+    B, H, L = 65535, 1, 64
+    x = pi.make_fwd_inputs(B, H, L, seed=73, device="cuda")
+    out, lse = run_fwd(lib, x)
+    torch.cuda.synchronize()
+    heads = [0, 1, 32767, 65533, 65534]
+    sel = {k: v[heads].cpu() for k, v in x.items()}
+    ref, ref_lse = oracle.path_fwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
+    check_bf16(out[heads], ref, lse[heads], ref_lse)
+    assert torch.isfinite(out).all()
+
+
+def test_very_long_sequence_sampled(lib):
+    # one head of 2^18 tokens (4096 key blocks), sampled rows including both ends
+    x = pi.make_fwd_inputs(1, 1, 1 << 18, seed=74, device="cuda")
+    out, lse = run_fwd(lib, x)
+    torch.cuda.synchronize()
+    rows = np.array([[0, 0], [0, 1], [0, 63], [0, 64], [0, 131071], [0, 131072],
+                     [0, (1 << 18) - 2], [0, (1 << 18) - 1], [0, 200000], [0, 77777]])
+    h = {k: v.reshape(1, *v.shape[2:]).cpu() for k, v in x.items()}
+    ref, ref_lse = oracle.path_rows(h["q"], h["k"], h["v"], h["w"], h["beta"], rows)
+    got = out.reshape(1 << 18, 64)[torch.as_tensor(rows[:, 1], device="cuda")]
+    got_lse = lse.reshape(1 << 18)[torch.as_tensor(rows[:, 1], device="cuda")]
+    check_bf16(got, ref)
+    assert np.abs(got_lse.double().cpu().numpy() - ref_lse).max() <= BF16_MAX_ABS
+
+
 def test_custom_scale(lib):
     x = pi.make_fwd_inputs(1, 2, 150, seed=9, device="cuda")
     out, lse = run_fwd(lib, x, scale=0.3)
