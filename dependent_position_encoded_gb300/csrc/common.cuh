@@ -36,7 +36,7 @@ constexpr uint32_t kStatusTimeout = 7u;
 struct FwdLayout {
     int BH, L, nblk, Lp, elt;
     size_t off_qt, off_kp, off_dg, off_pr, off_c2, off_pbase, off_mpre, off_kpre, off_fb;
-    size_t off_btot, off_bmin, off_boff, off_bkmax, total;
+    size_t off_btot, off_bmin, off_boff, off_bkmax, off_qn, off_dmax, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -67,6 +67,7 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     // key-norm maxima they come from
     lay.off_c2 = lay.off_pbase = lay.off_mpre = lay.off_kpre = lay.off_fb = off;
     lay.off_btot = lay.off_bmin = lay.off_boff = lay.off_bkmax = off;
+    lay.off_qn = lay.off_dmax = off;
     if (fox) {
         const size_t nb = bh * lay.nblk;
         off = align256(off + bh * lay.Lp * sizeof(float));
@@ -86,6 +87,12 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
         off = align256(off + nb * sizeof(double));
         lay.off_bkmax = off;
         off = align256(off + nb * sizeof(float));
+        // per query row: |q~_i| and the largest entry of its diagonal-table row (written by
+        // the bf16 preprocessing so that the early-exit pass need not re-read the rows)
+        lay.off_qn = off;
+        off = align256(off + bh * lay.Lp * sizeof(float));
+        lay.off_dmax = off;
+        off = align256(off + bh * lay.Lp * sizeof(float));
     }
     lay.total = off;
     return lay;

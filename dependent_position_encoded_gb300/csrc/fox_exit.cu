@@ -115,9 +115,10 @@ __device__ __forceinline__ double block_prefix(const float *__restrict__ log_f, 
 }
 
 // Per key block (64 threads): its total of log f, the minimum of its in-block prefix sums
-// (both fp64) and the largest |k~_j| over its real tokens (k~ from the preprocessing
-// workspace, which must already be written).
-template <typename T>
+// (both fp64) and, with ROWS, the largest |k~_j| over its real tokens (k~ from the
+// preprocessing workspace, which must already be written; without ROWS the bf16
+// preprocessing has written that maximum itself).
+template <typename T, bool ROWS>
 __global__ void __launch_bounds__(64)
 fox_block_kernel(const float *__restrict__ log_f, const T *__restrict__ kp, int L, int nblk,
                  double *__restrict__ btot, double *__restrict__ bmin, float *__restrict__ bkmax) {
@@ -127,7 +128,7 @@ fox_block_kernel(const float *__restrict__ log_f, const T *__restrict__ kp, int 
     const double loc = block_prefix(log_f, L, bh, b, warp_tot);
     const int t = b * kC + r;
     float kn = 0.f;
-    if (t < L) kn = sqrtf(row_norm2(kp + (((size_t)bh * nblk + b) * (2 * kC) + r) * kD));
+    if (ROWS && t < L) kn = sqrtf(row_norm2(kp + (((size_t)bh * nblk + b) * (2 * kC) + r) * kD));
     double m = loc;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -143,7 +144,7 @@ fox_block_kernel(const float *__restrict__ log_f, const T *__restrict__ kp, int 
     if (r == kC - 1) btot[(size_t)bh * nblk + b] = loc;
     if (r == 0) {
         bmin[(size_t)bh * nblk + b] = fmin(warp_min[0], warp_min[1]);
-        bkmax[(size_t)bh * nblk + b] = fmaxf(warp_kmax[0], warp_kmax[1]);
+        if (ROWS) bkmax[(size_t)bh * nblk + b] = fmaxf(warp_kmax[0], warp_kmax[1]);
     }
 }
 
@@ -225,11 +226,14 @@ fox_prefix_kernel(const double *__restrict__ btot, const double *__restrict__ bm
 // c2_i = log2(e) (offset of the block + in-block prefix), as an fp32 pair hi + lo (so that
 // differences c2_i - c2_j stay accurate to their own size however large the sums grow);
 // then first[bh][qb], the lowest key block any of its rows needs (qb itself when no
-// earlier block is needed).
-template <typename T, typename D>
+// earlier block is needed). With ROWS the row norms |q~_i| and diagonal-table maxima are
+// read from the rows; without, from the per-row values the bf16 preprocessing wrote.
+template <typename T, typename D, bool ROWS>
 __global__ void __launch_bounds__(64)
 fox_exit_kernel(const float *__restrict__ log_f, const double *__restrict__ boff,
-                const T *__restrict__ qt, const D *__restrict__ dg, float *__restrict__ c2,
+                const T *__restrict__ qt, const D *__restrict__ dg,
+                const float *__restrict__ qn_row, const float *__restrict__ dmax_row,
+                float *__restrict__ c2,
                 float *__restrict__ pbase, const float *__restrict__ mpre,
                 const float *__restrict__ kpre, int L, int Lp, int nblk, float abs_scale_log2,
                 int *__restrict__ first) {
@@ -251,8 +255,10 @@ fox_exit_kernel(const float *__restrict__ log_f, const double *__restrict__ boff
     }
     int lo = qb;
     if (i < L && qb > 0) {
-        const float qn = sqrtf(row_norm2(qt + ((size_t)bh * Lp + i) * kD));
-        const float dmax = row_max(dg + (((size_t)bh * nblk + qb) * kC + r) * kC);
+        const float qn = ROWS ? sqrtf(row_norm2(qt + ((size_t)bh * Lp + i) * kD))
+                              : qn_row[(size_t)bh * Lp + i];
+        const float dmax = ROWS ? row_max(dg + (((size_t)bh * nblk + qb) * kC + r) * kC)
+                                : dmax_row[(size_t)bh * Lp + i];
         const float rhs = dmax - kExitLog2;
         const float ci = c_hi;
         const float qk = 2.f * abs_scale_log2 * qn;
@@ -291,26 +297,32 @@ cudaError_t launch_fox_prepare(const float *log_f, int BH, int L, int elt_bytes,
     double *bmin = reinterpret_cast<double *>(basep + lay.off_bmin);
     double *boff = reinterpret_cast<double *>(basep + lay.off_boff);
     float *bkmax = reinterpret_cast<float *>(basep + lay.off_bkmax);
+    const float *qn = reinterpret_cast<const float *>(basep + lay.off_qn);
+    const float *dmax = reinterpret_cast<const float *>(basep + lay.off_dmax);
     const float s = fabsf(scale) * kLog2e;
     const dim3 grid(lay.nblk, BH);
+    // bf16: the tensor-core preprocessing has written |q~|, the table maxima and the
+    // key-norm maxima; fp32: they are read from the rows
     if (elt_bytes == 2)
-        fox_block_kernel<__nv_bfloat16><<<grid, 64, 0, stream>>>(
+        fox_block_kernel<__nv_bfloat16, false><<<grid, 64, 0, stream>>>(
             log_f, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_kp), L, lay.nblk, btot,
             bmin, bkmax);
     else
-        fox_block_kernel<float><<<grid, 64, 0, stream>>>(
+        fox_block_kernel<float, true><<<grid, 64, 0, stream>>>(
             log_f, reinterpret_cast<const float *>(basep + lay.off_kp), L, lay.nblk, btot, bmin,
             bkmax);
     fox_prefix_kernel<<<BH, 256, 0, stream>>>(btot, bmin, bkmax, lay.nblk, boff, mpre, kpre);
     if (elt_bytes == 2)
-        fox_exit_kernel<__nv_bfloat16, __half><<<grid, 64, 0, stream>>>(
+        fox_exit_kernel<__nv_bfloat16, __half, false><<<grid, 64, 0, stream>>>(
             log_f, boff, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_qt),
-            reinterpret_cast<const __half *>(basep + lay.off_dg), c2, pbase, mpre, kpre, L, lay.Lp,
+            reinterpret_cast<const __half *>(basep + lay.off_dg), qn, dmax, c2, pbase, mpre, kpre,
+            L, lay.Lp,
             lay.nblk, s, first);
     else
-        fox_exit_kernel<float, float><<<grid, 64, 0, stream>>>(
+        fox_exit_kernel<float, float, true><<<grid, 64, 0, stream>>>(
             log_f, boff, reinterpret_cast<const float *>(basep + lay.off_qt),
-            reinterpret_cast<const float *>(basep + lay.off_dg), c2, pbase, mpre, kpre, L, lay.Lp,
+            reinterpret_cast<const float *>(basep + lay.off_dg), qn, dmax, c2, pbase, mpre, kpre, L,
+            lay.Lp,
             lay.nblk, s, first);
     return cudaGetLastError();
 }

@@ -231,13 +231,18 @@ __device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, i
 // Thread layout: warp w reads TMEM lanes 32 (w mod 4) .. +31 (the accumulator rows lr) and
 // handles the 32-column half hf = w / 4 of every 64-column block of its row, so each row's
 // epilogue is split between two warps.
+// FOX: the forget-gate bias on the diagonal table, and per query row |q~_i| (qn) and the
+// largest entry of its table row (dmax), per key block the largest |k~_j| (bkmax), all from
+// the rounded values the workspace holds, for the early-exit pass.
+template <bool FOX>
 __global__ void __launch_bounds__(kThreads, 3)
 ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ beta,
                      const float *__restrict__ log_f, int L, int Lp, int nblk, float scale_log2,
                      __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ kp,
-                     __half *__restrict__ dg, uint32_t *status, uint64_t limit_ns) {
+                     __half *__restrict__ dg, float *__restrict__ qn, float *__restrict__ dmax,
+                     float *__restrict__ bkmax, uint32_t *status, uint64_t limit_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -280,7 +285,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     // beta is first needed after MMA1: its load overlaps the TMA loads and MMA1
     const float beta_r = (r < kC && t0 + r < L) ? beta[head + t0 + r] : 0.f;
-    if (log_f != nullptr && warp == 1) {
+    if (FOX && warp == 1) {
         const int ln = r - 32;
         const int ta = t0 + 2 * ln, tb = ta + 1;
         const float a = (ta < L) ? log_f[head + ta] : 0.f;
@@ -471,14 +476,22 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int c = 0; c < 32; ++c) y[c] -= x[c];
         store_global_half(qt + ((size_t)bh * Lp + t0 + i) * kD + c0, y);
+        float qs = 0.f;
+        if (FOX) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
+                qs = fmaf(r16, r16, qs);
+            }
+        }
         // diagonal logits, log2 units, j <= i
         tmem_row32(tmem + lane_off + 64 + c0, x);
-        const float lci = (log_f != nullptr) ? lc[i] : 0.f;
+        const float lci = FOX ? lc[i] : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int jj = c0 + j;
             float v = scale_log2 * x[j];
-            if (log_f != nullptr) v += kLog2e * (lci - lc[jj]);
+            if (FOX) v += kLog2e * (lci - lc[jj]);
             x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
         }
         uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
@@ -486,6 +499,15 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 4; ++c)
             dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
                                pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+        if (FOX) {
+            // half-row partials into the Lq slot (MMA4x, its only reader, has completed)
+            float dm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dm = fmaxf(dm, __half2float(__float2half_rn(x[j])));
+            float *part = reinterpret_cast<float *>(sm + T_LQ);
+            part[(i * 2 + hf) * 2] = qs;
+            part[(i * 2 + hf) * 2 + 1] = dm;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -500,6 +522,13 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a2 + 128 * kk, b2 + 128 * kk, ID2, kk > 0);
     }
     if (r == 0) umma_commit(bar_mma);
+    if (FOX && ok && hf == 0 && lr < kC) {
+        // (q~, table) row lr: combine the two half-row partials (MMA4y runs meanwhile)
+        const float *part = reinterpret_cast<const float *>(sm + T_LQ);
+        const size_t row = (size_t)bh * Lp + t0 + lr;
+        qn[row] = sqrtf(part[(lr * 2) * 2] + part[(lr * 2 + 1) * 2]);
+        dmax[row] = fmaxf(part[(lr * 2) * 2 + 1], part[(lr * 2 + 1) * 2 + 1]);
+    }
     if (ok) ok = wait_all(bar_mma, 1);
     if (ok) {
         tc_fence_after();
@@ -518,10 +547,29 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] -= x[c];
             store_global_half(kp_blk + j * kD + c0, y);
+            if (FOX) {
+                float ks = 0.f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
+                    ks = fmaf(r16, r16, ks);
+                }
+                // rows past L are padding: they take part in no logit
+                reinterpret_cast<float *>(sm + T_LQ)[256 + j * 2 + hf] = (t0 + j < L) ? ks : 0.f;
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (FOX && ok && warp == 2) {
+        // largest |k~_j| of the block: lane l takes rows l and l + 32
+        const float *kpart = reinterpret_cast<const float *>(sm + T_LQ) + 256;
+        float m = fmaxf(sqrtf(kpart[lane * 2] + kpart[lane * 2 + 1]),
+                        sqrtf(kpart[(lane + 32) * 2] + kpart[(lane + 32) * 2 + 1]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) bkmax[blk_base] = m;
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -574,17 +622,21 @@ cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, co
     if (!make_input_map(&tq, q, L, BH) || !make_input_map(&tk, k, L, BH) ||
         !make_input_map(&tw, w, L, BH))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(ut_prepare_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool fox = log_f != nullptr;
+    auto kern = fox ? ut_prepare_tc_kernel<true> : ut_prepare_tc_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     dim3 grid(lay.nblk, BH);
-    ut_prepare_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(
         tq, tk, tw, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
         reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_qt),
         reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_kp),
-        reinterpret_cast<__half *>(basep + lay.off_dg), reinterpret_cast<uint32_t *>(basep),
-        limit_ns);
+        reinterpret_cast<__half *>(basep + lay.off_dg),
+        fox ? reinterpret_cast<float *>(basep + lay.off_qn) : nullptr,
+        fox ? reinterpret_cast<float *>(basep + lay.off_dmax) : nullptr,
+        fox ? reinterpret_cast<float *>(basep + lay.off_bkmax) : nullptr,
+        reinterpret_cast<uint32_t *>(basep), limit_ns);
     return cudaGetLastError();
 }
 
