@@ -41,8 +41,12 @@
 //   warps 14 / 15    issue tile A's / B's P.V MMAs and release the stages; warp 14 also
 //                    feeds the TMA ring (both duties poll, neither blocks the other);
 //   warp 12 also owns TMEM.
-// One issuing thread sustains one M = 128, K = 16 MMA per ~150 cycles whatever N is, so
-// each MMA stream has its own thread. The state tile and the P tile are single-buffered:
+// Each MMA stream has its own issuing thread because the streams wait on different
+// conditions (a thread blocked on one would hold back the others); throughput is not the
+// reason: one thread issuing back to back keeps the SM's tensor pipe at its math rate for
+// N >= 128 (about 65 / 97 / 129 cycles per K = 16 MMA at N = 128 / 192 / 256), N = 64 costs
+// about 48 cycles against 32 of math, and more issuers do not raise an SM's rate.
+// The state tile and the P tile are single-buffered:
 // the state is rewritten once the S|state MMA that read it has completed, P once the
 // tile's previous P.V has completed.
 #include "common.cuh"
