@@ -87,10 +87,10 @@ template <> struct Vec<float> {
     }
 };
 
-// FoX holds a batch of key rows in registers; three CTAs per SM keep enough of them in
-// flight (the bound caps it at 80 registers).
+// Both variants hold rows of several passes in registers; three CTAs per SM keep enough
+// bytes in flight (the bound caps them at 80 registers).
 template <typename T, bool FOX, int D>
-__global__ void __launch_bounds__(kThreads, FOX ? 3 : 4)
+__global__ void __launch_bounds__(kThreads, 3)
 decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                     const float *__restrict__ beta, T *__restrict__ kc, const T *__restrict__ vc,
                     int cache_len, int cap, int nsplit, float scale_log2, float *__restrict__ part,
@@ -170,19 +170,27 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
         m = m_new;
     };
     if (!FOX) {
-        // warp-uniform trip count: every lane joins the shuffles, lanes past the end idle
-        for (int jb = j0 + warp * KPW; jb < j1; jb += kWarps * KPW) {
-            const int j = jb + g;
-            const bool valid = j < j1;
-            float kv[E], vv[E];
-            if (valid) {
-                Vec<T>::load(krow + (size_t)j * D, kv);
-                Vec<T>::load(vrow + (size_t)j * D, vv);
-            } else {
+        // warp-uniform trip count: every lane joins the shuffles, lanes past the end idle.
+        // Two passes' key and value rows are loaded together (raw, 16 bytes per lane each)
+        // so that each warp keeps twice the bytes in flight.
+        constexpr int kStride = kWarps * KPW;
+        for (int jb = j0 + warp * KPW; jb < j1; jb += 2 * kStride) {
+            uint4 kr[2], vr[2];
 #pragma unroll
-                for (int e = 0; e < E; ++e) kv[e] = vv[e] = 0.f;
+            for (int pb = 0; pb < 2; ++pb) {
+                const int j = jb + pb * kStride + g;
+                const bool valid = j < j1;
+                kr[pb] = valid ? Vec<T>::load_raw(krow + (size_t)j * D) : make_uint4(0u, 0u, 0u, 0u);
+                vr[pb] = valid ? Vec<T>::load_raw(vrow + (size_t)j * D) : make_uint4(0u, 0u, 0u, 0u);
             }
-            key_math(j, valid, 0.f, kv, vv);
+#pragma unroll
+            for (int pb = 0; pb < 2; ++pb) {
+                const int j = jb + pb * kStride + g;
+                float kv[E], vv[E];
+                Vec<T>::unpack(kr[pb], kv);
+                Vec<T>::unpack(vr[pb], vv);
+                key_math(j, j < j1, 0.f, kv, vv);
+            }
         }
     } else {
         // Each warp owns runs of 32 consecutive keys: lane i reads, advances and writes
