@@ -14,8 +14,9 @@
 //   P0 forms the tap-scaled up-projections W'_k = diag(conv[:,k]) W_up (bf16), so that the
 //      convolution becomes part of the second contraction: y'_t = sum_k W'_k z_{t-2+k};
 //   P1 (tcgen05): [z | beta logits] = x [W_down; u]^T for 128-token tiles, streaming x
-//      through a four-stage TMA ring; the epilogue writes z (bf16) and beta;
-//   P2 (tcgen05): for 128-token tiles of one sequence, three accumulating contractions of
+//      through a three-stage TMA ring; the epilogue writes z (bf16) and beta;
+//   P2 (tcgen05): persistent over (128-token tile, two-head chunk) units, each CTA an equal
+//      contiguous run of them; per unit three accumulating contractions of
 //      z tiles loaded at rows t0, t0-1, t0-2 (a negative start row reads zeros: the causal
 //      zero history) with W'_2, W'_1, W'_0, two heads (N = 128) per TMEM buffer, double
 //      buffered; the epilogue normalises each head row into a 128-byte-swizzled shared tile
@@ -300,7 +301,13 @@ producer_up_kernel(const __grid_constant__ CUtensorMap tm_z,
     const int nchunk = (H + 1) / 2;                // two heads per accumulator
     const int ntps = (L + 127) / 128;              // 128-token tiles per sequence
     const int nitems = ntps * nseq;                // work items (tile, sequence)
-    const int nmine = (int)blockIdx.x < nitems ? (nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    // units (item, chunk) in item-major order; CTA c takes the contiguous range [u0, u1), so
+    // every CTA gets the same number of two-head chunks within one and reloads z only where
+    // its range crosses into the next item
+    const long long nunits = (long long)nitems * nchunk;
+    const int u0 = (int)(nunits * blockIdx.x / gridDim.x);
+    const int u1 = (int)(nunits * (blockIdx.x + 1) / gridDim.x);
+    const int it0 = u0 / nchunk, it1 = u1 > u0 ? (u1 - 1) / nchunk + 1 : it0;  // items [it0, it1)
     if (threadIdx.x == 0) {
         abort_s = 0u;
         for (int s = 0; s < kP2Stages; ++s) {
@@ -331,9 +338,9 @@ producer_up_kernel(const __grid_constant__ CUtensorMap tm_z,
         tma_prefetch_desc(&tm_wk);
         int i = 0, j = 0;
         bool ok = true;
-        for (; j < nmine && ok; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
+        for (int item = it0; item < it1 && ok; ++item, ++j) {
             const int t0 = (item % ntps) * 128, bq = item / ntps;
+            const int c0 = max(u0 - item * nchunk, 0), c1 = min(u1 - item * nchunk, nchunk);
             if (j >= 1 && !wait_bounded(a_empty, (j - 1) & 1, limit_ns, status)) {
                 abort_s = 1u;
                 break;
@@ -341,7 +348,7 @@ producer_up_kernel(const __grid_constant__ CUtensorMap tm_z,
             mbar_arrive_expect_tx(a_full, (uint32_t)nkc * kZRows * 128);
             for (int kc = 0; kc < nkc; ++kc)
                 tma_load_3d(a_base + (uint32_t)kc * kZSlot, &tm_z, a_full, kc * 64, t0 - 2, bq);
-            for (int step = 0; step < nchunk * 3 * nkc; ++step, ++i) {
+            for (int step = c0 * 3 * nkc; step < c1 * 3 * nkc; ++step, ++i) {
                 const int s = i % kP2Stages;
                 if (i >= kP2Stages &&
                     !wait_bounded(empty(s), ((i / kP2Stages) - 1) & 1, limit_ns, status)) {
@@ -364,13 +371,14 @@ producer_up_kernel(const __grid_constant__ CUtensorMap tm_z,
         // of z_tap W'_tap^T (N = 128)
         const uint32_t idesc = idesc_bf16_kk(128, 128);
         bool ok = true;
-        int i = 0, g = 0;
-        for (int j = 0; j < nmine && ok; ++j) {
+        int i = 0, g = 0, j = 0;
+        for (int item = it0; item < it1 && ok; ++item, ++j) {
+            const int c0 = max(u0 - item * nchunk, 0), c1 = min(u1 - item * nchunk, nchunk);
             if (!wait_bounded(a_full, j & 1, limit_ns, status)) {
                 ok = false;
                 break;
             }
-            for (int chunk = 0; chunk < nchunk && ok; ++chunk, ++g) {
+            for (int chunk = c0; chunk < c1 && ok; ++chunk, ++g) {
                 const int buf = g & 1;
                 if (g >= 2 && !wait_bounded(acc_empty(buf), ((g >> 1) - 1) & 1, limit_ns, status)) {
                     ok = false;
@@ -413,8 +421,8 @@ producer_up_kernel(const __grid_constant__ CUtensorMap tm_z,
         const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
         const int r = 32 * warp + lane;
         int g = 0, hn = 0;
-        for (int jc = 0; jc < nmine * nchunk; ++jc, ++g) {
-            const int item = blockIdx.x + (jc / nchunk) * gridDim.x, chunk = jc % nchunk;
+        for (int u = u0; u < u1; ++u, ++g) {
+            const int item = u / nchunk, chunk = u % nchunk;
             const int t0 = (item % ntps) * 128, bq = item / ntps;
             const int buf = g & 1;
             if (threadIdx.x == 0 &&
@@ -560,9 +568,9 @@ cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up,
         tx, twd, tu, bias, beta_max, (int)BL, L, D, R, H, Hp, acc_cols, z, beta_out, status,
         limit_ns);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const long long items2 = (long long)((L + 127) / 128) * B;
+    const long long units2 = (long long)((L + 127) / 128) * B * ((H + 1) / 2);
     const int per_sm2 = 2 * (s2 + 1024) <= 228 * 1024 ? 2 : 1;  // TMEM: 2 x 256 columns fit
-    const unsigned g2 = (unsigned)std::min<long long>(items2, (long long)per_sm2 * nsm);
+    const unsigned g2 = (unsigned)std::min<long long>(units2, (long long)per_sm2 * nsm);
     producer_up_kernel<<<g2, kP2Threads, s2, stream>>>(tz, twk, tw, B, L, R, H, status, limit_ns);
     return cudaGetLastError();
 }

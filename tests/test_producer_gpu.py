@@ -39,6 +39,7 @@ def _check(w, beta, ref_w, ref_beta):
     (1, 130, 256, 128, 4),   # two K chunks in both contractions
     (1, 129, 128, 192, 64),  # R + H at the 256-column limit
     (5, 77, 192, 64, 5),     # B * L not a multiple of 128 (P1 tail crosses sequences)
+    (3, 2000, 128, 64, 31),  # several (tile, head-pair) units per P2 CTA, runs crossing tiles
 ])
 def test_producer_matches_oracle(lib, B, L, D, R, H):
     p = pi.make_producer_inputs(B, L, D, R, H, seed=B * 1000 + L, device="cuda")
