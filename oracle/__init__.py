@@ -50,6 +50,9 @@ def _configure(lib):
     lib.oracle_wbeta_produce.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_double] + \
         [ctypes.c_int] * 6 + [ctypes.c_double, dp, dp]
     lib.oracle_wbeta_produce.restype = None
+    lib.oracle_path_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 3 + [ctypes.c_double] + \
+        [dp] * 6 + [ctypes.c_int]
+    lib.oracle_path_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -227,3 +230,33 @@ def wbeta_produce(x, w_down, w_up, conv, u, bias, beta_max=2.0, eps=1e-12):
                                  _ptr(bias), float(beta_max), B, L, D, R, H, d, float(eps),
                                  _ptr(w), _ptr(beta))
     return w, beta
+
+
+def path_bwd(q, k, v, w, beta, dout, log_f=None, scale=None, nthreads=0):
+    """Gradients of the PaTH (log_f None) or PaTH-FoX forward for the loss
+    sum(dout * out), by reverse mode through the definition's per-row sweep
+    (path_oracle.c, oracle_path_bwd).
+
+    Returns a dict of float64 arrays: dq, dk, dv, dw (..., L, d), dbeta (..., L) and,
+    with log_f, dlog_f (..., L).
+    """
+    q, k, v, w, beta, log_f, dout = map(_f64, (q, k, v, w, beta, log_f, dout))
+    lead, L, d = q.shape[:-2], q.shape[-2], q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    qh, kh, vh, wh, dh = (np.ascontiguousarray(_heads(t, L, d)) for t in (q, k, v, w, dout))
+    nh = qh.shape[0]
+    bh = np.ascontiguousarray(beta.reshape(nh, L))
+    fh = None if log_f is None else np.ascontiguousarray(log_f.reshape(nh, L))
+    g = {n: np.empty((nh, L, d)) for n in ("dq", "dk", "dv", "dw")}
+    g["dbeta"] = np.empty((nh, L))
+    if fh is not None:
+        g["dlog_f"] = np.empty((nh, L))
+    _load().oracle_path_bwd(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(wh), _ptr(bh), _ptr(fh),
+                            _ptr(dh), nh, L, d, float(scale), _ptr(g["dq"]), _ptr(g["dk"]),
+                            _ptr(g["dv"]), _ptr(g["dw"]), _ptr(g["dbeta"]),
+                            _ptr(g.get("dlog_f")), int(nthreads))
+    out = {}
+    for n, a in g.items():
+        out[n] = a.reshape(*lead, L, d) if a.ndim == 3 else a.reshape(*lead, L)
+    return out

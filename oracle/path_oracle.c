@@ -350,3 +350,179 @@ void oracle_wbeta_produce(const double *x, const double *w_down, const double *w
     free(y);
     free(yc);
 }
+
+/* ---------------------------------------------------------------- backward */
+
+/*
+ * Gradients of the forward above for one head, by reverse mode through the
+ * per-row sweep of row_logits (the pages give no backward pass; this is the
+ * chain rule applied to the definition, step by step).
+ *
+ * Forward for row i: x_i = q_i; for j = i, i-1, ..., 0: logit_ij =
+ * scale * k_j . x_j + bias_ij, then x_{j-1} = H_j x_j; softmax over j <= i;
+ * out_i = sum_j p_ij v_j. With dout_i given:
+ *   dp_ij = dout_i . v_j,  D_i = sum_j p_ij dp_ij,  dS_ij = p_ij (dp_ij - D_i)
+ *   dv_j += p_ij dout_i
+ * and, walking back from j = 0 to j = i with g the gradient of x_j:
+ *   g += scale dS_ij k_j,   dk_j += scale dS_ij x_j;
+ *   through x_j = H_{j+1} x_{j+1}, H = I - beta w w^T, input u = x_{j+1}:
+ *     dbeta_{j+1} -= (w.g)(w.u),  dw_{j+1} -= beta ((w.u) g + (w.g) u),
+ *     g <- H g (the gradient of x_{j+1});
+ *   at j = i, dq_i += g.
+ * The FoX bias sum_{s=j+1..i} log f_s gives dlog_f_s += dS_ij for j < s <= i.
+ * xs holds the row's x_j (L * d), the other buffers L each.
+ */
+static void head_backward(const double *Q, const double *K, const double *V,
+                          const double *W, const double *beta, const double *log_f,
+                          const double *dO, int L, int d, double scale,
+                          double *dQ, double *dK, double *dV, double *dW,
+                          double *dbeta, double *dlogf, double *xs, double *logit,
+                          double *p, double *g)
+{
+    for (int i = 0; i < L; ++i) {
+        const double *q_i = Q + (size_t)i * d;
+        const double *do_i = dO + (size_t)i * d;
+        /* forward sweep, keeping x_j */
+        memcpy(xs + (size_t)i * d, q_i, (size_t)d * sizeof(double));
+        double bias = 0.0;
+        for (int j = i; j >= 0; --j) {
+            double *x_j = xs + (size_t)j * d;
+            if (j < i) {
+                memcpy(x_j, xs + (size_t)(j + 1) * d, (size_t)d * sizeof(double));
+                apply_transition(x_j, W + (size_t)(j + 1) * d, beta[j + 1], d);
+            }
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c)
+                dot += K[(size_t)j * d + c] * x_j[c];
+            logit[j] = bias + scale * dot;
+            if (log_f)
+                bias += log_f[j];
+        }
+        /* softmax and its gradient */
+        double m = -INFINITY;
+        for (int j = 0; j <= i; ++j)
+            if (logit[j] > m)
+                m = logit[j];
+        double z = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            p[j] = exp(logit[j] - m);
+            z += p[j];
+        }
+        double Dsum = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            p[j] /= z;
+            double dp = 0.0;
+            for (int c = 0; c < d; ++c)
+                dp += do_i[c] * V[(size_t)j * d + c];
+            logit[j] = dp; /* logit[] now holds dp_ij */
+            Dsum += p[j] * dp;
+        }
+        /* reverse sweep */
+        for (int c = 0; c < d; ++c)
+            g[c] = 0.0;
+        double gate_acc = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            const double dS = p[j] * (logit[j] - Dsum);
+            const double *x_j = xs + (size_t)j * d;
+            const double *k_j = K + (size_t)j * d;
+            for (int c = 0; c < d; ++c) {
+                dV[(size_t)j * d + c] += p[j] * do_i[c];
+                dK[(size_t)j * d + c] += scale * dS * x_j[c];
+                g[c] += scale * dS * k_j[c];
+            }
+            if (log_f) {
+                gate_acc += dS; /* sum of dS_ij' over j' <= j: the gradient of log f_{j+1} */
+                if (j < i)
+                    dlogf[j + 1] += gate_acc;
+            }
+            if (j < i) {
+                const double *w = W + (size_t)(j + 1) * d;
+                const double b = beta[j + 1];
+                const double *u = xs + (size_t)(j + 1) * d;
+                double wu = 0.0, wg = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    wu += w[c] * u[c];
+                    wg += w[c] * g[c];
+                }
+                dbeta[j + 1] -= wg * wu;
+                for (int c = 0; c < d; ++c)
+                    dW[(size_t)(j + 1) * d + c] -= b * (wu * g[c] + wg * u[c]);
+                for (int c = 0; c < d; ++c)
+                    g[c] -= b * wg * w[c];
+            }
+        }
+        for (int c = 0; c < d; ++c)
+            dQ[(size_t)i * d + c] += g[c];
+    }
+}
+
+typedef struct {
+    const double *q, *k, *v, *w, *beta, *log_f, *dout;
+    int nh, L, d;
+    double scale;
+    double *dq, *dk, *dv, *dw, *dbeta, *dlogf;
+    int next;
+    pthread_mutex_t mu;
+} bwd_job;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *job = (bwd_job *)arg;
+    const int L = job->L, d = job->d;
+    double *xs = (double *)malloc((size_t)L * d * sizeof(double));
+    double *logit = (double *)malloc((size_t)L * sizeof(double));
+    double *p = (double *)malloc((size_t)L * sizeof(double));
+    double *g = (double *)malloc((size_t)d * sizeof(double));
+    for (;;) {
+        pthread_mutex_lock(&job->mu);
+        const int h = job->next++;
+        pthread_mutex_unlock(&job->mu);
+        if (h >= job->nh)
+            break;
+        const size_t td = (size_t)h * L * d, t1 = (size_t)h * L;
+        head_backward(job->q + td, job->k + td, job->v + td, job->w + td, job->beta + t1,
+                      job->log_f ? job->log_f + t1 : NULL, job->dout + td, L, d, job->scale,
+                      job->dq + td, job->dk + td, job->dv + td, job->dw + td,
+                      job->dbeta + t1, job->dlogf ? job->dlogf + t1 : NULL, xs, logit, p, g);
+    }
+    free(xs);
+    free(logit);
+    free(p);
+    free(g);
+    return NULL;
+}
+
+/*
+ * Backward of oracle_path_fwd for the loss sum(dout * out): gradients with
+ * respect to q, k, v, w, beta and (PaTH-FoX) log_f, all (nh, L, d) or (nh, L),
+ * zeroed here first. dlogf may be NULL when log_f is. Heads run in parallel.
+ * Returns the thread count used.
+ */
+int oracle_path_bwd(const double *q, const double *k, const double *v, const double *w,
+                    const double *beta, const double *log_f, const double *dout, int nh,
+                    int L, int d, double scale, double *dq, double *dk, double *dv,
+                    double *dw, double *dbeta, double *dlogf, int nthreads)
+{
+    const size_t n = (size_t)nh * L * d, n1 = (size_t)nh * L;
+    memset(dq, 0, n * sizeof(double));
+    memset(dk, 0, n * sizeof(double));
+    memset(dv, 0, n * sizeof(double));
+    memset(dw, 0, n * sizeof(double));
+    memset(dbeta, 0, n1 * sizeof(double));
+    if (dlogf)
+        memset(dlogf, 0, n1 * sizeof(double));
+    bwd_job job = {q, k, v, w, beta, log_f, dout, nh, L, d, scale,
+                   dq, dk, dv, dw, dbeta, log_f ? dlogf : NULL, 0};
+    nthreads = resolve_threads(nthreads);
+    if (nthreads > nh)
+        nthreads = nh;
+    pthread_mutex_init(&job.mu, NULL);
+    pthread_t *tid = (pthread_t *)malloc((size_t)nthreads * sizeof(pthread_t));
+    for (int t = 0; t < nthreads; ++t)
+        pthread_create(&tid[t], NULL, bwd_worker, &job);
+    for (int t = 0; t < nthreads; ++t)
+        pthread_join(tid[t], NULL);
+    free(tid);
+    pthread_mutex_destroy(&job.mu);
+    return nthreads;
+}

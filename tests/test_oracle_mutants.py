@@ -14,6 +14,7 @@ import pytest
 import oracle
 from oracle import build as oracle_build
 from tests import test_oracle_pins as pins
+from tests import test_bwd_oracle as bpins
 from tests import test_producer_oracle as ppins
 
 SRC = oracle_build.SRC
@@ -60,6 +61,16 @@ MUTANTS = {
     "producer_projects_previous_token": (
         "acc += w_down[(size_t)r * D + c] * xb[(size_t)t * D + c];",
         "acc += w_down[(size_t)r * D + c] * xb[(size_t)(t > 0 ? t - 1 : 0) * D + c];"),
+    # backward
+    "bwd_dS_without_row_term": ("const double dS = p[j] * (logit[j] - Dsum);",
+                                "const double dS = p[j] * logit[j];"),
+    "bwd_dk_unscaled": ("dK[(size_t)j * d + c] += scale * dS * x_j[c];",
+                        "dK[(size_t)j * d + c] += dS * x_j[c];"),
+    "bwd_dw_drops_term": ("dW[(size_t)(j + 1) * d + c] -= b * (wu * g[c] + wg * u[c]);",
+                          "dW[(size_t)(j + 1) * d + c] -= b * (wu * g[c]);"),
+    "bwd_gradient_not_transported": ("g[c] -= b * wg * w[c];", "g[c] -= 0.0 * wg * w[c];"),
+    "bwd_dbeta_sign": ("dbeta[j + 1] -= wg * wu;", "dbeta[j + 1] += wg * wu;"),
+    "bwd_gate_index_shifted": ("dlogf[j + 1] += gate_acc;", "dlogf[j] += gate_acc;"),
 }
 
 
@@ -84,6 +95,11 @@ def run_all_pins():
         ("p_shift", ppins.test_lag_one_tap_shifts_the_output_by_one_token, ()),
         ("p_norm", ppins.test_unit_norm_scale_invariance_and_heads_independent, ()),
         ("p_beta", ppins.test_beta_limits, ()),
+        ("b_fd", bpins.test_bwd_matches_finite_differences, (False,)),
+        ("b_fd_fox", bpins.test_bwd_matches_finite_differences, (True,)),
+        ("b_beta0", bpins.test_bwd_beta_zero_closed_form, ()),
+        ("b_sign", bpins.test_bwd_sign_of_w, ()),
+        ("b_dv", bpins.test_bwd_dv_is_p_transpose_dout, ()),
     ]
     for name, fn, args in checks:
         try:
