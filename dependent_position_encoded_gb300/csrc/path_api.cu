@@ -38,6 +38,11 @@ cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up,
                             const void *u, const float *bias, float beta_max, void *w_out,
                             float *beta_out, int B, int L, int D, int R, int H, void *ws,
                             uint64_t limit_ns, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const void *w,
+                            const float *beta, const void *o, const float *lse, const void *dout,
+                            int B, int H, int L, float scale, float *dq, float *dk, float *dv,
+                            float *dw, float *dbeta, void *ws, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len, int d);
 template <typename T>
@@ -146,6 +151,10 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
             return fwd_layout(B, H, L, elt_bytes(dtype), op == PATH_OP_FOX_FWD).total;
         default: break;
     }
+    if (op == PATH_OP_BWD) {
+        if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+        return bwd_layout(B, H, L).total;
+    }
     if (check_decode_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
     switch (op) {
         case PATH_OP_DECODE: return decode_ws_bytes(B, H, L, d);
@@ -176,6 +185,30 @@ path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H,
                                        (size_t)lay.nblk * sizeof(int), (size_t)nq * sizeof(int),
                                        (size_t)B * H, cudaMemcpyDeviceToDevice,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+path_status path_attn_bwd(const void *q, const void *k, const void *v, const void *w,
+                          const float *beta, const void *out, const float *lse, const void *d_out,
+                          int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
+                          float *dv, float *dw, float *dbeta, void *ws, size_t ws_bytes,
+                          void *stream) {
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if (!std::isfinite(scale)) return PATH_ERR_ARG;
+    if ((long long)B * H * L == 0) return PATH_OK;
+    const void *in[] = {q, k, v, w, beta, out, lse, d_out, dq, dk, dv, dw, dbeta};
+    for (const void *p : in)
+        if (!p) return PATH_ERR_NULL;
+    for (const void *p : in)
+        if (!aligned(p, 16)) return PATH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, bwd_layout(B, H, L).total)) != PATH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dtype == PATH_BF16
+                        ? launch_path_bwd<__nv_bfloat16>(q, k, v, w, beta, out, lse, d_out, B, H,
+                                                         L, scale, dq, dk, dv, dw, dbeta, ws, s)
+                        : launch_path_bwd<float>(q, k, v, w, beta, out, lse, d_out, B, H, L,
+                                                 scale, dq, dk, dv, dw, dbeta, ws, s);
+    return from_cuda(e);
 }
 
 path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, int H, int L,

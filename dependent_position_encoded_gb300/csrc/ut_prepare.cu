@@ -75,11 +75,13 @@ __device__ __forceinline__ void store_row4<__nv_bfloat16>(__nv_bfloat16 *dst, co
     *reinterpret_cast<uint2 *>(dst) = u;
 }
 
-template <typename T>
+// T: input element type; TO: element type of q~, k~ and P_b (the backward recomputes them
+// in fp32 from bf16 inputs)
+template <typename T, typename TO = T>
 __global__ void __launch_bounds__(kPrepThreads)
 ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
                   const float *__restrict__ beta, const float *__restrict__ log_f, int L,
-                  int Lp, int nblk, float scale_log2, T *__restrict__ qt, T *__restrict__ kp,
+                  int Lp, int nblk, float scale_log2, TO *__restrict__ qt, TO *__restrict__ kp,
                   float *__restrict__ dg, uint32_t *status) {
     extern __shared__ __align__(16) float sm[];
     float *Wr = sm;            // W[s][c]
@@ -229,13 +231,13 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     {
         zero(acc);
         mm_acc(X, Wr, m0, n0, acc);
-        T *out = qt + ((size_t)bh * Lp + t0) * kD;
+        TO *out = qt + ((size_t)bh * Lp + t0) * kD;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = Qt[(n0 + j) * LD + m0 + i] - acc[i][j];
-            store_row4<T>(out + (m0 + i) * kD + n0, v);
+            store_row4<TO>(out + (m0 + i) * kD + n0, v);
         }
     }
     __syncthreads();
@@ -248,7 +250,7 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     __syncthreads();
 
     // ---- k~[j][c] = k[j][c] - sum_u Khat[j][u] W[u][c];  AW = A W -> X
-    T *kp_blk = kp + blk_base * (2 * kC) * kD;
+    TO *kp_blk = kp + blk_base * (2 * kC) * kD;
     {
         zero(acc);
         mm_acc(Y, Wr, m0, n0, acc);
@@ -257,7 +259,7 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
             float v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = Kt[(n0 + j) * LD + m0 + i] - acc[i][j];
-            store_row4<T>(kp_blk + (m0 + i) * kD + n0, v);
+            store_row4<TO>(kp_blk + (m0 + i) * kD + n0, v);
         }
         zero(acc);
         mm_acc(At, Wr, m0, n0, acc);
@@ -269,13 +271,13 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     {
         zero(acc);
         mm_acc(Wr, X, m0, n0, acc);
-        T *out = kp_blk + kC * kD;
+        TO *out = kp_blk + kC * kD;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float v[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = ((m0 + i) == (n0 + j) ? 1.f : 0.f) - acc[i][j];
-            store_row4<T>(out + (m0 + i) * kD + n0, v);
+            store_row4<TO>(out + (m0 + i) * kD + n0, v);
         }
     }
 }
@@ -302,6 +304,32 @@ cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const
         reinterpret_cast<uint32_t *>(base));
     return cudaGetLastError();
 }
+
+// The per-block factors in fp32 at explicit places (plain PaTH, no gate), for the backward:
+// qt (BH, Lp, 64), kp (BH, nblk, 128, 64) = [k~ rows; P_b rows] per block, dg (BH, nblk, 64,
+// 64) diagonal-block logits in log2 units (scale included, -inf above the diagonal and past L).
+template <typename T>
+cudaError_t launch_ut_prepare_f32out(const void *q, const void *k, const void *w,
+                                     const float *beta, int BH, int L, int Lp, int nblk,
+                                     float scale, float *qt, float *kp, float *dg,
+                                     uint32_t *status, cudaStream_t stream) {
+    const size_t smem = ut_prepare_smem_bytes();
+    cudaError_t err = cudaFuncSetAttribute(ut_prepare_kernel<T, float>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(nblk, BH);
+    ut_prepare_kernel<T, float><<<grid, kPrepThreads, smem, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
+        nullptr, L, Lp, nblk, scale * kLog2e, qt, kp, dg, status);
+    return cudaGetLastError();
+}
+template cudaError_t launch_ut_prepare_f32out<float>(const void *, const void *, const void *,
+                                                     const float *, int, int, int, int, float,
+                                                     float *, float *, float *, uint32_t *,
+                                                     cudaStream_t);
+template cudaError_t launch_ut_prepare_f32out<__nv_bfloat16>(
+    const void *, const void *, const void *, const float *, int, int, int, int, float, float *,
+    float *, float *, uint32_t *, cudaStream_t);
 
 // PaTH-FoX: log2(e) * inclusive prefix sums of log f per head into the workspace.
 template cudaError_t launch_ut_prepare<float>(const void *, const void *, const void *,

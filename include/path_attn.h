@@ -59,7 +59,8 @@ typedef enum {
     PATH_OP_FWD = 0,
     PATH_OP_FOX_FWD = 1,
     PATH_OP_DECODE = 2,
-    PATH_OP_FOX_DECODE = 3
+    PATH_OP_FOX_DECODE = 3,
+    PATH_OP_BWD = 4
 } path_op;
 
 /* Largest sizes accepted: B*H <= PATH_MAX_HEADS, L <= PATH_MAX_LEN. */
@@ -70,8 +71,9 @@ typedef enum {
  * Workspace bytes that `op` needs for the given sizes (L = cache capacity and d = 64 or
  * 128 for PATH_OP_DECODE and PATH_OP_FOX_DECODE). Returns 0 for invalid arguments. The workspace holds the
  * per-block factors of the forward (boundary-adjusted queries and keys, the
- * dense block transitions, the diagonal-block logits, the FoX prefix sums)
- * or the split partial results of decode, plus a 256-byte status header.
+ * dense block transitions, the diagonal-block logits, the FoX prefix sums),
+ * the split partial results of decode, or the fp32 factors, per-block gradients
+ * and carried query blocks of the backward, plus a 256-byte status header.
  */
 size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype);
 
@@ -115,6 +117,32 @@ path_status path_fox_fwd(const void *q, const void *k, const void *v, const void
 path_status path_fwd_prepare(const void *q, const void *k, const void *w, const float *beta,
                              const float *log_f, int B, int H, int L, int d, int dtype,
                              float scale, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * PaTH backward (plain PaTH): gradients of a loss L with respect to q, k, v, w and beta,
+ * given dL/d out. The pages give no backward pass (review "거리에서 경로로, PaTH
+ * Attention" §9 and technical summary "技術要約: PaTH Attention" §3 only say the blockwise
+ * algorithm makes training efficient); this is the chain rule applied to the forward of
+ * path_attn_fwd, with the softmax gradient dS_ij = p_ij (d_out_i . v_j - d_out_i . out_i).
+ *   q, k, v, w : (B, H, L, d) dtype     beta : (B, H, L) fp32    (the forward's inputs)
+ *   out        : (B, H, L, d) dtype     lse  : (B, H, L) fp32    (the forward's outputs)
+ *   d_out      : (B, H, L, d) dtype, the gradient of the loss with respect to out
+ *   dq, dk, dv, dw : (B, H, L, d) fp32 outputs;  dbeta : (B, H, L) fp32 output
+ *   scale      : the forward's softmax scale (finite)
+ *   ws         : ws_bytes >= path_workspace_bytes(PATH_OP_BWD, B, H, L, d, dtype), which
+ *                grows as B H (L / 64)^2 x 32 KB (the query pass keeps every carried
+ *                query block and its logit gradient, e.g. 1.0 GB at B H = 64, L = 2048)
+ * Every product runs in fp32 whatever dtype is (bf16 inputs are widened on load); w is
+ * used as given (no renormalisation). Gradients of several query blocks meet in dv and in
+ * internal per-block sums through fp32 atomic adds, so their rounding order (not their
+ * value beyond fp32 rounding) varies between runs. Outputs are written from zero: no
+ * accumulation into the caller's buffers.
+ */
+path_status path_attn_bwd(const void *q, const void *k, const void *v, const void *w,
+                          const float *beta, const void *out, const float *lse, const void *d_out,
+                          int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
+                          float *dv, float *dw, float *dbeta, void *ws, size_t ws_bytes,
+                          void *stream);
 
 /*
  * Second stage of the forward: the right-to-left scan over key blocks with

@@ -207,3 +207,41 @@ def test_fox_first_blocks_argument_checks(so):
     assert call(ws=FAKE + 8) == 4
     assert call(ws_bytes=1024) == 5
     assert call(L=0) == 0
+
+
+def test_bwd_workspace_size(lib):
+    # fp32 q~ (Lp x 64), [k~; P_b] (nblk x 128 x 64), diagonal logits, dq~, dk~, dP_b, diagonal
+    # dT, and per pair b < a the carried query block and its logit gradient (2 x 64 x 64)
+    L, nb = 130, 3
+    rows, blocks = nb * 64 * 64 * 4, nb * 64 * 64 * 4
+    want = 256 + rows + 2 * blocks + blocks + rows + rows + blocks + blocks + 3 * 2 * 64 * 64 * 4
+    for dt in (lib.F32, lib.BF16):
+        assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, dt) == want
+    assert lib.path_workspace_bytes(lib.OP_BWD, 2, 3, L, 64, lib.BF16) == 256 + 6 * (want - 256)
+    assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, 128, 128, lib.BF16) == 0
+
+
+def _bwd(so, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, w=FAKE, beta=FAKE, out=FAKE, lse=FAKE, d_out=FAKE, B=1,
+             H=1, L=128, d=64, dtype=1, scale=0.125, dq=FAKE, dk=FAKE, dv=FAKE, dw=FAKE,
+             dbeta=FAKE, ws=FAKE, ws_bytes=8, stream=None)
+    a.update(kw)
+    return so.path_attn_bwd(a["q"], a["k"], a["v"], a["w"], a["beta"], a["out"], a["lse"],
+                            a["d_out"], a["B"], a["H"], a["L"], a["d"], a["dtype"],
+                            ctypes.c_float(a["scale"]), a["dq"], a["dk"], a["dv"], a["dw"],
+                            a["dbeta"], a["ws"], ctypes.c_size_t(a["ws_bytes"]), a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(d_out=None), 1), (dict(dbeta=None), 1),
+    (dict(ws=None), 1), (dict(d=128), 2), (dict(L=-1), 2), (dict(dtype=2), 3),
+    (dict(dw=FAKE + 4), 4), (dict(out=FAKE + 8), 4), (dict(ws=FAKE + 16), 4),
+    (dict(scale=float("nan")), 9), (dict(), 5),
+])
+def test_bwd_rejects_bad_arguments_before_launch(so, kw, code):
+    # ws_bytes stays 8 throughout, so nothing can reach a launch
+    assert _bwd(so, **kw) == code
+
+
+def test_bwd_empty_problem_launches_nothing(so):
+    assert _bwd(so, L=0, q=None, ws=None) == 0

@@ -1,0 +1,85 @@
+"""Parity of the backward pass (path_attn_bwd, through the C ABI) against the fp64 oracle.
+
+The GPU forward supplies out and lse, as a caller's would. Every gradient is compared
+normwise: max |g - g*| / max |g*| over the tensor (the denominator at least 1% of the
+largest reference gradient of the case).
+- fp32 inputs: 1e-4, the fp32 forward's bar (every backward product is fp32 too).
+- bf16 inputs: 2e-2, the bf16 forward's bar. The bf16 inputs themselves are exact for both
+  sides. What differs is the forward's out, rounded to bf16 (a relative error of 2^-9),
+  which enters every dS_ij through dout_i . out_i.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import path_inputs as pi
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+NAMES = ("dq", "dk", "dv", "dw", "dbeta")
+
+
+def _case(lib, B, H, L, dtype, seed, beta_zero=False, wl=None):
+    if wl is None:
+        x = pi.make_fwd_inputs(B, H, L, seed=seed, dtype=dtype, device="cuda")
+    else:
+        x = pi.workload_inputs(wl, device="cuda")
+    if beta_zero:
+        x["beta"] = torch.zeros_like(x["beta"])
+    g = torch.Generator(device="cpu").manual_seed(seed + 1)
+    d_out = torch.randn((B, H, L, 64), generator=g).to(dtype).cuda()
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out)
+    torch.cuda.synchronize()
+    return x, d_out, grads
+
+
+def _compare(grads, ref, tol, heads=None):
+    # a gradient that is exactly zero (one token: the softmax weight is 1, so dS = 0) is
+    # measured against 1% of the largest reference gradient instead of against itself
+    floor = 1e-2 * max(np.abs(ref[n]).max() for n in NAMES)
+    for n in NAMES:
+        got = grads[n].double().cpu().numpy()
+        if heads is not None:
+            got = got.reshape(-1, *got.shape[2:])[heads]
+        r = ref[n]
+        assert np.isfinite(got).all(), n
+        err = np.abs(got - r).max() / max(np.abs(r).max(), floor)
+        assert err <= tol, "%s: normwise relative error %g (tolerance %g)" % (n, err, tol)
+
+
+@pytest.mark.parametrize("B,H,L,dtype", [
+    (1, 2, 128, torch.float32),    # two blocks
+    (1, 2, 200, torch.float32),    # ragged last block
+    (2, 2, 130, torch.bfloat16),   # bf16, ragged, three blocks
+    (1, 1, 64, torch.float32),     # one block: no inter-block term
+    (1, 1, 1, torch.float32),      # one token
+    (1, 3, 65, torch.bfloat16),    # one token in the last block
+    (1, 1, 384, torch.float32),    # six blocks: interior P_b gradients
+])
+def test_bwd_matches_oracle(lib, B, H, L, dtype):
+    x, d_out, grads = _case(lib, B, H, L, dtype, seed=B * 100 + L)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, TOL[dtype])
+
+
+def test_bwd_beta_zero_is_softmax_attention_gradient(lib):
+    # beta = 0: every H_s is the identity, so dw must vanish exactly and dq, dk, dv are the
+    # gradients of ordinary causal softmax attention
+    x, d_out, grads = _case(lib, 1, 2, 192, torch.float32, seed=3, beta_zero=True)
+    assert torch.count_nonzero(grads["dw"]) == 0
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, 1e-4)
+
+
+def test_bwd_workload_sampled_heads(lib):
+    # the bf16 check workload (B4 H16 L2048, as bench.py times it): the oracle on two heads
+    wl = pi.BF16_L2048
+    x, d_out, grads = _case(lib, wl.B, wl.H, wl.L, wl.dtype, seed=wl.seed, wl=wl)
+    heads = [5, wl.B * wl.H - 1]
+    sel = {k: x[k].reshape(-1, *x[k].shape[2:])[heads] for k in ("q", "k", "v", "w", "beta")}
+    ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          d_out.reshape(-1, wl.L, 64)[heads])
+    _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
