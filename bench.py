@@ -339,6 +339,58 @@ def time_producer(pa, wl, steps=5, warmup=3):
             "launches_per_step": 3}
 
 
+# FP32 FMA peak of the CUDA cores, from the unit counts and the maximum SM clock:
+# 152 SMs x 128 FP32 lanes x 2 FLOP per FMA x 2.07 GHz (nominal; no measured FP32 figure)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def bwd_flops(B, H, L):
+    """FP32 FLOPs of the backward's query pass (the 64 x 64 x 64 products it forms, each
+    2 * 64^3): per pair of query block a and key block b < a, the logits, dout V_b^T, the
+    dk~ and dv terms and dT K~_b (5 products), plus X P_b^T, G P_b and the dP_b term when
+    b > 0 (3 more); per diagonal block dout V^T and p^T dout."""
+    nb = (L + 63) // 64
+    pairs = nb * (nb - 1) // 2
+    t = 2 * 64 ** 3
+    return B * H * t * (5 * pairs + 3 * (pairs - (nb - 1)) + 2 * nb)
+
+
+def time_bwd(pa, wl, steps=5, warmup=3):
+    """Times path_attn_bwd on the workload (forward outputs and d_out resident)."""
+    dev = torch.device("cuda")
+    x = pi.workload_inputs(wl, device=dev)
+    g = torch.Generator(device=dev).manual_seed(wl.seed + 1)
+    d_out = torch.randn((wl.B, wl.H, wl.L, 64), generator=g, device=dev).to(wl.dtype)
+    out, lse = pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    ws = pa.new_workspace(pa.OP_BWD, wl.B, wl.H, wl.L, pa.BF16 if wl.dtype == torch.bfloat16
+                          else pa.F32, dev)
+    grads = {n: torch.empty((wl.B, wl.H, wl.L, 64), dtype=torch.float32, device=dev)
+             for n in ("dq", "dk", "dv", "dw")}
+    grads["dbeta"] = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        pa.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out,
+                         grads=grads, workspace=ws)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    fl = bwd_flops(wl.B, wl.H, wl.L)
+    return {"workload": wl.name.replace("fwd", "bwd"), "ms_per_step": ms,
+            "tokens_per_s": wl.B * wl.L / (ms * 1e-3), "query_pass_flops": fl,
+            "workspace_bytes": ws.numel(),
+            # fp32 UT recompute, query pass, block pass (plus three memsets)
+            "launches_per_step": 3}
+
+
 def cpu_baseline(x_cpu, wl, target_s=12.0):
     """The fp64 oracle on whole heads of the workload, timed on the host cores."""
     import oracle
@@ -376,6 +428,8 @@ PROFILE_CASES = {
                                     torch.bfloat16, 5, 1000),
     # a quarter of the producer workload: x 134 MB, w 134 MB (both larger than L2)
     "producer": pi.ProducerWorkload("path_wbeta_bf16_B8L4096D2048R64H32", 8, 4096, 2048, 64, 32, 6),
+    # the backward leg's own workload (1.3 GB of workspace, stash larger than L2)
+    "bwd": pi.BF16_L2048,
 }
 
 
@@ -395,6 +449,9 @@ def run_profile_case(args):
                                 wl.n_prefix + t, workspace=ws)
     elif args.profile == "producer":
         r = time_producer(pa, wl, steps=args.steps, warmup=args.warmup)
+        print(json.dumps(r))
+    elif args.profile == "bwd":
+        r = time_bwd(pa, wl, steps=args.steps, warmup=args.warmup)
         print(json.dumps(r))
     elif args.profile == "fox_decode":
         cap = wl.n_prefix + args.warmup + args.steps
@@ -502,7 +559,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
-    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer"],
+    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -616,6 +673,15 @@ def main():
                             "traffic": (t_down + t_up) if (t_down and t_up) else None,
                             "peak_source": "%s HBM copy" % peaks["source"]}
         line["producer"] = prod
+        del prod
+        torch.cuda.empty_cache()
+        bwd = time_bwd(pa, pi.BF16_L2048)
+        ach = bwd["query_pass_flops"] / (bwd["ms_per_step"] * 1e-3) / 1e12
+        bwd["roofline"] = {"kernels": "query-pass FP32 FLOPs over the whole backward call",
+                           "bound": "alu", "achieved": ach, "peak": FP32_ALU_TFLOPS,
+                           "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "traffic": None,
+                           "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
+        line["bwd"] = bwd
 
     if args.sweep and rank == 0:
         sweep = {}
