@@ -299,9 +299,12 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
 // One CTA per (block, head), 8 warps. Each warp takes sweeps w, w + 8, ... of 192: query
 // rows (q~_i and the diagonal logits, i = 0..63), columns of P_b (c = 0..63) and key rows
 // (k~_j, j = 0..63). Lane l holds dimensions 2l and 2l + 1 of every vector. A sweep first
-// applies its transitions keeping every intermediate vector (and w_s . x) in the warp's
-// stash, then walks back with the gradient. dk, dw and dbeta gather in shared memory
-// (several sweeps add to one token); dq is written by its query sweep.
+// applies its transitions, keeping only w_s . x of each step (64 floats per warp), then
+// walks back with the gradient, recovering each step's input by undoing the step: the step
+// is x' = x - c w_s with c = beta_s (w_s . x), so x = x' + c w_s, exact up to rounding (no
+// H_s is inverted; it is singular at beta_s = 1). dk, dw and dbeta gather in shared memory
+// (several sweeps add to one token); dq is written by its query sweep. 68 KB of shared
+// memory per CTA, three CTAs per SM.
 constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ float warp_dot(float2 a, float2 b) {
@@ -317,7 +320,7 @@ __device__ __forceinline__ float2 load2(const T *p) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 3)
 bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
                  const float *__restrict__ beta, const float *__restrict__ dqt,
                  const float *__restrict__ dkt, const float *__restrict__ dP,
@@ -328,8 +331,7 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     float2 *Ks = Ws + kBlkTile / 2;                        // k_j
     float2 *dWs = Ks + kBlkTile / 2;                       // gradient of w_s
     float2 *dKs = dWs + kBlkTile / 2;                      // gradient of k_j
-    float2 *stash = dKs + kBlkTile / 2;                    // per warp: 64 vectors
-    float *wxs = reinterpret_cast<float *>(stash + kWarps * kBlkTile / 2);  // per warp: 64 w.x
+    float *wxs = reinterpret_cast<float *>(dKs + kBlkTile / 2);  // per warp: 64 w.x
     float *bs = wxs + kWarps * kC;                      // beta_s
     float *dBs = bs + kC;                               // gradient of beta_s
 
@@ -355,7 +357,6 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     }
     __syncthreads();
 
-    float2 *stw = stash + warp * (kBlkTile / 2);
     float *wxw = wxs + warp * kC;
     // gradient through x' = H_s x (x = input, wx = w_s . x); g becomes the gradient of x
     auto back_step = [&](int s, float2 x, float wx, float2 &g) {
@@ -368,15 +369,21 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         g.x = fmaf(-be * wg, ws.x, g.x);
         g.y = fmaf(-be * wg, ws.y, g.y);
     };
-    // x <- H_s x, keeping x and w_s . x at stash slot `slot`
-    auto fwd_step = [&](int s, int slot, float2 &x) {
+    // x <- H_s x, recording w_s . x at wxw[s]
+    auto fwd_step = [&](int s, float2 &x) {
         const float2 ws = Ws[s * 32 + lane];
         const float wx = warp_dot(ws, x);
-        stw[slot * 32 + lane] = x;
-        if (lane == 0) wxw[slot] = wx;
+        if (lane == 0) wxw[s] = wx;
         const float a = bs[s] * wx;
         x.x = fmaf(-a, ws.x, x.x);
         x.y = fmaf(-a, ws.y, x.y);
+    };
+    // x <- the input of step s, from its output x and the recorded w_s . x
+    auto undo_step = [&](int s, float wx, float2 &x) {
+        const float2 ws = Ws[s * 32 + lane];
+        const float a = bs[s] * wx;
+        x.x = fmaf(a, ws.x, x.x);
+        x.y = fmaf(a, ws.y, x.y);
     };
 
     const bool has_dp = blk > 0 && blk < nblk - 1;  // P_0 and the last P_b reach no logit
@@ -388,9 +395,8 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
             const int i = idx;
             if (i >= nvalid) continue;
             float2 x = load2<T>(q + (hL + t0 + i) * kD + 2 * lane);
-            for (int s = i; s >= 1; --s) fwd_step(s, s, x);  // slot s holds x_s
-            stw[lane] = x;                                    // slot 0: x_0
-            const float wx0 = warp_dot(Ws[lane], x);
+            for (int s = i; s >= 1; --s) fwd_step(s, x);  // wxw[s] = w_s . x_s
+            const float wx0 = warp_dot(Ws[lane], x);       // x = x_0
             __syncwarp();
             float2 g = *reinterpret_cast<const float2 *>(dqt + ((size_t)bh * Lp + t0 + i) * kD + 2 * lane);
             const float2 dtr = *reinterpret_cast<const float2 *>(
@@ -400,13 +406,16 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
                 const float dtx = __shfl_sync(0xffffffffu, dtr.x, j >> 1);
                 const float dty = __shfl_sync(0xffffffffu, dtr.y, j >> 1);
                 const float dt = (j & 1) ? dty : dtx;
-                const float2 xj = stw[j * 32 + lane];
-                const float2 kj = Ks[j * 32 + lane];
+                const float2 kj = Ks[j * 32 + lane];  // x = x_j here
                 g.x = fmaf(dt, kj.x, g.x);
                 g.y = fmaf(dt, kj.y, g.y);
-                atomicAdd(&dKs[j * 32 + lane].x, dt * xj.x);
-                atomicAdd(&dKs[j * 32 + lane].y, dt * xj.y);
-                if (j < i) back_step(j + 1, stw[(j + 1) * 32 + lane], wxw[j + 1], g);
+                atomicAdd(&dKs[j * 32 + lane].x, dt * x.x);
+                atomicAdd(&dKs[j * 32 + lane].y, dt * x.y);
+                if (j < i) {
+                    const float wx = wxw[j + 1];
+                    undo_step(j + 1, wx, x);  // x = x_{j+1}
+                    back_step(j + 1, x, wx, g);
+                }
             }
             *reinterpret_cast<float2 *>(dq + (hL + t0 + i) * kD + 2 * lane) = g;
         } else if (kind == 1) {
@@ -414,27 +423,34 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
             if (!has_dp) continue;
             const int c = idx;
             float2 x = make_float2(2 * lane == c ? 1.f : 0.f, 2 * lane + 1 == c ? 1.f : 0.f);
-            for (int s = kC - 1; s >= 1; --s) fwd_step(s, s, x);
-            stw[lane] = x;
+            for (int s = kC - 1; s >= 1; --s) fwd_step(s, x);
             const float wx0 = warp_dot(Ws[lane], x);
             __syncwarp();
             const float *dpb = dP + ((size_t)bh * nblk + blk) * kBlkTile;
             float2 g = make_float2(dpb[(2 * lane) * kC + c], dpb[(2 * lane + 1) * kC + c]);
             back_step(0, x, wx0, g);
-            for (int j = 0; j + 1 < kC; ++j) back_step(j + 1, stw[(j + 1) * 32 + lane], wxw[j + 1], g);
+            for (int j = 0; j + 1 < kC; ++j) {
+                const float wx = wxw[j + 1];
+                undo_step(j + 1, wx, x);
+                back_step(j + 1, x, wx, g);
+            }
         } else {
             // ---- key row j: k~_j = H_63 ... H_{j+1} k_j
             const int j = idx;
             if (j >= nvalid || !has_dk) continue;
             float2 y = Ks[j * 32 + lane];
-            for (int s = j + 1; s < kC; ++s) fwd_step(s, s, y);  // slot s: input of H_s
+            for (int s = j + 1; s < kC; ++s) fwd_step(s, y);  // wxw[s]: w_s . (input of H_s)
             __syncwarp();
             float2 g = *reinterpret_cast<const float2 *>(dkt + ((size_t)bh * Lp + t0 + j) * kD + 2 * lane);
-            for (int s = kC - 1; s > j; --s) back_step(s, stw[s * 32 + lane], wxw[s], g);
+            for (int s = kC - 1; s > j; --s) {
+                const float wx = wxw[s];
+                undo_step(s, wx, y);  // y = input of H_s
+                back_step(s, y, wx, g);
+            }
             atomicAdd(&dKs[j * 32 + lane].x, g.x);
             atomicAdd(&dKs[j * 32 + lane].y, g.y);
         }
-        __syncwarp();  // the next sweep rewrites the stash
+        __syncwarp();  // the next sweep rewrites wxw
     }
     __syncthreads();
     for (int e = tid; e < nvalid * 32; e += kThreads) {
@@ -481,7 +497,7 @@ BwdLayout bwd_layout(int B, int H, int L) {
 }
 
 size_t bwd_query_smem() { return (size_t)(9 * BUF + 2 * kC) * sizeof(float); }
-size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kBlkTile + kWarps * kC + 2 * kC) * sizeof(float); }
+size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC + 2 * kC) * sizeof(float); }
 
 // dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32. dv gathers by atomics from zero.
 template <typename T>
