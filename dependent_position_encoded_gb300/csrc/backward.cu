@@ -43,22 +43,6 @@ constexpr int BUF = kC * LD;
 constexpr int kThreads = 256;
 constexpr int kBlkTile = kC * kD;  // floats in one 64 x 64 tile
 
-// acc[i][j] += sum_k X[k][m0 + i] * Y[k][n0 + j]  (both operands k-major in shared memory)
-__device__ __forceinline__ void mm_acc(const float *__restrict__ X, const float *__restrict__ Y,
-                                       int m0, int n0, float (&acc)[4][4]) {
-#pragma unroll 4
-    for (int k = 0; k < kC; ++k) {
-        const float4 a = *reinterpret_cast<const float4 *>(X + k * LD + m0);
-        const float4 b = *reinterpret_cast<const float4 *>(Y + k * LD + n0);
-        const float av[4] = {a.x, a.y, a.z, a.w};
-        const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-}
-
 __device__ __forceinline__ void zero4(float (&a)[4][4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -67,34 +51,100 @@ __device__ __forceinline__ void zero4(float (&a)[4][4]) {
 }
 
 // 64 x 64 fp32 tile from global (row-major, 64 floats per row) into shared memory, as is
-// (dst[r][c]) or transposed (dst[c][r]).
+// (dst[r][c]) or transposed (dst[c][r]). Each thread issues all four of its 16-byte loads
+// before the first store, so the tile costs one memory latency.
 __device__ __forceinline__ void load_tile(float *dst, const float *__restrict__ src, bool transpose) {
-    for (int e = threadIdx.x; e < kBlkTile; e += kThreads) {
-        const int r = e / kD, c = e % kD;
-        const float x = src[e];
-        if (transpose) dst[c * LD + r] = x;
-        else dst[r * LD + c] = x;
+    constexpr int kIt = kBlkTile / 4 / kThreads;
+    float4 x[kIt];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it)
+        x[it] = reinterpret_cast<const float4 *>(src)[threadIdx.x + it * kThreads];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+        const int e = 4 * (threadIdx.x + it * kThreads), r = e / kD, c = e % kD;
+        if (transpose) {
+            dst[c * LD + r] = x[it].x;
+            dst[(c + 1) * LD + r] = x[it].y;
+            dst[(c + 2) * LD + r] = x[it].z;
+            dst[(c + 3) * LD + r] = x[it].w;
+        } else {
+            *reinterpret_cast<float4 *>(dst + r * LD + c) = x[it];
+        }
     }
 }
 
 // Rows t0 .. t0 + 63 of a (rows, 64) tensor of type T, zero past L, as is and transposed
-// (either may be null).
+// (either may be null); four elements per thread and step, all loads issued first.
 template <typename T>
 __device__ __forceinline__ void load_rows(float *dst, float *dst_t, const T *__restrict__ src,
                                           int t0, int L) {
-    for (int e = threadIdx.x; e < kBlkTile; e += kThreads) {
-        const int r = e / kD, c = e % kD;
-        const float x = (t0 + r < L) ? Elt<T>::to_f(src[(size_t)(t0 + r) * kD + c]) : 0.f;
-        if (dst) dst[r * LD + c] = x;
-        if (dst_t) dst_t[c * LD + r] = x;
+    constexpr int kIt = kBlkTile / 4 / kThreads;
+    float x[kIt][4];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+        const int e = 4 * (threadIdx.x + it * kThreads), r = e / kD, c = e % kD;
+        const bool in = t0 + r < L;
+        const T *p = src + (size_t)(t0 + r) * kD + c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[it][q] = in ? Elt<T>::to_f(p[q]) : 0.f;
+    }
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+        const int e = 4 * (threadIdx.x + it * kThreads), r = e / kD, c = e % kD;
+        if (dst) *reinterpret_cast<float4 *>(dst + r * LD + c) = make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
+        if (dst_t)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst_t[(c + q) * LD + r] = x[it][q];
     }
 }
 
 // ---------------------------------------------------------------- B1: query pass
-// One CTA per (query block a, head); a runs from the last block down so that the longest
-// walks start first.
+// acc[i][j] += sum_k A[m0 + i][k] * B[k][n0 + j]: A row-major (the lanes of a quarter warp
+// share m0, so its loads are broadcasts), B k-major. Four k at a time: 8 16-byte loads per
+// 64 FMAs, as with both operands k-major, so no operand needs a second, transposed copy.
+__device__ __forceinline__ void mm_rowa(const float *__restrict__ A, const float *__restrict__ B,
+                                        int m0, int n0, float (&acc)[4][4]) {
+#pragma unroll 2
+    for (int k = 0; k < kC; k += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (m0 + i) * LD + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4 b = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + n0);
+            const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+            }
+        }
+    }
+}
+
+// A 4 x 4 register tile (rows m0.., columns n0..) into shared memory as is or transposed.
+__device__ __forceinline__ void put_acc(float *dst, const float (&v)[4][4], int m0, int n0,
+                                        bool transpose) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (transpose) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[(n0 + j) * LD + m0 + i] = v[i][j];
+        } else {
+            *reinterpret_cast<float4 *>(dst + (m0 + i) * LD + n0) =
+                make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+        }
+    }
+}
+
+// One CTA per (query block a, head), two per SM; a runs from the last block down so that
+// the longest walks start first. Six 64 x 64 fp32 buffers (R0-R5):
+//   pass 1: R0 X [i][c], R1 dout [i][c], R2 K~_b^T then p^T [j][i], R3 P_b^T then dT^T [j][i],
+//           R4 V_b^T [c][j]
+//   pass 2: R0 X, R1 dT [i][j], R2 K~_b [j][c], R3 P_b [n][c], R4 G [i][n], R5 G^T [n][i]
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__restrict__ dout,
                  const float *__restrict__ lse, const float *__restrict__ qt,
                  const float *__restrict__ kp, const float *__restrict__ dg,
@@ -102,17 +152,9 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                  float *__restrict__ dTd, float *__restrict__ stash, float *__restrict__ dv,
                  int L, int Lp, int nblk, float scale, float scale_log2) {
     extern __shared__ __align__(16) float sm[];
-    float *XT = sm;              // pass 1: X^T [c][i]
-    float *Xr = XT + BUF;        // X [i][c] (pass 2: from the stash)
-    float *KB = Xr + BUF;        // pass 1: K~_b^T [c][j];  pass 2: K~_b [j][c]
-    float *PB = KB + BUF;        // pass 1: P_b^T [c][n];   pass 2: P_b [n][c]
-    float *B4 = PB + BUF;        // pass 1: V_b^T [c][j];   pass 2: G^T [n][i]
-    float *B5 = B4 + BUF;        // pass 1: dout^T [c][i];  pass 2: G [i][n]
-    float *dOr = B5 + BUF;       // dout [i][c]
-    float *B7 = dOr + BUF;       // pass 1: p [i][j];       pass 2: dT^T [j][i]
-    float *dTm = B7 + BUF;       // pass 1: dT [i][j]
-    float *lse2 = dTm + BUF;     // per row: lse * log2(e)
-    float *Drow = lse2 + kC;     // per row: dout . out
+    float *R0 = sm, *R1 = R0 + BUF, *R2 = R1 + BUF, *R3 = R2 + BUF, *R4 = R3 + BUF, *R5 = R4 + BUF;
+    float *lse2 = R5 + BUF;     // per row: lse * log2(e)
+    float *Drow = lse2 + kC;    // per row: dout . out
 
     const int tid = threadIdx.x;
     const int a = nblk - 1 - (int)blockIdx.x;
@@ -120,6 +162,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
     const int t0 = a * kC;
     const size_t hL = (size_t)bh * L;
+    const T *vh = v + hL * kD;
 
     // ---- per row: lse in log2 units and D_i = dout_i . out_i (4 threads per row)
     {
@@ -138,17 +181,18 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
             lse2[row] = (t0 + row < L) ? lse[hL + t0 + row] * kLog2e : 0.f;
         }
     }
-    load_rows<T>(dOr, B5, dout + hL * kD, t0, L);
-    load_rows<T>(nullptr, B4, v + hL * kD, t0, L);
+    load_rows<T>(R1, nullptr, dout + hL * kD, t0, L);
+    load_rows<T>(nullptr, R4, vh, t0, L);
     __syncthreads();
 
+    float dpm[4][4];
     // ---- diagonal block: logits from the table; dT to the block pass, p^T dout to dv
-    float pr[4][4], dpm[4][4];
     {
         zero4(dpm);
-        mm_acc(B5, B4, m0, n0, dpm);  // dout_i . v_j
+        mm_rowa(R1, R4, m0, n0, dpm);  // dout_i . v_j
         const float *tab = dg + ((size_t)bh * nblk + a) * kBlkTile;
         float *dtd = dTd + ((size_t)bh * nblk + a) * kBlkTile;
+        float pr[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = m0 + i;
@@ -162,14 +206,14 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                 dt[j] = scale * p * (dpm[i][j] - Drow[r]);
             }
             *reinterpret_cast<float4 *>(dtd + r * kC + n0) = make_float4(dt[0], dt[1], dt[2], dt[3]);
-            *reinterpret_cast<float4 *>(B7 + r * LD + n0) = make_float4(pr[i][0], pr[i][1], pr[i][2], pr[i][3]);
         }
+        put_acc(R2, pr, m0, n0, true);  // p^T
     }
     __syncthreads();
     {
         float acc[4][4];
         zero4(acc);
-        mm_acc(B7, dOr, m0, n0, acc);  // sum_i p_ij dout_i[c]
+        mm_rowa(R2, R1, m0, n0, acc);  // sum_i p_ij dout_i[c]
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if (t0 + m0 + j < L)
@@ -179,58 +223,53 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     }
 
     // ---- pass 1: right to left over key blocks, X from Q~_a
-    const float *qa = qt + ((size_t)bh * Lp + t0) * kD;
+    auto kp_block = [&](int b) { return kp + ((size_t)bh * nblk + b) * 2 * kBlkTile; };
     __syncthreads();
-    for (int e = tid; e < kBlkTile; e += kThreads) {
-        const int r = e / kD, c = e % kD;
-        const float x = qa[e];
-        XT[c * LD + r] = x;
-        Xr[r * LD + c] = x;
-    }
+    load_tile(R0, qt + ((size_t)bh * Lp + t0) * kD, false);
     const size_t pair0 = (size_t)bh * ((size_t)nblk * (nblk - 1) / 2) + (size_t)a * (a - 1) / 2;
     for (int b = a - 1; b >= 0; --b) {
-        const float *blk = kp + ((size_t)bh * nblk + b) * 2 * kBlkTile;
         __syncthreads();
-        load_tile(KB, blk, true);
-        load_tile(PB, blk + kBlkTile, true);
-        load_rows<T>(nullptr, B4, v + hL * kD, b * kC, L);
+        load_tile(R2, kp_block(b), true);
+        load_tile(R3, kp_block(b) + kBlkTile, true);
+        load_rows<T>(nullptr, R4, vh, b * kC, L);
         __syncthreads();
         float s[4][4], xn[4][4];
         zero4(s);
         zero4(dpm);
         zero4(xn);
-        mm_acc(XT, KB, m0, n0, s);
-        mm_acc(B5, B4, m0, n0, dpm);
-        if (b > 0) mm_acc(XT, PB, m0, n0, xn);
+        mm_rowa(R0, R2, m0, n0, s);
+        mm_rowa(R1, R4, m0, n0, dpm);
+        if (b > 0) mm_rowa(R0, R3, m0, n0, xn);
         float *st = stash + (pair0 + b) * 2 * kBlkTile;  // [X_{a,b} | dT_ab], row-major
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = m0 + i;
-            float p4[4], d4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float p = (t0 + r < L) ? exp2f(s[i][j] * scale_log2 - lse2[r]) : 0.f;
-                p4[j] = p;
-                d4[j] = scale * p * (dpm[i][j] - Drow[r]);
+                s[i][j] = p;                                      // s now holds p
+                dpm[i][j] = scale * p * (dpm[i][j] - Drow[r]);   // dpm now holds dT
             }
-            *reinterpret_cast<float4 *>(B7 + r * LD + n0) = make_float4(p4[0], p4[1], p4[2], p4[3]);
-            *reinterpret_cast<float4 *>(dTm + r * LD + n0) = make_float4(d4[0], d4[1], d4[2], d4[3]);
-            *reinterpret_cast<float4 *>(st + kBlkTile + r * kC + n0) = make_float4(d4[0], d4[1], d4[2], d4[3]);
+            *reinterpret_cast<float4 *>(st + kBlkTile + r * kC + n0) =
+                make_float4(dpm[i][0], dpm[i][1], dpm[i][2], dpm[i][3]);
             *reinterpret_cast<float4 *>(st + r * kC + n0) =
-                *reinterpret_cast<const float4 *>(Xr + r * LD + n0);
+                *reinterpret_cast<const float4 *>(R0 + r * LD + n0);
         }
+        __syncthreads();  // K~_b^T and P_b^T are read: their buffers take p^T and dT^T
+        put_acc(R2, s, m0, n0, true);
+        put_acc(R3, dpm, m0, n0, true);
         __syncthreads();
         {
             float acc[4][4];
             zero4(acc);
-            mm_acc(dTm, Xr, m0, n0, acc);  // dK~_b[j][c] += sum_i dT_ij X_ic
+            mm_rowa(R3, R0, m0, n0, acc);  // dK~_b[j][c] += sum_i dT_ij X_ic
             float *dk = dkt + ((size_t)bh * Lp + (size_t)b * kC) * kD;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) atomicAdd(dk + (m0 + j) * kD + n0 + c, acc[j][c]);
             zero4(acc);
-            mm_acc(B7, dOr, m0, n0, acc);  // dv_j += sum_i p_ij dout_i (key block b < a is full)
+            mm_rowa(R2, R1, m0, n0, acc);  // dv_j += sum_i p_ij dout_i (key block b < a is full)
             float *dvb = dv + (hL + (size_t)b * kC) * kD;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -238,15 +277,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                 for (int c = 0; c < 4; ++c) atomicAdd(dvb + (m0 + j) * kD + n0 + c, acc[j][c]);
         }
         __syncthreads();
-        if (b > 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                *reinterpret_cast<float4 *>(Xr + (m0 + i) * LD + n0) =
-                    make_float4(xn[i][0], xn[i][1], xn[i][2], xn[i][3]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) XT[(n0 + j) * LD + m0 + i] = xn[i][j];
-            }
-        }
+        if (b > 0) put_acc(R0, xn, m0, n0, false);
     }
 
     // ---- pass 2: left to right, G = gradient of X_{a,b}
@@ -254,22 +285,21 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     zero4(g);
     __syncthreads();
     for (int e = tid; e < BUF; e += kThreads) {
-        B4[e] = 0.f;
-        B5[e] = 0.f;
+        R4[e] = 0.f;
+        R5[e] = 0.f;
     }
     for (int b = 0; b < a; ++b) {
-        const float *blk = kp + ((size_t)bh * nblk + b) * 2 * kBlkTile;
         const float *st = stash + (pair0 + b) * 2 * kBlkTile;
         __syncthreads();
-        load_tile(Xr, st, false);
-        load_tile(B7, st + kBlkTile, true);
-        load_tile(KB, blk, false);
-        load_tile(PB, blk + kBlkTile, false);
+        load_tile(R0, st, false);
+        load_tile(R1, st + kBlkTile, false);
+        load_tile(R2, kp_block(b), false);
+        load_tile(R3, kp_block(b) + kBlkTile, false);
         __syncthreads();
         if (b > 0) {
             float acc[4][4];
             zero4(acc);
-            mm_acc(B5, Xr, m0, n0, acc);  // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c]
+            mm_rowa(R5, R0, m0, n0, acc);  // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c]
             float *dpb = dP + ((size_t)bh * nblk + b) * kBlkTile;
 #pragma unroll
             for (int n = 0; n < 4; ++n)
@@ -277,16 +307,11 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                 for (int c = 0; c < 4; ++c) atomicAdd(dpb + (m0 + n) * kC + n0 + c, acc[n][c]);
         }
         zero4(g);
-        if (b > 0) mm_acc(B4, PB, m0, n0, g);  // G_{b-1} P_b
-        mm_acc(B7, KB, m0, n0, g);             // + dT_ab K~_b
+        if (b > 0) mm_rowa(R4, R3, m0, n0, g);  // G_{b-1} P_b
+        mm_rowa(R1, R2, m0, n0, g);             // + dT_ab K~_b
         __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            *reinterpret_cast<float4 *>(B5 + (m0 + i) * LD + n0) =
-                make_float4(g[i][0], g[i][1], g[i][2], g[i][3]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) B4[(n0 + j) * LD + m0 + i] = g[i][j];
-        }
+        put_acc(R4, g, m0, n0, false);
+        put_acc(R5, g, m0, n0, true);
     }
     // dQ~_a = G_{a-1} (zero for the first block)
     float *dq = dqt + ((size_t)bh * Lp + t0) * kD;
@@ -496,7 +521,7 @@ BwdLayout bwd_layout(int B, int H, int L) {
     return y;
 }
 
-size_t bwd_query_smem() { return (size_t)(9 * BUF + 2 * kC) * sizeof(float); }
+size_t bwd_query_smem() { return (size_t)(6 * BUF + 2 * kC) * sizeof(float); }
 size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC + 2 * kC) * sizeof(float); }
 
 // dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32. dv gathers by atomics from zero.
