@@ -321,22 +321,28 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
 }
 
 // ---------------------------------------------------------------- B2: block pass
-// One CTA per (block, head), 8 warps. Each warp takes sweeps w, w + 8, ... of 192: query
-// rows (q~_i and the diagonal logits, i = 0..63), columns of P_b (c = 0..63) and key rows
-// (k~_j, j = 0..63). Lane l holds dimensions 2l and 2l + 1 of every vector. A sweep first
-// applies its transitions, keeping only w_s . x of each step (64 floats per warp), then
-// walks back with the gradient, recovering each step's input by undoing the step: the step
-// is x' = x - c w_s with c = beta_s (w_s . x), so x = x' + c w_s, exact up to rounding (no
-// H_s is inverted; it is singular at beta_s = 1). dk, dw and dbeta gather in shared memory
-// (several sweeps add to one token); dq is written by its query sweep. 68 KB of shared
-// memory per CTA, three CTAs per SM.
+// One CTA per (block, head), 8 warps, two CTAs per SM. Warp w runs three groups of eight
+// sweeps, each group in lockstep: query rows i = 8w .. 8w + 7 (q~_i and the diagonal
+// logits), columns c = 8w .. 8w + 7 of P_b, and key rows j = 8w .. 8w + 7 (k~_j); short
+// query sweeps meet long key sweeps, so the warps' loads match. Lane l holds dimensions 2l
+// and 2l + 1 of every vector. A sweep first applies its transitions, recording only
+// w_s . x of each step, then walks back with the gradient, recovering each step's input by
+// undoing the step: the step is x' = x - c w_s with c = beta_s (w_s . x), so x = x' + c w_s,
+// exact up to rounding (no H_s is inverted; it is singular at beta_s = 1). Per step the
+// eight sweeps share one read of w_s and beta_s, run eight independent warp reductions,
+// and add their summed dw, dk and dbeta terms to shared memory with one atomic per lane.
+// dq is written by its query sweep.
 constexpr int kWarps = kThreads / 32;
+constexpr int kNS = 8;  // sweeps per warp group
 
-__device__ __forceinline__ float warp_dot(float2 a, float2 b) {
-    float s = fmaf(a.x, b.x, a.y * b.y);
+// out[k] = w . x[k] over the warp, for the eight vectors of a group
+__device__ __forceinline__ void dot8(const float2 (&x)[kNS], float2 w, float (&out)[kNS]) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    return s;
+    for (int k = 0; k < kNS; ++k) out[k] = fmaf(w.x, x[k].x, w.y * x[k].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int k = 0; k < kNS; ++k) out[k] += __shfl_xor_sync(0xffffffffu, out[k], o);
 }
 
 template <typename T>
@@ -345,20 +351,20 @@ __device__ __forceinline__ float2 load2(const T *p) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
                  const float *__restrict__ beta, const float *__restrict__ dqt,
                  const float *__restrict__ dkt, const float *__restrict__ dP,
                  const float *__restrict__ dTd, float *__restrict__ dq, float *__restrict__ dk,
                  float *__restrict__ dw, float *__restrict__ dbeta, int L, int Lp, int nblk) {
     extern __shared__ __align__(16) float sm[];
-    float2 *Ws = reinterpret_cast<float2 *>(sm);        // w_s, [s][lane]
-    float2 *Ks = Ws + kBlkTile / 2;                        // k_j
-    float2 *dWs = Ks + kBlkTile / 2;                       // gradient of w_s
-    float2 *dKs = dWs + kBlkTile / 2;                      // gradient of k_j
-    float *wxs = reinterpret_cast<float *>(dKs + kBlkTile / 2);  // per warp: 64 w.x
-    float *bs = wxs + kWarps * kC;                      // beta_s
-    float *dBs = bs + kC;                               // gradient of beta_s
+    float2 *Ws = reinterpret_cast<float2 *>(sm);             // w_s, [s][lane]
+    float2 *Ks = Ws + kBlkTile / 2;                          // k_j
+    float2 *dWs = Ks + kBlkTile / 2;                         // gradient of w_s
+    float2 *dKs = dWs + kBlkTile / 2;                        // gradient of k_j
+    float *wxs = reinterpret_cast<float *>(dKs + kBlkTile / 2);  // per warp: [s][sweep] w_s . x
+    float *bs = wxs + kWarps * kC * kNS;                     // beta_s
+    float *dBs = bs + kC;                                    // gradient of beta_s
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int blk = blockIdx.x, bh = blockIdx.y;
@@ -382,107 +388,150 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     }
     __syncthreads();
 
-    float *wxw = wxs + warp * kC;
-    // gradient through x' = H_s x (x = input, wx = w_s . x); g becomes the gradient of x
-    auto back_step = [&](int s, float2 x, float wx, float2 &g) {
+    float *wxw = wxs + warp * kC * kNS;
+    const int base = kNS * warp;  // first row / column of this warp's groups
+    float2 x[kNS], g[kNS];
+    float wx[kNS], wg[kNS];
+
+    // x[k] <- H_s x[k] for the sweeps with act(k), recording w_s . x[k] at wxw[s][k]
+    auto fwd = [&](int s, auto act) {
         const float2 ws = Ws[s * 32 + lane];
-        const float wg = warp_dot(ws, g);
         const float be = bs[s];
-        atomicAdd(&dWs[s * 32 + lane].x, -be * fmaf(wx, g.x, wg * x.x));
-        atomicAdd(&dWs[s * 32 + lane].y, -be * fmaf(wx, g.y, wg * x.y));
-        if (lane == 0) atomicAdd(&dBs[s], -wg * wx);
-        g.x = fmaf(-be * wg, ws.x, g.x);
-        g.y = fmaf(-be * wg, ws.y, g.y);
+        dot8(x, ws, wx);
+        if (lane == 0) {
+            *reinterpret_cast<float4 *>(wxw + s * kNS) = make_float4(wx[0], wx[1], wx[2], wx[3]);
+            *reinterpret_cast<float4 *>(wxw + s * kNS + 4) = make_float4(wx[4], wx[5], wx[6], wx[7]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk)
+            if (act(kk)) {
+                x[kk].x = fmaf(-be * wx[kk], ws.x, x[kk].x);
+                x[kk].y = fmaf(-be * wx[kk], ws.y, x[kk].y);
+            }
     };
-    // x <- H_s x, recording w_s . x at wxw[s]
-    auto fwd_step = [&](int s, float2 &x) {
+    // one step back through H_s for the sweeps with act(k): x[k] <- the step's input (undo),
+    // dw_s, dbeta_s gather the terms, g[k] <- H_s g[k]. `undo` false for a step whose input
+    // is already in x (the first step back, through H_0, with w_0 . x given in wx).
+    auto back = [&](int s, bool undo, auto act) {
         const float2 ws = Ws[s * 32 + lane];
-        const float wx = warp_dot(ws, x);
-        if (lane == 0) wxw[s] = wx;
-        const float a = bs[s] * wx;
-        x.x = fmaf(-a, ws.x, x.x);
-        x.y = fmaf(-a, ws.y, x.y);
-    };
-    // x <- the input of step s, from its output x and the recorded w_s . x
-    auto undo_step = [&](int s, float wx, float2 &x) {
-        const float2 ws = Ws[s * 32 + lane];
-        const float a = bs[s] * wx;
-        x.x = fmaf(a, ws.x, x.x);
-        x.y = fmaf(a, ws.y, x.y);
+        const float be = bs[s];
+        if (undo) {
+            const float4 a = *reinterpret_cast<const float4 *>(wxw + s * kNS);
+            const float4 b = *reinterpret_cast<const float4 *>(wxw + s * kNS + 4);
+            wx[0] = a.x; wx[1] = a.y; wx[2] = a.z; wx[3] = a.w;
+            wx[4] = b.x; wx[5] = b.y; wx[6] = b.z; wx[7] = b.w;
+#pragma unroll
+            for (int kk = 0; kk < kNS; ++kk)
+                if (act(kk)) {
+                    x[kk].x = fmaf(be * wx[kk], ws.x, x[kk].x);
+                    x[kk].y = fmaf(be * wx[kk], ws.y, x[kk].y);
+                }
+        }
+        dot8(g, ws, wg);
+        float2 dws = make_float2(0.f, 0.f);
+        float db = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk)
+            if (act(kk)) {
+                dws.x += fmaf(wx[kk], g[kk].x, wg[kk] * x[kk].x);
+                dws.y += fmaf(wx[kk], g[kk].y, wg[kk] * x[kk].y);
+                db = fmaf(wg[kk], wx[kk], db);
+                g[kk].x = fmaf(-be * wg[kk], ws.x, g[kk].x);
+                g[kk].y = fmaf(-be * wg[kk], ws.y, g[kk].y);
+            }
+        atomicAdd(&dWs[s * 32 + lane].x, -be * dws.x);
+        atomicAdd(&dWs[s * 32 + lane].y, -be * dws.y);
+        if (lane == 0) atomicAdd(&dBs[s], -db);
     };
 
-    const bool has_dp = blk > 0 && blk < nblk - 1;  // P_0 and the last P_b reach no logit
-    const bool has_dk = blk < nblk - 1;             // the last block's k~ reach no later query
-    for (int task = warp; task < 3 * kC; task += kWarps) {
-        const int kind = task / kC, idx = task % kC;
-        if (kind == 0) {
-            // ---- query row i: x_j = H_{j+1} ... H_i q_i, q~_i = H_0 x_0, T_ij = k_j . x_j
-            const int i = idx;
-            if (i >= nvalid) continue;
-            float2 x = load2<T>(q + (hL + t0 + i) * kD + 2 * lane);
-            for (int s = i; s >= 1; --s) fwd_step(s, x);  // wxw[s] = w_s . x_s
-            const float wx0 = warp_dot(Ws[lane], x);       // x = x_0
-            __syncwarp();
-            float2 g = *reinterpret_cast<const float2 *>(dqt + ((size_t)bh * Lp + t0 + i) * kD + 2 * lane);
-            const float2 dtr = *reinterpret_cast<const float2 *>(
-                dTd + (((size_t)bh * nblk + blk) * kC + i) * kC + 2 * lane);
-            back_step(0, x, wx0, g);
-            for (int j = 0; j <= i; ++j) {
-                const float dtx = __shfl_sync(0xffffffffu, dtr.x, j >> 1);
-                const float dty = __shfl_sync(0xffffffffu, dtr.y, j >> 1);
-                const float dt = (j & 1) ? dty : dtx;
-                const float2 kj = Ks[j * 32 + lane];  // x = x_j here
-                g.x = fmaf(dt, kj.x, g.x);
-                g.y = fmaf(dt, kj.y, g.y);
-                atomicAdd(&dKs[j * 32 + lane].x, dt * x.x);
-                atomicAdd(&dKs[j * 32 + lane].y, dt * x.y);
-                if (j < i) {
-                    const float wx = wxw[j + 1];
-                    undo_step(j + 1, wx, x);  // x = x_{j+1}
-                    back_step(j + 1, x, wx, g);
-                }
-            }
-            *reinterpret_cast<float2 *>(dq + (hL + t0 + i) * kD + 2 * lane) = g;
-        } else if (kind == 1) {
-            // ---- column c of P_b = H_0 ... H_63 e_c
-            if (!has_dp) continue;
-            const int c = idx;
-            float2 x = make_float2(2 * lane == c ? 1.f : 0.f, 2 * lane + 1 == c ? 1.f : 0.f);
-            for (int s = kC - 1; s >= 1; --s) fwd_step(s, x);
-            const float wx0 = warp_dot(Ws[lane], x);
-            __syncwarp();
-            const float *dpb = dP + ((size_t)bh * nblk + blk) * kBlkTile;
-            float2 g = make_float2(dpb[(2 * lane) * kC + c], dpb[(2 * lane + 1) * kC + c]);
-            back_step(0, x, wx0, g);
-            for (int j = 0; j + 1 < kC; ++j) {
-                const float wx = wxw[j + 1];
-                undo_step(j + 1, wx, x);
-                back_step(j + 1, x, wx, g);
-            }
-        } else {
-            // ---- key row j: k~_j = H_63 ... H_{j+1} k_j
-            const int j = idx;
-            if (j >= nvalid || !has_dk) continue;
-            float2 y = Ks[j * 32 + lane];
-            for (int s = j + 1; s < kC; ++s) fwd_step(s, y);  // wxw[s]: w_s . (input of H_s)
-            __syncwarp();
-            float2 g = *reinterpret_cast<const float2 *>(dkt + ((size_t)bh * Lp + t0 + j) * kD + 2 * lane);
-            for (int s = kC - 1; s > j; --s) {
-                const float wx = wxw[s];
-                undo_step(s, wx, y);  // y = input of H_s
-                back_step(s, y, wx, g);
-            }
-            atomicAdd(&dKs[j * 32 + lane].x, g.x);
-            atomicAdd(&dKs[j * 32 + lane].y, g.y);
+    const auto all = [](int) { return true; };
+    // ---- query rows i = base + k: x_j = H_{j+1} ... H_i q_i, q~_i = H_0 x_0, T_ij = k_j . x_j
+    {
+        float2 dtr[kNS];
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk) {
+            const int i = base + kk;
+            const bool in = i < nvalid;
+            x[kk] = in ? load2<T>(q + (hL + t0 + i) * kD + 2 * lane) : make_float2(0.f, 0.f);
+            g[kk] = in ? *reinterpret_cast<const float2 *>(dqt + ((size_t)bh * Lp + t0 + i) * kD + 2 * lane)
+                       : make_float2(0.f, 0.f);
+            dtr[kk] = in ? *reinterpret_cast<const float2 *>(
+                               dTd + (((size_t)bh * nblk + blk) * kC + i) * kC + 2 * lane)
+                         : make_float2(0.f, 0.f);
         }
-        __syncwarp();  // the next sweep rewrites wxw
+        for (int s = base + kNS - 1; s >= 1; --s) fwd(s, [&](int kk) { return s <= base + kk; });
+        __syncwarp();
+        dot8(x, Ws[lane], wx);  // w_0 . x_0
+        back(0, false, all);
+        for (int j = 0; j < base + kNS; ++j) {
+            const float2 kj = Ks[j * 32 + lane];  // x[k] = x_j here
+            float2 dka = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int kk = 0; kk < kNS; ++kk)
+                if (j <= base + kk) {
+                    const float dtx = __shfl_sync(0xffffffffu, dtr[kk].x, j >> 1);
+                    const float dty = __shfl_sync(0xffffffffu, dtr[kk].y, j >> 1);
+                    const float dt = (j & 1) ? dty : dtx;
+                    g[kk].x = fmaf(dt, kj.x, g[kk].x);
+                    g[kk].y = fmaf(dt, kj.y, g[kk].y);
+                    dka.x = fmaf(dt, x[kk].x, dka.x);
+                    dka.y = fmaf(dt, x[kk].y, dka.y);
+                }
+            atomicAdd(&dKs[j * 32 + lane].x, dka.x);
+            atomicAdd(&dKs[j * 32 + lane].y, dka.y);
+            if (j + 1 < base + kNS) back(j + 1, true, [&](int kk) { return j + 1 <= base + kk; });
+        }
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk)
+            if (base + kk < nvalid)
+                *reinterpret_cast<float2 *>(dq + (hL + t0 + base + kk) * kD + 2 * lane) = g[kk];
+    }
+    __syncwarp();  // the next group rewrites wxw
+
+    // ---- columns c = base + k of P_b = H_0 ... H_63 (P_0 and the last P_b reach no logit)
+    if (blk > 0 && blk < nblk - 1) {
+        const float *dpb = dP + ((size_t)bh * nblk + blk) * kBlkTile;
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk) {
+            const int c = base + kk;
+            x[kk] = make_float2(2 * lane == c ? 1.f : 0.f, 2 * lane + 1 == c ? 1.f : 0.f);
+            g[kk] = make_float2(dpb[(2 * lane) * kC + c], dpb[(2 * lane + 1) * kC + c]);
+        }
+        for (int s = kC - 1; s >= 1; --s) fwd(s, all);
+        __syncwarp();
+        dot8(x, Ws[lane], wx);
+        back(0, false, all);
+        for (int s = 1; s < kC; ++s) back(s, true, all);
+    }
+    __syncwarp();
+
+    // ---- key rows j = base + k: k~_j = H_63 ... H_{j+1} k_j (the last block's k~ reach no
+    // later query)
+    if (blk < nblk - 1) {
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk) {
+            const int j = base + kk;
+            const bool in = j < nvalid;
+            x[kk] = in ? Ks[j * 32 + lane] : make_float2(0.f, 0.f);
+            g[kk] = in ? *reinterpret_cast<const float2 *>(dkt + ((size_t)bh * Lp + t0 + j) * kD + 2 * lane)
+                       : make_float2(0.f, 0.f);
+        }
+        for (int s = base + 1; s < kC; ++s) fwd(s, [&](int kk) { return s > base + kk; });
+        __syncwarp();
+        for (int s = kC - 1; s > base; --s) back(s, true, [&](int kk) { return s > base + kk; });
+#pragma unroll
+        for (int kk = 0; kk < kNS; ++kk)
+            if (base + kk < nvalid) {
+                atomicAdd(&dKs[(base + kk) * 32 + lane].x, g[kk].x);
+                atomicAdd(&dKs[(base + kk) * 32 + lane].y, g[kk].y);
+            }
     }
     __syncthreads();
     for (int e = tid; e < nvalid * 32; e += kThreads) {
         const int r = e / 32, l = e % 32;
-        const size_t g = (hL + t0 + r) * kD + 2 * l;
-        *reinterpret_cast<float2 *>(dk + g) = dKs[e];
-        *reinterpret_cast<float2 *>(dw + g) = dWs[e];
+        const size_t gi = (hL + t0 + r) * kD + 2 * l;
+        *reinterpret_cast<float2 *>(dk + gi) = dKs[e];
+        *reinterpret_cast<float2 *>(dw + gi) = dWs[e];
     }
     if (tid < nvalid) dbeta[hL + t0 + tid] = dBs[tid];
 }
@@ -522,7 +571,7 @@ BwdLayout bwd_layout(int B, int H, int L) {
 }
 
 size_t bwd_query_smem() { return (size_t)(6 * BUF + 2 * kC) * sizeof(float); }
-size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC + 2 * kC) * sizeof(float); }
+size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC * kNS + 2 * kC) * sizeof(float); }
 
 // dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32. dv gathers by atomics from zero.
 template <typename T>
