@@ -22,13 +22,14 @@ from . import build as _build
 OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CAPACITY, ERR_TIMEOUT, \
     ERR_CUDA, ERR_ARG = range(10)
 F32, BF16 = 0, 1
-OP_FWD, OP_FOX_FWD, OP_DECODE, OP_FOX_DECODE, OP_BWD = 0, 1, 2, 3, 4
+OP_FWD, OP_FOX_FWD, OP_DECODE, OP_FOX_DECODE, OP_BWD, OP_FOX_BWD = 0, 1, 2, 3, 4, 5
 HEAD_DIM = 64
 
 EXPORTED = ("path_workspace_bytes", "path_attn_fwd", "path_fox_fwd", "path_fwd_prepare",
             "path_fwd_scan", "path_decode_step", "path_check_workspace", "path_status_string",
             "path_decode_step_noalloc", "path_fox_first_blocks", "path_fox_decode_step",
-            "path_wbeta_workspace_bytes", "path_wbeta_produce", "path_attn_bwd")
+            "path_wbeta_workspace_bytes", "path_wbeta_produce", "path_attn_bwd",
+            "path_fox_bwd")
 
 _lib = None
 
@@ -80,6 +81,8 @@ def _load():
     lib.path_wbeta_produce.restype = I
     lib.path_attn_bwd.argtypes = [P] * 8 + [I] * 5 + [F] + [P] * 6 + [S, P]
     lib.path_attn_bwd.restype = I
+    lib.path_fox_bwd.argtypes = [P] * 9 + [I] * 5 + [F] + [P] * 7 + [S, P]
+    lib.path_fox_bwd.restype = I
     lib.path_decode_step_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.path_decode_step_noalloc.restype = I
     lib.path_fox_first_blocks.argtypes = [P, S, I, I, I, I, I, P, P]
@@ -204,26 +207,38 @@ def path_attn_fwd(q, k, v, w, beta, out=None, lse=True, scale=None, workspace=No
     return out, lse
 
 
-def path_attn_bwd(q, k, v, w, beta, out, lse, d_out, scale=None, grads=None, workspace=None,
-                  stream=None):
-    """PaTH backward; returns a dict of fp32 gradients dq, dk, dv, dw (B, H, L, d) and
-    dbeta (B, H, L). `out` and `lse` are the forward's outputs for the same inputs and scale;
-    `grads` may hold preallocated fp32 buffers under those names."""
+def _bwd_grads(q, grads, B, H, L, d, fox):
     torch = _torch()
-    B, H, L, d, dt = _fwd_args(q, k, v, w, beta)
-    _cuda_tensor(out, "out", q.dtype)
-    _cuda_tensor(d_out, "d_out", q.dtype)
-    _cuda_tensor(lse, "lse", torch.float32)
-    if out.shape != q.shape or d_out.shape != q.shape or lse.shape != (B, H, L):
-        raise ValueError("out, d_out must be (B, H, L, d) and lse (B, H, L)")
     g = dict(grads or {})
     for n in ("dq", "dk", "dv", "dw"):
         if n not in g:
             g[n] = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
         _cuda_tensor(g[n], n, torch.float32)
-    if "dbeta" not in g:
-        g["dbeta"] = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
-    _cuda_tensor(g["dbeta"], "dbeta", torch.float32)
+    names = ("dbeta", "dlog_f") if fox else ("dbeta",)
+    for n in names:
+        if n not in g:
+            g[n] = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+        _cuda_tensor(g[n], n, torch.float32)
+    return g
+
+
+def _bwd_checks(q, out, lse, d_out, B, H, L):
+    torch = _torch()
+    _cuda_tensor(out, "out", q.dtype)
+    _cuda_tensor(d_out, "d_out", q.dtype)
+    _cuda_tensor(lse, "lse", torch.float32)
+    if out.shape != q.shape or d_out.shape != q.shape or lse.shape != (B, H, L):
+        raise ValueError("out, d_out must be (B, H, L, d) and lse (B, H, L)")
+
+
+def path_attn_bwd(q, k, v, w, beta, out, lse, d_out, scale=None, grads=None, workspace=None,
+                  stream=None):
+    """PaTH backward; returns a dict of fp32 gradients dq, dk, dv, dw (B, H, L, d) and
+    dbeta (B, H, L). `out` and `lse` are the forward's outputs for the same inputs and scale;
+    `grads` may hold preallocated fp32 buffers under those names."""
+    B, H, L, d, dt = _fwd_args(q, k, v, w, beta)
+    _bwd_checks(q, out, lse, d_out, B, H, L)
+    g = _bwd_grads(q, grads, B, H, L, d, False)
     if workspace is None:
         workspace = new_workspace(OP_BWD, B, H, L, dt, q.device)
     _check(_load().path_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(out),
@@ -231,6 +246,28 @@ def path_attn_bwd(q, k, v, w, beta, out, lse, d_out, scale=None, grads=None, wor
                                  _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dw"]),
                                  _ptr(g["dbeta"]), _ptr(workspace), workspace.numel(),
                                  _stream(stream, q.device)), "path_attn_bwd")
+    return g
+
+
+def path_fox_bwd(q, k, v, w, beta, log_f, out, lse, d_out, scale=None, grads=None,
+                 workspace=None, stream=None):
+    """PaTH-FoX backward; as path_attn_bwd plus dlog_f (B, H, L) fp32. `out` and `lse` are
+    path_fox_fwd's outputs."""
+    torch = _torch()
+    B, H, L, d, dt = _fwd_args(q, k, v, w, beta)
+    _cuda_tensor(log_f, "log_f", torch.float32)
+    if log_f.shape != (B, H, L):
+        raise ValueError("log_f must be (B, H, L) float32")
+    _bwd_checks(q, out, lse, d_out, B, H, L)
+    g = _bwd_grads(q, grads, B, H, L, d, True)
+    if workspace is None:
+        workspace = new_workspace(OP_FOX_BWD, B, H, L, dt, q.device)
+    _check(_load().path_fox_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
+                                _ptr(out), _ptr(lse), _ptr(d_out), B, H, L, d, dt,
+                                _scale(scale, d), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                _ptr(g["dw"]), _ptr(g["dbeta"]), _ptr(g["dlog_f"]),
+                                _ptr(workspace), workspace.numel(), _stream(stream, q.device)),
+           "path_fox_bwd")
     return g
 
 

@@ -32,8 +32,8 @@ namespace path {
 
 template <typename T>
 cudaError_t launch_ut_prepare_f32out(const void *q, const void *k, const void *w,
-                                     const float *beta, int BH, int L, int Lp, int nblk,
-                                     float scale, float *qt, float *kp, float *dg,
+                                     const float *beta, const float *log_f, int BH, int L, int Lp,
+                                     int nblk, float scale, float *qt, float *kp, float *dg,
                                      uint32_t *status, cudaStream_t stream);
 
 namespace {
@@ -143,18 +143,26 @@ __device__ __forceinline__ void put_acc(float *dst, const float (&v)[4][4], int 
 //   pass 1: R0 X [i][c], R1 dout [i][c], R2 K~_b^T then p^T [j][i], R3 P_b^T then dT^T [j][i],
 //           R4 V_b^T [c][j]
 //   pass 2: R0 X, R1 dT [i][j], R2 K~_b [j][c], R3 P_b [n][c], R4 G [i][n], R5 G^T [n][i]
-template <typename T>
+// PaTH-FoX (FOX): the gate bias c_i - c_j joins every logit, as (C_a - C_b) + loc_i - loc_j
+// with C the fp64 sums of log f before each block and loc the block-local inclusive sums;
+// the row sums of dS go to rsum and its column sums to csum (atomically), from which the
+// gate gradient is formed afterwards.
+template <typename T, bool FOX>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__restrict__ dout,
                  const float *__restrict__ lse, const float *__restrict__ qt,
                  const float *__restrict__ kp, const float *__restrict__ dg,
                  float *__restrict__ dqt, float *__restrict__ dkt, float *__restrict__ dP,
                  float *__restrict__ dTd, float *__restrict__ stash, float *__restrict__ dv,
-                 int L, int Lp, int nblk, float scale, float scale_log2) {
+                 int L, int Lp, int nblk, float scale, float scale_log2,
+                 const float *__restrict__ loc, const double *__restrict__ cb,
+                 float *__restrict__ rsum, float *__restrict__ csum) {
     extern __shared__ __align__(16) float sm[];
     float *R0 = sm, *R1 = R0 + BUF, *R2 = R1 + BUF, *R3 = R2 + BUF, *R4 = R3 + BUF, *R5 = R4 + BUF;
     float *lse2 = R5 + BUF;     // per row: lse * log2(e)
     float *Drow = lse2 + kC;    // per row: dout . out
+    float *loci = Drow + kC;    // FoX: block-local gate sums of the query rows
+    float *locj = loci + kC;    // FoX: those of the current key block
 
     const int tid = threadIdx.x;
     const int a = nblk - 1 - (int)blockIdx.x;
@@ -179,8 +187,25 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         if (part == 0) {
             Drow[row] = dsum;
             lse2[row] = (t0 + row < L) ? lse[hL + t0 + row] * kLog2e : 0.f;
+            if (FOX) loci[row] = (t0 + row < L) ? loc[(size_t)bh * Lp + t0 + row] : 0.f;
         }
     }
+    // FoX: row sums of dS stay in registers (every lane of a row's 16 ends with the total);
+    // column sums of a tile go out with one atomic per column and warp
+    float rs_acc[4] = {0.f, 0.f, 0.f, 0.f};
+    auto fox_sums = [&](float (&rp)[4], float (&cp)[4], int kb) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) rp[i] += __shfl_xor_sync(0xffffffffu, rp[i], o);
+            rs_acc[i] += rp[i];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 16);
+            if ((tid & 31) < 16) atomicAdd(csum + (size_t)bh * Lp + (size_t)kb * kC + n0 + j, cp[j]);
+        }
+    };
     load_rows<T>(R1, nullptr, dout + hL * kD, t0, L);
     load_rows<T>(nullptr, R4, vh, t0, L);
     __syncthreads();
@@ -192,7 +217,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         mm_rowa(R1, R4, m0, n0, dpm);  // dout_i . v_j
         const float *tab = dg + ((size_t)bh * nblk + a) * kBlkTile;
         float *dtd = dTd + ((size_t)bh * nblk + a) * kBlkTile;
-        float pr[4][4];
+        float pr[4][4], rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = m0 + i;
@@ -203,10 +228,16 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
             for (int j = 0; j < 4; ++j) {
                 const float p = (t0 + r < L) ? exp2f(sv[j] - lse2[r]) : 0.f;
                 pr[i][j] = p;
-                dt[j] = scale * p * (dpm[i][j] - Drow[r]);
+                const float ds = p * (dpm[i][j] - Drow[r]);
+                if (FOX) {
+                    rp[i] += ds;
+                    cp[j] += ds;
+                }
+                dt[j] = scale * ds;
             }
             *reinterpret_cast<float4 *>(dtd + r * kC + n0) = make_float4(dt[0], dt[1], dt[2], dt[3]);
         }
+        if (FOX) fox_sums(rp, cp, a);
         put_acc(R2, pr, m0, n0, true);  // p^T
     }
     __syncthreads();
@@ -232,6 +263,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         load_tile(R2, kp_block(b), true);
         load_tile(R3, kp_block(b) + kBlkTile, true);
         load_rows<T>(nullptr, R4, vh, b * kC, L);
+        if (FOX && tid < kC) locj[tid] = loc[(size_t)bh * Lp + (size_t)b * kC + tid];
         __syncthreads();
         float s[4][4], xn[4][4];
         zero4(s);
@@ -241,20 +273,30 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         mm_rowa(R1, R4, m0, n0, dpm);
         if (b > 0) mm_rowa(R0, R3, m0, n0, xn);
         float *st = stash + (pair0 + b) * 2 * kBlkTile;  // [X_{a,b} | dT_ab], row-major
+        float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
+        const float dcb = FOX ? (float)(cb[(size_t)bh * nblk + a] - cb[(size_t)bh * nblk + b]) : 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = m0 + i;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float p = (t0 + r < L) ? exp2f(s[i][j] * scale_log2 - lse2[r]) : 0.f;
-                s[i][j] = p;                                      // s now holds p
-                dpm[i][j] = scale * p * (dpm[i][j] - Drow[r]);   // dpm now holds dT
+                float x2 = s[i][j] * scale_log2;
+                if (FOX) x2 += kLog2e * ((dcb + loci[r]) - locj[n0 + j]);
+                const float p = (t0 + r < L) ? exp2f(x2 - lse2[r]) : 0.f;
+                const float ds = p * (dpm[i][j] - Drow[r]);
+                if (FOX) {
+                    rp[i] += ds;
+                    cp[j] += ds;
+                }
+                s[i][j] = p;             // s now holds p
+                dpm[i][j] = scale * ds;  // dpm now holds dT
             }
             *reinterpret_cast<float4 *>(st + kBlkTile + r * kC + n0) =
                 make_float4(dpm[i][0], dpm[i][1], dpm[i][2], dpm[i][3]);
             *reinterpret_cast<float4 *>(st + r * kC + n0) =
                 *reinterpret_cast<const float4 *>(R0 + r * LD + n0);
         }
+        if (FOX) fox_sums(rp, cp, b);
         __syncthreads();  // K~_b^T and P_b^T are read: their buffers take p^T and dT^T
         put_acc(R2, s, m0, n0, true);
         put_acc(R3, dpm, m0, n0, true);
@@ -318,6 +360,10 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         *reinterpret_cast<float4 *>(dq + (m0 + i) * kD + n0) = make_float4(g[i][0], g[i][1], g[i][2], g[i][3]);
+    if (FOX && tx == 0)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (t0 + m0 + i < L) rsum[(size_t)bh * Lp + t0 + m0 + i] = rs_acc[i];
 }
 
 // ---------------------------------------------------------------- B2: block pass
@@ -536,13 +582,86 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     if (tid < nvalid) dbeta[hL + t0 + tid] = dBs[tid];
 }
 
+// ---------------------------------------------------------------- PaTH-FoX gate sums
+// Per token the block-local inclusive sums of log f (fp32) and per block the fp64 sum of
+// log f over every earlier token of the head, so that c_i - c_j = (C_a - C_b) + loc_i - loc_j
+// keeps fp32 accuracy at any length. One CTA per head: a warp per 64-token block, then an
+// fp64 exclusive scan of the block totals (a contiguous run of blocks per thread).
+__global__ void __launch_bounds__(kThreads)
+bwd_fox_sums_kernel(const float *__restrict__ log_f, int L, int Lp, int nblk,
+                    float *__restrict__ loc, double *__restrict__ cb) {
+    __shared__ double part[kThreads];
+    const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t hL = (size_t)bh * L;
+    double *cbh = cb + (size_t)bh * nblk;
+    for (int b = warp; b < nblk; b += kThreads / 32) {
+        const int ta = b * kC + 2 * lane, tb = ta + 1;
+        const float x0 = ta < L ? log_f[hL + ta] : 0.f;
+        const float x1 = (tb < L ? log_f[hL + tb] : 0.f) + x0;
+        float run = x1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run += n;
+        }
+        loc[(size_t)bh * Lp + ta] = run - x1 + x0;
+        loc[(size_t)bh * Lp + tb] = run;
+        if (lane == 31) cbh[b] = (double)run;  // the block's total, scanned below
+    }
+    __syncthreads();
+    const int per = (nblk + kThreads - 1) / kThreads;
+    const int b0 = min(nblk, tid * per), b1 = min(nblk, b0 + per);
+    double sum = 0.0;
+    for (int b = b0; b < b1; ++b) sum += cbh[b];
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        double run = 0.0;
+        for (int i = 0; i < kThreads; ++i) {
+            const double t = part[i];
+            part[i] = run;
+            run += t;
+        }
+    }
+    __syncthreads();
+    double run = part[tid];
+    for (int b = b0; b < b1; ++b) {
+        const double t = cbh[b];
+        cbh[b] = run;
+        run += t;
+    }
+}
+
+// d log f_s = sum over pairs j < s <= i of dS_ij = sum_{t >= s} (rowsum_t - colsum_t) of dS,
+// since the bias c_i - c_j moves with c_i on row i and against c_j on column j, and
+// c_t = sum_{u <= t} log f_u. One warp per head walks the tokens from the end in fp64.
+__global__ void __launch_bounds__(32)
+bwd_fox_dlogf_kernel(const float *__restrict__ rsum, const float *__restrict__ csum, int L,
+                     int Lp, float *__restrict__ dlogf) {
+    const int bh = blockIdx.x, lane = threadIdx.x;
+    double acc = 0.0;
+    for (int top = L - 1; top >= 0; top -= 32) {
+        const int t = top - lane;
+        double v = t >= 0 ? (double)rsum[(size_t)bh * Lp + t] - (double)csum[(size_t)bh * Lp + t] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (t >= 0) dlogf[(size_t)bh * L + t] = (float)(acc + v);
+        acc += __shfl_sync(0xffffffffu, v, 31);
+    }
+}
+
 }  // namespace
 
 // Workspace of the backward: 256-byte status header, then fp32 q~ (BH, Lp, 64),
 // [k~; P_b] (BH, nblk, 128, 64), diagonal logits (BH, nblk, 64, 64), dq~ and dk~ (BH, Lp,
 // 64), dP_b and the diagonal dT (BH, nblk, 64, 64), and the query pass's stash: X_{a,b} and
-// dT_ab for every pair b < a (BH, nblk (nblk - 1) / 2, 2, 64, 64).
-BwdLayout bwd_layout(int B, int H, int L) {
+// dT_ab for every pair b < a (BH, nblk (nblk - 1) / 2, 2, 64, 64); PaTH-FoX adds the
+// block-local gate sums, the row and column sums of dS (BH, Lp) fp32 each, and the per-block
+// gate prefixes (BH, nblk) fp64.
+BwdLayout bwd_layout(int B, int H, int L, bool fox) {
     BwdLayout y;
     y.BH = B * H;
     y.nblk = (L + kC - 1) / kC;
@@ -566,62 +685,84 @@ BwdLayout bwd_layout(int B, int H, int L) {
     off = align256(off + blocks);
     y.off_stash = off;
     off = align256(off + bh * ((size_t)y.nblk * (y.nblk - 1) / 2) * 2 * tile);
+    y.off_loc = y.off_rs = y.off_cs = y.off_cb = off;
+    if (fox) {
+        const size_t tok = bh * y.Lp * 4;
+        y.off_rs = align256(off + tok);
+        y.off_cs = align256(y.off_rs + tok);
+        y.off_cb = align256(y.off_cs + tok);
+        off = align256(y.off_cb + bh * y.nblk * 8);
+    }
     y.total = off;
     return y;
 }
 
-size_t bwd_query_smem() { return (size_t)(6 * BUF + 2 * kC) * sizeof(float); }
+size_t bwd_query_smem() { return (size_t)(6 * BUF + 4 * kC) * sizeof(float); }
 size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC * kNS + 2 * kC) * sizeof(float); }
 
-// dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32. dv gathers by atomics from zero.
+// dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32; with log_f (PaTH-FoX) also dlogf
+// (B*H, L) fp32. dv gathers by atomics from zero.
 template <typename T>
 cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const void *w,
-                            const float *beta, const void *o, const float *lse, const void *dout,
-                            int B, int H, int L, float scale, float *dq, float *dk, float *dv,
-                            float *dw, float *dbeta, void *ws, cudaStream_t stream) {
-    const BwdLayout y = bwd_layout(B, H, L);
+                            const float *beta, const float *log_f, const void *o,
+                            const float *lse, const void *dout, int B, int H, int L, float scale,
+                            float *dq, float *dk, float *dv, float *dw, float *dbeta, float *dlogf,
+                            void *ws, cudaStream_t stream) {
+    const bool fox = log_f != nullptr;
+    const BwdLayout y = bwd_layout(B, H, L, fox);
     char *base = static_cast<char *>(ws);
-    float *qt = reinterpret_cast<float *>(base + y.off_qt);
-    float *kp = reinterpret_cast<float *>(base + y.off_kp);
-    float *dg = reinterpret_cast<float *>(base + y.off_dg);
-    float *dqt = reinterpret_cast<float *>(base + y.off_dqt);
-    float *dkt = reinterpret_cast<float *>(base + y.off_dkt);
-    float *dPb = reinterpret_cast<float *>(base + y.off_dP);
-    float *dTd = reinterpret_cast<float *>(base + y.off_dTd);
-    float *stash = reinterpret_cast<float *>(base + y.off_stash);
+    auto at = [&](size_t off) { return reinterpret_cast<float *>(base + off); };
+    float *qt = at(y.off_qt), *kp = at(y.off_kp), *dg = at(y.off_dg), *dqt = at(y.off_dqt);
+    float *dkt = at(y.off_dkt), *dPb = at(y.off_dP), *dTd = at(y.off_dTd), *stash = at(y.off_stash);
+    float *loc = at(y.off_loc), *rs = at(y.off_rs), *cs = at(y.off_cs);
+    double *cb = reinterpret_cast<double *>(base + y.off_cb);
+    const size_t tok = (size_t)y.BH * y.Lp * 4;
     cudaError_t e;
     if ((e = cudaMemsetAsync(base, 0, 4, stream)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(dkt, 0, (size_t)y.BH * y.Lp * kD * 4, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dkt, 0, tok * kD, stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dPb, 0, (size_t)y.BH * y.nblk * kBlkTile * 4, stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(dv, 0, (size_t)y.BH * L * kD * 4, stream)) != cudaSuccess) return e;
-    if ((e = launch_ut_prepare_f32out<T>(q, k, w, beta, y.BH, L, y.Lp, y.nblk, scale, qt, kp, dg,
-                                         reinterpret_cast<uint32_t *>(base), stream)) != cudaSuccess)
+    if (fox) {
+        if ((e = cudaMemsetAsync(rs, 0, tok, stream)) != cudaSuccess ||
+            (e = cudaMemsetAsync(cs, 0, tok, stream)) != cudaSuccess)
+            return e;
+        bwd_fox_sums_kernel<<<y.BH, kThreads, 0, stream>>>(log_f, L, y.Lp, y.nblk, loc, cb);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if ((e = launch_ut_prepare_f32out<T>(q, k, w, beta, log_f, y.BH, L, y.Lp, y.nblk, scale, qt,
+                                         kp, dg, reinterpret_cast<uint32_t *>(base), stream)) != cudaSuccess)
         return e;
+    auto kq = fox ? bwd_query_kernel<T, true> : bwd_query_kernel<T, false>;
     const size_t s1 = bwd_query_smem(), s2 = bwd_block_smem();
-    if ((e = cudaFuncSetAttribute(bwd_query_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)s1)) != cudaSuccess ||
+    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_block_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)s2)) != cudaSuccess)
         return e;
     const dim3 grid(y.nblk, y.BH);
-    bwd_query_kernel<T><<<grid, kThreads, s1, stream>>>(
+    kq<<<grid, kThreads, s1, stream>>>(
         static_cast<const T *>(v), static_cast<const T *>(o), static_cast<const T *>(dout), lse,
-        qt, kp, dg, dqt, dkt, dPb, dTd, stash, dv, L, y.Lp, y.nblk, scale, scale * kLog2e);
+        qt, kp, dg, dqt, dkt, dPb, dTd, stash, dv, L, y.Lp, y.nblk, scale, scale * kLog2e, loc, cb,
+        rs, cs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_block_kernel<T><<<grid, kThreads, s2, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
         dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, L, y.Lp, y.nblk);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (fox) {
+        bwd_fox_dlogf_kernel<<<y.BH, 32, 0, stream>>>(rs, cs, L, y.Lp, dlogf);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
-template cudaError_t launch_path_bwd<float>(const void *, const void *, const void *, const void *,
-                                            const float *, const void *, const float *,
-                                            const void *, int, int, int, float, float *, float *,
-                                            float *, float *, float *, void *, cudaStream_t);
-template cudaError_t launch_path_bwd<__nv_bfloat16>(const void *, const void *, const void *,
-                                                    const void *, const float *, const void *,
-                                                    const float *, const void *, int, int, int,
-                                                    float, float *, float *, float *, float *,
-                                                    float *, void *, cudaStream_t);
+#define PATH_BWD_INST(T)                                                                        \
+    template cudaError_t launch_path_bwd<T>(const void *, const void *, const void *,           \
+                                            const void *, const float *, const float *,         \
+                                            const void *, const float *, const void *, int, int, \
+                                            int, float, float *, float *, float *, float *,     \
+                                            float *, float *, void *, cudaStream_t);
+PATH_BWD_INST(float)
+PATH_BWD_INST(__nv_bfloat16)
+#undef PATH_BWD_INST
 
 }  // namespace path

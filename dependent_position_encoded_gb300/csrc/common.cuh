@@ -44,9 +44,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Workspace of the backward pass (defined in backward.cu).
 struct BwdLayout {
     int BH, nblk, Lp;
-    size_t off_qt, off_kp, off_dg, off_dqt, off_dkt, off_dP, off_dTd, off_stash, total;
+    size_t off_qt, off_kp, off_dg, off_dqt, off_dkt, off_dP, off_dTd, off_stash;
+    size_t off_loc, off_rs, off_cs, off_cb, total;  // PaTH-FoX only (else all equal to total)
 };
-BwdLayout bwd_layout(int B, int H, int L);
+BwdLayout bwd_layout(int B, int H, int L, bool fox);
 
 inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     FwdLayout lay;

@@ -40,9 +40,10 @@ cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up,
                             uint64_t limit_ns, cudaStream_t stream);
 template <typename T>
 cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const void *w,
-                            const float *beta, const void *o, const float *lse, const void *dout,
-                            int B, int H, int L, float scale, float *dq, float *dk, float *dv,
-                            float *dw, float *dbeta, void *ws, cudaStream_t stream);
+                            const float *beta, const float *log_f, const void *o,
+                            const float *lse, const void *dout, int B, int H, int L, float scale,
+                            float *dq, float *dk, float *dv, float *dw, float *dbeta, float *dlogf,
+                            void *ws, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len, int d);
 template <typename T>
@@ -141,6 +142,36 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
 
 }  // namespace
 
+namespace {
+path_status bwd_impl(const void *q, const void *k, const void *v, const void *w, const float *beta,
+                     const float *log_f, const void *out, const float *lse, const void *d_out,
+                     int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
+                     float *dv, float *dw, float *dbeta, float *dlog_f, bool fox, void *ws,
+                     size_t ws_bytes, void *stream) {
+    path_status st = check_sizes(B, H, L, d, dtype);
+    if (st != PATH_OK) return st;
+    if (!std::isfinite(scale)) return PATH_ERR_ARG;
+    if ((long long)B * H * L == 0) return PATH_OK;
+    const void *in[] = {q, k, v, w, beta, out, lse, d_out, dq, dk, dv, dw, dbeta,
+                        fox ? (const void *)log_f : q, fox ? (const void *)dlog_f : q};
+    for (const void *p : in)
+        if (!p) return PATH_ERR_NULL;
+    for (const void *p : in)
+        if (!aligned(p, 16)) return PATH_ERR_ALIGN;
+    if ((st = check_ws(ws, ws_bytes, bwd_layout(B, H, L, fox).total)) != PATH_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float *lf = fox ? log_f : nullptr;
+    float *dlf = fox ? dlog_f : nullptr;
+    cudaError_t e = dtype == PATH_BF16
+                        ? launch_path_bwd<__nv_bfloat16>(q, k, v, w, beta, lf, out, lse, d_out, B,
+                                                         H, L, scale, dq, dk, dv, dw, dbeta, dlf,
+                                                         ws, s)
+                        : launch_path_bwd<float>(q, k, v, w, beta, lf, out, lse, d_out, B, H, L,
+                                                 scale, dq, dk, dv, dw, dbeta, dlf, ws, s);
+    return from_cuda(e);
+}
+}  // namespace
+
 extern "C" {
 
 size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
@@ -151,9 +182,9 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
             return fwd_layout(B, H, L, elt_bytes(dtype), op == PATH_OP_FOX_FWD).total;
         default: break;
     }
-    if (op == PATH_OP_BWD) {
+    if (op == PATH_OP_BWD || op == PATH_OP_FOX_BWD) {
         if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
-        return bwd_layout(B, H, L).total;
+        return bwd_layout(B, H, L, op == PATH_OP_FOX_BWD).total;
     }
     if (check_decode_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
     switch (op) {
@@ -192,23 +223,17 @@ path_status path_attn_bwd(const void *q, const void *k, const void *v, const voi
                           int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
                           float *dv, float *dw, float *dbeta, void *ws, size_t ws_bytes,
                           void *stream) {
-    path_status st = check_sizes(B, H, L, d, dtype);
-    if (st != PATH_OK) return st;
-    if (!std::isfinite(scale)) return PATH_ERR_ARG;
-    if ((long long)B * H * L == 0) return PATH_OK;
-    const void *in[] = {q, k, v, w, beta, out, lse, d_out, dq, dk, dv, dw, dbeta};
-    for (const void *p : in)
-        if (!p) return PATH_ERR_NULL;
-    for (const void *p : in)
-        if (!aligned(p, 16)) return PATH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, bwd_layout(B, H, L).total)) != PATH_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dtype == PATH_BF16
-                        ? launch_path_bwd<__nv_bfloat16>(q, k, v, w, beta, out, lse, d_out, B, H,
-                                                         L, scale, dq, dk, dv, dw, dbeta, ws, s)
-                        : launch_path_bwd<float>(q, k, v, w, beta, out, lse, d_out, B, H, L,
-                                                 scale, dq, dk, dv, dw, dbeta, ws, s);
-    return from_cuda(e);
+    return bwd_impl(q, k, v, w, beta, nullptr, out, lse, d_out, B, H, L, d, dtype, scale, dq, dk,
+                    dv, dw, dbeta, nullptr, false, ws, ws_bytes, stream);
+}
+
+path_status path_fox_bwd(const void *q, const void *k, const void *v, const void *w,
+                         const float *beta, const float *log_f, const void *out, const float *lse,
+                         const void *d_out, int B, int H, int L, int d, int dtype, float scale,
+                         float *dq, float *dk, float *dv, float *dw, float *dbeta, float *dlog_f,
+                         void *ws, size_t ws_bytes, void *stream) {
+    return bwd_impl(q, k, v, w, beta, log_f, out, lse, d_out, B, H, L, d, dtype, scale, dq, dk,
+                    dv, dw, dbeta, dlog_f, true, ws, ws_bytes, stream);
 }
 
 path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, int H, int L,

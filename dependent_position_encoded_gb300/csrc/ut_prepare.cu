@@ -305,13 +305,14 @@ cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const
     return cudaGetLastError();
 }
 
-// The per-block factors in fp32 at explicit places (plain PaTH, no gate), for the backward:
+// The per-block factors in fp32 at explicit places, for the backward (log_f: PaTH-FoX
+// diagonal logits, else null):
 // qt (BH, Lp, 64), kp (BH, nblk, 128, 64) = [k~ rows; P_b rows] per block, dg (BH, nblk, 64,
 // 64) diagonal-block logits in log2 units (scale included, -inf above the diagonal and past L).
 template <typename T>
 cudaError_t launch_ut_prepare_f32out(const void *q, const void *k, const void *w,
-                                     const float *beta, int BH, int L, int Lp, int nblk,
-                                     float scale, float *qt, float *kp, float *dg,
+                                     const float *beta, const float *log_f, int BH, int L, int Lp,
+                                     int nblk, float scale, float *qt, float *kp, float *dg,
                                      uint32_t *status, cudaStream_t stream) {
     const size_t smem = ut_prepare_smem_bytes();
     cudaError_t err = cudaFuncSetAttribute(ut_prepare_kernel<T, float>,
@@ -320,16 +321,16 @@ cudaError_t launch_ut_prepare_f32out(const void *q, const void *k, const void *w
     dim3 grid(nblk, BH);
     ut_prepare_kernel<T, float><<<grid, kPrepThreads, smem, stream>>>(
         static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
-        nullptr, L, Lp, nblk, scale * kLog2e, qt, kp, dg, status);
+        log_f, L, Lp, nblk, scale * kLog2e, qt, kp, dg, status);
     return cudaGetLastError();
 }
 template cudaError_t launch_ut_prepare_f32out<float>(const void *, const void *, const void *,
-                                                     const float *, int, int, int, int, float,
-                                                     float *, float *, float *, uint32_t *,
-                                                     cudaStream_t);
+                                                     const float *, const float *, int, int, int,
+                                                     int, float, float *, float *, float *,
+                                                     uint32_t *, cudaStream_t);
 template cudaError_t launch_ut_prepare_f32out<__nv_bfloat16>(
-    const void *, const void *, const void *, const float *, int, int, int, int, float, float *,
-    float *, float *, uint32_t *, cudaStream_t);
+    const void *, const void *, const void *, const float *, const float *, int, int, int, int,
+    float, float *, float *, float *, uint32_t *, cudaStream_t);
 
 // PaTH-FoX: log2(e) * inclusive prefix sums of log f per head into the workspace.
 template cudaError_t launch_ut_prepare<float>(const void *, const void *, const void *,

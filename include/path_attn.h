@@ -60,7 +60,8 @@ typedef enum {
     PATH_OP_FOX_FWD = 1,
     PATH_OP_DECODE = 2,
     PATH_OP_FOX_DECODE = 3,
-    PATH_OP_BWD = 4
+    PATH_OP_BWD = 4,
+    PATH_OP_FOX_BWD = 5
 } path_op;
 
 /* Largest sizes accepted: B*H <= PATH_MAX_HEADS, L <= PATH_MAX_LEN. */
@@ -143,6 +144,22 @@ path_status path_attn_bwd(const void *q, const void *k, const void *v, const voi
                           int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
                           float *dv, float *dw, float *dbeta, void *ws, size_t ws_bytes,
                           void *stream);
+
+/*
+ * PaTH-FoX backward: as path_attn_bwd for the forward of path_fox_fwd, plus the gradient of
+ * the per-token log forget gate:
+ *   log_f  : (B, H, L) fp32, the forward's gate        dlog_f : (B, H, L) fp32 output,
+ *            d log f_s = sum over pairs j < s <= i of dS_ij (the bias sum_{s=j+1..i} log f_s
+ *            enters logit (i, j) once for every s in that range)
+ *   out, lse : the outputs of path_fox_fwd on the same inputs
+ *   ws     : ws_bytes >= path_workspace_bytes(PATH_OP_FOX_BWD, B, H, L, d, dtype)
+ * Every key block is visited (no early exit): blocks whose weights vanish contribute dS = 0.
+ */
+path_status path_fox_bwd(const void *q, const void *k, const void *v, const void *w,
+                         const float *beta, const float *log_f, const void *out, const float *lse,
+                         const void *d_out, int B, int H, int L, int d, int dtype, float scale,
+                         float *dq, float *dk, float *dv, float *dw, float *dbeta, float *dlog_f,
+                         void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Second stage of the forward: the right-to-left scan over key blocks with

@@ -245,3 +245,35 @@ def test_bwd_rejects_bad_arguments_before_launch(so, kw, code):
 
 def test_bwd_empty_problem_launches_nothing(so):
     assert _bwd(so, L=0, q=None, ws=None) == 0
+
+
+def test_fox_bwd_workspace_size(lib):
+    # the plain backward's workspace plus block-local gate sums, row and column sums of dS
+    # (Lp fp32 each) and per-block fp64 gate prefixes, each region rounded up to 256 B
+    L, nb = 130, 3
+    plain = lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, lib.F32)
+    tok = nb * 64 * 4
+    want = plain + 3 * tok + (nb * 8 + 255) // 256 * 256
+    assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 64, lib.BF16) == want
+    assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 96, lib.BF16) == 0
+
+
+def _fox_bwd(so, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, w=FAKE, beta=FAKE, log_f=FAKE, out=FAKE, lse=FAKE,
+             d_out=FAKE, B=1, H=1, L=128, d=64, dtype=1, scale=0.125, dq=FAKE, dk=FAKE, dv=FAKE,
+             dw=FAKE, dbeta=FAKE, dlog_f=FAKE, ws=FAKE, ws_bytes=8, stream=None)
+    a.update(kw)
+    return so.path_fox_bwd(a["q"], a["k"], a["v"], a["w"], a["beta"], a["log_f"], a["out"],
+                           a["lse"], a["d_out"], a["B"], a["H"], a["L"], a["d"], a["dtype"],
+                           ctypes.c_float(a["scale"]), a["dq"], a["dk"], a["dv"], a["dw"],
+                           a["dbeta"], a["dlog_f"], a["ws"], ctypes.c_size_t(a["ws_bytes"]),
+                           a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(log_f=None), 1), (dict(dlog_f=None), 1), (dict(q=None), 1), (dict(d=32), 2),
+    (dict(dtype=5), 3), (dict(log_f=FAKE + 4), 4), (dict(dlog_f=FAKE + 8), 4),
+    (dict(scale=float("inf")), 9), (dict(), 5),
+])
+def test_fox_bwd_rejects_bad_arguments_before_launch(so, kw, code):
+    assert _fox_bwd(so, **kw) == code

@@ -39,8 +39,9 @@ def _case(lib, B, H, L, dtype, seed, beta_zero=False, wl=None):
 def _compare(grads, ref, tol, heads=None):
     # a gradient that is exactly zero (one token: the softmax weight is 1, so dS = 0) is
     # measured against 1% of the largest reference gradient instead of against itself
-    floor = 1e-2 * max(np.abs(ref[n]).max() for n in NAMES)
-    for n in NAMES:
+    names = NAMES + (("dlog_f",) if "dlog_f" in ref else ())
+    floor = 1e-2 * max(np.abs(ref[n]).max() for n in names)
+    for n in names:
         got = grads[n].double().cpu().numpy()
         if heads is not None:
             got = got.reshape(-1, *got.shape[2:])[heads]
@@ -82,4 +83,58 @@ def test_bwd_workload_sampled_heads(lib):
     sel = {k: x[k].reshape(-1, *x[k].shape[2:])[heads] for k in ("q", "k", "v", "w", "beta")}
     ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
                           d_out.reshape(-1, wl.L, 64)[heads])
+    _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
+
+
+def _fox_case(lib, B, H, L, dtype, seed, gate_scale=1.0, wl=None):
+    if wl is None:
+        x = pi.make_fwd_inputs(B, H, L, seed=seed, dtype=dtype, fox=True, device="cuda")
+    else:
+        x = pi.make_fwd_inputs(wl.B, wl.H, wl.L, seed=seed, dtype=wl.dtype, clip=wl.clip,
+                               fox=True, device="cuda")
+    x["log_f"] = (x["log_f"] * gate_scale).contiguous()
+    g = torch.Generator(device="cpu").manual_seed(seed + 1)
+    d_out = torch.randn((B, H, L, 64), generator=g).to(dtype).cuda()
+    out, lse = lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    grads = lib.path_fox_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], out, lse,
+                             d_out)
+    torch.cuda.synchronize()
+    return x, d_out, grads
+
+
+@pytest.mark.parametrize("B,H,L,dtype,gate_scale", [
+    (1, 2, 200, torch.float32, 1.0),   # workload gate, ragged
+    (2, 2, 130, torch.bfloat16, 1.0),  # bf16
+    (1, 1, 64, torch.float32, 1.0),    # one block: the diagonal table carries the gate
+    (1, 1, 384, torch.float32, 20.0),  # strong gate: the forward's early exit skips blocks
+    (1, 2, 320, torch.bfloat16, 5.0),  # bf16, moderate gate
+])
+def test_fox_bwd_matches_oracle(lib, B, H, L, dtype, gate_scale):
+    x, d_out, grads = _fox_case(lib, B, H, L, dtype, seed=7 * L + B, gate_scale=gate_scale)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, log_f=x["log_f"])
+    _compare(grads, ref, TOL[dtype])
+
+
+def test_fox_bwd_zero_gate_equals_plain_backward(lib):
+    # log f = 0: the forward is plain PaTH, so dq .. dbeta equal the plain backward's within
+    # fp32 rounding, while d log f still carries the gradient of the gate
+    x, d_out, grads = _fox_case(lib, 1, 2, 256, torch.float32, seed=11, gate_scale=0.0)
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    plain = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out)
+    for n in NAMES:
+        a, b = grads[n].double(), plain[n].double()
+        assert (a - b).abs().max().item() <= 1e-5 * max(b.abs().max().item(), 1.0), n
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, log_f=x["log_f"])
+    _compare(grads, ref, 1e-4)
+
+
+def test_fox_bwd_workload_sampled_heads(lib):
+    # the B4 H16 L2048 bf16 workload with the PaTH-FoX gate: the oracle on two heads
+    wl = pi.BF16_L2048
+    x, d_out, grads = _fox_case(lib, wl.B, wl.H, wl.L, wl.dtype, seed=wl.seed, wl=wl)
+    heads = [3, wl.B * wl.H - 2]
+    sel = {k: x[k].reshape(-1, *x[k].shape[2:])[heads]
+           for k in ("q", "k", "v", "w", "beta", "log_f")}
+    ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          d_out.reshape(-1, wl.L, 64)[heads], log_f=sel["log_f"])
     _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
