@@ -355,23 +355,32 @@ def bwd_flops(B, H, L):
     return B * H * t * (5 * pairs + 3 * (pairs - (nb - 1)) + 2 * nb)
 
 
-def time_bwd(pa, wl, steps=5, warmup=3):
-    """Times path_attn_bwd on the workload (forward outputs and d_out resident)."""
+def time_bwd(pa, wl, steps=5, warmup=3, fox=False):
+    """Times path_attn_bwd (path_fox_bwd with fox) on the workload (forward outputs and
+    d_out resident)."""
     dev = torch.device("cuda")
-    x = pi.workload_inputs(wl, device=dev)
+    x = pi.make_fwd_inputs(wl.B, wl.H, wl.L, wl.d, wl.dtype, wl.seed, wl.clip, fox, dev)
     g = torch.Generator(device=dev).manual_seed(wl.seed + 1)
     d_out = torch.randn((wl.B, wl.H, wl.L, 64), generator=g, device=dev).to(wl.dtype)
-    out, lse = pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
-    ws = pa.new_workspace(pa.OP_BWD, wl.B, wl.H, wl.L, pa.BF16 if wl.dtype == torch.bfloat16
-                          else pa.F32, dev)
+    if fox:
+        out, lse = pa.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    else:
+        out, lse = pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    ws = pa.new_workspace(pa.OP_FOX_BWD if fox else pa.OP_BWD, wl.B, wl.H, wl.L,
+                          pa.BF16 if wl.dtype == torch.bfloat16 else pa.F32, dev)
     grads = {n: torch.empty((wl.B, wl.H, wl.L, 64), dtype=torch.float32, device=dev)
              for n in ("dq", "dk", "dv", "dw")}
     grads["dbeta"] = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device=dev)
+    grads["dlog_f"] = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def one():
-        pa.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out,
-                         grads=grads, workspace=ws)
+        if fox:
+            pa.path_fox_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], out, lse,
+                            d_out, grads=grads, workspace=ws)
+        else:
+            pa.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out,
+                             grads=grads, workspace=ws)
 
     for _ in range(warmup):
         one()
@@ -384,11 +393,12 @@ def time_bwd(pa, wl, steps=5, warmup=3):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     fl = bwd_flops(wl.B, wl.H, wl.L)
-    return {"workload": wl.name.replace("fwd", "bwd"), "ms_per_step": ms,
+    name = wl.name.replace("path_fwd", "path_fox_bwd" if fox else "path_bwd")
+    return {"workload": name, "ms_per_step": ms,
             "tokens_per_s": wl.B * wl.L / (ms * 1e-3), "query_pass_flops": fl,
             "workspace_bytes": ws.numel(),
-            # fp32 UT recompute, query pass, block pass (plus three memsets)
-            "launches_per_step": 3}
+            # fp32 UT recompute, query pass, block pass; FoX adds the gate sums and d log f
+            "launches_per_step": 5 if fox else 3}
 
 
 def cpu_baseline(x_cpu, wl, target_s=12.0):
@@ -682,6 +692,10 @@ def main():
                            "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "traffic": None,
                            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
         line["bwd"] = bwd
+        fbwd = time_bwd(pa, pi.BF16_L2048, fox=True)
+        ach = fbwd["query_pass_flops"] / (fbwd["ms_per_step"] * 1e-3) / 1e12
+        fbwd["roofline"] = dict(bwd["roofline"], achieved=ach, frac=ach / FP32_ALU_TFLOPS)
+        line["fox_bwd"] = fbwd
 
     if args.sweep and rank == 0:
         sweep = {}
