@@ -43,13 +43,6 @@ constexpr int BUF = kC * LD;
 constexpr int kThreads = 256;
 constexpr int kBlkTile = kC * kD;  // floats in one 64 x 64 tile
 
-__device__ __forceinline__ void zero4(float (&a)[4][4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
-}
-
 // 64 x 64 fp32 tile from global (row-major, 64 floats per row) into shared memory, as is
 // (dst[r][c]) or transposed (dst[c][r]). Each thread issues all four of its 16-byte loads
 // before the first store, so the tile costs one memory latency.
@@ -99,42 +92,74 @@ __device__ __forceinline__ void load_rows(float *dst, float *dst_t, const T *__r
 }
 
 // ---------------------------------------------------------------- B1: query pass
-// acc[i][j] += sum_k A[m0 + i][k] * B[k][n0 + j]: A row-major (the lanes of a quarter warp
-// share m0, so its loads are broadcasts), B k-major. Four k at a time: 8 16-byte loads per
-// 64 FMAs, as with both operands k-major, so no operand needs a second, transposed copy.
-__device__ __forceinline__ void mm_rowa(const float *__restrict__ A, const float *__restrict__ B,
-                                        int m0, int n0, float (&acc)[4][4]) {
+// Four groups of 64 threads; a group computes half (32 rows) of a 64 x 64 x 64 product as
+// 4 x 8 register tiles. Thread (ty, tx) of a group holds rows rb + ty + 8i (i < 4; rows
+// interleaved so that the four row addresses of a warp fall in distinct banks) and columns
+// 4tx .. 4tx + 3 and 32 + 4tx .. 32 + 4tx + 3 (the eight lanes of a quarter warp read one
+// contiguous 128-byte piece of B). 12 16-byte shared loads per 128 FMAs.
+__device__ __forceinline__ int col48(int c0, int j) { return c0 + (j < 4 ? j : 28 + j); }
+
+// acc[i][j] += sum_k A[r0 + 8i][k] * B[k][col48(c0, j)]: A row-major, B k-major
+__device__ __forceinline__ void mm48(const float *__restrict__ A, const float *__restrict__ B,
+                                     int r0, int c0, float (&acc)[4][8]) {
 #pragma unroll 2
     for (int k = 0; k < kC; k += 4) {
         float4 a[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (m0 + i) * LD + k);
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 8 * i) * LD + k);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const float4 b = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + n0);
-            const float bv[4] = {b.x, b.y, b.z, b.w};
+            const float4 b0 = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + c0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + c0 + 32);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
             }
         }
     }
 }
 
-// A 4 x 4 register tile (rows m0.., columns n0..) into shared memory as is or transposed.
-__device__ __forceinline__ void put_acc(float *dst, const float (&v)[4][4], int m0, int n0,
-                                        bool transpose) {
+__device__ __forceinline__ void zero48(float (&a)[4][8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[i][j] = 0.f;
+}
+
+// a 4 x 8 tile into shared memory, as is (dst[r][c]) or transposed (dst[c][r])
+__device__ __forceinline__ void put48(float *dst, const float (&v)[4][8], int r0, int c0,
+                                      bool transpose) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+        const int r = r0 + 8 * i;
         if (transpose) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[(n0 + j) * LD + m0 + i] = v[i][j];
+            for (int j = 0; j < 8; ++j) dst[col48(c0, j) * LD + r] = v[i][j];
         } else {
-            *reinterpret_cast<float4 *>(dst + (m0 + i) * LD + n0) =
-                make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+            *reinterpret_cast<float4 *>(dst + r * LD + c0) = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+            *reinterpret_cast<float4 *>(dst + r * LD + c0 + 32) = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
         }
+    }
+}
+
+// a 4 x 8 tile added into a row-major (64 floats per row) global tile
+__device__ __forceinline__ void red48(float *dst, const float (&v)[4][8], int r0, int c0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) atomicAdd(dst + (r0 + 8 * i) * kC + col48(c0, j), v[i][j]);
+}
+
+// a 4 x 8 tile stored into a row-major global tile
+__device__ __forceinline__ void st48(float *dst, const float (&v)[4][8], int r0, int c0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + 8 * i;
+        *reinterpret_cast<float4 *>(dst + r * kC + c0) = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+        *reinterpret_cast<float4 *>(dst + r * kC + c0 + 32) = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
     }
 }
 
@@ -143,6 +168,9 @@ __device__ __forceinline__ void put_acc(float *dst, const float (&v)[4][4], int 
 //   pass 1: R0 X [i][c], R1 dout [i][c], R2 K~_b^T then p^T [j][i], R3 P_b^T then dT^T [j][i],
 //           R4 V_b^T [c][j]
 //   pass 2: R0 X, R1 dT [i][j], R2 K~_b [j][c], R3 P_b [n][c], R4 G [i][n], R5 G^T [n][i]
+// Groups 0 and 1 form the logits and dout V_b^T of their rows (so p and dS stay in their
+// registers) and, in pass 2, the new G; groups 2 and 3 carry X to the next key block and,
+// in pass 2, add the dP_b terms; in between each group takes half of dk~ or dv.
 // PaTH-FoX (FOX): the gate bias c_i - c_j joins every logit, as (C_a - C_b) + loc_i - loc_j
 // with C the fp64 sums of log f before each block and loc the block-local inclusive sums;
 // the row sums of dS go to rsum and its column sums to csum (atomically), from which the
@@ -164,10 +192,12 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     float *loci = Drow + kC;    // FoX: block-local gate sums of the query rows
     float *locj = loci + kC;    // FoX: those of the current key block
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int a = nblk - 1 - (int)blockIdx.x;
     const int bh = blockIdx.y;
-    const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
+    const int grp = tid >> 6, lt = tid & 63, ty = lt >> 3, tx = lt & 7;
+    const int r0 = (grp & 1) * 32 + ty, c0 = 4 * tx;  // rows r0 + 8i, columns col48(c0, j)
+    const bool lead = grp < 2;                        // groups 0 and 1: logits, p, dS, G
     const int t0 = a * kC;
     const size_t hL = (size_t)bh * L;
     const T *vh = v + hL * kD;
@@ -190,67 +220,65 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
             if (FOX) loci[row] = (t0 + row < L) ? loc[(size_t)bh * Lp + t0 + row] : 0.f;
         }
     }
-    // FoX: row sums of dS stay in registers (every lane of a row's 16 ends with the total);
+    // FoX: row sums of dS stay in registers (the eight lanes of a row end with its total);
     // column sums of a tile go out with one atomic per column and warp
     float rs_acc[4] = {0.f, 0.f, 0.f, 0.f};
-    auto fox_sums = [&](float (&rp)[4], float (&cp)[4], int kb) {
+    auto fox_sums = [&](float (&rp)[4], float (&cp)[8], int kb) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) rp[i] += __shfl_xor_sync(0xffffffffu, rp[i], o);
+            for (int o = 1; o < 8; o <<= 1) rp[i] += __shfl_xor_sync(0xffffffffu, rp[i], o);
             rs_acc[i] += rp[i];
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
+            cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 8);
             cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 16);
-            if ((tid & 31) < 16) atomicAdd(csum + (size_t)bh * Lp + (size_t)kb * kC + n0 + j, cp[j]);
+            if (lane < 8) atomicAdd(csum + (size_t)bh * Lp + (size_t)kb * kC + col48(c0, j), cp[j]);
         }
     };
+
     load_rows<T>(R1, nullptr, dout + hL * kD, t0, L);
     load_rows<T>(nullptr, R4, vh, t0, L);
     __syncthreads();
 
-    float dpm[4][4];
     // ---- diagonal block: logits from the table; dT to the block pass, p^T dout to dv
-    {
-        zero4(dpm);
-        mm_rowa(R1, R4, m0, n0, dpm);  // dout_i . v_j
+    if (lead) {
+        float dt[4][8], pr[4][8], rp[4] = {0.f, 0.f, 0.f, 0.f};
+        float cp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        zero48(dt);
+        mm48(R1, R4, r0, c0, dt);  // dout_i . v_j
         const float *tab = dg + ((size_t)bh * nblk + a) * kBlkTile;
-        float *dtd = dTd + ((size_t)bh * nblk + a) * kBlkTile;
-        float pr[4][4], rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = m0 + i;
-            const float4 s4 = *reinterpret_cast<const float4 *>(tab + r * kC + n0);
-            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-            float dt[4];
+            const int r = r0 + 8 * i;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float p = (t0 + r < L) ? exp2f(sv[j] - lse2[r]) : 0.f;
-                pr[i][j] = p;
-                const float ds = p * (dpm[i][j] - Drow[r]);
+            for (int j = 0; j < 8; ++j) {
+                const float p = (t0 + r < L) ? exp2f(tab[r * kC + col48(c0, j)] - lse2[r]) : 0.f;
+                const float ds = p * (dt[i][j] - Drow[r]);
                 if (FOX) {
                     rp[i] += ds;
                     cp[j] += ds;
                 }
-                dt[j] = scale * ds;
+                pr[i][j] = p;
+                dt[i][j] = scale * ds;
             }
-            *reinterpret_cast<float4 *>(dtd + r * kC + n0) = make_float4(dt[0], dt[1], dt[2], dt[3]);
         }
+        st48(dTd + ((size_t)bh * nblk + a) * kBlkTile, dt, r0, c0);
         if (FOX) fox_sums(rp, cp, a);
-        put_acc(R2, pr, m0, n0, true);  // p^T
+        put48(R2, pr, r0, c0, true);  // p^T
     }
     __syncthreads();
-    {
-        float acc[4][4];
-        zero4(acc);
-        mm_rowa(R2, R1, m0, n0, acc);  // sum_i p_ij dout_i[c]
+    if (!lead) {
+        float acc[4][8];
+        zero48(acc);
+        mm48(R2, R1, r0, c0, acc);  // sum_i p_ij dout_i[c]
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (t0 + m0 + j < L)
+        for (int i = 0; i < 4; ++i)
+            if (t0 + r0 + 8 * i < L)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    atomicAdd(dv + (hL + t0 + m0 + j) * kD + n0 + c, acc[j][c]);
+                for (int j = 0; j < 8; ++j)
+                    atomicAdd(dv + (hL + t0 + r0 + 8 * i) * kD + col48(c0, j), acc[i][j]);
     }
 
     // ---- pass 1: right to left over key blocks, X from Q~_a
@@ -265,66 +293,69 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         load_rows<T>(nullptr, R4, vh, b * kC, L);
         if (FOX && tid < kC) locj[tid] = loc[(size_t)bh * Lp + (size_t)b * kC + tid];
         __syncthreads();
-        float s[4][4], xn[4][4];
-        zero4(s);
-        zero4(dpm);
-        zero4(xn);
-        mm_rowa(R0, R2, m0, n0, s);
-        mm_rowa(R1, R4, m0, n0, dpm);
-        if (b > 0) mm_rowa(R0, R3, m0, n0, xn);
-        float *st = stash + (pair0 + b) * 2 * kBlkTile;  // [X_{a,b} | dT_ab], row-major
-        float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
-        const float dcb = FOX ? (float)(cb[(size_t)bh * nblk + a] - cb[(size_t)bh * nblk + b]) : 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = m0 + i;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float x2 = s[i][j] * scale_log2;
-                if (FOX) x2 += kLog2e * ((dcb + loci[r]) - locj[n0 + j]);
-                const float p = (t0 + r < L) ? exp2f(x2 - lse2[r]) : 0.f;
-                const float ds = p * (dpm[i][j] - Drow[r]);
-                if (FOX) {
-                    rp[i] += ds;
-                    cp[j] += ds;
-                }
-                s[i][j] = p;             // s now holds p
-                dpm[i][j] = scale * ds;  // dpm now holds dT
-            }
-            *reinterpret_cast<float4 *>(st + kBlkTile + r * kC + n0) =
-                make_float4(dpm[i][0], dpm[i][1], dpm[i][2], dpm[i][3]);
-            *reinterpret_cast<float4 *>(st + r * kC + n0) =
-                *reinterpret_cast<const float4 *>(R0 + r * LD + n0);
+        // lead groups: acc1 = logits, acc2 = dout V_b^T; the others: acc1 = X P_b^T
+        float acc1[4][8], acc2[4][8];
+        zero48(acc1);
+        zero48(acc2);
+        if (lead) {
+            mm48(R0, R2, r0, c0, acc1);
+            mm48(R1, R4, r0, c0, acc2);
+        } else if (b > 0) {
+            mm48(R0, R3, r0, c0, acc1);
         }
-        if (FOX) fox_sums(rp, cp, b);
+        float *st = stash + (pair0 + b) * 2 * kBlkTile;  // [X_{a,b} | dT_ab], row-major
+#pragma unroll
+        for (int it = 0; it < kBlkTile / 4 / kThreads; ++it) {
+            const int e = 4 * (tid + it * kThreads), r = e / kD, c = e % kD;
+            *reinterpret_cast<float4 *>(st + e) = *reinterpret_cast<const float4 *>(R0 + r * LD + c);
+        }
+        if (lead) {
+            float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float dcb = FOX ? (float)(cb[(size_t)bh * nblk + a] - cb[(size_t)bh * nblk + b]) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = r0 + 8 * i;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float x2 = acc1[i][j] * scale_log2;
+                    if (FOX) x2 += kLog2e * ((dcb + loci[r]) - locj[col48(c0, j)]);
+                    const float p = (t0 + r < L) ? exp2f(x2 - lse2[r]) : 0.f;
+                    const float ds = p * (acc2[i][j] - Drow[r]);
+                    if (FOX) {
+                        rp[i] += ds;
+                        cp[j] += ds;
+                    }
+                    acc1[i][j] = p;           // acc1 now holds p
+                    acc2[i][j] = scale * ds;  // acc2 now holds dT
+                }
+            }
+            st48(st + kBlkTile, acc2, r0, c0);
+            if (FOX) fox_sums(rp, cp, b);
+        }
         __syncthreads();  // K~_b^T and P_b^T are read: their buffers take p^T and dT^T
-        put_acc(R2, s, m0, n0, true);
-        put_acc(R3, dpm, m0, n0, true);
+        if (lead) {
+            put48(R2, acc1, r0, c0, true);
+            put48(R3, acc2, r0, c0, true);
+        }
         __syncthreads();
         {
-            float acc[4][4];
-            zero4(acc);
-            mm_rowa(R3, R0, m0, n0, acc);  // dK~_b[j][c] += sum_i dT_ij X_ic
-            float *dk = dkt + ((size_t)bh * Lp + (size_t)b * kC) * kD;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) atomicAdd(dk + (m0 + j) * kD + n0 + c, acc[j][c]);
-            zero4(acc);
-            mm_rowa(R2, R1, m0, n0, acc);  // dv_j += sum_i p_ij dout_i (key block b < a is full)
-            float *dvb = dv + (hL + (size_t)b * kC) * kD;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) atomicAdd(dvb + (m0 + j) * kD + n0 + c, acc[j][c]);
+            float acc[4][8];
+            zero48(acc);
+            if (lead) {  // dK~_b[j][c] += sum_i dT_ij X_ic
+                mm48(R3, R0, r0, c0, acc);
+                red48(dkt + ((size_t)bh * Lp + (size_t)b * kC) * kD, acc, r0, c0);
+            } else {     // dv_j += sum_i p_ij dout_i (key block b < a is full)
+                mm48(R2, R1, r0, c0, acc);
+                red48(dv + (hL + (size_t)b * kC) * kD, acc, r0, c0);
+            }
         }
         __syncthreads();
-        if (b > 0) put_acc(R0, xn, m0, n0, false);
+        if (!lead && b > 0) put48(R0, acc1, r0, c0, false);
     }
 
     // ---- pass 2: left to right, G = gradient of X_{a,b}
-    float g[4][4];
-    zero4(g);
+    float g[4][8];
+    zero48(g);
     __syncthreads();
     for (int e = tid; e < BUF; e += kThreads) {
         R4[e] = 0.f;
@@ -338,32 +369,30 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         load_tile(R2, kp_block(b), false);
         load_tile(R3, kp_block(b) + kBlkTile, false);
         __syncthreads();
-        if (b > 0) {
-            float acc[4][4];
-            zero4(acc);
-            mm_rowa(R5, R0, m0, n0, acc);  // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c]
-            float *dpb = dP + ((size_t)bh * nblk + b) * kBlkTile;
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) atomicAdd(dpb + (m0 + n) * kC + n0 + c, acc[n][c]);
+        if (lead) {
+            zero48(g);
+            if (b > 0) mm48(R4, R3, r0, c0, g);  // G_{b-1} P_b
+            mm48(R1, R2, r0, c0, g);             // + dT_ab K~_b
+        } else if (b > 0) {                      // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c]
+            float acc[4][8];
+            zero48(acc);
+            mm48(R5, R0, r0, c0, acc);
+            red48(dP + ((size_t)bh * nblk + b) * kBlkTile, acc, r0, c0);
         }
-        zero4(g);
-        if (b > 0) mm_rowa(R4, R3, m0, n0, g);  // G_{b-1} P_b
-        mm_rowa(R1, R2, m0, n0, g);             // + dT_ab K~_b
         __syncthreads();
-        put_acc(R4, g, m0, n0, false);
-        put_acc(R5, g, m0, n0, true);
+        if (lead) {
+            put48(R4, g, r0, c0, false);
+            put48(R5, g, r0, c0, true);
+        }
     }
-    // dQ~_a = G_{a-1} (zero for the first block)
-    float *dq = dqt + ((size_t)bh * Lp + t0) * kD;
+    if (lead) {
+        // dQ~_a = G_{a-1} (zero for the first block)
+        st48(dqt + ((size_t)bh * Lp + t0) * kD, g, r0, c0);
+        if (FOX && tx == 0)
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4 *>(dq + (m0 + i) * kD + n0) = make_float4(g[i][0], g[i][1], g[i][2], g[i][3]);
-    if (FOX && tx == 0)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (t0 + m0 + i < L) rsum[(size_t)bh * Lp + t0 + m0 + i] = rs_acc[i];
+            for (int i = 0; i < 4; ++i)
+                if (t0 + r0 + 8 * i < L) rsum[(size_t)bh * Lp + t0 + r0 + 8 * i] = rs_acc[i];
+    }
 }
 
 // ---------------------------------------------------------------- B2: block pass
