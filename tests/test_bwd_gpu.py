@@ -138,3 +138,43 @@ def test_fox_bwd_workload_sampled_heads(lib):
     ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
                           d_out.reshape(-1, wl.L, 64)[heads], log_f=sel["log_f"])
     _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
+
+
+@pytest.mark.parametrize("kind", ["projection", "reflection", "identity"])
+def test_bwd_degenerate_transitions(lib, kind):
+    # beta = 1: every H_s is a projection (singular; the block pass undoes its steps from
+    # the recorded w . x and never inverts H_s); beta = 2: exact reflections; w = 0: H = I
+    x = pi.make_fwd_inputs(1, 2, 200, seed=31, dtype=torch.float32, clip=0.0, device="cuda")
+    if kind == "projection":
+        x["beta"] = torch.ones_like(x["beta"])
+    elif kind == "reflection":
+        x["beta"] = torch.full_like(x["beta"], 2.0)
+    else:
+        x["w"] = torch.zeros_like(x["w"])
+    g = torch.Generator(device="cpu").manual_seed(32)
+    d_out = torch.randn((1, 2, 200, 64), generator=g).cuda()
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out)
+    torch.cuda.synchronize()
+    if kind == "identity":
+        assert torch.count_nonzero(grads["dw"]) == 0 and torch.count_nonzero(grads["dbeta"]) == 0
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, 1e-4)
+
+
+def test_bwd_long_head_fp32(lib):
+    # one fp32 head of 4096 tokens: 64 blocks, 2016 carried pairs, the fp32 bar throughout
+    x, d_out, grads = _case(lib, 1, 1, 4096, torch.float32, seed=41)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, 1e-4)
+
+
+def test_bwd_max_heads(lib):
+    # B * H at the 65535 limit (the grid's second dimension), two blocks per head
+    B, L = 65535, 65
+    x, d_out, grads = _case(lib, B, 1, L, torch.bfloat16, seed=43)
+    heads = [0, 1, 32767, B - 1]
+    sel = {k: x[k].reshape(-1, *x[k].shape[2:])[heads] for k in ("q", "k", "v", "w", "beta")}
+    ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          d_out.reshape(-1, L, 64)[heads])
+    _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
