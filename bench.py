@@ -175,9 +175,9 @@ class ClockSampler:
 
 def time_forward(pa, x, steps, warmup, fox=False):
     """Times `steps` forwards (prepare + scan); returns (total_ms, scan_ms_list, prep_ms_list)."""
-    B, H, L, _ = x["q"].shape
+    B, H, L, d = x["q"].shape
     op = pa.OP_FOX_FWD if fox else pa.OP_FWD
-    ws = pa.new_workspace(op, B, H, L, pa.BF16, x["q"].device)
+    ws = pa.new_workspace(op, B, H, L, pa.BF16, x["q"].device, d=d)
     out = torch.empty_like(x["q"])
     lse = torch.empty((B, H, L), dtype=torch.float32, device=x["q"].device)
     log_f = x.get("log_f") if fox else None
@@ -692,6 +692,22 @@ def main():
                            "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "traffic": None,
                            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
         line["bwd"] = bwd
+        # head size 128 (fp32 CUDA-core kernels): the bf16 check workload's width in 8 heads
+        xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, device=dev)
+        d_tot, d_scan, d_prep = time_forward(pa, xd, 3, 3)
+        d_ms = d_tot / 3
+        fa, fc, fp = fwd_flops(4, 8, 2048, d=128)
+        d_ach = (fa + fc + fp) / (d_ms * 1e-3) / 1e12
+        line["fwd_d128"] = {"workload": "path_fwd_bf16_B4H8L2048_d128", "ms_per_step": d_ms,
+                            "tokens_per_s": 4 * 2048 / (d_ms * 1e-3),
+                            "scan_ms": statistics.mean(d_scan), "prepare_ms": statistics.mean(d_prep),
+                            "roofline": {"kernels": "prep_d128_kernel + scan_d128_kernel",
+                                         "bound": "alu", "achieved": d_ach,
+                                         "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                                         "frac": d_ach / FP32_ALU_TFLOPS, "traffic": None,
+                                         "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
+        del xd
+        torch.cuda.empty_cache()
         fbwd = time_bwd(pa, pi.BF16_L2048, fox=True)
         ach = fbwd["query_pass_flops"] / (fbwd["ms_per_step"] * 1e-3) / 1e12
         fbwd["roofline"] = dict(bwd["roofline"], achieved=ach, frac=ach / FP32_ALU_TFLOPS)

@@ -200,7 +200,7 @@ def path_attn_fwd(q, k, v, w, beta, out=None, lse=True, scale=None, workspace=No
     B, H, L, d, dt = _fwd_args(q, k, v, w, beta)
     out, lse = _outputs(q, out, lse, B, H, L)
     if workspace is None:
-        workspace = new_workspace(OP_FWD, B, H, L, dt, q.device)
+        workspace = new_workspace(OP_FWD, B, H, L, dt, q.device, d=d)
     _check(_load().path_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(out),
                                  _ptr(lse), B, H, L, d, dt, _scale(scale, d), _ptr(workspace),
                                  workspace.numel(), _stream(stream, q.device)), "path_attn_fwd")

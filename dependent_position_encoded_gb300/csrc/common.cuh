@@ -41,6 +41,13 @@ struct FwdLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Workspace of the d = 128 forward (defined in fwd_d128.cu).
+struct D128Layout {
+    int BH, nblk, Lp;
+    size_t off_qt, off_kp, off_dg, total;
+};
+D128Layout d128_layout(int B, int H, int L);
+
 // Workspace of the backward pass (defined in backward.cu).
 struct BwdLayout {
     int BH, nblk, Lp;

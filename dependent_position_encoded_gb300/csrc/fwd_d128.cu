@@ -1,0 +1,442 @@
+// PaTH forward at head size d = 128, fp32 on the CUDA cores (both input dtypes; the output
+// keeps the input dtype). The same algorithm as the d = 64 kernels (technical summary
+// "技術要約: PaTH Attention" §3 "UT変換による表現" and the block-wise algorithm; review
+// "거리에서 경로로, PaTH Attention" §9, which flags larger heads as costlier): per block of
+// C = 64 tokens the UT factor A = (I + D N)^{-1} D with N = strictly-upper(W W^T), the
+// boundary-adjusted q~ and k~, the dense block transition P_b = I - W^T A W (here 128 x 128)
+// and the diagonal-block logits; then per 64-row query block a right-to-left scan over key
+// blocks with online softmax, carrying X <- X P_b^T. Contractions over the head dimension
+// run to 128; the triangular solve is unchanged (64 x 64).
+#include "common.cuh"
+
+namespace path {
+
+namespace {
+
+constexpr int kD2 = 128;           // head size of this file
+constexpr int LDA = kC + 4;        // stride of buffers with 64 columns
+constexpr int LDB = kD2 + 4;       // stride of buffers with 128 columns
+constexpr int kThreads = 256;
+
+// acc[i][j] += sum_{k < K} X[k][m0 + i] * Y[k][n0 + j]  (k-major operands)
+template <int K>
+__device__ __forceinline__ void mmk(const float *__restrict__ X, int ldx, const float *__restrict__ Y,
+                                    int ldy, int m0, int n0, float (&acc)[4][4]) {
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        const float4 a = *reinterpret_cast<const float4 *>(X + k * ldx + m0);
+        const float4 b = *reinterpret_cast<const float4 *>(Y + k * ldy + n0);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+__device__ __forceinline__ void zero(float (&a)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
+}
+
+__device__ __forceinline__ void store4(float *Z, int ld, int m0, int n0, const float (&a)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(Z + (m0 + i) * ld + n0) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+}
+
+template <typename T> __device__ __forceinline__ void put4(T *dst, const float *v);
+template <> __device__ __forceinline__ void put4<float>(float *dst, const float *v) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <> __device__ __forceinline__ void put4<__nv_bfloat16>(__nv_bfloat16 *dst, const float *v) {
+    uint2 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    *reinterpret_cast<uint2 *>(dst) = u;
+}
+
+// ---------------------------------------------------------------- preparation
+// One CTA of 256 threads per (block, head). Shared memory: W [s][c] and its transpose, Q^T,
+// K^T (the 128-wide operands), and four 64 x 64 buffers (A, A^T, two scratch).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
+                 const float *__restrict__ beta, int L, int Lp, int nblk, float scale_log2,
+                 float *__restrict__ qt, float *__restrict__ kp, float *__restrict__ dg) {
+    extern __shared__ __align__(16) float sm[];
+    float *Wr = sm;                  // W [s][c], 64 x LDB
+    float *Wt = Wr + kC * LDB;       // W^T [c][s], 128 x LDA
+    float *Qt = Wt + kD2 * LDA;      // Q^T [c][i]; later (A W) [s][c] (64 x LDB)
+    float *Kt = Qt + kD2 * LDA;      // K^T [c][j]
+    float *Ar = Kt + kD2 * LDA;      // A [s][u]
+    float *At = Ar + kC * LDA;       // A^T [u][s]
+    float *X = At + kC * LDA;        // scratch 64 x 64
+    float *Y = X + kC * LDA;         // scratch 64 x 64
+    float *bs = Y + kC * LDA;        // beta [64]
+
+    const int tid = threadIdx.x, blk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = blk * kC;
+    const size_t head = (size_t)bh * L;
+    for (int e = tid; e < kC * kD2; e += kThreads) {
+        const int s = e / kD2, c = e % kD2, t = t0 + s;
+        float wv = 0.f, qv = 0.f, kv = 0.f;
+        if (t < L) {
+            const size_t g = (head + t) * kD2 + c;
+            wv = Elt<T>::to_f(w[g]);
+            qv = Elt<T>::to_f(q[g]);
+            kv = Elt<T>::to_f(k[g]);
+        }
+        Wr[s * LDB + c] = wv;
+        Wt[c * LDA + s] = wv;
+        Qt[c * LDA + s] = qv;
+        Kt[c * LDA + s] = kv;
+    }
+    for (int e = tid; e < kC * kC; e += kThreads) Ar[(e / kC) * LDA + e % kC] = 0.f;
+    if (tid < kC) bs[tid] = (t0 + tid < L) ? beta[head + t0 + tid] : 0.f;
+    __syncthreads();
+
+    const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
+    float acc[4][4];
+    // G = W W^T -> X
+    zero(acc);
+    mmk<kD2>(Wt, LDA, Wt, LDA, m0, n0, acc);
+    store4(X, LDA, m0, n0, acc);
+    __syncthreads();
+    // A = (I + D N)^{-1} D, one column per four threads: A[u][u] = beta_u and, for s < u,
+    // A[s][u] = -beta_s sum_{v = s+1..u} G[s][v] A[v][u]
+    {
+        const int u = tid >> 2, part = tid & 3;
+        for (int s = kC - 1; s >= 0; --s) {
+            float sum = 0.f;
+            for (int v = s + 1 + part; v < kC; v += 4) sum = fmaf(X[s * LDA + v], Ar[v * LDA + u], sum);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (part == 0) Ar[s * LDA + u] = (s == u) ? bs[u] : (s < u ? -bs[s] * sum : 0.f);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < kC * kC; e += kThreads) {
+        const int s = e / kC, u = e % kC;
+        At[u * LDA + s] = Ar[s * LDA + u];
+    }
+    // Lq^T [u][i] = w_u . q_i (u <= i) -> X;  Rk^T [s][j] = w_s . k_j (s > j) -> Y
+    zero(acc);
+    mmk<kD2>(Wt, LDA, Qt, LDA, m0, n0, acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (m0 + i > n0 + j) acc[i][j] = 0.f;
+    float acc2[4][4];
+    zero(acc2);
+    mmk<kD2>(Wt, LDA, Kt, LDA, m0, n0, acc2);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (m0 + i <= n0 + j) acc2[i][j] = 0.f;
+    __syncthreads();
+    store4(X, LDA, m0, n0, acc);
+    store4(Y, LDA, m0, n0, acc2);
+    __syncthreads();
+    // Qhat^T [s][i] = sum_u A[s][u] Lq^T[u][i] (in place in X)
+    zero(acc);
+    mmk<kC>(At, LDA, X, LDA, m0, n0, acc);
+    __syncthreads();
+    store4(X, LDA, m0, n0, acc);
+    __syncthreads();
+
+    const size_t blk_base = (size_t)bh * nblk + blk;
+    // diagonal-block logits, log2 units: scale (q_i . k_j - sum_s Qhat[i][s] Rk[j][s]), j <= i
+    {
+        float qk[4][4], corr[4][4];
+        zero(qk);
+        zero(corr);
+        mmk<kD2>(Qt, LDA, Kt, LDA, m0, n0, qk);
+        mmk<kC>(X, LDA, Y, LDA, m0, n0, corr);
+        float *out = dg + blk_base * kC * kC;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ii = m0 + i, jj = n0 + j;
+                v[j] = (jj <= ii && t0 + jj < L) ? scale_log2 * (qk[i][j] - corr[i][j]) : -INFINITY;
+            }
+            put4<float>(out + (m0 + i) * kC + n0, v);
+        }
+    }
+    // q~[i][c] = q[i][c] - sum_s Qhat[i][s] W[s][c], two passes of 64 columns
+    for (int p = 0; p < 2; ++p) {
+        zero(acc);
+        mmk<kC>(X, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
+        float *out = qt + ((size_t)bh * Lp + t0) * kD2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = Qt[(n0 + 64 * p + j) * LDA + m0 + i] - acc[i][j];
+            put4<float>(out + (m0 + i) * kD2 + n0 + 64 * p, v);
+        }
+    }
+    __syncthreads();
+    // Khat^T [u][j] = sum_s A[s][u] Rk^T[s][j] (in place in Y)
+    zero(acc);
+    mmk<kC>(Ar, LDA, Y, LDA, m0, n0, acc);
+    __syncthreads();
+    store4(Y, LDA, m0, n0, acc);
+    __syncthreads();
+    // k~[j][c] = k[j][c] - sum_u Khat[j][u] W[u][c]
+    float *kp_blk = kp + blk_base * (kC + kD2) * kD2;
+    for (int p = 0; p < 2; ++p) {
+        zero(acc);
+        mmk<kC>(Y, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = Kt[(n0 + 64 * p + j) * LDA + m0 + i] - acc[i][j];
+            put4<float>(kp_blk + (m0 + i) * kD2 + n0 + 64 * p, v);
+        }
+    }
+    __syncthreads();
+    // (A W)[s][c] = sum_u A[s][u] W[u][c] -> the Q^T buffer, as 64 x LDB
+    float *AW = Qt;
+    for (int p = 0; p < 2; ++p) {
+        zero(acc);
+        mmk<kC>(At, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
+        store4(AW, LDB, m0, n0 + 64 * p, acc);
+    }
+    __syncthreads();
+    // P_b[n][c] = delta(n, c) - sum_s W[s][n] (A W)[s][c], four 64 x 64 quadrants
+    for (int pq = 0; pq < 4; ++pq) {
+        const int nb = 64 * (pq >> 1), cb = 64 * (pq & 1);
+        zero(acc);
+        mmk<kC>(Wr, LDB, AW, LDB, nb + m0, cb + n0, acc);
+        float *out = kp_blk + kC * kD2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = ((nb + m0 + i) == (cb + n0 + j) ? 1.f : 0.f) - acc[i][j];
+            put4<float>(out + (nb + m0 + i) * kD2 + cb + n0, v);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- scan
+// One CTA per (64-row query block, head): the state X = (q~_i) transposed in shared memory;
+// for key block b = ib, ib-1, ..., 0 the logits (diagonal block: the table; earlier blocks:
+// X K~_b^T), the online softmax, O += P V_b and X <- X P_b^T.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const float *__restrict__ kp,
+                 const float *__restrict__ dg, T *__restrict__ out, float *__restrict__ lse, int L,
+                 int Lp, int nblk, float scale_log2) {
+    extern __shared__ __align__(16) float sm[];
+    float *XT = sm;                 // X^T [c][i], 128 x LDA
+    float *KT = XT + kD2 * LDA;     // K~_b^T [c][j], 128 x LDA
+    float *PT = KT + kD2 * LDA;     // P_b^T [c][n], 128 x LDB
+    float *Vs = PT + kD2 * LDB;     // V_b [j][c], 64 x LDB
+    float *Ss = Vs + kC * LDB;      // logits [i][j] (log2 units)
+    float *PsT = Ss + kC * LDA;     // probabilities [j][i]
+    float *alpha_s = PsT + kC * LDA;
+
+    const int tid = threadIdx.x, ib = blockIdx.x, bh = blockIdx.y;
+    if (ib * kC >= L) return;
+    const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
+    const int row = tid >> 2, part = tid & 3;
+    const size_t hL = (size_t)bh * L;
+    for (int e = tid; e < kC * kD2; e += kThreads) {
+        const int i = e / kD2, c = e % kD2;
+        XT[c * LDA + i] = qt[((size_t)bh * Lp + (size_t)ib * kC + i) * kD2 + c];
+    }
+    float acc[2][4][4];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) zero(acc[p]);
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int b = ib; b >= 0; --b) {
+        __syncthreads();
+        for (int e = tid; e < kC * kD2; e += kThreads) {
+            const int j = e / kD2, c = e % kD2, t = b * kC + j;
+            Vs[j * LDB + c] = (t < L) ? Elt<T>::to_f(v[(hL + t) * kD2 + c]) : 0.f;
+        }
+        if (b < ib) {
+            const float *blk = kp + ((size_t)bh * nblk + b) * (kC + kD2) * kD2;
+            for (int e = tid; e < kC * kD2; e += kThreads) {
+                const int j = e / kD2, c = e % kD2;
+                KT[c * LDA + j] = blk[e];
+            }
+            for (int e = tid; e < kD2 * kD2; e += kThreads) {
+                const int n = e / kD2, c = e % kD2;
+                PT[c * LDB + n] = blk[kC * kD2 + e];
+            }
+        } else {
+            const float *tab = dg + ((size_t)bh * nblk + b) * kC * kC;
+            for (int e = tid; e < kC * kC; e += kThreads) Ss[(e / kC) * LDA + e % kC] = tab[e];
+        }
+        __syncthreads();
+        if (b < ib) {
+            float sv[4][4], xn[2][4][4];
+            zero(sv);
+            mmk<kD2>(XT, LDA, KT, LDA, m0, n0, sv);
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                zero(xn[p]);
+                mmk<kD2>(XT, LDA, PT, LDB, m0, n0 + 64 * p, xn[p]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4 *>(Ss + (m0 + i) * LDA + n0) =
+                    make_float4(sv[i][0] * scale_log2, sv[i][1] * scale_log2, sv[i][2] * scale_log2,
+                                sv[i][3] * scale_log2);
+            __syncthreads();
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) XT[(n0 + 64 * p + j) * LDA + m0 + i] = xn[p][i][j];
+        }
+        __syncthreads();
+        // ---- online softmax, 4 threads per row, 16 columns each
+        {
+            float x[16];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                x[j] = Ss[row * LDA + part * 16 + j];
+                mx = fmaxf(mx, x[j]);
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float pj = exp2f(x[j] - m_use);
+                sum += pj;
+                PsT[(part * 16 + j) * LDA + row] = pj;
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            l_run = l_run * alpha + sum;
+            m_run = m_new;
+            if (part == 0) alpha_s[row] = alpha;
+        }
+        __syncthreads();
+        {
+            float al[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) al[i] = alpha_s[m0 + i];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[p][i][j] *= al[i];
+                mmk<kC>(PsT, LDA, Vs, LDB, m0, n0 + 64 * p, acc[p]);
+            }
+        }
+    }
+    __syncthreads();
+    if (part == 0) alpha_s[row] = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    if (lse != nullptr && part == 0 && ib * kC + row < L)
+        lse[hL + ib * kC + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = ib * kC + m0 + i;
+        if (t < L) {
+            const float inv = alpha_s[m0 + i];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const float o4[4] = {acc[p][i][0] * inv, acc[p][i][1] * inv, acc[p][i][2] * inv,
+                                     acc[p][i][3] * inv};
+                put4<T>(out + (hL + t) * kD2 + n0 + 64 * p, o4);
+            }
+        }
+    }
+}
+
+size_t prep_d128_smem() {
+    return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + kC) * sizeof(float);
+}
+size_t scan_d128_smem() {
+    return (size_t)(2 * kD2 * LDA + kD2 * LDB + kC * LDB + 2 * kC * LDA + kC) * sizeof(float);
+}
+
+}  // namespace
+
+// Workspace of the d = 128 forward: 256-byte status header, fp32 q~ (BH, Lp, 128), per block
+// [k~ (64 rows); P_b (128 rows)] (BH, nblk, 192, 128), diagonal logits (BH, nblk, 64, 64).
+D128Layout d128_layout(int B, int H, int L) {
+    D128Layout y;
+    y.BH = B * H;
+    y.nblk = (L + kC - 1) / kC;
+    y.Lp = y.nblk * kC;
+    const size_t bh = (size_t)y.BH;
+    size_t off = 256;
+    y.off_qt = off;
+    off = align256(off + bh * y.Lp * kD2 * 4);
+    y.off_kp = off;
+    off = align256(off + bh * y.nblk * (kC + kD2) * kD2 * 4);
+    y.off_dg = off;
+    off = align256(off + bh * y.nblk * kC * kC * 4);
+    y.total = off;
+    return y;
+}
+
+template <typename T>
+cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const float *beta,
+                             int B, int H, int L, float scale, void *ws, cudaStream_t stream) {
+    const D128Layout y = d128_layout(B, H, L);
+    char *base = static_cast<char *>(ws);
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(base, 0, 4, stream)) != cudaSuccess) return e;
+    const size_t sm = prep_d128_smem();
+    if ((e = cudaFuncSetAttribute(prep_d128_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm)) != cudaSuccess)
+        return e;
+    prep_d128_kernel<T><<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta, L,
+        y.Lp, y.nblk, scale * kLog2e, reinterpret_cast<float *>(base + y.off_qt),
+        reinterpret_cast<float *>(base + y.off_kp), reinterpret_cast<float *>(base + y.off_dg));
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_scan_d128(const void *v, void *out, float *lse, int B, int H, int L, float scale,
+                             void *ws, cudaStream_t stream) {
+    const D128Layout y = d128_layout(B, H, L);
+    const char *base = static_cast<const char *>(ws);
+    cudaError_t e;
+    const size_t sm = scan_d128_smem();
+    if ((e = cudaFuncSetAttribute(scan_d128_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm)) != cudaSuccess)
+        return e;
+    scan_d128_kernel<T><<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
+        static_cast<const T *>(v), reinterpret_cast<const float *>(base + y.off_qt),
+        reinterpret_cast<const float *>(base + y.off_kp), reinterpret_cast<const float *>(base + y.off_dg),
+        static_cast<T *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e);
+    return cudaGetLastError();
+}
+
+#define PATH_D128_INST(T)                                                                        \
+    template cudaError_t launch_prep_d128<T>(const void *, const void *, const void *,           \
+                                             const float *, int, int, int, float, void *,        \
+                                             cudaStream_t);                                      \
+    template cudaError_t launch_scan_d128<T>(const void *, void *, float *, int, int, int, float, \
+                                             void *, cudaStream_t);
+PATH_D128_INST(float)
+PATH_D128_INST(__nv_bfloat16)
+#undef PATH_D128_INST
+
+}  // namespace path

@@ -44,6 +44,12 @@ cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const v
                             const float *lse, const void *dout, int B, int H, int L, float scale,
                             float *dq, float *dk, float *dv, float *dw, float *dbeta, float *dlogf,
                             void *ws, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const float *beta,
+                             int B, int H, int L, float scale, void *ws, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_scan_d128(const void *v, void *out, float *lse, int B, int H, int L, float scale,
+                             void *ws, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len, int d);
 template <typename T>
@@ -80,7 +86,12 @@ path_status check_sizes(int B, int H, int L, int d, int dtype) {
     return PATH_OK;
 }
 
-// Decode works on head sizes 64 and 128 (the forward on 64 only).
+// The plain forward also takes d = 128 (fp32 CUDA-core kernels); PaTH-FoX takes 64 only.
+path_status check_fwd_sizes(int B, int H, int L, int d, int dtype, bool fox) {
+    return check_sizes(B, H, L, (d == 128 && !fox) ? kD : d, dtype);
+}
+
+// Decode works on head sizes 64 and 128.
 path_status check_decode_sizes(int B, int H, int cap, int d, int dtype) {
     return check_sizes(B, H, cap, d == 128 ? kD : (d == kD ? kD : -1), dtype);
 }
@@ -97,7 +108,7 @@ path_status check_ws(void *ws, size_t ws_bytes, size_t need) {
 path_status prepare_impl(const void *q, const void *k, const void *w, const float *beta,
                          const float *log_f, bool fox, int B, int H, int L, int d, int dtype,
                          float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    path_status st = check_sizes(B, H, L, d, dtype);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype, fox);
     if (st != PATH_OK) return st;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
     if ((long long)B * H * L == 0) return PATH_OK;
@@ -105,6 +116,12 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 16) || !aligned(beta, 16) ||
         (fox && !aligned(log_f, 16)))
         return PATH_ERR_ALIGN;
+    if (d == 128) {
+        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L).total)) != PATH_OK) return st;
+        return from_cuda(dtype == PATH_BF16
+                             ? launch_prep_d128<__nv_bfloat16>(q, k, w, beta, B, H, L, scale, ws, stream)
+                             : launch_prep_d128<float>(q, k, w, beta, B, H, L, scale, ws, stream));
+    }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
     const float *lf = fox ? log_f : nullptr;
@@ -122,12 +139,18 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
 
 path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int H, int L, int d,
                       int dtype, float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    path_status st = check_sizes(B, H, L, d, dtype);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype, fox);
     if (st != PATH_OK) return st;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
     if ((long long)B * H * L == 0) return PATH_OK;
     if (!v || !out) return PATH_ERR_NULL;
     if (!aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16))) return PATH_ERR_ALIGN;
+    if (d == 128) {
+        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L).total)) != PATH_OK) return st;
+        return from_cuda(dtype == PATH_BF16
+                             ? launch_scan_d128<__nv_bfloat16>(v, out, lse, B, H, L, scale, ws, stream)
+                             : launch_scan_d128<float>(v, out, lse, B, H, L, scale, ws, stream));
+    }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
     if (dtype == PATH_BF16) {
@@ -178,7 +201,8 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
     switch (op) {
         case PATH_OP_FWD:
         case PATH_OP_FOX_FWD:
-            if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+            if (check_fwd_sizes(B, H, L, d, dtype, op == PATH_OP_FOX_FWD) != PATH_OK) return 0;
+            if (d == 128) return d128_layout(B, H, L).total;
             return fwd_layout(B, H, L, elt_bytes(dtype), op == PATH_OP_FOX_FWD).total;
         default: break;
     }
@@ -248,7 +272,7 @@ path_status path_attn_fwd(const void *q, const void *k, const void *v, const voi
                           int dtype, float scale, void *ws, size_t ws_bytes, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // every argument of both stages is checked before the first launch
-    path_status st = check_sizes(B, H, L, d, dtype);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype, false);
     if (st != PATH_OK) return st;
     if ((long long)B * H * L > 0) {
         if (!v || !out) return PATH_ERR_NULL;

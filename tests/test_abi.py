@@ -62,9 +62,13 @@ def test_workspace_sizes(lib):
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 64, lib.BF16) == \
         256 + (part + 255) // 256 * 256
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 32, lib.BF16) == 0
-    # head size 128: decode only; partials (m, l, o[128])
-    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, lib.BF16) == 0
+    # head size 128: the plain forward keeps fp32 q~ (Lp x 128), per block [k~; P_b]
+    # (192 x 128) and the fp32 diagonal table, whatever the dtype; PaTH-FoX is d = 64 only
+    for dt in (lib.BF16, lib.F32):
+        assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, dt) == \
+            256 + 128 * 128 * 4 + 2 * 192 * 128 * 4 + 2 * 64 * 64 * 4
     assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, lib.BF16) == 0
+    # decode partials (m, l, o[128])
     part128 = 4 * 2 * 130 * 4
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 128, lib.BF16) == \
         256 + (part128 + 255) // 256 * 256
@@ -277,3 +281,12 @@ def _fox_bwd(so, **kw):
 ])
 def test_fox_bwd_rejects_bad_arguments_before_launch(so, kw, code):
     assert _fox_bwd(so, **kw) == code
+
+
+def test_fwd_head_size_128_checks(so):
+    # d = 128 passes the size checks of the plain forward (the workspace check then stops
+    # it); 96 does not, and PaTH-FoX stays d = 64 only
+    assert _fwd(so, d=128, ws_bytes=1000) == 5
+    assert _fwd(so, d=96) == 2
+    assert so.path_fox_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 128, 128, 1,
+                           ctypes.c_float(0.125), FAKE, ctypes.c_size_t(1 << 30), None) == 2
