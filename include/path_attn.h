@@ -14,8 +14,10 @@
  *  - Device pointers, contiguous row-major: q, k, v, w, out are (B, H, L, d);
  *    beta, log_f, lse are (B, H, L) fp32. Element type of q, k, v, w, out and of
  *    the decode caches is given by `dtype` (PATH_F32 or PATH_BF16).
- *  - d must be 64 (the head size the pages benchmark); the decode steps also take
- *    d = 128 (the larger head the pages mention). Anything else returns PATH_ERR_SHAPE.
+ *  - d must be 64 (the head size the pages benchmark); the plain forward (path_attn_fwd,
+ *    path_fwd_prepare, path_fwd_scan) and the decode steps also take d = 128 (the larger
+ *    head the pages mention; the forward then runs on fp32 CUDA-core kernels for either
+ *    dtype). Anything else returns PATH_ERR_SHAPE.
  *  - Every tensor pointer and the workspace must be 16-byte aligned
  *    (PATH_ERR_ALIGN); the workspace must be 256-byte aligned.
  *  - The caller owns every buffer, the workspace included. The library
