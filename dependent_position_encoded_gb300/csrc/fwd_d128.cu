@@ -48,6 +48,45 @@ __device__ __forceinline__ void store4(float *Z, int ld, int m0, int n0, const f
         *reinterpret_cast<float4 *>(Z + (m0 + i) * ld + n0) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
 }
 
+// rows x 128 fp32 tile (row-major, 128 floats per row) into shared memory as is
+// (dst[r * ld + c]) or transposed (dst[c * ld + r]); eight 16-byte loads in flight per
+// thread before the first store
+__device__ __forceinline__ void load128(float *dst, int ld, const float *__restrict__ src, int rows,
+                                        bool transpose) {
+    const int n4 = rows * (kD2 / 4);
+    for (int base = 0; base < n4; base += 8 * kThreads) {
+        float4 x[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int e = base + (int)threadIdx.x + it * kThreads;
+            x[it] = e < n4 ? reinterpret_cast<const float4 *>(src)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int e = base + (int)threadIdx.x + it * kThreads;
+            if (e < n4) {
+                const int r = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
+                if (transpose) {
+                    dst[c * ld + r] = x[it].x;
+                    dst[(c + 1) * ld + r] = x[it].y;
+                    dst[(c + 2) * ld + r] = x[it].z;
+                    dst[(c + 3) * ld + r] = x[it].w;
+                } else {
+                    *reinterpret_cast<float4 *>(dst + r * ld + c) = x[it];
+                }
+            }
+        }
+    }
+}
+
+// four consecutive elements of type T, widened
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 template <typename T> __device__ __forceinline__ void put4(T *dst, const float *v);
 template <> __device__ __forceinline__ void put4<float>(float *dst, const float *v) {
     *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
@@ -81,19 +120,34 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     const int tid = threadIdx.x, blk = blockIdx.x, bh = blockIdx.y;
     const int t0 = blk * kC;
     const size_t head = (size_t)bh * L;
-    for (int e = tid; e < kC * kD2; e += kThreads) {
-        const int s = e / kD2, c = e % kD2, t = t0 + s;
-        float wv = 0.f, qv = 0.f, kv = 0.f;
-        if (t < L) {
-            const size_t g = (head + t) * kD2 + c;
-            wv = Elt<T>::to_f(w[g]);
-            qv = Elt<T>::to_f(q[g]);
-            kv = Elt<T>::to_f(k[g]);
+    // four elements per thread and step, all of a thread's loads issued first
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float4 wv[4], qv[4], kv[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + (4 * half + it) * kThreads, s = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
+            const bool in = t0 + s < L;
+            const size_t g = (head + t0 + s) * kD2 + c;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            wv[it] = in ? ld4(w + g) : z;
+            qv[it] = in ? ld4(q + g) : z;
+            kv[it] = in ? ld4(k + g) : z;
         }
-        Wr[s * LDB + c] = wv;
-        Wt[c * LDA + s] = wv;
-        Qt[c * LDA + s] = qv;
-        Kt[c * LDA + s] = kv;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + (4 * half + it) * kThreads, s = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
+            *reinterpret_cast<float4 *>(Wr + s * LDB + c) = wv[it];
+            const float wa[4] = {wv[it].x, wv[it].y, wv[it].z, wv[it].w};
+            const float qa[4] = {qv[it].x, qv[it].y, qv[it].z, qv[it].w};
+            const float ka[4] = {kv[it].x, kv[it].y, kv[it].z, kv[it].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                Wt[(c + j) * LDA + s] = wa[j];
+                Qt[(c + j) * LDA + s] = qa[j];
+                Kt[(c + j) * LDA + s] = ka[j];
+            }
+        }
     }
     for (int e = tid; e < kC * kC; e += kThreads) Ar[(e / kC) * LDA + e % kC] = 0.f;
     if (tid < kC) bs[tid] = (t0 + tid < L) ? beta[head + t0 + tid] : 0.f;
@@ -252,33 +306,38 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
     const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
     const int row = tid >> 2, part = tid & 3;
     const size_t hL = (size_t)bh * L;
-    for (int e = tid; e < kC * kD2; e += kThreads) {
-        const int i = e / kD2, c = e % kD2;
-        XT[c * LDA + i] = qt[((size_t)bh * Lp + (size_t)ib * kC + i) * kD2 + c];
-    }
+    load128(XT, LDA, qt + ((size_t)bh * Lp + (size_t)ib * kC) * kD2, kC, true);
     float acc[2][4][4];
 #pragma unroll
     for (int p = 0; p < 2; ++p) zero(acc[p]);
     float m_run = -INFINITY, l_run = 0.f;
     for (int b = ib; b >= 0; --b) {
         __syncthreads();
-        for (int e = tid; e < kC * kD2; e += kThreads) {
-            const int j = e / kD2, c = e % kD2, t = b * kC + j;
-            Vs[j * LDB + c] = (t < L) ? Elt<T>::to_f(v[(hL + t) * kD2 + c]) : 0.f;
+        {
+            float4 vv[8];
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int e = tid + it * kThreads, j = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
+                vv[it] = (b * kC + j < L) ? ld4(v + (hL + b * kC + j) * kD2 + c)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int e = tid + it * kThreads, j = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
+                *reinterpret_cast<float4 *>(Vs + j * LDB + c) = vv[it];
+            }
         }
         if (b < ib) {
             const float *blk = kp + ((size_t)bh * nblk + b) * (kC + kD2) * kD2;
-            for (int e = tid; e < kC * kD2; e += kThreads) {
-                const int j = e / kD2, c = e % kD2;
-                KT[c * LDA + j] = blk[e];
-            }
-            for (int e = tid; e < kD2 * kD2; e += kThreads) {
-                const int n = e / kD2, c = e % kD2;
-                PT[c * LDB + n] = blk[kC * kD2 + e];
-            }
+            load128(KT, LDA, blk, kC, true);
+            load128(PT, LDB, blk + kC * kD2, kD2, true);
         } else {
             const float *tab = dg + ((size_t)bh * nblk + b) * kC * kC;
-            for (int e = tid; e < kC * kC; e += kThreads) Ss[(e / kC) * LDA + e % kC] = tab[e];
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int e = tid + it * kThreads, r = e / (kC / 4), c = 4 * (e % (kC / 4));
+                *reinterpret_cast<float4 *>(Ss + r * LDA + c) = reinterpret_cast<const float4 *>(tab)[e];
+            }
         }
         __syncthreads();
         if (b < ib) {
