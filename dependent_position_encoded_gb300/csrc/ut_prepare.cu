@@ -102,22 +102,35 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     const size_t head = (size_t)bh * L;
     if (blk == 0 && bh == 0 && tid == 0 && status) *status = 0u;
 
-    // ---- load W, Q, K (fp32, both layouts for W), beta; padded tokens are zero
-    for (int e = tid; e < kC * kD; e += kPrepThreads) {
-        const int s = e / kD, c = e % kD;
-        const int t = t0 + s;
-        float wv = 0.f, qv = 0.f, kv = 0.f;
-        if (t < L) {
-            const size_t g = (head + t) * kD + c;
-            wv = Elt<T>::to_f(w[g]);
-            qv = Elt<T>::to_f(q[g]);
-            kv = Elt<T>::to_f(k[g]);
+    // ---- load W, Q, K (fp32, both layouts for W), beta; padded tokens are zero. Four
+    // elements per thread and step, all of a thread's loads issued before the first store.
+    {
+        constexpr int kIt = kC * kD / 4 / kPrepThreads;
+        float wv[kIt][4], qv[kIt][4], kv[kIt][4];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = 4 * (tid + it * kPrepThreads), s = e / kD, c = e % kD;
+            const bool in = t0 + s < L;
+            const size_t g = (head + t0 + s) * kD + c;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                wv[it][j] = in ? Elt<T>::to_f(w[g + j]) : 0.f;
+                qv[it][j] = in ? Elt<T>::to_f(q[g + j]) : 0.f;
+                kv[it][j] = in ? Elt<T>::to_f(k[g + j]) : 0.f;
+            }
         }
-        Wr[s * LD + c] = wv;
-        Wt[c * LD + s] = wv;
-        Qt[c * LD + s] = qv;
-        Kt[c * LD + s] = kv;
-        Ar[s * LD + c] = 0.f;
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = 4 * (tid + it * kPrepThreads), s = e / kD, c = e % kD;
+            *reinterpret_cast<float4 *>(Wr + s * LD + c) = make_float4(wv[it][0], wv[it][1], wv[it][2], wv[it][3]);
+            *reinterpret_cast<float4 *>(Ar + s * LD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                Wt[(c + j) * LD + s] = wv[it][j];
+                Qt[(c + j) * LD + s] = qv[it][j];
+                Kt[(c + j) * LD + s] = kv[it][j];
+            }
+        }
     }
     if (tid < kC) {
         const int t = t0 + tid;
