@@ -284,32 +284,67 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
 }
 
 // ---------------------------------------------------------------- scan
-// One CTA per (64-row query block, head): the state X = (q~_i) transposed in shared memory;
+// acc[i][j] += sum_{k < K} A[r0 + 16i][k] * B[k][col(j)] with A row-major and B k-major;
+// col(j) = c0 + j for j < 4 and c0 + 64 + j - 4 for j >= 4 (NJ = 8). The 16 lanes of a
+// half warp share the A rows (broadcast loads) and the eight lanes of a quarter warp read
+// one contiguous 128-byte piece of B.
+template <int K, int NJ>
+__device__ __forceinline__ void mmr(const float *__restrict__ A, int lda, const float *__restrict__ B,
+                                    int ldb, int r0, int c0, float (&acc)[4][NJ]) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float bv[NJ];
+            const float4 b0 = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + c0);
+            bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+            if (NJ == 8) {
+                const float4 b1 = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + c0 + 64);
+                bv[NJ == 8 ? 4 : 0] = b1.x; bv[NJ == 8 ? 5 : 1] = b1.y;
+                bv[NJ == 8 ? 6 : 2] = b1.z; bv[NJ == 8 ? 7 : 3] = b1.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+            }
+        }
+    }
+}
+
+// One CTA per (64-row query block, head): the state X = (q~_i) as rows in shared memory;
 // for key block b = ib, ib-1, ..., 0 the logits (diagonal block: the table; earlier blocks:
-// X K~_b^T), the online softmax, O += P V_b and X <- X P_b^T.
+// X K~_b^T), the online softmax, O += P V_b and X <- X P_b^T. Thread (ty, tx) owns rows
+// ty + 16i (i < 4) and, of the 128-wide results, columns 4tx .. 4tx + 3 and 64 + 4tx ..
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const float *__restrict__ kp,
                  const float *__restrict__ dg, T *__restrict__ out, float *__restrict__ lse, int L,
                  int Lp, int nblk, float scale_log2) {
     extern __shared__ __align__(16) float sm[];
-    float *XT = sm;                 // X^T [c][i], 128 x LDA
-    float *KT = XT + kD2 * LDA;     // K~_b^T [c][j], 128 x LDA
+    float *Xr = sm;                 // X [i][c], 64 x LDB
+    float *KT = Xr + kC * LDB;      // K~_b^T [c][j], 128 x LDA
     float *PT = KT + kD2 * LDA;     // P_b^T [c][n], 128 x LDB
     float *Vs = PT + kD2 * LDB;     // V_b [j][c], 64 x LDB
     float *Ss = Vs + kC * LDB;      // logits [i][j] (log2 units)
-    float *PsT = Ss + kC * LDA;     // probabilities [j][i]
-    float *alpha_s = PsT + kC * LDA;
+    float *Pm = Ss + kC * LDA;      // probabilities [i][j]
+    float *alpha_s = Pm + kC * LDA;
 
     const int tid = threadIdx.x, ib = blockIdx.x, bh = blockIdx.y;
     if (ib * kC >= L) return;
-    const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
+    const int ty = tid / 16, tx = tid % 16, r0 = ty, c0 = 4 * tx;
     const int row = tid >> 2, part = tid & 3;
     const size_t hL = (size_t)bh * L;
-    load128(XT, LDA, qt + ((size_t)bh * Lp + (size_t)ib * kC) * kD2, kC, true);
-    float acc[2][4][4];
+    load128(Xr, LDB, qt + ((size_t)bh * Lp + (size_t)ib * kC) * kD2, kC, false);
+    float acc[4][8];
 #pragma unroll
-    for (int p = 0; p < 2; ++p) zero(acc[p]);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     for (int b = ib; b >= 0; --b) {
         __syncthreads();
@@ -341,26 +376,28 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
         }
         __syncthreads();
         if (b < ib) {
-            float sv[4][4], xn[2][4][4];
-            zero(sv);
-            mmk<kD2>(XT, LDA, KT, LDA, m0, n0, sv);
+            float sv[4][4], xn[4][8];
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                zero(xn[p]);
-                mmk<kD2>(XT, LDA, PT, LDB, m0, n0 + 64 * p, xn[p]);
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sv[i][j] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xn[i][j] = 0.f;
             }
+            mmr<kD2, 4>(Xr, LDB, KT, LDA, r0, c0, sv);
+            mmr<kD2, 8>(Xr, LDB, PT, LDB, r0, c0, xn);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4 *>(Ss + (m0 + i) * LDA + n0) =
+                *reinterpret_cast<float4 *>(Ss + (r0 + 16 * i) * LDA + c0) =
                     make_float4(sv[i][0] * scale_log2, sv[i][1] * scale_log2, sv[i][2] * scale_log2,
                                 sv[i][3] * scale_log2);
             __syncthreads();
 #pragma unroll
-            for (int p = 0; p < 2; ++p)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) XT[(n0 + 64 * p + j) * LDA + m0 + i] = xn[p][i][j];
+            for (int i = 0; i < 4; ++i) {
+                float *xr = Xr + (r0 + 16 * i) * LDB;
+                *reinterpret_cast<float4 *>(xr + c0) = make_float4(xn[i][0], xn[i][1], xn[i][2], xn[i][3]);
+                *reinterpret_cast<float4 *>(xr + c0 + 64) = make_float4(xn[i][4], xn[i][5], xn[i][6], xn[i][7]);
+            }
         }
         __syncthreads();
         // ---- online softmax, 4 threads per row, 16 columns each
@@ -379,10 +416,14 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float pj = exp2f(x[j] - m_use);
-                sum += pj;
-                PsT[(part * 16 + j) * LDA + row] = pj;
+            for (int j = 0; j < 16; j += 4) {
+                float pj[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    pj[q] = exp2f(x[j + q] - m_use);
+                    sum += pj[q];
+                }
+                *reinterpret_cast<float4 *>(Pm + row * LDA + part * 16 + j) = make_float4(pj[0], pj[1], pj[2], pj[3]);
             }
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -392,17 +433,13 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
         }
         __syncthreads();
         {
-            float al[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) al[i] = alpha_s[m0 + i];
+            for (int i = 0; i < 4; ++i) {
+                const float al = alpha_s[r0 + 16 * i];
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[p][i][j] *= al[i];
-                mmk<kC>(PsT, LDA, Vs, LDB, m0, n0 + 64 * p, acc[p]);
+                for (int j = 0; j < 8; ++j) acc[i][j] *= al;
             }
+            mmr<kC, 8>(Pm, LDA, Vs, LDB, r0, c0, acc);
         }
     }
     __syncthreads();
@@ -412,15 +449,13 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int t = ib * kC + m0 + i;
+        const int r = r0 + 16 * i, t = ib * kC + r;
         if (t < L) {
-            const float inv = alpha_s[m0 + i];
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const float o4[4] = {acc[p][i][0] * inv, acc[p][i][1] * inv, acc[p][i][2] * inv,
-                                     acc[p][i][3] * inv};
-                put4<T>(out + (hL + t) * kD2 + n0 + 64 * p, o4);
-            }
+            const float inv = alpha_s[r];
+            const float o0[4] = {acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv};
+            const float o1[4] = {acc[i][4] * inv, acc[i][5] * inv, acc[i][6] * inv, acc[i][7] * inv};
+            put4<T>(out + (hL + t) * kD2 + c0, o0);
+            put4<T>(out + (hL + t) * kD2 + c0 + 64, o1);
         }
     }
 }
@@ -429,7 +464,7 @@ size_t prep_d128_smem() {
     return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + kC) * sizeof(float);
 }
 size_t scan_d128_smem() {
-    return (size_t)(2 * kD2 * LDA + kD2 * LDB + kC * LDB + 2 * kC * LDA + kC) * sizeof(float);
+    return (size_t)(2 * kC * LDB + kD2 * LDA + kD2 * LDB + 2 * kC * LDA + kC) * sizeof(float);
 }
 
 }  // namespace
