@@ -426,6 +426,50 @@ def cpu_baseline(x_cpu, wl, target_s=12.0):
                       "time extrapolated by head count" % (n, nh_total, t)}
 
 
+def leg_cpu_baselines(wl_bwd, wl_dec, wl_prod):
+    """The fp64 oracle beside the backward, decode and producer legs, each on a bounded
+    sample of its workload's shapes and distributions (fresh draws of a few heads or
+    tokens), extrapolated to the workload in the leg's own unit."""
+    import numpy as np
+    import oracle
+    out = {}
+    # backward: two whole heads of L tokens
+    x = pi.make_fwd_inputs(1, 2, wl_bwd.L, seed=wl_bwd.seed, device="cpu")
+    d_out = torch.randn((1, 2, wl_bwd.L, 64), generator=torch.Generator().manual_seed(1))
+    t0 = time.perf_counter()
+    oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out.to(torch.bfloat16))
+    t = (time.perf_counter() - t0) * (wl_bwd.B * wl_bwd.H) / 2
+    out["bwd"] = {"value": wl_bwd.B * wl_bwd.L / t, "unit": "tokens/s", "cores": 2,
+                  "kind": "oracle", "sample": "2 of %d heads, L %d, one thread per head; "
+                  "time extrapolated by head count" % (wl_bwd.B * wl_bwd.H, wl_bwd.L)}
+    # decode: one step over 4 heads of the prefix cache
+    nh, n0 = 4, wl_dec.n_prefix
+    g = torch.Generator().manual_seed(wl_dec.seed)
+    cache = oracle.DecodeCache(torch.randn((nh, n0, 64), generator=g).to(torch.bfloat16),
+                               torch.randn((nh, n0, 64), generator=g).to(torch.bfloat16), n0 + 1)
+    q, k, v = (torch.randn((nh, 64), generator=g) for _ in range(3))
+    w = torch.nn.functional.normalize(torch.randn((nh, 64), generator=g), dim=-1)
+    beta = 2 * torch.sigmoid(torch.randn((nh,), generator=g))
+    t0 = time.perf_counter()
+    cache.step(q, k, v, w, beta)
+    t = (time.perf_counter() - t0) * (wl_dec.B * wl_dec.H) / nh
+    out["decode"] = {"value": decode_bytes(wl_dec.B, wl_dec.H, n0) / t / 1e9, "unit": "GB/s",
+                     "cores": 1, "kind": "oracle",
+                     "sample": "one step over %d of %d heads of a %d-key cache; time "
+                               "extrapolated by head count" % (nh, wl_dec.B * wl_dec.H, n0)}
+    # producer: one sequence of 256 tokens
+    Lp = 256
+    pr = pi.make_producer_inputs(1, Lp, wl_prod.D, wl_prod.R, wl_prod.H, seed=wl_prod.seed)
+    t0 = time.perf_counter()
+    oracle.wbeta_produce(pr["x"], pr["w_down"], pr["w_up"], pr["conv"], pr["u"], pr["bias"],
+                         beta_max=pi.BETA_CLIP)
+    t = (time.perf_counter() - t0) * (wl_prod.B * wl_prod.L) / Lp
+    out["producer"] = {"value": producer_bytes(wl_prod) / t / 1e9, "unit": "GB/s", "cores": 1,
+                       "kind": "oracle", "sample": "%d of %d tokens; time extrapolated by "
+                       "token count" % (Lp, wl_prod.B * wl_prod.L)}
+    return out
+
+
 PROFILE_CASES = {
     # a quarter of the speed workload: 1.3 GB on the device, inputs larger than L2
     "fwd": pi.FwdWorkload("path_fwd_bf16_B8H32L4096", 8, 32, 4096, 64, torch.bfloat16, 3,
@@ -725,6 +769,11 @@ def main():
             torch.cuda.empty_cache()
         line["sweep_L"] = sweep
 
+    if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
+        legs = leg_cpu_baselines(pi.BF16_L2048, pi.DECODE_32K, pi.PRODUCER_L4096)
+        for name, cb in legs.items():
+            if name in line:
+                line[name]["cpu_baseline"] = cb
     if rank == 0 and not args.no_cpu_baseline:
         xc = pi.make_fwd_inputs(1, 64, wl.L, seed=wl.seed, device="cpu")
         line["cpu_baseline"] = cpu_baseline(xc, pi.FwdWorkload(wl.name, wl.B, wl.H, wl.L, 64,
