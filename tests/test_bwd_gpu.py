@@ -178,3 +178,24 @@ def test_bwd_max_heads(lib):
     ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
                           d_out.reshape(-1, L, 64)[heads])
     _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
+
+
+def test_bwd_custom_scale(lib):
+    # a softmax scale other than 1/sqrt(d): it multiplies the whole logit, so every
+    # gradient but dv carries it
+    x = pi.make_fwd_inputs(1, 2, 150, seed=51, dtype=torch.float32, clip=0.0, device="cuda")
+    d_out = torch.randn((1, 2, 150, 64), generator=torch.Generator().manual_seed(52)).cuda()
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=0.3)
+    grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out,
+                              scale=0.3)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, scale=0.3)
+    _compare(grads, ref, 1e-4)
+
+
+@pytest.mark.parametrize("L", [1, 65])
+def test_fox_bwd_short(lib, L):
+    # one token (every gradient but dv and d log f of a single logit is zero) and one token
+    # in the last block
+    x, d_out, grads = _fox_case(lib, 1, 2, L, torch.float32, seed=60 + L)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, log_f=x["log_f"])
+    _compare(grads, ref, 1e-4)

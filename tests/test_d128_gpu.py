@@ -70,3 +70,12 @@ def test_d128_fox_is_rejected(lib):
     x = pi.make_fwd_inputs(1, 1, 64, d=D, dtype=torch.bfloat16, seed=1, fox=True, device="cuda")
     with pytest.raises(Exception):
         lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+
+
+def test_d128_custom_scale(lib):
+    x = pi.make_fwd_inputs(1, 2, 140, d=D, dtype=torch.float32, seed=21, clip=0.0, device="cuda")
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=0.05)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=0.05)
+    rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert rel <= 1e-4, rel
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
