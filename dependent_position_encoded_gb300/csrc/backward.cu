@@ -1,4 +1,4 @@
-// Backward pass of PaTH attention (plain PaTH), fp32 on the CUDA cores.
+// Backward pass of PaTH attention and PaTH-FoX, fp32 on the CUDA cores.
 //
 // The pages give no backward (review "거리에서 경로로, PaTH Attention" §9 and technical
 // summary "技術要約: PaTH Attention" §3 say the block-wise algorithm makes training
@@ -25,7 +25,9 @@
 //     dbeta_s -= (w_s . g)(w_s . x),  dw_s -= beta_s ((w_s . x) g + (w_s . g) x),
 //     gradient of x = H_s g.
 // Before both passes the fp32 UT preparation kernel recomputes q~, k~, P_b and the diagonal
-// logits from the inputs.
+// logits from the inputs. PaTH-FoX adds the bias c_i - c_j (c = cumsum of log f) to every
+// logit; it leaves dT unchanged and gives d log f_s = sum over j < s <= i of dS_ij, formed
+// from the row and column sums of dS. Every key block is visited (no early exit).
 #include "common.cuh"
 
 namespace path {
