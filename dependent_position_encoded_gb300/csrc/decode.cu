@@ -202,11 +202,10 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
         constexpr int kBatch = kPasses < 4 ? kPasses : 4;
         for (int rb = j0 + warp * 32; rb < j1; rb += kWarps * 32) {
             const int jl = rb + lane;
+            // the gate sums' load and the first key rows' loads are in flight together; the
+            // advanced sums are stored once they arrive, after those loads are issued
+            const float g_old = (jl < j1) ? grow[jl] : 0.f;
             float gl = 0.f;
-            if (jl < j1) {
-                gl = grow[jl] + lf;
-                grow[jl] = gl;
-            }
 #pragma unroll
             for (int b0 = 0; b0 < kPasses; b0 += kBatch) {
                 uint4 kraw[kBatch];
@@ -215,6 +214,10 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
                     const int j = rb + (b0 + pb) * KPW + g;
                     kraw[pb] = (j < j1) ? Vec<T>::load_raw(krow + (size_t)j * D)
                                         : make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (b0 == 0) {
+                    gl = g_old + lf;
+                    if (jl < j1) grow[jl] = gl;
                 }
 #pragma unroll
                 for (int pb = 0; pb < kBatch; ++pb) {
