@@ -14,7 +14,8 @@
 //   P0 forms the tap-scaled up-projections W'_k = diag(conv[:,k]) W_up (bf16), so that the
 //      convolution becomes part of the second contraction: y'_t = sum_k W'_k z_{t-2+k};
 //   P1 (tcgen05): [z | beta logits] = x [W_down; u]^T for 128-token tiles, streaming x
-//      through a three-stage TMA ring; the epilogue writes z (bf16) and beta;
+//      through a TMA ring (six stages and one CTA per SM where they fit, else three stages);
+//      the epilogue writes z (bf16) and beta;
 //   P2 (tcgen05): persistent over (128-token tile, two-head chunk) units, each CTA an equal
 //      contiguous run of them; per unit three accumulating contractions of
 //      z tiles loaded at rows t0, t0-1, t0-2 (a negative start row reads zeros: the causal
@@ -94,12 +95,13 @@ __global__ void producer_scale_kernel(const __nv_bfloat16 *__restrict__ w_up,
 }
 
 // ---------------------------------------------------------------- P1: z and beta
-constexpr int kP1Stages = 3;
+constexpr int kP1StagesMax = 6;  // ring depth when it fits (else 3)
 constexpr int kP1Threads = 192;  // warps 0-3: epilogue (TMEM lanes 0-127); 4: TMA; 5: MMA
 
 // Persistent: CTA c takes the 128-token tiles c, c + grid, ... The TMA ring runs across
 // tile boundaries and the accumulator is double-buffered in TMEM (acc_cols columns each),
 // so one tile's epilogue overlaps the next tile's loads and MMAs.
+template <int kP1Stages>
 __global__ void __launch_bounds__(kP1Threads, 1)
 producer_down_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_wd,
@@ -515,8 +517,8 @@ size_t producer_ws_bytes(int B, int L, int R, int H) {
     return 256 + align256((size_t)B * L * R * 2) + align256((size_t)3 * H * kD * R * 2);
 }
 
-size_t producer_down_smem(int R, int Hp) {
-    return (size_t)kP1Stages * (kRowTile + (size_t)(R + Hp) * 128) + 8 * (2 * kP1Stages + 5) + 1024;
+size_t producer_down_smem(int R, int Hp, int stages) {
+    return (size_t)stages * (kRowTile + (size_t)(R + Hp) * 128) + 8 * (2 * stages + 5) + 1024;
 }
 size_t producer_up_smem(int R) {
     return (size_t)(R / 64) * kZSlot + (size_t)(kP2Stages + 2) * kRowTile +
@@ -549,13 +551,16 @@ cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up,
     if (!map2d(&tx, x, D, BL, 128) || !map2d(&twd, w_down, D, R, R) || !map2d(&tu, u, D, H, Hp) ||
         !map3d(&tz, z, R, L, B, kZRows) || !map3d(&twk, wk, R, C, 3) || !map3d(&tw, w_out, kD, L, B * H))
         return cudaErrorInvalidValue;
-    // with 256-column accumulators (2 x 256 = all of TMEM) a second CTA on the SM would
-    // block in its TMEM allocation: ask for enough shared memory to keep it off
-    const size_t s1 = acc_cols == 128 ? producer_down_smem(R, Hp)
-                                      : std::max<size_t>(producer_down_smem(R, Hp), 120 * 1024);
+    // one CTA per SM with a deep ring (kP1StagesMax stages) when it fits in shared memory,
+    // else three stages; with 256-column accumulators (2 x 256 = all of TMEM) a second CTA
+    // on the SM would block in its TMEM allocation: ask for enough shared memory to keep it off
+    const bool deep = producer_down_smem(R, Hp, kP1StagesMax) <= 227 * 1024;
+    const size_t s1n = producer_down_smem(R, Hp, deep ? kP1StagesMax : 3);
+    const size_t s1 = (acc_cols == 128 || deep) ? s1n : std::max<size_t>(s1n, 120 * 1024);
     const size_t s2 = producer_up_smem(R);
-    if ((err = cudaFuncSetAttribute(producer_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)s1)) != cudaSuccess)
+    auto k1 = deep ? producer_down_kernel<kP1StagesMax> : producer_down_kernel<3>;
+    if ((err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) !=
+        cudaSuccess)
         return err;
     if ((err = cudaFuncSetAttribute(producer_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)s2)) != cudaSuccess)
@@ -564,7 +569,7 @@ cudaError_t launch_producer(const void *x, const void *w_down, const void *w_up,
     const long long tiles1 = (BL + 127) / 128;
     const int per_sm1 = (acc_cols == 128 && 2 * (s1 + 1024) <= 228 * 1024) ? 2 : 1;
     const unsigned g1 = (unsigned)std::min<long long>(tiles1, (long long)per_sm1 * nsm);
-    producer_down_kernel<<<g1, kP1Threads, s1, stream>>>(
+    k1<<<g1, kP1Threads, s1, stream>>>(
         tx, twd, tu, bias, beta_max, (int)BL, L, D, R, H, Hp, acc_cols, z, beta_out, status,
         limit_ns);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
