@@ -412,14 +412,29 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
 constexpr int kWarps = kThreads / 32;
 constexpr int kNS = 8;  // sweeps per warp group
 
-// out[k] = w . x[k] over the warp, for the eight vectors of a group
+// out[k] = w . x[k] over the warp, for the eight vectors of a group. A transposed butterfly:
+// at xor 16, 8 and 4 each lane keeps half of its partial sums and adds its partner's copy
+// of them, so lane l ends with the total of vector 4 bit4(l) + 2 bit3(l) + bit2(l) after
+// two more levels; eight shuffles from lanes 4k broadcast the totals (17 shuffles, not 40)
 __device__ __forceinline__ void dot8(const float2 (&x)[kNS], float2 w, float (&out)[kNS]) {
+    constexpr unsigned kAll = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    float p[kNS];
 #pragma unroll
-    for (int k = 0; k < kNS; ++k) out[k] = fmaf(w.x, x[k].x, w.y * x[k].y);
+    for (int k = 0; k < kNS; ++k) p[k] = fmaf(w.x, x[k].x, w.y * x[k].y);
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float a[4], b[2];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
+    for (int i = 0; i < 4; ++i)
+        a[i] = (h16 ? p[4 + i] : p[i]) + __shfl_xor_sync(kAll, h16 ? p[i] : p[4 + i], 16);
 #pragma unroll
-        for (int k = 0; k < kNS; ++k) out[k] += __shfl_xor_sync(0xffffffffu, out[k], o);
+    for (int i = 0; i < 2; ++i)
+        b[i] = (h8 ? a[2 + i] : a[i]) + __shfl_xor_sync(kAll, h8 ? a[i] : a[2 + i], 8);
+    float c = (h4 ? b[1] : b[0]) + __shfl_xor_sync(kAll, h4 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(kAll, c, 2);
+    c += __shfl_xor_sync(kAll, c, 1);
+#pragma unroll
+    for (int k = 0; k < kNS; ++k) out[k] = __shfl_sync(kAll, c, 4 * k);
 }
 
 template <typename T>
