@@ -316,6 +316,33 @@ __device__ __forceinline__ void mmr(const float *__restrict__ A, int lda, const 
     }
 }
 
+// acc[i][j] += sum_{k < K} A[r0 + 16i][k] * B[n0 + 16j][k]: both operands row-major (the
+// contraction index contiguous in memory), so B^T products need no transposed copy. The
+// eight lanes of a quarter warp read eight consecutive B rows (n0 = tx): at a row stride of
+// LDB = 132 floats their 16-byte pieces fall in eight distinct bank groups.
+template <int K, int NJ>
+__device__ __forceinline__ void mmrb(const float *__restrict__ A, int lda, const float *__restrict__ B,
+                                     int ldb, int r0, int n0, float (&acc)[4][NJ]) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[4], b[NJ];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) b[j] = *reinterpret_cast<const float4 *>(B + (n0 + 16 * j) * ldb + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                float t = acc[i][j];
+                t = fmaf(a[i].x, b[j].x, t);
+                t = fmaf(a[i].y, b[j].y, t);
+                t = fmaf(a[i].z, b[j].z, t);
+                acc[i][j] = fmaf(a[i].w, b[j].w, t);
+            }
+    }
+}
+
 // One CTA per (64-row query block, head): the state X = (q~_i) as rows in shared memory;
 // for key block b = ib, ib-1, ..., 0 the logits (diagonal block: the table; earlier blocks:
 // X K~_b^T), the online softmax, O += P V_b and X <- X P_b^T. Thread (ty, tx) owns rows
@@ -327,9 +354,9 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
                  int Lp, int nblk, float scale_log2) {
     extern __shared__ __align__(16) float sm[];
     float *Xr = sm;                 // X [i][c], 64 x LDB
-    float *KT = Xr + kC * LDB;      // K~_b^T [c][j], 128 x LDA
-    float *PT = KT + kD2 * LDA;     // P_b^T [c][n], 128 x LDB
-    float *Vs = PT + kD2 * LDB;     // V_b [j][c], 64 x LDB
+    float *KB = Xr + kC * LDB;      // K~_b [j][c], 64 x LDB (slot of 128 x LDA)
+    float *PB = KB + kD2 * LDA;     // P_b [n][c], 128 x LDB
+    float *Vs = PB + kD2 * LDB;     // V_b [j][c], 64 x LDB
     float *Ss = Vs + kC * LDB;      // logits [i][j] (log2 units)
     float *Pm = Ss + kC * LDA;      // probabilities [i][j]
     float *alpha_s = Pm + kC * LDA;
@@ -364,8 +391,8 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
         }
         if (b < ib) {
             const float *blk = kp + ((size_t)bh * nblk + b) * (kC + kD2) * kD2;
-            load128(KT, LDA, blk, kC, true);
-            load128(PT, LDB, blk + kC * kD2, kD2, true);
+            load128(KB, LDB, blk, kC, false);
+            load128(PB, LDB, blk + kC * kD2, kD2, false);
         } else {
             const float *tab = dg + ((size_t)bh * nblk + b) * kC * kC;
 #pragma unroll
@@ -384,20 +411,18 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
 #pragma unroll
                 for (int j = 0; j < 8; ++j) xn[i][j] = 0.f;
             }
-            mmr<kD2, 4>(Xr, LDB, KT, LDA, r0, c0, sv);
-            mmr<kD2, 8>(Xr, LDB, PT, LDB, r0, c0, xn);
+            // logits and the new state, columns tx + 16j of rows r0 + 16i
+            mmrb<kD2, 4>(Xr, LDB, KB, LDB, r0, tx, sv);
+            mmrb<kD2, 8>(Xr, LDB, PB, LDB, r0, tx, xn);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4 *>(Ss + (r0 + 16 * i) * LDA + c0) =
-                    make_float4(sv[i][0] * scale_log2, sv[i][1] * scale_log2, sv[i][2] * scale_log2,
-                                sv[i][3] * scale_log2);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) Ss[(r0 + 16 * i) * LDA + tx + 16 * j] = sv[i][j] * scale_log2;
             __syncthreads();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float *xr = Xr + (r0 + 16 * i) * LDB;
-                *reinterpret_cast<float4 *>(xr + c0) = make_float4(xn[i][0], xn[i][1], xn[i][2], xn[i][3]);
-                *reinterpret_cast<float4 *>(xr + c0 + 64) = make_float4(xn[i][4], xn[i][5], xn[i][6], xn[i][7]);
-            }
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) Xr[(r0 + 16 * i) * LDB + tx + 16 * j] = xn[i][j];
         }
         __syncthreads();
         // ---- online softmax, 4 threads per row, 16 columns each
