@@ -95,13 +95,19 @@ __device__ __forceinline__ void load_rows(float *dst, float *dst_t, const T *__r
 
 // ---------------------------------------------------------------- B1: query pass
 // Four groups of 64 threads; a group computes half (32 rows) of a 64 x 64 x 64 product as
-// 4 x 8 register tiles. Thread (ty, tx) of a group holds rows rb + ty + 8i (i < 4; rows
-// interleaved so that the four row addresses of a warp fall in distinct banks) and columns
-// 4tx .. 4tx + 3 and 32 + 4tx .. 32 + 4tx + 3 (the eight lanes of a quarter warp read one
-// contiguous 128-byte piece of B). 12 16-byte shared loads per 128 FMAs.
+// a 4 x 8 register tile per thread. Every operand stays in its stored row-major layout
+// (no transposed copies); the three forms of product are
+//   mm48:   A row-major (rows r0 + 8i), B k-major (columns col48(c0, j))     e.g. G P_b
+//   mmrb48: A and B row-major, the contraction index contiguous in both (rows r0 + 8i,
+//           columns n0 + 8j)                                                  e.g. X K~_b^T
+//   mmkk48: A and B k-major (rows m0 + i, columns col48(c0, j))               e.g. dT^T X
+// With ty, tx = the thread's row and column in its group (8 x 8), r0 = rb + ty,
+// m0 = rb + 4 ty, c0 = 4 tx and n0 = tx (rb = 0 or 32, the group's half). The lanes of a
+// quarter warp share the A rows (broadcast loads) and read eight distinct 16-byte pieces of
+// B (contiguous, or eight consecutive rows at a stride of 68 floats).
 __device__ __forceinline__ int col48(int c0, int j) { return c0 + (j < 4 ? j : 28 + j); }
 
-// acc[i][j] += sum_k A[r0 + 8i][k] * B[k][col48(c0, j)]: A row-major, B k-major
+// acc[i][j] += sum_k A[r0 + 8i][k] * B[k][col48(c0, j)]
 __device__ __forceinline__ void mm48(const float *__restrict__ A, const float *__restrict__ B,
                                      int r0, int c0, float (&acc)[4][8]) {
 #pragma unroll 2
@@ -124,6 +130,46 @@ __device__ __forceinline__ void mm48(const float *__restrict__ A, const float *_
     }
 }
 
+// acc[i][j] += sum_k A[r0 + 8i][k] * B[n0 + 8j][k]
+__device__ __forceinline__ void mmrb48(const float *__restrict__ A, const float *__restrict__ B,
+                                       int r0, int n0, float (&acc)[4][8]) {
+#pragma unroll 1
+    for (int k = 0; k < kC; k += 4) {
+        float4 a[4], b[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 8 * i) * LD + k);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = *reinterpret_cast<const float4 *>(B + (n0 + 8 * j) * LD + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float t = acc[i][j];
+                t = fmaf(a[i].x, b[j].x, t);
+                t = fmaf(a[i].y, b[j].y, t);
+                t = fmaf(a[i].z, b[j].z, t);
+                acc[i][j] = fmaf(a[i].w, b[j].w, t);
+            }
+    }
+}
+
+// acc[i][j] += sum_k A[k][m0 + i] * B[k][col48(c0, j)]
+__device__ __forceinline__ void mmkk48(const float *__restrict__ A, const float *__restrict__ B,
+                                       int m0, int c0, float (&acc)[4][8]) {
+#pragma unroll 4
+    for (int k = 0; k < kC; ++k) {
+        const float4 a = *reinterpret_cast<const float4 *>(A + k * LD + m0);
+        const float4 b0 = *reinterpret_cast<const float4 *>(B + k * LD + c0);
+        const float4 b1 = *reinterpret_cast<const float4 *>(B + k * LD + c0 + 32);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
 __device__ __forceinline__ void zero48(float (&a)[4][8]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -131,31 +177,17 @@ __device__ __forceinline__ void zero48(float (&a)[4][8]) {
         for (int j = 0; j < 8; ++j) a[i][j] = 0.f;
 }
 
-// a 4 x 8 tile into shared memory, as is (dst[r][c]) or transposed (dst[c][r])
-__device__ __forceinline__ void put48(float *dst, const float (&v)[4][8], int r0, int c0,
-                                      bool transpose) {
+// an mm48 tile (rows r0 + 8i, columns col48) into shared memory
+__device__ __forceinline__ void put48(float *dst, const float (&v)[4][8], int r0, int c0) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = r0 + 8 * i;
-        if (transpose) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) dst[col48(c0, j) * LD + r] = v[i][j];
-        } else {
-            *reinterpret_cast<float4 *>(dst + r * LD + c0) = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
-            *reinterpret_cast<float4 *>(dst + r * LD + c0 + 32) = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
-        }
+        *reinterpret_cast<float4 *>(dst + r * LD + c0) = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+        *reinterpret_cast<float4 *>(dst + r * LD + c0 + 32) = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
     }
 }
 
-// a 4 x 8 tile added into a row-major (64 floats per row) global tile
-__device__ __forceinline__ void red48(float *dst, const float (&v)[4][8], int r0, int c0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) atomicAdd(dst + (r0 + 8 * i) * kC + col48(c0, j), v[i][j]);
-}
-
-// a 4 x 8 tile stored into a row-major global tile
+// an mm48 tile stored into a row-major (64 floats per row) global tile
 __device__ __forceinline__ void st48(float *dst, const float (&v)[4][8], int r0, int c0) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -165,11 +197,27 @@ __device__ __forceinline__ void st48(float *dst, const float (&v)[4][8], int r0,
     }
 }
 
+// an mmrb48 tile (rows r0 + 8i, columns n0 + 8j) into a row-major buffer of stride ld
+__device__ __forceinline__ void put_rb(float *dst, int ld, const float (&v)[4][8], int r0, int n0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[(r0 + 8 * i) * ld + n0 + 8 * j] = v[i][j];
+}
+
+// an mmkk48 tile (rows m0 + i, columns col48) added into a row-major global tile
+__device__ __forceinline__ void red_kk(float *dst, const float (&v)[4][8], int m0, int c0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) atomicAdd(dst + (m0 + i) * kC + col48(c0, j), v[i][j]);
+}
+
 // One CTA per (query block a, head), two per SM; a runs from the last block down so that
-// the longest walks start first. Six 64 x 64 fp32 buffers (R0-R5):
-//   pass 1: R0 X [i][c], R1 dout [i][c], R2 K~_b^T then p^T [j][i], R3 P_b^T then dT^T [j][i],
-//           R4 V_b^T [c][j]
-//   pass 2: R0 X, R1 dT [i][j], R2 K~_b [j][c], R3 P_b [n][c], R4 G [i][n], R5 G^T [n][i]
+// the longest walks start first. Five 64 x 64 fp32 buffers, all row-major:
+//   pass 1: R0 X [i][c], R1 dout [i][c], R2 K~_b [j][c] then p [i][j], R3 P_b [n][c] then
+//           dT [i][j], R4 V_b [j][c]
+//   pass 2: R0 X, R1 dT [i][j], R2 K~_b [j][c], R3 P_b [n][c], R4 G [i][n]
 // Groups 0 and 1 form the logits and dout V_b^T of their rows (so p and dS stay in their
 // registers) and, in pass 2, the new G; groups 2 and 3 carry X to the next key block and,
 // in pass 2, add the dP_b terms; in between each group takes half of dk~ or dv.
@@ -188,8 +236,8 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                  const float *__restrict__ loc, const double *__restrict__ cb,
                  float *__restrict__ rsum, float *__restrict__ csum) {
     extern __shared__ __align__(16) float sm[];
-    float *R0 = sm, *R1 = R0 + BUF, *R2 = R1 + BUF, *R3 = R2 + BUF, *R4 = R3 + BUF, *R5 = R4 + BUF;
-    float *lse2 = R5 + BUF;     // per row: lse * log2(e)
+    float *R0 = sm, *R1 = R0 + BUF, *R2 = R1 + BUF, *R3 = R2 + BUF, *R4 = R3 + BUF;
+    float *lse2 = R4 + BUF;     // per row: lse * log2(e)
     float *Drow = lse2 + kC;    // per row: dout . out
     float *loci = Drow + kC;    // FoX: block-local gate sums of the query rows
     float *locj = loci + kC;    // FoX: those of the current key block
@@ -198,8 +246,9 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     const int a = nblk - 1 - (int)blockIdx.x;
     const int bh = blockIdx.y;
     const int grp = tid >> 6, lt = tid & 63, ty = lt >> 3, tx = lt & 7;
-    const int r0 = (grp & 1) * 32 + ty, c0 = 4 * tx;  // rows r0 + 8i, columns col48(c0, j)
-    const bool lead = grp < 2;                        // groups 0 and 1: logits, p, dS, G
+    const int rb = (grp & 1) * 32;
+    const int r0 = rb + ty, m0 = rb + 4 * ty, c0 = 4 * tx, n0 = tx;
+    const bool lead = grp < 2;  // groups 0 and 1: logits, p, dS, G
     const int t0 = a * kC;
     const size_t hL = (size_t)bh * L;
     const T *vh = v + hL * kD;
@@ -236,12 +285,12 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         for (int j = 0; j < 8; ++j) {
             cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 8);
             cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 16);
-            if (lane < 8) atomicAdd(csum + (size_t)bh * Lp + (size_t)kb * kC + col48(c0, j), cp[j]);
+            if (lane < 8) atomicAdd(csum + (size_t)bh * Lp + (size_t)kb * kC + n0 + 8 * j, cp[j]);
         }
     };
 
     load_rows<T>(R1, nullptr, dout + hL * kD, t0, L);
-    load_rows<T>(nullptr, R4, vh, t0, L);
+    load_rows<T>(R4, nullptr, vh, t0, L);
     __syncthreads();
 
     // ---- diagonal block: logits from the table; dT to the block pass, p^T dout to dv
@@ -249,14 +298,14 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         float dt[4][8], pr[4][8], rp[4] = {0.f, 0.f, 0.f, 0.f};
         float cp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         zero48(dt);
-        mm48(R1, R4, r0, c0, dt);  // dout_i . v_j
+        mmrb48(R1, R4, r0, n0, dt);  // dout_i . v_j
         const float *tab = dg + ((size_t)bh * nblk + a) * kBlkTile;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = r0 + 8 * i;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float p = (t0 + r < L) ? exp2f(tab[r * kC + col48(c0, j)] - lse2[r]) : 0.f;
+                const float p = (t0 + r < L) ? exp2f(tab[r * kC + n0 + 8 * j] - lse2[r]) : 0.f;
                 const float ds = p * (dt[i][j] - Drow[r]);
                 if (FOX) {
                     rp[i] += ds;
@@ -266,21 +315,21 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                 dt[i][j] = scale * ds;
             }
         }
-        st48(dTd + ((size_t)bh * nblk + a) * kBlkTile, dt, r0, c0);
+        put_rb(dTd + ((size_t)bh * nblk + a) * kBlkTile, kC, dt, r0, n0);
         if (FOX) fox_sums(rp, cp, a);
-        put48(R2, pr, r0, c0, true);  // p^T
+        put_rb(R2, LD, pr, r0, n0);  // p [i][j]
     }
     __syncthreads();
     if (!lead) {
         float acc[4][8];
         zero48(acc);
-        mm48(R2, R1, r0, c0, acc);  // sum_i p_ij dout_i[c]
+        mmkk48(R2, R1, m0, c0, acc);  // sum_i p_ij dout_i[c]
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            if (t0 + r0 + 8 * i < L)
+            if (t0 + m0 + i < L)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    atomicAdd(dv + (hL + t0 + r0 + 8 * i) * kD + col48(c0, j), acc[i][j]);
+                    atomicAdd(dv + (hL + t0 + m0 + i) * kD + col48(c0, j), acc[i][j]);
     }
 
     // ---- pass 1: right to left over key blocks, X from Q~_a
@@ -290,9 +339,9 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     const size_t pair0 = (size_t)bh * ((size_t)nblk * (nblk - 1) / 2) + (size_t)a * (a - 1) / 2;
     for (int b = a - 1; b >= 0; --b) {
         __syncthreads();
-        load_tile(R2, kp_block(b), true);
-        load_tile(R3, kp_block(b) + kBlkTile, true);
-        load_rows<T>(nullptr, R4, vh, b * kC, L);
+        load_tile(R2, kp_block(b), false);
+        load_tile(R3, kp_block(b) + kBlkTile, false);
+        load_rows<T>(R4, nullptr, vh, b * kC, L);
         if (FOX && tid < kC) locj[tid] = loc[(size_t)bh * Lp + (size_t)b * kC + tid];
         __syncthreads();
         // lead groups: acc1 = logits, acc2 = dout V_b^T; the others: acc1 = X P_b^T
@@ -300,10 +349,10 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         zero48(acc1);
         zero48(acc2);
         if (lead) {
-            mm48(R0, R2, r0, c0, acc1);
-            mm48(R1, R4, r0, c0, acc2);
+            mmrb48(R0, R2, r0, n0, acc1);
+            mmrb48(R1, R4, r0, n0, acc2);
         } else if (b > 0) {
-            mm48(R0, R3, r0, c0, acc1);
+            mmrb48(R0, R3, r0, n0, acc1);
         }
         float *st = stash + (pair0 + b) * 2 * kBlkTile;  // [X_{a,b} | dT_ab], row-major
 #pragma unroll
@@ -320,7 +369,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float x2 = acc1[i][j] * scale_log2;
-                    if (FOX) x2 += kLog2e * ((dcb + loci[r]) - locj[col48(c0, j)]);
+                    if (FOX) x2 += kLog2e * ((dcb + loci[r]) - locj[n0 + 8 * j]);
                     const float p = (t0 + r < L) ? exp2f(x2 - lse2[r]) : 0.f;
                     const float ds = p * (acc2[i][j] - Drow[r]);
                     if (FOX) {
@@ -331,38 +380,35 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
                     acc2[i][j] = scale * ds;  // acc2 now holds dT
                 }
             }
-            st48(st + kBlkTile, acc2, r0, c0);
+            put_rb(st + kBlkTile, kC, acc2, r0, n0);
             if (FOX) fox_sums(rp, cp, b);
         }
-        __syncthreads();  // K~_b^T and P_b^T are read: their buffers take p^T and dT^T
+        __syncthreads();  // K~_b and P_b are read: their buffers take p and dT
         if (lead) {
-            put48(R2, acc1, r0, c0, true);
-            put48(R3, acc2, r0, c0, true);
+            put_rb(R2, LD, acc1, r0, n0);
+            put_rb(R3, LD, acc2, r0, n0);
         }
         __syncthreads();
         {
             float acc[4][8];
             zero48(acc);
             if (lead) {  // dK~_b[j][c] += sum_i dT_ij X_ic
-                mm48(R3, R0, r0, c0, acc);
-                red48(dkt + ((size_t)bh * Lp + (size_t)b * kC) * kD, acc, r0, c0);
+                mmkk48(R3, R0, m0, c0, acc);
+                red_kk(dkt + ((size_t)bh * Lp + (size_t)b * kC) * kD, acc, m0, c0);
             } else {     // dv_j += sum_i p_ij dout_i (key block b < a is full)
-                mm48(R2, R1, r0, c0, acc);
-                red48(dv + (hL + (size_t)b * kC) * kD, acc, r0, c0);
+                mmkk48(R2, R1, m0, c0, acc);
+                red_kk(dv + (hL + (size_t)b * kC) * kD, acc, m0, c0);
             }
         }
         __syncthreads();
-        if (!lead && b > 0) put48(R0, acc1, r0, c0, false);
+        if (!lead && b > 0) put_rb(R0, LD, acc1, r0, n0);
     }
 
     // ---- pass 2: left to right, G = gradient of X_{a,b}
     float g[4][8];
     zero48(g);
     __syncthreads();
-    for (int e = tid; e < BUF; e += kThreads) {
-        R4[e] = 0.f;
-        R5[e] = 0.f;
-    }
+    for (int e = tid; e < BUF; e += kThreads) R4[e] = 0.f;
     for (int b = 0; b < a; ++b) {
         const float *st = stash + (pair0 + b) * 2 * kBlkTile;
         __syncthreads();
@@ -378,14 +424,11 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
         } else if (b > 0) {                      // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c]
             float acc[4][8];
             zero48(acc);
-            mm48(R5, R0, r0, c0, acc);
-            red48(dP + ((size_t)bh * nblk + b) * kBlkTile, acc, r0, c0);
+            mmkk48(R4, R0, m0, c0, acc);
+            red_kk(dP + ((size_t)bh * nblk + b) * kBlkTile, acc, m0, c0);
         }
         __syncthreads();
-        if (lead) {
-            put48(R4, g, r0, c0, false);
-            put48(R5, g, r0, c0, true);
-        }
+        if (lead) put48(R4, g, r0, c0);
     }
     if (lead) {
         // dQ~_a = G_{a-1} (zero for the first block)
@@ -743,7 +786,7 @@ BwdLayout bwd_layout(int B, int H, int L, bool fox) {
     return y;
 }
 
-size_t bwd_query_smem() { return (size_t)(6 * BUF + 4 * kC) * sizeof(float); }
+size_t bwd_query_smem() { return (size_t)(5 * BUF + 4 * kC) * sizeof(float); }
 size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC * kNS + 2 * kC) * sizeof(float); }
 
 // dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32; with log_f (PaTH-FoX) also dlogf
