@@ -16,9 +16,10 @@
 // the inverse of a triangular matrix restricted to a contiguous diagonal range
 // is the inverse of that range's sub-block.
 //
-// One CTA of 256 threads per (block, head). Every product is a 64 x 64 x 64
-// contraction over shared memory with both operands stored k-major, each thread
-// owning a 4 x 4 output tile.
+// One CTA of 256 threads per (block, head), two per SM (six 64 x 64 buffers). Every product
+// is a 64 x 64 x 64 contraction over shared memory with W, Q, K and A kept row-major only:
+// contractions over the head dimension read both operands as rows, the others read A as
+// rows or both operands k-major; each thread owns a 4 x 4 output tile.
 #include "common.cuh"
 
 namespace path {
@@ -53,6 +54,81 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 }
 
+// Products whose operands are both stored with the contraction index contiguous
+// (A[m][k], B[n][k]; e.g. W W^T from W alone) use an interleaved thread tile: rows
+// ty + 16i, columns tx + 16j, so that the eight lanes of a quarter warp read eight
+// consecutive B rows, whose 16-byte pieces fall in distinct bank groups at a row stride of
+// 68 floats. acc[i][j] += sum_k A[ty + 16i][k] * B[tx + 16j][k].
+__device__ __forceinline__ void mm_rows(const float *__restrict__ A, const float *__restrict__ B,
+                                        int ty, int tx, float (&acc)[4][4]) {
+#pragma unroll 2
+    for (int k = 0; k < kC; k += 4) {
+        float4 a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (ty + 16 * i) * LD + k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4 *>(B + (tx + 16 * j) * LD + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float t = acc[i][j];
+                t = fmaf(a[i].x, b[j].x, t);
+                t = fmaf(a[i].y, b[j].y, t);
+                t = fmaf(a[i].z, b[j].z, t);
+                acc[i][j] = fmaf(a[i].w, b[j].w, t);
+            }
+    }
+}
+
+// The interleaved tile from k-major operands: acc[i][j] += sum_k X[k][ty + 16i] Y[k][tx + 16j]
+__device__ __forceinline__ void mm_kk_il(const float *__restrict__ X, const float *__restrict__ Y,
+                                         int ty, int tx, float (&acc)[4][4]) {
+#pragma unroll 4
+    for (int k = 0; k < kC; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            av[i] = X[k * LD + ty + 16 * i];
+            bv[i] = Y[k * LD + tx + 16 * i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+// A row-major, B k-major (standard tile): acc[i][j] += sum_k A[m0 + i][k] * B[k][n0 + j]
+__device__ __forceinline__ void mm_rowa(const float *__restrict__ A, const float *__restrict__ B,
+                                        int m0, int n0, float (&acc)[4][4]) {
+#pragma unroll 2
+    for (int k = 0; k < kC; k += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (m0 + i) * LD + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4 b = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + n0);
+            const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+            }
+        }
+    }
+}
+
+// Writes an interleaved tile (rows ty + 16i, cols tx + 16j) into buffer Z as Z[m][n].
+__device__ __forceinline__ void store_il(float *Z, int ty, int tx, const float (&acc)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Z[(ty + 16 * i) * LD + tx + 16 * j] = acc[i][j];
+}
+
 // Writes acc (rows m0.., cols n0..) into buffer Z as Z[m][n].
 __device__ __forceinline__ void store_rm(float *Z, int m0, int n0, const float (&acc)[4][4]) {
 #pragma unroll
@@ -67,13 +143,6 @@ template <>
 __device__ __forceinline__ void store_row4<float>(float *dst, const float *v) {
     *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
 }
-template <>
-__device__ __forceinline__ void store_row4<__nv_bfloat16>(__nv_bfloat16 *dst, const float *v) {
-    uint2 u;
-    u.x = pack_bf16x2(v[0], v[1]);
-    u.y = pack_bf16x2(v[2], v[3]);
-    *reinterpret_cast<uint2 *>(dst) = u;
-}
 
 // T: input element type; TO: element type of q~, k~ and P_b (the backward recomputes them
 // in fp32 from bf16 inputs)
@@ -85,12 +154,10 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
                   float *__restrict__ dg, uint32_t *status) {
     extern __shared__ __align__(16) float sm[];
     float *Wr = sm;            // W[s][c]
-    float *Wt = Wr + BUF;      // W[c][s]
-    float *Qt = Wt + BUF;      // Q[c][i]
-    float *Kt = Qt + BUF;      // K[c][j]
-    float *Ar = Kt + BUF;      // A[s][u]
-    float *At = Ar + BUF;      // A[u][s]
-    float *X = At + BUF;       // scratch
+    float *Qr = Wr + BUF;      // Q[i][c]
+    float *Kr = Qr + BUF;      // K[j][c]
+    float *Ar = Kr + BUF;      // A[s][u]
+    float *X = Ar + BUF;       // scratch
     float *Y = X + BUF;        // scratch
     float *bs = Y + BUF;       // beta[64]
     float *lc = bs + kC;       // block-local inclusive cumsum of log f [64]
@@ -102,7 +169,7 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     const size_t head = (size_t)bh * L;
     if (blk == 0 && bh == 0 && tid == 0 && status) *status = 0u;
 
-    // ---- load W, Q, K (fp32, both layouts for W), beta; padded tokens are zero. Four
+    // ---- load W, Q, K (fp32, row-major), beta; padded tokens are zero. Four
     // elements per thread and step, all of a thread's loads issued before the first store.
     {
         constexpr int kIt = kC * kD / 4 / kPrepThreads;
@@ -123,13 +190,9 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         for (int it = 0; it < kIt; ++it) {
             const int e = 4 * (tid + it * kPrepThreads), s = e / kD, c = e % kD;
             *reinterpret_cast<float4 *>(Wr + s * LD + c) = make_float4(wv[it][0], wv[it][1], wv[it][2], wv[it][3]);
+            *reinterpret_cast<float4 *>(Qr + s * LD + c) = make_float4(qv[it][0], qv[it][1], qv[it][2], qv[it][3]);
+            *reinterpret_cast<float4 *>(Kr + s * LD + c) = make_float4(kv[it][0], kv[it][1], kv[it][2], kv[it][3]);
             *reinterpret_cast<float4 *>(Ar + s * LD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                Wt[(c + j) * LD + s] = wv[it][j];
-                Qt[(c + j) * LD + s] = qv[it][j];
-                Kt[(c + j) * LD + s] = kv[it][j];
-            }
         }
     }
     if (tid < kC) {
@@ -160,8 +223,8 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
 
     // ---- G = W W^T -> X (row-major G[s][u])
     zero(acc);
-    mm_acc(Wt, Wt, m0, n0, acc);
-    store_rm(X, m0, n0, acc);
+    mm_rows(Wr, Wr, ty, tx, acc);
+    store_il(X, ty, tx, acc);
     __syncthreads();
 
     // ---- A = (I + D N)^{-1} D, one column per group of 4 threads.
@@ -183,34 +246,29 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         }
     }
     __syncthreads();
-    for (int e = tid; e < kC * kC; e += kPrepThreads) {
-        const int s = e / kC, u = e % kC;
-        At[u * LD + s] = Ar[s * LD + u];
-    }
-    __syncthreads();
 
     // ---- Lq^T -> X ([u][i], u <= i), Rk^T -> Y ([s][j], s > j)
     zero(acc);
-    mm_acc(Wt, Qt, m0, n0, acc);
+    mm_rows(Wr, Qr, ty, tx, acc);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (m0 + i > n0 + j) acc[i][j] = 0.f;
-    store_rm(X, m0, n0, acc);
+            if (ty + 16 * i > tx + 16 * j) acc[i][j] = 0.f;
+    store_il(X, ty, tx, acc);
     zero(acc);
-    mm_acc(Wt, Kt, m0, n0, acc);
+    mm_rows(Wr, Kr, ty, tx, acc);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (m0 + i <= n0 + j) acc[i][j] = 0.f;
-    store_rm(Y, m0, n0, acc);
+            if (ty + 16 * i <= tx + 16 * j) acc[i][j] = 0.f;
+    store_il(Y, ty, tx, acc);
     __syncthreads();
 
     // ---- Qhat^T[s][i] = sum_u A[s][u] Lq^T[u][i]  (in place in X)
     zero(acc);
-    mm_acc(At, X, m0, n0, acc);
+    mm_rowa(Ar, X, m0, n0, acc);
     __syncthreads();
     store_rm(X, m0, n0, acc);
     __syncthreads();
@@ -218,25 +276,24 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     const size_t blk_base = (size_t)bh * nblk + blk;
 
     // ---- diagonal-block logits: Dg[i][j] = scale_log2 * (q_i.k_j - sum_s Qhat[i][s] Rk[j][s])
+    // (interleaved tile: rows ty + 16i, columns tx + 16j)
     {
         float qk[4][4], corr[4][4];
         zero(qk);
         zero(corr);
-        mm_acc(Qt, Kt, m0, n0, qk);
-        mm_acc(X, Y, m0, n0, corr);
+        mm_rows(Qr, Kr, ty, tx, qk);
+        mm_kk_il(X, Y, ty, tx, corr);
         float *out = dg + blk_base * kC * kC;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float v[4];
-            const int ii = m0 + i;
+            const int ii = ty + 16 * i;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int jj = n0 + j;
+                const int jj = tx + 16 * j;
                 float x = scale_log2 * (qk[i][j] - corr[i][j]);
                 if (log_f != nullptr) x += kLog2e * (lc[ii] - lc[jj]);
-                v[j] = (jj <= ii && t0 + jj < L) ? x : -INFINITY;
+                out[ii * kC + jj] = (jj <= ii && t0 + jj < L) ? x : -INFINITY;
             }
-            store_row4<float>(out + ii * kC + n0, v);
         }
     }
 
@@ -249,7 +306,7 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         for (int i = 0; i < 4; ++i) {
             float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = Qt[(n0 + j) * LD + m0 + i] - acc[i][j];
+            for (int j = 0; j < 4; ++j) v[j] = Qr[(m0 + i) * LD + n0 + j] - acc[i][j];
             store_row4<TO>(out + (m0 + i) * kD + n0, v);
         }
     }
@@ -271,11 +328,11 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         for (int i = 0; i < 4; ++i) {
             float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = Kt[(n0 + j) * LD + m0 + i] - acc[i][j];
+            for (int j = 0; j < 4; ++j) v[j] = Kr[(m0 + i) * LD + n0 + j] - acc[i][j];
             store_row4<TO>(kp_blk + (m0 + i) * kD + n0, v);
         }
         zero(acc);
-        mm_acc(At, Wr, m0, n0, acc);
+        mm_rowa(Ar, Wr, m0, n0, acc);
         store_rm(X, m0, n0, acc);
     }
     __syncthreads();
@@ -297,7 +354,7 @@ ut_prepare_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
 
 }  // namespace
 
-size_t ut_prepare_smem_bytes() { return (size_t)(8 * BUF + 2 * kC) * sizeof(float); }
+size_t ut_prepare_smem_bytes() { return (size_t)(6 * BUF + 2 * kC) * sizeof(float); }
 
 template <typename T>
 cudaError_t launch_ut_prepare(const void *q, const void *k, const void *w, const float *beta,
