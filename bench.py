@@ -484,6 +484,9 @@ PROFILE_CASES = {
     "producer": pi.ProducerWorkload("path_wbeta_bf16_B8L4096D2048R64H32", 8, 4096, 2048, 64, 32, 6),
     # the backward leg's own workload (1.3 GB of workspace, stash larger than L2)
     "bwd": pi.BF16_L2048,
+    # the head-size-128 forward leg's own workload (FP32 ALU-bound kernels)
+    "fwd_d128": pi.FwdWorkload("path_fwd_bf16_B4H8L2048_d128", 4, 8, 2048, 128, torch.bfloat16, 12,
+                               pi.BETA_CLIP, False),
 }
 
 
@@ -613,7 +616,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
-    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd"],
+    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd", "fwd_d128"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
