@@ -754,6 +754,13 @@ def main():
                                          "frac": d_ach / FP32_ALU_TFLOPS, "traffic": None,
                                          "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
         del xd
+        # PaTH-FoX at head size 128 (every key block visited: no early exit at d = 128)
+        xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, fox=True,
+                                device=dev)
+        f_tot, _, _ = time_forward(pa, xd, 3, 3, fox=True)
+        line["fwd_d128"]["fox_ms_per_step"] = f_tot / 3
+        line["fwd_d128"]["fox_tokens_per_s"] = 4 * 2048 / (f_tot / 3 * 1e-3)
+        del xd
         torch.cuda.empty_cache()
         fbwd = time_bwd(pa, pi.BF16_L2048, fox=True)
         ach = fbwd["query_pass_flops"] / (fbwd["ms_per_step"] * 1e-3) / 1e12

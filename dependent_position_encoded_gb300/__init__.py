@@ -281,7 +281,7 @@ def path_fox_fwd(q, k, v, w, beta, log_f, out=None, lse=True, scale=None, worksp
         raise ValueError("log_f must be (B, H, L) float32")
     out, lse = _outputs(q, out, lse, B, H, L)
     if workspace is None:
-        workspace = new_workspace(OP_FOX_FWD, B, H, L, dt, q.device)
+        workspace = new_workspace(OP_FOX_FWD, B, H, L, dt, q.device, d=d)
     _check(_load().path_fox_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
                                 _ptr(out), _ptr(lse), B, H, L, d, dt, _scale(scale, d),
                                 _ptr(workspace), workspace.numel(), _stream(stream, q.device)),

@@ -14,6 +14,7 @@ constexpr int kD = 64;      // head size (the only one supported)
 constexpr int kC = 64;      // tokens per UT block
 constexpr int kTile = 128;  // query rows per tensor-core tile (two UT blocks)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr double kLog2eD = 1.4426950408889634;
 
 // Status word codes written by kernels into the workspace header.
 constexpr uint32_t kStatusTimeout = 7u;
@@ -44,9 +45,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Workspace of the d = 128 forward (defined in fwd_d128.cu).
 struct D128Layout {
     int BH, nblk, Lp;
-    size_t off_qt, off_kp, off_dg, total;
+    size_t off_qt, off_kp, off_dg;
+    size_t off_lc, off_tail, off_tot, total;  // PaTH-FoX only (else all equal to total)
 };
-D128Layout d128_layout(int B, int H, int L);
+D128Layout d128_layout(int B, int H, int L, bool fox);
 
 // Workspace of the backward pass (defined in backward.cu).
 struct BwdLayout {

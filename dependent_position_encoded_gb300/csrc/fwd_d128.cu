@@ -7,6 +7,17 @@
 // and the diagonal-block logits; then per 64-row query block a right-to-left scan over key
 // blocks with online softmax, carrying X <- X P_b^T. Contractions over the head dimension
 // run to 128; the triangular solve is unchanged (64 x 64).
+//
+// PaTH-FoX (technical summary §2 "拡張: PaTH-FoX"; review §4): every logit also takes the
+// forget-gate bias sum_{s=j+1..i} log f_s = c_i - c_j, in log2 units like the logits. The
+// preparation forms, per block and in fp64, the inclusive in-block sums lc_i of
+// log2(e) log f_s and the block total T_b; the diagonal table takes lc_i - lc_j. For a key
+// j of an earlier block b the scan splits the bias as
+//     c_i - c_j = [lc_i + sum_{b < b' < ib} T_b'] + [T_b - lc_j],
+// a per-row term with an fp64 running sum (exact where the weights are not negligible:
+// its rounding grows with the bias itself) and the key's tail sum within its block, so no
+// difference of two large prefix sums is ever taken. There is no early exit at d = 128:
+// the scan visits every key block.
 #include "common.cuh"
 
 namespace path {
@@ -101,11 +112,13 @@ template <> __device__ __forceinline__ void put4<__nv_bfloat16>(__nv_bfloat16 *d
 // ---------------------------------------------------------------- preparation
 // One CTA of 256 threads per (block, head). Shared memory: W [s][c] and its transpose, Q^T,
 // K^T (the 128-wide operands), and four 64 x 64 buffers (A, A^T, two scratch).
-template <typename T>
+template <typename T, bool FOX>
 __global__ void __launch_bounds__(kThreads)
 prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
-                 const float *__restrict__ beta, int L, int Lp, int nblk, float scale_log2,
-                 float *__restrict__ qt, float *__restrict__ kp, float *__restrict__ dg) {
+                 const float *__restrict__ beta, const float *__restrict__ log_f, int L, int Lp,
+                 int nblk, float scale_log2, float *__restrict__ qt, float *__restrict__ kp,
+                 float *__restrict__ dg, float *__restrict__ lc, float *__restrict__ tail,
+                 double *__restrict__ tot) {
     extern __shared__ __align__(16) float sm[];
     float *Wr = sm;                  // W [s][c], 64 x LDB
     float *Wt = Wr + kC * LDB;       // W^T [c][s], 128 x LDA
@@ -116,6 +129,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     float *X = At + kC * LDA;        // scratch 64 x 64
     float *Y = X + kC * LDA;         // scratch 64 x 64
     float *bs = Y + kC * LDA;        // beta [64]
+    double *lcs = reinterpret_cast<double *>(bs + kC);  // FoX: in-block sums lc [64], fp64
 
     const int tid = threadIdx.x, blk = blockIdx.x, bh = blockIdx.y;
     const int t0 = blk * kC;
@@ -151,7 +165,27 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     }
     for (int e = tid; e < kC * kC; e += kThreads) Ar[(e / kC) * LDA + e % kC] = 0.f;
     if (tid < kC) bs[tid] = (t0 + tid < L) ? beta[head + t0 + tid] : 0.f;
+    if (FOX && tid < 32) {
+        // inclusive prefix of log2(e) log f over the block (tokens past L add 0): lane l
+        // holds tokens 2l and 2l + 1 and scans the pair sums over the warp
+        const double f0 = (t0 + 2 * tid < L) ? (double)log_f[head + t0 + 2 * tid] * kLog2eD : 0.0;
+        const double f1 = (t0 + 2 * tid + 1 < L) ? (double)log_f[head + t0 + 2 * tid + 1] * kLog2eD : 0.0;
+        double x = f0 + f1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, x, o);
+            if (tid >= o) x += y;
+        }
+        lcs[2 * tid] = x - f1;
+        lcs[2 * tid + 1] = x;
+    }
     __syncthreads();
+    if (FOX && tid < kC) {
+        const size_t tok = (size_t)bh * Lp + t0 + tid;
+        lc[tok] = (float)lcs[tid];
+        tail[tok] = (float)(lcs[kC - 1] - lcs[tid]);
+        if (tid == 0) tot[(size_t)bh * nblk + blk] = lcs[kC - 1];
+    }
 
     const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
     float acc[4][4];
@@ -220,7 +254,8 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int ii = m0 + i, jj = n0 + j;
-                v[j] = (jj <= ii && t0 + jj < L) ? scale_log2 * (qk[i][j] - corr[i][j]) : -INFINITY;
+                const float bias = FOX ? (float)(lcs[ii] - lcs[jj]) : 0.f;
+                v[j] = (jj <= ii && t0 + jj < L) ? scale_log2 * (qk[i][j] - corr[i][j]) + bias : -INFINITY;
             }
             put4<float>(out + (m0 + i) * kC + n0, v);
         }
@@ -347,11 +382,14 @@ __device__ __forceinline__ void mmrb(const float *__restrict__ A, int lda, const
 // for key block b = ib, ib-1, ..., 0 the logits (diagonal block: the table; earlier blocks:
 // X K~_b^T), the online softmax, O += P V_b and X <- X P_b^T. Thread (ty, tx) owns rows
 // ty + 16i (i < 4) and, of the 128-wide results, columns 4tx .. 4tx + 3 and 64 + 4tx ..
-template <typename T>
+// FOX: the forget-gate bias of every earlier block's logits, [row term] + [key tail].
+template <typename T, bool FOX>
 __global__ void __launch_bounds__(kThreads, 1)
 scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const float *__restrict__ kp,
-                 const float *__restrict__ dg, T *__restrict__ out, float *__restrict__ lse, int L,
-                 int Lp, int nblk, float scale_log2) {
+                 const float *__restrict__ dg, const float *__restrict__ lc,
+                 const float *__restrict__ tail, const double *__restrict__ tot,
+                 T *__restrict__ out, float *__restrict__ lse, int L, int Lp, int nblk,
+                 float scale_log2) {
     extern __shared__ __align__(16) float sm[];
     float *Xr = sm;                 // X [i][c], 64 x LDB
     float *KB = Xr + kC * LDB;      // K~_b [j][c], 64 x LDB (slot of 128 x LDA)
@@ -360,6 +398,8 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
     float *Ss = Vs + kC * LDB;      // logits [i][j] (log2 units)
     float *Pm = Ss + kC * LDA;      // probabilities [i][j]
     float *alpha_s = Pm + kC * LDA;
+    float *rbias = alpha_s + kC;    // FoX: row terms lc_i + sum of the blocks in between
+    float *kbias = rbias + kC;      // FoX: tail sums T_b - lc_j of the keys of block b
 
     const int tid = threadIdx.x, ib = blockIdx.x, bh = blockIdx.y;
     if (ib * kC >= L) return;
@@ -373,6 +413,9 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
+    // FoX: row lc_i (threads 0-63) and the fp64 sum of the totals of blocks b + 1 .. ib - 1
+    const float lci = (FOX && tid < kC) ? lc[(size_t)bh * Lp + (size_t)ib * kC + tid] : 0.f;
+    double between = 0.0;
     for (int b = ib; b >= 0; --b) {
         __syncthreads();
         {
@@ -391,6 +434,14 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
         }
         if (b < ib) {
             const float *blk = kp + ((size_t)bh * nblk + b) * (kC + kD2) * kD2;
+            if (FOX) {
+                if (tid < kC) {
+                    rbias[tid] = (float)((double)lci + between);
+                    between += tot[(size_t)bh * nblk + b];
+                } else if (tid < 2 * kC) {
+                    kbias[tid - kC] = tail[(size_t)bh * Lp + (size_t)b * kC + tid - kC];
+                }
+            }
             load128(KB, LDB, blk, kC, false);
             load128(PB, LDB, blk + kC * kD2, kD2, false);
         } else {
@@ -417,7 +468,10 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) Ss[(r0 + 16 * i) * LDA + tx + 16 * j] = sv[i][j] * scale_log2;
+                for (int j = 0; j < 4; ++j) {
+                    const float bias = FOX ? rbias[r0 + 16 * i] + kbias[tx + 16 * j] : 0.f;
+                    Ss[(r0 + 16 * i) * LDA + tx + 16 * j] = fmaf(sv[i][j], scale_log2, bias);
+                }
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -486,17 +540,19 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
 }
 
 size_t prep_d128_smem() {
-    return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + kC) * sizeof(float);
+    return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + kC) * sizeof(float) + kC * sizeof(double);
 }
 size_t scan_d128_smem() {
-    return (size_t)(2 * kC * LDB + kD2 * LDA + kD2 * LDB + 2 * kC * LDA + kC) * sizeof(float);
+    return (size_t)(2 * kC * LDB + kD2 * LDA + kD2 * LDB + 2 * kC * LDA + 3 * kC) * sizeof(float);
 }
 
 }  // namespace
 
 // Workspace of the d = 128 forward: 256-byte status header, fp32 q~ (BH, Lp, 128), per block
-// [k~ (64 rows); P_b (128 rows)] (BH, nblk, 192, 128), diagonal logits (BH, nblk, 64, 64).
-D128Layout d128_layout(int B, int H, int L) {
+// [k~ (64 rows); P_b (128 rows)] (BH, nblk, 192, 128), diagonal logits (BH, nblk, 64, 64);
+// PaTH-FoX adds the in-block sums lc and the tail sums (BH, Lp) fp32 and the block totals
+// (BH, nblk) fp64, all in log2 units.
+D128Layout d128_layout(int B, int H, int L, bool fox) {
     D128Layout y;
     y.BH = B * H;
     y.nblk = (L + kC - 1) / kC;
@@ -509,51 +565,68 @@ D128Layout d128_layout(int B, int H, int L) {
     off = align256(off + bh * y.nblk * (kC + kD2) * kD2 * 4);
     y.off_dg = off;
     off = align256(off + bh * y.nblk * kC * kC * 4);
+    y.off_lc = y.off_tail = y.off_tot = off;
+    if (fox) {
+        off = align256(off + bh * y.Lp * 4);
+        y.off_tail = off;
+        off = align256(off + bh * y.Lp * 4);
+        y.off_tot = off;
+        off = align256(off + bh * y.nblk * 8);
+    }
     y.total = off;
     return y;
 }
 
+// log_f non-null: PaTH-FoX (the workspace laid out with the FoX sums).
 template <typename T>
 cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const float *beta,
-                             int B, int H, int L, float scale, void *ws, cudaStream_t stream) {
-    const D128Layout y = d128_layout(B, H, L);
+                             const float *log_f, int B, int H, int L, float scale, void *ws,
+                             cudaStream_t stream) {
+    const bool fox = log_f != nullptr;
+    const D128Layout y = d128_layout(B, H, L, fox);
     char *base = static_cast<char *>(ws);
     cudaError_t e;
     if ((e = cudaMemsetAsync(base, 0, 4, stream)) != cudaSuccess) return e;
     const size_t sm = prep_d128_smem();
-    if ((e = cudaFuncSetAttribute(prep_d128_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm)) != cudaSuccess)
+    auto kern = fox ? prep_d128_kernel<T, true> : prep_d128_kernel<T, false>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
+        cudaSuccess)
         return e;
-    prep_d128_kernel<T><<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
-        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta, L,
-        y.Lp, y.nblk, scale * kLog2e, reinterpret_cast<float *>(base + y.off_qt),
-        reinterpret_cast<float *>(base + y.off_kp), reinterpret_cast<float *>(base + y.off_dg));
+    kern<<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
+        log_f, L, y.Lp, y.nblk, scale * kLog2e, reinterpret_cast<float *>(base + y.off_qt),
+        reinterpret_cast<float *>(base + y.off_kp), reinterpret_cast<float *>(base + y.off_dg),
+        reinterpret_cast<float *>(base + y.off_lc), reinterpret_cast<float *>(base + y.off_tail),
+        reinterpret_cast<double *>(base + y.off_tot));
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_scan_d128(const void *v, void *out, float *lse, int B, int H, int L, float scale,
-                             void *ws, cudaStream_t stream) {
-    const D128Layout y = d128_layout(B, H, L);
+cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int B, int H, int L,
+                             float scale, void *ws, cudaStream_t stream) {
+    const D128Layout y = d128_layout(B, H, L, fox);
     const char *base = static_cast<const char *>(ws);
     cudaError_t e;
     const size_t sm = scan_d128_smem();
-    if ((e = cudaFuncSetAttribute(scan_d128_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sm)) != cudaSuccess)
+    auto kern = fox ? scan_d128_kernel<T, true> : scan_d128_kernel<T, false>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
+        cudaSuccess)
         return e;
-    scan_d128_kernel<T><<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
+    kern<<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
         static_cast<const T *>(v), reinterpret_cast<const float *>(base + y.off_qt),
         reinterpret_cast<const float *>(base + y.off_kp), reinterpret_cast<const float *>(base + y.off_dg),
-        static_cast<T *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e);
+        reinterpret_cast<const float *>(base + y.off_lc), reinterpret_cast<const float *>(base + y.off_tail),
+        reinterpret_cast<const double *>(base + y.off_tot), static_cast<T *>(out), lse, L, y.Lp,
+        y.nblk, scale * kLog2e);
     return cudaGetLastError();
 }
 
 #define PATH_D128_INST(T)                                                                        \
     template cudaError_t launch_prep_d128<T>(const void *, const void *, const void *,           \
-                                             const float *, int, int, int, float, void *,        \
-                                             cudaStream_t);                                      \
-    template cudaError_t launch_scan_d128<T>(const void *, void *, float *, int, int, int, float, \
-                                             void *, cudaStream_t);
+                                             const float *, const float *, int, int, int, float, \
+                                             void *, cudaStream_t);                              \
+    template cudaError_t launch_scan_d128<T>(const void *, void *, float *, bool, int, int, int,  \
+                                             float, void *, cudaStream_t);
 PATH_D128_INST(float)
 PATH_D128_INST(__nv_bfloat16)
 #undef PATH_D128_INST

@@ -46,10 +46,11 @@ cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const v
                             void *ws, cudaStream_t stream);
 template <typename T>
 cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const float *beta,
-                             int B, int H, int L, float scale, void *ws, cudaStream_t stream);
+                             const float *log_f, int B, int H, int L, float scale, void *ws,
+                             cudaStream_t stream);
 template <typename T>
-cudaError_t launch_scan_d128(const void *v, void *out, float *lse, int B, int H, int L, float scale,
-                             void *ws, cudaStream_t stream);
+cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int B, int H, int L,
+                             float scale, void *ws, cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len, int d);
 template <typename T>
@@ -86,9 +87,9 @@ path_status check_sizes(int B, int H, int L, int d, int dtype) {
     return PATH_OK;
 }
 
-// The plain forward also takes d = 128 (fp32 CUDA-core kernels); PaTH-FoX takes 64 only.
-path_status check_fwd_sizes(int B, int H, int L, int d, int dtype, bool fox) {
-    return check_sizes(B, H, L, (d == 128 && !fox) ? kD : d, dtype);
+// The forward (PaTH and PaTH-FoX) also takes d = 128 (fp32 CUDA-core kernels).
+path_status check_fwd_sizes(int B, int H, int L, int d, int dtype) {
+    return check_sizes(B, H, L, d == 128 ? kD : d, dtype);
 }
 
 // Decode works on head sizes 64 and 128.
@@ -108,7 +109,7 @@ path_status check_ws(void *ws, size_t ws_bytes, size_t need) {
 path_status prepare_impl(const void *q, const void *k, const void *w, const float *beta,
                          const float *log_f, bool fox, int B, int H, int L, int d, int dtype,
                          float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    path_status st = check_fwd_sizes(B, H, L, d, dtype, fox);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype);
     if (st != PATH_OK) return st;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
     if ((long long)B * H * L == 0) return PATH_OK;
@@ -117,10 +118,11 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
         (fox && !aligned(log_f, 16)))
         return PATH_ERR_ALIGN;
     if (d == 128) {
-        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L).total)) != PATH_OK) return st;
+        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L, fox).total)) != PATH_OK) return st;
+        const float *lf = fox ? log_f : nullptr;
         return from_cuda(dtype == PATH_BF16
-                             ? launch_prep_d128<__nv_bfloat16>(q, k, w, beta, B, H, L, scale, ws, stream)
-                             : launch_prep_d128<float>(q, k, w, beta, B, H, L, scale, ws, stream));
+                             ? launch_prep_d128<__nv_bfloat16>(q, k, w, beta, lf, B, H, L, scale, ws, stream)
+                             : launch_prep_d128<float>(q, k, w, beta, lf, B, H, L, scale, ws, stream));
     }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
@@ -139,17 +141,17 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
 
 path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int H, int L, int d,
                       int dtype, float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    path_status st = check_fwd_sizes(B, H, L, d, dtype, fox);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype);
     if (st != PATH_OK) return st;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
     if ((long long)B * H * L == 0) return PATH_OK;
     if (!v || !out) return PATH_ERR_NULL;
     if (!aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16))) return PATH_ERR_ALIGN;
     if (d == 128) {
-        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L).total)) != PATH_OK) return st;
+        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L, fox).total)) != PATH_OK) return st;
         return from_cuda(dtype == PATH_BF16
-                             ? launch_scan_d128<__nv_bfloat16>(v, out, lse, B, H, L, scale, ws, stream)
-                             : launch_scan_d128<float>(v, out, lse, B, H, L, scale, ws, stream));
+                             ? launch_scan_d128<__nv_bfloat16>(v, out, lse, fox, B, H, L, scale, ws, stream)
+                             : launch_scan_d128<float>(v, out, lse, fox, B, H, L, scale, ws, stream));
     }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
@@ -201,8 +203,8 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
     switch (op) {
         case PATH_OP_FWD:
         case PATH_OP_FOX_FWD:
-            if (check_fwd_sizes(B, H, L, d, dtype, op == PATH_OP_FOX_FWD) != PATH_OK) return 0;
-            if (d == 128) return d128_layout(B, H, L).total;
+            if (check_fwd_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+            if (d == 128) return d128_layout(B, H, L, op == PATH_OP_FOX_FWD).total;
             return fwd_layout(B, H, L, elt_bytes(dtype), op == PATH_OP_FOX_FWD).total;
         default: break;
     }
@@ -272,7 +274,7 @@ path_status path_attn_fwd(const void *q, const void *k, const void *v, const voi
                           int dtype, float scale, void *ws, size_t ws_bytes, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // every argument of both stages is checked before the first launch
-    path_status st = check_fwd_sizes(B, H, L, d, dtype, false);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype);
     if (st != PATH_OK) return st;
     if ((long long)B * H * L > 0) {
         if (!v || !out) return PATH_ERR_NULL;
@@ -289,7 +291,7 @@ path_status path_fox_fwd(const void *q, const void *k, const void *v, const void
                          int H, int L, int d, int dtype, float scale, void *ws, size_t ws_bytes,
                          void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    path_status st = check_sizes(B, H, L, d, dtype);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype);
     if (st != PATH_OK) return st;
     if ((long long)B * H * L > 0) {
         if (!v || !out || !log_f) return PATH_ERR_NULL;

@@ -14,10 +14,11 @@
  *  - Device pointers, contiguous row-major: q, k, v, w, out are (B, H, L, d);
  *    beta, log_f, lse are (B, H, L) fp32. Element type of q, k, v, w, out and of
  *    the decode caches is given by `dtype` (PATH_F32 or PATH_BF16).
- *  - d must be 64 (the head size the pages benchmark); the plain forward (path_attn_fwd,
- *    path_fwd_prepare, path_fwd_scan) and the decode steps also take d = 128 (the larger
- *    head the pages mention; the forward then runs on fp32 CUDA-core kernels for either
- *    dtype). Anything else returns PATH_ERR_SHAPE.
+ *  - d must be 64 (the head size the pages benchmark); the forward (path_attn_fwd,
+ *    path_fox_fwd, path_fwd_prepare, path_fwd_scan) and the decode steps also take
+ *    d = 128 (the larger head the pages mention; the forward then runs on fp32 CUDA-core
+ *    kernels for either dtype, and PaTH-FoX visits every key block: no early exit).
+ *    Anything else returns PATH_ERR_SHAPE.
  *  - Every tensor pointer and the workspace must be 16-byte aligned
  *    (PATH_ERR_ALIGN); the workspace must be 256-byte aligned.
  *  - The caller owns every buffer, the workspace included. The library
@@ -103,7 +104,9 @@ path_status path_attn_fwd(const void *q, const void *k, const void *v, const voi
  * is at most |scale| |q~_i| |k~_j|; the scan of a 128-row tile stops above the key
  * blocks whose every key, bias included, weighs below e^-40 relative to the largest
  * logit of the row's own block (with the bound doubled for rounding). See
- * path_fox_first_blocks.
+ * path_fox_first_blocks. At d = 128 there is no early exit (the scan visits every key
+ * block), and the bias of a key in an earlier block is formed from in-block prefix sums,
+ * block totals summed in fp64 and the key's in-block tail sum.
  */
 path_status path_fox_fwd(const void *q, const void *k, const void *v, const void *w,
                          const float *beta, const float *log_f, void *out, float *lse,
@@ -183,6 +186,8 @@ path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, 
  * path_workspace_bytes(PATH_OP_FOX_FWD, ...). The pages give no such call: it exposes
  * the rule of review "거리에서 경로로, PaTH Attention" §4 / technical summary
  * "技術要約: PaTH Attention" §2 (the gate makes distant keys vanish) for testing.
+ * d = 64 only (the d = 128 forward has no early exit): other head sizes return
+ * PATH_ERR_SHAPE.
  */
 path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H, int L,
                                   int d, int dtype, int *first_block, void *stream);

@@ -63,11 +63,13 @@ def test_workspace_sizes(lib):
         256 + (part + 255) // 256 * 256
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 32, lib.BF16) == 0
     # head size 128: the plain forward keeps fp32 q~ (Lp x 128), per block [k~; P_b]
-    # (192 x 128) and the fp32 diagonal table, whatever the dtype; PaTH-FoX is d = 64 only
+    # (192 x 128) and the fp32 diagonal table, whatever the dtype; PaTH-FoX adds the fp32
+    # in-block and tail sums (Lp each) and the fp64 block totals, each rounded up to 256 B
     for dt in (lib.BF16, lib.F32):
-        assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, dt) == \
-            256 + 128 * 128 * 4 + 2 * 192 * 128 * 4 + 2 * 64 * 64 * 4
-    assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, lib.BF16) == 0
+        plain = 256 + 128 * 128 * 4 + 2 * 192 * 128 * 4 + 2 * 64 * 64 * 4
+        assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, dt) == plain
+        assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, dt) == \
+            plain + 512 + 512 + 256
     # decode partials (m, l, o[128])
     part128 = 4 * 2 * 130 * 4
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 128, lib.BF16) == \
@@ -284,9 +286,13 @@ def test_fox_bwd_rejects_bad_arguments_before_launch(so, kw, code):
 
 
 def test_fwd_head_size_128_checks(so):
-    # d = 128 passes the size checks of the plain forward (the workspace check then stops
-    # it); 96 does not, and PaTH-FoX stays d = 64 only
+    # d = 128 passes the size checks of both forwards (the workspace check then stops
+    # them); 96 does not; the early-exit extents exist at d = 64 only
     assert _fwd(so, d=128, ws_bytes=1000) == 5
     assert _fwd(so, d=96) == 2
     assert so.path_fox_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 128, 128, 1,
+                           ctypes.c_float(0.125), FAKE, ctypes.c_size_t(1000), None) == 5
+    assert so.path_fox_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 128, 96, 1,
                            ctypes.c_float(0.125), FAKE, ctypes.c_size_t(1 << 30), None) == 2
+    assert so.path_fox_first_blocks(FAKE, ctypes.c_size_t(1 << 30), 1, 1, 128, 128, 1, FAKE,
+                                    None) == 2

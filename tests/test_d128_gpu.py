@@ -1,4 +1,5 @@
-"""Parity of the head-size-128 PaTH forward (through the C ABI) against the fp64 oracle.
+"""Parity of the head-size-128 PaTH and PaTH-FoX forward (through the C ABI) against the
+fp64 oracle.
 
 The same bars as the d = 64 forward: fp32 inputs, max normwise relative error <= 1e-4 and
 LSE within 1e-4; bf16 inputs, max absolute error <= 2e-2 on every element, mean absolute
@@ -66,10 +67,96 @@ def test_d128_workload_sampled_rows(lib):
     check_bf16(got, ref, got_lse, ref_lse)
 
 
-def test_d128_fox_is_rejected(lib):
-    x = pi.make_fwd_inputs(1, 1, 64, d=D, dtype=torch.bfloat16, seed=1, fox=True, device="cuda")
-    with pytest.raises(Exception):
-        lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+def _fox(lib, x, scale=None):
+    return lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], scale=scale)
+
+
+def _check_fp32(out, lse, ref, ref_lse):
+    rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    assert rel <= 1e-4, rel
+    assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
+
+
+@pytest.mark.parametrize("B,H,L", [(1, 2, 200), (1, 1, 1), (2, 1, 64), (1, 2, 65), (1, 1, 384)])
+def test_d128_fox_fp32(lib, B, H, L):
+    x = pi.make_fwd_inputs(B, H, L, d=D, dtype=torch.float32, seed=L + 7, clip=0.0, fox=True,
+                           device="cuda")
+    out, lse = _fox(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    _check_fp32(out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("B,H,L", [(2, 2, 130), (1, 3, 257)])
+def test_d128_fox_bf16(lib, B, H, L):
+    x = pi.make_fwd_inputs(B, H, L, d=D, dtype=torch.bfloat16, seed=L + 8, fox=True,
+                           device="cuda")
+    out, lse = _fox(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_d128_fox_two_stages_equal_the_fused_call(lib):
+    x = pi.make_fwd_inputs(1, 2, 300, d=D, dtype=torch.bfloat16, seed=19, fox=True, device="cuda")
+    out, lse = _fox(lib, x)
+    ws = lib.new_workspace(lib.OP_FOX_FWD, 1, 2, 300, lib.BF16, x["q"].device, d=D)
+    lib.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws, log_f=x["log_f"])
+    out2, lse2 = lib.path_fwd_scan(x["v"], ws, fox=True)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_d128_fox_zero_gate_is_path(lib):
+    # log f = 0: every bias is an exact zero, so PaTH-FoX gives PaTH's bits
+    x = pi.make_fwd_inputs(1, 2, 333, d=D, dtype=torch.bfloat16, seed=23, fox=True, device="cuda")
+    x["log_f"] = torch.zeros_like(x["log_f"])
+    out, lse = _fox(lib, x)
+    out2, lse2 = _run(lib, x)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_d128_fox_long_gate_sums_fp32(lib):
+    # 8192 tokens at log f ~ -1.3: the gate prefix sums reach about -10^4 while the bias
+    # against recent keys stays small; it must be accurate to its own size for the fp32
+    # bars to hold on rows all along the sequence
+    x = pi.make_fwd_inputs(1, 1, 8192, d=D, dtype=torch.float32, seed=47, clip=0.0, fox=True,
+                           device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(147)
+    x["log_f"] = torch.nn.functional.logsigmoid(
+        torch.randn(x["log_f"].shape, generator=g) - 1.0).to("cuda").contiguous()
+    out, lse = _fox(lib, x)
+    rows = np.arange(0, 8192, 61)
+    pairs = np.stack([np.zeros_like(rows), rows], axis=1)
+    h = {k: v[0].cpu() for k, v in x.items()}
+    ref, ref_lse = oracle.path_rows(h["q"], h["k"], h["v"], h["w"], h["beta"], pairs, h["log_f"])
+    got = out[0, 0].double().cpu().numpy()[rows]
+    assert np.abs(got - ref).max() / np.abs(ref).max() <= 1e-4
+    assert np.abs(lse[0, 0].double().cpu().numpy()[rows] - ref_lse).max() <= 1e-4
+
+
+def test_d128_fox_mixed_sign_gate(lib):
+    # log f of both signs (the bias against older keys can be positive), custom scale
+    x = pi.make_fwd_inputs(2, 2, 640, d=D, dtype=torch.bfloat16, seed=49, fox=True, device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(149)
+    x["log_f"] = (0.5 * torch.randn(x["log_f"].shape, generator=g) - 0.3).to("cuda").contiguous()
+    out, lse = _fox(lib, x, scale=0.2)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"],
+                                   scale=0.2)
+    check_bf16(out, ref, lse, ref_lse)
+
+
+def test_d128_fox_workload_sampled_rows(lib):
+    # PaTH-FoX on B4 H8 L2048 d128 bf16, 300 sampled rows with the first and last rows
+    B, H, L = 4, 8, 2048
+    x = pi.make_fwd_inputs(B, H, L, d=D, dtype=torch.bfloat16, seed=13, fox=True, device="cuda")
+    out, lse = _fox(lib, x)
+    g = np.random.default_rng(4)
+    heads = g.integers(0, B * H, 100)
+    rows = np.concatenate([np.stack([heads, g.integers(0, L, 100)], 1),
+                           np.stack([heads, np.zeros(100, np.int64)], 1),
+                           np.stack([heads, np.full(100, L - 1)], 1)]).astype(np.int64)
+    ref, ref_lse = oracle.path_rows(x["q"], x["k"], x["v"], x["w"], x["beta"], rows, x["log_f"])
+    got = out.reshape(B * H, L, D)[rows[:, 0], rows[:, 1]]
+    got_lse = lse.reshape(B * H, L)[rows[:, 0], rows[:, 1]]
+    check_bf16(got, ref, got_lse, ref_lse)
 
 
 def test_d128_custom_scale(lib):
