@@ -482,11 +482,15 @@ PROFILE_CASES = {
                                     torch.bfloat16, 5, 1000),
     # a quarter of the producer workload: x 134 MB, w 134 MB (both larger than L2)
     "producer": pi.ProducerWorkload("path_wbeta_bf16_B8L4096D2048R64H32", 8, 4096, 2048, 64, 32, 6),
-    # the backward leg's own workload (1.3 GB of workspace, stash larger than L2)
+    # the backward legs' own workload (1.3 GB of workspace, stash larger than L2)
     "bwd": pi.BF16_L2048,
+    "fox_bwd": pi.BF16_L2048,
     # the head-size-128 forward leg's own workload (FP32 ALU-bound kernels)
     "fwd_d128": pi.FwdWorkload("path_fwd_bf16_B4H8L2048_d128", 4, 8, 2048, 128, torch.bfloat16, 12,
                                pi.BETA_CLIP, False),
+    # a quarter of the head-size-128 decode workload (B8 H16 d128, 32K cache)
+    "decode_d128": pi.DecodeWorkload("path_decode_bf16_B8H16d128N32768x4", 8, 16, 32768, 4, 128,
+                                     torch.bfloat16, 5, 1000),
 }
 
 
@@ -496,10 +500,10 @@ def run_profile_case(args):
     pa.ensure_built()
     dev = torch.device("cuda")
     wl = PROFILE_CASES[args.profile]
-    if args.profile == "decode":
+    if args.profile in ("decode", "decode_d128"):
         cap = wl.n_prefix + args.warmup + args.steps
         kc, vc = pi.make_decode_prefix(wl, cap, device=dev)
-        ws = pa.new_workspace(pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16, dev)
+        ws = pa.new_workspace(pa.OP_DECODE, wl.B, wl.H, cap, pa.BF16, dev, wl.d)
         s = pi.make_decode_step(wl, 0, device=dev)
         for t in range(args.warmup + args.steps):
             pa.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
@@ -507,8 +511,8 @@ def run_profile_case(args):
     elif args.profile == "producer":
         r = time_producer(pa, wl, steps=args.steps, warmup=args.warmup)
         print(json.dumps(r))
-    elif args.profile == "bwd":
-        r = time_bwd(pa, wl, steps=args.steps, warmup=args.warmup)
+    elif args.profile in ("bwd", "fox_bwd"):
+        r = time_bwd(pa, wl, steps=args.steps, warmup=args.warmup, fox=args.profile == "fox_bwd")
         print(json.dumps(r))
     elif args.profile == "fox_decode":
         cap = wl.n_prefix + args.warmup + args.steps
@@ -616,7 +620,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
-    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd", "fwd_d128"],
+    ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd", "fwd_d128",
+                                          "decode_d128", "fox_bwd"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -717,7 +722,8 @@ def main():
         d128["workload"] = pi.DECODE_32K_D128.name
         d128["roofline"] = {"kernel": "decode_split_kernel<d=128>", "bound": "hbm",
                             "achieved": d128["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": d128["gbs"] / peaks["hbm_gbs"], "traffic": None,
+                            "frac": d128["gbs"] / peaks["hbm_gbs"],
+                            "traffic": ncu_traffic("decode_split_kernel_d128"),
                             "peak_source": "%s HBM copy" % peaks["source"]}
         line["decode_d128"] = d128
         del fdec
@@ -736,7 +742,8 @@ def main():
         ach = bwd["query_pass_flops"] / (bwd["ms_per_step"] * 1e-3) / 1e12
         bwd["roofline"] = {"kernels": "query-pass FP32 FLOPs over the whole backward call",
                            "bound": "alu", "achieved": ach, "peak": FP32_ALU_TFLOPS,
-                           "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS, "traffic": None,
+                           "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS,
+                           "traffic": ncu_traffic("bwd_query_kernel"), "traffic_kernel": "bwd_query_kernel",
                            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
         line["bwd"] = bwd
         # head size 128 (fp32 CUDA-core kernels): the bf16 check workload's width in 8 heads
@@ -751,7 +758,9 @@ def main():
                             "roofline": {"kernels": "prep_d128_kernel + scan_d128_kernel",
                                          "bound": "alu", "achieved": d_ach,
                                          "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-                                         "frac": d_ach / FP32_ALU_TFLOPS, "traffic": None,
+                                         "frac": d_ach / FP32_ALU_TFLOPS,
+                                         "traffic": ncu_traffic("scan_d128_kernel"),
+                                         "traffic_kernel": "scan_d128_kernel",
                                          "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
         del xd
         # PaTH-FoX at head size 128 (every key block visited: no early exit at d = 128)
@@ -764,7 +773,8 @@ def main():
         torch.cuda.empty_cache()
         fbwd = time_bwd(pa, pi.BF16_L2048, fox=True)
         ach = fbwd["query_pass_flops"] / (fbwd["ms_per_step"] * 1e-3) / 1e12
-        fbwd["roofline"] = dict(bwd["roofline"], achieved=ach, frac=ach / FP32_ALU_TFLOPS)
+        fbwd["roofline"] = dict(bwd["roofline"], achieved=ach, frac=ach / FP32_ALU_TFLOPS,
+                                traffic=ncu_traffic("bwd_query_kernel_fox"))
         line["fox_bwd"] = fbwd
 
     if args.sweep and rank == 0:
