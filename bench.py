@@ -763,7 +763,7 @@ def main():
                                          "traffic_kernel": "scan_d128_kernel",
                                          "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
         del xd
-        # PaTH-FoX at head size 128 (every key block visited: no early exit at d = 128)
+        # PaTH-FoX at head size 128 (the scan's early exit decided as it runs)
         xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, fox=True,
                                 device=dev)
         f_tot, _, _ = time_forward(pa, xd, 3, 3, fox=True)

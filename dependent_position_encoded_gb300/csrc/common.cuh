@@ -46,7 +46,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct D128Layout {
     int BH, nblk, Lp;
     size_t off_qt, off_kp, off_dg;
-    size_t off_lc, off_tail, off_tot, total;  // PaTH-FoX only (else all equal to total)
+    size_t off_lc, off_tail, off_tot;  // PaTH-FoX only (else all equal to total)
+    size_t off_mlc, off_kmax, off_cst, off_mpre, off_kpre, total;  // PaTH-FoX early exit
 };
 D128Layout d128_layout(int B, int H, int L, bool fox);
 

@@ -16,8 +16,17 @@
 //     c_i - c_j = [lc_i + sum_{b < b' < ib} T_b'] + [T_b - lc_j],
 // a per-row term with an fp64 running sum (exact where the weights are not negligible:
 // its rounding grows with the bias itself) and the key's tail sum within its block, so no
-// difference of two large prefix sums is ever taken. There is no early exit at d = 128:
-// the scan visits every key block.
+// difference of two large prefix sums is ever taken.
+// Early exit, exact within rounding (review §4: the gate makes distant keys vanish): every
+// H_s with beta_s in [0, 2] and unit w_s is a contraction, so the state a row carries is no
+// longer than q~_i, and against any key of blocks 0..b its logit is at most
+//     bound_i(b) = 2 |scale| log2(e) |q~_i| Kpre(b) + c2_i - Mpre(b),
+// with Kpre(b) the largest |k~_j| and Mpre(b) the smallest c2_j over blocks 0..b (the factor
+// 2 covers rounding). Before visiting block b the scan stops if bound_i(b) is below the
+// row's running maximum minus 40 log2(e) for every row of the query block: what remains
+// weighs less than e^-40 relative to the row's largest weight. The preparation records per
+// block the largest |k~_j| and the smallest in-block sum; a per-head pass forms the block
+// start offsets C_b (fp64), Mpre and Kpre.
 #include "common.cuh"
 
 namespace path {
@@ -28,6 +37,7 @@ constexpr int kD2 = 128;           // head size of this file
 constexpr int LDA = kC + 4;        // stride of buffers with 64 columns
 constexpr int LDB = kD2 + 4;       // stride of buffers with 128 columns
 constexpr int kThreads = 256;
+constexpr float kExitLog2 = 40.f * kLog2e;  // e^-40 relative weight, in log2 units
 
 // acc[i][j] += sum_{k < K} X[k][m0 + i] * Y[k][n0 + j]  (k-major operands)
 template <int K>
@@ -118,7 +128,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
                  const float *__restrict__ beta, const float *__restrict__ log_f, int L, int Lp,
                  int nblk, float scale_log2, float *__restrict__ qt, float *__restrict__ kp,
                  float *__restrict__ dg, float *__restrict__ lc, float *__restrict__ tail,
-                 double *__restrict__ tot) {
+                 double *__restrict__ tot, double *__restrict__ mlc, float *__restrict__ kmax) {
     extern __shared__ __align__(16) float sm[];
     float *Wr = sm;                  // W [s][c], 64 x LDB
     float *Wt = Wr + kC * LDB;       // W^T [c][s], 128 x LDA
@@ -130,6 +140,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     float *Y = X + kC * LDA;         // scratch 64 x 64
     float *bs = Y + kC * LDA;        // beta [64]
     double *lcs = reinterpret_cast<double *>(bs + kC);  // FoX: in-block sums lc [64], fp64
+    float *kn2 = reinterpret_cast<float *>(lcs + kC);    // FoX: |k~_j|^2 [64]
 
     const int tid = threadIdx.x, blk = blockIdx.x, bh = blockIdx.y;
     const int t0 = blk * kC;
@@ -165,6 +176,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     }
     for (int e = tid; e < kC * kC; e += kThreads) Ar[(e / kC) * LDA + e % kC] = 0.f;
     if (tid < kC) bs[tid] = (t0 + tid < L) ? beta[head + t0 + tid] : 0.f;
+    if (FOX && tid < kC) kn2[tid] = 0.f;
     if (FOX && tid < 32) {
         // inclusive prefix of log2(e) log f over the block (tokens past L add 0): lane l
         // holds tokens 2l and 2l + 1 and scans the pair sums over the warp
@@ -282,6 +294,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     __syncthreads();
     // k~[j][c] = k[j][c] - sum_u Khat[j][u] W[u][c]
     float *kp_blk = kp + blk_base * (kC + kD2) * kD2;
+    float kq[4] = {0.f, 0.f, 0.f, 0.f};  // FoX: partial |k~_j|^2 of this thread's rows
     for (int p = 0; p < 2; ++p) {
         zero(acc);
         mmk<kC>(Y, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
@@ -289,11 +302,40 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         for (int i = 0; i < 4; ++i) {
             float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = Kt[(n0 + 64 * p + j) * LDA + m0 + i] - acc[i][j];
+            for (int j = 0; j < 4; ++j) {
+                v[j] = Kt[(n0 + 64 * p + j) * LDA + m0 + i] - acc[i][j];
+                if (FOX) kq[i] = fmaf(v[j], v[j], kq[i]);
+            }
             put4<float>(kp_blk + (m0 + i) * kD2 + n0 + 64 * p, v);
         }
     }
+    if (FOX) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) atomicAdd(&kn2[m0 + i], kq[i]);
+    }
     __syncthreads();
+    if (FOX && tid < 32) {
+        // the block's largest |k~_j| and smallest in-block sum, over its tokens below L
+        float km = 0.f;
+        double ml = INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = tid + 32 * h;
+            if (t0 + j < L) {
+                km = fmaxf(km, sqrtf(kn2[j]));
+                ml = fmin(ml, lcs[j]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+            ml = fmin(ml, __shfl_xor_sync(0xffffffffu, ml, o));
+        }
+        if (tid == 0) {
+            kmax[(size_t)bh * nblk + blk] = km;
+            mlc[(size_t)bh * nblk + blk] = ml;
+        }
+    }
     // (A W)[s][c] = sum_u A[s][u] W[u][c] -> the Q^T buffer, as 64 x LDB
     float *AW = Qt;
     for (int p = 0; p < 2; ++p) {
@@ -315,6 +357,55 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
             for (int j = 0; j < 4; ++j) v[j] = ((nb + m0 + i) == (cb + n0 + j) ? 1.f : 0.f) - acc[i][j];
             put4<float>(out + (nb + m0 + i) * kD2 + cb + n0, v);
         }
+    }
+}
+
+// ---------------------------------------------------------------- PaTH-FoX exit bounds
+// One warp per head, 32 blocks per round: C_b = sum of the totals of blocks 0..b-1 (fp64),
+// Mpre(b) = min over blocks b' <= b of C_b' + (smallest in-block sum of b'), and Kpre(b) =
+// max over blocks b' <= b of the block's largest |k~_j|; all in log2 units.
+__global__ void __launch_bounds__(128)
+fox_bounds_d128_kernel(const double *__restrict__ tot, const double *__restrict__ mlc,
+                       const float *__restrict__ kmax, double *__restrict__ cst,
+                       double *__restrict__ mpre, float *__restrict__ kpre, int BH, int nblk) {
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (bh >= BH) return;
+    const size_t h0 = (size_t)bh * nblk;
+    double carry_c = 0.0, carry_m = INFINITY;
+    float carry_k = 0.f;
+    for (int b0 = 0; b0 < nblk; b0 += 32) {
+        const int b = b0 + lane;
+        const bool in = b < nblk;
+        const double t = in ? tot[h0 + b] : 0.0;
+        double inc = t;  // inclusive prefix of the totals within this round
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const double c = carry_c + (inc - t);
+        double m = in ? c + mlc[h0 + b] : INFINITY;
+        float k = in ? kmax[h0 + b] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double ym = __shfl_up_sync(0xffffffffu, m, o);
+            const float yk = __shfl_up_sync(0xffffffffu, k, o);
+            if (lane >= o) {
+                m = fmin(m, ym);
+                k = fmaxf(k, yk);
+            }
+        }
+        m = fmin(m, carry_m);
+        k = fmaxf(k, carry_k);
+        if (in) {
+            cst[h0 + b] = c;
+            mpre[h0 + b] = m;
+            kpre[h0 + b] = k;
+        }
+        carry_c = __shfl_sync(0xffffffffu, carry_c + inc, 31);
+        carry_m = __shfl_sync(0xffffffffu, m, 31);
+        carry_k = __shfl_sync(0xffffffffu, k, 31);
     }
 }
 
@@ -388,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const float *__restrict__ kp,
                  const float *__restrict__ dg, const float *__restrict__ lc,
                  const float *__restrict__ tail, const double *__restrict__ tot,
-                 T *__restrict__ out, float *__restrict__ lse, int L, int Lp, int nblk,
-                 float scale_log2) {
+                 const double *__restrict__ cst, const double *__restrict__ mpre,
+                 const float *__restrict__ kpre, T *__restrict__ out, float *__restrict__ lse,
+                 int L, int Lp, int nblk, float scale_log2) {
     extern __shared__ __align__(16) float sm[];
     float *Xr = sm;                 // X [i][c], 64 x LDB
     float *KB = Xr + kC * LDB;      // K~_b [j][c], 64 x LDB (slot of 128 x LDA)
@@ -416,7 +508,32 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
     // FoX: row lc_i (threads 0-63) and the fp64 sum of the totals of blocks b + 1 .. ib - 1
     const float lci = (FOX && tid < kC) ? lc[(size_t)bh * Lp + (size_t)ib * kC + tid] : 0.f;
     double between = 0.0;
+    // FoX early exit: per softmax row, 2 |scale| log2(e) |q~_i|, c2_i - C_ib and whether the
+    // row lies past L (such rows never hold the scan back)
+    float qk2 = 0.f, lcr = 0.f;
+    double cst_ib = 0.0;
+    bool pad = true;
+    if (FOX) {
+        __syncthreads();
+        float n2 = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < 32; ++c) {
+            const float x = Xr[row * LDB + part * 32 + c];
+            n2 = fmaf(x, x, n2);
+        }
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+        qk2 = 2.f * fabsf(scale_log2) * sqrtf(n2);
+        lcr = lc[(size_t)bh * Lp + (size_t)ib * kC + row];
+        cst_ib = cst[(size_t)bh * nblk + ib];
+        pad = ib * kC + row >= L;
+    }
     for (int b = ib; b >= 0; --b) {
+        if (FOX && b < ib) {
+            const size_t kb = (size_t)bh * nblk + b;
+            const float bound = (float)((cst_ib - mpre[kb]) + (double)lcr) + qk2 * kpre[kb];
+            if (__syncthreads_and(pad || bound < m_run - kExitLog2)) break;
+        }
         __syncthreads();
         {
             float4 vv[8];
@@ -540,7 +657,8 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
 }
 
 size_t prep_d128_smem() {
-    return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + kC) * sizeof(float) + kC * sizeof(double);
+    return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + 2 * kC) * sizeof(float) +
+           kC * sizeof(double);
 }
 size_t scan_d128_smem() {
     return (size_t)(2 * kC * LDB + kD2 * LDA + kD2 * LDB + 2 * kC * LDA + 3 * kC) * sizeof(float);
@@ -550,8 +668,10 @@ size_t scan_d128_smem() {
 
 // Workspace of the d = 128 forward: 256-byte status header, fp32 q~ (BH, Lp, 128), per block
 // [k~ (64 rows); P_b (128 rows)] (BH, nblk, 192, 128), diagonal logits (BH, nblk, 64, 64);
-// PaTH-FoX adds the in-block sums lc and the tail sums (BH, Lp) fp32 and the block totals
-// (BH, nblk) fp64, all in log2 units.
+// PaTH-FoX adds the in-block sums lc and the tail sums (BH, Lp) fp32, the block totals
+// (BH, nblk) fp64, all in log2 units, and the early-exit bounds per block: smallest in-block
+// sum (fp64), largest |k~_j| (fp32), block start offset C_b and prefix minimum Mpre (fp64),
+// prefix maximum Kpre (fp32).
 D128Layout d128_layout(int B, int H, int L, bool fox) {
     D128Layout y;
     y.BH = B * H;
@@ -566,12 +686,24 @@ D128Layout d128_layout(int B, int H, int L, bool fox) {
     y.off_dg = off;
     off = align256(off + bh * y.nblk * kC * kC * 4);
     y.off_lc = y.off_tail = y.off_tot = off;
+    y.off_mlc = y.off_kmax = y.off_cst = y.off_mpre = y.off_kpre = off;
     if (fox) {
+        const size_t nb = bh * y.nblk;
         off = align256(off + bh * y.Lp * 4);
         y.off_tail = off;
         off = align256(off + bh * y.Lp * 4);
         y.off_tot = off;
-        off = align256(off + bh * y.nblk * 8);
+        off = align256(off + nb * 8);
+        y.off_mlc = off;
+        off = align256(off + nb * 8);
+        y.off_kmax = off;
+        off = align256(off + nb * 4);
+        y.off_cst = off;
+        off = align256(off + nb * 8);
+        y.off_mpre = off;
+        off = align256(off + nb * 8);
+        y.off_kpre = off;
+        off = align256(off + nb * 4);
     }
     y.total = off;
     return y;
@@ -597,7 +729,14 @@ cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const 
         log_f, L, y.Lp, y.nblk, scale * kLog2e, reinterpret_cast<float *>(base + y.off_qt),
         reinterpret_cast<float *>(base + y.off_kp), reinterpret_cast<float *>(base + y.off_dg),
         reinterpret_cast<float *>(base + y.off_lc), reinterpret_cast<float *>(base + y.off_tail),
-        reinterpret_cast<double *>(base + y.off_tot));
+        reinterpret_cast<double *>(base + y.off_tot), reinterpret_cast<double *>(base + y.off_mlc),
+        reinterpret_cast<float *>(base + y.off_kmax));
+    if ((e = cudaGetLastError()) != cudaSuccess || !fox) return e;
+    fox_bounds_d128_kernel<<<(y.BH + 3) / 4, 128, 0, stream>>>(
+        reinterpret_cast<const double *>(base + y.off_tot), reinterpret_cast<const double *>(base + y.off_mlc),
+        reinterpret_cast<const float *>(base + y.off_kmax), reinterpret_cast<double *>(base + y.off_cst),
+        reinterpret_cast<double *>(base + y.off_mpre), reinterpret_cast<float *>(base + y.off_kpre),
+        y.BH, y.nblk);
     return cudaGetLastError();
 }
 
@@ -616,8 +755,9 @@ cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int
         static_cast<const T *>(v), reinterpret_cast<const float *>(base + y.off_qt),
         reinterpret_cast<const float *>(base + y.off_kp), reinterpret_cast<const float *>(base + y.off_dg),
         reinterpret_cast<const float *>(base + y.off_lc), reinterpret_cast<const float *>(base + y.off_tail),
-        reinterpret_cast<const double *>(base + y.off_tot), static_cast<T *>(out), lse, L, y.Lp,
-        y.nblk, scale * kLog2e);
+        reinterpret_cast<const double *>(base + y.off_tot), reinterpret_cast<const double *>(base + y.off_cst),
+        reinterpret_cast<const double *>(base + y.off_mpre), reinterpret_cast<const float *>(base + y.off_kpre),
+        static_cast<T *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e);
     return cudaGetLastError();
 }
 

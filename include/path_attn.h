@@ -17,7 +17,7 @@
  *  - d must be 64 (the head size the pages benchmark); the forward (path_attn_fwd,
  *    path_fox_fwd, path_fwd_prepare, path_fwd_scan) and the decode steps also take
  *    d = 128 (the larger head the pages mention; the forward then runs on fp32 CUDA-core
- *    kernels for either dtype, and PaTH-FoX visits every key block: no early exit).
+ *    kernels for either dtype; the PaTH-FoX scan decides its early exit as it goes).
  *    Anything else returns PATH_ERR_SHAPE.
  *  - Every tensor pointer and the workspace must be 16-byte aligned
  *    (PATH_ERR_ALIGN); the workspace must be 256-byte aligned.
@@ -104,9 +104,10 @@ path_status path_attn_fwd(const void *q, const void *k, const void *v, const voi
  * is at most |scale| |q~_i| |k~_j|; the scan of a 128-row tile stops above the key
  * blocks whose every key, bias included, weighs below e^-40 relative to the largest
  * logit of the row's own block (with the bound doubled for rounding). See
- * path_fox_first_blocks. At d = 128 there is no early exit (the scan visits every key
- * block), and the bias of a key in an earlier block is formed from in-block prefix sums,
- * block totals summed in fp64 and the key's in-block tail sum.
+ * path_fox_first_blocks. At d = 128 the same bound is tested inside the scan against each
+ * row's running maximum before every key block (the scan of a 64-row query block stops once
+ * all its rows pass it), and the bias of a key in an earlier block is formed from in-block
+ * prefix sums, block totals summed in fp64 and the key's in-block tail sum.
  */
 path_status path_fox_fwd(const void *q, const void *k, const void *v, const void *w,
                          const float *beta, const float *log_f, void *out, float *lse,
@@ -186,7 +187,7 @@ path_status path_fwd_scan(const void *v, void *out, float *lse, int fox, int B, 
  * path_workspace_bytes(PATH_OP_FOX_FWD, ...). The pages give no such call: it exposes
  * the rule of review "거리에서 경로로, PaTH Attention" §4 / technical summary
  * "技術要約: PaTH Attention" §2 (the gate makes distant keys vanish) for testing.
- * d = 64 only (the d = 128 forward has no early exit): other head sizes return
+ * d = 64 only (the d = 128 scan decides its exit as it runs): other head sizes return
  * PATH_ERR_SHAPE.
  */
 path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H, int L,

@@ -132,6 +132,25 @@ def test_d128_fox_long_gate_sums_fp32(lib):
     assert np.abs(lse[0, 0].double().cpu().numpy()[rows] - ref_lse).max() <= 1e-4
 
 
+def test_d128_fox_early_exit_skips_blocks(lib):
+    # log f = -5 per token: keys a block or more behind a query weigh about e^-300. The
+    # values of blocks 0 and 1 are NaN: a query block that visited them would turn NaN
+    # (0 x NaN), so finite rows from block 3 on show the scan stopped above them, and they
+    # match the oracle on the clean values (the skipped weights are below e^-40)
+    L = 640
+    x = pi.make_fwd_inputs(1, 2, L, d=D, dtype=torch.float32, seed=51, clip=0.0, fox=True,
+                           device="cuda")
+    x["log_f"] = torch.full_like(x["log_f"], -5.0)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    x["v"][:, :, :128] = float("nan")
+    out, lse = _fox(lib, x)
+    got = out[:, :, 192:].double().cpu().numpy()
+    assert np.isfinite(got).all()
+    r = ref[:, :, 192:]
+    assert np.abs(got - r).max() / np.abs(r).max() <= 1e-4
+    assert np.abs(lse[:, :, 192:].double().cpu().numpy() - ref_lse[:, :, 192:]).max() <= 1e-4
+
+
 def test_d128_fox_mixed_sign_gate(lib):
     # log f of both signs (the bias against older keys can be positive), custom scale
     x = pi.make_fwd_inputs(2, 2, 640, d=D, dtype=torch.bfloat16, seed=49, fox=True, device="cuda")
