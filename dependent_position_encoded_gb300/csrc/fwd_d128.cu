@@ -119,11 +119,74 @@ template <> __device__ __forceinline__ void put4<__nv_bfloat16>(__nv_bfloat16 *d
     *reinterpret_cast<uint2 *>(dst) = u;
 }
 
+// ---------------------------------------------------------------- register-tiled products
+// acc[i][j] += sum_{k < K} A[r0 + 16i][k] * B[k][col(j)] with A row-major and B k-major;
+// col(j) = c0 + j for j < 4 and c0 + 64 + j - 4 for j >= 4 (NJ = 8). The 16 lanes of a
+// half warp share the A rows (broadcast loads) and the eight lanes of a quarter warp read
+// one contiguous 128-byte piece of B.
+template <int K, int NJ>
+__device__ __forceinline__ void mmr(const float *__restrict__ A, int lda, const float *__restrict__ B,
+                                    int ldb, int r0, int c0, float (&acc)[4][NJ]) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float bv[NJ];
+            const float4 b0 = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + c0);
+            bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+            if (NJ == 8) {
+                const float4 b1 = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + c0 + 64);
+                bv[NJ == 8 ? 4 : 0] = b1.x; bv[NJ == 8 ? 5 : 1] = b1.y;
+                bv[NJ == 8 ? 6 : 2] = b1.z; bv[NJ == 8 ? 7 : 3] = b1.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+            }
+        }
+    }
+}
+
+// acc[i][j] += sum_{k < K} A[r0 + 16i][k] * B[n0 + 16j][k]: both operands row-major (the
+// contraction index contiguous in memory), so B^T products need no transposed copy. The
+// eight lanes of a quarter warp read eight consecutive B rows (n0 = tx): at a row stride of
+// LDB = 132 floats their 16-byte pieces fall in eight distinct bank groups.
+template <int K, int NJ>
+__device__ __forceinline__ void mmrb(const float *__restrict__ A, int lda, const float *__restrict__ B,
+                                     int ldb, int r0, int n0, float (&acc)[4][NJ]) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[4], b[NJ];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) b[j] = *reinterpret_cast<const float4 *>(B + (n0 + 16 * j) * ldb + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                float t = acc[i][j];
+                t = fmaf(a[i].x, b[j].x, t);
+                t = fmaf(a[i].y, b[j].y, t);
+                t = fmaf(a[i].z, b[j].z, t);
+                acc[i][j] = fmaf(a[i].w, b[j].w, t);
+            }
+    }
+}
+
 // ---------------------------------------------------------------- preparation
-// One CTA of 256 threads per (block, head). Shared memory: W [s][c] and its transpose, Q^T,
-// K^T (the 128-wide operands), and four 64 x 64 buffers (A, A^T, two scratch).
+// One CTA of 256 threads per (block, head), two CTAs per SM. Every operand stays in its
+// stored row-major layout (products over the head dimension read both operands as rows):
+// phase 1 holds W, Q and K and forms G = W W^T, Lq = Q W^T, Rk = K W^T and Q K^T in
+// registers; then four 64 x 64 slots replace Q and K (G, A, Lq, Rk; later Qhat, Khat and
+// A W), and the epilogues of q~ and k~ read q and k again from global memory.
 template <typename T, bool FOX>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
                  const float *__restrict__ beta, const float *__restrict__ log_f, int L, int Lp,
                  int nblk, float scale_log2, float *__restrict__ qt, float *__restrict__ kp,
@@ -131,14 +194,10 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
                  double *__restrict__ tot, double *__restrict__ mlc, float *__restrict__ kmax) {
     extern __shared__ __align__(16) float sm[];
     float *Wr = sm;                  // W [s][c], 64 x LDB
-    float *Wt = Wr + kC * LDB;       // W^T [c][s], 128 x LDA
-    float *Qt = Wt + kD2 * LDA;      // Q^T [c][i]; later (A W) [s][c] (64 x LDB)
-    float *Kt = Qt + kD2 * LDA;      // K^T [c][j]
-    float *Ar = Kt + kD2 * LDA;      // A [s][u]
-    float *At = Ar + kC * LDA;       // A^T [u][s]
-    float *X = At + kC * LDA;        // scratch 64 x 64
-    float *Y = X + kC * LDA;         // scratch 64 x 64
-    float *bs = Y + kC * LDA;        // beta [64]
+    float *R = Wr + kC * LDB;        // phase 1: Q [i][c] and K [j][c] (64 x LDB each)
+    float *Qr = R, *Kr = R + kC * LDB;
+    float *S0 = R, *Ar = R + kC * LDA, *S2 = R + 2 * kC * LDA, *S3 = R + 3 * kC * LDA;
+    float *bs = R + 4 * kC * LDA;    // beta [64]
     double *lcs = reinterpret_cast<double *>(bs + kC);  // FoX: in-block sums lc [64], fp64
     float *kn2 = reinterpret_cast<float *>(lcs + kC);    // FoX: |k~_j|^2 [64]
 
@@ -163,18 +222,10 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         for (int it = 0; it < 4; ++it) {
             const int e = tid + (4 * half + it) * kThreads, s = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
             *reinterpret_cast<float4 *>(Wr + s * LDB + c) = wv[it];
-            const float wa[4] = {wv[it].x, wv[it].y, wv[it].z, wv[it].w};
-            const float qa[4] = {qv[it].x, qv[it].y, qv[it].z, qv[it].w};
-            const float ka[4] = {kv[it].x, kv[it].y, kv[it].z, kv[it].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                Wt[(c + j) * LDA + s] = wa[j];
-                Qt[(c + j) * LDA + s] = qa[j];
-                Kt[(c + j) * LDA + s] = ka[j];
-            }
+            *reinterpret_cast<float4 *>(Qr + s * LDB + c) = qv[it];
+            *reinterpret_cast<float4 *>(Kr + s * LDB + c) = kv[it];
         }
     }
-    for (int e = tid; e < kC * kC; e += kThreads) Ar[(e / kC) * LDA + e % kC] = 0.f;
     if (tid < kC) bs[tid] = (t0 + tid < L) ? beta[head + t0 + tid] : 0.f;
     if (FOX && tid < kC) kn2[tid] = 0.f;
     if (FOX && tid < 32) {
@@ -199,12 +250,29 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         if (tid == 0) tot[(size_t)bh * nblk + blk] = lcs[kC - 1];
     }
 
-    const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
-    float acc[4][4];
-    // G = W W^T -> X
-    zero(acc);
-    mmk<kD2>(Wt, LDA, Wt, LDA, m0, n0, acc);
-    store4(X, LDA, m0, n0, acc);
+    // thread (ty, tx): rows ty + 16a, columns tx + 16b of the 64 x 64 products (mmrb), or
+    // columns 4tx .. 4tx + 3 (+ 64) of the row-times-k-major products (mmr)
+    const int ty = tid / 16, tx = tid % 16;
+    float g[4][4], lq[4][4], rk[4][4], qk[4][4];
+    zero(g);
+    zero(lq);
+    zero(rk);
+    zero(qk);
+    mmrb<kD2, 4>(Wr, LDB, Wr, LDB, ty, tx, g);   // G[s][v] = w_s . w_v
+    mmrb<kD2, 4>(Qr, LDB, Wr, LDB, ty, tx, lq);  // Lq[i][u] = q_i . w_u (u <= i)
+    mmrb<kD2, 4>(Kr, LDB, Wr, LDB, ty, tx, rk);  // Rk[j][s] = k_j . w_s (s > j)
+    mmrb<kD2, 4>(Qr, LDB, Kr, LDB, ty, tx, qk);  // q_i . k_j
+    __syncthreads();  // Q and K are no longer read from shared memory
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int r = ty + 16 * a, c = tx + 16 * b;
+            S0[r * LDA + c] = g[a][b];
+            S2[r * LDA + c] = (c <= r) ? lq[a][b] : 0.f;
+            S3[r * LDA + c] = (c > r) ? rk[a][b] : 0.f;
+            Ar[r * LDA + c] = 0.f;
+        }
     __syncthreads();
     // A = (I + D N)^{-1} D, one column per four threads: A[u][u] = beta_u and, for s < u,
     // A[s][u] = -beta_s sum_{v = s+1..u} G[s][v] A[v][u]
@@ -212,7 +280,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         const int u = tid >> 2, part = tid & 3;
         for (int s = kC - 1; s >= 0; --s) {
             float sum = 0.f;
-            for (int v = s + 1 + part; v < kC; v += 4) sum = fmaf(X[s * LDA + v], Ar[v * LDA + u], sum);
+            for (int v = s + 1 + part; v < kC; v += 4) sum = fmaf(S0[s * LDA + v], Ar[v * LDA + u], sum);
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             if (part == 0) Ar[s * LDA + u] = (s == u) ? bs[u] : (s < u ? -bs[s] * sum : 0.f);
@@ -220,100 +288,82 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         }
     }
     __syncthreads();
-    for (int e = tid; e < kC * kC; e += kThreads) {
-        const int s = e / kC, u = e % kC;
-        At[u * LDA + s] = Ar[s * LDA + u];
+    // Qhat[i][s] = sum_u Lq[i][u] A[s][u] -> slot 0 (G is no longer read)
+    {
+        float qh[4][4];
+        zero(qh);
+        mmrb<kC, 4>(S2, LDA, Ar, LDA, ty, tx, qh);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) S0[(ty + 16 * a) * LDA + tx + 16 * b] = qh[a][b];
     }
-    // Lq^T [u][i] = w_u . q_i (u <= i) -> X;  Rk^T [s][j] = w_s . k_j (s > j) -> Y
-    zero(acc);
-    mmk<kD2>(Wt, LDA, Qt, LDA, m0, n0, acc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (m0 + i > n0 + j) acc[i][j] = 0.f;
-    float acc2[4][4];
-    zero(acc2);
-    mmk<kD2>(Wt, LDA, Kt, LDA, m0, n0, acc2);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (m0 + i <= n0 + j) acc2[i][j] = 0.f;
     __syncthreads();
-    store4(X, LDA, m0, n0, acc);
-    store4(Y, LDA, m0, n0, acc2);
-    __syncthreads();
-    // Qhat^T [s][i] = sum_u A[s][u] Lq^T[u][i] (in place in X)
-    zero(acc);
-    mmk<kC>(At, LDA, X, LDA, m0, n0, acc);
-    __syncthreads();
-    store4(X, LDA, m0, n0, acc);
-    __syncthreads();
-
     const size_t blk_base = (size_t)bh * nblk + blk;
     // diagonal-block logits, log2 units: scale (q_i . k_j - sum_s Qhat[i][s] Rk[j][s]), j <= i
     {
-        float qk[4][4], corr[4][4];
-        zero(qk);
+        float corr[4][4];
         zero(corr);
-        mmk<kD2>(Qt, LDA, Kt, LDA, m0, n0, qk);
-        mmk<kC>(X, LDA, Y, LDA, m0, n0, corr);
+        mmrb<kC, 4>(S0, LDA, S3, LDA, ty, tx, corr);
         float *out = dg + blk_base * kC * kC;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float v[4];
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int ii = m0 + i, jj = n0 + j;
+            for (int b = 0; b < 4; ++b) {
+                const int ii = ty + 16 * a, jj = tx + 16 * b;
                 const float bias = FOX ? (float)(lcs[ii] - lcs[jj]) : 0.f;
-                v[j] = (jj <= ii && t0 + jj < L) ? scale_log2 * (qk[i][j] - corr[i][j]) + bias : -INFINITY;
+                out[ii * kC + jj] = (jj <= ii && t0 + jj < L)
+                                        ? scale_log2 * (qk[a][b] - corr[a][b]) + bias
+                                        : -INFINITY;
             }
-            put4<float>(out + (m0 + i) * kC + n0, v);
-        }
     }
-    // q~[i][c] = q[i][c] - sum_s Qhat[i][s] W[s][c], two passes of 64 columns
-    for (int p = 0; p < 2; ++p) {
-        zero(acc);
-        mmk<kC>(X, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
-        float *out = qt + ((size_t)bh * Lp + t0) * kD2;
+    // Khat[j][u] = sum_s Rk[j][s] A[s][u] -> slot 2 (Lq is no longer read)
+    {
+        float kh[4][4];
+        zero(kh);
+        mmr<kC, 4>(S3, LDA, Ar, LDA, ty, 4 * tx, kh);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = Qt[(n0 + 64 * p + j) * LDA + m0 + i] - acc[i][j];
-            put4<float>(out + (m0 + i) * kD2 + n0 + 64 * p, v);
-        }
+        for (int a = 0; a < 4; ++a)
+            *reinterpret_cast<float4 *>(S2 + (ty + 16 * a) * LDA + 4 * tx) =
+                make_float4(kh[a][0], kh[a][1], kh[a][2], kh[a][3]);
     }
     __syncthreads();
-    // Khat^T [u][j] = sum_s A[s][u] Rk^T[s][j] (in place in Y)
-    zero(acc);
-    mmk<kC>(Ar, LDA, Y, LDA, m0, n0, acc);
-    __syncthreads();
-    store4(Y, LDA, m0, n0, acc);
-    __syncthreads();
-    // k~[j][c] = k[j][c] - sum_u Khat[j][u] W[u][c]
-    float *kp_blk = kp + blk_base * (kC + kD2) * kD2;
+    // q~[i][c] = q[i][c] - sum_s Qhat[i][s] W[s][c] and k~[j][c] = k[j][c] - sum_u Khat[j][u]
+    // W[u][c], q and k read again from global memory
     float kq[4] = {0.f, 0.f, 0.f, 0.f};  // FoX: partial |k~_j|^2 of this thread's rows
-    for (int p = 0; p < 2; ++p) {
-        zero(acc);
-        mmk<kC>(Y, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
+    float *kp_blk = kp + blk_base * (kC + kD2) * kD2;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const T *src = pass == 0 ? q : k;
+        float acc[4][8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float v[4];
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[j] = Kt[(n0 + 64 * p + j) * LDA + m0 + i] - acc[i][j];
-                if (FOX) kq[i] = fmaf(v[j], v[j], kq[i]);
+            for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        mmr<kC, 8>(pass == 0 ? S0 : S2, LDA, Wr, LDB, ty, 4 * tx, acc);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int r = ty + 16 * a;
+            const bool in = t0 + r < L;
+            const size_t g0 = (head + t0 + r) * kD2 + 4 * tx;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 x0 = in ? ld4(src + g0) : z, x1 = in ? ld4(src + g0 + 64) : z;
+            const float v0[4] = {x0.x - acc[a][0], x0.y - acc[a][1], x0.z - acc[a][2], x0.w - acc[a][3]};
+            const float v1[4] = {x1.x - acc[a][4], x1.y - acc[a][5], x1.z - acc[a][6], x1.w - acc[a][7]};
+            float *dst = pass == 0 ? qt + ((size_t)bh * Lp + t0 + r) * kD2 : kp_blk + r * kD2;
+            put4<float>(dst + 4 * tx, v0);
+            put4<float>(dst + 4 * tx + 64, v1);
+            if (FOX && pass == 1) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kq[a] = fmaf(v0[e], v0[e], fmaf(v1[e], v1[e], kq[a]));
             }
-            put4<float>(kp_blk + (m0 + i) * kD2 + n0 + 64 * p, v);
         }
     }
     if (FOX) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) atomicAdd(&kn2[m0 + i], kq[i]);
+        for (int a = 0; a < 4; ++a) atomicAdd(&kn2[ty + 16 * a], kq[a]);
     }
-    __syncthreads();
+    __syncthreads();  // slots 2 and 3 (Khat, Rk) are free
     if (FOX && tid < 32) {
         // the block's largest |k~_j| and smallest in-block sum, over its tokens below L
         float km = 0.f;
@@ -332,21 +382,32 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
             ml = fmin(ml, __shfl_xor_sync(0xffffffffu, ml, o));
         }
         if (tid == 0) {
-            kmax[(size_t)bh * nblk + blk] = km;
-            mlc[(size_t)bh * nblk + blk] = ml;
+            kmax[blk_base] = km;
+            mlc[blk_base] = ml;
         }
     }
-    // (A W)[s][c] = sum_u A[s][u] W[u][c] -> the Q^T buffer, as 64 x LDB
-    float *AW = Qt;
-    for (int p = 0; p < 2; ++p) {
-        zero(acc);
-        mmk<kC>(At, LDA, Wr, LDB, m0, n0 + 64 * p, acc);
-        store4(AW, LDB, m0, n0 + 64 * p, acc);
+    // (A W)[s][c] = sum_u A[s][u] W[u][c] -> slots 2-3 as 64 x LDB
+    float *AW = S2;
+    {
+        float acc[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        mmr<kC, 8>(Ar, LDA, Wr, LDB, ty, 4 * tx, acc);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            float *row = AW + (ty + 16 * a) * LDB + 4 * tx;
+            *reinterpret_cast<float4 *>(row) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+            *reinterpret_cast<float4 *>(row + 64) = make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
+        }
     }
     __syncthreads();
     // P_b[n][c] = delta(n, c) - sum_s W[s][n] (A W)[s][c], four 64 x 64 quadrants
+    const int m0 = ty * 4, n0 = tx * 4;
     for (int pq = 0; pq < 4; ++pq) {
         const int nb = 64 * (pq >> 1), cb = 64 * (pq & 1);
+        float acc[4][4];
         zero(acc);
         mmk<kC>(Wr, LDB, AW, LDB, nb + m0, cb + n0, acc);
         float *out = kp_blk + kC * kD2;
@@ -410,65 +471,6 @@ fox_bounds_d128_kernel(const double *__restrict__ tot, const double *__restrict_
 }
 
 // ---------------------------------------------------------------- scan
-// acc[i][j] += sum_{k < K} A[r0 + 16i][k] * B[k][col(j)] with A row-major and B k-major;
-// col(j) = c0 + j for j < 4 and c0 + 64 + j - 4 for j >= 4 (NJ = 8). The 16 lanes of a
-// half warp share the A rows (broadcast loads) and the eight lanes of a quarter warp read
-// one contiguous 128-byte piece of B.
-template <int K, int NJ>
-__device__ __forceinline__ void mmr(const float *__restrict__ A, int lda, const float *__restrict__ B,
-                                    int ldb, int r0, int c0, float (&acc)[4][NJ]) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float4 a[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            float bv[NJ];
-            const float4 b0 = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + c0);
-            bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
-            if (NJ == 8) {
-                const float4 b1 = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + c0 + 64);
-                bv[NJ == 8 ? 4 : 0] = b1.x; bv[NJ == 8 ? 5 : 1] = b1.y;
-                bv[NJ == 8 ? 6 : 2] = b1.z; bv[NJ == 8 ? 7 : 3] = b1.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
-            }
-        }
-    }
-}
-
-// acc[i][j] += sum_{k < K} A[r0 + 16i][k] * B[n0 + 16j][k]: both operands row-major (the
-// contraction index contiguous in memory), so B^T products need no transposed copy. The
-// eight lanes of a quarter warp read eight consecutive B rows (n0 = tx): at a row stride of
-// LDB = 132 floats their 16-byte pieces fall in eight distinct bank groups.
-template <int K, int NJ>
-__device__ __forceinline__ void mmrb(const float *__restrict__ A, int lda, const float *__restrict__ B,
-                                     int ldb, int r0, int n0, float (&acc)[4][NJ]) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float4 a[4], b[NJ];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) b[j] = *reinterpret_cast<const float4 *>(B + (n0 + 16 * j) * ldb + k);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                float t = acc[i][j];
-                t = fmaf(a[i].x, b[j].x, t);
-                t = fmaf(a[i].y, b[j].y, t);
-                t = fmaf(a[i].z, b[j].z, t);
-                acc[i][j] = fmaf(a[i].w, b[j].w, t);
-            }
-    }
-}
-
 // One CTA per (64-row query block, head): the state X = (q~_i) as rows in shared memory;
 // for key block b = ib, ib-1, ..., 0 the logits (diagonal block: the table; earlier blocks:
 // X K~_b^T), the online softmax, O += P V_b and X <- X P_b^T. Thread (ty, tx) owns rows
@@ -657,8 +659,7 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
 }
 
 size_t prep_d128_smem() {
-    return (size_t)(kC * LDB + 3 * kD2 * LDA + 4 * kC * LDA + 2 * kC) * sizeof(float) +
-           kC * sizeof(double);
+    return (size_t)(kC * LDB + 4 * kC * LDA + 2 * kC) * sizeof(float) + kC * sizeof(double);
 }
 size_t scan_d128_smem() {
     return (size_t)(2 * kC * LDB + kD2 * LDA + kD2 * LDB + 2 * kC * LDA + 3 * kC) * sizeof(float);
