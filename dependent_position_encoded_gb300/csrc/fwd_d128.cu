@@ -69,11 +69,9 @@ __device__ __forceinline__ void store4(float *Z, int ld, int m0, int n0, const f
         *reinterpret_cast<float4 *>(Z + (m0 + i) * ld + n0) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
 }
 
-// rows x 128 fp32 tile (row-major, 128 floats per row) into shared memory as is
-// (dst[r * ld + c]) or transposed (dst[c * ld + r]); eight 16-byte loads in flight per
-// thread before the first store
-__device__ __forceinline__ void load128(float *dst, int ld, const float *__restrict__ src, int rows,
-                                        bool transpose) {
+// rows x 128 fp32 tile (row-major, 128 floats per row) into shared memory rows of stride
+// ld; eight 16-byte loads in flight per thread before the first store
+__device__ __forceinline__ void load128(float *dst, int ld, const float *__restrict__ src, int rows) {
     const int n4 = rows * (kD2 / 4);
     for (int base = 0; base < n4; base += 8 * kThreads) {
         float4 x[8];
@@ -87,14 +85,7 @@ __device__ __forceinline__ void load128(float *dst, int ld, const float *__restr
             const int e = base + (int)threadIdx.x + it * kThreads;
             if (e < n4) {
                 const int r = e / (kD2 / 4), c = 4 * (e % (kD2 / 4));
-                if (transpose) {
-                    dst[c * ld + r] = x[it].x;
-                    dst[(c + 1) * ld + r] = x[it].y;
-                    dst[(c + 2) * ld + r] = x[it].z;
-                    dst[(c + 3) * ld + r] = x[it].w;
-                } else {
-                    *reinterpret_cast<float4 *>(dst + r * ld + c) = x[it];
-                }
+                *reinterpret_cast<float4 *>(dst + r * ld + c) = x[it];
             }
         }
     }
@@ -500,7 +491,7 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
     const int ty = tid / 16, tx = tid % 16, r0 = ty, c0 = 4 * tx;
     const int row = tid >> 2, part = tid & 3;
     const size_t hL = (size_t)bh * L;
-    load128(Xr, LDB, qt + ((size_t)bh * Lp + (size_t)ib * kC) * kD2, kC, false);
+    load128(Xr, LDB, qt + ((size_t)bh * Lp + (size_t)ib * kC) * kD2, kC);
     float acc[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -561,8 +552,8 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
                     kbias[tid - kC] = tail[(size_t)bh * Lp + (size_t)b * kC + tid - kC];
                 }
             }
-            load128(KB, LDB, blk, kC, false);
-            load128(PB, LDB, blk + kC * kD2, kD2, false);
+            load128(KB, LDB, blk, kC);
+            load128(PB, LDB, blk + kC * kD2, kD2);
         } else {
             const float *tab = dg + ((size_t)bh * nblk + b) * kC * kC;
 #pragma unroll
