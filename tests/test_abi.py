@@ -112,6 +112,15 @@ def test_empty_problems_launch_nothing(so):
     assert _fwd(so, B=0) == 0
 
 
+def test_head_128_empty_problems_launch_nothing(so):
+    assert _fwd(so, d=128, L=0, q=None, k=None, v=None, w=None, beta=None, out=None,
+                ws=None) == 0
+    assert so.path_fox_fwd(None, None, None, None, None, None, None, None, 1, 1, 0, 128, 1,
+                           ctypes.c_float(0.125), None, ctypes.c_size_t(0), None) == 0
+    assert so.path_fox_fwd(None, None, None, None, None, None, None, None, 0, 4, 64, 128, 1,
+                           ctypes.c_float(0.125), None, ctypes.c_size_t(0), None) == 0
+
+
 def test_fox_needs_log_f(so):
     r = so.path_fox_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 1, 128, 64, 1,
                         ctypes.c_float(0.125), FAKE, ctypes.c_size_t(1 << 30), None)

@@ -185,3 +185,10 @@ def test_d128_custom_scale(lib):
     rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
     assert rel <= 1e-4, rel
     assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_d128_empty_sequence(lib, fox):
+    x = pi.make_fwd_inputs(2, 3, 0, d=D, dtype=torch.bfloat16, seed=1, fox=fox, device="cuda")
+    out, lse = _fox(lib, x) if fox else _run(lib, x)
+    assert out.shape == (2, 3, 0, D) and lse.shape == (2, 3, 0)

@@ -410,6 +410,30 @@ def test_fox_long_gate_sums_fp32(lib):
     assert np.abs(lse[0, 0].double().cpu().numpy()[rows] - ref_lse).max() <= 1e-4
 
 
+@pytest.mark.parametrize("dtype,first", [(torch.bfloat16, 256), (torch.float32, 192)])
+def test_fox_early_exit_never_reads_skipped_values(lib, dtype, first):
+    # log f = -5 per token and the values of blocks 0 and 1 set to NaN: a query block whose
+    # scan visited them would turn NaN (0 x NaN). Rows from block 3 on (fp32 scan, one query
+    # block per CTA) or block 4 on (tensor-core scan: 128-row tiles over key-block pairs)
+    # stay finite, so the scan stopped above those blocks, and they match the oracle on the
+    # clean values (the skipped weights are below e^-40)
+    L = 640
+    x = pi.make_fwd_inputs(1, 2, L, dtype=dtype, seed=53, clip=0.0 if dtype == torch.float32
+                           else pi.BETA_CLIP, fox=True, device="cuda")
+    x["log_f"] = torch.full_like(x["log_f"], -5.0)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    x["v"][:, :, :128] = float("nan")
+    out, lse = run_fwd(lib, x, fox=True)
+    got = out[:, :, first:]
+    assert torch.isfinite(got).all()
+    if dtype == torch.bfloat16:
+        check_bf16(got, ref[:, :, first:], lse[:, :, first:], ref_lse[:, :, first:])
+    else:
+        r = ref[:, :, first:]
+        assert np.abs(got.double().cpu().numpy() - r).max() / np.abs(r).max() <= F32_MAX_REL
+        assert np.abs(lse[:, :, first:].double().cpu().numpy() - ref_lse[:, :, first:]).max() <= 1e-4
+
+
 def test_fox_zero_gate_has_no_exit(lib):
     # log f = 0: no bias, nothing can be skipped, and FoX equals PaTH (up to rounding:
     # the FoX scan applies the scale in another order than the PaTH scan)
