@@ -115,7 +115,7 @@ def test_hand_example_logits_outputs_and_fox():
 
 # ----------------------------------------------------------------- special cases
 
-@pytest.mark.parametrize("L,d", [(1, 4), (37, 8), (130, 64)])
+@pytest.mark.parametrize("L,d", [(1, 4), (37, 8), (130, 64), (70, 128)])
 def test_beta_zero_is_causal_softmax_attention(L, d):
     rng = np.random.default_rng(L)
     q, k, v, w, _ = rand_head(rng, L, d)
@@ -138,7 +138,7 @@ def test_diagonal_logit_is_plain_dot_product():
     assert np.all(np.isneginf(lg[np.triu_indices(40, 1)]))
 
 
-@pytest.mark.parametrize("L,d", [(2, 3), (9, 8), (16, 64)])
+@pytest.mark.parametrize("L,d", [(2, 3), (9, 8), (16, 64), (10, 128)])
 def test_brute_force_explicit_matrices(L, d):
     rng = np.random.default_rng(100 + L)
     q, k, v, w, beta = rand_head(rng, L, d)
@@ -255,10 +255,10 @@ def test_fox_reductions():
 
 # ----------------------------------------------------------------- decode
 
-@pytest.mark.parametrize("fox", [False, True])
-def test_decode_from_empty_cache_matches_prefill(fox):
+@pytest.mark.parametrize("fox,d", [(False, 16), (True, 16), (False, 128), (True, 128)])
+def test_decode_from_empty_cache_matches_prefill(fox, d):
     rng = np.random.default_rng(19)
-    nh, T, d = 3, 40, 16
+    nh, T = 3, 40
     q, k, v, g = (rng.standard_normal((nh, T, d)) for _ in range(4))
     w = g / np.linalg.norm(g, axis=-1, keepdims=True)
     beta = rng.uniform(0, 2, size=(nh, T))
