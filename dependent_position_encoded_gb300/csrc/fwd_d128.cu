@@ -170,6 +170,36 @@ __device__ __forceinline__ void mmrb(const float *__restrict__ A, int lda, const
     }
 }
 
+// mmrb for two products that share the A rows: acc1 = A B1^T (NJ1 columns) and acc2 =
+// A B2^T (NJ2 columns), each A piece loaded once for both.
+template <int K, int NJ1, int NJ2>
+__device__ __forceinline__ void mmrb2(const float *__restrict__ A, int lda,
+                                      const float *__restrict__ B1, const float *__restrict__ B2,
+                                      int ldb, int r0, int n0, float (&acc1)[4][NJ1],
+                                      float (&acc2)[4][NJ2]) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * lda + k);
+#pragma unroll
+        for (int j = 0; j < NJ1 + NJ2; ++j) {
+            const float4 b = j < NJ1 ? *reinterpret_cast<const float4 *>(B1 + (n0 + 16 * j) * ldb + k)
+                                     : *reinterpret_cast<const float4 *>(B2 + (n0 + 16 * (j - NJ1)) * ldb + k);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float t = j < NJ1 ? acc1[i][j < NJ1 ? j : 0] : acc2[i][j < NJ1 ? 0 : j - NJ1];
+                t = fmaf(a[i].x, b.x, t);
+                t = fmaf(a[i].y, b.y, t);
+                t = fmaf(a[i].z, b.z, t);
+                t = fmaf(a[i].w, b.w, t);
+                if (j < NJ1) acc1[i][j < NJ1 ? j : 0] = t;
+                else acc2[i][j < NJ1 ? 0 : j - NJ1] = t;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- preparation
 // One CTA of 256 threads per (block, head), two CTAs per SM. Every operand stays in its
 // stored row-major layout (products over the head dimension read both operands as rows):
@@ -250,9 +280,9 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     zero(rk);
     zero(qk);
     mmrb<kD2, 4>(Wr, LDB, Wr, LDB, ty, tx, g);   // G[s][v] = w_s . w_v
-    mmrb<kD2, 4>(Qr, LDB, Wr, LDB, ty, tx, lq);  // Lq[i][u] = q_i . w_u (u <= i)
     mmrb<kD2, 4>(Kr, LDB, Wr, LDB, ty, tx, rk);  // Rk[j][s] = k_j . w_s (s > j)
-    mmrb<kD2, 4>(Qr, LDB, Kr, LDB, ty, tx, qk);  // q_i . k_j
+    // Lq[i][u] = q_i . w_u (u <= i) and q_i . k_j, one pass over the Q rows
+    mmrb2<kD2, 4, 4>(Qr, LDB, Wr, Kr, LDB, ty, tx, lq, qk);
     __syncthreads();  // Q and K are no longer read from shared memory
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -573,8 +603,7 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
                 for (int j = 0; j < 8; ++j) xn[i][j] = 0.f;
             }
             // logits and the new state, columns tx + 16j of rows r0 + 16i
-            mmrb<kD2, 4>(Xr, LDB, KB, LDB, r0, tx, sv);
-            mmrb<kD2, 8>(Xr, LDB, PB, LDB, r0, tx, xn);
+            mmrb2<kD2, 4, 8>(Xr, LDB, KB, PB, LDB, r0, tx, sv, xn);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
