@@ -312,13 +312,15 @@ def path_fwd_scan(v, workspace, out=None, lse=True, fox=False, scale=None, strea
     return out, lse
 
 
-def path_fox_first_blocks(workspace, B, H, L, dtype, stream=None):
+def path_fox_first_blocks(workspace, B, H, L, dtype, stream=None, d=HEAD_DIM):
     """PaTH-FoX early-exit extents left in `workspace` by path_fwd_prepare(..., log_f):
-    an int32 tensor (B, H, ceil(L / 64)) of the lowest key block each query block needs."""
+    an int32 tensor (B, H, ceil(L / 64)) of the lowest key block each query block needs.
+    Head size 64 only: the head-size-128 scan decides its exit as it runs (d = 128 raises
+    PathError with ERR_SHAPE)."""
     torch = _torch()
     nq = (L + 63) // 64
     first = torch.empty((B, H, nq), dtype=torch.int32, device=workspace.device)
-    _check(_load().path_fox_first_blocks(_ptr(workspace), workspace.numel(), B, H, L, 64,
+    _check(_load().path_fox_first_blocks(_ptr(workspace), workspace.numel(), B, H, L, int(d),
                                          _dtype_code_of(dtype), _ptr(first),
                                          _stream(stream, workspace.device)),
            "path_fox_first_blocks")

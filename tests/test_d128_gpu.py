@@ -192,3 +192,11 @@ def test_d128_empty_sequence(lib, fox):
     x = pi.make_fwd_inputs(2, 3, 0, d=D, dtype=torch.bfloat16, seed=1, fox=fox, device="cuda")
     out, lse = _fox(lib, x) if fox else _run(lib, x)
     assert out.shape == (2, 3, 0, D) and lse.shape == (2, 3, 0)
+
+
+def test_d128_has_no_precomputed_extents(lib):
+    x = pi.make_fwd_inputs(1, 1, 128, d=D, dtype=torch.bfloat16, seed=2, fox=True, device="cuda")
+    ws = lib.new_workspace(lib.OP_FOX_FWD, 1, 1, 128, lib.BF16, "cuda", d=D)
+    lib.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws, log_f=x["log_f"])
+    with pytest.raises(lib.PathError):
+        lib.path_fox_first_blocks(ws, 1, 1, 128, torch.bfloat16, d=D)

@@ -255,8 +255,17 @@ def test_fox_reductions():
 
 # ----------------------------------------------------------------- decode
 
-@pytest.mark.parametrize("fox,d", [(False, 16), (True, 16), (False, 128), (True, 128)])
-def test_decode_from_empty_cache_matches_prefill(fox, d):
+@pytest.mark.parametrize("fox", [False, True])
+def test_decode_from_empty_cache_matches_prefill(fox):
+    _decode_from_empty_matches_prefill(fox, 16)
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_decode_from_empty_cache_matches_prefill_head_128(fox):
+    _decode_from_empty_matches_prefill(fox, 128)
+
+
+def _decode_from_empty_matches_prefill(fox, d):
     rng = np.random.default_rng(19)
     nh, T = 3, 40
     q, k, v, g = (rng.standard_normal((nh, T, d)) for _ in range(4))
