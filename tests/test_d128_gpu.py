@@ -200,3 +200,25 @@ def test_d128_has_no_precomputed_extents(lib):
     lib.path_fwd_prepare(x["q"], x["k"], x["w"], x["beta"], ws, log_f=x["log_f"])
     with pytest.raises(lib.PathError):
         lib.path_fox_first_blocks(ws, 1, 1, 128, torch.bfloat16, d=D)
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_d128_max_heads(lib, fox):
+    # 65535 heads (the grid's y limit) of 70 tokens (two blocks, the second ragged); sampled
+    # rows of sampled heads against the oracle
+    B, H, L = 65535, 1, 70
+    x = pi.make_fwd_inputs(B, H, L, d=D, dtype=torch.bfloat16, seed=31, fox=fox, device="cuda")
+    out, lse = _fox(lib, x) if fox else _run(lib, x)
+    g = np.random.default_rng(5)
+    heads = np.concatenate([[0, B * H - 1], g.integers(0, B * H, 60)])
+    rows = np.stack([heads, g.integers(0, L, heads.size)], 1).astype(np.int64)
+    rows = np.concatenate([rows, np.stack([heads, np.full(heads.size, L - 1)], 1)])
+    sel = torch.as_tensor(np.unique(rows[:, 0]), device="cuda")
+    sub = {k: v.reshape(B * H, *v.shape[2:])[sel] for k, v in x.items()}
+    remap = {int(h): i for i, h in enumerate(sel.tolist())}
+    local = np.stack([[remap[int(h)] for h in rows[:, 0]], rows[:, 1]], 1).astype(np.int64)
+    ref, ref_lse = oracle.path_rows(sub["q"], sub["k"], sub["v"], sub["w"], sub["beta"], local,
+                                    sub.get("log_f"))
+    got = out.reshape(B * H, L, D)[rows[:, 0], rows[:, 1]]
+    got_lse = lse.reshape(B * H, L)[rows[:, 0], rows[:, 1]]
+    check_bf16(got, ref, got_lse, ref_lse)
