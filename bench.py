@@ -44,17 +44,29 @@ def fwd_flops(B, H, L, d=64):
     return f_attn, f_corr, f_pre
 
 
-def scan_executed_flops(B, H, L):
+def scan_executed_flops(B, H, L, first=None):
     """Tensor-core FLOPs the block-scan kernel actually issues (128-row tiles; per
-    visited key block S = X K~^T and, except at the last block, X P_b^T; P V every block)."""
+    visited key block S = X K~^T and, except at the last block, X P_b^T; P V every block).
+    first: PaTH-FoX early-exit extents (B*H rows of per-query-block lowest key blocks, as
+    path_fox_first_blocks returns them); a tile then visits its key-block pairs down to the
+    pair holding the lower extent of its two query blocks."""
     nblk = (L + C - 1) // C
+    nq = nblk
     nblk += nblk & 1
     mm = 2.0 * 128 * 64 * 64
+
+    def tile_flops(steps):
+        return (steps - 1) * mm + (steps - 2) * mm + steps * mm
+
+    if first is None:
+        return B * H * sum(tile_flops(2 * t + 2) for t in range(nblk // 2))
     total = 0.0
-    for t in range(nblk // 2):
-        steps = 2 * t + 2
-        total += (steps - 1) * mm + (steps - 2) * mm + steps * mm
-    return B * H * total
+    for row in first:
+        for t in range(nblk // 2):
+            lo = row[2 * t] if 2 * t + 1 >= nq else min(row[2 * t], row[2 * t + 1])
+            fp = min(lo >> 1, t)
+            total += tile_flops(2 * t + 2 - 2 * fp)
+    return total
 
 
 def decode_bytes(B, H, n, d=64):
@@ -696,10 +708,24 @@ def main():
         fox_total, fox_scan, fox_prep = time_forward(pa, xf, 3, 3, fox=True)
         fox_ms = fox_total / 3
         # the early exit skips the key blocks whose weights vanish, so the fixed
-        # algorithmic-FLOP formula does not describe the work done: no FLOP rate here
+        # algorithmic-FLOP formula does not describe the work done: the scan's rate is taken
+        # on the tensor-core FLOPs of the key blocks it visits (from the recorded extents)
+        wsf = pa.new_workspace(pa.OP_FOX_FWD, fw.B, fw.H, fw.L, pa.BF16, dev)
+        pa.path_fwd_prepare(xf["q"], xf["k"], xf["w"], xf["beta"], wsf, log_f=xf["log_f"])
+        first = pa.path_fox_first_blocks(wsf, fw.B, fw.H, fw.L, xf["q"].dtype).cpu()
+        f_ex = scan_executed_flops(fw.B, fw.H, fw.L, first.reshape(fw.B * fw.H, -1).tolist())
+        del wsf
+        f_scan = statistics.mean(fox_scan)
+        f_ach = f_ex / (f_scan * 1e-3) / 1e12
         line["fox"] = {"workload": fw.name, "ms_per_step": fox_ms,
                        "tokens_per_s": fw.B * fw.L / (fox_ms * 1e-3), "early_exit": True,
-                       "scan_ms": statistics.mean(fox_scan), "prepare_ms": statistics.mean(fox_prep)}
+                       "scan_ms": f_scan, "prepare_ms": statistics.mean(fox_prep),
+                       "roofline": {"kernel": "path_scan_tc_kernel<FOX=1>", "bound": "tensor",
+                                    "achieved": f_ach, "peak": peaks["bf16_tflops"],
+                                    "unit": "TFLOP/s", "frac": f_ach / peaks["bf16_tflops"],
+                                    "traffic": None,
+                                    "basis": "executed tensor FLOPs of the visited key blocks",
+                                    "executed_flops_per_launch": f_ex}}
         del xf
         torch.cuda.empty_cache()
         dec = time_decode(pa, pi.DECODE_32K)
