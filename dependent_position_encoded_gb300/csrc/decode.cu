@@ -132,9 +132,6 @@ decode_split_kernel(const T *__restrict__ q, const T *__restrict__ w,
 
     T *krow = kc + head * cap * D + e0;
     const T *vrow = vc + head * cap * D + e0;
-    // One cached key: update it in place, score it (bias gj, log2 units) and fold it into
-    // the lane's online softmax. Every lane calls it (the shuffles are warp-wide); lanes
-    // whose key is past the end load nothing and store nothing.
     // The arithmetic of one cached key whose row kv is in registers: update it in place,
     // score it (bias gj, log2 units) and fold it into the lane's online softmax. Every lane
     // calls it (the shuffles are warp-wide); lanes whose key is past the end store nothing.
