@@ -189,7 +189,8 @@ def time_forward(pa, x, steps, warmup, fox=False):
     """Times `steps` forwards (prepare + scan); returns (total_ms, scan_ms_list, prep_ms_list)."""
     B, H, L, d = x["q"].shape
     op = pa.OP_FOX_FWD if fox else pa.OP_FWD
-    ws = pa.new_workspace(op, B, H, L, pa.BF16, x["q"].device, d=d)
+    dt = pa.F32 if x["q"].dtype == torch.float32 else pa.BF16
+    ws = pa.new_workspace(op, B, H, L, dt, x["q"].device, d=d)
     out = torch.empty_like(x["q"])
     lse = torch.empty((B, H, L), dtype=torch.float32, device=x["q"].device)
     log_f = x.get("log_f") if fox else None
@@ -789,6 +790,21 @@ def main():
                                          "traffic_kernel": "scan_d128_kernel",
                                          "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
         del xd
+        # fp32 inputs (fp32 CUDA-core preparation and scan) on the bf16 check workload's shape
+        x32 = pi.make_fwd_inputs(4, 16, 2048, dtype=torch.float32, seed=2, clip=0.0, device=dev)
+        s_tot, s_scan, s_prep = time_forward(pa, x32, 3, 3)
+        s_ms = s_tot / 3
+        fa, fc, fp = fwd_flops(4, 16, 2048)
+        s_ach = (fa + fc + fp) / (s_ms * 1e-3) / 1e12
+        line["fwd_f32"] = {"workload": "path_fwd_f32_B4H16L2048", "ms_per_step": s_ms,
+                           "tokens_per_s": 4 * 2048 / (s_ms * 1e-3),
+                           "scan_ms": statistics.mean(s_scan), "prepare_ms": statistics.mean(s_prep),
+                           "roofline": {"kernels": "ut_prepare_kernel<float> + path_scan_f32_kernel",
+                                        "bound": "alu", "achieved": s_ach, "peak": FP32_ALU_TFLOPS,
+                                        "unit": "TFLOP/s", "frac": s_ach / FP32_ALU_TFLOPS,
+                                        "traffic": None,
+                                        "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
+        del x32
         # PaTH-FoX at head size 128 (the scan's early exit decided as it runs)
         xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, fox=True,
                                 device=dev)
