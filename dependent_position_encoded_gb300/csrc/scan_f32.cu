@@ -16,21 +16,77 @@ constexpr int LD = 68;
 constexpr int BUF = kC * LD;
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ void mm_acc(const float *__restrict__ X, const float *__restrict__ Y,
-                                       int m0, int n0, float (&acc)[4][4]) {
-#pragma unroll 4
-    for (int k = 0; k < kC; ++k) {
-        const float4 a = *reinterpret_cast<const float4 *>(X + k * LD + m0);
-        const float4 b = *reinterpret_cast<const float4 *>(Y + k * LD + n0);
-        const float av[4] = {a.x, a.y, a.z, a.w};
-        const float bv[4] = {b.x, b.y, b.z, b.w};
+// acc1[i][j] += sum_k A[r0 + 16i][k] B1[n0 + 16j][k] and acc2 likewise with B2: all three
+// row-major with the contraction (the head dimension) contiguous, each A piece loaded once
+// for both products. The eight lanes of a quarter warp read eight consecutive B rows: at a
+// stride of LD = 68 floats their 16-byte pieces fall in distinct bank groups.
+__device__ __forceinline__ void mm_rows2(const float *__restrict__ A, const float *__restrict__ B1,
+                                         const float *__restrict__ B2, int r0, int n0,
+                                         float (&acc1)[4][4], float (&acc2)[4][4]) {
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+        float4 a[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * LD + k);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) {
+            const float4 b = *reinterpret_cast<const float4 *>((j < 4 ? B1 : B2) + (n0 + 16 * (j & 3)) * LD + k);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float t = j < 4 ? acc1[i][j & 3] : acc2[i][j & 3];
+                t = fmaf(a[i].x, b.x, t);
+                t = fmaf(a[i].y, b.y, t);
+                t = fmaf(a[i].z, b.z, t);
+                t = fmaf(a[i].w, b.w, t);
+                if (j < 4) acc1[i][j & 3] = t;
+                else acc2[i][j & 3] = t;
+            }
+        }
     }
 }
 
+// acc[i][j] += sum_k A[r0 + 16i][k] B[k][c0 + j]: A row-major, B with the contraction as
+// its row index (k-major).
+__device__ __forceinline__ void mm_rowk(const float *__restrict__ A, const float *__restrict__ B,
+                                        int r0, int c0, float (&acc)[4][4]) {
+#pragma unroll 2
+    for (int k = 0; k < kC; k += 4) {
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 16 * i) * LD + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4 b = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                acc[i][0] = fmaf(av, b.x, acc[i][0]);
+                acc[i][1] = fmaf(av, b.y, acc[i][1]);
+                acc[i][2] = fmaf(av, b.z, acc[i][2]);
+                acc[i][3] = fmaf(av, b.w, acc[i][3]);
+            }
+        }
+    }
+}
+
+// 64 rows of 64 floats (row-major in global memory) into shared rows of stride LD; rows at
+// or past `valid` are zero. Four 16-byte loads per thread, all in flight before the stores.
+__device__ __forceinline__ void load_rows64(float *dst, const float *__restrict__ src, int valid) {
+    float4 x[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int e = (int)threadIdx.x + it * kThreads, r = e >> 4;
+        x[it] = r < valid ? reinterpret_cast<const float4 *>(src)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int e = (int)threadIdx.x + it * kThreads, r = e >> 4, c = 4 * (e & 15);
+        *reinterpret_cast<float4 *>(dst + r * LD + c) = x[it];
+    }
+}
+
+// Thread (ty, tx) owns rows ty + 16i of every 64 x 64 product: columns tx + 16j of the
+// logits and the new state, columns 4tx .. 4tx + 3 of the output.
 template <bool FOX>
 __global__ void __launch_bounds__(kThreads)
 path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
@@ -40,13 +96,13 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
                      float *__restrict__ out, float *__restrict__ lse, int L, int Lp, int nblk,
                      float scale_log2) {
     extern __shared__ __align__(16) float sm[];
-    float *XT = sm;          // state, transposed: XT[c][i]
-    float *KT = XT + BUF;    // k~_b transposed: KT[c][j]
-    float *PT = KT + BUF;    // P_b transposed: PT[c][n] = P_b[n][c]
-    float *Vs = PT + BUF;    // V_b[j][c]
+    float *Xr = sm;          // state X[i][c]
+    float *KB = Xr + BUF;    // k~_b [j][c]
+    float *PB = KB + BUF;    // P_b [n][c]
+    float *Vs = PB + BUF;    // V_b [j][c]
     float *Ss = Vs + BUF;    // logits S[i][j] (log2 units)
-    float *PsT = Ss + BUF;   // probabilities, transposed: PsT[j][i]
-    float *alpha_s = PsT + BUF;
+    float *Pm = Ss + BUF;    // probabilities [i][j]
+    float *alpha_s = Pm + BUF;
     float *c2k = alpha_s + kC;
 
     const int tid = threadIdx.x;
@@ -54,7 +110,7 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
     const int bh = blockIdx.y;
     if (ib * kC >= L) return;
     const size_t head = (size_t)bh;
-    const int ty = tid / 16, tx = tid % 16, m0 = ty * 4, n0 = tx * 4;
+    const int ty = tid / 16, tx = tid % 16, c0 = 4 * tx;
     const int row = tid >> 2, part = tid & 3;  // softmax: 4 threads per row
     float m_run = -INFINITY, l_run = 0.f;
     // gate sums relative to the base of their pair of blocks; per key block the row's
@@ -64,10 +120,7 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
     const float2 base_own = FOX ? *reinterpret_cast<const float2 *>(pbase + (head * npair + (ib >> 1)) * 2)
                                 : make_float2(0.f, 0.f);
 
-    for (int e = tid; e < kC * kD; e += kThreads) {
-        const int i = e / kD, c = e % kD;
-        XT[c * LD + i] = qt[(head * Lp + (size_t)ib * kC + i) * kD + c];
-    }
+    load_rows64(Xr, qt + (head * Lp + (size_t)ib * kC) * kD, kC);
     float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -78,17 +131,13 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
     const int b_last = FOX ? first_blk[head * nblk + ib] : 0;
     for (int b = ib; b >= b_last; --b) {
         __syncthreads();
-        for (int e = tid; e < kC * kD; e += kThreads) {
-            const int j = e / kD, c = e % kD;
-            const int t = b * kC + j;
-            Vs[j * LD + c] = (t < L) ? v[(head * L + t) * kD + c] : 0.f;
-            if (b < ib) {
-                const float *blk = kp + ((head * nblk + b) * 2 * kC) * kD;
-                KT[c * LD + j] = blk[j * kD + c];
-                PT[c * LD + j] = blk[(kC + j) * kD + c];
-            } else {
-                Ss[j * LD + c] = dg[((head * nblk + b) * kC + j) * kC + c];
-            }
+        load_rows64(Vs, v + (head * L + (size_t)b * kC) * kD, L - b * kC);
+        if (b < ib) {
+            const float *blk = kp + ((head * nblk + b) * 2 * kC) * kD;
+            load_rows64(KB, blk, kC);
+            load_rows64(PB, blk + kC * kD, kC);
+        } else {
+            load_rows64(Ss, dg + (head * nblk + b) * kC * kC, kC);
         }
         if (FOX && b < ib && tid < kC) c2k[tid] = c2[head * Lp + b * kC + tid];
         float c2_row = 0.f;
@@ -103,18 +152,16 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) s[i][j] = xn[i][j] = 0.f;
-            mm_acc(XT, KT, m0, n0, s);
-            mm_acc(XT, PT, m0, n0, xn);
+            mm_rows2(Xr, KB, PB, ty, tx, s, xn);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4 *>(Ss + (m0 + i) * LD + n0) =
-                    make_float4(s[i][0] * scale_log2, s[i][1] * scale_log2, s[i][2] * scale_log2,
-                                s[i][3] * scale_log2);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) Ss[(ty + 16 * i) * LD + tx + 16 * j] = s[i][j] * scale_log2;
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) XT[(n0 + j) * LD + m0 + i] = xn[i][j];
+                for (int j = 0; j < 4; ++j) Xr[(ty + 16 * i) * LD + tx + 16 * j] = xn[i][j];
         }
         __syncthreads();
         // ---- online softmax, 4 threads per row, 16 columns each
@@ -134,10 +181,14 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float p = exp2f(x[j] - m_use);
-                sum += p;
-                PsT[(part * 16 + j) * LD + row] = p;
+            for (int j = 0; j < 16; j += 4) {
+                float pj[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    pj[q] = exp2f(x[j + q] - m_use);
+                    sum += pj[q];
+                }
+                *reinterpret_cast<float4 *>(Pm + row * LD + part * 16 + j) = make_float4(pj[0], pj[1], pj[2], pj[3]);
             }
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -147,14 +198,13 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
         }
         __syncthreads();
         {
-            float a[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = alpha_s[m0 + i];
+            for (int i = 0; i < 4; ++i) {
+                const float al = alpha_s[ty + 16 * i];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] *= a[i];
-            mm_acc(PsT, Vs, m0, n0, acc);
+                for (int j = 0; j < 4; ++j) acc[i][j] *= al;
+            }
+            mm_rowk(Pm, Vs, ty, c0, acc);
         }
     }
     __syncthreads();
@@ -164,10 +214,10 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int t = ib * kC + m0 + i;
+        const int r = ty + 16 * i, t = ib * kC + r;
         if (t < L) {
-            const float inv = alpha_s[m0 + i];
-            *reinterpret_cast<float4 *>(out + (head * L + t) * kD + n0) =
+            const float inv = alpha_s[r];
+            *reinterpret_cast<float4 *>(out + (head * L + t) * kD + c0) =
                 make_float4(acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv);
         }
     }
