@@ -501,6 +501,9 @@ PROFILE_CASES = {
     # the head-size-128 forward leg's own workload (FP32 ALU-bound kernels)
     "fwd_d128": pi.FwdWorkload("path_fwd_bf16_B4H8L2048_d128", 4, 8, 2048, 128, torch.bfloat16, 12,
                                pi.BETA_CLIP, False),
+    # the fp32-input forward leg's own workload (fp32 CUDA-core kernels)
+    "fwd_f32": pi.FwdWorkload("path_fwd_f32_B4H16L2048", 4, 16, 2048, 64, torch.float32, 2, 0.0,
+                              False),
     # a quarter of the head-size-128 decode workload (B8 H16 d128, 32K cache)
     "decode_d128": pi.DecodeWorkload("path_decode_bf16_B8H16d128N32768x4", 8, 16, 32768, 4, 128,
                                      torch.bfloat16, 5, 1000),
@@ -634,7 +637,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
     ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd", "fwd_d128",
-                                          "decode_d128", "fox_bwd"],
+                                          "decode_d128", "fox_bwd", "fwd_f32"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
