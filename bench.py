@@ -105,6 +105,20 @@ def load_peaks():
             "source": "fallback"}
 
 
+def compact(obj, sig=5):
+    """Rounds every float in a nested dict/list to `sig` significant digits (keeps the JSON
+    line short; integers and strings pass through)."""
+    if isinstance(obj, float):
+        if obj == 0.0 or not math.isfinite(obj):
+            return obj
+        return float("%.*g" % (sig, obj))
+    if isinstance(obj, dict):
+        return {k: compact(v, sig) for k, v in obj.items()}
+    if isinstance(obj, (list, tuple)):
+        return [compact(v, sig) for v in obj]
+    return obj
+
+
 def kernel_source_hash(name):
     src = os.path.join(ROOT, "dependent_position_encoded_gb300", "csrc", name)
     with open(src, "rb") as f:
@@ -439,7 +453,7 @@ def cpu_baseline(x_cpu, wl, target_s=12.0):
                       "time extrapolated by head count" % (n, nh_total, t)}
 
 
-def leg_cpu_baselines(wl_bwd, wl_dec, wl_prod):
+def leg_cpu_baselines(wl_bwd, wl_dec, wl_prod, wl_fox=None):
     """The fp64 oracle beside the backward, decode and producer legs, each on a bounded
     sample of its workload's shapes and distributions (fresh draws of a few heads or
     tokens), extrapolated to the workload in the leg's own unit."""
@@ -480,7 +494,184 @@ def leg_cpu_baselines(wl_bwd, wl_dec, wl_prod):
     out["producer"] = {"value": producer_bytes(wl_prod) / t / 1e9, "unit": "GB/s", "cores": 1,
                        "kind": "oracle", "sample": "%d of %d tokens; time extrapolated by "
                        "token count" % (Lp, wl_prod.B * wl_prod.L)}
+    # the bf16 check workload (B4 H16 L2048): two whole heads, every query row
+    x = pi.make_fwd_inputs(1, 2, wl_bwd.L, seed=wl_bwd.seed, device="cpu")
+    t0 = time.perf_counter()
+    oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    t = (time.perf_counter() - t0) * (wl_bwd.B * wl_bwd.H) / 2
+    out["fwd_L2048"] = {"value": wl_bwd.B * wl_bwd.L / t, "unit": "tokens/s",
+                        "cores": os.cpu_count(), "kind": "oracle",
+                        "sample": "2 of %d heads, every query row; time extrapolated by head "
+                                  "count" % (wl_bwd.B * wl_bwd.H)}
+    if wl_fox is not None:
+        # PaTH-FoX (B8 H16 L16384): 512 seeded query rows of one fresh head; the oracle's
+        # cost of row i is proportional to i + 1, so the time is extrapolated by that sum
+        x = pi.make_fwd_inputs(1, 1, wl_fox.L, seed=wl_fox.seed, fox=True, device="cpu")
+        rows = np.sort(np.random.default_rng(wl_fox.seed).choice(wl_fox.L, 512, replace=False))
+        r2 = np.stack([np.zeros_like(rows), rows], 1)
+        t0 = time.perf_counter()
+        oracle.path_rows(x["q"], x["k"], x["v"], x["w"], x["beta"], r2, log_f=x["log_f"])
+        t = time.perf_counter() - t0
+        L = wl_fox.L
+        t_full = t * (L * (L + 1) / 2) / float((rows + 1).sum()) * (wl_fox.B * wl_fox.H)
+        out["fox"] = {"value": wl_fox.B * L / t_full, "unit": "tokens/s",
+                      "cores": os.cpu_count(), "kind": "oracle",
+                      "sample": "512 query rows of one head (%.1f s); time extrapolated by the "
+                                "rows' cost (i + 1 per row i) and by head count" % t}
     return out
+
+
+# kernels of one bf16 forward at head size 64: UT preprocessing, block-pair products, scan
+LAUNCHES_PER_FWD = 3
+
+
+def bench_parity(pa, x, n_rows=300):
+    """Parity figures carried in the bench line: the tiny fp32 workload against the oracle
+    in full (normwise max|o - o*| / max|o*| and element-wise max |o - o*| / max(|o*|, 1e-3)),
+    and `n_rows` seeded sampled rows of the timed workload (max absolute error, bf16)."""
+    import numpy as np
+    import oracle
+    t = pi.workload_inputs(pi.TINY_FP32, device="cuda")
+    out, _ = pa.path_attn_fwd(t["q"], t["k"], t["v"], t["w"], t["beta"])
+    ref, _ = oracle.path_fwd(t["q"], t["k"], t["v"], t["w"], t["beta"])
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref)
+    res = {"tiny_fp32": {"normwise_rel": float(err.max() / np.abs(ref).max()),
+                         "elementwise_rel": float((err / np.maximum(np.abs(ref), 1e-3)).max()),
+                         "bar": "normwise <= 1e-4"}}
+    B, H, L, d = x["q"].shape
+    rows = pi.sample_rows(B * H, L, n_rows, seed=3)
+    out, _ = pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    got = out.reshape(B * H, L, d)[torch.as_tensor(rows[:, 0]), torch.as_tensor(rows[:, 1])]
+    cpu = {k: v.reshape(B * H, L, -1)[torch.as_tensor(np.unique(rows[:, 0]))].cpu()
+           for k, v in x.items()}
+    remap = {h: i for i, h in enumerate(np.unique(rows[:, 0]))}
+    r2 = np.array([[remap[h], i] for h, i in rows])
+    ref, _ = oracle.path_rows(cpu["q"], cpu["k"], cpu["v"], cpu["w"], cpu["beta"][..., 0], r2)
+    res["speed_workload_rows"] = {"rows": int(len(rows)),
+                                  "max_abs": float(np.abs(got.double().cpu().numpy() - ref).max()),
+                                  "bar": "max_abs <= 2e-2"}
+    return res
+
+
+def run_legs(pa, peaks, dev, rank):
+    """The secondary legs: the bf16 check workload, the producer, the backward (plain and
+    PaTH-FoX), head size 128 (forward and decode), fp32 inputs and the PaTH-FoX decode."""
+    legs = {}
+    wl2 = shard_workload(pi.BF16_L2048, rank)
+    x2 = pi.workload_inputs(wl2, device=dev)
+    t2, sc2, pr2 = time_forward(pa, x2, 5, 3)
+    a, c, p = fwd_flops(wl2.B, wl2.H, wl2.L)
+    legs["fwd_L2048"] = {"workload": wl2.name, "ms_per_step": t2 / 5,
+                         "tokens_per_s": wl2.B * wl2.L / (t2 / 5 * 1e-3),
+                         "tflops": (a + c + p) / (t2 / 5 * 1e-3) / 1e12}
+    del x2
+    prod = time_producer(pa, pi.PRODUCER_L4096)
+    t_down, t_up = ncu_traffic("producer_down_kernel"), ncu_traffic("producer_up_kernel")
+    prod["roofline"] = {"bound": "hbm", "achieved": prod["gbs"], "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": prod["gbs"] / peaks["hbm_gbs"],
+                        "traffic": (t_down + t_up) if (t_down and t_up) else None}
+    legs["producer"] = prod
+    torch.cuda.empty_cache()
+    for fox in (False, True):
+        bwd = time_bwd(pa, pi.BF16_L2048, fox=fox)
+        ach = bwd["query_pass_flops"] / (bwd["ms_per_step"] * 1e-3) / 1e12
+        bwd["roofline"] = BWD_ROOFLINE(ach, peaks, fox)
+        legs["fox_bwd" if fox else "bwd"] = bwd
+        torch.cuda.empty_cache()
+    # head size 128: the bf16 check workload's width in 8 heads
+    xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, device=dev)
+    d_tot, d_scan, d_prep = time_forward(pa, xd, 3, 3)
+    d_ms = d_tot / 3
+    fa, fc, fp = fwd_flops(4, 8, 2048, d=128)
+    d_ach = (fa + fc + fp) / (d_ms * 1e-3) / 1e12
+    legs["fwd_d128"] = {"workload": "path_fwd_bf16_B4H8L2048_d128", "ms_per_step": d_ms,
+                        "tokens_per_s": 4 * 2048 / (d_ms * 1e-3),
+                        "scan_ms": statistics.mean(d_scan), "prepare_ms": statistics.mean(d_prep),
+                        "roofline": D128_ROOFLINE(d_ach, peaks)}
+    del xd
+    xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, fox=True,
+                            device=dev)
+    f_tot, _, _ = time_forward(pa, xd, 3, 3, fox=True)
+    legs["fwd_d128"]["fox_ms_per_step"] = f_tot / 3
+    del xd
+    # fp32 inputs (fp32 CUDA-core preparation and scan) on the bf16 check workload's shape
+    x32 = pi.make_fwd_inputs(4, 16, 2048, dtype=torch.float32, seed=2, clip=0.0, device=dev)
+    s_tot, s_scan, s_prep = time_forward(pa, x32, 3, 3)
+    s_ms = s_tot / 3
+    fa, fc, fp = fwd_flops(4, 16, 2048)
+    s_ach = (fa + fc + fp) / (s_ms * 1e-3) / 1e12
+    legs["fwd_f32"] = {"workload": "path_fwd_f32_B4H16L2048", "ms_per_step": s_ms,
+                       "tokens_per_s": 4 * 2048 / (s_ms * 1e-3),
+                       "roofline": {"bound": "alu", "achieved": s_ach, "peak": FP32_ALU_TFLOPS,
+                                    "unit": "TFLOP/s", "frac": s_ach / FP32_ALU_TFLOPS,
+                                    "traffic": None}}
+    del x32
+    torch.cuda.empty_cache()
+    for key, wl, fox, kern in (("decode_d128", pi.DECODE_32K_D128, False, "decode_split_kernel_d128"),
+                               ("fox_decode", pi.FOX_DECODE_32K, True, "decode_split_kernel_fox")):
+        r = time_decode(pa, wl, fox=fox)
+        r["workload"] = wl.name
+        r["roofline"] = {"bound": "hbm", "achieved": r["gbs"], "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": r["gbs"] / peaks["hbm_gbs"],
+                         "traffic": ncu_traffic(kern)}
+        legs[key] = r
+        torch.cuda.empty_cache()
+    return legs
+
+
+def run_headline_legs(pa, peaks, dev, rank):
+    """The decode step on the 32K cache and the PaTH-FoX forward: printed last in the line."""
+    out = {}
+    dec = time_decode(pa, pi.DECODE_32K)
+    dec["workload"] = pi.DECODE_32K.name
+    dec["roofline"] = {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": dec["gbs"],
+                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": dec["gbs"] / peaks["hbm_gbs"],
+                       "traffic": ncu_traffic("decode_split_kernel"),
+                       "peak_source": "%s HBM copy" % peaks["source"]}
+    out["decode"] = dec
+    torch.cuda.empty_cache()
+    fw = shard_workload(pi.FOX_L16384, rank)
+    xf = pi.workload_inputs(fw, device=dev)
+    fox_total, fox_scan, fox_prep = time_forward(pa, xf, 3, 3, fox=True)
+    fox_ms = fox_total / 3
+    # the early exit skips the key blocks whose weights vanish, so the fixed algorithmic-FLOP
+    # formula does not describe the work done: the scan's rate is taken on the tensor-core
+    # FLOPs of the key blocks it visits (from the recorded extents)
+    wsf = pa.new_workspace(pa.OP_FOX_FWD, fw.B, fw.H, fw.L, pa.BF16, dev)
+    pa.path_fwd_prepare(xf["q"], xf["k"], xf["w"], xf["beta"], wsf, log_f=xf["log_f"])
+    first = pa.path_fox_first_blocks(wsf, fw.B, fw.H, fw.L, xf["q"].dtype).cpu()
+    f_ex = scan_executed_flops(fw.B, fw.H, fw.L, first.reshape(fw.B * fw.H, -1).tolist())
+    del wsf, xf
+    torch.cuda.empty_cache()
+    f_scan = statistics.mean(fox_scan)
+    f_ach = f_ex / (f_scan * 1e-3) / 1e12
+    out["fox"] = {"workload": fw.name, "ms_per_step": fox_ms,
+                  "tokens_per_s": fw.B * fw.L / (fox_ms * 1e-3), "early_exit": True,
+                  "scan_ms": f_scan, "prepare_ms": statistics.mean(fox_prep),
+                  "roofline": {"kernel": "path_scan_tc_kernel<FOX=1>", "bound": "tensor",
+                               "achieved": f_ach, "peak": peaks["bf16_tflops"],
+                               "unit": "TFLOP/s", "frac": f_ach / peaks["bf16_tflops"],
+                               "traffic": ncu_traffic("path_scan_tc_kernel_fox"),
+                               "basis": "executed tensor FLOPs of the visited key blocks",
+                               "executed_flops_per_launch": f_ex}}
+    return out
+
+
+def BWD_ROOFLINE(ach, peaks, fox):
+    return {"kernels": "query-pass FP32 FLOPs over the whole backward call", "bound": "alu",
+            "achieved": ach, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+            "frac": ach / FP32_ALU_TFLOPS,
+            "traffic": ncu_traffic("bwd_query_kernel_fox" if fox else "bwd_query_kernel"),
+            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
+
+
+def D128_ROOFLINE(ach, peaks):
+    return {"kernels": "prep_d128_kernel + scan_d128_kernel", "bound": "alu", "achieved": ach,
+            "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS,
+            "traffic": ncu_traffic("scan_d128_kernel"),
+            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
 
 
 PROFILE_CASES = {
@@ -635,7 +826,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
-    ap.add_argument("--sweep", action="store_true", help="also time the L sweep")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the L sweep")
     ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd", "fwd_d128",
                                           "decode_d128", "fox_bwd", "fwd_f32"],
                     help="run only that operation on a reduced case (for ncu captures)")
@@ -682,7 +873,7 @@ def main():
                 "algorithmic_flops_per_launch": f_attn + f_corr,
                 "executed_tensor_tflops": scan_executed_flops(B, H, L) / (scan_avg * 1e-3) / 1e12,
                 "ms_per_launch": scan_avg}
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    head = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
@@ -695,156 +886,52 @@ def main():
             "fwd_roofline_frac": F / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"],
             "prepare_ms": prep_avg, "scan_ms": scan_avg,
             "roofline": roofline, "clocks": clocks,
-            # per step: UT preprocessing, block-pair products, block scan
-            "gpu_launches": 3 * args.steps}
+            "gpu_launches": LAUNCHES_PER_FWD * args.steps}
+    legs = {}    # secondary legs, printed before the headline legs
+    tail = {}    # decode, PaTH-FoX and the L sweep: printed last
 
     if not args.no_extras:
         n_e2e = max(4, args.steps)
         e2e_ms, h2d, d2h = time_e2e(pa, x, n_e2e, 3)
-        line["e2e"] = {"value": aggregate(e2e_ms, world, B, L, n_e2e)[2], "unit": "tokens/s",
+        head["e2e"] = {"value": aggregate(e2e_ms, world, B, L, n_e2e)[2], "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "overlap": "copy-in, forward and read-back on three streams, "
                                   "double-buffered; every step moves its own bytes"}
+        if rank == 0:
+            head["parity"] = bench_parity(pa, x)
         del x
         torch.cuda.empty_cache()
-        fw = shard_workload(pi.FOX_L16384, rank)
-        xf = pi.workload_inputs(fw, device=dev)
-        fox_total, fox_scan, fox_prep = time_forward(pa, xf, 3, 3, fox=True)
-        fox_ms = fox_total / 3
-        # the early exit skips the key blocks whose weights vanish, so the fixed
-        # algorithmic-FLOP formula does not describe the work done: the scan's rate is taken
-        # on the tensor-core FLOPs of the key blocks it visits (from the recorded extents)
-        wsf = pa.new_workspace(pa.OP_FOX_FWD, fw.B, fw.H, fw.L, pa.BF16, dev)
-        pa.path_fwd_prepare(xf["q"], xf["k"], xf["w"], xf["beta"], wsf, log_f=xf["log_f"])
-        first = pa.path_fox_first_blocks(wsf, fw.B, fw.H, fw.L, xf["q"].dtype).cpu()
-        f_ex = scan_executed_flops(fw.B, fw.H, fw.L, first.reshape(fw.B * fw.H, -1).tolist())
-        del wsf
-        f_scan = statistics.mean(fox_scan)
-        f_ach = f_ex / (f_scan * 1e-3) / 1e12
-        line["fox"] = {"workload": fw.name, "ms_per_step": fox_ms,
-                       "tokens_per_s": fw.B * fw.L / (fox_ms * 1e-3), "early_exit": True,
-                       "scan_ms": f_scan, "prepare_ms": statistics.mean(fox_prep),
-                       "roofline": {"kernel": "path_scan_tc_kernel<FOX=1>", "bound": "tensor",
-                                    "achieved": f_ach, "peak": peaks["bf16_tflops"],
-                                    "unit": "TFLOP/s", "frac": f_ach / peaks["bf16_tflops"],
-                                    "traffic": None,
-                                    "basis": "executed tensor FLOPs of the visited key blocks",
-                                    "executed_flops_per_launch": f_ex}}
-        del xf
-        torch.cuda.empty_cache()
-        dec = time_decode(pa, pi.DECODE_32K)
-        dec["workload"] = pi.DECODE_32K.name
-        dec["roofline"] = {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": dec["gbs"],
-                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": dec["gbs"] / peaks["hbm_gbs"],
-                           "traffic": ncu_traffic("decode_split_kernel"),
-                           "peak_source": "%s HBM copy" % peaks["source"]}
-        line["decode"] = dec
-        fdec = time_decode(pa, pi.FOX_DECODE_32K, fox=True)
-        fdec["workload"] = pi.FOX_DECODE_32K.name
-        fdec["roofline"] = {"kernel": "decode_split_kernel<FOX>", "bound": "hbm",
-                            "achieved": fdec["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": fdec["gbs"] / peaks["hbm_gbs"],
-                            "traffic": ncu_traffic("decode_split_kernel_fox"),
-                            "peak_source": "%s HBM copy" % peaks["source"]}
-        line["fox_decode"] = fdec
-        d128 = time_decode(pa, pi.DECODE_32K_D128)
-        d128["workload"] = pi.DECODE_32K_D128.name
-        d128["roofline"] = {"kernel": "decode_split_kernel<d=128>", "bound": "hbm",
-                            "achieved": d128["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": d128["gbs"] / peaks["hbm_gbs"],
-                            "traffic": ncu_traffic("decode_split_kernel_d128"),
-                            "peak_source": "%s HBM copy" % peaks["source"]}
-        line["decode_d128"] = d128
-        del fdec
-        torch.cuda.empty_cache()
-        prod = time_producer(pa, pi.PRODUCER_L4096)
-        t_down, t_up = ncu_traffic("producer_down_kernel"), ncu_traffic("producer_up_kernel")
-        prod["roofline"] = {"kernels": "producer_down_kernel + producer_up_kernel (+ scale)",
-                            "bound": "hbm", "achieved": prod["gbs"], "peak": peaks["hbm_gbs"],
-                            "unit": "GB/s", "frac": prod["gbs"] / peaks["hbm_gbs"],
-                            "traffic": (t_down + t_up) if (t_down and t_up) else None,
-                            "peak_source": "%s HBM copy" % peaks["source"]}
-        line["producer"] = prod
-        del prod
-        torch.cuda.empty_cache()
-        bwd = time_bwd(pa, pi.BF16_L2048)
-        ach = bwd["query_pass_flops"] / (bwd["ms_per_step"] * 1e-3) / 1e12
-        bwd["roofline"] = {"kernels": "query-pass FP32 FLOPs over the whole backward call",
-                           "bound": "alu", "achieved": ach, "peak": FP32_ALU_TFLOPS,
-                           "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS,
-                           "traffic": ncu_traffic("bwd_query_kernel"), "traffic_kernel": "bwd_query_kernel",
-                           "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
-        line["bwd"] = bwd
-        # head size 128 (fp32 CUDA-core kernels): the bf16 check workload's width in 8 heads
-        xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, device=dev)
-        d_tot, d_scan, d_prep = time_forward(pa, xd, 3, 3)
-        d_ms = d_tot / 3
-        fa, fc, fp = fwd_flops(4, 8, 2048, d=128)
-        d_ach = (fa + fc + fp) / (d_ms * 1e-3) / 1e12
-        line["fwd_d128"] = {"workload": "path_fwd_bf16_B4H8L2048_d128", "ms_per_step": d_ms,
-                            "tokens_per_s": 4 * 2048 / (d_ms * 1e-3),
-                            "scan_ms": statistics.mean(d_scan), "prepare_ms": statistics.mean(d_prep),
-                            "roofline": {"kernels": "prep_d128_kernel + scan_d128_kernel",
-                                         "bound": "alu", "achieved": d_ach,
-                                         "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-                                         "frac": d_ach / FP32_ALU_TFLOPS,
-                                         "traffic": ncu_traffic("scan_d128_kernel"),
-                                         "traffic_kernel": "scan_d128_kernel",
-                                         "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
-        del xd
-        # fp32 inputs (fp32 CUDA-core preparation and scan) on the bf16 check workload's shape
-        x32 = pi.make_fwd_inputs(4, 16, 2048, dtype=torch.float32, seed=2, clip=0.0, device=dev)
-        s_tot, s_scan, s_prep = time_forward(pa, x32, 3, 3)
-        s_ms = s_tot / 3
-        fa, fc, fp = fwd_flops(4, 16, 2048)
-        s_ach = (fa + fc + fp) / (s_ms * 1e-3) / 1e12
-        line["fwd_f32"] = {"workload": "path_fwd_f32_B4H16L2048", "ms_per_step": s_ms,
-                           "tokens_per_s": 4 * 2048 / (s_ms * 1e-3),
-                           "scan_ms": statistics.mean(s_scan), "prepare_ms": statistics.mean(s_prep),
-                           "roofline": {"kernels": "ut_prepare_kernel<float> + path_scan_f32_kernel",
-                                        "bound": "alu", "achieved": s_ach, "peak": FP32_ALU_TFLOPS,
-                                        "unit": "TFLOP/s", "frac": s_ach / FP32_ALU_TFLOPS,
-                                        "traffic": None,
-                                        "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}}
-        del x32
-        # PaTH-FoX at head size 128 (the scan's early exit decided as it runs)
-        xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, fox=True,
-                                device=dev)
-        f_tot, _, _ = time_forward(pa, xd, 3, 3, fox=True)
-        line["fwd_d128"]["fox_ms_per_step"] = f_tot / 3
-        line["fwd_d128"]["fox_tokens_per_s"] = 4 * 2048 / (f_tot / 3 * 1e-3)
-        del xd
-        torch.cuda.empty_cache()
-        fbwd = time_bwd(pa, pi.BF16_L2048, fox=True)
-        ach = fbwd["query_pass_flops"] / (fbwd["ms_per_step"] * 1e-3) / 1e12
-        fbwd["roofline"] = dict(bwd["roofline"], achieved=ach, frac=ach / FP32_ALU_TFLOPS,
-                                traffic=ncu_traffic("bwd_query_kernel_fox"))
-        line["fox_bwd"] = fbwd
+        legs.update(run_legs(pa, peaks, dev, rank))
+        tail.update(run_headline_legs(pa, peaks, dev, rank))
 
-    if args.sweep and rank == 0:
+    if not args.no_sweep and rank == 0:
         sweep = {}
         for Ls in pi.SPEED_SWEEP_L:
             xs = pi.workload_inputs(pi.speed_shape(Ls), device=dev)
             tot, sc, pr = time_forward(pa, xs, 3, 3)
             a, c, p = fwd_flops(32, 32, Ls)
             sweep[str(Ls)] = {"ms": tot / 3, "tflops": (a + c + p) / (tot / 3 * 1e-3) / 1e12,
-                              "tokens_per_s": 32 * Ls / (tot / 3 * 1e-3)}
+                              "frac": (a + c + p) / (tot / 3 * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                              "Mtok_s": 32 * Ls / (tot / 3 * 1e-3) / 1e6}
             del xs
             torch.cuda.empty_cache()
-        line["sweep_L"] = sweep
+        tail["sweep_L"] = sweep
 
-    if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
-        legs = leg_cpu_baselines(pi.BF16_L2048, pi.DECODE_32K, pi.PRODUCER_L4096)
-        for name, cb in legs.items():
-            if name in line:
-                line[name]["cpu_baseline"] = cb
     if rank == 0 and not args.no_cpu_baseline:
+        if not args.no_extras:
+            for name, cb in leg_cpu_baselines(pi.BF16_L2048, pi.DECODE_32K, pi.PRODUCER_L4096,
+                                              pi.FOX_L16384).items():
+                target = tail if name in tail else legs
+                if name in target:
+                    target[name]["cpu_baseline"] = cb
         xc = pi.make_fwd_inputs(1, 64, wl.L, seed=wl.seed, device="cpu")
-        line["cpu_baseline"] = cpu_baseline(xc, pi.FwdWorkload(wl.name, wl.B, wl.H, wl.L, 64,
+        head["cpu_baseline"] = cpu_baseline(xc, pi.FwdWorkload(wl.name, wl.B, wl.H, wl.L, 64,
                                                                wl.dtype, wl.seed, wl.clip, False))
     if rank == 0:
-        print(json.dumps(line))
+        line = dict(head)
+        line.update(legs)
+        line.update(tail)
+        print(json.dumps(compact(line)))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -328,27 +328,37 @@ def path_fox_first_blocks(workspace, B, H, L, dtype, stream=None, d=HEAD_DIM):
 
 
 def _decode_args(q, k, v, w, beta, k_cache, v_cache, out):
+    """Checks the decode arguments and returns (inputs, out, (B, H, cap, d)). Shapes and
+    dtypes are checked before devices, so every size error is raised before any call."""
     torch = _torch()
-    _cuda_tensor(k_cache, "k_cache")
+    named = [(k_cache, "k_cache"), (v_cache, "v_cache"), (q, "q"), (k, "k"), (v, "v"),
+             (w, "w"), (beta, "beta")] + ([(out, "out")] if out is not None else [])
+    for t, n in named:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a tensor" % n)
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must have shape (B, H, cap, d)")
     dt_t = k_cache.dtype
     B, H, cap, d = k_cache.shape
-    _cuda_tensor(v_cache, "v_cache", dt_t)
-    if v_cache.shape != k_cache.shape:
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
         raise ValueError("v_cache must match k_cache")
-    ins = []
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (w, "w")):
-        _cuda_tensor(t, n, dt_t)
-        if t.numel() != B * H * d:
-            raise ValueError("%s must hold (B, H, d) values" % n)
-        ins.append(t)
-    _cuda_tensor(beta, "beta", torch.float32)
-    if beta.numel() != B * H:
-        raise ValueError("beta must hold (B, H) values")
+    for t, n, dt, count in ((v_cache, "v_cache", dt_t, None), (q, "q", dt_t, B * H * d),
+                            (k, "k", dt_t, B * H * d), (v, "v", dt_t, B * H * d),
+                            (w, "w", dt_t, B * H * d), (beta, "beta", torch.float32, B * H),
+                            (out, "out", dt_t, B * H * d)):
+        if t is None:
+            continue
+        if t.dtype != dt:
+            raise TypeError("%s must be %s, got %s" % (n, dt, t.dtype))
+        if count is not None and t.numel() != count:
+            raise ValueError("%s must hold %d values, got %d" % (n, count, t.numel()))
+    for t, n in named:
+        _cuda_tensor(t, n)
+        if t.device != k_cache.device:
+            raise ValueError("%s must be on %s" % (n, k_cache.device))
     if out is None:
         out = torch.empty((B, H, d), dtype=dt_t, device=k_cache.device)
-    else:
-        _cuda_tensor(out, "out", dt_t)
-    return ins, out, (B, H, cap, d)
+    return [q, k, v, w], out, (B, H, cap, d)
 
 
 def path_decode_step(q, k, v, w, beta, k_cache, v_cache, cache_len, scale=None, out=None,
@@ -405,14 +415,7 @@ def path_decode_step_noalloc(q, k, v, w, beta, k_cache, v_cache, cache_len, scal
     for the library on the call path. The split partials live in a fixed 16 MiB array inside
     the library; calls that overlap on one GPU share it and must be serialised. Raises
     PathError(ERR_WORKSPACE) when B * H * ceil(cache_len / 1024) partials do not fit."""
-    torch = _torch()
-    _cuda_tensor(k_cache, "k_cache")
-    B, H, cap, d = k_cache.shape
-    _cuda_tensor(v_cache, "v_cache", k_cache.dtype)
-    ins = [_cuda_tensor(t, n, k_cache.dtype) for t, n in ((q, "q"), (k, "k"), (v, "v"), (w, "w"))]
-    _cuda_tensor(beta, "beta", torch.float32)
-    if out is None:
-        out = torch.empty((B, H, d), dtype=k_cache.dtype, device=k_cache.device)
+    ins, out, (B, H, cap, d) = _decode_args(q, k, v, w, beta, k_cache, v_cache, out)
     _check(_load().path_decode_step_noalloc(_ptr(ins[0]), _ptr(ins[1]), _ptr(ins[2]),
                                             _ptr(ins[3]), _ptr(beta), _ptr(k_cache),
                                             _ptr(v_cache), B, H, int(cache_len), cap, d,

@@ -373,22 +373,61 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // context id the pointer belongs to
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Id of the calling thread's current context (unique for the life of the process, so a
+// context created after a device reset never matches one from before it).
+cudaError_t current_context_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &r1) != cudaSuccess ||
+            r1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) !=
+                cudaSuccess ||
+            r2 != cudaDriverEntryPointSuccess)
+            return cudaErrorNotSupported;
+        get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        get_id = reinterpret_cast<CtxGetIdFn>(q);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+    if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
 }  // namespace
 
 // Device address of the static scratch on the current device. The first call on a
-// device looks it up (host code only holds a stand-in for the symbol, never its device
-// address) and caches it; later calls reuse the cached pointer.
+// device (with that device current) looks it up: host code only holds a stand-in for
+// the symbol, never its device address. The pointer is cached together with the id of
+// the context it was looked up in; after a device reset the runtime makes a new context
+// (and reloads the module), the ids differ and the address is looked up again.
 static cudaError_t static_scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    // no context may be current yet on this thread (the runtime makes the primary context
+    // current on first use, which the symbol lookup below is)
+    std::lock_guard<std::mutex> lock(g_scratch_mu);  // also guards the entry-point lookup
+    unsigned long long ctx_id = 0;
+    const bool have_id = current_context_id(&ctx_id) == cudaSuccess;
+    if (!have_id || g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx_id) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess) return e;
+        if (!have_id) {
+            e = current_context_id(&ctx_id);
+            if (e != cudaSuccess) return e;
+        }
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx_id;
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;

@@ -83,6 +83,12 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype);
 
 /*
  * PaTH forward: out = softmax_j(scale * k_j^T (H_{j+1}...H_i) q_i) v, causal.
+ * Defined in review "거리에서 경로로, PaTH Attention" §3 (the data-dependent transition
+ * H_s = I - beta_s w_s w_s^T and the logit through the product of the transitions between
+ * key and query) and §4 (softmax attention over those logits); technical summary
+ * "技術要約: PaTH Attention" §2 "コアメカニズム". Computed blockwise as in technical
+ * summary §3 (UT-form block factors, boundary-adjusted queries and keys, a right-to-left
+ * scan with online softmax).
  *   q, k, v, w : (B, H, L, d) dtype      beta : (B, H, L) fp32
  *   out        : (B, H, L, d) dtype      lse  : (B, H, L) fp32, natural-log
  *                                               log-sum-exp of the logits; may be NULL
@@ -194,7 +200,8 @@ path_status path_fox_first_blocks(const void *ws, size_t ws_bytes, int B, int H,
                                   int d, int dtype, int *first_block, void *stream);
 
 /*
- * One PaTH decode step (the pages' inference scheme: the new token's
+ * One PaTH decode step (the inference scheme of review "거리에서 경로로, PaTH Attention"
+ * §9 and technical summary "技術要約: PaTH Attention" §3 "推論": the new token's
  * transition updates the cached keys in place, no w/beta cache is kept):
  *   1. k_j <- H_t k_j = k_j - beta_t (w_t . k_j) w_t for every cached j < cache_len,
  *      written back into k_cache (rounded to dtype);
@@ -249,7 +256,10 @@ path_status path_fox_decode_step(const void *q, const void *k, const void *v, co
  * B*H = 1024 heads with up to 63488 cached keys); larger problems return
  * PATH_ERR_WORKSPACE before any launch. The call allocates nothing. The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call outside any stream capture. All calls on a device share
+ * current; make that first call outside any stream capture. The address is kept per
+ * device together with the id of the context it was looked up in: after a device reset
+ * (cudaDeviceReset, or the primary context released and made again) the next call looks
+ * it up again, and that call, too, should come before any stream capture. All calls on a device share
  * the array: calls that may overlap on the GPU (different streams or host threads) race
  * and must be serialised by the caller. No part of the array needs to start at zero.
  */

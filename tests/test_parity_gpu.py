@@ -38,12 +38,20 @@ def check_bf16(got, ref, lse=None, ref_lse=None):
 
 # ---------------------------------------------------------------- fp32
 
-def test_tiny_fp32_workload(lib):
+def test_tiny_fp32_workload(lib, record_property):
     x = pi.workload_inputs(pi.TINY_FP32, device="cuda")
     out, lse = run_fwd(lib, x)
     ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
-    rel = np.abs(out.double().cpu().numpy() - ref).max() / np.abs(ref).max()
+    err = np.abs(out.double().cpu().numpy() - ref)
+    rel = err.max() / np.abs(ref).max()
     assert rel <= F32_MAX_REL, rel
+    # the element-wise figure |o - o*| / max(|o*|, 1e-3), reported beside the normwise one;
+    # the normwise bar implies it is at most 1e-4 * max|o*| / 1e-3 everywhere
+    elem = (err / np.maximum(np.abs(ref), 1e-3)).max()
+    record_property("normwise_rel", float(rel))
+    record_property("elementwise_rel", float(elem))
+    print("tiny fp32: normwise %.3g, element-wise %.3g" % (rel, elem))
+    assert elem <= F32_MAX_REL * np.abs(ref).max() / 1e-3
     assert np.abs(lse.double().cpu().numpy() - ref_lse).max() <= 1e-4
 
 
@@ -504,11 +512,13 @@ def test_decode_head_dim_128(lib, dtype):
 
 
 def test_decode_workload_sampled_heads(lib):
+    # 16 heads spread over the batch, compared with the oracle at every one of the 64 steps
     wl = pi.DECODE_32K
     cap = wl.n_prefix + wl.steps
     kc, vc = pi.make_decode_prefix(wl, cap, device="cuda")
-    heads = [0, 77, 513, 1023]
     nh = wl.B * wl.H
+    heads = sorted({0, nh - 1} | {int(h) for h in np.linspace(37, nh - 2, 14)})
+    assert len(heads) == 16
     ocache = oracle.DecodeCache(kc.reshape(nh, cap, 64)[heads, :wl.n_prefix].cpu(),
                                 vc.reshape(nh, cap, 64)[heads, :wl.n_prefix].cpu(), cap)
     ws = lib.new_workspace(lib.OP_DECODE, wl.B, wl.H, cap, lib.BF16, "cuda")
@@ -517,16 +527,11 @@ def test_decode_workload_sampled_heads(lib):
         s = pi.make_decode_step(wl, t, device="cuda")
         o = lib.path_decode_step(s["q"], s["k"], s["v"], s["w"], s["beta"], kc, vc,
                                  wl.n_prefix + t, workspace=ws)
-        if t % 8 == 7 or t == 0:
-            sel = {k: v.reshape(nh, -1)[heads].cpu() for k, v in s.items()}
-            # the oracle steps every time; compare on a subset of steps
-            ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
-            got = o.reshape(nh, 64)[heads].double().cpu().numpy()
-            assert np.abs(got - ref).max() <= BF16_MAX_ABS
-            rel.append(np.abs(got - ref).max() / np.abs(ref).max())
-        else:
-            sel = {k: v.reshape(nh, -1)[heads].cpu() for k, v in s.items()}
-            ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
+        sel = {k: v.reshape(nh, -1)[heads].cpu() for k, v in s.items()}
+        ref = ocache.step(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"])
+        got = o.reshape(nh, 64)[heads].double().cpu().numpy()
+        assert np.abs(got - ref).max() <= BF16_MAX_ABS, t
+        rel.append(np.abs(got - ref).max() / np.abs(ref).max())
     assert max(rel) <= 5e-2, rel
 
 
