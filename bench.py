@@ -504,20 +504,16 @@ def leg_cpu_baselines(wl_bwd, wl_dec, wl_prod, wl_fox=None):
                         "sample": "2 of %d heads, every query row; time extrapolated by head "
                                   "count" % (wl_bwd.B * wl_bwd.H)}
     if wl_fox is not None:
-        # PaTH-FoX (B8 H16 L16384): 512 seeded query rows of one fresh head; the oracle's
-        # cost of row i is proportional to i + 1, so the time is extrapolated by that sum
-        x = pi.make_fwd_inputs(1, 1, wl_fox.L, seed=wl_fox.seed, fox=True, device="cpu")
-        rows = np.sort(np.random.default_rng(wl_fox.seed).choice(wl_fox.L, 512, replace=False))
-        r2 = np.stack([np.zeros_like(rows), rows], 1)
+        # PaTH-FoX (B8 H16 L16384): two whole fresh heads, every query row
+        x = pi.make_fwd_inputs(1, 2, wl_fox.L, seed=wl_fox.seed, fox=True, device="cpu")
         t0 = time.perf_counter()
-        oracle.path_rows(x["q"], x["k"], x["v"], x["w"], x["beta"], r2, log_f=x["log_f"])
+        oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], log_f=x["log_f"])
         t = time.perf_counter() - t0
-        L = wl_fox.L
-        t_full = t * (L * (L + 1) / 2) / float((rows + 1).sum()) * (wl_fox.B * wl_fox.H)
-        out["fox"] = {"value": wl_fox.B * L / t_full, "unit": "tokens/s",
+        t_full = t * (wl_fox.B * wl_fox.H) / 2
+        out["fox"] = {"value": wl_fox.B * wl_fox.L / t_full, "unit": "tokens/s",
                       "cores": os.cpu_count(), "kind": "oracle",
-                      "sample": "512 query rows of one head (%.1f s); time extrapolated by the "
-                                "rows' cost (i + 1 per row i) and by head count" % t}
+                      "sample": "2 of %d heads, every query row (%.1f s); time extrapolated "
+                                "by head count" % (wl_fox.B * wl_fox.H, t)}
     return out
 
 
