@@ -51,6 +51,13 @@ cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const 
 template <typename T>
 cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int B, int H, int L,
                              float scale, void *ws, cudaStream_t stream);
+size_t bwd_tc_ws_bytes(int B, int H, int L, bool fox);
+cudaError_t launch_path_bwd_tc(const void *q, const void *k, const void *v, const void *w,
+                               const float *beta, const float *log_f, const void *o,
+                               const float *lse, const void *dout, int B, int H, int L,
+                               float scale, float *dq, float *dk, float *dv, float *dw,
+                               float *dbeta, float *dlogf, void *ws, uint64_t limit_ns,
+                               cudaStream_t stream);
 size_t decode_static_scratch_bytes();
 size_t decode_static_scratch_needed(int BH, int cache_len, int d);
 template <typename T>
@@ -168,6 +175,10 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
 }  // namespace
 
 namespace {
+size_t bwd_ws_bytes(int B, int H, int L, int dtype, bool fox) {
+    return dtype == PATH_BF16 ? bwd_tc_ws_bytes(B, H, L, fox) : bwd_layout(B, H, L, fox).total;
+}
+
 path_status bwd_impl(const void *q, const void *k, const void *v, const void *w, const float *beta,
                      const float *log_f, const void *out, const float *lse, const void *d_out,
                      int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
@@ -183,14 +194,16 @@ path_status bwd_impl(const void *q, const void *k, const void *v, const void *w,
         if (!p) return PATH_ERR_NULL;
     for (const void *p : in)
         if (!aligned(p, 16)) return PATH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, bwd_layout(B, H, L, fox).total)) != PATH_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, bwd_ws_bytes(B, H, L, dtype, fox))) != PATH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float *lf = fox ? log_f : nullptr;
     float *dlf = fox ? dlog_f : nullptr;
+    // bf16 inputs: tensor-core query pass; fp32 inputs: the fp32 CUDA-core kernels, whose
+    // accuracy the fp32 bar needs
     cudaError_t e = dtype == PATH_BF16
-                        ? launch_path_bwd<__nv_bfloat16>(q, k, v, w, beta, lf, out, lse, d_out, B,
-                                                         H, L, scale, dq, dk, dv, dw, dbeta, dlf,
-                                                         ws, s)
+                        ? launch_path_bwd_tc(q, k, v, w, beta, lf, out, lse, d_out, B, H, L,
+                                             scale, dq, dk, dv, dw, dbeta, dlf, ws, kWaitLimitNs,
+                                             s)
                         : launch_path_bwd<float>(q, k, v, w, beta, lf, out, lse, d_out, B, H, L,
                                                  scale, dq, dk, dv, dw, dbeta, dlf, ws, s);
     return from_cuda(e);
@@ -210,7 +223,7 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
     }
     if (op == PATH_OP_BWD || op == PATH_OP_FOX_BWD) {
         if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
-        return bwd_layout(B, H, L, op == PATH_OP_FOX_BWD).total;
+        return bwd_ws_bytes(B, H, L, dtype, op == PATH_OP_FOX_BWD);
     }
     if (check_decode_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
     switch (op) {

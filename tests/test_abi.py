@@ -81,25 +81,41 @@ def test_workspace_sizes(lib):
 
 
 def test_bwd_workspace_size(lib):
-    # fp32 q~ (Lp x 64), [k~; P_b] (nblk x 128 x 64), diagonal logits, dq~, dk~, dP_b, diagonal
-    # dT, and per pair b < a the carried query block and its logit gradient (2 x 64 x 64)
+    # fp32 inputs: fp32 q~ (Lp x 64), [k~; P_b] (nblk x 128 x 64), diagonal logits, dq~, dk~,
+    # dP_b, diagonal dT, and per pair b < a the carried query block and its logit gradient
+    # (2 x 64 x 64)
     L, nb = 130, 3
     rows, blocks = nb * 64 * 64 * 4, nb * 64 * 64 * 4
     want = 256 + rows + 2 * blocks + blocks + rows + rows + blocks + blocks + 3 * 2 * 64 * 64 * 4
-    for dt in (lib.F32, lib.BF16):
-        assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, dt) == want
-    assert lib.path_workspace_bytes(lib.OP_BWD, 2, 3, L, 64, lib.BF16) == 256 + 6 * (want - 256)
+    assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, lib.F32) == want
+    # bf16 inputs (tensor-core query pass): the forward's bf16 preparation workspace, fp32
+    # dq~, dk~ (Lp x 64), dP_b and diagonal dT (nblk x 64 x 64), and the bf16 stash: per
+    # tile t of two query blocks, records b = 0 .. 2t of [X_b; dT_b] (256 x 64), i.e.
+    # (blocks rounded up to even / 2)^2 records per head
+    fwd = lib.path_workspace_bytes(lib.OP_FWD, 1, 1, L, 64, lib.BF16)
+    npair = 2
+    want16 = fwd + 2 * rows + 2 * blocks + npair * npair * 256 * 64 * 2
+    assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, lib.BF16) == want16
+    fwd6 = lib.path_workspace_bytes(lib.OP_FWD, 2, 3, L, 64, lib.BF16)
+    assert lib.path_workspace_bytes(lib.OP_BWD, 2, 3, L, 64, lib.BF16) == \
+        fwd6 + 6 * (want16 - fwd)
     assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, 128, 128, lib.BF16) == 0
 
 
 def test_fox_bwd_workspace_size(lib):
     # the plain backward's workspace plus block-local gate sums, row and column sums of dS
-    # (Lp fp32 each) and per-block fp64 gate prefixes, each region rounded up to 256 B
+    # (Lp fp32 each) and per-block fp64 gate prefixes, each region rounded up to 256 B; for
+    # bf16 inputs the forward preparation part is the PaTH-FoX one
     L, nb = 130, 3
-    plain = lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, lib.F32)
     tok = nb * 64 * 4
-    want = plain + 3 * tok + (nb * 8 + 255) // 256 * 256
-    assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 64, lib.BF16) == want
+    extra = 3 * tok + (nb * 8 + 255) // 256 * 256
+    plain = lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, lib.F32)
+    assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 64, lib.F32) == plain + extra
+    plain16 = lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 64, lib.BF16)
+    fwd = lib.path_workspace_bytes(lib.OP_FWD, 1, 1, L, 64, lib.BF16)
+    fwd_fox = lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, L, 64, lib.BF16)
+    assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 64, lib.BF16) == \
+        plain16 - fwd + fwd_fox + extra
     assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 96, lib.BF16) == 0
 
 

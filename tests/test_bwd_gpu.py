@@ -199,3 +199,60 @@ def test_fox_bwd_short(lib, L):
     x, d_out, grads = _fox_case(lib, 1, 2, L, torch.float32, seed=60 + L)
     ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, log_f=x["log_f"])
     _compare(grads, ref, 1e-4)
+
+
+# ---------------------------------------------------------------- bf16: tensor-core query pass
+
+@pytest.mark.parametrize("L", [1, 64, 127, 384, 1000])
+def test_bwd_bf16_lengths(lib, L):
+    # one token, one block, a ragged second block, six blocks (interior P_b) and 16 blocks
+    # with a ragged last one: the tile steps, the diagonal pair and the pass-2 walk
+    x, d_out, grads = _case(lib, 1, 2, L, torch.bfloat16, seed=700 + L)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("kind", ["beta_zero", "projection", "reflection", "identity", "scale"])
+def test_bwd_bf16_special_transitions(lib, kind):
+    x = pi.make_fwd_inputs(1, 2, 300, seed=77, dtype=torch.bfloat16, device="cuda")
+    scale = None
+    if kind == "beta_zero":
+        x["beta"] = torch.zeros_like(x["beta"])
+    elif kind == "projection":
+        x["beta"] = torch.ones_like(x["beta"])
+    elif kind == "reflection":
+        x["beta"] = torch.full_like(x["beta"], 2.0)
+    elif kind == "identity":
+        x["w"] = torch.zeros_like(x["w"])
+    else:
+        scale = 0.3
+    d_out = torch.randn((1, 2, 300, 64), generator=torch.Generator().manual_seed(78))
+    d_out = d_out.to(torch.bfloat16).cuda()
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=scale)
+    grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out,
+                              scale=scale)
+    torch.cuda.synchronize()
+    if kind in ("beta_zero", "identity"):
+        assert torch.count_nonzero(grads["dw"]) == 0
+    if kind == "identity":
+        assert torch.count_nonzero(grads["dbeta"]) == 0
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, scale=scale)
+    _compare(grads, ref, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("L,gate_scale", [(1, 1.0), (64, 1.0), (700, 1.0), (700, 20.0)])
+def test_fox_bwd_bf16(lib, L, gate_scale):
+    x, d_out, grads = _fox_case(lib, 1, 2, L, torch.bfloat16, seed=900 + L,
+                                gate_scale=gate_scale)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, log_f=x["log_f"])
+    _compare(grads, ref, TOL[torch.bfloat16])
+
+
+def test_bwd_bf16_deterministic_up_to_atomics(lib):
+    # two runs agree within fp32 reassociation of the gathered gradients
+    x, d_out, g1 = _case(lib, 1, 3, 500, torch.bfloat16, seed=5)
+    out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    g2 = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out)
+    for n in NAMES:
+        a, b = g1[n].double(), g2[n].double()
+        assert (a - b).abs().max().item() <= 1e-4 * max(b.abs().max().item(), 1e-6), n
