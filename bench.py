@@ -372,7 +372,7 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def bwd_flops(B, H, L):
-    """FP32 FLOPs of the backward's query pass (the 64 x 64 x 64 products it forms, each
+    """Algorithmic FLOPs of the backward's query pass (the 64 x 64 x 64 products it forms, each
     2 * 64^3): per pair of query block a and key block b < a, the logits, dout V_b^T, the
     dk~ and dv terms and dT K~_b (5 products), plus X P_b^T, G P_b and the dP_b term when
     b > 0 (3 more); per diagonal block dout V^T and p^T dout."""
@@ -570,9 +570,12 @@ def run_legs(pa, peaks, dev, rank):
     legs["producer"] = prod
     torch.cuda.empty_cache()
     for fox in (False, True):
-        bwd = time_bwd(pa, pi.BF16_L2048, fox=fox)
-        ach = bwd["query_pass_flops"] / (bwd["ms_per_step"] * 1e-3) / 1e12
-        bwd["roofline"] = BWD_ROOFLINE(ach, peaks, fox)
+        wlb = pi.BF16_L2048
+        bwd = time_bwd(pa, wlb, fox=fox)
+        sec = bwd["ms_per_step"] * 1e-3
+        ach = bwd["query_pass_flops"] / sec / 1e12
+        ex = bwd_tc_executed_flops(wlb.B, wlb.H, wlb.L) / sec / 1e12
+        bwd["roofline"] = BWD_ROOFLINE(ach, peaks, fox, ex)
         legs["fox_bwd" if fox else "bwd"] = bwd
         torch.cuda.empty_cache()
     # head size 128: the bf16 check workload's width in 8 heads
@@ -655,19 +658,40 @@ def run_headline_legs(pa, peaks, dev, rank):
     return out
 
 
-def BWD_ROOFLINE(ach, peaks, fox):
-    return {"kernels": "query-pass FP32 FLOPs over the whole backward call", "bound": "alu",
-            "achieved": ach, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-            "frac": ach / FP32_ALU_TFLOPS,
-            "traffic": ncu_traffic("bwd_query_kernel_fox" if fox else "bwd_query_kernel"),
-            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
+def bwd_tc_executed_flops(B, H, L):
+    """Tensor-core FLOPs the bf16 backward's query pass issues (128-row tiles t of query
+    blocks 2t, 2t+1): pass 1, per key block, [S|X'] = X [K~; P]^T (N = 128, not at the tile's
+    first, diagonal-only step), dout V^T (N = 64) and [p^T; dT^T][X | dout] (N = 128,
+    K = 128); pass 2, per key block, dT K~ and, past the first, G_hi P + G_lo P and
+    [G_hi^T; G_lo^T] X (K = 128)."""
+    nbe = -(-L // 64)
+    nbe += nbe & 1
+    u = 2.0 * 128 * 64 * 64  # one M = 128, N = 64, K = 64 product
+    total = 0.0
+    for t in range(nbe // 2):
+        s1 = 2 * t + 2
+        total += (s1 - 1) * 2 * u + s1 * u + s1 * 4 * u
+        s2 = 2 * t + 1
+        total += s2 * u + (s2 - 1) * (2 * u + 2 * u)
+    return B * H * total
+
+
+def BWD_ROOFLINE(ach, peaks, fox, executed=None):
+    return {"kernels": "query-pass algorithmic FLOPs (the 64 x 64 x 64 products of the "
+                       "gradient) over the whole backward call", "bound": "tensor",
+            "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"],
+            "traffic": ncu_traffic("bwd_query_tc_kernel_fox" if fox else "bwd_query_tc_kernel"),
+            "executed_tensor_tflops": executed,
+            "peak_source": "%s bf16 dense (burst)" % peaks["source"]}
 
 
 def D128_ROOFLINE(ach, peaks):
-    return {"kernels": "prep_d128_kernel + scan_d128_kernel", "bound": "alu", "achieved": ach,
-            "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP32_ALU_TFLOPS,
-            "traffic": ncu_traffic("scan_d128_kernel"),
-            "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz (nominal)"}
+    return {"kernels": "ut_prepare_tc128_kernel + scan_tc128_kernel (tcgen05)",
+            "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+            "traffic": ncu_traffic("scan_tc128_kernel"),
+            "peak_source": "%s bf16 dense (burst)" % peaks["source"]}
 
 
 PROFILE_CASES = {

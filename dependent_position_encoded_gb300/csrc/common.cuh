@@ -51,6 +51,43 @@ struct D128Layout {
 };
 D128Layout d128_layout(int B, int H, int L, bool fox);
 
+// Workspace of the tensor-core d = 128 forward (bf16 inputs). nblk = ceil(L / 64) rounded up
+// to even, Lp = 64 nblk:
+//   qt  : (BH, Lp, 128) bf16 boundary-adjusted queries
+//   kp  : (BH, nblk, 192, 128) bf16: rows 0-63 k~_j, rows 64-191 the block transition P_b
+//   dg  : (BH, nblk, 64, 64) fp16 diagonal-block logits, log2 units, -inf where masked
+//   PaTH-FoX: lc2, tail2 (BH, Lp) fp32 in-block inclusive gate sums and the keys' tail sums
+//   T2_b - lc2_j, tot2 (BH, nblk) fp64 block totals, all in log2 units
+struct D128TcLayout {
+    int BH, nblk, Lp;
+    size_t off_qt, off_kp, off_dg, off_lc2, off_tail2, off_tot2, total;
+};
+inline D128TcLayout d128_tc_layout(int B, int H, int L, bool fox) {
+    D128TcLayout y;
+    y.BH = B * H;
+    const int nb = (L + kC - 1) / kC;
+    y.nblk = (nb + 1) & ~1;
+    y.Lp = y.nblk * kC;
+    const size_t bh = (size_t)y.BH;
+    size_t off = 256;
+    y.off_qt = off;
+    off = align256(off + bh * y.Lp * 128 * 2);
+    y.off_kp = off;
+    off = align256(off + bh * y.nblk * 192 * 128 * 2);
+    y.off_dg = off;
+    off = align256(off + bh * y.nblk * kC * kC * 2);
+    y.off_lc2 = y.off_tail2 = y.off_tot2 = off;
+    if (fox) {
+        off = align256(off + bh * y.Lp * 4);
+        y.off_tail2 = off;
+        off = align256(off + bh * y.Lp * 4);
+        y.off_tot2 = off;
+        off = align256(off + bh * y.nblk * 8);
+    }
+    y.total = off;
+    return y;
+}
+
 // Workspace of the backward pass (defined in backward.cu).
 struct BwdLayout {
     int BH, nblk, Lp;

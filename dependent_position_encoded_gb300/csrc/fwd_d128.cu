@@ -1,5 +1,6 @@
-// PaTH forward at head size d = 128, fp32 on the CUDA cores (both input dtypes; the output
-// keeps the input dtype). The same algorithm as the d = 64 kernels (technical summary
+// PaTH forward at head size d = 128 for fp32 inputs, fp32 on the CUDA cores (the fp32 bar
+// needs fp32 products; bf16 inputs take the tensor-core kernels of ut_prepare_tc.cu and
+// scan_tc128.cu). The same algorithm as the d = 64 kernels (technical summary
 // "技術要約: PaTH Attention" §3 "UT変換による表現" and the block-wise algorithm; review
 // "거리에서 경로로, PaTH Attention" §9, which flags larger heads as costlier): per block of
 // C = 64 tokens the UT factor A = (I + D N)^{-1} D with N = strictly-upper(W W^T), the
@@ -789,7 +790,6 @@ cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int
     template cudaError_t launch_scan_d128<T>(const void *, void *, float *, bool, int, int, int,  \
                                              float, void *, cudaStream_t);
 PATH_D128_INST(float)
-PATH_D128_INST(__nv_bfloat16)
 #undef PATH_D128_INST
 
 }  // namespace path

@@ -51,6 +51,12 @@ cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const 
 template <typename T>
 cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int B, int H, int L,
                              float scale, void *ws, cudaStream_t stream);
+cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
+                                    const float *beta, const float *log_f, int BH, int L,
+                                    float scale, void *ws, uint64_t limit_ns,
+                                    cudaStream_t stream);
+cudaError_t launch_scan_tc128(const void *v, void *out, float *lse, bool fox, int BH, int L,
+                              float scale, void *ws, uint64_t limit_ns, cudaStream_t stream);
 size_t bwd_tc_ws_bytes(int B, int H, int L, bool fox);
 cudaError_t launch_path_bwd_tc(const void *q, const void *k, const void *v, const void *w,
                                const float *beta, const float *log_f, const void *o,
@@ -113,6 +119,14 @@ path_status check_ws(void *ws, size_t ws_bytes, size_t need) {
     return PATH_OK;
 }
 
+// Forward workspace size for a (d, dtype) pair.
+size_t fwd_ws_bytes(int B, int H, int L, int d, int dtype, bool fox) {
+    if (d == 128)
+        return dtype == PATH_BF16 ? d128_tc_layout(B, H, L, fox).total
+                                  : d128_layout(B, H, L, fox).total;
+    return fwd_layout(B, H, L, elt_bytes(dtype), fox).total;
+}
+
 path_status prepare_impl(const void *q, const void *k, const void *w, const float *beta,
                          const float *log_f, bool fox, int B, int H, int L, int d, int dtype,
                          float scale, void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -125,10 +139,12 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
         (fox && !aligned(log_f, 16)))
         return PATH_ERR_ALIGN;
     if (d == 128) {
-        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L, fox).total)) != PATH_OK) return st;
+        if ((st = check_ws(ws, ws_bytes, fwd_ws_bytes(B, H, L, d, dtype, fox))) != PATH_OK) return st;
         const float *lf = fox ? log_f : nullptr;
+        // bf16: tensor-core preparation; fp32: the fp32 CUDA-core kernel (the fp32 bar)
         return from_cuda(dtype == PATH_BF16
-                             ? launch_prep_d128<__nv_bfloat16>(q, k, w, beta, lf, B, H, L, scale, ws, stream)
+                             ? launch_ut_prepare_tc128(q, k, w, beta, lf, B * H, L, scale, ws,
+                                                       kWaitLimitNs, stream)
                              : launch_prep_d128<float>(q, k, w, beta, lf, B, H, L, scale, ws, stream));
     }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
@@ -155,9 +171,10 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
     if (!v || !out) return PATH_ERR_NULL;
     if (!aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16))) return PATH_ERR_ALIGN;
     if (d == 128) {
-        if ((st = check_ws(ws, ws_bytes, d128_layout(B, H, L, fox).total)) != PATH_OK) return st;
+        if ((st = check_ws(ws, ws_bytes, fwd_ws_bytes(B, H, L, d, dtype, fox))) != PATH_OK) return st;
         return from_cuda(dtype == PATH_BF16
-                             ? launch_scan_d128<__nv_bfloat16>(v, out, lse, fox, B, H, L, scale, ws, stream)
+                             ? launch_scan_tc128(v, out, lse, fox, B * H, L, scale, ws,
+                                                 kWaitLimitNs, stream)
                              : launch_scan_d128<float>(v, out, lse, fox, B, H, L, scale, ws, stream));
     }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
@@ -217,8 +234,7 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
         case PATH_OP_FWD:
         case PATH_OP_FOX_FWD:
             if (check_fwd_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
-            if (d == 128) return d128_layout(B, H, L, op == PATH_OP_FOX_FWD).total;
-            return fwd_layout(B, H, L, elt_bytes(dtype), op == PATH_OP_FOX_FWD).total;
+            return fwd_ws_bytes(B, H, L, d, dtype, op == PATH_OP_FOX_FWD);
         default: break;
     }
     if (op == PATH_OP_BWD || op == PATH_OP_FOX_BWD) {

@@ -576,6 +576,375 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
 }
 
+// ---------------------------------------------------------------- head size 128
+// The same per-block preprocessing at d = 128 (technical summary "技術要約: PaTH Attention"
+// §3; review "거리에서 경로로, PaTH Attention" §9 flags larger heads as costlier): W, Q, K are
+// 64 x 128, the UT factor A stays 64 x 64, U = A^T W and V' = A W are 64 x 128 and the dense
+// block transition P_b = I - W^T V' is 128 x 128. A 64 x 128 16-bit operand is two 64 x 64
+// swizzled atoms (columns 0-63 and 64-127); K-major operands walk the two atoms in their
+// k-steps, MN-major ones stack them at a fixed byte stride.
+//   MMA1 (bf16, K = 128):  [Q; W] x [W; K]^T                -> Q W^T | (Q K^T) / W W^T | W K^T
+//   MMA3 (fp16, N = 192):  [A^T; A] x [W | Rk^T]            -> U | Khat^T / V' | (unused)
+//   MMA4x:                 Lq x U (fp16, N = 128) ; Q x K^T (bf16, K = 128) - Lq x Khat^T
+//   MMA4y (fp16):          W^T x V' (M = 128, N = 128)      -> I - P_b
+//                          Rk x V'                          -> k~ = K - Rk V'
+// Outputs: q~ (BH, Lp, 128) bf16; per block [k~ (64 rows); P_b (128 rows)] x 128 bf16; the
+// fp16 diagonal table. PaTH-FoX also writes, in log2 units, the rows' in-block inclusive gate
+// sums lc2, the keys' tail sums T2_b - lc2_j and the block totals T2_b (fp64).
+// 8 KB slots: 0 Q0 1 W0 2 K0 3 Q1 4 W1 5 K1 (bf16 inputs, [Q;W;K] per column half so that
+// [Q;W] and [W;K] are contiguous in each half); 6 Wh0 7 Wh1 8 Rk^T (fp16, MMA3's B at an 8 KB
+// stride); 9 Lq; 10-12 the solve scratch, then A^T, A; after MMA3: U0 = 10, U1 = 11,
+// Khat^T = 12, V'0 = 1, V'1 = 4 (W's bf16 halves are dead after MMA1).
+constexpr uint32_t k2Slots = 13;
+constexpr uint32_t P2_Q0 = 0 * kT, P2_W0 = 1 * kT, P2_K0 = 2 * kT, P2_Q1 = 3 * kT, P2_W1 = 4 * kT,
+                   P2_K1 = 5 * kT, P2_WH0 = 6 * kT, P2_WH1 = 7 * kT, P2_RKT = 8 * kT,
+                   P2_LQ = 9 * kT, P2_SCR = 10 * kT, P2_AT = 10 * kT, P2_A = 11 * kT,
+                   P2_U0 = 10 * kT, P2_U1 = 11 * kT, P2_KHT = 12 * kT, P2_V0 = 1 * kT,
+                   P2_V1 = 4 * kT;
+constexpr uint32_t P2_Y = P2_SCR + 64 * XLD * 4;
+constexpr uint32_t P2_BAR = k2Slots * kT, P2_SLOT = P2_BAR + 16, P2_BETA = P2_SLOT + 16,
+                   P2_LC = P2_BETA + 256;
+constexpr uint32_t k2SmemBytes = P2_LC + 256 + 1024;
+static_assert(P2_Y + 32 * YLD * 4 <= 13 * kT, "d = 128 solve scratch fits in slots 10-12");
+
+// 64 consecutive 16-bit values (one swizzled atom row) as fp32
+__device__ __forceinline__ void load_row_bf16(const uint8_t *tile, int row, float *x) {
+    load_half_bf16(tile, row, 0, x);
+    load_half_bf16(tile, row, 1, x + 32);
+}
+
+template <bool FOX>
+__global__ void __launch_bounds__(kThreads, 2)
+ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ beta,
+                        const float *__restrict__ log_f, int L, int Lp, int nblk,
+                        float scale_log2, __nv_bfloat16 *__restrict__ qt,
+                        __nv_bfloat16 *__restrict__ kp, __half *__restrict__ dg,
+                        float *__restrict__ lc2, float *__restrict__ tail2,
+                        double *__restrict__ tot2, uint32_t *status, uint64_t limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const sm = smem_raw + (base - raw);
+    float *const X = reinterpret_cast<float *>(sm + P2_SCR);
+    float *const Y = reinterpret_cast<float *>(sm + P2_Y);
+    float *const bs = reinterpret_cast<float *>(sm + P2_BETA);
+    float *const lc = reinterpret_cast<float *>(sm + P2_LC);
+    uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + P2_SLOT);
+    const uint32_t bar_tma = base + P2_BAR, bar_mma = base + P2_BAR + 8;
+
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int qd = warp & 3, hf = warp >> 2;
+    const int lr = 32 * qd + lane;
+    const int c0 = 32 * hf;
+    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = blk * kC;
+    const size_t head = (size_t)bh * L;
+    if (blk == 0 && bh == 0 && r == 0 && status) *status = 0u;
+
+    __shared__ uint32_t abort_s;
+    if (r == 0) {
+        abort_s = 0u;
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_w);
+        mbar_arrive_expect_tx(bar_tma, 6 * kT);
+        tma_load_3d(base + P2_Q0, &tm_q, bar_tma, 0, t0, bh);
+        tma_load_3d(base + P2_Q1, &tm_q, bar_tma, 64, t0, bh);
+        tma_load_3d(base + P2_W0, &tm_w, bar_tma, 0, t0, bh);
+        tma_load_3d(base + P2_W1, &tm_w, bar_tma, 64, t0, bh);
+        tma_load_3d(base + P2_K0, &tm_k, bar_tma, 0, t0, bh);
+        tma_load_3d(base + P2_K1, &tm_k, bar_tma, 64, t0, bh);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    const float beta_r = (r < kC && t0 + r < L) ? beta[head + t0 + r] : 0.f;
+    if (FOX && warp == 1) {
+        const int ln = r - 32;
+        const int ta = t0 + 2 * ln, tb = ta + 1;
+        const float a = (ta < L) ? log_f[head + ta] : 0.f;
+        const float b = ((tb < L) ? log_f[head + tb] : 0.f) + a;
+        float run = b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, run, o);
+            if (ln >= o) run += n;
+        }
+        const float la = run - b + a, lb = run;
+        lc[2 * ln] = la;
+        lc[2 * ln + 1] = lb;
+        const float tot = __shfl_sync(0xffffffffu, run, 31);
+        const size_t row = (size_t)bh * Lp + t0 + 2 * ln;
+        lc2[row] = kLog2e * la;
+        lc2[row + 1] = kLog2e * lb;
+        tail2[row] = kLog2e * (tot - la);
+        tail2[row + 1] = kLog2e * (tot - lb);
+        if (ln == 0) tot2[(size_t)bh * nblk + blk] = kLog2eD * (double)tot;
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
+
+    auto wait_all = [&](uint32_t bar, uint32_t par) {
+        if (r == 0) {
+            bool ok = mbar_try_wait(bar, par);
+            if (!ok) {
+                const uint64_t tstart = cycles_now();
+                while (!(ok = mbar_try_wait(bar, par)) &&
+                       cycles_now() - tstart < ns_to_cycles(limit_ns)) {
+                }
+            }
+            if (!ok) {
+                report_status(status, kStatusTimeout);
+                abort_s = 1u;
+            }
+        }
+        __syncthreads();
+        return abort_s == 0u;
+    };
+
+    // ---- MMA1: [Q; W] x [W; K]^T (bf16, K = 128: atoms at slot 0 / 3 and 1 / 4)
+    if (r == 0) {
+        const uint64_t t0s = cycles_now();
+        bool ok = mbar_try_wait(bar_tma, 0);
+        while (!ok && cycles_now() - t0s < ns_to_cycles(limit_ns)) ok = mbar_try_wait(bar_tma, 0);
+        if (ok) {
+            tc_fence_after();
+            constexpr uint32_t ID = idesc16(128, 128, 1, false, false);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ha = kk < 4 ? P2_Q0 : P2_Q1, hb = kk < 4 ? P2_W0 : P2_W1;
+                umma_bf16(tmem, sdesc_sw128(base + ha, 16, 1024) + 2 * (kk & 3),
+                          sdesc_sw128(base + hb, 16, 1024) + 2 * (kk & 3), ID, kk > 0);
+            }
+        } else {
+            report_status(status, kStatusTimeout);
+        }
+        umma_commit(bar_mma);
+    }
+    if (r < kC) bs[r] = beta_r;
+    bool ok = wait_all(bar_mma, 0);
+    if (ok) {
+        tc_fence_after();
+        float x[64];
+        if (lr < kC) {
+            const int i = lr;
+            tmem_row32(tmem + lane_off + c0, x);
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                if (c0 + u > i) x[u] = 0.f;
+            store_half16<true>(sm + P2_LQ, i, hf, x);
+            // W row i, column half hf, to fp16 (MMA3 and MMA4y take fp16 operands)
+            load_row_bf16(sm + (hf ? P2_W1 : P2_W0), i, x);
+            store_half16<true>(sm + (hf ? P2_WH1 : P2_WH0), i, 0, x);
+            store_half16<true>(sm + (hf ? P2_WH1 : P2_WH0), i, 1, x + 32);
+        } else {
+            const int s = lr - kC;
+            tmem_row32(tmem + lane_off + c0, x);
+            const float bsv = bs[s];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float e[4];
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int v = c0 + 4 * q4 + e4;
+                    e[e4] = (v > s) ? bsv * x[4 * q4 + e4] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(X + s * XLD + c0 + 4 * q4) =
+                    make_float4(e[0], e[1], e[2], e[3]);
+            }
+            tmem_row32(tmem + lane_off + 64 + c0, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (s <= c0 + j) x[j] = 0.f;
+            store_half16<true>(sm + P2_RKT, s, hf, x);
+        }
+    }
+    __syncthreads();
+
+    // ---- A = (I + E)^{-1} D as A (rows s) and A^T (rows u), fp16
+    if (ok) {
+        blocked_unit_upper_inverse(X, Y, r);
+        float a[32];
+        if (lr < kC) {
+            const int s = lr;
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const int u = c0 + 4 * u4;
+                const float4 xv = *reinterpret_cast<const float4 *>(X + s * XLD + u);
+                const float4 bv = *reinterpret_cast<const float4 *>(bs + u);
+                a[4 * u4] = (u >= s) ? xv.x * bv.x : 0.f;
+                a[4 * u4 + 1] = (u + 1 >= s) ? xv.y * bv.y : 0.f;
+                a[4 * u4 + 2] = (u + 2 >= s) ? xv.z * bv.z : 0.f;
+                a[4 * u4 + 3] = (u + 3 >= s) ? xv.w * bv.w : 0.f;
+            }
+        } else {
+            const int u = lr - kC;
+            const float bu = bs[u];
+#pragma unroll
+            for (int s2 = 0; s2 < 32; ++s2)
+                a[s2] = (c0 + s2 <= u) ? X[(c0 + s2) * XLD + u] * bu : 0.f;
+        }
+        __syncthreads();  // the scratch overlays the A tiles
+        if (lr < kC) store_half16<true>(sm + P2_A, lr, hf, a);
+        else store_half16<true>(sm + P2_AT, lr - kC, hf, a);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA3: [A^T; A] x [Wh0 | Wh1 | Rk^T] (fp16, B MN-major at an 8 KB stride, N = 192)
+    if (r == 0 && ok) {
+        tc_fence_after();
+        const uint64_t a = sdesc_sw128(base + P2_AT, 16, 1024);
+        const uint64_t b = sdesc_sw128(base + P2_WH0, kT, 1024);
+        constexpr uint32_t ID = idesc16(128, 192, 0, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 2 * kk, b + 128 * kk, ID, kk > 0);
+    }
+    if (r == 0) umma_commit(bar_mma);
+    if (ok) ok = wait_all(bar_mma, 1);
+    if (ok) {
+        tc_fence_after();
+        float x[32];
+        if (lr < kC) {
+            // U row u, column half hf (64 values), and Khat^T row u, half hf (32 values)
+            uint8_t *ut = sm + (hf ? P2_U1 : P2_U0);
+            tmem_row32(tmem + lane_off + 64 * hf, x);
+            store_half16<true>(ut, lr, 0, x);
+            tmem_row32(tmem + lane_off + 64 * hf + 32, x);
+            store_half16<true>(ut, lr, 1, x);
+            tmem_row32(tmem + lane_off + 128 + c0, x);
+            store_half16<true>(sm + P2_KHT, lr, hf, x);
+        } else {
+            uint8_t *vt = sm + (hf ? P2_V1 : P2_V0);
+            tmem_row32(tmem + lane_off + 64 * hf, x);
+            store_half16<true>(vt, lr - kC, 0, x);
+            tmem_row32(tmem + lane_off + 64 * hf + 32, x);
+            store_half16<true>(vt, lr - kC, 1, x);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA4x: Lq U -> cols 0..127;  Q K^T - Lq Khat^T -> cols 128..191
+    if (r == 0 && ok) {
+        tc_fence_after();
+        const uint64_t a1 = sdesc_sw128(base + P2_LQ, 16, 1024);
+        const uint64_t b1 = sdesc_sw128(base + P2_U0, kT, 1024);
+        constexpr uint32_t ID1 = idesc16(128, 128, 0, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a1 + 2 * kk, b1 + 128 * kk, ID1, kk > 0);
+        constexpr uint32_t IDQK = idesc16(128, 64, 1, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ha = kk < 4 ? P2_Q0 : P2_Q1, hb = kk < 4 ? P2_K0 : P2_K1;
+            umma_bf16(tmem + 128, sdesc_sw128(base + ha, 16, 1024) + 2 * (kk & 3),
+                      sdesc_sw128(base + hb, 16, 1024) + 2 * (kk & 3), IDQK, kk > 0);
+        }
+        const uint64_t bh2 = sdesc_sw128(base + P2_KHT, 1024, 1024);
+        constexpr uint32_t IDC = idesc16(128, 64, 0, false, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 128, a1 + 2 * kk, bh2 + 128 * kk, IDC, 1);
+    }
+    if (r == 0) umma_commit(bar_mma);
+    if (ok) ok = wait_all(bar_mma, 0);
+
+    const size_t blk_base = (size_t)bh * nblk + blk;
+    __nv_bfloat16 *kp_blk = kp + blk_base * (kC + 128) * 128;
+    if (ok && lr < kC) {
+        tc_fence_after();
+        const int i = lr;
+        float x[32], y[32];
+        // q~_i = q_i - (Lq U)_i, column half hf
+        const uint8_t *qtile = sm + (hf ? P2_Q1 : P2_Q0);
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+            load_half_bf16(qtile, i, h2, y);
+            tmem_row32(tmem + lane_off + 64 * hf + 32 * h2, x);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) y[c] -= x[c];
+            store_global_half(qt + ((size_t)bh * Lp + t0 + i) * 128 + 64 * hf + 32 * h2, y);
+        }
+        // diagonal logits, log2 units, j <= i
+        tmem_row32(tmem + lane_off + 128 + c0, x);
+        const float lci = FOX ? lc[i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int jj = c0 + j;
+            float v = scale_log2 * x[j];
+            if (FOX) v += kLog2e * (lci - lc[jj]);
+            x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
+        }
+        uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
+                               pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA4y: W^T V' -> cols 0..127 (rows n of P_b); Rk V' -> cols 128..255 (rows j)
+    if (r == 0 && ok) {
+        tc_fence_after();
+        const uint64_t bv = sdesc_sw128(base + P2_V0, P2_V1 - P2_V0, 1024);
+        const uint64_t aw = sdesc_sw128(base + P2_WH0, kT, 1024);
+        constexpr uint32_t IDP = idesc16(128, 128, 0, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, aw + 128 * kk, bv + 128 * kk, IDP, kk > 0);
+        const uint64_t ar = sdesc_sw128(base + P2_RKT, kT, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + 128, ar + 128 * kk, bv + 128 * kk, IDP, kk > 0);
+    }
+    if (r == 0) umma_commit(bar_mma);
+    if (ok) ok = wait_all(bar_mma, 1);
+    if (ok) {
+        tc_fence_after();
+        float x[32];
+        // P_b row n = lr, column half hf: delta - (W^T V')_n
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int cb = 64 * hf + 32 * h2;
+            tmem_row32(tmem + lane_off + cb, x);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[c] = (cb + c == lr ? 1.f : 0.f) - x[c];
+            store_global_half(kp_blk + (size_t)(kC + lr) * 128 + cb, x);
+        }
+        if (lr < kC) {
+            // k~_j = k_j - (Rk V')_j
+            const int j = lr;
+            float y[32];
+            const uint8_t *ktile = sm + (hf ? P2_K1 : P2_K0);
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                load_half_bf16(ktile, j, h2, y);
+                tmem_row32(tmem + lane_off + 128 + 64 * hf + 32 * h2, x);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) y[c] -= x[c];
+                store_global_half(kp_blk + (size_t)j * 128 + 64 * hf + 32 * h2, y);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -611,7 +980,49 @@ bool make_input_map(CUtensorMap *m, const void *ptr, int L, int heads) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// (heads, L rows, 128 columns) bf16 input, (64 columns, 64 rows) boxes, 128-byte swizzle.
+bool make_input_map128(CUtensorMap *m, const void *ptr, int L, int heads) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)L, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)L * 128 * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+// Head size 128, bf16 inputs: the tensor-core preparation into the d128_tc_layout workspace.
+cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
+                                    const float *beta, const float *log_f, int BH, int L,
+                                    float scale, void *ws, uint64_t limit_ns,
+                                    cudaStream_t stream) {
+    const bool fox = log_f != nullptr;
+    const D128TcLayout lay = d128_tc_layout(1, BH, L, fox);
+    char *basep = static_cast<char *>(ws);
+    CUtensorMap tq, tk, tw;
+    if (!make_input_map128(&tq, q, L, BH) || !make_input_map128(&tk, k, L, BH) ||
+        !make_input_map128(&tw, w, L, BH))
+        return cudaErrorInvalidValue;
+    auto kern = fox ? ut_prepare_tc128_kernel<true> : ut_prepare_tc128_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)k2SmemBytes);
+    if (err != cudaSuccess) return err;
+    kern<<<dim3(lay.nblk, BH), kThreads, k2SmemBytes, stream>>>(
+        tq, tk, tw, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
+        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_qt),
+        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_kp),
+        reinterpret_cast<__half *>(basep + lay.off_dg),
+        fox ? reinterpret_cast<float *>(basep + lay.off_lc2) : nullptr,
+        fox ? reinterpret_cast<float *>(basep + lay.off_tail2) : nullptr,
+        fox ? reinterpret_cast<double *>(basep + lay.off_tot2) : nullptr,
+        reinterpret_cast<uint32_t *>(basep), limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, const float *beta,
                                  const float *log_f, int BH, int L, float scale, void *ws,

@@ -60,15 +60,22 @@ def test_workspace_sizes(lib):
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 64, lib.BF16) == \
         256 + (part + 255) // 256 * 256
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 32, lib.BF16) == 0
-    # head size 128: the plain forward keeps fp32 q~ (Lp x 128), per block [k~; P_b]
-    # (192 x 128) and the fp32 diagonal table, whatever the dtype; PaTH-FoX adds the fp32
-    # in-block and tail sums (Lp each), the fp64 block totals and five per-block arrays of
-    # early-exit bounds, each rounded up to 256 B
-    for dt in (lib.BF16, lib.F32):
-        plain = 256 + 128 * 128 * 4 + 2 * 192 * 128 * 4 + 2 * 64 * 64 * 4
-        assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, dt) == plain
-        assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, dt) == \
-            plain + 512 + 512 + 256 + 5 * 256
+    # head size 128, fp32 inputs: fp32 q~ (Lp x 128), per block [k~; P_b] (192 x 128) and
+    # the fp32 diagonal table; PaTH-FoX adds the fp32 in-block and tail sums (Lp each), the
+    # fp64 block totals and five per-block arrays of early-exit bounds, each rounded up to
+    # 256 B
+    plain = 256 + 128 * 128 * 4 + 2 * 192 * 128 * 4 + 2 * 64 * 64 * 4
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, lib.F32) == plain
+    assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, lib.F32) == \
+        plain + 512 + 512 + 256 + 5 * 256
+    # bf16 inputs (tensor-core kernels): the same regions in bf16 with an fp16 table, the
+    # block count rounded up to even; PaTH-FoX adds the fp32 in-block and tail sums (Lp
+    # each) and the fp64 block totals
+    plain16 = 256 + 128 * 128 * 2 + 2 * 192 * 128 * 2 + 2 * 64 * 64 * 2
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, lib.BF16) == plain16
+    assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 65, 128, lib.BF16) == plain16
+    assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, lib.BF16) == \
+        plain16 + 512 + 512 + 256
     # decode partials (m, l, o[128])
     part128 = 4 * 2 * 130 * 4
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 128, lib.BF16) == \

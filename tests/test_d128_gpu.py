@@ -222,3 +222,39 @@ def test_d128_max_heads(lib, fox):
     got = out.reshape(B * H, L, D)[rows[:, 0], rows[:, 1]]
     got_lse = lse.reshape(B * H, L)[rows[:, 0], rows[:, 1]]
     check_bf16(got, ref, got_lse, ref_lse)
+
+
+# ---------------------------------------------------------------- bf16: tensor-core kernels
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 127, 128, 129, 384, 1000])
+def test_d128_bf16_lengths(lib, L):
+    # the tile's diagonal pair, a padded odd last block, and walks of up to 16 key blocks
+    x = pi.make_fwd_inputs(1, 2, L, d=D, dtype=torch.bfloat16, seed=1100 + L, device="cuda")
+    out, lse = _run(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+@pytest.mark.parametrize("gate_scale", [1.0, 8.0])
+def test_d128_fox_bf16_lengths_and_gates(lib, gate_scale):
+    # PaTH-FoX through the tensor-core scan (no early exit there: vanishing keys weigh 0)
+    x = pi.make_fwd_inputs(1, 2, 700, d=D, dtype=torch.bfloat16, seed=1200, fox=True,
+                           device="cuda")
+    x["log_f"] = (x["log_f"] * gate_scale).contiguous()
+    out, lse = _fox(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
+@pytest.mark.parametrize("kind", ["beta_zero", "reflection", "identity"])
+def test_d128_bf16_special_transitions(lib, kind):
+    x = pi.make_fwd_inputs(1, 2, 260, d=D, dtype=torch.bfloat16, seed=1300, device="cuda")
+    if kind == "beta_zero":
+        x["beta"] = torch.zeros_like(x["beta"])
+    elif kind == "reflection":
+        x["beta"] = torch.full_like(x["beta"], 1.99)
+    else:
+        x["w"] = torch.zeros_like(x["w"])
+    out, lse = _run(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    check_bf16(out, ref, lse, ref_lse)
