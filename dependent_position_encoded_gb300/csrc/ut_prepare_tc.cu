@@ -16,9 +16,10 @@
 //
 // (I + E)^{-1} is formed blockwise: the four 16 x 16 diagonal blocks by back-substitution,
 // then X12 = -X11 E12 X22 for the 16-blocks and for the 32-blocks, each 16 x 8 output tile
-// one warp's mma.sync over tf32 head/tail splits (fp32 accuracy; these products are too
-// small for tcgen05, and the fragment loads keep shared-memory traffic low). Every factor
-// is bounded (X_su = A_su / beta_u), so no intermediate grows.
+// one warp's mma.sync with tf32 operands (these products are too small for tcgen05, and the
+// fragment loads keep shared-memory traffic low; A goes on as fp16, so tf32's 10-bit
+// significand matches its use). Every factor is bounded (X_su = A_su / beta_u), so no
+// intermediate grows.
 //
 // tcgen05.mma groups, all M = 128, with 64x64 16-bit tiles in 128-byte-swizzled shared
 // memory (K-major tiles stacked in M must be adjacent; MN-major atoms use the LBO stride):
@@ -124,14 +125,6 @@ __device__ __forceinline__ void store_global_half(__nv_bfloat16 *dst, const floa
                           pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
 }
 
-// fp32 split into a tf32 head and a tf32 tail: head + tail carries about 21 significant
-// bits, so the three products head*head + head*tail + tail*head keep fp32-level accuracy.
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-    const float rest = x - __uint_as_float(hi);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(rest));
-}
-
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
                                          const uint32_t (&b)[2]) {
     asm volatile(
@@ -142,9 +135,16 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
 }
 
 // One warp: the 16 x 8 tile acc = A (16 x K, row-major, stride lda) x B (K x 8, row-major,
-// stride ldb) in fp32 accuracy on the tensor cores (three tf32 products per k-step).
+// stride ldb) on the tensor cores with tf32 operands (one product per k-step: the products
+// feed A, which later MMAs take as fp16, so a 10-bit operand significand is enough).
 // Fragment layout of m16n8k8: g = lane / 4, t = lane % 4; A rows g, g + 8 and columns
 // t, t + 4; B rows t, t + 4 and column g; acc rows g (0, 1), g + 8 (2, 3), columns 2t, 2t + 1.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
 template <int K>
 __device__ __forceinline__ void warp_tile_16x8(const float *A, int lda, const float *B, int ldb,
                                                int lane, float (&acc)[4]) {
@@ -152,16 +152,11 @@ __device__ __forceinline__ void warp_tile_16x8(const float *A, int lda, const fl
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
     for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(A[g * lda + k0 + t], ah[0], al[0]);
-        split_tf32(A[(g + 8) * lda + k0 + t], ah[1], al[1]);
-        split_tf32(A[g * lda + k0 + t + 4], ah[2], al[2]);
-        split_tf32(A[(g + 8) * lda + k0 + t + 4], ah[3], al[3]);
-        split_tf32(B[(k0 + t) * ldb + g], bh[0], bl[0]);
-        split_tf32(B[(k0 + t + 4) * ldb + g], bh[1], bl[1]);
-        mma_tf32(acc, al, bh);
-        mma_tf32(acc, ah, bl);
-        mma_tf32(acc, ah, bh);
+        const uint32_t a[4] = {to_tf32(A[g * lda + k0 + t]), to_tf32(A[(g + 8) * lda + k0 + t]),
+                               to_tf32(A[g * lda + k0 + t + 4]),
+                               to_tf32(A[(g + 8) * lda + k0 + t + 4])};
+        const uint32_t b[2] = {to_tf32(B[(k0 + t) * ldb + g]), to_tf32(B[(k0 + t + 4) * ldb + g])};
+        mma_tf32(acc, a, b);
     }
 }
 
