@@ -273,12 +273,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 const int st = s % NS1;
                 if (!(ok = wait(bar(B_FULL1 + st), (done1 / NS1) & 1))) break;
                 ++done1;
-                if (s > 0) {
-                    if (!(ok = wait(bar(B_EPI), (s - 1) & 1))) break;
-                    if (!(ok = mma2(s - 1))) break;
-                    // the stage of step s - 1 is free (its MMA1 completed before that epilogue)
-                    if (s - 1 + NS1 < steps1) load1(s - 1 + NS1);
-                }
+                if (s > 0 && !(ok = wait(bar(B_EPI), (s - 1) & 1))) break;
                 tc_fence_after();
                 const uint32_t stg = base + S_STG1 + (uint32_t)st * kStage1;
                 if (s > 0) {
@@ -299,6 +294,13 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         umma_bf16(tmem + C_OV, a + 2 * kk, b + 2 * kk, ID, kk > 0);
                 }
                 umma_commit(bar(B_M1));
+                // then step s - 1's gradient gather (off the critical path: the row epilogue of
+                // step s waits for it only before it overwrites that MMA's operands)
+                if (s > 0) {
+                    if (!(ok = mma2(s - 1))) break;
+                    // the stage of step s - 1 is free (its MMA1 completed before that epilogue)
+                    if (s - 1 + NS1 < steps1) load1(s - 1 + NS1);
+                }
             }
             if (ok) ok = wait(bar(B_EPI), (steps1 - 1) & 1);
             if (ok) ok = mma2(steps1 - 1);
@@ -347,6 +349,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(tmem + C_G, ad + 2 * kk, bk + 128 * kk, IDG, (b > 0 || kk > 0));
                 }
+                umma_commit(bar(B_M1B));
                 if (b > 0) {
                     ++dp_uses[i];
                     // [G_hi^T; G_lo^T] X_b: A MN-major over the two G tiles, K = 128 rows
@@ -358,9 +361,8 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         umma_bf16(tmem + (i ? C_DP1 : C_DP0), a + 128 * kk, bx + 128 * kk, IDP,
                                   kk > 0);
                 }
-                // one commit for both groups: the row epilogue overwrites the G tiles that the
-                // dP_b MMAs read, so it waits for them too
-                umma_commit(bar(B_M1B));
+                // the row epilogue overwrites the G tiles that the dP_b MMAs read: it waits for
+                // this commit before it writes them
                 if (b > 0) umma_commit(bar(B_M2B + i));
             }
             // wait for every MMA issued and every copy in flight before TMEM is freed
@@ -424,8 +426,18 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 float ov[32], x[32];
-                tld32(tmem + lane_off + C_OV + 32 * h, ov);
-                if (offd) tld32(tmem + lane_off + C_SX + 32 * h, x);
+                {
+                    // both loads of the half in flight before one wait
+                    uint32_t u1[32], u2[32];
+                    tmem_ld32(tmem + lane_off + C_OV + 32 * h, u1);
+                    if (offd) tmem_ld32(tmem + lane_off + C_SX + 32 * h, u2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        ov[j] = __uint_as_float(u1[j]);
+                        x[j] = __uint_as_float(u2[j]);
+                    }
+                }
                 if (diag) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(tab + 32 * h);
 #pragma unroll
@@ -460,6 +472,11 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         csb[(32 * h + j) * kCsLd + r] = ds;
                     }
                 }
+                // the p, dT and carried-row tiles are operands of the previous step's gather
+                // MMA, which runs while this step's loads and exponentials are done
+                if (h == 0 && s >= 1 &&
+                    !(ok = wait_warp(bar(B_M2 + ((s - 1) & 1)), ((s - 1) >> 1) & 1)))
+                    break;
                 st_row_half(sm + S_PT, r, h, p);
                 if (diag && b < nblk) {
                     float4 *dd = reinterpret_cast<float4 *>(
@@ -478,6 +495,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                                             128 + r) * kD + 32 * h,
                                    dt);
             }
+            if (!ok) break;
             // the carried rows for the next key block (and their stash record)
             if (s == 0) {
                 // stash record 2t holds the state at key block 2t: zero for block 2t's rows
@@ -513,7 +531,8 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 }
             }
             fence_proxy_async_smem();
-            fence_proxy_async_global();
+            // the stash is read back by TMA in pass 2, which starts after this pass's last step
+            if (s == steps1 - 1) fence_proxy_async_global();
             tc_fence_before();
             mbar_arrive_warp(bar(B_EPI));
             if (FOX) {
@@ -558,6 +577,8 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                                                      g[h][4 * c + 3]);
             }
             if (b < 2 * t) {
+                // the dP_b MMA of this step reads the G tiles being replaced
+                if (b > 0 && !(ok = wait_warp(bar(B_M2B + (b & 1)), ((b - 1) >> 1) & 1))) break;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float lo[32];

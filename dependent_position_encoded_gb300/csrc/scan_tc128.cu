@@ -180,6 +180,28 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
             for (int s = 1; s < steps && s <= NR; ++s) load_r(s);
             for (int s = 0; s < steps && s < NV; ++s) load_v(s);
             bool ok = true;
+            auto issue_pv = [&](int s) -> bool {
+                const int vs = s % NV;
+                if (!wait(bar(B_VF + vs), (s / NV) & 1)) return false;
+                ++v_done;
+                if (!wait(bar(B_PR), s & 1)) return false;
+                tc_fence_after();
+                const uint64_t a = sdesc_sw128(base + S_P, 16, 1024);
+                const uint64_t bv = sdesc_sw128(base + S_V + (uint32_t)vs * kVBytes, kVAtom, 1024);
+                constexpr uint32_t ID = idesc_b16(128, 128, false, true);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(tmem + C_O, a + 2 * kk, bv + 128 * kk, ID, (s > 0 || kk > 0));
+                umma_commit(bar(B_PV));
+                umma_commit(bar(B_VE + vs));
+                // the V stage of step s - 1 refills with step s + 1
+                if (s >= 1 && s + 1 < steps && s + 1 >= NV) {
+                    const int pvs = (s - 1) % NV;
+                    if (!wait(bar(B_VE + pvs), ((s - 1) / NV) & 1)) return false;
+                    load_v(s + 1);
+                }
+                return true;
+            };
             for (int s = 0; ok && s < steps; ++s) {
                 if (s >= 1) {
                     const int st = (s - 1) % NR;
@@ -211,28 +233,11 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         load_r(s + 2);
                     }
                 }
-                const int vs = s % NV;
-                if (!(ok = wait(bar(B_VF + vs), (s / NV) & 1))) break;
-                ++v_done;
-                if (!(ok = wait(bar(B_PR), s & 1))) break;
-                tc_fence_after();
-                {
-                    const uint64_t a = sdesc_sw128(base + S_P, 16, 1024);
-                    const uint64_t bv = sdesc_sw128(base + S_V + (uint32_t)vs * kVBytes, kVAtom, 1024);
-                    constexpr uint32_t ID = idesc_b16(128, 128, false, true);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + C_O, a + 2 * kk, bv + 128 * kk, ID, (s > 0 || kk > 0));
-                }
-                umma_commit(bar(B_PV));
-                umma_commit(bar(B_VE + vs));
-                // the V stage of step s - 1 refills with step s + 1
-                if (s >= 1 && s + 1 < steps && s + 1 >= NV) {
-                    const int pvs = (s - 1) % NV;
-                    if (!(ok = wait(bar(B_VE + pvs), ((s - 1) / NV) & 1))) break;
-                    load_v(s + 1);
-                }
+                // P.V of the previous step after this step's logits MMA, so that the softmax
+                // stays off the chain of carried rows
+                if (s >= 1 && !(ok = issue_pv(s - 1))) break;
             }
+            if (ok) ok = issue_pv(steps - 1);
             umma_commit(bar(B_FIN));
             mbar_wait(bar(B_FIN), 0, limit_ns);
             while (r_done < r_iss) {
