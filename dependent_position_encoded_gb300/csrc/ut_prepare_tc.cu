@@ -25,13 +25,16 @@
 // memory (K-major tiles stacked in M must be adjacent; MN-major atoms use the LBO stride):
 //   MMA1 (bf16):  [Q; W] x [W; K]^T          -> Q W^T | (Q K^T)  /  W W^T | W K^T
 //   MMA3 (fp16):  [A^T; A] x [W | Rk^T]      -> U | Khat^T       /  V' | (unused)
-//   MMA4x:        Lq x U (fp16)              -> Lq U
-//                 Q x K^T (bf16) - Lq x Khat^T (fp16), one accumulator -> diag logits
-//   MMA4y (fp16): [W^T; Rk] x V'             -> W^T V'          /  Rk V'
+//   G1 (fp16):    [W^T; Lq] x [U | V']       -> (unused) | W^T V'  /  Lq U | (unused)
+//   G2:           [Q; W] x [K; 0]^T (bf16) - [Lq; Rk] x [Khat^T | V'] (fp16), one
+//                 accumulator                -> diag logits | 0    /  (unused) | -Rk V'
+// The last two groups stack their operands so that every TMEM lane holds a row somebody
+// needs (P_b or q~ after G1, the diagonal table or k~ after G2): their epilogues run on all
+// eight warps, at the price of MMAs half of whose output is discarded.
 // Second-level operands are fp16 (11-bit significand; all bounded, |A_su| <= 4), fp32
 // accumulation. One CTA of 256 threads per (block, head): warps w and w + 4 read the same
 // 32 TMEM lanes (rows) and split every 64-column epilogue into halves, thread 0 issues
-// the TMA loads and the MMAs. 128 TMEM columns, 64 KB of tiles and 80 registers per
+// the TMA loads and the MMAs. 128 TMEM columns, 72 KB of tiles and 80 registers per
 // thread, so three CTAs (24 warps) share an SM.
 #include "common.cuh"
 
@@ -43,21 +46,24 @@ constexpr int kThreads = 256;
 constexpr uint32_t kT = 8192;  // one 64 x 64 16-bit tile
 
 // Tile slots (from the 1024-aligned base). Q, W, K adjacent (MMA1 A = [Q; W], B = [W; K]);
-// AT, A adjacent (MMA3 A). U, KhT, V reuse the slots of AT, A and the solve scratch.
-constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_RKT = 3 * kT, T_LQ = 4 * kT,
-                   T_AT = 5 * kT, T_A = 6 * kT, T_U = 5 * kT, T_KHT = 6 * kT, T_V = 7 * kT;
-constexpr uint32_t SCR = 5 * kT;           // solve scratch (E/X fp32 + Y) overlays slots 5-7
+// a zero tile after K (B = [K; 0] in the last group); Lq^T and Rk^T adjacent (A = [Lq; Rk]);
+// AT, A adjacent (MMA3 A). U, KhT, V reuse the slots of AT, A and the solve scratch (KhT and
+// V adjacent: B = [Khat^T | V']).
+constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_Z = 3 * kT, T_LQ = 4 * kT,
+                   T_RKT = 5 * kT, T_AT = 6 * kT, T_A = 7 * kT, T_U = 6 * kT, T_KHT = 7 * kT,
+                   T_V = 8 * kT;
+constexpr uint32_t SCR = 6 * kT;           // solve scratch (E/X fp32 + Y) overlays slots 6-8
 constexpr int XLD = 68;
 constexpr uint32_t Y_OFF = SCR + 64 * XLD * 4;
 constexpr int YLD = 40;  // B-fragment loads of Y (rows t, columns g) hit 32 banks
-constexpr uint32_t BAR_OFF = 8 * kT;       // 2 mbarriers
+constexpr uint32_t BAR_OFF = 9 * kT;       // 2 mbarriers
 constexpr uint32_t SLOT_OFF = BAR_OFF + 16;
 constexpr uint32_t BETA_OFF = SLOT_OFF + 16;
 constexpr uint32_t LC_OFF = BETA_OFF + 256;
 constexpr uint32_t kSmemBytes = LC_OFF + 256 + 1024;
 constexpr uint32_t kTmemCols = 128;
 
-static_assert(Y_OFF + 32 * YLD * 4 <= 8 * kT, "solve scratch fits in slots 5-7");
+static_assert(Y_OFF + 32 * YLD * 4 <= 9 * kT, "solve scratch fits in slots 6-8");
 
 // idesc for kind::f16 with both operands bf16 (fmt 1) or fp16 (fmt 0)
 __host__ __device__ constexpr uint32_t idesc16(int M, int N, uint32_t fmt, bool a_mn, bool b_mn,
@@ -294,6 +300,9 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         lc[2 * ln] = run - b + a;
         lc[2 * ln + 1] = run;
     }
+    // the zero tile: the rows of B = [K; 0] that pair with the W rows of A = [Q; W]
+    reinterpret_cast<uint4 *>(sm + T_Z)[r] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4 *>(sm + T_Z)[r + kThreads] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
@@ -344,12 +353,14 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         float x[32];
         if (lr < kC) {
             const int i = lr;
-            // row i of Q W^T -> Lq (u <= i), fp16
+            // row i of Q W^T -> Lq (u <= i), fp16, stored transposed (tile rows u): Lq is
+            // an MN-major operand of the last two groups
             tmem_row32(tmem + lane_off + c0, x);
+            uint8_t *lqt = sm + T_LQ + 2 * (i & 7);
 #pragma unroll
             for (int u = 0; u < 32; ++u)
-                if (c0 + u > i) x[u] = 0.f;
-            store_half16<true>(sm + T_LQ, i, hf, x);
+                *reinterpret_cast<__half *>(lqt + sw128_offset(c0 + u, i >> 3)) =
+                    __float2half_rn(c0 + u > i ? 0.f : x[u]);
             // W to fp16 in place (MMA1 has completed; later MMAs take fp16 operands)
             load_half_bf16(sm + T_W, i, hf, x);
             store_half16<true>(sm + T_W, i, hf, x);
@@ -438,109 +449,109 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA4x: Lq U -> cols 0..63;  Q K^T - Lq Khat^T -> cols 64..127
+    // ---- G1: [W^T; Lq] x [U | V'] (fp16, both MN-major, N = 128): rows n (0-63) give
+    // W^T V' (columns 64-127), rows 64 + i give Lq U (columns 0-63); the off-diagonal
+    // blocks are unused
     if (r == 0 && ok) {
         tc_fence_after();
-        const uint64_t a1 = sdesc_sw128(base + T_LQ, 16, 1024);
-        const uint64_t b1 = sdesc_sw128(base + T_U, 1024, 1024);
-        constexpr uint32_t ID1 = idesc16(128, 64, 0, false, true);
+        const uint64_t a = sdesc_sw128(base + T_W, T_LQ - T_W, 1024);
+        const uint64_t b = sdesc_sw128(base + T_U, T_V - T_U, 1024);
+        constexpr uint32_t ID = idesc16(128, 128, 0, true, true);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a1 + 2 * kk, b1 + 128 * kk, ID1, kk > 0);
-        const uint64_t aq = sdesc_sw128(base + T_Q, 16, 1024);
-        const uint64_t bk = sdesc_sw128(base + T_K, 16, 1024);
-        constexpr uint32_t IDQK = idesc16(128, 64, 1, false, false);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 64, aq + 2 * kk, bk + 2 * kk, IDQK, kk > 0);
-        const uint64_t bh2 = sdesc_sw128(base + T_KHT, 1024, 1024);
-        constexpr uint32_t IDC = idesc16(128, 64, 0, false, true, true);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 64, a1 + 2 * kk, bh2 + 128 * kk, IDC, 1);
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 128 * kk, b + 128 * kk, ID, kk > 0);
     }
     if (r == 0) umma_commit(bar_mma);
     if (ok) ok = wait_all(bar_mma, 0);
 
     const size_t blk_base = (size_t)bh * nblk + blk;
     __nv_bfloat16 *kp_blk = kp + blk_base * (2 * kC) * kD;
-    if (ok && lr < kC) {  // warps whose lanes hold rows 0-63; the others have nothing here
+    // FoX partial sums (row norms, table maxima, key norms) in the U slot, free after G1
+    float *const part = reinterpret_cast<float *>(sm + T_U);
+    if (ok) {
         tc_fence_after();
-        const int i = lr;
-        float x[32], y[32];
-        // q~_i = q_i - (Lq U)_i
-        load_half_bf16(sm + T_Q, i, hf, y);
-        tmem_row32(tmem + lane_off + c0, x);
+        float x[32];
+        if (lr < kC) {
+            // P_b row n = lr: delta - (W^T V')_n
+            tmem_row32(tmem + lane_off + 64 + c0, x);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) y[c] -= x[c];
-        store_global_half(qt + ((size_t)bh * Lp + t0 + i) * kD + c0, y);
-        float qs = 0.f;
-        if (FOX) {
+            for (int c = 0; c < 32; ++c) x[c] = (c0 + c == lr ? 1.f : 0.f) - x[c];
+            store_global_half(kp_blk + (kC + lr) * kD + c0, x);
+        } else {
+            // q~_i = q_i - (Lq U)_i
+            const int i = lr - kC;
+            float y[32];
+            load_half_bf16(sm + T_Q, i, hf, y);
+            tmem_row32(tmem + lane_off + c0, x);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
-                qs = fmaf(r16, r16, qs);
+            for (int c = 0; c < 32; ++c) y[c] -= x[c];
+            store_global_half(qt + ((size_t)bh * Lp + t0 + i) * kD + c0, y);
+            if (FOX) {
+                float qs = 0.f;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
+                    qs = fmaf(r16, r16, qs);
+                }
+                part[(i * 2 + hf) * 2] = qs;
             }
-        }
-        // diagonal logits, log2 units, j <= i
-        tmem_row32(tmem + lane_off + 64 + c0, x);
-        const float lci = FOX ? lc[i] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int jj = c0 + j;
-            float v = scale_log2 * x[j];
-            if (FOX) v += kLog2e * (lci - lc[jj]);
-            x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
-        }
-        uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
-                               pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
-        if (FOX) {
-            // half-row partials into the Lq slot (MMA4x, its only reader, has completed)
-            float dm = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) dm = fmaxf(dm, __half2float(__float2half_rn(x[j])));
-            float *part = reinterpret_cast<float *>(sm + T_LQ);
-            part[(i * 2 + hf) * 2] = qs;
-            part[(i * 2 + hf) * 2 + 1] = dm;
         }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA4y: [W^T; Rk] x V' (fp16, A and B MN-major) -> cols 0..63
+    // ---- G2: [Q; W] x [K; 0]^T (bf16) - [Lq; Rk] x [Khat^T | V'] (fp16, MN-major): rows i
+    // (0-63) give Q K^T - Lq Khat^T (columns 0-63), rows 64 + j give -Rk V' (columns 64-127);
+    // W is fp16 by now, so the W rows of the first product are unused, like the off-diagonal
+    // blocks
     if (r == 0 && ok) {
         tc_fence_after();
-        const uint64_t a2 = sdesc_sw128(base + T_W, T_RKT - T_W, 1024);
-        const uint64_t b2 = sdesc_sw128(base + T_V, 1024, 1024);
-        constexpr uint32_t ID2 = idesc16(128, 64, 0, true, true);
+        const uint64_t aq = sdesc_sw128(base + T_Q, 16, 1024);
+        const uint64_t bk = sdesc_sw128(base + T_K, 16, 1024);
+        constexpr uint32_t IDQK = idesc16(128, 128, 1, false, false);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a2 + 128 * kk, b2 + 128 * kk, ID2, kk > 0);
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, aq + 2 * kk, bk + 2 * kk, IDQK, kk > 0);
+        const uint64_t a = sdesc_sw128(base + T_LQ, T_RKT - T_LQ, 1024);
+        const uint64_t b = sdesc_sw128(base + T_KHT, T_V - T_KHT, 1024);
+        constexpr uint32_t IDN = idesc16(128, 128, 0, true, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 128 * kk, b + 128 * kk, IDN, 1);
     }
     if (r == 0) umma_commit(bar_mma);
-    if (FOX && ok && hf == 0 && lr < kC) {
-        // (q~, table) row lr: combine the two half-row partials (MMA4y runs meanwhile)
-        const float *part = reinterpret_cast<const float *>(sm + T_LQ);
-        const size_t row = (size_t)bh * Lp + t0 + lr;
-        qn[row] = sqrtf(part[(lr * 2) * 2] + part[(lr * 2 + 1) * 2]);
-        dmax[row] = fmaxf(part[(lr * 2) * 2 + 1], part[(lr * 2 + 1) * 2 + 1]);
-    }
     if (ok) ok = wait_all(bar_mma, 1);
     if (ok) {
         tc_fence_after();
         float x[32];
-        tmem_row32(tmem + lane_off + c0, x);
         if (lr < kC) {
-            // P_b row n = lr: delta - (W^T V')_n
+            // diagonal logits of row i, log2 units, j <= i
+            const int i = lr;
+            tmem_row32(tmem + lane_off + c0, x);
+            const float lci = FOX ? lc[i] : 0.f;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) x[c] = (c0 + c == lr ? 1.f : 0.f) - x[c];
-            store_global_half(kp_blk + (kC + lr) * kD + c0, x);
+            for (int j = 0; j < 32; ++j) {
+                const int jj = c0 + j;
+                float v = scale_log2 * x[j];
+                if (FOX) v += kLog2e * (lci - lc[jj]);
+                x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
+            }
+            uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
+                                   pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+            if (FOX) {
+                float dm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dm = fmaxf(dm, __half2float(__float2half_rn(x[j])));
+                part[(i * 2 + hf) * 2 + 1] = dm;
+            }
         } else {
             // k~_j = k_j - (Rk V')_j
             const int j = lr - kC;
             float y[32];
             load_half_bf16(sm + T_K, j, hf, y);
+            tmem_row32(tmem + lane_off + 64 + c0, x);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) y[c] -= x[c];
+            for (int c = 0; c < 32; ++c) y[c] += x[c];
             store_global_half(kp_blk + j * kD + c0, y);
             if (FOX) {
                 float ks = 0.f;
@@ -550,15 +561,21 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     ks = fmaf(r16, r16, ks);
                 }
                 // rows past L are padding: they take part in no logit
-                reinterpret_cast<float *>(sm + T_LQ)[256 + j * 2 + hf] = (t0 + j < L) ? ks : 0.f;
+                part[256 + j * 2 + hf] = (t0 + j < L) ? ks : 0.f;
             }
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (FOX && ok && hf == 0 && lr < kC) {
+        // (q~, table) row lr: combine the two half-row partials
+        const size_t row = (size_t)bh * Lp + t0 + lr;
+        qn[row] = sqrtf(part[(lr * 2) * 2] + part[(lr * 2 + 1) * 2]);
+        dmax[row] = fmaxf(part[(lr * 2) * 2 + 1], part[(lr * 2 + 1) * 2 + 1]);
+    }
     if (FOX && ok && warp == 2) {
         // largest |k~_j| of the block: lane l takes rows l and l + 32
-        const float *kpart = reinterpret_cast<const float *>(sm + T_LQ) + 256;
+        const float *kpart = part + 256;
         float m = fmaxf(sqrtf(kpart[lane * 2] + kpart[lane * 2 + 1]),
                         sqrtf(kpart[(lane + 32) * 2] + kpart[(lane + 32) * 2 + 1]));
 #pragma unroll
