@@ -11,9 +11,10 @@
 // base as an fp32 pair hi + lo; the scan forms c2_i - c2_j as
 //     [(hi_P(i) - hi_u) + (lo_P(i) - lo_u) + rel_i] - rel_j      (j in pair u),
 // the bracket once per row and step, accurate to the size of the bias.
-// Three passes: per key block (fp64 total, in-block minimum, key-norm maximum), per head
-// over the block totals (offsets and prefix bounds), per query block (its c2 values and
-// its early-exit extent).
+// Three passes: per key block (fp64 total, in-block minimum, key-norm maximum; for bf16
+// inputs the tensor-core preparation forms these as it goes, so this pass runs for fp32
+// inputs only), per head over the block totals (offsets and prefix bounds), per query
+// block (its c2 values and its early-exit extent).
 //
 // Early exit. Every H_s = I - beta_s w_s w_s^T with beta_s in [0, 2] and unit w_s is a
 // contraction, so the state a row carries down the scan, x = P_{b+1} ... q~_i, has
@@ -301,13 +302,9 @@ cudaError_t launch_fox_prepare(const float *log_f, int BH, int L, int elt_bytes,
     const float *dmax = reinterpret_cast<const float *>(basep + lay.off_dmax);
     const float s = fabsf(scale) * kLog2e;
     const dim3 grid(lay.nblk, BH);
-    // bf16: the tensor-core preprocessing has written |q~|, the table maxima and the
-    // key-norm maxima; fp32: they are read from the rows
-    if (elt_bytes == 2)
-        fox_block_kernel<__nv_bfloat16, false><<<grid, 64, 0, stream>>>(
-            log_f, reinterpret_cast<const __nv_bfloat16 *>(basep + lay.off_kp), L, lay.nblk, btot,
-            bmin, bkmax);
-    else
+    // bf16: the tensor-core preprocessing has written |q~|, the table maxima, the key-norm
+    // maxima and the blocks' fp64 gate totals and minima; fp32: a per-block pass forms them
+    if (elt_bytes != 2)
         fox_block_kernel<float, true><<<grid, 64, 0, stream>>>(
             log_f, reinterpret_cast<const float *>(basep + lay.off_kp), L, lay.nblk, btot, bmin,
             bkmax);

@@ -234,7 +234,8 @@ __device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, i
 // epilogue is split between two warps.
 // FOX: the forget-gate bias on the diagonal table, and per query row |q~_i| (qn) and the
 // largest entry of its table row (dmax), per key block the largest |k~_j| (bkmax), all from
-// the rounded values the workspace holds, for the early-exit pass.
+// the rounded values the workspace holds, and the block's fp64 total of log f (btot) and
+// smallest in-block prefix sum (bmin), for the early-exit pass.
 template <bool FOX>
 __global__ void __launch_bounds__(kThreads, 3)
 ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -243,7 +244,8 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const float *__restrict__ log_f, int L, int Lp, int nblk, float scale_log2,
                      __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ kp,
                      __half *__restrict__ dg, float *__restrict__ qn, float *__restrict__ dmax,
-                     float *__restrict__ bkmax, uint32_t *status, uint64_t limit_ns) {
+                     float *__restrict__ bkmax, double *__restrict__ btot,
+                     double *__restrict__ bmin, uint32_t *status, uint64_t limit_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -572,6 +574,25 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const size_t row = (size_t)bh * Lp + t0 + lr;
         qn[row] = sqrtf(part[(lr * 2) * 2] + part[(lr * 2 + 1) * 2]);
         dmax[row] = fmaxf(part[(lr * 2) * 2 + 1], part[(lr * 2 + 1) * 2 + 1]);
+    }
+    if (FOX && warp == 1) {
+        // for the early-exit bounds, in fp64 (off the block's critical path: fp64 is slow
+        // here): the block's total of log f and the smallest of its inclusive prefix sums
+        const int ta = t0 + 2 * lane, tb = ta + 1;
+        const double da = (ta < L) ? (double)log_f[head + ta] : 0.0;
+        const double db = ((tb < L) ? (double)log_f[head + tb] : 0.0) + da;
+        double drun = db;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double n = __shfl_up_sync(0xffffffffu, drun, o);
+            if (lane >= o) drun += n;
+        }
+        double dm = fmin(drun - db + da, drun);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dm = fmin(dm, __shfl_xor_sync(0xffffffffu, dm, o));
+        const size_t bb = (size_t)bh * nblk + blk;
+        if (lane == 31) btot[bb] = drun;
+        if (lane == 0) bmin[bb] = dm;
     }
     if (FOX && ok && warp == 2) {
         // largest |k~_j| of the block: lane l takes rows l and l + 32
@@ -1059,6 +1080,8 @@ cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, co
         fox ? reinterpret_cast<float *>(basep + lay.off_qn) : nullptr,
         fox ? reinterpret_cast<float *>(basep + lay.off_dmax) : nullptr,
         fox ? reinterpret_cast<float *>(basep + lay.off_bkmax) : nullptr,
+        fox ? reinterpret_cast<double *>(basep + lay.off_btot) : nullptr,
+        fox ? reinterpret_cast<double *>(basep + lay.off_bmin) : nullptr,
         reinterpret_cast<uint32_t *>(basep), limit_ns);
     return cudaGetLastError();
 }
