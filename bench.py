@@ -45,27 +45,29 @@ def fwd_flops(B, H, L, d=64):
 
 
 def scan_executed_flops(B, H, L, first=None):
-    """Tensor-core FLOPs the block-scan kernel actually issues (128-row tiles; per
-    visited key block S = X K~^T and, except at the last block, X P_b^T; P V every block).
-    first: PaTH-FoX early-exit extents (B*H rows of per-query-block lowest key blocks, as
-    path_fox_first_blocks returns them); a tile then visits its key-block pairs down to the
-    pair holding the lower extent of its two query blocks."""
+    """Tensor-core FLOPs the block-scan kernels actually issue, on 128-row tiles t (query
+    blocks 2t, 2t+1) in units of mm = one 128 x 64 x 64 product.
+    first None (PaTH, two key blocks per step): per visited key block S = X K~^T, except at
+    the last block X P_b^T (as pair products), P V every block.
+    first given (PaTH-FoX, one key block per step): the early-exit extents (B*H rows of
+    per-query-block lowest key blocks, as path_fox_first_blocks returns them); a tile walks
+    key blocks 2t+1 down to the lower extent of its two query blocks, with [S | X'] =
+    X [K~_b; P_b]^T (N = 128) at every block but its first and P V_b at every block."""
     nblk = (L + C - 1) // C
     nq = nblk
     nblk += nblk & 1
     mm = 2.0 * 128 * 64 * 64
 
-    def tile_flops(steps):
-        return (steps - 1) * mm + (steps - 2) * mm + steps * mm
-
     if first is None:
+        def tile_flops(steps):
+            return (steps - 1) * mm + (steps - 2) * mm + steps * mm
         return B * H * sum(tile_flops(2 * t + 2) for t in range(nblk // 2))
     total = 0.0
     for row in first:
         for t in range(nblk // 2):
             lo = row[2 * t] if 2 * t + 1 >= nq else min(row[2 * t], row[2 * t + 1])
-            fp = min(lo >> 1, t)
-            total += tile_flops(2 * t + 2 - 2 * fp)
+            n = 2 * t + 2 - min(lo, 2 * t)
+            total += 2 * (n - 1) * mm + n * mm
     return total
 
 
@@ -649,7 +651,7 @@ def run_headline_legs(pa, peaks, dev, rank):
     out["fox"] = {"workload": fw.name, "ms_per_step": fox_ms,
                   "tokens_per_s": fw.B * fw.L / (fox_ms * 1e-3), "early_exit": True,
                   "scan_ms": f_scan, "prepare_ms": statistics.mean(fox_prep),
-                  "roofline": {"kernel": "path_scan_tc_kernel<FOX=1>", "bound": "tensor",
+                  "roofline": {"kernel": "path_scan_tc_fox_kernel", "bound": "tensor",
                                "achieved": f_ach, "peak": peaks["bf16_tflops"],
                                "unit": "TFLOP/s", "frac": f_ach / peaks["bf16_tflops"],
                                "traffic": ncu_traffic("path_scan_tc_kernel_fox"),

@@ -112,8 +112,10 @@ inline FwdLayout fwd_layout(int B, int H, int L, int elt_bytes, bool fox) {
     off = align256(off + bh * lay.nblk * 2 * kC * kD * elt_bytes);
     lay.off_dg = off;
     off = align256(off + bh * lay.nblk * kC * kC * (elt_bytes == 2 ? 2 : 4));
+    // bf16 PaTH: the block-pair products of the two-block scan steps (the PaTH-FoX scan takes
+    // one block per step and needs none)
     lay.off_pr = off;
-    if (elt_bytes == 2) off = align256(off + bh * (lay.nblk / 2) * 2 * kC * kD * 2);
+    if (elt_bytes == 2 && !fox) off = align256(off + bh * (lay.nblk / 2) * 2 * kC * kD * 2);
     // PaTH-FoX only, with c2 = log2(e) * cumsum(log f): c2 relative to the base of its
     // pair of blocks, c2_t - c2_base(t / 128) (BH, Lp) fp32, and the pair bases as fp32 pairs
     // hi + lo (BH, nblk / 2, 2); per key block the prefix minimum of c2 and prefix maximum
@@ -219,6 +221,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` nanoseconds for the phase to
+// complete (it wakes when the phase completes), so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }

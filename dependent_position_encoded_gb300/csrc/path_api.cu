@@ -19,7 +19,10 @@ cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, co
                                  const float *log_f, int BH, int L, float scale, void *ws,
                                  uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_pair_combine(int BH, int L, void *ws, uint64_t limit_ns, cudaStream_t stream);
-cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int BH, int L,
+cudaError_t launch_scan_tc_fox(const void *v, void *out, float *lse, int BH, int L, float scale,
+                               void *ws, uint64_t limit_ns, int force_timeout,
+                               cudaStream_t stream);
+cudaError_t launch_scan_tc(const void *v, void *out, float *lse, int BH, int L,
                            float scale, void *ws, uint64_t limit_ns, int force_timeout,
                            cudaStream_t stream);
 cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int BH, int L,
@@ -154,8 +157,9 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
                         ? launch_ut_prepare_tc(q, k, w, beta, lf, B * H, L, scale, ws,
                                                kWaitLimitNs, stream)
                         : launch_ut_prepare<float>(q, k, w, beta, lf, B * H, L, scale, ws, stream);
-    // bf16: the block-pair products the two-block scan steps use
-    if (e == cudaSuccess && dtype == PATH_BF16) e = launch_pair_combine(B * H, L, ws, kWaitLimitNs, stream);
+    // bf16 PaTH: the block-pair products the two-block scan steps use
+    if (e == cudaSuccess && dtype == PATH_BF16 && !fox)
+        e = launch_pair_combine(B * H, L, ws, kWaitLimitNs, stream);
     // FoX: gate prefix sums and the scan's early-exit extents (reads K1's q~, k~ and table)
     if (e == cudaSuccess && fox)
         e = launch_fox_prepare(lf, B * H, L, elt_bytes(dtype), scale, ws, stream);
@@ -181,9 +185,11 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;
     if (dtype == PATH_BF16) {
         const bool force = debug_force_timeout();
-        cudaError_t e = launch_scan_tc(v, out, lse, fox, B * H, L, scale, ws,
-                                       force ? kDebugWaitLimitNs : kWaitLimitNs, force ? 1 : 0,
-                                       stream);
+        const uint64_t lim = force ? kDebugWaitLimitNs : kWaitLimitNs;
+        cudaError_t e = fox ? launch_scan_tc_fox(v, out, lse, B * H, L, scale, ws, lim,
+                                                 force ? 1 : 0, stream)
+                            : launch_scan_tc(v, out, lse, B * H, L, scale, ws, lim,
+                                             force ? 1 : 0, stream);
         return from_cuda(e);
     }
     return from_cuda(launch_scan_f32(v, out, lse, fox, B * H, L, scale, ws, stream));

@@ -1,5 +1,5 @@
 // K2 (bf16): the right-to-left block scan of PaTH attention on tcgen05 tensor cores,
-// two key blocks per step.
+// two key blocks per step (the PaTH-FoX forward has its own scan, scan_tc_fox.cu).
 //
 // Technical summary "技術要約: PaTH Attention" §3 (FlashAttention-style algorithm: per-block
 // boundary-adjusted queries and keys, a right-to-left scan over key/value blocks that
@@ -22,8 +22,7 @@
 // rows of block 2t keep q~_i.
 //
 // One CTA owns the tiles A = 2p and B = 2p + 1 of one head and streams the key-block pairs
-// 2p+1, 2p, ..., 0 (PaTH-FoX: down to the lower of the two tiles' early-exit extents from
-// fox_exit.cu) once, so each pair serves both tiles, through two TMA rings: one of
+// 2p+1, 2p, ..., 0 once, so each pair serves both tiles, through two TMA rings: one of
 // [K^_{2u}; K~_{2u+1}; Pi_u] (released as soon as both S|state MMAs on it have completed)
 // and one of [V_{2u}; V_{2u+1}] (released after the P.V MMAs, which run a softmax later).
 // Step 0's operand [K~_{2t}; P_{2t}] is staged in the tile's P buffer, which the softmax
@@ -136,18 +135,16 @@ __device__ __forceinline__ void load_diag_row(const __half *row, float *v) {
     }
 }
 
-// RAW: no bias and a positive scale, so the scale is applied inside the exponent's FFMA.
-template <bool FOX, bool RAW>
+// RAW: a positive scale, applied inside the exponent's FFMA.
+template <bool RAW>
 __global__ void __launch_bounds__(kScanThreads, 1)
 path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_kp128,
                     const __grid_constant__ CUtensorMap tm_kp64,
                     const __grid_constant__ CUtensorMap tm_pr64,
                     const __grid_constant__ CUtensorMap tm_v128,
-                    const __half *__restrict__ dg, const float *__restrict__ c2,
-                    const float *__restrict__ pbase,
-                    const int *__restrict__ first_blk, __nv_bfloat16 *__restrict__ out,
-                    float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
+                    const __half *__restrict__ dg, __nv_bfloat16 *__restrict__ out,
+                    float *__restrict__ lse, int L, int nblk, float scale_log2,
                     uint32_t *status, uint64_t limit_ns, int force_timeout) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -161,20 +158,10 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const int bh = blockIdx.y;
     const bool hasB = 2 * pair + 1 < ntile;
     const int top = hasB ? 2 * pair + 1 : 2 * pair;  // first key-block pair of the stream
-    // lowest key-block pair each tile visits: 0, or for PaTH-FoX the pair holding the lower
-    // early-exit extent of its two query blocks (never above the tile's own pair)
-    int fp[2] = {0, 0};
-    if (FOX) {
-        for (int t = 0; t < (hasB ? 2 : 1); ++t) {
-            const int tile = 2 * pair + t;
-            const int *f = first_blk + (size_t)bh * nblk + 2 * tile;
-            fp[t] = min(min(__ldg(f), __ldg(f + 1)) >> 1, tile);
-        }
-    }
-    const int nstream = top + 1 - (hasB ? min(fp[0], fp[1]) : fp[0]);
+    const int nstream = top + 1;
     // tile t (0 = A, 1 = B): tile index, its step count, and stream position of its step 0
     auto tile_of = [&](int t) { return 2 * pair + t; };
-    auto nsteps_of = [&](int t) { return tile_of(t) + 1 - fp[t]; };
+    auto nsteps_of = [&](int t) { return tile_of(t) + 1; };
     auto off_of = [&](int t) { return top - tile_of(t); };
     // whether tile t reads stream position n (its values), and the S|state operand of
     // position n (every step but the tile's first); the operand ring skips position 0,
@@ -468,15 +455,6 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         const int i = tile * kTile + r;          // query index
         const size_t head = (size_t)bh;
         float m_run = -INFINITY, l_run = 0.f;
-        // gate sums relative to the base of their pair of blocks; per step the row's offset
-        // against pair u is (base_tile - base_u) in fp32-pair arithmetic + rel_i
-        const float rel_i = FOX ? c2[head * Lp + i] : 0.f;
-        const float2 base_own = FOX ? *reinterpret_cast<const float2 *>(pbase + (head * ntile + tile) * 2)
-                                    : make_float2(0.f, 0.f);
-        auto row_offset = [&](int u) {
-            const float2 bu = *reinterpret_cast<const float2 *>(pbase + (head * ntile + u) * 2);
-            return ((base_own.x - bu.x) + (base_own.y - bu.y)) + rel_i;
-        };
         bool ok = true;
         // every lane of a warp leaves together: tcgen05.ld/st are warp-collective
         auto wwait = [&](uint32_t b_, uint32_t par) {
@@ -486,7 +464,6 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         const uint32_t T_O = t_o(t) + lane_base;
 
         for (int s = 0; s < nsteps && ok; ++s) {
-            const int u = tile - s;              // key-block pair of this step
             if (!(ok = wwait(tbar(t, ScanSmem::BAR_SX), s & 1))) break;
             tc_fence_after();
             // the step's 128 logits: column c is key 128 u + c (block 2u, then 2u+1)
@@ -511,18 +488,6 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         v[j] = __uint_as_float(a[j]) * scale_log2;
                         v[32 + j] = __uint_as_float(b[j]) * scale_log2;
                     }
-                    if (FOX) {
-                        const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
-                        const float ci = row_offset(u);
-#pragma unroll
-                        for (int q4 = 0; q4 < 16; ++q4) {
-                            const float4 c = __ldg(cj + q4);
-                            v[4 * q4 + 0] += ci - c.x;
-                            v[4 * q4 + 1] += ci - c.y;
-                            v[4 * q4 + 2] += ci - c.z;
-                            v[4 * q4 + 3] += ci - c.w;
-                        }
-                    }
                     load_diag_row(dg + ((head * nblk + 2 * tile + 1) * kC + (r - 64)) * kC, v + 64);
                 }
             } else {
@@ -539,24 +504,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     v[64 + j] = __uint_as_float(c[j]);
                     v[96 + j] = __uint_as_float(d[j]);
                 }
-                if (FOX) {
-                    // v = scale log2(e) S + c2_i - c2_j, two columns per instruction
-                    const float4 *cj = reinterpret_cast<const float4 *>(c2 + head * Lp + u * kTile);
-                    const float2 sl2 = make_float2(scale_log2, scale_log2);
-                    const float ci = row_offset(u);
-                    const float2 ci2 = make_float2(ci, ci);
-                    const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll
-                    for (int q4 = 0; q4 < 32; ++q4) {
-                        const float4 cc = __ldg(cj + q4);
-                        const float2 b0 = ffma2(make_float2(cc.x, cc.y), neg1, ci2);
-                        const float2 b1 = ffma2(make_float2(cc.z, cc.w), neg1, ci2);
-                        const float2 w0 = ffma2(make_float2(v[4 * q4], v[4 * q4 + 1]), sl2, b0);
-                        const float2 w1 = ffma2(make_float2(v[4 * q4 + 2], v[4 * q4 + 3]), sl2, b1);
-                        v[4 * q4] = w0.x; v[4 * q4 + 1] = w0.y;
-                        v[4 * q4 + 2] = w1.x; v[4 * q4 + 3] = w1.y;
-                    }
-                } else if (!RAW) {
+                if (!RAW) {
                     const float2 sl2 = make_float2(scale_log2, scale_log2);
                     const float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -677,10 +625,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 // Returns cudaErrorInvalidValue if the tensor maps cannot be encoded, and
 // cudaErrorInvalidConfiguration if the compiled kernel was given fewer registers than the
 // warpgroup split redistributes (its setmaxnreg.inc could then never be satisfied).
-cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int BH, int L,
-                           float scale, void *ws, uint64_t limit_ns, int force_timeout,
-                           cudaStream_t stream) {
-    const FwdLayout lay = fwd_layout(1, BH, L, 2, fox);
+cudaError_t launch_scan_tc(const void *v, void *out, float *lse, int BH, int L, float scale,
+                           void *ws, uint64_t limit_ns, int force_timeout, cudaStream_t stream) {
+    const FwdLayout lay = fwd_layout(1, BH, L, 2, false);
     char *basep = static_cast<char *>(ws);
     CUtensorMap tm_qt, tm_kp128, tm_kp64, tm_pr64, tm_v128;
     const int nrows_kp = lay.nblk * 2 * kC, nrows_pr = (lay.nblk / 2) * 2 * kC;
@@ -690,9 +637,7 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
         !make_map_bf16(&tm_pr64, basep + lay.off_pr, nrows_pr, BH, kC) ||
         !make_map_bf16(&tm_v128, v, L, BH, kTile))
         return cudaErrorInvalidValue;
-    auto kern = fox ? path_scan_tc_kernel<true, false>
-                    : (scale > 0.f ? path_scan_tc_kernel<false, true>
-                                   : path_scan_tc_kernel<false, false>);
+    auto kern = scale > 0.f ? path_scan_tc_kernel<true> : path_scan_tc_kernel<false>;
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, kern);
     if (err != cudaSuccess) return err;
@@ -704,11 +649,8 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, bool fox, int B
     dim3 grid((ntile + 1) / 2, BH);
     kern<<<grid, kScanThreads, kScanSmemBytes, stream>>>(
         tm_qt, tm_kp128, tm_kp64, tm_pr64, tm_v128,
-        reinterpret_cast<const __half *>(basep + lay.off_dg),
-        fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
-        fox ? reinterpret_cast<const float *>(basep + lay.off_pbase) : nullptr,
-        fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,
-        static_cast<__nv_bfloat16 *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e,
+        reinterpret_cast<const __half *>(basep + lay.off_dg), static_cast<__nv_bfloat16 *>(out),
+        lse, L, lay.nblk, scale * kLog2e,
         reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout);
     return cudaGetLastError();
 }

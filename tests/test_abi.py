@@ -46,13 +46,14 @@ def test_workspace_sizes(lib):
     # fp32: every region fp32
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.F32) == \
         256 + 128 * 64 * 4 + 2 * 128 * 64 * 4 + 2 * 64 * 64 * 4
-    # FoX adds the pair-relative gate sums (Lp fp32), the pair bases (hi, lo fp32 per pair),
-    # per key block two fp32 bounds, one int32 extent, three fp64 block values and one fp32
-    # key-norm maximum, and per query row |q~| and the diagonal-table maximum (Lp fp32 each),
-    # each region rounded up to 256 B
+    # FoX has no pair products (its scan takes one key block per step) and adds the
+    # pair-relative gate sums (Lp fp32), the pair bases (hi, lo fp32 per pair), per key block
+    # two fp32 bounds, one int32 extent, three fp64 block values and one fp32 key-norm
+    # maximum, and per query row |q~| and the diagonal-table maximum (Lp fp32 each), each
+    # region rounded up to 256 B
     fox = lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 64, lib.BF16)
-    assert fox == lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) + 512 + \
-        8 * 256 + 2 * 512
+    assert fox == lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16) - 128 * 64 * 2 + \
+        512 + 8 * 256 + 2 * 512
     # ragged L rounds up to an even number of 64-token blocks
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 65, 64, lib.BF16) == \
         lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 64, lib.BF16)

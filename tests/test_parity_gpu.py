@@ -249,16 +249,17 @@ def test_prepare_factors_match_explicit_products(lib, L, fox):
     dg = ws[off_dg:off_dg + BH * nblk * 64 * 64 * 2].view(torch.float16).reshape(
         BH, nblk, 64, 64)
     off_pr = _align256(off_dg + BH * nblk * 64 * 64 * 2)
-    pr = ws[off_pr:off_pr + BH * (nblk // 2) * 128 * 64 * 2].view(torch.bfloat16).reshape(
-        BH, nblk // 2, 128, 64)
+    if not fox:
+        pr = ws[off_pr:off_pr + BH * (nblk // 2) * 128 * 64 * 2].view(torch.bfloat16).reshape(
+            BH, nblk // 2, 128, 64)
     h = {k_: v.reshape(BH, L, *v.shape[3:]).double().cpu().numpy() for k_, v in x.items()}
     for bh in range(BH):
         refs = [_block_reference(h["q"][bh], h["k"][bh], h["w"][bh], h["beta"][bh],
                                  h["log_f"][bh] if fox else None, 64 * b, L, 0.125)
                 for b in range(nb)]
-        # block-pair products for the two-block scan steps: K^ = K~_{2u} P_{2u+1},
-        # Pi = P_{2u} P_{2u+1} (a block past the end is the identity transition)
-        for u in range(nblk // 2):
+        # block-pair products for the two-block scan steps (plain PaTH only): K^ = K~_{2u}
+        # P_{2u+1}, Pi = P_{2u} P_{2u+1} (a block past the end is the identity transition)
+        for u in range(nblk // 2 if not fox else 0):
             k_lo, p_lo = refs[2 * u][1], refs[2 * u][2]
             p_hi = refs[2 * u + 1][2] if 2 * u + 1 < nb else np.eye(64)
             n = min(64, L - 128 * u)
@@ -422,7 +423,7 @@ def test_fox_long_gate_sums_fp32(lib):
 def test_fox_early_exit_never_reads_skipped_values(lib, dtype, first):
     # log f = -5 per token and the values of blocks 0 and 1 set to NaN: a query block whose
     # scan visited them would turn NaN (0 x NaN). Rows from block 3 on (fp32 scan, one query
-    # block per CTA) or block 4 on (tensor-core scan: 128-row tiles over key-block pairs)
+    # block per CTA) or block 4 on (tensor-core scan: 128-row tiles of two query blocks)
     # stay finite, so the scan stopped above those blocks, and they match the oracle on the
     # clean values (the skipped weights are below e^-40)
     L = 640
