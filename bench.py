@@ -654,7 +654,7 @@ def run_headline_legs(pa, peaks, dev, rank):
                   "roofline": {"kernel": "path_scan_tc_fox_kernel", "bound": "tensor",
                                "achieved": f_ach, "peak": peaks["bf16_tflops"],
                                "unit": "TFLOP/s", "frac": f_ach / peaks["bf16_tflops"],
-                               "traffic": ncu_traffic("path_scan_tc_kernel_fox"),
+                               "traffic": ncu_traffic("path_scan_tc_fox_kernel"),
                                "basis": "executed tensor FLOPs of the visited key blocks",
                                "executed_flops_per_launch": f_ex}}
     return out
