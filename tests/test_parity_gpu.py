@@ -673,14 +673,25 @@ def test_decode_capacity_error(lib):
 
 # ---------------------------------------------------------------- bounded waits
 
-def test_forced_timeout_reports_status_and_context_survives(lib, monkeypatch):
-    x = pi.make_fwd_inputs(1, 1, 256, seed=5, device="cuda")
-    ws = lib.new_workspace(lib.OP_FWD, 1, 1, 256, lib.BF16, "cuda")
+@pytest.mark.parametrize("fox", [False, True])
+def test_forced_timeout_reports_status_and_context_survives(lib, monkeypatch, fox):
+    # PaTH-FoX: 40 heads x 4 tile pairs = 160 items, more than one per CTA of the persistent
+    # scan, so the abort has to stop CTAs in the middle of their item loops
+    B, H, L = (1, 40, 1024) if fox else (1, 1, 256)
+    x = pi.make_fwd_inputs(B, H, L, seed=5, fox=fox, device="cuda")
+    ws = lib.new_workspace(lib.OP_FOX_FWD if fox else lib.OP_FWD, B, H, L, lib.BF16, "cuda")
+
+    def fwd():
+        if fox:
+            return lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"],
+                                    workspace=ws)
+        return lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], workspace=ws)
+
     monkeypatch.setenv("PATH_ATTN_DEBUG_FORCE_TIMEOUT", "1")
-    lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], workspace=ws)
+    fwd()
     assert lib.path_check_workspace(ws) == lib.ERR_TIMEOUT
     monkeypatch.delenv("PATH_ATTN_DEBUG_FORCE_TIMEOUT")
-    out, _ = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], workspace=ws)
+    out, _ = fwd()
     assert lib.path_check_workspace(ws) == lib.OK
-    ref, _ = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+    ref, _ = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x.get("log_f"))
     check_bf16(out, ref)
