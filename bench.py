@@ -580,22 +580,33 @@ def run_legs(pa, peaks, dev, rank):
         bwd["roofline"] = BWD_ROOFLINE(ach, peaks, fox, ex)
         legs["fox_bwd" if fox else "bwd"] = bwd
         torch.cuda.empty_cache()
-    # head size 128: the bf16 check workload's width in 8 heads
-    xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, device=dev)
-    d_tot, d_scan, d_prep = time_forward(pa, xd, 3, 3)
-    d_ms = d_tot / 3
-    fa, fc, fp = fwd_flops(4, 8, 2048, d=128)
-    d_ach = (fa + fc + fp) / (d_ms * 1e-3) / 1e12
-    legs["fwd_d128"] = {"workload": "path_fwd_bf16_B4H8L2048_d128", "ms_per_step": d_ms,
-                        "tokens_per_s": 4 * 2048 / (d_ms * 1e-3),
-                        "scan_ms": statistics.mean(d_scan), "prepare_ms": statistics.mean(d_prep),
-                        "roofline": D128_ROOFLINE(d_ach, peaks)}
-    del xd
-    xd = pi.make_fwd_inputs(4, 8, 2048, d=128, dtype=torch.bfloat16, seed=12, fox=True,
-                            device=dev)
-    f_tot, _, _ = time_forward(pa, xd, 3, 3, fox=True)
-    legs["fwd_d128"]["fox_ms_per_step"] = f_tot / 3
-    del xd
+    # head size 128 at the speed workload's tokens and model width (B32, 16 heads of 128 =
+    # 32 heads of 64), and on the bf16 check workload's width in 8 heads (B4 H8 L2048)
+    for key, (B_, H_, L_) in (("", (32, 16, 4096)), ("small_", (4, 8, 2048))):
+        xd = pi.make_fwd_inputs(B_, H_, L_, d=128, dtype=torch.bfloat16, seed=12, device=dev)
+        d_tot, d_scan, d_prep = time_forward(pa, xd, 3, 3)
+        d_ms = d_tot / 3
+        fa, fc, fp = fwd_flops(B_, H_, L_, d=128)
+        d_ach = (fa + fc + fp) / (d_ms * 1e-3) / 1e12
+        del xd
+        xd = pi.make_fwd_inputs(B_, H_, L_, d=128, dtype=torch.bfloat16, seed=12, fox=True,
+                                device=dev)
+        f_tot, _, _ = time_forward(pa, xd, 3, 3, fox=True)
+        del xd
+        torch.cuda.empty_cache()
+        name = "path_fwd_bf16_B%dH%dL%d_d128" % (B_, H_, L_)
+        if not key:
+            legs["fwd_d128"] = {"workload": name, "ms_per_step": d_ms,
+                                "tokens_per_s": B_ * L_ / (d_ms * 1e-3),
+                                "scan_ms": statistics.mean(d_scan),
+                                "prepare_ms": statistics.mean(d_prep),
+                                "roofline": D128_ROOFLINE(d_ach, peaks),
+                                "fox_ms_per_step": f_tot / 3}
+        else:
+            legs["fwd_d128"].update({"small_workload": name, "small_ms_per_step": d_ms,
+                                     "small_tflops": d_ach,
+                                     "small_frac": d_ach / peaks["bf16_tflops"],
+                                     "small_fox_ms_per_step": f_tot / 3})
     # fp32 inputs (fp32 CUDA-core preparation and scan) on the bf16 check workload's shape
     x32 = pi.make_fwd_inputs(4, 16, 2048, dtype=torch.float32, seed=2, clip=0.0, device=dev)
     s_tot, s_scan, s_prep = time_forward(pa, x32, 3, 3)
@@ -711,8 +722,8 @@ PROFILE_CASES = {
     # the backward legs' own workload (1.3 GB of workspace, stash larger than L2)
     "bwd": pi.BF16_L2048,
     "fox_bwd": pi.BF16_L2048,
-    # the head-size-128 forward leg's own workload (FP32 ALU-bound kernels)
-    "fwd_d128": pi.FwdWorkload("path_fwd_bf16_B4H8L2048_d128", 4, 8, 2048, 128, torch.bfloat16, 12,
+    # a quarter of the head-size-128 forward leg's workload (B8 of B32, H16 L4096 d128)
+    "fwd_d128": pi.FwdWorkload("path_fwd_bf16_B8H16L4096_d128", 8, 16, 4096, 128, torch.bfloat16, 12,
                                pi.BETA_CLIP, False),
     # the fp32-input forward leg's own workload (fp32 CUDA-core kernels)
     "fwd_f32": pi.FwdWorkload("path_fwd_f32_B4H16L2048", 4, 16, 2048, 64, torch.float32, 2, 0.0,

@@ -67,6 +67,28 @@ def test_d128_workload_sampled_rows(lib):
     check_bf16(got, ref, got_lse, ref_lse)
 
 
+def test_d128_speed_width_sampled_rows(lib):
+    # B32 H16 L4096 d128 (the speed workload's tokens and model width in heads of 128, the
+    # bench's head-size-128 leg) on 300 sampled rows, with first and last rows
+    B, H, L = 32, 16, 4096
+    x = pi.make_fwd_inputs(B, H, L, d=D, dtype=torch.bfloat16, seed=12, device="cuda")
+    out, lse = _run(lib, x)
+    g = np.random.default_rng(5)
+    heads = g.integers(0, B * H, 100)
+    rows = np.concatenate([np.stack([heads, g.integers(0, L, 100)], 1),
+                           np.stack([heads, np.zeros(100, np.int64)], 1),
+                           np.stack([heads, np.full(100, L - 1)], 1)]).astype(np.int64)
+    hs = np.unique(heads)
+    h = {k: v.reshape(B * H, L, *v.shape[3:])[torch.as_tensor(hs, device=v.device)].cpu()
+         for k, v in x.items()}
+    loc = np.searchsorted(hs, rows[:, 0])
+    ref, ref_lse = oracle.path_rows(h["q"], h["k"], h["v"], h["w"], h["beta"],
+                                    np.stack([loc, rows[:, 1]], 1))
+    got = out.reshape(B * H, L, D)[rows[:, 0], rows[:, 1]]
+    got_lse = lse.reshape(B * H, L)[rows[:, 0], rows[:, 1]]
+    check_bf16(got, ref, got_lse, ref_lse)
+
+
 def _fox(lib, x, scale=None):
     return lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], scale=scale)
 
