@@ -57,10 +57,16 @@ D128Layout d128_layout(int B, int H, int L, bool fox);
 //   kp  : (BH, nblk, 192, 128) bf16: rows 0-63 k~_j, rows 64-191 the block transition P_b
 //   dg  : (BH, nblk, 64, 64) fp16 diagonal-block logits, log2 units, -inf where masked
 //   PaTH-FoX: lc2, tail2 (BH, Lp) fp32 in-block inclusive gate sums and the keys' tail sums
-//   T2_b - lc2_j, tot2 (BH, nblk) fp64 block totals, all in log2 units
+//   T2_b - lc2_j, tot2 (BH, nblk) fp64 block totals, all in log2 units; for the early exit
+//   per query row |q~_i| and the diagonal-table row maximum qn, dmax (BH, Lp) fp32, per key
+//   block the fp64 total and in-block minimum of the gate prefix sums btot, bmin (natural
+//   log), the largest |k~_j| bkmax, the block offsets boff (fp64), the prefix bounds mpre,
+//   kpre (fp32) and per query block the first key block it needs (int32), all (BH, nblk)
 struct D128TcLayout {
     int BH, nblk, Lp;
-    size_t off_qt, off_kp, off_dg, off_lc2, off_tail2, off_tot2, total;
+    size_t off_qt, off_kp, off_dg, off_lc2, off_tail2, off_tot2;
+    size_t off_qn, off_dmax, off_btot, off_bmin, off_bkmax, off_boff, off_mpre, off_kpre,
+        off_first, total;
 };
 inline D128TcLayout d128_tc_layout(int B, int H, int L, bool fox) {
     D128TcLayout y;
@@ -77,12 +83,33 @@ inline D128TcLayout d128_tc_layout(int B, int H, int L, bool fox) {
     y.off_dg = off;
     off = align256(off + bh * y.nblk * kC * kC * 2);
     y.off_lc2 = y.off_tail2 = y.off_tot2 = off;
+    y.off_qn = y.off_dmax = y.off_btot = y.off_bmin = y.off_bkmax = y.off_boff = off;
+    y.off_mpre = y.off_kpre = y.off_first = off;
     if (fox) {
-        off = align256(off + bh * y.Lp * 4);
+        const size_t rows = bh * y.Lp, blocks = bh * y.nblk;
+        off = align256(off + rows * 4);
         y.off_tail2 = off;
-        off = align256(off + bh * y.Lp * 4);
+        off = align256(off + rows * 4);
         y.off_tot2 = off;
-        off = align256(off + bh * y.nblk * 8);
+        off = align256(off + blocks * 8);
+        y.off_qn = off;
+        off = align256(off + rows * 4);
+        y.off_dmax = off;
+        off = align256(off + rows * 4);
+        y.off_btot = off;
+        off = align256(off + blocks * 8);
+        y.off_bmin = off;
+        off = align256(off + blocks * 8);
+        y.off_boff = off;
+        off = align256(off + blocks * 8);
+        y.off_bkmax = off;
+        off = align256(off + blocks * 4);
+        y.off_mpre = off;
+        off = align256(off + blocks * 4);
+        y.off_kpre = off;
+        off = align256(off + blocks * 4);
+        y.off_first = off;
+        off = align256(off + blocks * 4);
     }
     y.total = off;
     return y;

@@ -223,13 +223,14 @@ fox_prefix_kernel(const double *__restrict__ btot, const double *__restrict__ bm
     }
 }
 
-// Per query block (64 threads, one row each): first writes c2 of its 64 positions,
+// Per query block (64 threads, one row each): with C2 first writes c2 of its 64 positions,
 // c2_i = log2(e) (offset of the block + in-block prefix), as an fp32 pair hi + lo (so that
-// differences c2_i - c2_j stay accurate to their own size however large the sums grow);
-// then first[bh][qb], the lowest key block any of its rows needs (qb itself when no
-// earlier block is needed). With ROWS the row norms |q~_i| and diagonal-table maxima are
-// read from the rows; without, from the per-row values the bf16 preprocessing wrote.
-template <typename T, typename D, bool ROWS>
+// differences c2_i - c2_j stay accurate to their own size however large the sums grow; the
+// head-size-128 scan forms its bias from its own sums and needs none); then
+// first[bh][qb], the lowest key block any of its rows needs (qb itself when no earlier
+// block is needed). With ROWS the row norms |q~_i| and diagonal-table maxima are read from
+// the rows; without, from the per-row values the bf16 preprocessing wrote.
+template <typename T, typename D, bool ROWS, bool C2 = true>
 __global__ void __launch_bounds__(64)
 fox_exit_kernel(const float *__restrict__ log_f, const double *__restrict__ boff,
                 const T *__restrict__ qt, const D *__restrict__ dg,
@@ -246,8 +247,8 @@ fox_exit_kernel(const float *__restrict__ log_f, const double *__restrict__ boff
     const double own = boff[(size_t)bh * nblk + qb], base = boff[(size_t)bh * nblk + (qb & ~1)];
     const double cd = (own + loc) * (double)kLog2e;
     const float c_hi = (float)cd;
-    c2[(size_t)bh * Lp + i] = (float)((own - base + loc) * (double)kLog2e);
-    if (r == 0 && (qb & 1) == 0) {
+    if (C2) c2[(size_t)bh * Lp + i] = (float)((own - base + loc) * (double)kLog2e);
+    if (C2 && r == 0 && (qb & 1) == 0) {
         const double bd = base * (double)kLog2e;
         const float bh_hi = (float)bd;
         float *pb = pbase + ((size_t)bh * (nblk >> 1) + (qb >> 1)) * 2;
@@ -284,6 +285,26 @@ fox_exit_kernel(const float *__restrict__ log_f, const double *__restrict__ boff
 }
 
 }  // namespace
+
+// Head size 128 (bf16, tensor-core preparation): the same prefix and extent passes over the
+// d128_tc_layout workspace, from the per-row and per-block values the preparation wrote.
+cudaError_t launch_fox_exit_d128(const float *log_f, int BH, int L, float scale, void *ws,
+                                 cudaStream_t stream) {
+    const D128TcLayout y = d128_tc_layout(1, BH, L, true);
+    char *basep = static_cast<char *>(ws);
+    double *btot = reinterpret_cast<double *>(basep + y.off_btot);
+    double *bmin = reinterpret_cast<double *>(basep + y.off_bmin);
+    double *boff = reinterpret_cast<double *>(basep + y.off_boff);
+    float *bkmax = reinterpret_cast<float *>(basep + y.off_bkmax);
+    float *mpre = reinterpret_cast<float *>(basep + y.off_mpre);
+    float *kpre = reinterpret_cast<float *>(basep + y.off_kpre);
+    fox_prefix_kernel<<<BH, 256, 0, stream>>>(btot, bmin, bkmax, y.nblk, boff, mpre, kpre);
+    fox_exit_kernel<__nv_bfloat16, __half, false, false><<<dim3(y.nblk, BH), 64, 0, stream>>>(
+        log_f, boff, nullptr, nullptr, reinterpret_cast<const float *>(basep + y.off_qn),
+        reinterpret_cast<const float *>(basep + y.off_dmax), nullptr, nullptr, mpre, kpre, L,
+        y.Lp, y.nblk, fabsf(scale) * kLog2e, reinterpret_cast<int *>(basep + y.off_first));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fox_prepare(const float *log_f, int BH, int L, int elt_bytes, float scale,
                                void *ws, cudaStream_t stream) {

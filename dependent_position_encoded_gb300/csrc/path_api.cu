@@ -54,6 +54,8 @@ cudaError_t launch_prep_d128(const void *q, const void *k, const void *w, const 
 template <typename T>
 cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int B, int H, int L,
                              float scale, void *ws, cudaStream_t stream);
+cudaError_t launch_fox_exit_d128(const float *log_f, int BH, int L, float scale, void *ws,
+                                 cudaStream_t stream);
 cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
                                     const float *beta, const float *log_f, int BH, int L,
                                     float scale, void *ws, uint64_t limit_ns,
@@ -144,11 +146,14 @@ path_status prepare_impl(const void *q, const void *k, const void *w, const floa
     if (d == 128) {
         if ((st = check_ws(ws, ws_bytes, fwd_ws_bytes(B, H, L, d, dtype, fox))) != PATH_OK) return st;
         const float *lf = fox ? log_f : nullptr;
-        // bf16: tensor-core preparation; fp32: the fp32 CUDA-core kernel (the fp32 bar)
-        return from_cuda(dtype == PATH_BF16
-                             ? launch_ut_prepare_tc128(q, k, w, beta, lf, B * H, L, scale, ws,
-                                                       kWaitLimitNs, stream)
-                             : launch_prep_d128<float>(q, k, w, beta, lf, B, H, L, scale, ws, stream));
+        // bf16: tensor-core preparation (PaTH-FoX: then the early-exit extents); fp32: the
+        // fp32 CUDA-core kernel (the fp32 bar), whose scan decides its exit as it runs
+        if (dtype != PATH_BF16)
+            return from_cuda(launch_prep_d128<float>(q, k, w, beta, lf, B, H, L, scale, ws, stream));
+        cudaError_t e = launch_ut_prepare_tc128(q, k, w, beta, lf, B * H, L, scale, ws,
+                                                kWaitLimitNs, stream);
+        if (e == cudaSuccess && fox) e = launch_fox_exit_d128(lf, B * H, L, scale, ws, stream);
+        return from_cuda(e);
     }
     const FwdLayout lay = fwd_layout(B, H, L, elt_bytes(dtype), fox);
     if ((st = check_ws(ws, ws_bytes, lay.total)) != PATH_OK) return st;

@@ -18,7 +18,9 @@
 // At d = 128 a tile needs S 64 + X' 128 + O 128 TMEM columns, so a CTA holds one tile.
 // PaTH-FoX: the bias c_i - c_j of a key in an earlier block is formed, in log2 units, as
 // (lc2_i + sum of the block totals strictly between the two blocks, an fp64 running sum per
-// row) + (T2_b - lc2_j), so no difference of two long prefix sums is taken.
+// row) + (T2_b - lc2_j), so no difference of two long prefix sums is taken; the tile stops
+// at the lower of its two query blocks' early-exit extents (fox_exit.cu, from the bounds
+// the preparation wrote), below which every key weighs less than e^-40 of the row maximum.
 //
 // Warp roles (288 threads): warps 0-3 softmax, one row per thread (logits or the table
 // row, lazy rescaling of O when the running maximum rises by more than 2^8, the P tile),
@@ -115,7 +117,8 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
                   const __grid_constant__ CUtensorMap tm_kp,
                   const __grid_constant__ CUtensorMap tm_v, const __half *__restrict__ dg,
                   const float *__restrict__ lc2, const float *__restrict__ tail2,
-                  const double *__restrict__ tot2, __nv_bfloat16 *__restrict__ out,
+                  const double *__restrict__ tot2, const int *__restrict__ first_blk,
+                  __nv_bfloat16 *__restrict__ out,
                   float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
                   uint32_t *status, uint64_t limit_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -130,7 +133,14 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const int npair = nblk >> 1;
     const int t = npair - 1 - (int)blockIdx.x;  // longest walks first
     const int bh = blockIdx.y;
-    const int steps = 2 * t + 2;
+    // key blocks 2t+1 down to 0, or for PaTH-FoX down to the lower early-exit extent of the
+    // tile's two query blocks (never above block 2t, its own lower diagonal block)
+    int lo = 0;
+    if (FOX) {
+        const int *f = first_blk + (size_t)bh * nblk + 2 * t;
+        lo = min(min(__ldg(f), __ldg(f + 1)), 2 * t);
+    }
+    const int steps = 2 * t + 2 - lo;
     const Wait wait{abort_f, status, limit_ns};
     auto wait_warp = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, wait(b, parity)) != 0;
@@ -382,8 +392,7 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
         const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
         bool ok = true;
         for (int s = 1; ok && s < steps; ++s) {
-            const int b = 2 * t + 1 - s;
-            if (b == 0) break;  // the last key block carries nothing further
+            if (s == steps - 1) break;  // the last key block carries nothing further
             if (!(ok = wait_warp(bar(B_SX), (s - 1) & 1))) break;
             tc_fence_after();
             // block 2t's rows keep q~ past their own (diagonal) block
@@ -429,6 +438,7 @@ cudaError_t launch_scan_tc128(const void *v, void *out, float *lse, bool fox, in
         fox ? reinterpret_cast<const float *>(base + y.off_lc2) : nullptr,
         fox ? reinterpret_cast<const float *>(base + y.off_tail2) : nullptr,
         fox ? reinterpret_cast<const double *>(base + y.off_tot2) : nullptr,
+        fox ? reinterpret_cast<const int *>(base + y.off_first) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e,
         reinterpret_cast<uint32_t *>(base), limit_ns);
     return cudaGetLastError();

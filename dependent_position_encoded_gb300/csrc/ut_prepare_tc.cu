@@ -637,7 +637,9 @@ constexpr uint32_t P2_Q0 = 0 * kT, P2_W0 = 1 * kT, P2_K0 = 2 * kT, P2_Q1 = 3 * k
 constexpr uint32_t P2_Y = P2_SCR + 64 * XLD * 4;
 constexpr uint32_t P2_BAR = k2Slots * kT, P2_SLOT = P2_BAR + 16, P2_BETA = P2_SLOT + 16,
                    P2_LC = P2_BETA + 256;
-constexpr uint32_t k2SmemBytes = P2_LC + 256 + 1024;
+// PaTH-FoX: per row and column half the partial |q~|^2, table maximum and |k~|^2
+constexpr uint32_t P2_PART = P2_LC + 256;
+constexpr uint32_t k2SmemBytes = P2_PART + 3 * 128 * 4 + 1024;
 static_assert(P2_Y + 32 * YLD * 4 <= 13 * kT, "d = 128 solve scratch fits in slots 10-12");
 
 // 64 consecutive 16-bit values (one swizzled atom row) as fp32
@@ -655,7 +657,10 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
                         float scale_log2, __nv_bfloat16 *__restrict__ qt,
                         __nv_bfloat16 *__restrict__ kp, __half *__restrict__ dg,
                         float *__restrict__ lc2, float *__restrict__ tail2,
-                        double *__restrict__ tot2, uint32_t *status, uint64_t limit_ns) {
+                        double *__restrict__ tot2, float *__restrict__ qn,
+                        float *__restrict__ dmax, float *__restrict__ bkmax,
+                        double *__restrict__ btot, double *__restrict__ bmin, uint32_t *status,
+                        uint64_t limit_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -664,6 +669,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
     float *const Y = reinterpret_cast<float *>(sm + P2_Y);
     float *const bs = reinterpret_cast<float *>(sm + P2_BETA);
     float *const lc = reinterpret_cast<float *>(sm + P2_LC);
+    float *const part = reinterpret_cast<float *>(sm + P2_PART);  // [3][64 rows][2 halves]
     uint32_t *const slot = reinterpret_cast<uint32_t *>(sm + P2_SLOT);
     const uint32_t bar_tma = base + P2_BAR, bar_mma = base + P2_BAR + 8;
 
@@ -721,6 +727,21 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
         tail2[row] = kLog2e * (tot - la);
         tail2[row + 1] = kLog2e * (tot - lb);
         if (ln == 0) tot2[(size_t)bh * nblk + blk] = kLog2eD * (double)tot;
+        // for the early-exit bounds, in fp64: the block's total of log f and the smallest of
+        // its inclusive prefix sums
+        const double da = (ta < L) ? (double)log_f[head + ta] : 0.0;
+        const double db = ((tb < L) ? (double)log_f[head + tb] : 0.0) + da;
+        double drun = db;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double n = __shfl_up_sync(0xffffffffu, drun, o);
+            if (ln >= o) drun += n;
+        }
+        double dm = fmin(drun - db + da, drun);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dm = fmin(dm, __shfl_xor_sync(0xffffffffu, dm, o));
+        if (ln == 31) btot[(size_t)bh * nblk + blk] = drun;
+        if (ln == 0) bmin[(size_t)bh * nblk + blk] = dm;
     }
     __syncthreads();
     tc_fence_after();
@@ -901,6 +922,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
         float x[32], y[32];
         // q~_i = q_i - (Lq U)_i, column half hf
         const uint8_t *qtile = sm + (hf ? P2_Q1 : P2_Q0);
+        float qs = 0.f;
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
             load_half_bf16(qtile, i, h2, y);
@@ -908,7 +930,15 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] -= x[c];
             store_global_half(qt + ((size_t)bh * Lp + t0 + i) * 128 + 64 * hf + 32 * h2, y);
+            if (FOX) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
+                    qs = fmaf(r16, r16, qs);
+                }
+            }
         }
+        if (FOX) part[i * 2 + hf] = qs;
         // diagonal logits, log2 units, j <= i
         tmem_row32(tmem + lane_off + 128 + c0, x);
         const float lci = FOX ? lc[i] : 0.f;
@@ -924,9 +954,21 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 4; ++c)
             dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
                                pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+        if (FOX) {
+            float dm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dm = fmaxf(dm, __half2float(__float2half_rn(x[j])));
+            part[128 + i * 2 + hf] = dm;
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (FOX && ok && hf == 0 && lr < kC) {
+        // (q~, table) row lr: combine the two half-row partials
+        const size_t row = (size_t)bh * Lp + t0 + lr;
+        qn[row] = sqrtf(part[lr * 2] + part[lr * 2 + 1]);
+        dmax[row] = fmaxf(part[128 + lr * 2], part[128 + lr * 2 + 1]);
+    }
 
     // ---- MMA4y: W^T V' -> cols 0..127 (rows n of P_b); Rk V' -> cols 128..255 (rows j)
     if (r == 0 && ok) {
@@ -960,6 +1002,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int j = lr;
             float y[32];
             const uint8_t *ktile = sm + (hf ? P2_K1 : P2_K0);
+            float ks = 0.f;
 #pragma unroll 1
             for (int h2 = 0; h2 < 2; ++h2) {
                 load_half_bf16(ktile, j, h2, y);
@@ -967,11 +1010,29 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int c = 0; c < 32; ++c) y[c] -= x[c];
                 store_global_half(kp_blk + (size_t)j * 128 + 64 * hf + 32 * h2, y);
+                if (FOX) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
+                        ks = fmaf(r16, r16, ks);
+                    }
+                }
             }
+            // rows past L are padding: they take part in no logit
+            if (FOX) part[256 + j * 2 + hf] = (t0 + j < L) ? ks : 0.f;
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (FOX && ok && warp == 2) {
+        // largest |k~_j| of the block: lane l takes rows l and l + 32
+        const float *kpart = part + 256;
+        float m = fmaxf(sqrtf(kpart[lane * 2] + kpart[lane * 2 + 1]),
+                        sqrtf(kpart[(lane + 32) * 2] + kpart[(lane + 32) * 2 + 1]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) bkmax[blk_base] = m;
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -1053,6 +1114,11 @@ cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
         fox ? reinterpret_cast<float *>(basep + lay.off_lc2) : nullptr,
         fox ? reinterpret_cast<float *>(basep + lay.off_tail2) : nullptr,
         fox ? reinterpret_cast<double *>(basep + lay.off_tot2) : nullptr,
+        fox ? reinterpret_cast<float *>(basep + lay.off_qn) : nullptr,
+        fox ? reinterpret_cast<float *>(basep + lay.off_dmax) : nullptr,
+        fox ? reinterpret_cast<float *>(basep + lay.off_bkmax) : nullptr,
+        fox ? reinterpret_cast<double *>(basep + lay.off_btot) : nullptr,
+        fox ? reinterpret_cast<double *>(basep + lay.off_bmin) : nullptr,
         reinterpret_cast<uint32_t *>(basep), limit_ns);
     return cudaGetLastError();
 }

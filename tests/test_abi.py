@@ -71,12 +71,13 @@ def test_workspace_sizes(lib):
         plain + 512 + 512 + 256 + 5 * 256
     # bf16 inputs (tensor-core kernels): the same regions in bf16 with an fp16 table, the
     # block count rounded up to even; PaTH-FoX adds the fp32 in-block and tail sums (Lp
-    # each) and the fp64 block totals
+    # each), the fp64 block totals, for the early exit |q~| and the table maxima (Lp fp32
+    # each) and seven per-block arrays (three fp64, three fp32, the int32 extents)
     plain16 = 256 + 128 * 128 * 2 + 2 * 192 * 128 * 2 + 2 * 64 * 64 * 2
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 128, 128, lib.BF16) == plain16
     assert lib.path_workspace_bytes(lib.OP_FWD, 1, 1, 65, 128, lib.BF16) == plain16
     assert lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, 128, 128, lib.BF16) == \
-        plain16 + 512 + 512 + 256
+        plain16 + 512 + 512 + 256 + 512 + 512 + 7 * 256
     # decode partials (m, l, o[128])
     part128 = 4 * 2 * 130 * 4
     assert lib.path_workspace_bytes(lib.OP_DECODE, 2, 2, 2048, 128, lib.BF16) == \

@@ -173,6 +173,21 @@ def test_d128_fox_early_exit_skips_blocks(lib):
     assert np.abs(lse[:, :, 192:].double().cpu().numpy() - ref_lse[:, :, 192:]).max() <= 1e-4
 
 
+def test_d128_fox_early_exit_skips_blocks_bf16(lib):
+    # the tensor-core scan (bf16) stops at the extents computed before it: with log f = -5
+    # per token and the values of blocks 0 and 1 NaN, rows from block 4 on (128-row tiles of
+    # two query blocks) stay finite and match the oracle on the clean values
+    L = 640
+    x = pi.make_fwd_inputs(1, 2, L, d=D, dtype=torch.bfloat16, seed=52, fox=True, device="cuda")
+    x["log_f"] = torch.full_like(x["log_f"], -5.0)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    x["v"][:, :, :128] = float("nan")
+    out, lse = _fox(lib, x)
+    got = out[:, :, 256:]
+    assert torch.isfinite(got).all()
+    check_bf16(got, ref[:, :, 256:], lse[:, :, 256:], ref_lse[:, :, 256:])
+
+
 def test_d128_fox_mixed_sign_gate(lib):
     # log f of both signs (the bias against older keys can be positive), custom scale
     x = pi.make_fwd_inputs(2, 2, 640, d=D, dtype=torch.bfloat16, seed=49, fox=True, device="cuda")
