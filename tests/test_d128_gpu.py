@@ -188,6 +188,17 @@ def test_d128_fox_early_exit_skips_blocks_bf16(lib):
     check_bf16(got, ref[:, :, 256:], lse[:, :, 256:], ref_lse[:, :, 256:])
 
 
+@pytest.mark.parametrize("L", [384, 1000])
+def test_d128_fox_own_block_only_gate(lib, L):
+    # log f = -200 per token: every query block needs only its own block (the bf16 scan
+    # walks two blocks per tile), with an odd tile count at L = 384
+    x = pi.make_fwd_inputs(2, 2, L, d=D, dtype=torch.bfloat16, seed=54, fox=True, device="cuda")
+    x["log_f"] = torch.full_like(x["log_f"], -200.0)
+    out, lse = _fox(lib, x)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
 def test_d128_fox_mixed_sign_gate(lib):
     # log f of both signs (the bias against older keys can be positive), custom scale
     x = pi.make_fwd_inputs(2, 2, 640, d=D, dtype=torch.bfloat16, seed=49, fox=True, device="cuda")

@@ -378,6 +378,23 @@ def test_fox_early_exit_strong_gate(lib, dtype):
         check_bf16(out, ref, lse, ref_lse)
 
 
+@pytest.mark.parametrize("L", [384, 1000])
+def test_fox_own_block_only_gate(lib, L):
+    # log f = -200 per token: a key one token back weighs e^-200 of the query's own key, far
+    # below the bound's slack, so every query block's extent is its own block; the PaTH-FoX
+    # scan then has tile pairs
+    # whose second tile stops at its own lower block (the operand position no MMA reads is
+    # skipped) and, at L = 384 (three tiles), a last item with one tile only
+    x = pi.make_fwd_inputs(2, 2, L, seed=44, fox=True, device="cuda")
+    x["log_f"] = torch.full_like(x["log_f"], -200.0)
+    first, out, lse = _fox_with_extents(lib, x)
+    nq = (L + 63) // 64
+    assert np.array_equal(first, np.broadcast_to(np.arange(nq), (2, 2, nq)))
+    _check_extents_safe(x, first)
+    ref, ref_lse = oracle.path_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+    check_bf16(out, ref, lse, ref_lse)
+
+
 def test_fox_early_exit_workload_gate(lib):
     # the FoX workload's gate, logsigmoid(N(2, 1)): the exit is active from a few blocks on
     x = pi.make_fwd_inputs(1, 2, 2048, seed=42, fox=True, device="cuda")
