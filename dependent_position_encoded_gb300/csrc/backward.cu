@@ -844,28 +844,9 @@ cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const v
     return e;
 }
 
-// The block pass, the PaTH-FoX gate sums and d log f on their own, for the tensor-core
-// query pass (backward_tc.cu), which keeps its own workspace layout.
-template <typename T>
-cudaError_t launch_bwd_block(const void *q, const void *k, const void *w, const float *beta,
-                             const float *dqt, const float *dkt, const float *dP,
-                             const float *dTd, float *dq, float *dk, float *dw, float *dbeta,
-                             int BH, int L, int Lp, int nblk, cudaStream_t stream) {
-    const size_t s2 = bwd_block_smem();
-    cudaError_t e = cudaFuncSetAttribute(bwd_block_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
-    if (e != cudaSuccess) return e;
-    bwd_block_kernel<T><<<dim3(nblk, BH), kThreads, s2, stream>>>(
-        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
-        dqt, dkt, dP, dTd, dq, dk, dw, dbeta, L, Lp, nblk);
-    return cudaGetLastError();
-}
-template cudaError_t launch_bwd_block<__nv_bfloat16>(const void *, const void *, const void *,
-                                                     const float *, const float *, const float *,
-                                                     const float *, const float *, float *,
-                                                     float *, float *, float *, int, int, int,
-                                                     int, cudaStream_t);
-
+// The PaTH-FoX gate sums and d log f on their own, for the tensor-core query pass
+// (backward_tc.cu), which keeps its own workspace layout (its block pass for bf16 inputs is
+// backward_block_mm.cu).
 cudaError_t launch_bwd_fox_sums(const float *log_f, int BH, int L, int Lp, int nblk, float *loc,
                                 double *cb, cudaStream_t stream) {
     bwd_fox_sums_kernel<<<BH, kThreads, 0, stream>>>(log_f, L, Lp, nblk, loc, cb);

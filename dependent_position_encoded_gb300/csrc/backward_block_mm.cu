@@ -1,0 +1,412 @@
+// Backward block pass of PaTH attention for bf16 inputs, in matrix form on the tensor
+// cores (mma.sync, tf32 operands, fp32 accumulation).
+//
+// The pages give no backward (review "거리에서 경로로, PaTH Attention" §9 and technical
+// summary "技術要約: PaTH Attention" §3 only say the block-wise algorithm makes training
+// efficient). The query pass hands each 64-token block the gradients of its
+// boundary-adjusted queries dq~, keys dk~, dense transition dP and diagonal-block logits dT
+// (j <= i). The block's forward, in the UT form of summary §3 (D = diag(beta)):
+//     G = W W^T,  A = (I + D strictly-upper(G))^{-1} D,
+//     Lq = lower-incl(Q W^T),  Rk = strictly-upper(K W^T),  U = A^T W,  V = A W,
+//     q~ = Q - Lq U,  k~ = K - Rk V,  P = I - W^T V,  T = Q K^T - Lq A^T Rk^T,
+// so reverse mode gives dense 64 x 64 products only (Y = Lq A^T, dY = -dT Rk, X = the
+// inverse, dX = dA D, dTT the gradient of I + D strictly-upper(G)):
+//     dLq = tril(-dq~ U^T + dY A)             dRk = striu(-dk~ V^T - dT^T Y)
+//     dU = -Lq^T dq~                          dV = -Rk^T dk~ - W dP
+//     dA = dY^T Lq + W dU^T + dV W^T          dbeta_u += sum_s dA_su X_su
+//     dTT = -X^T dX X^T                       dbeta_s += sum_{v>s} dTT_sv G_sv
+//     dG = D strictly-upper(dTT)
+//     dq = dq~ + dT K + dLq W                 dk = dk~ + dT^T Q + dRk W
+//     dw = -V dP^T + dLq^T Q + dRk^T K + A dU + A^T dV + (dG + dG^T) W
+// The same gradient as the token-level sweeps of backward.cu, which stay for fp32 inputs
+// (the fp32 bar): those walk 192 sweeps of up to 64 dependent steps per block, whereas here
+// each block is 31 products on the tensor cores. The products are small and on one
+// dependent chain, so each is a warp-level mma.sync over fp32 tiles in shared memory (any
+// operand read transposed by its fragment addressing); tf32 keeps the fp32 range with a
+// 10-bit significand, well inside the bf16 inputs' error.
+// One CTA of 256 threads per (block, head), twelve 64 x 64 fp32 tiles (204 KB), one CTA per
+// SM. Warp w computes rows 16 (w >> 1) .. + 15 and columns 32 (w & 1) .. + 31 of every
+// product (four m16n8k8 tiles). Padded tokens (past L) have zero q, k, w and beta, so their
+// transitions are the identity; the inputs the sweeps ignore are zero here too: dP of the
+// first and last block, dk~ of the last block, dT above the diagonal.
+#include "common.cuh"
+#include "ut_inverse.cuh"
+
+namespace path {
+
+namespace {
+
+using ut_inverse::blocked_unit_upper_inverse;
+using ut_inverse::mma_tf32;
+using ut_inverse::XLD;
+using ut_inverse::YLD;
+
+constexpr int kThreads = 256;
+constexpr int LD = XLD;                               // row stride of every tile (floats)
+constexpr uint32_t kTile = 64 * LD * 4;               // one fp32 tile
+constexpr int kTiles = 12;
+constexpr uint32_t kYOff = kTiles * kTile;            // the inverse's 32 x YLD scratch
+constexpr uint32_t kBetaOff = kYOff + 32 * YLD * 4;   // beta (64), d beta (64)
+constexpr uint32_t kSmem = kBetaOff + 2 * 64 * 4;
+static_assert(kSmem <= 227u * 1024u, "block-pass shared memory");
+
+using Acc = float[4][4];  // four m16n8 tiles: [n-tile][c0, c1, c2, c3]
+
+__device__ __forceinline__ void zero(Acc &a) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[j][e] = 0.f;
+}
+
+// Row and column of accumulator element (j, e) for the calling thread.
+struct Frag {
+    int m0, n0, g, t;
+    __device__ Frag() {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        m0 = 16 * (w >> 1);
+        n0 = 32 * (w & 1);
+        g = lane >> 2;
+        t = lane & 3;
+    }
+    __device__ __forceinline__ int row(int e) const { return m0 + g + 8 * (e >> 1); }
+    __device__ __forceinline__ int col(int j, int e) const { return n0 + 8 * j + 2 * t + (e & 1); }
+};
+
+// acc += (NEG ? -1 : 1) * opA x opB over K = 64, with opA(i, k) = TA ? A[k][i] : A[i][k] and
+// opB(k, j) = TB ? B[j][k] : B[k][j] (tiles row-major at stride LD). The operands go to the
+// tf32 MMA as their fp32 bits, which it reads truncated to a 10-bit significand.
+template <bool TA, bool TB, bool NEG = false>
+__device__ __forceinline__ void mm(const float *A, const float *B, const Frag &f, Acc &acc) {
+    auto a_at = [&](int i, int k) { return TA ? A[k * LD + i] : A[i * LD + k]; };
+    auto b_at = [&](int k, int j) { return TB ? B[j * LD + k] : B[k * LD + j]; };
+#pragma unroll 2
+    for (int k0 = 0; k0 < 64; k0 += 8) {
+        float av[4] = {a_at(f.m0 + f.g, k0 + f.t), a_at(f.m0 + f.g + 8, k0 + f.t),
+                       a_at(f.m0 + f.g, k0 + f.t + 4), a_at(f.m0 + f.g + 8, k0 + f.t + 4)};
+        uint32_t a[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = __float_as_uint(NEG ? -av[e] : av[e]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = f.n0 + 8 * j + f.g;
+            const uint32_t b[2] = {__float_as_uint(b_at(k0 + f.t, n)),
+                                   __float_as_uint(b_at(k0 + f.t + 4, n))};
+            mma_tf32(acc[j], a, b);
+        }
+    }
+}
+
+// Two independent products in one loop (twice the independent MMA chains per warp):
+// acc1 += op1, acc2 += op2, each as in mm.
+template <bool TA1, bool TB1, bool NEG1, bool TA2, bool TB2, bool NEG2>
+__device__ __forceinline__ void mm2(const float *A1, const float *B1, Acc &acc1,
+                                    const float *A2, const float *B2, Acc &acc2, const Frag &f) {
+    auto at = [&](const float *M, bool T, int i, int k) { return T ? M[k * LD + i] : M[i * LD + k]; };
+#pragma unroll 2
+    for (int k0 = 0; k0 < 64; k0 += 8) {
+        uint32_t a1[4], a2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = f.m0 + f.g + 8 * (e & 1), kk = k0 + f.t + 4 * (e >> 1);
+            const float x1 = at(A1, TA1, i, kk), x2 = at(A2, TA2, i, kk);
+            a1[e] = __float_as_uint(NEG1 ? -x1 : x1);
+            a2[e] = __float_as_uint(NEG2 ? -x2 : x2);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = f.n0 + 8 * j + f.g;
+            const uint32_t b1[2] = {__float_as_uint(at(B1, !TB1, n, k0 + f.t)),
+                                    __float_as_uint(at(B1, !TB1, n, k0 + f.t + 4))};
+            const uint32_t b2[2] = {__float_as_uint(at(B2, !TB2, n, k0 + f.t)),
+                                    __float_as_uint(at(B2, !TB2, n, k0 + f.t + 4))};
+            mma_tf32(acc1[j], a1, b1);
+            mma_tf32(acc2[j], a2, b2);
+        }
+    }
+}
+
+// tile[r][c] = acc (where keep(r, c)), else 0
+template <typename Keep>
+__device__ __forceinline__ void put(float *tile, const Acc &acc, const Frag &f, Keep keep) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = f.row(e), c = f.col(j, e);
+            tile[r * LD + c] = keep(r, c) ? acc[j][e] : 0.f;
+        }
+}
+__device__ __forceinline__ void get(const float *tile, const Frag &f, Acc &acc) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = tile[f.row(e) * LD + f.col(j, e)];
+}
+// rows r < nvalid of a (64-row) global fp32 tensor, row-major at 64 floats per row
+__device__ __forceinline__ void store_rows(float *dst, const Acc &acc, const Frag &f, int nvalid) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            const int r = f.row(e);
+            if (r < nvalid)
+                *reinterpret_cast<float2 *>(dst + (size_t)r * kD + f.col(j, e)) =
+                    make_float2(acc[j][e], acc[j][e + 1]);
+        }
+}
+
+// 64 x 64 fp32 tile from 64 rows of global memory at stride 64 floats, zero past nvalid or
+// everywhere if !use: asynchronous 16-byte copies (zero-filled where not used), waited for
+// by cp_async_wait
+__device__ __forceinline__ void load_tile_async(float *tile, const float *src, int nvalid, bool use) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int e = threadIdx.x + it * kThreads, r = e >> 4, c = (e & 15) * 4;
+        const bool in = use && r < nvalid;
+        const uint32_t dst = smem_u32(tile + r * LD + c);
+        const float *g = in ? src + (size_t)r * kD + c : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(g),
+                     "r"(in ? 16 : 0)
+                     : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+// Three bf16 64 x 64 tiles (rows of (.., L, 64) tensors, zero past nvalid) as fp32: every
+// load is issued before the first conversion
+__device__ __forceinline__ void load_bf16_tiles(float *const (&dst)[3],
+                                                const __nv_bfloat16 *const (&src)[3], int nvalid) {
+    uint2 u[3][4];
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = threadIdx.x + it * kThreads, r = e >> 4, c = (e & 15) * 4;
+            u[m][it] = r < nvalid ? *reinterpret_cast<const uint2 *>(src[m] + (size_t)r * kD + c)
+                                  : make_uint2(0u, 0u);
+        }
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = threadIdx.x + it * kThreads, r = e >> 4, c = (e & 15) * 4;
+            const float2 a = unpack_bf16x2(u[m][it].x), b = unpack_bf16x2(u[m][it].y);
+            *reinterpret_cast<float4 *>(dst[m] + r * LD + c) = make_float4(a.x, a.y, b.x, b.y);
+        }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_block_mm_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                    const __nv_bfloat16 *__restrict__ w, const float *__restrict__ beta,
+                    const float *__restrict__ dqt, const float *__restrict__ dkt,
+                    const float *__restrict__ dP, const float *__restrict__ dTd,
+                    float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dw,
+                    float *__restrict__ dbeta, int L, int Lp, int nblk) {
+    extern __shared__ __align__(16) float sm[];
+    float *S[kTiles];
+#pragma unroll
+    for (int i = 0; i < kTiles; ++i) S[i] = sm + i * (kTile / 4);
+    float *const Ys = sm + kYOff / 4;
+    float *const bs = sm + kBetaOff / 4;
+    float *const dbs = bs + 64;
+
+    const int tid = threadIdx.x;
+    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = blk * kC;
+    const size_t hL = (size_t)bh * L;
+    const int nvalid = min(kC, L - t0);
+    const bool last = blk == nblk - 1;
+    const Frag f;
+
+    // tiles: 0 W, 1 Q, 2 K, 3 dq~, 4 dk~, 5 dP, 6 dT, then 7-11 as noted per step
+    float *const W = S[0], *const Q = S[1], *const K = S[2];
+    load_tile_async(S[3], dqt + ((size_t)bh * Lp + t0) * kD, nvalid, true);
+    load_tile_async(S[4], dkt + ((size_t)bh * Lp + t0) * kD, nvalid, !last);
+    load_tile_async(S[5], dP + ((size_t)bh * nblk + blk) * kC * kC, kC, blk > 0 && !last);
+    load_tile_async(S[6], dTd + ((size_t)bh * nblk + blk) * kC * kC, nvalid, true);
+    {
+        float *const dst[3] = {W, Q, K};
+        const __nv_bfloat16 *const src[3] = {w + (hL + t0) * kD, q + (hL + t0) * kD,
+                                             k + (hL + t0) * kD};
+        load_bf16_tiles(dst, src, nvalid);
+    }
+    cp_async_wait();
+    if (tid < kC) {
+        bs[tid] = tid < nvalid ? beta[hL + t0 + tid] : 0.f;
+        dbs[tid] = 0.f;
+    }
+    __syncthreads();
+    // dT only where j <= i
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        if (c > r) S[6][r * LD + c] = 0.f;
+    }
+
+    Acc a0, a1, a2;
+    // ---- G = W W^T -> E = D strictly-upper(G) (tile 10); Lq (8), Rk (9)
+    zero(a0);
+    mm<false, true>(W, W, f, a0);
+    put(S[10], a0, f, [](int, int) { return true; });
+    zero(a1);
+    zero(a2);
+    mm2<false, true, false, false, true, false>(Q, W, a1, K, W, a2, f);
+    put(S[8], a1, f, [](int r, int c) { return c <= r; });
+    put(S[9], a2, f, [](int r, int c) { return c > r; });
+    __syncthreads();
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        S[10][r * LD + c] = c > r ? bs[r] * S[10][r * LD + c] : 0.f;
+    }
+    __syncthreads();
+    // ---- X = (I + E)^{-1} in place (tile 10), A = X D (tile 11)
+    blocked_unit_upper_inverse(S[10], Ys, tid);
+    float *const X = S[10], *const A = S[11], *const Lq = S[8], *const Rk = S[9];
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        A[r * LD + c] = X[r * LD + c] * bs[c];
+    }
+    __syncthreads();
+
+    // ---- U = A^T W (tile 7); dLq = -dq~ U^T; dU = -Lq^T dq~ (tile 7); dq = dq~ + ...
+    Acc dLq, dQ, dRk, dK, dW, dA;
+    zero(a0);
+    mm<true, false>(A, W, f, a0);
+    put(S[7], a0, f, [](int, int) { return true; });
+    get(S[3], f, dQ);
+    __syncthreads();
+    zero(dLq);
+    zero(a0);
+    mm2<false, true, true, true, false, true>(S[3], S[7], dLq, Lq, S[3], a0, f);  // dLq, dU
+    __syncthreads();
+    put(S[7], a0, f, [](int, int) { return true; });
+    float *const dU = S[7];
+    // ---- V = A W (tile 3); dRk = -dk~ V^T; dV = -Rk^T dk~ - W dP (tile 4 after); dw = -V dP^T
+    zero(a0);
+    mm<false, false>(A, W, f, a0);
+    put(S[3], a0, f, [](int, int) { return true; });
+    get(S[4], f, dK);
+    __syncthreads();
+    zero(dRk);
+    zero(a1);
+    mm2<false, true, true, true, false, true>(S[4], S[3], dRk, Rk, S[4], a1, f);
+    zero(dW);
+    mm2<false, false, true, false, true, true>(W, S[5], a1, S[3], S[5], dW, f);
+    __syncthreads();
+    put(S[4], a1, f, [](int, int) { return true; });
+    float *const dV = S[4];
+    // ---- with dT (tile 6): dq += dT K; dk += dT^T Q; dY = -dT Rk (tile 3); Y = Lq A^T (5)
+    mm2<false, false, false, true, false, false>(S[6], K, dQ, S[6], Q, dK, f);
+    zero(a0);
+    zero(a1);
+    mm2<false, false, true, false, true, false>(S[6], Rk, a0, Lq, A, a1, f);  // dY, Y
+    put(S[3], a0, f, [](int, int) { return true; });
+    put(S[5], a1, f, [](int, int) { return true; });
+    __syncthreads();
+    float *const dY = S[3];
+    mm2<true, false, true, false, false, false>(S[6], S[5], dRk, dY, A, dLq, f);  // -dT^T Y, dY A
+    zero(dA);
+    mm<true, false>(dY, Lq, f, dA);             // dY^T Lq
+    __syncthreads();
+    // ---- dLq = tril (tile 5), dRk = striu (tile 6); dq, dk complete
+    put(S[5], dLq, f, [](int r, int c) { return c <= r; });
+    put(S[6], dRk, f, [](int r, int c) { return c > r; });
+    __syncthreads();
+    mm2<false, false, false, false, false, false>(S[5], W, dQ, S[6], W, dK, f);
+    mm<true, false>(S[5], Q, f, dW);
+    mm<true, false>(S[6], K, f, dW);
+    store_rows(dq + (hL + t0) * kD, dQ, f, nvalid);
+    store_rows(dk + (hL + t0) * kD, dK, f, nvalid);
+    // ---- dA += W dU^T + dV W^T; dw += A dU + A^T dV
+    mm2<false, true, false, false, false, false>(W, dU, dA, A, dU, dW, f);
+    mm2<false, true, false, true, false, false>(dV, W, dA, A, dV, dW, f);
+    // ---- A = X D: dbeta_u += sum_s dA_su X_su, dX = dA D (tile 1)
+    {
+        float cs[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cs[j][0] = cs[j][1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = f.row(e), c = f.col(j, e);
+                cs[j][e & 1] = fmaf(dA[j][e], X[r * LD + c], cs[j][e & 1]);
+                dA[j][e] *= bs[c];
+            }
+        // column sums over the warp's 16 rows: lanes with the same t hold the same columns
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v = cs[j][h];
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (f.g == 0) atomicAdd(&dbs[f.n0 + 8 * j + 2 * f.t + h], v);
+            }
+    }
+    __syncthreads();  // Q no longer read: tile 1 takes dX
+    put(S[1], dA, f, [](int, int) { return true; });
+    __syncthreads();
+    // ---- dTT = -X^T dX X^T (P1 = X^T dX in tile 2)
+    zero(a0);
+    mm<true, false>(X, S[1], f, a0);
+    __syncthreads();  // K no longer read
+    put(S[2], a0, f, [](int, int) { return true; });
+    __syncthreads();
+    zero(a1);
+    zero(a2);
+    mm2<false, true, true, false, true, false>(S[2], X, a1, W, W, a2, f);  // dTT, G again
+    // ---- T = I + D strictly-upper(G): dbeta_s += sum_{v>s} dTT_sv G_sv, dG = D su(dTT)
+    {
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = f.row(e), c = f.col(j, e);
+                const bool up = c > r;
+                rs[e >> 1] = fmaf(up ? a1[j][e] : 0.f, a2[j][e], rs[e >> 1]);
+                a1[j][e] = up ? bs[r] * a1[j][e] : 0.f;
+            }
+        // row sums over the warp's 32 columns: the four lanes with the same g
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v = rs[h];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (f.t == 0) atomicAdd(&dbs[f.m0 + f.g + 8 * h], v);
+        }
+    }
+    put(S[3], a1, f, [](int, int) { return true; });  // dG
+    __syncthreads();
+    zero(a0);
+    mm2<false, false, false, true, false, false>(S[3], W, dW, S[3], W, a0, f);  // dG W, dG^T W
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dW[j][e] += a0[j][e];
+    store_rows(dw + (hL + t0) * kD, dW, f, nvalid);
+    if (tid < nvalid) dbeta[hL + t0 + tid] = dbs[tid];
+}
+
+}  // namespace
+
+// The block pass for bf16 inputs: dq, dk, dw (B, H, L, 64) and dbeta (B, H, L), fp32, from
+// the query pass's dq~, dk~ (BH, Lp, 64), dP and the diagonal dT (BH, nblk, 64, 64).
+cudaError_t launch_bwd_block_mm(const void *q, const void *k, const void *w, const float *beta,
+                                const float *dqt, const float *dkt, const float *dP,
+                                const float *dTd, float *dq, float *dk, float *dw,
+                                float *dbeta, int BH, int L, int Lp, int nblk,
+                                cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_block_mm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    bwd_block_mm_kernel<<<dim3(nblk, BH), kThreads, kSmem, stream>>>(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(w), beta, dqt, dkt, dP, dTd, dq, dk, dw, dbeta, L, Lp,
+        nblk);
+    return cudaGetLastError();
+}
+
+}  // namespace path

@@ -47,11 +47,11 @@ namespace path {
 cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, const float *beta,
                                  const float *log_f, int BH, int L, float scale, void *ws,
                                  uint64_t limit_ns, cudaStream_t stream);
-template <typename T>
-cudaError_t launch_bwd_block(const void *q, const void *k, const void *w, const float *beta,
-                             const float *dqt, const float *dkt, const float *dP,
-                             const float *dTd, float *dq, float *dk, float *dw, float *dbeta,
-                             int BH, int L, int Lp, int nblk, cudaStream_t stream);
+cudaError_t launch_bwd_block_mm(const void *q, const void *k, const void *w, const float *beta,
+                                const float *dqt, const float *dkt, const float *dP,
+                                const float *dTd, float *dq, float *dk, float *dw,
+                                float *dbeta, int BH, int L, int Lp, int nblk,
+                                cudaStream_t stream);
 cudaError_t launch_bwd_fox_sums(const float *log_f, int BH, int L, int Lp, int nblk, float *loc,
                                 double *cb, cudaStream_t stream);
 cudaError_t launch_bwd_fox_dlogf(const float *rsum, const float *csum, int BH, int L, int Lp,
@@ -772,8 +772,8 @@ cudaError_t launch_path_bwd_tc(const void *q, const void *k, const void *v, cons
         rs, cs, L, y.Lp, y.nblk, y.nbe, scale, scale * kLog2e, reinterpret_cast<uint32_t *>(base),
         limit_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_bwd_block<__nv_bfloat16>(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw, dbeta,
-                                             y.BH, L, y.Lp, y.nblk, stream)) != cudaSuccess)
+    if ((e = launch_bwd_block_mm(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, y.BH, L,
+                                 y.Lp, y.nblk, stream)) != cudaSuccess)
         return e;
     if (fox) e = launch_bwd_fox_dlogf(rs, cs, y.BH, L, y.Lp, dlogf, stream);
     return e;

@@ -14,12 +14,11 @@
 // Lq U equals (Lq A^T) W and Lq Khat^T equals Lq A^T Rk^T, the leading/trailing partial
 // products of the UT form (sub-blocks of A invert the matching sub-blocks of T).
 //
-// (I + E)^{-1} is formed blockwise: the four 16 x 16 diagonal blocks by back-substitution,
-// then X12 = -X11 E12 X22 for the 16-blocks and for the 32-blocks, each 16 x 8 output tile
+// (I + E)^{-1} is formed blockwise (ut_inverse.cuh): the four 16 x 16 diagonal blocks by
+// back-substitution, then the 16- and 32-block combine products, each 16 x 8 output tile
 // one warp's mma.sync with tf32 operands (these products are too small for tcgen05, and the
 // fragment loads keep shared-memory traffic low; A goes on as fp16, so tf32's 10-bit
-// significand matches its use). Every factor is bounded (X_su = A_su / beta_u), so no
-// intermediate grows.
+// significand matches its use).
 //
 // tcgen05.mma groups, all M = 128, with 64x64 16-bit tiles in 128-byte-swizzled shared
 // memory (K-major tiles stacked in M must be adjacent; MN-major atoms use the LBO stride):
@@ -37,6 +36,7 @@
 // the TMA loads and the MMAs. 128 TMEM columns, 72 KB of tiles and 80 registers per
 // thread, so three CTAs (24 warps) share an SM.
 #include "common.cuh"
+#include "ut_inverse.cuh"
 
 namespace path {
 
@@ -53,9 +53,13 @@ constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_Z = 3 * kT, T_LQ 
                    T_RKT = 5 * kT, T_AT = 6 * kT, T_A = 7 * kT, T_U = 6 * kT, T_KHT = 7 * kT,
                    T_V = 8 * kT;
 constexpr uint32_t SCR = 6 * kT;           // solve scratch (E/X fp32 + Y) overlays slots 6-8
-constexpr int XLD = 68;
+using ut_inverse::XLD;
+using ut_inverse::YLD;
+using ut_inverse::blocked_unit_upper_inverse;
+using ut_inverse::mma_tf32;
+using ut_inverse::to_tf32;
+using ut_inverse::warp_tile_16x8;
 constexpr uint32_t Y_OFF = SCR + 64 * XLD * 4;
-constexpr int YLD = 40;  // B-fragment loads of Y (rows t, columns g) hit 32 banks
 constexpr uint32_t BAR_OFF = 9 * kT;       // 2 mbarriers
 constexpr uint32_t SLOT_OFF = BAR_OFF + 16;
 constexpr uint32_t BETA_OFF = SLOT_OFF + 16;
@@ -129,104 +133,6 @@ __device__ __forceinline__ void store_global_half(__nv_bfloat16 *dst, const floa
         d[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]), pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
                           pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
                           pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// One warp: the 16 x 8 tile acc = A (16 x K, row-major, stride lda) x B (K x 8, row-major,
-// stride ldb) on the tensor cores with tf32 operands (one product per k-step: the products
-// feed A, which later MMAs take as fp16, so a 10-bit operand significand is enough).
-// Fragment layout of m16n8k8: g = lane / 4, t = lane % 4; A rows g, g + 8 and columns
-// t, t + 4; B rows t, t + 4 and column g; acc rows g (0, 1), g + 8 (2, 3), columns 2t, 2t + 1.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-template <int K>
-__device__ __forceinline__ void warp_tile_16x8(const float *A, int lda, const float *B, int ldb,
-                                               int lane, float (&acc)[4]) {
-    const int g = lane >> 2, t = lane & 3;
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-#pragma unroll
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        const uint32_t a[4] = {to_tf32(A[g * lda + k0 + t]), to_tf32(A[(g + 8) * lda + k0 + t]),
-                               to_tf32(A[g * lda + k0 + t + 4]),
-                               to_tf32(A[(g + 8) * lda + k0 + t + 4])};
-        const uint32_t b[2] = {to_tf32(B[(k0 + t) * ldb + g]), to_tf32(B[(k0 + t + 4) * ldb + g])};
-        mma_tf32(acc, a, b);
-    }
-}
-
-// (I + E)^{-1} in place over E (upper triangle; E is zero on and below the diagonal),
-// all 256 threads. On return X[s][u] (s <= u) holds the inverse.
-__device__ __forceinline__ void blocked_unit_upper_inverse(float *X, float *Y, int r) {
-    // level 0: the four 16 x 16 diagonal blocks, one column per thread (threads 0-63).
-    // Column u of the inverse solves x_l = -sum_{m>l} E_lm x_m (x_lu = 1, x_l = 0 below);
-    // right-looking: once x_m is final it is folded into the partial sums of every row
-    // above, so the dependent chain is one FMA per row instead of a whole dot product.
-    float x[16];
-    const int u = r & 63, b0 = (u >> 4) << 4, lu = u & 15;
-    if (r < 64) {
-#pragma unroll
-        for (int l = 0; l < 16; ++l) x[l] = 0.f;
-#pragma unroll
-        for (int m = 15; m >= 0; --m) {
-            x[m] = (m == lu) ? 1.f : ((m < lu) ? -x[m] : 0.f);
-#pragma unroll
-            for (int l = 0; l < m; ++l) x[l] = fmaf(X[(b0 + l) * XLD + b0 + m], x[m], x[l]);
-        }
-    }
-    __syncthreads();
-    if (r < 64) {
-#pragma unroll
-        for (int l = 0; l < 16; ++l) X[(b0 + l) * XLD + u] = x[l];
-    }
-    __syncthreads();
-    const int warp = r >> 5, lane = r & 31, g = lane >> 2, t = lane & 3;
-    float acc[4];
-    // level 1: X[o:o+16, o+16:o+32] = -X11 E12 X22 for the two 32-blocks (o = 0, 32);
-    // warps 0-3, warp = (block p, 8-column tile n)
-    if (warp < 4) {
-        const int o = 32 * (warp >> 1), n0 = 8 * (warp & 1);
-        warp_tile_16x8<16>(X + o * XLD + o + 16, XLD, X + (o + 16) * XLD + o + 16 + n0, XLD,
-                           lane, acc);
-        float *y = Y + (o >> 1) * YLD + n0;  // rows 16 p .. 16 p + 15 of Y
-        *reinterpret_cast<float2 *>(y + g * YLD + 2 * t) = make_float2(acc[0], acc[1]);
-        *reinterpret_cast<float2 *>(y + (g + 8) * YLD + 2 * t) = make_float2(acc[2], acc[3]);
-    }
-    __syncthreads();
-    if (warp < 4) {
-        const int o = 32 * (warp >> 1), n0 = 8 * (warp & 1);
-        warp_tile_16x8<16>(X + o * XLD + o, XLD, Y + (o >> 1) * YLD + n0, YLD, lane, acc);
-        float *x12 = X + o * XLD + o + 16 + n0;
-        *reinterpret_cast<float2 *>(x12 + g * XLD + 2 * t) = make_float2(-acc[0], -acc[1]);
-        *reinterpret_cast<float2 *>(x12 + (g + 8) * XLD + 2 * t) = make_float2(-acc[2], -acc[3]);
-    }
-    __syncthreads();
-    // level 2: X[0:32, 32:64] = -X[0:32, 0:32] E[0:32, 32:64] X[32:64, 32:64];
-    // warp = (16-row tile m, 8-column tile n)
-    {
-        const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
-        warp_tile_16x8<32>(X + m0 * XLD + 32, XLD, X + 32 * XLD + 32 + n0, XLD, lane, acc);
-        float *y = Y + m0 * YLD + n0;
-        *reinterpret_cast<float2 *>(y + g * YLD + 2 * t) = make_float2(acc[0], acc[1]);
-        *reinterpret_cast<float2 *>(y + (g + 8) * YLD + 2 * t) = make_float2(acc[2], acc[3]);
-        __syncthreads();
-        warp_tile_16x8<32>(X + m0 * XLD, XLD, Y + n0, YLD, lane, acc);
-        float *x12 = X + m0 * XLD + 32 + n0;
-        *reinterpret_cast<float2 *>(x12 + g * XLD + 2 * t) = make_float2(-acc[0], -acc[1]);
-        *reinterpret_cast<float2 *>(x12 + (g + 8) * XLD + 2 * t) = make_float2(-acc[2], -acc[3]);
-    }
-    __syncthreads();
 }
 
 // Thread layout: warp w reads TMEM lanes 32 (w mod 4) .. +31 (the accumulator rows lr) and

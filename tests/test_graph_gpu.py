@@ -88,9 +88,11 @@ def test_backward_graph_replay(lib):
     bwd()
     torch.cuda.synchronize()
     # the backward accumulates some gradients with atomics: replay and eager may add the
-    # same terms in another order, so compare to fp32 rounding of the largest entry
+    # same terms in another order, and the bf16 block pass reads those sums as tf32 operands
+    # (a 10-bit significand), so an order-dependent last bit can move a result by about
+    # 2^-10 of its size; a replay of stale inputs would differ by the whole gradient
     for n, t in grads.items():
-        tol = 1e-5 * t.abs().max().item() + 1e-30
+        tol = 2e-3 * t.abs().max().item() + 1e-30
         assert (got[n] - t).abs().max().item() <= tol, n
 
 
