@@ -240,7 +240,7 @@ def path_attn_bwd(q, k, v, w, beta, out, lse, d_out, scale=None, grads=None, wor
     _bwd_checks(q, out, lse, d_out, B, H, L)
     g = _bwd_grads(q, grads, B, H, L, d, False)
     if workspace is None:
-        workspace = new_workspace(OP_BWD, B, H, L, dt, q.device)
+        workspace = new_workspace(OP_BWD, B, H, L, dt, q.device, d=d)
     _check(_load().path_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(out),
                                  _ptr(lse), _ptr(d_out), B, H, L, d, dt, _scale(scale, d),
                                  _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dw"]),
@@ -261,7 +261,7 @@ def path_fox_bwd(q, k, v, w, beta, log_f, out, lse, d_out, scale=None, grads=Non
     _bwd_checks(q, out, lse, d_out, B, H, L)
     g = _bwd_grads(q, grads, B, H, L, d, True)
     if workspace is None:
-        workspace = new_workspace(OP_FOX_BWD, B, H, L, dt, q.device)
+        workspace = new_workspace(OP_FOX_BWD, B, H, L, dt, q.device, d=d)
     _check(_load().path_fox_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f),
                                 _ptr(out), _ptr(lse), _ptr(d_out), B, H, L, d, dt,
                                 _scale(scale, d), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),

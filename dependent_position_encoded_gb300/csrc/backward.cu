@@ -28,7 +28,7 @@
 // logits from the inputs. PaTH-FoX adds the bias c_i - c_j (c = cumsum of log f) to every
 // logit; it leaves dT unchanged and gives d log f_s = sum over j < s <= i of dS_ij, formed
 // from the row and column sums of dS. Every key block is visited (no early exit).
-#include "common.cuh"
+#include "bwd_f32_tiles.cuh"
 
 namespace path {
 
@@ -40,179 +40,9 @@ cudaError_t launch_ut_prepare_f32out(const void *q, const void *k, const void *w
 
 namespace {
 
-constexpr int LD = 68;          // padded row stride (floats) of a 64 x 64 shared buffer
-constexpr int BUF = kC * LD;
-constexpr int kThreads = 256;
-constexpr int kBlkTile = kC * kD;  // floats in one 64 x 64 tile
-
-// 64 x 64 fp32 tile from global (row-major, 64 floats per row) into shared memory, as is
-// (dst[r][c]) or transposed (dst[c][r]). Each thread issues all four of its 16-byte loads
-// before the first store, so the tile costs one memory latency.
-__device__ __forceinline__ void load_tile(float *dst, const float *__restrict__ src, bool transpose) {
-    constexpr int kIt = kBlkTile / 4 / kThreads;
-    float4 x[kIt];
-#pragma unroll
-    for (int it = 0; it < kIt; ++it)
-        x[it] = reinterpret_cast<const float4 *>(src)[threadIdx.x + it * kThreads];
-#pragma unroll
-    for (int it = 0; it < kIt; ++it) {
-        const int e = 4 * (threadIdx.x + it * kThreads), r = e / kD, c = e % kD;
-        if (transpose) {
-            dst[c * LD + r] = x[it].x;
-            dst[(c + 1) * LD + r] = x[it].y;
-            dst[(c + 2) * LD + r] = x[it].z;
-            dst[(c + 3) * LD + r] = x[it].w;
-        } else {
-            *reinterpret_cast<float4 *>(dst + r * LD + c) = x[it];
-        }
-    }
-}
-
-// Rows t0 .. t0 + 63 of a (rows, 64) tensor of type T, zero past L, as is and transposed
-// (either may be null); four elements per thread and step, all loads issued first.
-template <typename T>
-__device__ __forceinline__ void load_rows(float *dst, float *dst_t, const T *__restrict__ src,
-                                          int t0, int L) {
-    constexpr int kIt = kBlkTile / 4 / kThreads;
-    float x[kIt][4];
-#pragma unroll
-    for (int it = 0; it < kIt; ++it) {
-        const int e = 4 * (threadIdx.x + it * kThreads), r = e / kD, c = e % kD;
-        const bool in = t0 + r < L;
-        const T *p = src + (size_t)(t0 + r) * kD + c;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) x[it][q] = in ? Elt<T>::to_f(p[q]) : 0.f;
-    }
-#pragma unroll
-    for (int it = 0; it < kIt; ++it) {
-        const int e = 4 * (threadIdx.x + it * kThreads), r = e / kD, c = e % kD;
-        if (dst) *reinterpret_cast<float4 *>(dst + r * LD + c) = make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
-        if (dst_t)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst_t[(c + q) * LD + r] = x[it][q];
-    }
-}
+using namespace bwd_f32;
 
 // ---------------------------------------------------------------- B1: query pass
-// Four groups of 64 threads; a group computes half (32 rows) of a 64 x 64 x 64 product as
-// a 4 x 8 register tile per thread. Every operand stays in its stored row-major layout
-// (no transposed copies); the three forms of product are
-//   mm48:   A row-major (rows r0 + 8i), B k-major (columns col48(c0, j))     e.g. G P_b
-//   mmrb48: A and B row-major, the contraction index contiguous in both (rows r0 + 8i,
-//           columns n0 + 8j)                                                  e.g. X K~_b^T
-//   mmkk48: A and B k-major (rows m0 + i, columns col48(c0, j))               e.g. dT^T X
-// With ty, tx = the thread's row and column in its group (8 x 8), r0 = rb + ty,
-// m0 = rb + 4 ty, c0 = 4 tx and n0 = tx (rb = 0 or 32, the group's half). The lanes of a
-// quarter warp share the A rows (broadcast loads) and read eight distinct 16-byte pieces of
-// B (contiguous, or eight consecutive rows at a stride of 68 floats).
-__device__ __forceinline__ int col48(int c0, int j) { return c0 + (j < 4 ? j : 28 + j); }
-
-// acc[i][j] += sum_k A[r0 + 8i][k] * B[k][col48(c0, j)]
-__device__ __forceinline__ void mm48(const float *__restrict__ A, const float *__restrict__ B,
-                                     int r0, int c0, float (&acc)[4][8]) {
-#pragma unroll 2
-    for (int k = 0; k < kC; k += 4) {
-        float4 a[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 8 * i) * LD + k);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const float4 b0 = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + c0);
-            const float4 b1 = *reinterpret_cast<const float4 *>(B + (k + kk) * LD + c0 + 32);
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
-            }
-        }
-    }
-}
-
-// acc[i][j] += sum_k A[r0 + 8i][k] * B[n0 + 8j][k]
-__device__ __forceinline__ void mmrb48(const float *__restrict__ A, const float *__restrict__ B,
-                                       int r0, int n0, float (&acc)[4][8]) {
-#pragma unroll 1
-    for (int k = 0; k < kC; k += 4) {
-        float4 a[4], b[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(A + (r0 + 8 * i) * LD + k);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) b[j] = *reinterpret_cast<const float4 *>(B + (n0 + 8 * j) * LD + k);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float t = acc[i][j];
-                t = fmaf(a[i].x, b[j].x, t);
-                t = fmaf(a[i].y, b[j].y, t);
-                t = fmaf(a[i].z, b[j].z, t);
-                acc[i][j] = fmaf(a[i].w, b[j].w, t);
-            }
-    }
-}
-
-// acc[i][j] += sum_k A[k][m0 + i] * B[k][col48(c0, j)]
-__device__ __forceinline__ void mmkk48(const float *__restrict__ A, const float *__restrict__ B,
-                                       int m0, int c0, float (&acc)[4][8]) {
-#pragma unroll 4
-    for (int k = 0; k < kC; ++k) {
-        const float4 a = *reinterpret_cast<const float4 *>(A + k * LD + m0);
-        const float4 b0 = *reinterpret_cast<const float4 *>(B + k * LD + c0);
-        const float4 b1 = *reinterpret_cast<const float4 *>(B + k * LD + c0 + 32);
-        const float av[4] = {a.x, a.y, a.z, a.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-}
-
-__device__ __forceinline__ void zero48(float (&a)[4][8]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a[i][j] = 0.f;
-}
-
-// an mm48 tile (rows r0 + 8i, columns col48) into shared memory
-__device__ __forceinline__ void put48(float *dst, const float (&v)[4][8], int r0, int c0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = r0 + 8 * i;
-        *reinterpret_cast<float4 *>(dst + r * LD + c0) = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
-        *reinterpret_cast<float4 *>(dst + r * LD + c0 + 32) = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
-    }
-}
-
-// an mm48 tile stored into a row-major (64 floats per row) global tile
-__device__ __forceinline__ void st48(float *dst, const float (&v)[4][8], int r0, int c0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = r0 + 8 * i;
-        *reinterpret_cast<float4 *>(dst + r * kC + c0) = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
-        *reinterpret_cast<float4 *>(dst + r * kC + c0 + 32) = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
-    }
-}
-
-// an mmrb48 tile (rows r0 + 8i, columns n0 + 8j) into a row-major buffer of stride ld
-__device__ __forceinline__ void put_rb(float *dst, int ld, const float (&v)[4][8], int r0, int n0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dst[(r0 + 8 * i) * ld + n0 + 8 * j] = v[i][j];
-}
-
-// an mmkk48 tile (rows m0 + i, columns col48) added into a row-major global tile
-__device__ __forceinline__ void red_kk(float *dst, const float (&v)[4][8], int m0, int c0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) atomicAdd(dst + (m0 + i) * kC + col48(c0, j), v[i][j]);
-}
-
 // One CTA per (query block a, head), two per SM; a runs from the last block down so that
 // the longest walks start first. Five 64 x 64 fp32 buffers, all row-major:
 //   pass 1: R0 X [i][c], R1 dout [i][c], R2 K~_b [j][c] then p [i][j], R3 P_b [n][c] then
@@ -242,7 +72,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     float *loci = Drow + kC;    // FoX: block-local gate sums of the query rows
     float *locj = loci + kC;    // FoX: those of the current key block
 
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int a = nblk - 1 - (int)blockIdx.x;
     const int bh = blockIdx.y;
     const int grp = tid >> 6, lt = tid & 63, ty = lt >> 3, tx = lt & 7;
@@ -275,18 +105,7 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
     // column sums of a tile go out with one atomic per column and warp
     float rs_acc[4] = {0.f, 0.f, 0.f, 0.f};
     auto fox_sums = [&](float (&rp)[4], float (&cp)[8], int kb) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) rp[i] += __shfl_xor_sync(0xffffffffu, rp[i], o);
-            rs_acc[i] += rp[i];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 8);
-            cp[j] += __shfl_xor_sync(0xffffffffu, cp[j], 16);
-            if (lane < 8) atomicAdd(csum + (size_t)bh * Lp + (size_t)kb * kC + n0 + 8 * j, cp[j]);
-        }
+        fox_tile_sums(rp, cp, rs_acc, csum + (size_t)bh * Lp + (size_t)kb * kC, n0);
     };
 
     load_rows<T>(R1, nullptr, dout + hL * kD, t0, L);
@@ -441,30 +260,72 @@ bwd_query_kernel(const T *__restrict__ v, const T *__restrict__ o, const T *__re
 }
 
 // ---------------------------------------------------------------- B2: block pass
-// One CTA per (block, head), 8 warps, two CTAs per SM. Warp w runs three groups of eight
-// sweeps, each group in lockstep: query rows i = 8w .. 8w + 7 (q~_i and the diagonal
-// logits), columns c = 8w .. 8w + 7 of P_b, and key rows j = 8w .. 8w + 7 (k~_j); short
-// query sweeps meet long key sweeps, so the warps' loads match. Lane l holds dimensions 2l
-// and 2l + 1 of every vector. A sweep first applies its transitions, recording only
+// One CTA per (block, head), 8 warps (two CTAs per SM at d = 64, one at d = 128). Warp w runs
+// groups of eight sweeps, each group in lockstep: query rows i = 8w .. 8w + 7 (q~_i and the
+// diagonal logits), columns c = (d / 8) w .. (d / 8) w + d / 8 - 1 of P_b (one group at
+// d = 64, two at d = 128), and key rows j = 8w .. 8w + 7 (k~_j); short query sweeps meet
+// long key sweeps, so the warps' loads match. Lane l holds dimensions NE l .. NE l + NE - 1
+// (NE = d / 32) of every vector. A sweep first applies its transitions, recording only
 // w_s . x of each step, then walks back with the gradient, recovering each step's input by
 // undoing the step: the step is x' = x - c w_s with c = beta_s (w_s . x), so x = x' + c w_s,
 // exact up to rounding (no H_s is inverted; it is singular at beta_s = 1). Per step the
 // eight sweeps share one read of w_s and beta_s, run eight independent warp reductions,
-// and add their summed dw, dk and dbeta terms to shared memory with one atomic per lane.
-// dq is written by its query sweep.
+// and add their summed dw, dk and dbeta terms to shared memory with one atomic per lane
+// and dimension. dq is written by its query sweep.
 constexpr int kWarps = kThreads / 32;
 constexpr int kNS = 8;  // sweeps per warp group
+
+// NE consecutive fp32 values from / to memory (8- or 16-byte aligned)
+template <int NE>
+__device__ __forceinline__ void ldv(float (&r)[NE], const float *p) {
+    static_assert(NE == 2 || NE == 4, "two or four dimensions per lane");
+    if constexpr (NE == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        r[0] = t.x;
+        r[1] = t.y;
+    } else {
+        const float4 t = *reinterpret_cast<const float4 *>(p);
+        r[0] = t.x;
+        r[1] = t.y;
+        r[2] = t.z;
+        r[3] = t.w;
+    }
+}
+template <int NE>
+__device__ __forceinline__ void stv(float *p, const float (&r)[NE]) {
+    if constexpr (NE == 2)
+        *reinterpret_cast<float2 *>(p) = make_float2(r[0], r[1]);
+    else
+        *reinterpret_cast<float4 *>(p) = make_float4(r[0], r[1], r[2], r[3]);
+}
+template <typename T, int NE>
+__device__ __forceinline__ void loadv(float (&r)[NE], const T *p) {
+#pragma unroll
+    for (int e = 0; e < NE; ++e) r[e] = Elt<T>::to_f(p[e]);
+}
+template <int NE>
+__device__ __forceinline__ void zerov(float (&r)[NE]) {
+#pragma unroll
+    for (int e = 0; e < NE; ++e) r[e] = 0.f;
+}
 
 // out[k] = w . x[k] over the warp, for the eight vectors of a group. A transposed butterfly:
 // at xor 16, 8 and 4 each lane keeps half of its partial sums and adds its partner's copy
 // of them, so lane l ends with the total of vector 4 bit4(l) + 2 bit3(l) + bit2(l) after
 // two more levels; eight shuffles from lanes 4k broadcast the totals (17 shuffles, not 40)
-__device__ __forceinline__ void dot8(const float2 (&x)[kNS], float2 w, float (&out)[kNS]) {
+template <int NE>
+__device__ __forceinline__ void dot8(const float (&x)[kNS][NE], const float (&w)[NE],
+                                     float (&out)[kNS]) {
     constexpr unsigned kAll = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     float p[kNS];
 #pragma unroll
-    for (int k = 0; k < kNS; ++k) p[k] = fmaf(w.x, x[k].x, w.y * x[k].y);
+    for (int k = 0; k < kNS; ++k) {
+        float t = w[NE - 1] * x[k][NE - 1];
+#pragma unroll
+        for (int e = NE - 2; e >= 0; --e) t = fmaf(w[e], x[k][e], t);
+        p[k] = t;
+    }
     const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
     float a[4], b[2];
 #pragma unroll
@@ -480,42 +341,49 @@ __device__ __forceinline__ void dot8(const float2 (&x)[kNS], float2 w, float (&o
     for (int k = 0; k < kNS; ++k) out[k] = __shfl_sync(kAll, c, 4 * k);
 }
 
-template <typename T>
-__device__ __forceinline__ float2 load2(const T *p) {
-    return make_float2(Elt<T>::to_f(p[0]), Elt<T>::to_f(p[1]));
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+// Workspace inputs (fp32): dqt, dkt (BH, Lp, D), dP (BH, nblk, D, D), dTd (BH, nblk, 64, 64).
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
 bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
                  const float *__restrict__ beta, const float *__restrict__ dqt,
                  const float *__restrict__ dkt, const float *__restrict__ dP,
                  const float *__restrict__ dTd, float *__restrict__ dq, float *__restrict__ dk,
                  float *__restrict__ dw, float *__restrict__ dbeta, int L, int Lp, int nblk) {
+    constexpr int NE = D / 32;
+    constexpr int kTile = kC * D;  // floats in one 64 x D tile
     extern __shared__ __align__(16) float sm[];
-    float2 *Ws = reinterpret_cast<float2 *>(sm);             // w_s, [s][lane]
-    float2 *Ks = Ws + kBlkTile / 2;                          // k_j
-    float2 *dWs = Ks + kBlkTile / 2;                         // gradient of w_s
-    float2 *dKs = dWs + kBlkTile / 2;                        // gradient of k_j
-    float *wxs = reinterpret_cast<float *>(dKs + kBlkTile / 2);  // per warp: [s][sweep] w_s . x
-    float *bs = wxs + kWarps * kC * kNS;                     // beta_s
-    float *dBs = bs + kC;                                    // gradient of beta_s
+    float *Ws = sm;               // w_s, [s][dimension]
+    float *Ks = Ws + kTile;       // k_j
+    float *dWs = Ks + kTile;      // gradient of w_s
+    float *dKs = dWs + kTile;     // gradient of k_j
+    float *wxs = dKs + kTile;     // per warp: [s][sweep] w_s . x
+    float *bs = wxs + kWarps * kC * kNS;  // beta_s
+    float *dBs = bs + kC;                 // gradient of beta_s
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int blk = blockIdx.x, bh = blockIdx.y;
     const int t0 = blk * kC;
     const size_t hL = (size_t)bh * L;
     const int nvalid = min(kC, L - t0);
+    const int el = NE * lane;  // this lane's first dimension
 
     // w, k (zero past L: a padded token's transition is the identity), beta
-    for (int e = tid; e < kBlkTile / 2; e += kThreads) {
-        const int r = e / 32, l = e % 32;
-        const bool in = r < nvalid;
-        const size_t g = (hL + t0 + r) * kD + 2 * l;
-        Ws[e] = in ? load2<T>(w + g) : make_float2(0.f, 0.f);
-        Ks[e] = in ? load2<T>(k + g) : make_float2(0.f, 0.f);
-        dWs[e] = make_float2(0.f, 0.f);
-        dKs[e] = make_float2(0.f, 0.f);
+    for (int e = tid; e < kTile / NE; e += kThreads) {
+        const int r = e / 32;
+        const size_t g = (hL + t0 + r) * D + NE * (e % 32);
+        float wv[NE], kv[NE], z[NE];
+        zerov(z);
+        if (r < nvalid) {
+            loadv<T, NE>(wv, w + g);
+            loadv<T, NE>(kv, k + g);
+        } else {
+            zerov(wv);
+            zerov(kv);
+        }
+        stv<NE>(Ws + NE * e, wv);
+        stv<NE>(Ks + NE * e, kv);
+        stv<NE>(dWs + NE * e, z);
+        stv<NE>(dKs + NE * e, z);
     }
     if (tid < kC) {
         bs[tid] = tid < nvalid ? beta[hL + t0 + tid] : 0.f;
@@ -524,31 +392,32 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     __syncthreads();
 
     float *wxw = wxs + warp * kC * kNS;
-    const int base = kNS * warp;  // first row / column of this warp's groups
-    float2 x[kNS], g[kNS];
+    const int base = kNS * warp;  // first query / key row of this warp's groups
+    float x[kNS][NE], g[kNS][NE];
     float wx[kNS], wg[kNS];
 
     // x[k] <- H_s x[k] for the sweeps with act(k), recording w_s . x[k] at wxw[s][k]
     auto fwd = [&](int s, auto act) {
-        const float2 ws = Ws[s * 32 + lane];
+        float ws[NE];
+        ldv<NE>(ws, Ws + s * D + el);
         const float be = bs[s];
-        dot8(x, ws, wx);
+        dot8<NE>(x, ws, wx);
         if (lane == 0) {
             *reinterpret_cast<float4 *>(wxw + s * kNS) = make_float4(wx[0], wx[1], wx[2], wx[3]);
             *reinterpret_cast<float4 *>(wxw + s * kNS + 4) = make_float4(wx[4], wx[5], wx[6], wx[7]);
         }
 #pragma unroll
         for (int kk = 0; kk < kNS; ++kk)
-            if (act(kk)) {
-                x[kk].x = fmaf(-be * wx[kk], ws.x, x[kk].x);
-                x[kk].y = fmaf(-be * wx[kk], ws.y, x[kk].y);
-            }
+            if (act(kk))
+#pragma unroll
+                for (int e = 0; e < NE; ++e) x[kk][e] = fmaf(-be * wx[kk], ws[e], x[kk][e]);
     };
     // one step back through H_s for the sweeps with act(k): x[k] <- the step's input (undo),
     // dw_s, dbeta_s gather the terms, g[k] <- H_s g[k]. `undo` false for a step whose input
     // is already in x (the first step back, through H_0, with w_0 . x given in wx).
     auto back = [&](int s, bool undo, auto act) {
-        const float2 ws = Ws[s * 32 + lane];
+        float ws[NE];
+        ldv<NE>(ws, Ws + s * D + el);
         const float be = bs[s];
         if (undo) {
             const float4 a = *reinterpret_cast<const float4 *>(wxw + s * kNS);
@@ -557,25 +426,25 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
             wx[4] = b.x; wx[5] = b.y; wx[6] = b.z; wx[7] = b.w;
 #pragma unroll
             for (int kk = 0; kk < kNS; ++kk)
-                if (act(kk)) {
-                    x[kk].x = fmaf(be * wx[kk], ws.x, x[kk].x);
-                    x[kk].y = fmaf(be * wx[kk], ws.y, x[kk].y);
-                }
+                if (act(kk))
+#pragma unroll
+                    for (int e = 0; e < NE; ++e) x[kk][e] = fmaf(be * wx[kk], ws[e], x[kk][e]);
         }
-        dot8(g, ws, wg);
-        float2 dws = make_float2(0.f, 0.f);
+        dot8<NE>(g, ws, wg);
+        float dws[NE];
+        zerov(dws);
         float db = 0.f;
 #pragma unroll
         for (int kk = 0; kk < kNS; ++kk)
             if (act(kk)) {
-                dws.x += fmaf(wx[kk], g[kk].x, wg[kk] * x[kk].x);
-                dws.y += fmaf(wx[kk], g[kk].y, wg[kk] * x[kk].y);
+#pragma unroll
+                for (int e = 0; e < NE; ++e) dws[e] += fmaf(wx[kk], g[kk][e], wg[kk] * x[kk][e]);
                 db = fmaf(wg[kk], wx[kk], db);
-                g[kk].x = fmaf(-be * wg[kk], ws.x, g[kk].x);
-                g[kk].y = fmaf(-be * wg[kk], ws.y, g[kk].y);
+#pragma unroll
+                for (int e = 0; e < NE; ++e) g[kk][e] = fmaf(-be * wg[kk], ws[e], g[kk][e]);
             }
-        atomicAdd(&dWs[s * 32 + lane].x, -be * dws.x);
-        atomicAdd(&dWs[s * 32 + lane].y, -be * dws.y);
+#pragma unroll
+        for (int e = 0; e < NE; ++e) atomicAdd(dWs + s * D + el + e, -be * dws[e]);
         if (lane == 0) atomicAdd(&dBs[s], -db);
     };
 
@@ -586,59 +455,77 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
 #pragma unroll
         for (int kk = 0; kk < kNS; ++kk) {
             const int i = base + kk;
-            const bool in = i < nvalid;
-            x[kk] = in ? load2<T>(q + (hL + t0 + i) * kD + 2 * lane) : make_float2(0.f, 0.f);
-            g[kk] = in ? *reinterpret_cast<const float2 *>(dqt + ((size_t)bh * Lp + t0 + i) * kD + 2 * lane)
-                       : make_float2(0.f, 0.f);
-            dtr[kk] = in ? *reinterpret_cast<const float2 *>(
-                               dTd + (((size_t)bh * nblk + blk) * kC + i) * kC + 2 * lane)
-                         : make_float2(0.f, 0.f);
+            if (i < nvalid) {
+                loadv<T, NE>(x[kk], q + (hL + t0 + i) * D + el);
+                ldv<NE>(g[kk], dqt + ((size_t)bh * Lp + t0 + i) * D + el);
+                dtr[kk] = *reinterpret_cast<const float2 *>(
+                    dTd + (((size_t)bh * nblk + blk) * kC + i) * kC + 2 * lane);
+            } else {
+                zerov(x[kk]);
+                zerov(g[kk]);
+                dtr[kk] = make_float2(0.f, 0.f);
+            }
         }
         for (int s = base + kNS - 1; s >= 1; --s) fwd(s, [&](int kk) { return s <= base + kk; });
         __syncwarp();
-        dot8(x, Ws[lane], wx);  // w_0 . x_0
+        {
+            float w0[NE];
+            ldv<NE>(w0, Ws + el);
+            dot8<NE>(x, w0, wx);  // w_0 . x_0
+        }
         back(0, false, all);
         for (int j = 0; j < base + kNS; ++j) {
-            const float2 kj = Ks[j * 32 + lane];  // x[k] = x_j here
-            float2 dka = make_float2(0.f, 0.f);
+            float kj[NE], dka[NE];  // x[k] = x_j here
+            ldv<NE>(kj, Ks + j * D + el);
+            zerov(dka);
 #pragma unroll
             for (int kk = 0; kk < kNS; ++kk)
                 if (j <= base + kk) {
                     const float dtx = __shfl_sync(0xffffffffu, dtr[kk].x, j >> 1);
                     const float dty = __shfl_sync(0xffffffffu, dtr[kk].y, j >> 1);
                     const float dt = (j & 1) ? dty : dtx;
-                    g[kk].x = fmaf(dt, kj.x, g[kk].x);
-                    g[kk].y = fmaf(dt, kj.y, g[kk].y);
-                    dka.x = fmaf(dt, x[kk].x, dka.x);
-                    dka.y = fmaf(dt, x[kk].y, dka.y);
+#pragma unroll
+                    for (int e = 0; e < NE; ++e) {
+                        g[kk][e] = fmaf(dt, kj[e], g[kk][e]);
+                        dka[e] = fmaf(dt, x[kk][e], dka[e]);
+                    }
                 }
-            atomicAdd(&dKs[j * 32 + lane].x, dka.x);
-            atomicAdd(&dKs[j * 32 + lane].y, dka.y);
+#pragma unroll
+            for (int e = 0; e < NE; ++e) atomicAdd(dKs + j * D + el + e, dka[e]);
             if (j + 1 < base + kNS) back(j + 1, true, [&](int kk) { return j + 1 <= base + kk; });
         }
 #pragma unroll
         for (int kk = 0; kk < kNS; ++kk)
-            if (base + kk < nvalid)
-                *reinterpret_cast<float2 *>(dq + (hL + t0 + base + kk) * kD + 2 * lane) = g[kk];
+            if (base + kk < nvalid) stv<NE>(dq + (hL + t0 + base + kk) * D + el, g[kk]);
     }
     __syncwarp();  // the next group rewrites wxw
 
-    // ---- columns c = base + k of P_b = H_0 ... H_63 (P_0 and the last P_b reach no logit)
+    // ---- columns c of P_b = H_0 ... H_63 (P_0 and the last P_b reach no logit)
     if (blk > 0 && blk < nblk - 1) {
-        const float *dpb = dP + ((size_t)bh * nblk + blk) * kBlkTile;
+        const float *dpb = dP + ((size_t)bh * nblk + blk) * D * D;
+        for (int cg = 0; cg < D / 64; ++cg) {
+            const int cbase = (D / 8) * warp + kNS * cg;
 #pragma unroll
-        for (int kk = 0; kk < kNS; ++kk) {
-            const int c = base + kk;
-            x[kk] = make_float2(2 * lane == c ? 1.f : 0.f, 2 * lane + 1 == c ? 1.f : 0.f);
-            g[kk] = make_float2(dpb[(2 * lane) * kC + c], dpb[(2 * lane + 1) * kC + c]);
+            for (int kk = 0; kk < kNS; ++kk) {
+                const int c = cbase + kk;
+#pragma unroll
+                for (int e = 0; e < NE; ++e) {
+                    x[kk][e] = el + e == c ? 1.f : 0.f;
+                    g[kk][e] = dpb[(el + e) * D + c];
+                }
+            }
+            for (int s = kC - 1; s >= 1; --s) fwd(s, all);
+            __syncwarp();
+            {
+                float w0[NE];
+                ldv<NE>(w0, Ws + el);
+                dot8<NE>(x, w0, wx);
+            }
+            back(0, false, all);
+            for (int s = 1; s < kC; ++s) back(s, true, all);
+            __syncwarp();
         }
-        for (int s = kC - 1; s >= 1; --s) fwd(s, all);
-        __syncwarp();
-        dot8(x, Ws[lane], wx);
-        back(0, false, all);
-        for (int s = 1; s < kC; ++s) back(s, true, all);
     }
-    __syncwarp();
 
     // ---- key rows j = base + k: k~_j = H_63 ... H_{j+1} k_j (the last block's k~ reach no
     // later query)
@@ -646,27 +533,31 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
 #pragma unroll
         for (int kk = 0; kk < kNS; ++kk) {
             const int j = base + kk;
-            const bool in = j < nvalid;
-            x[kk] = in ? Ks[j * 32 + lane] : make_float2(0.f, 0.f);
-            g[kk] = in ? *reinterpret_cast<const float2 *>(dkt + ((size_t)bh * Lp + t0 + j) * kD + 2 * lane)
-                       : make_float2(0.f, 0.f);
+            if (j < nvalid) {
+                ldv<NE>(x[kk], Ks + j * D + el);
+                ldv<NE>(g[kk], dkt + ((size_t)bh * Lp + t0 + j) * D + el);
+            } else {
+                zerov(x[kk]);
+                zerov(g[kk]);
+            }
         }
         for (int s = base + 1; s < kC; ++s) fwd(s, [&](int kk) { return s > base + kk; });
         __syncwarp();
         for (int s = kC - 1; s > base; --s) back(s, true, [&](int kk) { return s > base + kk; });
 #pragma unroll
         for (int kk = 0; kk < kNS; ++kk)
-            if (base + kk < nvalid) {
-                atomicAdd(&dKs[(base + kk) * 32 + lane].x, g[kk].x);
-                atomicAdd(&dKs[(base + kk) * 32 + lane].y, g[kk].y);
-            }
+            if (base + kk < nvalid)
+#pragma unroll
+                for (int e = 0; e < NE; ++e) atomicAdd(dKs + (base + kk) * D + el + e, g[kk][e]);
     }
     __syncthreads();
     for (int e = tid; e < nvalid * 32; e += kThreads) {
-        const int r = e / 32, l = e % 32;
-        const size_t gi = (hL + t0 + r) * kD + 2 * l;
-        *reinterpret_cast<float2 *>(dk + gi) = dKs[e];
-        *reinterpret_cast<float2 *>(dw + gi) = dWs[e];
+        const size_t gi = (hL + t0 + e / 32) * D + NE * (e % 32);
+        float a[NE];
+        ldv<NE>(a, dKs + NE * e);
+        stv<NE>(dk + gi, a);
+        ldv<NE>(a, dWs + NE * e);
+        stv<NE>(dw + gi, a);
     }
     if (tid < nvalid) dbeta[hL + t0 + tid] = dBs[tid];
 }
@@ -787,7 +678,25 @@ BwdLayout bwd_layout(int B, int H, int L, bool fox) {
 }
 
 size_t bwd_query_smem() { return (size_t)(5 * BUF + 4 * kC) * sizeof(float); }
-size_t bwd_block_smem() { return (size_t)(4 * kBlkTile + kWarps * kC * kNS + 2 * kC) * sizeof(float); }
+
+// The token-level block pass at head size D (64 or 128): dq, dk, dw (BH, L, D) and dbeta
+// (BH, L) fp32 from dqt, dkt (BH, Lp, D), dP (BH, nblk, D, D) and the diagonal dT
+// (BH, nblk, 64, 64).
+template <typename T>
+cudaError_t launch_bwd_block_sweep(const void *q, const void *k, const void *w, const float *beta,
+                                   const float *dqt, const float *dkt, const float *dP,
+                                   const float *dTd, float *dq, float *dk, float *dw,
+                                   float *dbeta, int BH, int L, int Lp, int nblk, int D,
+                                   cudaStream_t stream) {
+    auto kern = D == 128 ? bwd_block_kernel<T, 128> : bwd_block_kernel<T, 64>;
+    const size_t sm = (size_t)(4 * kC * D + kWarps * kC * kNS + 2 * kC) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(nblk, BH), kThreads, sm, stream>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta, dqt,
+        dkt, dP, dTd, dq, dk, dw, dbeta, L, Lp, nblk);
+    return cudaGetLastError();
+}
 
 // dq, dk, dv, dw (B*H, L, 64) and dbeta (B*H, L) fp32; with log_f (PaTH-FoX) also dlogf
 // (B*H, L) fp32. dv gathers by atomics from zero.
@@ -822,10 +731,8 @@ cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const v
                                          kp, dg, reinterpret_cast<uint32_t *>(base), stream)) != cudaSuccess)
         return e;
     auto kq = fox ? bwd_query_kernel<T, true> : bwd_query_kernel<T, false>;
-    const size_t s1 = bwd_query_smem(), s2 = bwd_block_smem();
-    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_block_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)s2)) != cudaSuccess)
+    const size_t s1 = bwd_query_smem();
+    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1)) != cudaSuccess)
         return e;
     const dim3 grid(y.nblk, y.BH);
     kq<<<grid, kThreads, s1, stream>>>(
@@ -833,10 +740,9 @@ cudaError_t launch_path_bwd(const void *q, const void *k, const void *v, const v
         qt, kp, dg, dqt, dkt, dPb, dTd, stash, dv, L, y.Lp, y.nblk, scale, scale * kLog2e, loc, cb,
         rs, cs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_block_kernel<T><<<grid, kThreads, s2, stream>>>(
-        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(w), beta,
-        dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, L, y.Lp, y.nblk);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_bwd_block_sweep<T>(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, y.BH,
+                                       L, y.Lp, y.nblk, kD, stream)) != cudaSuccess)
+        return e;
     if (fox) {
         bwd_fox_dlogf_kernel<<<y.BH, 32, 0, stream>>>(rs, cs, L, y.Lp, dlogf);
         e = cudaGetLastError();
@@ -868,5 +774,14 @@ cudaError_t launch_bwd_fox_dlogf(const float *rsum, const float *csum, int BH, i
 PATH_BWD_INST(float)
 PATH_BWD_INST(__nv_bfloat16)
 #undef PATH_BWD_INST
+template cudaError_t launch_bwd_block_sweep<float>(const void *, const void *, const void *,
+                                                   const float *, const float *, const float *,
+                                                   const float *, const float *, float *, float *,
+                                                   float *, float *, int, int, int, int, int,
+                                                   cudaStream_t);
+template cudaError_t launch_bwd_block_sweep<__nv_bfloat16>(
+    const void *, const void *, const void *, const float *, const float *, const float *,
+    const float *, const float *, float *, float *, float *, float *, int, int, int, int, int,
+    cudaStream_t);
 
 }  // namespace path

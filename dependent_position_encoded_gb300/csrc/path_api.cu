@@ -63,6 +63,13 @@ cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
 cudaError_t launch_scan_tc128(const void *v, void *out, float *lse, bool fox, int BH, int L,
                               float scale, void *ws, uint64_t limit_ns, cudaStream_t stream);
 size_t bwd_tc_ws_bytes(int B, int H, int L, bool fox);
+size_t bwd128_ws_bytes(int B, int H, int L, bool fox);
+template <typename T>
+cudaError_t launch_path_bwd128(const void *q, const void *k, const void *v, const void *w,
+                               const float *beta, const float *log_f, const void *o,
+                               const float *lse, const void *dout, int B, int H, int L,
+                               float scale, float *dq, float *dk, float *dv, float *dw,
+                               float *dbeta, float *dlogf, void *ws, cudaStream_t stream);
 cudaError_t launch_path_bwd_tc(const void *q, const void *k, const void *v, const void *w,
                                const float *beta, const float *log_f, const void *o,
                                const float *lse, const void *dout, int B, int H, int L,
@@ -105,7 +112,7 @@ path_status check_sizes(int B, int H, int L, int d, int dtype) {
     return PATH_OK;
 }
 
-// The forward (PaTH and PaTH-FoX) also takes d = 128 (fp32 CUDA-core kernels).
+// The forward and the backward (PaTH and PaTH-FoX) also take d = 128.
 path_status check_fwd_sizes(int B, int H, int L, int d, int dtype) {
     return check_sizes(B, H, L, d == 128 ? kD : d, dtype);
 }
@@ -203,7 +210,8 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
 }  // namespace
 
 namespace {
-size_t bwd_ws_bytes(int B, int H, int L, int dtype, bool fox) {
+size_t bwd_ws_bytes(int B, int H, int L, int d, int dtype, bool fox) {
+    if (d == 128) return bwd128_ws_bytes(B, H, L, fox);
     return dtype == PATH_BF16 ? bwd_tc_ws_bytes(B, H, L, fox) : bwd_layout(B, H, L, fox).total;
 }
 
@@ -212,7 +220,7 @@ path_status bwd_impl(const void *q, const void *k, const void *v, const void *w,
                      int B, int H, int L, int d, int dtype, float scale, float *dq, float *dk,
                      float *dv, float *dw, float *dbeta, float *dlog_f, bool fox, void *ws,
                      size_t ws_bytes, void *stream) {
-    path_status st = check_sizes(B, H, L, d, dtype);
+    path_status st = check_fwd_sizes(B, H, L, d, dtype);
     if (st != PATH_OK) return st;
     if (!std::isfinite(scale)) return PATH_ERR_ARG;
     if ((long long)B * H * L == 0) return PATH_OK;
@@ -222,10 +230,19 @@ path_status bwd_impl(const void *q, const void *k, const void *v, const void *w,
         if (!p) return PATH_ERR_NULL;
     for (const void *p : in)
         if (!aligned(p, 16)) return PATH_ERR_ALIGN;
-    if ((st = check_ws(ws, ws_bytes, bwd_ws_bytes(B, H, L, dtype, fox))) != PATH_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, bwd_ws_bytes(B, H, L, d, dtype, fox))) != PATH_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float *lf = fox ? log_f : nullptr;
     float *dlf = fox ? dlog_f : nullptr;
+    // d = 128: the fp32 CUDA-core kernels for both input types
+    if (d == 128)
+        return from_cuda(dtype == PATH_BF16
+                             ? launch_path_bwd128<__nv_bfloat16>(q, k, v, w, beta, lf, out, lse,
+                                                                 d_out, B, H, L, scale, dq, dk,
+                                                                 dv, dw, dbeta, dlf, ws, s)
+                             : launch_path_bwd128<float>(q, k, v, w, beta, lf, out, lse, d_out, B,
+                                                         H, L, scale, dq, dk, dv, dw, dbeta, dlf,
+                                                         ws, s));
     // bf16 inputs: tensor-core query pass; fp32 inputs: the fp32 CUDA-core kernels, whose
     // accuracy the fp32 bar needs
     cudaError_t e = dtype == PATH_BF16
@@ -249,8 +266,8 @@ size_t path_workspace_bytes(int op, int B, int H, int L, int d, int dtype) {
         default: break;
     }
     if (op == PATH_OP_BWD || op == PATH_OP_FOX_BWD) {
-        if (check_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
-        return bwd_ws_bytes(B, H, L, dtype, op == PATH_OP_FOX_BWD);
+        if (check_fwd_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
+        return bwd_ws_bytes(B, H, L, d, dtype, op == PATH_OP_FOX_BWD);
     }
     if (check_decode_sizes(B, H, L, d, dtype) != PATH_OK) return 0;
     switch (op) {

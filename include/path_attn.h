@@ -141,12 +141,16 @@ path_status path_fwd_prepare(const void *q, const void *k, const void *w, const 
  *   out        : (B, H, L, d) dtype     lse  : (B, H, L) fp32    (the forward's outputs)
  *   d_out      : (B, H, L, d) dtype, the gradient of the loss with respect to out
  *   dq, dk, dv, dw : (B, H, L, d) fp32 outputs;  dbeta : (B, H, L) fp32 output
+ *   d          : 64 or 128 (other head sizes return PATH_ERR_SHAPE)
  *   scale      : the forward's softmax scale (finite)
  *   ws         : ws_bytes >= path_workspace_bytes(PATH_OP_BWD, B, H, L, d, dtype), which
- *                grows as B H (L / 64)^2 x 32 KB (the query pass keeps every carried
- *                query block and its logit gradient, e.g. 1.0 GB at B H = 64, L = 2048)
- * Every product runs in fp32 whatever dtype is (bf16 inputs are widened on load); w is
- * used as given (no renormalisation). Gradients of several query blocks meet in dv and in
+ *                grows as B H (L / 64)^2 (the query pass keeps every carried query block
+ *                and its logit gradient: about 32 KB per block pair for fp32 inputs at
+ *                d = 64, e.g. 1.0 GB at B H = 64, L = 2048, and 48 KB at d = 128)
+ * Gradients are fp32 whatever dtype is (bf16 inputs are widened on load). At d = 64, bf16
+ * inputs take bf16 tensor-core products with fp32 accumulation in the query pass and tf32
+ * products in the block pass; fp32 inputs, and every input at d = 128, take fp32 products
+ * throughout. w is used as given (no renormalisation). Gradients of several query blocks meet in dv and in
  * internal per-block sums through fp32 atomic adds, so their rounding order (not their
  * value beyond fp32 rounding) varies between runs. Outputs are written from zero: no
  * accumulation into the caller's buffers.

@@ -256,3 +256,88 @@ def test_bwd_bf16_deterministic_up_to_atomics(lib):
     for n in NAMES:
         a, b = g1[n].double(), g2[n].double()
         assert (a - b).abs().max().item() <= 1e-4 * max(b.abs().max().item(), 1e-6), n
+
+
+# ---------------------------------------------------------------- head size 128 (fp32 kernels)
+
+def _case128(lib, B, H, L, dtype, seed, fox=False, gate_scale=1.0, mutate=None, x=None):
+    if x is None:
+        x = pi.make_fwd_inputs(B, H, L, d=128, seed=seed, dtype=dtype, fox=fox, device="cuda")
+    if fox:
+        x["log_f"] = (x["log_f"] * gate_scale).contiguous()
+    if mutate is not None:
+        mutate(x)
+    g = torch.Generator(device="cpu").manual_seed(seed + 1)
+    d_out = torch.randn((B, H, L, 128), generator=g).to(dtype).cuda()
+    if fox:
+        out, lse = lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
+        grads = lib.path_fox_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], out,
+                                 lse, d_out)
+    else:
+        out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
+        grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out)
+    torch.cuda.synchronize()
+    assert grads["dq"].shape == (B, H, L, 128)
+    return x, d_out, grads
+
+
+@pytest.mark.parametrize("B,H,L,dtype", [
+    (1, 2, 128, torch.float32),    # two blocks
+    (1, 2, 200, torch.float32),    # ragged last block
+    (1, 1, 1, torch.float32),      # one token
+    (1, 1, 64, torch.float32),     # one block: no inter-block term
+    (1, 1, 320, torch.float32),    # five blocks: interior 128 x 128 P_b gradients
+    (2, 2, 130, torch.bfloat16),   # bf16, ragged, three blocks
+    (1, 2, 384, torch.bfloat16),   # bf16, six blocks
+])
+def test_bwd_d128_matches_oracle(lib, B, H, L, dtype):
+    x, d_out, grads = _case128(lib, B, H, L, dtype, seed=3000 + 10 * B + L)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, TOL[dtype])
+
+
+@pytest.mark.parametrize("B,H,L,dtype,gate_scale", [
+    (1, 2, 200, torch.float32, 1.0),   # workload gate, ragged
+    (1, 1, 1, torch.float32, 1.0),     # one token
+    (1, 1, 384, torch.float32, 20.0),  # strong gate: the forward's early exit skips blocks
+    (2, 2, 130, torch.bfloat16, 1.0),  # bf16
+    (1, 2, 320, torch.bfloat16, 5.0),  # bf16, moderate gate
+])
+def test_fox_bwd_d128_matches_oracle(lib, B, H, L, dtype, gate_scale):
+    x, d_out, grads = _case128(lib, B, H, L, dtype, seed=3100 + 7 * L + B, fox=True,
+                               gate_scale=gate_scale)
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, log_f=x["log_f"])
+    _compare(grads, ref, TOL[dtype])
+
+
+@pytest.mark.parametrize("kind", ["projection", "reflection", "identity"])
+def test_bwd_d128_degenerate_transitions(lib, kind):
+    # beta = 1 (singular projections), beta = 2 (reflections), w = 0 (H = I), at d = 128
+    def mutate(x):
+        if kind == "projection":
+            x["beta"] = torch.ones_like(x["beta"])
+        elif kind == "reflection":
+            x["beta"] = torch.full_like(x["beta"], 2.0)
+        else:
+            x["w"] = torch.zeros_like(x["w"])
+    x0 = pi.make_fwd_inputs(1, 2, 200, d=128, seed=3200, dtype=torch.float32, clip=0.0,
+                            device="cuda")
+    x, d_out, grads = _case128(lib, 1, 2, 200, torch.float32, seed=3200, mutate=mutate, x=x0)
+    if kind == "identity":
+        assert torch.count_nonzero(grads["dw"]) == 0 and torch.count_nonzero(grads["dbeta"]) == 0
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
+    _compare(grads, ref, 1e-4)
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_bwd_d128_workload_sampled_heads(lib, fox):
+    # B4 H8 L2048 bf16 at head size 128 (32 blocks per head, 496 carried pairs): the oracle
+    # on two heads
+    B, H, L = 4, 8, 2048
+    x, d_out, grads = _case128(lib, B, H, L, torch.bfloat16, seed=3300, fox=fox)
+    heads = [1, B * H - 1]
+    names = ("q", "k", "v", "w", "beta") + (("log_f",) if fox else ())
+    sel = {k: x[k].reshape(-1, *x[k].shape[2:])[heads] for k in names}
+    ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          d_out.reshape(-1, L, 128)[heads], log_f=sel.get("log_f"))
+    _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
