@@ -373,15 +373,15 @@ def time_producer(pa, wl, steps=5, warmup=3):
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
-def bwd_flops(B, H, L):
-    """Algorithmic FLOPs of the backward's query pass (the 64 x 64 x 64 products it forms, each
-    2 * 64^3): per pair of query block a and key block b < a, the logits, dout V_b^T, the
-    dk~ and dv terms and dT K~_b (5 products), plus X P_b^T, G P_b and the dP_b term when
-    b > 0 (3 more); per diagonal block dout V^T and p^T dout."""
+def bwd_flops(B, H, L, d=64):
+    """Algorithmic FLOPs of the backward's query pass: per pair of query block a and key block
+    b < a, the logits, dout V_b^T, the dk~ and dv terms and dT K~_b (5 products of
+    2 * 64^2 * d each), plus X P_b^T, G P_b and the dP_b term when b > 0 (3 products of
+    2 * 64 * d^2); per diagonal block dout V^T and p^T dout (2 * 64^2 * d each)."""
     nb = (L + 63) // 64
     pairs = nb * (nb - 1) // 2
-    t = 2 * 64 ** 3
-    return B * H * t * (5 * pairs + 3 * (pairs - (nb - 1)) + 2 * nb)
+    t, u = 2 * 64 * 64 * d, 2 * 64 * d * d
+    return B * H * (5 * t * pairs + 3 * u * (pairs - (nb - 1)) + 2 * t * nb)
 
 
 def time_bwd(pa, wl, steps=5, warmup=3, fox=False):
@@ -390,14 +390,14 @@ def time_bwd(pa, wl, steps=5, warmup=3, fox=False):
     dev = torch.device("cuda")
     x = pi.make_fwd_inputs(wl.B, wl.H, wl.L, wl.d, wl.dtype, wl.seed, wl.clip, fox, dev)
     g = torch.Generator(device=dev).manual_seed(wl.seed + 1)
-    d_out = torch.randn((wl.B, wl.H, wl.L, 64), generator=g, device=dev).to(wl.dtype)
+    d_out = torch.randn((wl.B, wl.H, wl.L, wl.d), generator=g, device=dev).to(wl.dtype)
     if fox:
         out, lse = pa.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"])
     else:
         out, lse = pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
     ws = pa.new_workspace(pa.OP_FOX_BWD if fox else pa.OP_BWD, wl.B, wl.H, wl.L,
-                          pa.BF16 if wl.dtype == torch.bfloat16 else pa.F32, dev)
-    grads = {n: torch.empty((wl.B, wl.H, wl.L, 64), dtype=torch.float32, device=dev)
+                          pa.BF16 if wl.dtype == torch.bfloat16 else pa.F32, dev, d=wl.d)
+    grads = {n: torch.empty((wl.B, wl.H, wl.L, wl.d), dtype=torch.float32, device=dev)
              for n in ("dq", "dk", "dv", "dw")}
     grads["dbeta"] = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device=dev)
     grads["dlog_f"] = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device=dev)
@@ -421,13 +421,14 @@ def time_bwd(pa, wl, steps=5, warmup=3, fox=False):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    fl = bwd_flops(wl.B, wl.H, wl.L)
+    fl = bwd_flops(wl.B, wl.H, wl.L, wl.d)
     name = wl.name.replace("path_fwd", "path_fox_bwd" if fox else "path_bwd")
     return {"workload": name, "ms_per_step": ms,
             "tokens_per_s": wl.B * wl.L / (ms * 1e-3), "query_pass_flops": fl,
             "workspace_bytes": ws.numel(),
-            # fp32 UT recompute, query pass, block pass; FoX adds the gate sums and d log f
-            "launches_per_step": 5 if fox else 3}
+            # UT preparation, query pass, block pass; FoX adds the gate sums and d log f (and,
+            # at d = 128, the preparation's exit-bound pass)
+            "launches_per_step": (6 if wl.d == 128 else 5) if fox else 3}
 
 
 def cpu_baseline(x_cpu, wl, target_s=12.0):
@@ -580,6 +581,18 @@ def run_legs(pa, peaks, dev, rank):
         bwd["roofline"] = BWD_ROOFLINE(ach, peaks, fox, ex)
         legs["fox_bwd" if fox else "bwd"] = bwd
         torch.cuda.empty_cache()
+    # the backward at head size 128 on the same model width (bf16: warp-level tensor-core query
+    # pass, token-level block pass)
+    bwd = time_bwd(pa, pi.BF16_L2048_D128)
+    ach = bwd["query_pass_flops"] / (bwd["ms_per_step"] * 1e-3) / 1e12
+    bwd["roofline"] = {"kernels": "query-pass algorithmic FLOPs over the whole backward call "
+                                  "(bwd_query128_mma_kernel: mma.sync bf16)",
+                       "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                       "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                       "traffic": ncu_traffic("bwd_query128_mma_kernel"),
+                       "peak_source": "%s bf16 dense (burst)" % peaks["source"]}
+    legs["bwd_d128"] = bwd
+    torch.cuda.empty_cache()
     # head size 128 at the speed workload's tokens and model width (B32, 16 heads of 128 =
     # 32 heads of 64), and on the bf16 check workload's width in 8 heads (B4 H8 L2048)
     for key, (B_, H_, L_) in (("", (32, 16, 4096)), ("small_", (4, 8, 2048))):
@@ -722,6 +735,7 @@ PROFILE_CASES = {
     # the backward legs' own workload (1.3 GB of workspace, stash larger than L2)
     "bwd": pi.BF16_L2048,
     "fox_bwd": pi.BF16_L2048,
+    "bwd_d128": pi.BF16_L2048_D128,
     # a quarter of the head-size-128 forward leg's workload (B8 of B32, H16 L4096 d128)
     "fwd_d128": pi.FwdWorkload("path_fwd_bf16_B8H16L4096_d128", 8, 16, 4096, 128, torch.bfloat16, 12,
                                pi.BETA_CLIP, False),
@@ -751,7 +765,7 @@ def run_profile_case(args):
     elif args.profile == "producer":
         r = time_producer(pa, wl, steps=args.steps, warmup=args.warmup)
         print(json.dumps(r))
-    elif args.profile in ("bwd", "fox_bwd"):
+    elif args.profile in ("bwd", "fox_bwd", "bwd_d128"):
         r = time_bwd(pa, wl, steps=args.steps, warmup=args.warmup, fox=args.profile == "fox_bwd")
         print(json.dumps(r))
     elif args.profile == "fox_decode":
@@ -861,7 +875,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip FoX, decode and e2e legs")
     ap.add_argument("--no-sweep", action="store_true", help="skip the L sweep")
     ap.add_argument("--profile", choices=["fwd", "fox", "decode", "fox_decode", "producer", "bwd", "fwd_d128",
-                                          "decode_d128", "fox_bwd", "fwd_f32"],
+                                          "decode_d128", "fox_bwd", "bwd_d128", "fwd_f32"],
                     help="run only that operation on a reduced case (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:

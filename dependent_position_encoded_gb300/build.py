@@ -19,7 +19,7 @@ LIB = os.path.join(OUT_DIR, "libpath_attn.so")
 
 SOURCES = ["path_api.cu", "ut_prepare.cu", "ut_prepare_tc.cu", "pair_combine.cu",
            "fox_exit.cu", "scan_tc.cu", "scan_tc_fox.cu", "scan_tc128.cu", "scan_f32.cu", "decode.cu", "producer.cu", "backward.cu", "backward_tc.cu",
-           "backward_block_mm.cu", "backward_d128.cu",
+           "backward_block_mm.cu", "backward_d128.cu", "backward_tc128.cu",
            "fwd_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -303,6 +303,37 @@ __device__ __forceinline__ void loadv(float (&r)[NE], const T *p) {
 #pragma unroll
     for (int e = 0; e < NE; ++e) r[e] = Elt<T>::to_f(p[e]);
 }
+// NE consecutive values of type T in shared memory as fp32 (one 8- or 16-byte load for
+// fp32, 4 or 8 bytes for bf16)
+template <int NE>
+__device__ __forceinline__ void ldsv(float (&r)[NE], const float *p) { ldv<NE>(r, p); }
+template <int NE>
+__device__ __forceinline__ void ldsv(float (&r)[NE], const __nv_bfloat16 *p) {
+    if constexpr (NE == 2) {
+        const float2 t = unpack_bf16x2(*reinterpret_cast<const uint32_t *>(p));
+        r[0] = t.x;
+        r[1] = t.y;
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        const float2 t0 = unpack_bf16x2(u.x), t1 = unpack_bf16x2(u.y);
+        r[0] = t0.x;
+        r[1] = t0.y;
+        r[2] = t1.x;
+        r[3] = t1.y;
+    }
+}
+// NE consecutive values of type T copied from global to shared memory, or zeros
+template <typename T, int NE>
+__device__ __forceinline__ void copyv(T *dst, const T *src, bool in) {
+    if constexpr (sizeof(T) * NE == 8) {
+        *reinterpret_cast<uint2 *>(dst) = in ? *reinterpret_cast<const uint2 *>(src) : make_uint2(0u, 0u);
+    } else if constexpr (sizeof(T) * NE == 16) {
+        *reinterpret_cast<uint4 *>(dst) = in ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        static_assert(sizeof(T) * NE == 4, "4, 8 or 16 bytes per lane");
+        *reinterpret_cast<uint32_t *>(dst) = in ? *reinterpret_cast<const uint32_t *>(src) : 0u;
+    }
+}
 template <int NE>
 __device__ __forceinline__ void zerov(float (&r)[NE]) {
 #pragma unroll
@@ -342,8 +373,10 @@ __device__ __forceinline__ void dot8(const float (&x)[kNS][NE], const float (&w)
 }
 
 // Workspace inputs (fp32): dqt, dkt (BH, Lp, D), dP (BH, nblk, D, D), dTd (BH, nblk, 64, 64).
+// w and k stay in shared memory in their input type (exact), so that at d = 128 bf16 inputs
+// fit two CTAs per SM.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, (D == 64 || sizeof(T) == 2) ? 2 : 1)
 bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
                  const float *__restrict__ beta, const float *__restrict__ dqt,
                  const float *__restrict__ dkt, const float *__restrict__ dP,
@@ -352,13 +385,13 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     constexpr int NE = D / 32;
     constexpr int kTile = kC * D;  // floats in one 64 x D tile
     extern __shared__ __align__(16) float sm[];
-    float *Ws = sm;               // w_s, [s][dimension]
-    float *Ks = Ws + kTile;       // k_j
-    float *dWs = Ks + kTile;      // gradient of w_s
+    float *dWs = sm;              // gradient of w_s, [s][dimension]
     float *dKs = dWs + kTile;     // gradient of k_j
     float *wxs = dKs + kTile;     // per warp: [s][sweep] w_s . x
     float *bs = wxs + kWarps * kC * kNS;  // beta_s
     float *dBs = bs + kC;                 // gradient of beta_s
+    T *Ws = reinterpret_cast<T *>(dBs + kC);  // w_s (input type)
+    T *Ks = Ws + kTile;                       // k_j
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int blk = blockIdx.x, bh = blockIdx.y;
@@ -371,17 +404,10 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     for (int e = tid; e < kTile / NE; e += kThreads) {
         const int r = e / 32;
         const size_t g = (hL + t0 + r) * D + NE * (e % 32);
-        float wv[NE], kv[NE], z[NE];
+        float z[NE];
         zerov(z);
-        if (r < nvalid) {
-            loadv<T, NE>(wv, w + g);
-            loadv<T, NE>(kv, k + g);
-        } else {
-            zerov(wv);
-            zerov(kv);
-        }
-        stv<NE>(Ws + NE * e, wv);
-        stv<NE>(Ks + NE * e, kv);
+        copyv<T, NE>(Ws + NE * e, w + g, r < nvalid);
+        copyv<T, NE>(Ks + NE * e, k + g, r < nvalid);
         stv<NE>(dWs + NE * e, z);
         stv<NE>(dKs + NE * e, z);
     }
@@ -399,7 +425,7 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     // x[k] <- H_s x[k] for the sweeps with act(k), recording w_s . x[k] at wxw[s][k]
     auto fwd = [&](int s, auto act) {
         float ws[NE];
-        ldv<NE>(ws, Ws + s * D + el);
+        ldsv<NE>(ws, Ws + s * D + el);
         const float be = bs[s];
         dot8<NE>(x, ws, wx);
         if (lane == 0) {
@@ -417,7 +443,7 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
     // is already in x (the first step back, through H_0, with w_0 . x given in wx).
     auto back = [&](int s, bool undo, auto act) {
         float ws[NE];
-        ldv<NE>(ws, Ws + s * D + el);
+        ldsv<NE>(ws, Ws + s * D + el);
         const float be = bs[s];
         if (undo) {
             const float4 a = *reinterpret_cast<const float4 *>(wxw + s * kNS);
@@ -470,13 +496,13 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         __syncwarp();
         {
             float w0[NE];
-            ldv<NE>(w0, Ws + el);
+            ldsv<NE>(w0, Ws + el);
             dot8<NE>(x, w0, wx);  // w_0 . x_0
         }
         back(0, false, all);
         for (int j = 0; j < base + kNS; ++j) {
             float kj[NE], dka[NE];  // x[k] = x_j here
-            ldv<NE>(kj, Ks + j * D + el);
+            ldsv<NE>(kj, Ks + j * D + el);
             zerov(dka);
 #pragma unroll
             for (int kk = 0; kk < kNS; ++kk)
@@ -518,7 +544,7 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
             __syncwarp();
             {
                 float w0[NE];
-                ldv<NE>(w0, Ws + el);
+                ldsv<NE>(w0, Ws + el);
                 dot8<NE>(x, w0, wx);
             }
             back(0, false, all);
@@ -534,7 +560,7 @@ bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
         for (int kk = 0; kk < kNS; ++kk) {
             const int j = base + kk;
             if (j < nvalid) {
-                ldv<NE>(x[kk], Ks + j * D + el);
+                ldsv<NE>(x[kk], Ks + j * D + el);
                 ldv<NE>(g[kk], dkt + ((size_t)bh * Lp + t0 + j) * D + el);
             } else {
                 zerov(x[kk]);
@@ -689,7 +715,8 @@ cudaError_t launch_bwd_block_sweep(const void *q, const void *k, const void *w, 
                                    float *dbeta, int BH, int L, int Lp, int nblk, int D,
                                    cudaStream_t stream) {
     auto kern = D == 128 ? bwd_block_kernel<T, 128> : bwd_block_kernel<T, 64>;
-    const size_t sm = (size_t)(4 * kC * D + kWarps * kC * kNS + 2 * kC) * sizeof(float);
+    const size_t sm = (size_t)(2 * kC * D + kWarps * kC * kNS + 2 * kC) * sizeof(float) +
+                      (size_t)2 * kC * D * sizeof(T);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     kern<<<dim3(nblk, BH), kThreads, sm, stream>>>(

@@ -1,5 +1,6 @@
-// Backward pass of PaTH attention and PaTH-FoX at head size d = 128, fp32 on the CUDA cores
-// for both input types (bf16 inputs are widened on load; every product is fp32).
+// Backward pass of PaTH attention and PaTH-FoX at head size d = 128 for fp32 inputs, fp32 on
+// the CUDA cores (the fp32 bar needs fp32 products; bf16 inputs take the tensor-core query
+// pass of backward_tc128.cu).
 //
 // The pages give no backward (review "거리에서 경로로, PaTH Attention" §9 and technical
 // summary "技術要約: PaTH Attention" §3 say the block-wise algorithm makes training
@@ -409,7 +410,6 @@ cudaError_t launch_path_bwd128(const void *q, const void *k, const void *v, cons
                                                int, int, float, float *, float *, float *,       \
                                                float *, float *, float *, void *, cudaStream_t);
 PATH_BWD128_INST(float)
-PATH_BWD128_INST(__nv_bfloat16)
 #undef PATH_BWD128_INST
 
 }  // namespace path

@@ -791,9 +791,5 @@ cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int
                                              float, void *, cudaStream_t);
 PATH_D128_INST(float)
 #undef PATH_D128_INST
-// the backward at d = 128 widens bf16 inputs in this preparation too
-template cudaError_t launch_prep_d128<__nv_bfloat16>(const void *, const void *, const void *,
-                                                     const float *, const float *, int, int, int,
-                                                     float, void *, cudaStream_t);
 
 }  // namespace path

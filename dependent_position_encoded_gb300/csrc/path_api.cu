@@ -64,6 +64,13 @@ cudaError_t launch_scan_tc128(const void *v, void *out, float *lse, bool fox, in
                               float scale, void *ws, uint64_t limit_ns, cudaStream_t stream);
 size_t bwd_tc_ws_bytes(int B, int H, int L, bool fox);
 size_t bwd128_ws_bytes(int B, int H, int L, bool fox);
+size_t bwd_tc128_ws_bytes(int B, int H, int L, bool fox);
+cudaError_t launch_path_bwd128_tc(const void *q, const void *k, const void *v, const void *w,
+                                  const float *beta, const float *log_f, const void *o,
+                                  const float *lse, const void *dout, int B, int H, int L,
+                                  float scale, float *dq, float *dk, float *dv, float *dw,
+                                  float *dbeta, float *dlogf, void *ws, uint64_t limit_ns,
+                                  cudaStream_t stream);
 template <typename T>
 cudaError_t launch_path_bwd128(const void *q, const void *k, const void *v, const void *w,
                                const float *beta, const float *log_f, const void *o,
@@ -211,7 +218,8 @@ path_status scan_impl(const void *v, void *out, float *lse, bool fox, int B, int
 
 namespace {
 size_t bwd_ws_bytes(int B, int H, int L, int d, int dtype, bool fox) {
-    if (d == 128) return bwd128_ws_bytes(B, H, L, fox);
+    if (d == 128)
+        return dtype == PATH_BF16 ? bwd_tc128_ws_bytes(B, H, L, fox) : bwd128_ws_bytes(B, H, L, fox);
     return dtype == PATH_BF16 ? bwd_tc_ws_bytes(B, H, L, fox) : bwd_layout(B, H, L, fox).total;
 }
 
@@ -234,12 +242,13 @@ path_status bwd_impl(const void *q, const void *k, const void *v, const void *w,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float *lf = fox ? log_f : nullptr;
     float *dlf = fox ? dlog_f : nullptr;
-    // d = 128: the fp32 CUDA-core kernels for both input types
+    // d = 128: bf16 inputs take the warp-level tensor-core query pass, fp32 inputs the fp32
+    // CUDA-core kernels
     if (d == 128)
         return from_cuda(dtype == PATH_BF16
-                             ? launch_path_bwd128<__nv_bfloat16>(q, k, v, w, beta, lf, out, lse,
-                                                                 d_out, B, H, L, scale, dq, dk,
-                                                                 dv, dw, dbeta, dlf, ws, s)
+                             ? launch_path_bwd128_tc(q, k, v, w, beta, lf, out, lse, d_out, B, H, L,
+                                                     scale, dq, dk, dv, dw, dbeta, dlf, ws,
+                                                     kWaitLimitNs, s)
                              : launch_path_bwd128<float>(q, k, v, w, beta, lf, out, lse, d_out, B,
                                                          H, L, scale, dq, dk, dv, dw, dbeta, dlf,
                                                          ws, s));

@@ -58,6 +58,8 @@ class DecodeWorkload:
 # PaTH-FoX at long context, and 64 decode steps over a 32K-token cache.
 TINY_FP32 = FwdWorkload("path_fwd_tiny_fp32_B1H2L128", 1, 2, 128, D, torch.float32, 0, 0.0, False)
 BF16_L2048 = FwdWorkload("path_fwd_bf16_B4H16L2048", 4, 16, 2048, D, torch.bfloat16, 2, BETA_CLIP, False)
+# the same model width (1024) in eight heads of 128
+BF16_L2048_D128 = FwdWorkload("path_fwd_bf16_B4H8L2048_d128", 4, 8, 2048, 128, torch.bfloat16, 2, BETA_CLIP, False)
 BF16_L4096 = FwdWorkload("path_fwd_bf16_B32H32L4096", 32, 32, 4096, D, torch.bfloat16, 3, BETA_CLIP, False)
 FOX_L16384 = FwdWorkload("path_fox_fwd_bf16_B8H16L16384", 8, 16, 16384, D, torch.bfloat16, 4, BETA_CLIP, True)
 DECODE_32K = DecodeWorkload("path_decode_bf16_B32H32N32768x64", 32, 32, 32768, 64, D, torch.bfloat16, 5, 1000)

@@ -112,19 +112,20 @@ def test_bwd_workspace_size(lib):
 
 
 def test_bwd_d128_workspace_size(lib):
-    # head size 128, either input type: the fp32 d = 128 forward's preparation workspace,
-    # then fp32 dq~, dk~ (Lp x 128), dP_b (nblk x 128 x 128), diagonal dT (nblk x 64 x 64)
-    # and per pair b < a the carried query block (64 x 128) and its logit gradient (64 x 64);
+    # head size 128: the d = 128 forward's preparation workspace (fp32 for fp32 inputs, the
+    # bf16 tensor-core one for bf16 inputs), then fp32 dq~, dk~ (Lp x 128), dP_b
+    # (nblk x 128 x 128), diagonal dT (nblk x 64 x 64) and per pair b < a the carried query
+    # block (64 x 128) and its logit gradient (64 x 64), fp32 or bf16 like the inputs;
     # PaTH-FoX adds the gate sums as at d = 64
     L, nb = 130, 3
     rows = nb * 64 * 128 * 4
-    tail = 2 * rows + nb * 128 * 128 * 4 + nb * 64 * 64 * 4 + 3 * (64 * 128 + 64 * 64) * 4
     tok = nb * 64 * 4
     extra = 3 * tok + (nb * 8 + 255) // 256 * 256
-    for dt in (lib.F32, lib.BF16):
-        fwd = lib.path_workspace_bytes(lib.OP_FWD, 1, 1, L, 128, lib.F32)
+    for dt, elt in ((lib.F32, 4), (lib.BF16, 2)):
+        tail = 2 * rows + nb * 128 * 128 * 4 + nb * 64 * 64 * 4 + 3 * (64 * 128 + 64 * 64) * elt
+        fwd = lib.path_workspace_bytes(lib.OP_FWD, 1, 1, L, 128, dt)
         assert lib.path_workspace_bytes(lib.OP_BWD, 1, 1, L, 128, dt) == fwd + tail
-        fwd_fox = lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, L, 128, lib.F32)
+        fwd_fox = lib.path_workspace_bytes(lib.OP_FOX_FWD, 1, 1, L, 128, dt)
         assert lib.path_workspace_bytes(lib.OP_FOX_BWD, 1, 1, L, 128, dt) == \
             fwd_fox + tail + extra
 

@@ -179,7 +179,8 @@ def _bwd(so, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(lse=None), 1), (dict(d_out=None), 1), (dict(dbeta=None), 1),
-    (dict(ws=None), 1), (dict(d=128), 2), (dict(L=-1), 2), (dict(dtype=2), 3),
+    (dict(ws=None), 1), (dict(d=96), 2), (dict(L=-1), 2), (dict(dtype=2), 3),
+    (dict(d=128), 5),  # head size 128 accepted, workspace too small
     (dict(dw=FAKE + 4), 4), (dict(out=FAKE + 8), 4), (dict(ws=FAKE + 16), 4),
     (dict(scale=float("nan")), 9), (dict(), 5),
 ])
@@ -211,6 +212,13 @@ def _fox_bwd(so, **kw):
 ])
 def test_fox_bwd_rejects_bad_arguments_before_launch(so, kw, code):
     assert _fox_bwd(so, **kw) == code
+
+
+def test_bwd_head_size_128_checks(so):
+    # d = 128 passes the size checks of both backwards (the workspace check then stops them)
+    assert _bwd(so, d=128, ws_bytes=1000) == 5
+    assert _fox_bwd(so, d=128, ws_bytes=1000) == 5
+    assert _fox_bwd(so, d=96) == 2
 
 
 def test_fwd_head_size_128_checks(so):
