@@ -47,9 +47,19 @@ constexpr int kThr = 256;
 constexpr int kD2 = 128;                   // head size of this file
 constexpr int SLD = 72;                    // bf16 elements per shared tile row (64 + 8 pad)
 constexpr uint32_t kTile = 64 * SLD * 2;   // bytes of one 64 x 64 bf16 tile
-// tile slots; pass 2 keeps G's bf16 head and tail in the slots of dout and V
-enum : int { X0, X1, D0, D1, K0, K1, P00, P01, P10, P11, V0, V1, PT, DT, kNumTiles };
-constexpr int G0H = D0, G1H = D1, G0L = V0, G1L = V1;
+// Tile slots. Pass 1: X0 X1 (carried rows), D0 D1 (dout), PT DT (p and dT), and two sets of
+// the key block's operands (K0 K1, the P_b quadrants P00 P01 P10 P11, V0 V1), so that the
+// next block's loads overlap the current block's MMAs. Pass 2: two sets of the stash's X_b
+// (two tiles) and dT_b and the key block's K~_b and P_b; G's bf16 head and tail take D0, D1
+// and the V tiles of set 1.
+enum : int { X0, X1, D0, D1, PT, DT, SET0, kNumTiles = SET0 + 16 };
+enum : int { K0, K1, P00, P01, P10, P11, V0, V1 };  // offsets within a pass-1 set
+__host__ __device__ constexpr int s1(int set, int t) { return SET0 + 8 * set + t; }
+// pass 2, set 0: X = slots X0, X1, dT = DT, K~_b and P_b = the first six tiles of pass-1 set 0;
+// set 1: X = the V tiles of pass-1 set 0, dT = PT, K~_b and P_b = the first six of set 1
+__host__ __device__ constexpr int s2x(int set, int h) { return set ? s1(0, V0 + h) : X0 + h; }
+__host__ __device__ constexpr int s2dt(int set) { return set ? PT : DT; }
+constexpr int G0H = D0, G1H = D1, G0L = s1(1, V0), G1L = s1(1, V1);
 constexpr uint32_t kRowsOff = kNumTiles * kTile;  // lse2, Drow, loci, locj: 64 fp32 each
 constexpr uint32_t kSmem = kRowsOff + 4 * 64 * 4;
 constexpr size_t kKpRows = (size_t)(64 + kD2) * kD2;   // [k~ (64 rows); P_b (128 rows)]
@@ -116,7 +126,7 @@ __device__ __forceinline__ void wmma64(Acc &acc, uint32_t a, uint32_t b, int wm,
 }
 
 // 64 rows x 64 bf16 from global (row stride ld elements; rows >= nrows read as zero) into a
-// tile, asynchronously (16-byte copies, waited for by cp_wait_all)
+// tile, asynchronously (16-byte copies; the caller commits them as a group)
 __device__ __forceinline__ void cp_tile(uint32_t dst, const __nv_bfloat16 *src, int ld, int nrows) {
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
@@ -128,8 +138,11 @@ __device__ __forceinline__ void cp_tile(uint32_t dst, const __nv_bfloat16 *src, 
                      : "memory");
     }
 }
-__device__ __forceinline__ void cp_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits until at most N of this thread's committed copy groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // two bf16 at (r, c), (r, c + 1) of a tile
@@ -228,22 +241,59 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
     }
     float rs[2] = {0.f, 0.f};  // FoX: row sums of dS (rows 16 wm + g, + 8; this warp's columns)
 
+    // pass 1's operands of key block b into set `set`: K~_b, the P_b quadrants, V_b
+    auto stage1 = [&](int set, int b) {
+        const __nv_bfloat16 *kb = kp + ((size_t)bh * nblk_p + b) * kKpRows;
+        cp_tile(tile(s1(set, K0)), kb, kD2, 64);
+        cp_tile(tile(s1(set, K1)), kb + 64, kD2, 64);
+        cp_tile(tile(s1(set, P00)), kb + 64 * kD2, kD2, 64);
+        cp_tile(tile(s1(set, P01)), kb + 64 * kD2 + 64, kD2, 64);
+        cp_tile(tile(s1(set, P10)), kb + 128 * kD2, kD2, 64);
+        cp_tile(tile(s1(set, P11)), kb + 128 * kD2 + 64, kD2, 64);
+        cp_tile(tile(s1(set, V0)), vh + (size_t)b * 64 * kD2, kD2, 64);
+        cp_tile(tile(s1(set, V1)), vh + (size_t)b * 64 * kD2 + 64, kD2, 64);
+        cp_commit();
+    };
+    const size_t pair0 = (size_t)bh * ((size_t)nb * (nb - 1) / 2) + (size_t)a * (a - 1) / 2;
+    // pass 2's operands of key block b into set `set`: the stashed X_{a,b} and dT_ab, K~_b, P_b
+    auto stage2 = [&](int set, int b) {
+        const __nv_bfloat16 *st = stash + (pair0 + b) * kStash;
+        const __nv_bfloat16 *kb = kp + ((size_t)bh * nblk_p + b) * kKpRows;
+        cp_tile(tile(s2x(set, 0)), st, kD2, 64);
+        cp_tile(tile(s2x(set, 1)), st + 64, kD2, 64);
+        cp_tile(tile(s2dt(set)), st + 64 * kD2, 64, 64);
+        cp_tile(tile(s1(set, K0)), kb, kD2, 64);
+        cp_tile(tile(s1(set, K1)), kb + 64, kD2, 64);
+        cp_tile(tile(s1(set, P00)), kb + 64 * kD2, kD2, 64);
+        cp_tile(tile(s1(set, P01)), kb + 64 * kD2 + 64, kD2, 64);
+        cp_tile(tile(s1(set, P10)), kb + 128 * kD2, kD2, 64);
+        cp_tile(tile(s1(set, P11)), kb + 128 * kD2 + 64, kD2, 64);
+        cp_commit();
+    };
+
+    // the diagonal block's dout, V (into set 1) and Q~_a; then key block a - 1 into set 0
     const __nv_bfloat16 *qa = qt + ((size_t)bh * Lp_p + t0) * kD2;
     cp_tile(tile(D0), douth + (size_t)t0 * kD2, kD2, nq);
     cp_tile(tile(D1), douth + (size_t)t0 * kD2 + 64, kD2, nq);
-    cp_tile(tile(V0), vh + (size_t)t0 * kD2, kD2, nq);
-    cp_tile(tile(V1), vh + (size_t)t0 * kD2 + 64, kD2, nq);
+    cp_tile(tile(s1(1, V0)), vh + (size_t)t0 * kD2, kD2, nq);
+    cp_tile(tile(s1(1, V1)), vh + (size_t)t0 * kD2 + 64, kD2, nq);
     cp_tile(tile(X0), qa, kD2, 64);
     cp_tile(tile(X1), qa + 64, kD2, 64);
-    cp_wait_all();
+    cp_commit();
+    if (a > 0) {
+        stage1(0, a - 1);
+        cp_wait<1>();
+    } else {
+        cp_wait<0>();
+    }
     __syncthreads();
 
     // ---- diagonal block: logits from the preparation's table; dT to the block pass
     {
         Acc ov;
         zero(ov);
-        wmma64<false, false>(ov, tile(D0), tile(V0), wm, wn, lane);  // dout_i . v_j
-        wmma64<false, false>(ov, tile(D1), tile(V1), wm, wn, lane);
+        wmma64<false, false>(ov, tile(D0), tile(s1(1, V0)), wm, wn, lane);  // dout_i . v_j
+        wmma64<false, false>(ov, tile(D1), tile(s1(1, V1)), wm, wn, lane);
         const __half *tab = dg + ((size_t)bh * nblk_p + a) * 64 * 64;
         float *dtd = dTd + ((size_t)bh * nb + a) * 64 * 64;
         float cs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
@@ -279,36 +329,32 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
         red_block(dv + (hL + t0) * kD2 + 64 * h, kD2, acc, wm, wn, lane, nq);
     }
 
-    // ---- pass 1: right to left over key blocks, X from Q~_a
-    const size_t pair0 = (size_t)bh * ((size_t)nb * (nb - 1) / 2) + (size_t)a * (a - 1) / 2;
+    // ---- pass 1: right to left over key blocks, X from Q~_a; key block b in set (a-1-b) % 2
     for (int b = a - 1; b >= 0; --b) {
-        __syncthreads();  // the previous step's readers of K, P, V, p and dT are done
-        const __nv_bfloat16 *kb = kp + ((size_t)bh * nblk_p + b) * kKpRows;
-        cp_tile(tile(K0), kb, kD2, 64);
-        cp_tile(tile(K1), kb + 64, kD2, 64);
-        cp_tile(tile(P00), kb + 64 * kD2, kD2, 64);
-        cp_tile(tile(P01), kb + 64 * kD2 + 64, kD2, 64);
-        cp_tile(tile(P10), kb + 128 * kD2, kD2, 64);
-        cp_tile(tile(P11), kb + 128 * kD2 + 64, kD2, 64);
-        cp_tile(tile(V0), vh + (size_t)b * 64 * kD2, kD2, 64);
-        cp_tile(tile(V1), vh + (size_t)b * 64 * kD2 + 64, kD2, 64);
+        const int set = (a - 1 - b) & 1;
+        __syncthreads();  // the previous step's readers of its set, p and dT are done
+        if (b > 0) {
+            stage1(set ^ 1, b - 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
         if (FOX && tid < 64) locj[tid] = loc[(size_t)bh * Lp + (size_t)b * 64 + tid];
-        cp_wait_all();
         __syncthreads();
         Acc s, ov, xn0, xn1;
         zero(s);
         zero(ov);
         zero(xn0);
         zero(xn1);
-        wmma64<false, false>(s, tile(X0), tile(K0), wm, wn, lane);   // x_i . k~_j
-        wmma64<false, false>(s, tile(X1), tile(K1), wm, wn, lane);
-        wmma64<false, false>(ov, tile(D0), tile(V0), wm, wn, lane);  // dout_i . v_j
-        wmma64<false, false>(ov, tile(D1), tile(V1), wm, wn, lane);
+        wmma64<false, false>(s, tile(X0), tile(s1(set, K0)), wm, wn, lane);   // x_i . k~_j
+        wmma64<false, false>(s, tile(X1), tile(s1(set, K1)), wm, wn, lane);
+        wmma64<false, false>(ov, tile(D0), tile(s1(set, V0)), wm, wn, lane);  // dout_i . v_j
+        wmma64<false, false>(ov, tile(D1), tile(s1(set, V1)), wm, wn, lane);
         if (b > 0) {  // X P_b^T, column halves 0 and 1
-            wmma64<false, false>(xn0, tile(X0), tile(P00), wm, wn, lane);
-            wmma64<false, false>(xn0, tile(X1), tile(P01), wm, wn, lane);
-            wmma64<false, false>(xn1, tile(X0), tile(P10), wm, wn, lane);
-            wmma64<false, false>(xn1, tile(X1), tile(P11), wm, wn, lane);
+            wmma64<false, false>(xn0, tile(X0), tile(s1(set, P00)), wm, wn, lane);
+            wmma64<false, false>(xn0, tile(X1), tile(s1(set, P01)), wm, wn, lane);
+            wmma64<false, false>(xn1, tile(X0), tile(s1(set, P10)), wm, wn, lane);
+            wmma64<false, false>(xn1, tile(X1), tile(s1(set, P11)), wm, wn, lane);
         }
         {
             const float dcb = FOX ? (float)(cb[(size_t)bh * nb + a] - cb[(size_t)bh * nb + b]) : 0.f;
@@ -382,36 +428,36 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
     Acc g0, g1;
     zero(g0);
     zero(g1);
+    if (a > 0) {
+        __syncthreads();  // pass 1 is done with every tile
+        stage2(0, 0);
+    }
     for (int b = 0; b < a; ++b) {
-        const __nv_bfloat16 *st = stash + (pair0 + b) * kStash;
-        const __nv_bfloat16 *kb = kp + ((size_t)bh * nblk_p + b) * kKpRows;
+        const int set = b & 1;
+        __syncthreads();  // the previous step's readers of its set and of G are done
+        if (b + 1 < a) {
+            stage2(set ^ 1, b + 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
         __syncthreads();
-        cp_tile(tile(X0), st, kD2, 64);
-        cp_tile(tile(X1), st + 64, kD2, 64);
-        cp_tile(tile(DT), st + 64 * kD2, 64, 64);
-        cp_tile(tile(K0), kb, kD2, 64);
-        cp_tile(tile(K1), kb + 64, kD2, 64);
-        cp_tile(tile(P00), kb + 64 * kD2, kD2, 64);
-        cp_tile(tile(P01), kb + 64 * kD2 + 64, kD2, 64);
-        cp_tile(tile(P10), kb + 128 * kD2, kD2, 64);
-        cp_tile(tile(P11), kb + 128 * kD2 + 64, kD2, 64);
-        cp_wait_all();
-        __syncthreads();
+        const int xa = s2x(set, 0), xb = s2x(set, 1), dts = s2dt(set);
         Acc n0, n1;
         zero(n0);
         zero(n1);
         if (b > 0) {  // G_{b-1} P_b, head and tail
-            wmma64<false, true>(n0, tile(G0H), tile(P00), wm, wn, lane);
-            wmma64<false, true>(n0, tile(G1H), tile(P10), wm, wn, lane);
-            wmma64<false, true>(n0, tile(G0L), tile(P00), wm, wn, lane);
-            wmma64<false, true>(n0, tile(G1L), tile(P10), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G0H), tile(P01), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G1H), tile(P11), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G0L), tile(P01), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G1L), tile(P11), wm, wn, lane);
+            wmma64<false, true>(n0, tile(G0H), tile(s1(set, P00)), wm, wn, lane);
+            wmma64<false, true>(n0, tile(G1H), tile(s1(set, P10)), wm, wn, lane);
+            wmma64<false, true>(n0, tile(G0L), tile(s1(set, P00)), wm, wn, lane);
+            wmma64<false, true>(n0, tile(G1L), tile(s1(set, P10)), wm, wn, lane);
+            wmma64<false, true>(n1, tile(G0H), tile(s1(set, P01)), wm, wn, lane);
+            wmma64<false, true>(n1, tile(G1H), tile(s1(set, P11)), wm, wn, lane);
+            wmma64<false, true>(n1, tile(G0L), tile(s1(set, P01)), wm, wn, lane);
+            wmma64<false, true>(n1, tile(G1L), tile(s1(set, P11)), wm, wn, lane);
         }
-        wmma64<false, true>(n0, tile(DT), tile(K0), wm, wn, lane);  // + dT_ab K~_b
-        wmma64<false, true>(n1, tile(DT), tile(K1), wm, wn, lane);
+        wmma64<false, true>(n0, tile(dts), tile(s1(set, K0)), wm, wn, lane);  // + dT_ab K~_b
+        wmma64<false, true>(n1, tile(dts), tile(s1(set, K1)), wm, wn, lane);
         if (b > 0) {  // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c], four quadrants
             float *dpb = dP + ((size_t)bh * nb + b) * kD2 * kD2;
 #pragma unroll 1
@@ -419,8 +465,8 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
                 const int nh = qd >> 1, ch = qd & 1;
                 Acc acc;
                 zero(acc);
-                wmma64<true, true>(acc, tile(nh ? G1H : G0H), tile(X0 + ch), wm, wn, lane);
-                wmma64<true, true>(acc, tile(nh ? G1L : G0L), tile(X0 + ch), wm, wn, lane);
+                wmma64<true, true>(acc, tile(nh ? G1H : G0H), tile(ch ? xb : xa), wm, wn, lane);
+                wmma64<true, true>(acc, tile(nh ? G1L : G0L), tile(ch ? xb : xa), wm, wn, lane);
                 red_block(dpb + (size_t)64 * nh * kD2 + 64 * ch, kD2, acc, wm, wn, lane, 64);
             }
         }
