@@ -58,6 +58,34 @@ def test_bwd_matches_finite_differences(fox):
         assert err < 1e-6, "%s: relative error %g against finite differences" % (gname, err)
 
 
+@pytest.mark.parametrize("fox", [False, True])
+def test_bwd_head_size_128_matches_finite_differences_sampled(fox):
+    # the head size of the second model width: nothing in the derivation or the oracle's
+    # loops depends on d, so a few sampled entries per gradient suffice
+    rng = np.random.default_rng(21 + fox)
+    q, k, v, w, beta, log_f, dout = rand_case(rng, 5, 128)
+    if not fox:
+        log_f = None
+    g = oracle.path_bwd(q, k, v, w, beta, dout, log_f=log_f)
+    args = {"q": q, "k": k, "v": v, "w": w, "beta": beta, "log_f": log_f}
+    names = [("dq", "q"), ("dk", "k"), ("dv", "v"), ("dw", "w"), ("dbeta", "beta")]
+    if fox:
+        names.append(("dlog_f", "log_f"))
+    h = 1e-6
+    for gname, aname in names:
+        base = args[aname]
+        flat = rng.choice(base.size, size=min(24, base.size), replace=False)
+        for f in flat:
+            idx = np.unravel_index(f, base.shape)
+            hi, lo = base.copy(), base.copy()
+            hi[idx] += h
+            lo[idx] -= h
+            fd = (loss(**{**args, aname: hi}, dout=dout) -
+                  loss(**{**args, aname: lo}, dout=dout)) / (2 * h)
+            scale = max(np.abs(g[gname]).max(), 1e-3)
+            assert abs(fd - g[gname][idx]) <= 1e-6 * scale, (gname, idx, fd, g[gname][idx])
+
+
 def test_bwd_beta_zero_closed_form():
     rng = np.random.default_rng(5)
     L, d = 23, 8
