@@ -75,6 +75,12 @@ constexpr uint32_t S_END = S_STG1 + NS1 * kStage1;
 static_assert(S_STG2 + NS2 * kStage2 <= S_END, "pass-2 ring fits");
 constexpr uint32_t S_CS = S_END;  // FoX only
 constexpr uint32_t kCsBytes = 64 * kCsLd * 4;
+// FoX: a constant K-major B operand of 16 rows x 128 columns whose row 0 is all ones;
+// [p^T; dS^T] times it gives in column 0 the column sums of dS over the tile's rows
+constexpr uint32_t S_ONES = (S_CS + kCsBytes + 1023u) & ~1023u;
+constexpr uint32_t kOnesBytes = 16 * 128 * 2;
+template <bool FOX>
+__host__ __device__ constexpr uint32_t bwd_tc_smem_end() { return FOX ? S_ONES + kOnesBytes : S_END; }
 
 // barrier indices
 constexpr int B_FULL1 = 0, B_FULL2 = B_FULL1 + NS1, B_LD0 = B_FULL2 + NS2, B_M1 = B_LD0 + 1,
@@ -84,11 +90,12 @@ constexpr int B_FULL1 = 0, B_FULL2 = B_FULL1 + NS1, B_LD0 = B_FULL2 + NS2, B_M1 
 
 // TMEM columns
 constexpr uint32_t C_SX = 0, C_OV = 128, C_KV0 = 256, C_KV1 = 384;  // pass 1
+constexpr uint32_t C_CS0 = 192, C_CS1 = 208;                        // pass 1, FoX: dS column sums
 constexpr uint32_t C_G = 0, C_DP0 = 256, C_DP1 = 384;                // pass 2
 
 template <bool FOX>
 constexpr uint32_t bwd_tc_smem() {
-    return 1024 + S_END + (FOX ? kCsBytes : 0) + NBAR * 8 + 16;
+    return 1024 + bwd_tc_smem_end<FOX>() + NBAR * 8 + 16;
 }
 
 __host__ __device__ constexpr uint32_t idesc_b16(int M, int N, bool a_mn, bool b_mn) {
@@ -177,7 +184,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *const sm = smem_raw + (base - raw);
-    constexpr uint32_t S_BAR = S_END + (FOX ? kCsBytes : 0);
+    constexpr uint32_t S_BAR = bwd_tc_smem_end<FOX>();
     auto bar = [&](int i) { return base + S_BAR + 8u * (uint32_t)i; };
     uint32_t *const tslot = reinterpret_cast<uint32_t *>(sm + S_BAR + 8 * NBAR);
     volatile uint32_t *const abort_f = tslot + 1;
@@ -210,6 +217,15 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         tmem_alloc(smem_u32(tslot), 512);
         tmem_relinquish();
         tc_fence_before();
+    }
+    if (FOX && tid < (int)(kOnesBytes / 16)) {
+        // row 0 of each 64-column half: 128 bytes of bf16 ones (the swizzle moves chunks
+        // only within a row); every other row zero
+        const uint32_t off = 16u * (uint32_t)tid;
+        const uint32_t one2 = 0x3F803F80u;
+        *reinterpret_cast<uint4 *>(sm + S_ONES + off) =
+            (off % 2048u) < 128u ? make_uint4(one2, one2, one2, one2) : make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
     }
     __syncthreads();
     tc_fence_after();
@@ -266,6 +282,16 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     umma_bf16(tmem + (i ? C_KV1 : C_KV0), a + 128 * kk, b + 128 * kk, ID, kk > 0);
+                if (FOX) {
+                    // [p^T; dS^T] x ones: rows 64 + j of column 0 hold sum_i dS_ij (K-major
+                    // operand: 32 bytes per k-step, the second 64 columns 2 KB on)
+                    constexpr uint32_t IDC = idesc_b16(128, 16, true, false);
+                    const uint64_t bo = sdesc_sw128(base + S_ONES, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16(tmem + (i ? C_CS1 : C_CS0), a + 128 * kk,
+                                  bo + (uint64_t)(128 * (kk >> 2) + 2 * (kk & 3)), IDC, kk > 0);
+                }
                 umma_commit(bar(B_M2 + i));
                 return true;
             };
@@ -453,7 +479,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         }
                     }
                 }
-                float p[32], dt[32];
+                float p[32], dt[32], dsv[FOX ? 32 : 1];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     float l2 = x[j];
@@ -469,7 +495,10 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     dt[j] = scale * ds;
                     if (FOX) {
                         rs_acc += ds;
-                        csb[(32 * h + j) * kCsLd + r] = ds;
+                        dsv[j] = offd ? ds : 0.f;
+                        // the MMA sums the off-diagonal columns; the diagonal blocks (steps 0
+                        // and 1) go through the transposed buffer
+                        if (s <= 1) csb[(32 * h + j) * kCsLd + r] = diag ? ds : 0.f;
                     }
                 }
                 // the p, dT and carried-row tiles are operands of the previous step's gather
@@ -489,7 +518,12 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dt[j] = 0.f;
                 }
-                st_row_half(sm + S_DT, r, h, dt);
+                // PaTH-FoX keeps dS (unscaled) in the tile, so that its column sums come out of
+                // the MMA for any scale; the gather then scales dK~
+                if (FOX)
+                    st_row_half(sm + S_DT, r, h, dsv);
+                else
+                    st_row_half(sm + S_DT, r, h, dt);
                 if (s >= 1)
                     st_global_half(stash + ((((size_t)bh * npair * npair) + rec0 + (size_t)b) * 256 +
                                             128 + r) * kD + 32 * h,
@@ -535,10 +569,10 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             if (s == steps1 - 1) fence_proxy_async_global();
             tc_fence_before();
             mbar_arrive_warp(bar(B_EPI));
-            if (FOX) {
-                // column sums of dS over the tile's 128 rows: each thread sums half a column
-                // once all four warps have written theirs (B_CSA), and the buffer is rewritten
-                // only after every thread has read it (B_CSB)
+            if (FOX && s <= 1) {
+                // column sums of the diagonal blocks' dS over the tile's 128 rows: each thread
+                // sums half a column once all four warps have written theirs (B_CSA), and the
+                // buffer is rewritten only after every thread has read it (B_CSB)
                 mbar_arrive_warp(bar(B_CSA));
                 if (!(ok = wait_warp(bar(B_CSA), s & 1))) break;
                 const int j = r & 63, half = r >> 6;
@@ -609,15 +643,23 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 // block)
                 if (s >= 1 && b < nblk) {
                     float *dst = dkt + ((size_t)bh * Lp + 64 * b + (m - 64)) * kD;
+                    const float ks = FOX ? scale : 1.f;  // PaTH-FoX: the tile held dS
 #pragma unroll 1
                     for (int h = 0; h < 2; ++h) {
                         float x[32];
                         tld32(acc + 32 * h, x);
 #pragma unroll
                         for (int c = 0; c < 8; ++c)
-                            red_add_v4(dst + 32 * h + 4 * c, x[4 * c], x[4 * c + 1], x[4 * c + 2],
-                                       x[4 * c + 3]);
+                            red_add_v4(dst + 32 * h + 4 * c, ks * x[4 * c], ks * x[4 * c + 1],
+                                       ks * x[4 * c + 2], ks * x[4 * c + 3]);
                     }
+                }
+                if (FOX && s >= 1) {
+                    // sum over the tile's rows of dS_ij, j = m - 64 of key block b
+                    float x[32];
+                    tld32(tmem + lane_off + (i ? C_CS1 : C_CS0), x);
+                    const int j = 64 * b + (m - 64);
+                    if (j < L) atomicAdd(csum + (size_t)bh * Lp + j, x[0]);
                 }
             } else {
                 // dv row j: p^T dout. The TMEM loads are warp-collective, so every lane loads
