@@ -34,9 +34,10 @@
 // their owners. The block pass of backward.cu then takes dq~, dk~, dP_b and the diagonal
 // dT to q, k, w and beta.
 //
-// Warp roles (288 threads): warps 0-3 read the TMEM lanes of their rows after each MMA1
-// (softmax gradient, p, dT, the carried rows) and after each pass-2 MMA (G); warps 4-7
-// drain D_kv / D_p into the gathered gradients; warp 8 allocates TMEM and its lane 0 issues
+// Warp roles (416 threads): warps 0-7 read the TMEM lanes of their rows after each MMA1
+// (softmax gradient, p, dT, the carried rows) and after each pass-2 MMA (G), two warps per
+// lane quadrant, each on one 32-column half of every row; warps 8-11 drain D_kv / D_p into
+// the gathered gradients; warp 12 allocates TMEM and its lane 0 issues
 // every TMA load and MMA. Every wait is bounded; on a timeout the CTA records
 // PATH_ERR_TIMEOUT in the workspace status word, every role leaves its loop, the issuing
 // lane waits for its copies and MMAs in flight, and TMEM is freed.
@@ -59,7 +60,7 @@ cudaError_t launch_bwd_fox_dlogf(const float *rsum, const float *csum, int BH, i
 
 namespace {
 
-constexpr int kThr = 288;
+constexpr int kThr = 416;
 constexpr uint32_t kT128 = 128 * 128;  // 128 rows x 64 bf16
 constexpr uint32_t kT64 = 64 * 128;    // 64 rows x 64 bf16
 constexpr int NS1 = 4, NS2 = 3;
@@ -121,6 +122,19 @@ struct Wait {
         }
     }
 };
+
+// Registers per thread after the split (launch: 128 for all 416 threads, the share of a
+// sub-partition holding four warps); rows 8 x 152 + drains 4 x 80 + issuer 104 <= 13 x 128.
+constexpr int kRegRow = 152, kRegDrain = 80, kRegIssue = 104;
+static_assert(8 * kRegRow + 4 * kRegDrain + kRegIssue <= 13 * 128, "register split");
+template <int N>
+__device__ __forceinline__ void reg_alloc_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
 
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -206,14 +220,15 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         *abort_f = 0u;
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if (i == B_EPI || i == B_KVF || i == B_KVF + 1 || i == B_EPIB || i == B_DPF ||
-                i == B_DPF + 1 || i == B_CSA || i == B_CSB)
-                cnt = 4;
+            if (i == B_EPI || i == B_EPIB || i == B_CSA || i == B_CSB)
+                cnt = 8;  // the row warps
+            if (i == B_KVF || i == B_KVF + 1 || i == B_DPF || i == B_DPF + 1)
+                cnt = 4;  // the gather drains
             mbar_init(bar(i), cnt);
         }
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == 12) {
         tmem_alloc(smem_u32(tslot), 512);
         tmem_relinquish();
         tc_fence_before();
@@ -231,8 +246,9 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ================================================================ issuer
+        reg_alloc_dec<kRegIssue>();
         if (lane == 0) {
             tma_prefetch_desc(&tm_qt);
             tma_prefetch_desc(&tm_kp);
@@ -407,10 +423,14 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 *abort_f = 1u;
             }
         }
-    } else if (warp < 4) {
+    } else if (warp < 8) {
         // ================================================================ row epilogue
-        const int r = tid;  // tile row = TMEM lane
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        reg_alloc_inc<kRegRow>();
+        // two warps per TMEM lane quadrant: warp w takes columns 32 hw .. 32 hw + 31 of every
+        // 64-column block of its rows (hw = w / 4)
+        const int hw = warp >> 2;
+        const int r = 32 * (warp & 3) + lane;  // tile row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const int tok = 128 * t + r;
         const bool valid = tok < L;
         const int blk_row = 2 * t + (r >> 6);  // the row's query block
@@ -450,7 +470,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             float dcb = 0.f;
             if (FOX && offd && valid) dcb = (float)(ca - cb[(size_t)bh * nblk + b]);
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
+            for (int h = hw; h < hw + 1; ++h) {
                 float ov[32], x[32];
                 {
                     // both loads of the half in flight before one wait
@@ -479,7 +499,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         }
                     }
                 }
-                float p[32], dt[32], dsv[FOX ? 32 : 1];
+                float p[32], dd[32];  // p and dS of the half row
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     float l2 = x[j];
@@ -492,10 +512,9 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const float pj = (valid && (diag || offd)) ? ex2_approx(l2 - lse2) : 0.f;
                     const float ds = pj * (ov[j] - Drow);
                     p[j] = pj;
-                    dt[j] = scale * ds;
+                    dd[j] = ds;
                     if (FOX) {
                         rs_acc += ds;
-                        dsv[j] = offd ? ds : 0.f;
                         // the MMA sums the off-diagonal columns; the diagonal blocks (steps 0
                         // and 1) go through the transposed buffer
                         if (s <= 1) csb[(32 * h + j) * kCsLd + r] = diag ? ds : 0.f;
@@ -503,31 +522,33 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 }
                 // the p, dT and carried-row tiles are operands of the previous step's gather
                 // MMA, which runs while this step's loads and exponentials are done
-                if (h == 0 && s >= 1 &&
-                    !(ok = wait_warp(bar(B_M2 + ((s - 1) & 1)), ((s - 1) >> 1) & 1)))
+                if (s >= 1 && !(ok = wait_warp(bar(B_M2 + ((s - 1) & 1)), ((s - 1) >> 1) & 1)))
                     break;
                 st_row_half(sm + S_PT, r, h, p);
-                if (diag && b < nblk) {
-                    float4 *dd = reinterpret_cast<float4 *>(
+                if (diag && b < nblk) {  // the diagonal dT, fp32, for the block pass
+                    float4 *d4 = reinterpret_cast<float4 *>(
                         dTd + (((size_t)bh * nblk + b) * kC + (r & 63)) * kC + 32 * h);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        dd[c] = make_float4(dt[4 * c], dt[4 * c + 1], dt[4 * c + 2], dt[4 * c + 3]);
+                        d4[c] = make_float4(scale * dd[4 * c], scale * dd[4 * c + 1],
+                                            scale * dd[4 * c + 2], scale * dd[4 * c + 3]);
                 }
-                if (!offd) {
+                // the dT operand tile (p's registers, now free): off-diagonal rows only;
+                // PaTH-FoX keeps dS unscaled there, so that its column sums come out of the
+                // MMA for any scale (the gather then scales dK~)
+                float *tv = p;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) dt[j] = 0.f;
-                }
-                // PaTH-FoX keeps dS (unscaled) in the tile, so that its column sums come out of
-                // the MMA for any scale; the gather then scales dK~
-                if (FOX)
-                    st_row_half(sm + S_DT, r, h, dsv);
-                else
-                    st_row_half(sm + S_DT, r, h, dt);
-                if (s >= 1)
+                for (int j = 0; j < 32; ++j) tv[j] = offd ? (FOX ? dd[j] : scale * dd[j]) : 0.f;
+                st_row_half(sm + S_DT, r, h, tv);
+                if (s >= 1) {  // the stash record of dT
+                    if (FOX) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) tv[j] *= scale;
+                    }
                     st_global_half(stash + ((((size_t)bh * npair * npair) + rec0 + (size_t)b) * 256 +
                                             128 + r) * kD + 32 * h,
-                                   dt);
+                                   tv);
+                }
             }
             if (!ok) break;
             // the carried rows for the next key block (and their stash record)
@@ -538,7 +559,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     stash + ((((size_t)bh * npair * npair) + rec0 + (size_t)(2 * t)) * 256 + r) * kD;
                 uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
+                for (int c = 4 * hw; c < 4 * hw + 4; ++c)
                     d4[c] = (r < 64) ? make_uint4(0u, 0u, 0u, 0u)
                                      : *reinterpret_cast<const uint4 *>(sm + S_XB0 + sw128_offset(r, c));
             } else if (b > 0) {
@@ -549,14 +570,14 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     // block 2t's rows keep q~ (their walk starts at key block 2t - 1)
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 4 * hw; c < 4 * hw + 4; ++c) {
                         const uint4 u = *reinterpret_cast<const uint4 *>(sm + S_XB0 + sw128_offset(r, c));
                         *reinterpret_cast<uint4 *>(xn + sw128_offset(r, c)) = u;
                         d4[c] = u;
                     }
                 } else {
 #pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = hw; h < hw + 1; ++h) {
                         float x[32];
                         tld32(tmem + lane_off + C_SX + 64 + 32 * h, x);
                         st_row_half(xn, r, h, x);
@@ -571,57 +592,49 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             mbar_arrive_warp(bar(B_EPI));
             if (FOX && s <= 1) {
                 // column sums of the diagonal blocks' dS over the tile's 128 rows: each thread
-                // sums half a column once all four warps have written theirs (B_CSA), and the
+                // sums a quarter column once all eight warps have written theirs (B_CSA), and the
                 // buffer is rewritten only after every thread has read it (B_CSB)
                 mbar_arrive_warp(bar(B_CSA));
                 if (!(ok = wait_warp(bar(B_CSA), s & 1))) break;
-                const int j = r & 63, half = r >> 6;
-                const float *col = csb + j * kCsLd + 64 * half;
+                const int rt = 128 * hw + r, j = rt & 63, quarter = rt >> 6;
+                const float *col = csb + j * kCsLd + 32 * quarter;
                 float acc = 0.f;
 #pragma unroll 8
-                for (int i = 0; i < 64; ++i) acc += col[i];
+                for (int i = 0; i < 32; ++i) acc += col[i];
                 if (64 * b + j < L) atomicAdd(csum + (size_t)bh * Lp + 64 * b + j, acc);
                 mbar_arrive_warp(bar(B_CSB));
                 if (!(ok = wait_warp(bar(B_CSB), s & 1))) break;
             }
         }
-        if (FOX && valid) rsum[(size_t)bh * Lp + tok] = rs_acc;
+        if (FOX && valid) atomicAdd(rsum + (size_t)bh * Lp + tok, rs_acc);  // two halves per row
         // ---------------- pass 2
         if (ok && t == 0 && r < 64 && 0 < nblk) {
             // block 0 carries nothing: dq~ = 0
             float4 *dq4 = reinterpret_cast<float4 *>(dqt + ((size_t)bh * Lp + r) * kD);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) dq4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 8 * hw; c < 8 * hw + 8; ++c) dq4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         for (int b = 0; ok && b < steps2; ++b) {
             if (!(ok = wait_warp(bar(B_M1B), b & 1))) break;
             tc_fence_after();
-            float g[2][32];
-            tld32(tmem + lane_off + C_G, g[0]);
-            tld32(tmem + lane_off + C_G + 32, g[1]);
+            float g[32];  // this warp's half of the row of G
+            tld32(tmem + lane_off + C_G + 32 * hw, g);
             const bool last_a0 = (b == 2 * t - 1) && r < 64 && 2 * t < nblk;
             const bool last_a1 = (b == 2 * t) && r >= 64 && 2 * t + 1 < nblk;
             if (last_a0 || last_a1) {
                 float4 *dq4 = reinterpret_cast<float4 *>(dqt + ((size_t)bh * Lp + tok) * kD);
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dq4[8 * h + c] = make_float4(g[h][4 * c], g[h][4 * c + 1], g[h][4 * c + 2],
-                                                     g[h][4 * c + 3]);
+                for (int c = 0; c < 8; ++c)
+                    dq4[8 * hw + c] = make_float4(g[4 * c], g[4 * c + 1], g[4 * c + 2], g[4 * c + 3]);
             }
             if (b < 2 * t) {
                 // the dP_b MMA of this step reads the G tiles being replaced
                 if (b > 0 && !(ok = wait_warp(bar(B_M2B + (b & 1)), ((b - 1) >> 1) & 1))) break;
+                float lo[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float lo[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        lo[j] = g[h][j] - __bfloat162float(__float2bfloat16_rn(g[h][j]));
-                    st_row_half(sm + S_XB0, r, h, g[h]);
-                    st_row_half(sm + S_XB1, r, h, lo);
-                }
+                for (int j = 0; j < 32; ++j) lo[j] = g[j] - __bfloat162float(__float2bfloat16_rn(g[j]));
+                st_row_half(sm + S_XB0, r, hw, g);
+                st_row_half(sm + S_XB1, r, hw, lo);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive_warp(bar(B_EPIB));
@@ -629,8 +642,9 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
         }
     } else {
         // ================================================================ gather drains
-        const int m = tid - 128;  // TMEM lane
-        const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+        reg_alloc_dec<kRegDrain>();
+        const int m = tid - 256;  // TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp - 8)) << 16;
         const size_t hL = (size_t)bh * L;
         bool ok = true;
         for (int s = 0; ok && s < steps1; ++s) {
@@ -707,7 +721,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == 12) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -788,7 +802,9 @@ cudaError_t launch_path_bwd_tc(const void *q, const void *k, const void *v, cons
         return e;
     if ((e = cudaMemsetAsync(dv, 0, (size_t)y.BH * L * kD * 4, stream)) != cudaSuccess) return e;
     if (fox) {
-        if ((e = cudaMemsetAsync(cs, 0, tok, stream)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(cs, 0, tok, stream)) != cudaSuccess ||
+            (e = cudaMemsetAsync(rs, 0, tok, stream)) != cudaSuccess)
+            return e;
         if ((e = launch_bwd_fox_sums(log_f, y.BH, L, y.Lp, y.nblk, loc, cb, stream)) != cudaSuccess)
             return e;
     }
