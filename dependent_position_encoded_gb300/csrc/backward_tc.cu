@@ -166,17 +166,6 @@ __device__ __forceinline__ void st_row_half(uint8_t *tile, int r, int h, const f
     }
 }
 
-// the same 32 values as 64 contiguous bytes of bf16 in global memory
-__device__ __forceinline__ void st_global_half(__nv_bfloat16 *dst, const float *x) {
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const float *s = x + 8 * c;
-        d[c] = make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]),
-                          pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
-    }
-}
-
 // One CTA per (tile t of query blocks 2t, 2t+1; head). nblk: real blocks of the head;
 // nbe: blocks rounded up to even (the forward preparation's layout); Lp = 64 nblk.
 template <bool FOX>
@@ -283,8 +272,21 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             // MMA2 of pass-1 step s: D_kv[s % 2] = [p^T; dT^T] [X_s | dout] (the p tile sits
             // below the dT tile, so both M halves are addressed upward from it)
             uint32_t kv_uses[2] = {0, 0}, kvf_waits[2] = {0, 0};
+            // the stash records of pass-1 step s (s >= 1), by TMA from the tiles the row
+            // epilogue left: dS of key block b (rows 128-255 of record b) and the carried rows
+            // for key block b - 1 (rows 0-127 of record b - 1); record 2t is written at step 0
+            // by the row epilogue
+            auto stash_stores = [&](int s) {
+                const int b = 2 * t + 1 - s;
+                if (s < 1) return;
+                tma_store_3d(&tm_st, base + S_DT, 0, (int)((rec0 + (size_t)b) * 256 + 128), bh);
+                if (b > 0)
+                    tma_store_3d(&tm_st, base + ((s & 1) ? S_XB1 : S_XB0), 0,
+                                 (int)((rec0 + (size_t)(b - 1)) * 256), bh);
+            };
             auto mma2 = [&](int s) -> bool {
                 const int i = s & 1;
+                bulk_wait_read();  // the stash stores have read the tiles this MMA's successors rewrite
                 if (kv_uses[i] > 0) {  // the drain of step s - 2 has read this accumulator
                     if (!wait(bar(B_KVF + i), kvf_waits[i] & 1)) return false;
                     ++kvf_waits[i];
@@ -316,6 +318,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 if (!(ok = wait(bar(B_FULL1 + st), (done1 / NS1) & 1))) break;
                 ++done1;
                 if (s > 0 && !(ok = wait(bar(B_EPI), (s - 1) & 1))) break;
+                if (s > 0) stash_stores(s - 1);
                 tc_fence_after();
                 const uint32_t stg = base + S_STG1 + (uint32_t)st * kStage1;
                 if (s > 0) {
@@ -345,7 +348,9 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 }
             }
             if (ok) ok = wait(bar(B_EPI), (steps1 - 1) & 1);
+            if (ok) stash_stores(steps1 - 1);
             if (ok) ok = mma2(steps1 - 1);
+            bulk_wait_all();  // pass 2 reads the stash back (and rewrites the X tiles)
             // pass 2 starts once both D_kv drains are done (their TMEM columns become D_p,
             // and the last MMA2, which read dout, p and dT, has completed)
             for (int i = 0; ok && i < 2; ++i)
@@ -533,22 +538,14 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                         d4[c] = make_float4(scale * dd[4 * c], scale * dd[4 * c + 1],
                                             scale * dd[4 * c + 2], scale * dd[4 * c + 3]);
                 }
-                // the dT operand tile (p's registers, now free): off-diagonal rows only;
-                // PaTH-FoX keeps dS unscaled there, so that its column sums come out of the
-                // MMA for any scale (the gather then scales dK~)
+                // the dS operand tile (p's registers, now free), off-diagonal rows only and
+                // unscaled (the products that use it are scaled on output, so PaTH-FoX's
+                // column sums come out of the MMA for any scale); the issuer stores the tile
+                // as the step's stash record of dS by TMA
                 float *tv = p;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) tv[j] = offd ? (FOX ? dd[j] : scale * dd[j]) : 0.f;
+                for (int j = 0; j < 32; ++j) tv[j] = offd ? dd[j] : 0.f;
                 st_row_half(sm + S_DT, r, h, tv);
-                if (s >= 1) {  // the stash record of dT
-                    if (FOX) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) tv[j] *= scale;
-                    }
-                    st_global_half(stash + ((((size_t)bh * npair * npair) + rec0 + (size_t)b) * 256 +
-                                            128 + r) * kD + 32 * h,
-                                   tv);
-                }
             }
             if (!ok) break;
             // the carried rows for the next key block (and their stash record)
@@ -563,30 +560,24 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     d4[c] = (r < 64) ? make_uint4(0u, 0u, 0u, 0u)
                                      : *reinterpret_cast<const uint4 *>(sm + S_XB0 + sw128_offset(r, c));
             } else if (b > 0) {
+                // the carried rows for key block b - 1 (the issuer stores the tile as its stash
+                // record by TMA)
                 uint8_t *xn = sm + ((s & 1) ? S_XB1 : S_XB0);
-                __nv_bfloat16 *dst =
-                    stash + ((((size_t)bh * npair * npair) + rec0 + (size_t)(b - 1)) * 256 + r) * kD;
                 if (s == 1 && r < 64) {
                     // block 2t's rows keep q~ (their walk starts at key block 2t - 1)
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                    for (int c = 4 * hw; c < 4 * hw + 4; ++c) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(sm + S_XB0 + sw128_offset(r, c));
-                        *reinterpret_cast<uint4 *>(xn + sw128_offset(r, c)) = u;
-                        d4[c] = u;
-                    }
+                    for (int c = 4 * hw; c < 4 * hw + 4; ++c)
+                        *reinterpret_cast<uint4 *>(xn + sw128_offset(r, c)) =
+                            *reinterpret_cast<const uint4 *>(sm + S_XB0 + sw128_offset(r, c));
                 } else {
-#pragma unroll 1
-                    for (int h = hw; h < hw + 1; ++h) {
-                        float x[32];
-                        tld32(tmem + lane_off + C_SX + 64 + 32 * h, x);
-                        st_row_half(xn, r, h, x);
-                        st_global_half(dst + 32 * h, x);
-                    }
+                    float x[32];
+                    tld32(tmem + lane_off + C_SX + 64 + 32 * hw, x);
+                    st_row_half(xn, r, hw, x);
                 }
             }
             fence_proxy_async_smem();
-            // the stash is read back by TMA in pass 2, which starts after this pass's last step
+            // the stash record written above at step 0 is read back by TMA in pass 2, which
+            // starts after this pass's last step
             if (s == steps1 - 1) fence_proxy_async_global();
             tc_fence_before();
             mbar_arrive_warp(bar(B_EPI));
@@ -622,10 +613,12 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
             const bool last_a0 = (b == 2 * t - 1) && r < 64 && 2 * t < nblk;
             const bool last_a1 = (b == 2 * t) && r >= 64 && 2 * t + 1 < nblk;
             if (last_a0 || last_a1) {
+                // the recursion runs on G / scale (its dS operand is unscaled)
                 float4 *dq4 = reinterpret_cast<float4 *>(dqt + ((size_t)bh * Lp + tok) * kD);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    dq4[8 * hw + c] = make_float4(g[4 * c], g[4 * c + 1], g[4 * c + 2], g[4 * c + 3]);
+                    dq4[8 * hw + c] = make_float4(scale * g[4 * c], scale * g[4 * c + 1],
+                                                  scale * g[4 * c + 2], scale * g[4 * c + 3]);
             }
             if (b < 2 * t) {
                 // the dP_b MMA of this step reads the G tiles being replaced
@@ -657,7 +650,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 // block)
                 if (s >= 1 && b < nblk) {
                     float *dst = dkt + ((size_t)bh * Lp + 64 * b + (m - 64)) * kD;
-                    const float ks = FOX ? scale : 1.f;  // PaTH-FoX: the tile held dS
+                    const float ks = scale;  // the tile held dS
 #pragma unroll 1
                     for (int h = 0; h < 2; ++h) {
                         float x[32];
@@ -709,10 +702,11 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                 for (int h = 0; h < 2; ++h) {
                     float x[32];
                     tld32(acc + 32 * h, x);
+                    // G / scale in the recursion: scale on output
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        red_add_v4(dst + 32 * h + 4 * c, x[4 * c], x[4 * c + 1], x[4 * c + 2],
-                                   x[4 * c + 3]);
+                        red_add_v4(dst + 32 * h + 4 * c, scale * x[4 * c], scale * x[4 * c + 1],
+                                   scale * x[4 * c + 2], scale * x[4 * c + 3]);
                 }
             }
             tc_fence_before();

@@ -48,25 +48,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// Tensor store of a 128-byte-swizzled shared tile (box of the map) at (c0, c1, c2); one
-// bulk group per store.
-__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1,
-                                             int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
-        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until every committed store has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Waits until every committed store has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Named barrier over the four epilogue warps (ids 1..; 0 is __syncthreads).
 __device__ __forceinline__ void epi_sync() {
     asm volatile("bar.sync 1, 128;" ::: "memory");
