@@ -125,6 +125,42 @@ __device__ __forceinline__ void wmma64(Acc &acc, uint32_t a, uint32_t b, int wm,
     }
 }
 
+// acc[j] += sum_i A_i B_j over k = 0..63 for this warp's block, NA A tiles and NB B tiles in
+// the layouts of wmma64; every fragment is loaded once per k step and used by every product
+// that shares it.
+template <bool AT, bool BT, int NA, int NB>
+__device__ __forceinline__ void wmma64_sum(Acc (&acc)[NB], const uint32_t (&a)[NA],
+                                           const uint32_t (&b)[NB], int wm, int wn, int lane) {
+    const int li = lane & 7, l3 = (lane >> 3) & 1, l4 = lane >> 4;
+#pragma unroll
+    for (int k0 = 0; k0 < 64; k0 += 16) {
+        uint32_t af[NA][4];
+#pragma unroll
+        for (int i = 0; i < NA; ++i) {
+            if (!AT)
+                ldsm_x4(a[i] + ((16 * wm + (lane & 15)) * SLD + k0 + 8 * l4) * 2, af[i]);
+            else
+                ldsm_x4_t(a[i] + ((k0 + 8 * l4 + li) * SLD + 16 * wm + 8 * l3) * 2, af[i]);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+#pragma unroll
+            for (int np = 0; np < 2; ++np) {
+                const int n0 = 32 * wn + 16 * np;
+                uint32_t bf[4];
+                if (!BT)
+                    ldsm_x4(b[j] + ((n0 + 8 * l4 + li) * SLD + k0 + 8 * l3) * 2, bf);
+                else
+                    ldsm_x4_t(b[j] + ((k0 + 8 * l3 + li) * SLD + n0 + 8 * l4) * 2, bf);
+#pragma unroll
+                for (int i = 0; i < NA; ++i) {
+                    mma_bf16(acc[j][2 * np], af[i], bf[0], bf[1]);
+                    mma_bf16(acc[j][2 * np + 1], af[i], bf[2], bf[3]);
+                }
+            }
+    }
+}
+
 // 64 rows x 64 bf16 from global (row stride ld elements; rows >= nrows read as zero) into a
 // tile, asynchronously (16-byte copies; the caller commits them as a group)
 __device__ __forceinline__ void cp_tile(uint32_t dst, const __nv_bfloat16 *src, int ld, int nrows) {
@@ -321,12 +357,13 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
         if (FOX) fox_col_sums(cs, csum + (size_t)bh * Lp + (size_t)a * 64, wn, lane);
     }
     __syncthreads();
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {  // dv_j += sum_i p_ij dout_i, j in the diagonal block
-        Acc acc;
-        zero(acc);
-        wmma64<true, true>(acc, tile(PT), tile(D0 + h), wm, wn, lane);
-        red_block(dv + (hL + t0) * kD2 + 64 * h, kD2, acc, wm, wn, lane, nq);
+    {  // dv_j += sum_i p_ij dout_i, j in the diagonal block, both column halves
+        Acc acc[2];
+        zero(acc[0]);
+        zero(acc[1]);
+        wmma64_sum<true, true, 1, 2>(acc, {tile(PT)}, {tile(D0), tile(D1)}, wm, wn, lane);
+        red_block(dv + (hL + t0) * kD2, kD2, acc[0], wm, wn, lane, nq);
+        red_block(dv + (hL + t0) * kD2 + 64, kD2, acc[1], wm, wn, lane, nq);
     }
 
     // ---- pass 1: right to left over key blocks, X from Q~_a; key block b in set (a-1-b) % 2
@@ -341,21 +378,27 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
         }
         if (FOX && tid < 64) locj[tid] = loc[(size_t)bh * Lp + (size_t)b * 64 + tid];
         __syncthreads();
-        Acc s, ov, xn0, xn1;
-        zero(s);
+        // sx[0]: x_i . k~_j; sx[1], sx[2]: column halves 0 and 1 of X P_b^T (b > 0); each X
+        // half's fragments serve all three
+        Acc sx[3], ov;
+        zero(sx[0]);
+        zero(sx[1]);
+        zero(sx[2]);
         zero(ov);
-        zero(xn0);
-        zero(xn1);
-        wmma64<false, false>(s, tile(X0), tile(s1(set, K0)), wm, wn, lane);   // x_i . k~_j
-        wmma64<false, false>(s, tile(X1), tile(s1(set, K1)), wm, wn, lane);
+        if (b > 0) {
+            wmma64_sum<false, false, 1, 3>(sx, {tile(X0)},
+                                           {tile(s1(set, K0)), tile(s1(set, P00)), tile(s1(set, P10))},
+                                           wm, wn, lane);
+            wmma64_sum<false, false, 1, 3>(sx, {tile(X1)},
+                                           {tile(s1(set, K1)), tile(s1(set, P01)), tile(s1(set, P11))},
+                                           wm, wn, lane);
+        } else {
+            wmma64<false, false>(sx[0], tile(X0), tile(s1(set, K0)), wm, wn, lane);
+            wmma64<false, false>(sx[0], tile(X1), tile(s1(set, K1)), wm, wn, lane);
+        }
         wmma64<false, false>(ov, tile(D0), tile(s1(set, V0)), wm, wn, lane);  // dout_i . v_j
         wmma64<false, false>(ov, tile(D1), tile(s1(set, V1)), wm, wn, lane);
-        if (b > 0) {  // X P_b^T, column halves 0 and 1
-            wmma64<false, false>(xn0, tile(X0), tile(s1(set, P00)), wm, wn, lane);
-            wmma64<false, false>(xn0, tile(X1), tile(s1(set, P01)), wm, wn, lane);
-            wmma64<false, false>(xn1, tile(X0), tile(s1(set, P10)), wm, wn, lane);
-            wmma64<false, false>(xn1, tile(X1), tile(s1(set, P11)), wm, wn, lane);
-        }
+        Acc &s = sx[0], &xn0 = sx[1], &xn1 = sx[2];
         {
             const float dcb = FOX ? (float)(cb[(size_t)bh * nb + a] - cb[(size_t)bh * nb + b]) : 0.f;
             float cs[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
@@ -400,15 +443,20 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
                     *reinterpret_cast<const uint4 *>(tptr(DT) + (r * SLD + c) * 2);
             }
         }
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-            Acc acc;
-            zero(acc);  // dK~_b[j][c] += sum_i dT_ij X_ic
-            wmma64<true, true>(acc, tile(DT), tile(X0 + h), wm, wn, lane);
-            red_block(dkt + ((size_t)bh * Lp + (size_t)b * 64) * kD2 + 64 * h, kD2, acc, wm, wn, lane, 64);
-            zero(acc);  // dv_j += sum_i p_ij dout_i (key block b < a is full)
-            wmma64<true, true>(acc, tile(PT), tile(D0 + h), wm, wn, lane);
-            red_block(dv + (hL + (size_t)b * 64) * kD2 + 64 * h, kD2, acc, wm, wn, lane, 64);
+        {
+            Acc acc[2];
+            zero(acc[0]);  // dK~_b[j][c] += sum_i dT_ij X_ic, both column halves
+            zero(acc[1]);
+            wmma64_sum<true, true, 1, 2>(acc, {tile(DT)}, {tile(X0), tile(X1)}, wm, wn, lane);
+            float *dk_b = dkt + ((size_t)bh * Lp + (size_t)b * 64) * kD2;
+            red_block(dk_b, kD2, acc[0], wm, wn, lane, 64);
+            red_block(dk_b + 64, kD2, acc[1], wm, wn, lane, 64);
+            zero(acc[0]);  // dv_j += sum_i p_ij dout_i (key block b < a is full)
+            zero(acc[1]);
+            wmma64_sum<true, true, 1, 2>(acc, {tile(PT)}, {tile(D0), tile(D1)}, wm, wn, lane);
+            float *dv_b = dv + (hL + (size_t)b * 64) * kD2;
+            red_block(dv_b, kD2, acc[0], wm, wn, lane, 64);
+            red_block(dv_b + 64, kD2, acc[1], wm, wn, lane, 64);
         }
         __syncthreads();  // X is no longer read: it takes X P_b^T
         if (b > 0) {
@@ -443,31 +491,30 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
         }
         __syncthreads();
         const int xa = s2x(set, 0), xb = s2x(set, 1), dts = s2dt(set);
-        Acc n0, n1;
-        zero(n0);
-        zero(n1);
-        if (b > 0) {  // G_{b-1} P_b, head and tail
-            wmma64<false, true>(n0, tile(G0H), tile(s1(set, P00)), wm, wn, lane);
-            wmma64<false, true>(n0, tile(G1H), tile(s1(set, P10)), wm, wn, lane);
-            wmma64<false, true>(n0, tile(G0L), tile(s1(set, P00)), wm, wn, lane);
-            wmma64<false, true>(n0, tile(G1L), tile(s1(set, P10)), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G0H), tile(s1(set, P01)), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G1H), tile(s1(set, P11)), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G0L), tile(s1(set, P01)), wm, wn, lane);
-            wmma64<false, true>(n1, tile(G1L), tile(s1(set, P11)), wm, wn, lane);
+        Acc nn[2];  // column halves 0 and 1 of G_b
+        zero(nn[0]);
+        zero(nn[1]);
+        if (b > 0) {  // G_{b-1} P_b: each row half of G (head and tail) against its P_b quadrants
+            wmma64_sum<false, true, 2, 2>(nn, {tile(G0H), tile(G0L)},
+                                          {tile(s1(set, P00)), tile(s1(set, P01))}, wm, wn, lane);
+            wmma64_sum<false, true, 2, 2>(nn, {tile(G1H), tile(G1L)},
+                                          {tile(s1(set, P10)), tile(s1(set, P11))}, wm, wn, lane);
         }
-        wmma64<false, true>(n0, tile(dts), tile(s1(set, K0)), wm, wn, lane);  // + dT_ab K~_b
-        wmma64<false, true>(n1, tile(dts), tile(s1(set, K1)), wm, wn, lane);
+        // + dT_ab K~_b
+        wmma64_sum<false, true, 1, 2>(nn, {tile(dts)}, {tile(s1(set, K0)), tile(s1(set, K1))}, wm,
+                                      wn, lane);
+        Acc &n0 = nn[0], &n1 = nn[1];
         if (b > 0) {  // dP_b[n][c] += sum_i G_{b-1}[i][n] X_{a,b}[i][c], four quadrants
             float *dpb = dP + ((size_t)bh * nb + b) * kD2 * kD2;
 #pragma unroll 1
-            for (int qd = 0; qd < 4; ++qd) {
-                const int nh = qd >> 1, ch = qd & 1;
-                Acc acc;
-                zero(acc);
-                wmma64<true, true>(acc, tile(nh ? G1H : G0H), tile(ch ? xb : xa), wm, wn, lane);
-                wmma64<true, true>(acc, tile(nh ? G1L : G0L), tile(ch ? xb : xa), wm, wn, lane);
-                red_block(dpb + (size_t)64 * nh * kD2 + 64 * ch, kD2, acc, wm, wn, lane, 64);
+            for (int nh = 0; nh < 2; ++nh) {  // row half nh of dP_b, both column halves
+                Acc acc[2];
+                zero(acc[0]);
+                zero(acc[1]);
+                wmma64_sum<true, true, 2, 2>(acc, {tile(nh ? G1H : G0H), tile(nh ? G1L : G0L)},
+                                             {tile(xa), tile(xb)}, wm, wn, lane);
+                red_block(dpb + (size_t)64 * nh * kD2, kD2, acc[0], wm, wn, lane, 64);
+                red_block(dpb + (size_t)64 * nh * kD2 + 64, kD2, acc[1], wm, wn, lane, 64);
             }
         }
         __syncthreads();  // G_{b-1} is no longer read
