@@ -472,6 +472,16 @@ def leg_cpu_baselines(wl_bwd, wl_dec, wl_prod, wl_fox=None):
     out["bwd"] = {"value": wl_bwd.B * wl_bwd.L / t, "unit": "tokens/s", "cores": 2,
                   "kind": "oracle", "sample": "2 of %d heads, L %d, one thread per head; "
                   "time extrapolated by head count" % (wl_bwd.B * wl_bwd.H, wl_bwd.L)}
+    # backward at head size 128 (B4 H8 L2048): two whole heads
+    wl_b2 = pi.BF16_L2048_D128
+    x = pi.make_fwd_inputs(1, 2, wl_b2.L, d=128, seed=wl_b2.seed, device="cpu")
+    d_out = torch.randn((1, 2, wl_b2.L, 128), generator=torch.Generator().manual_seed(1))
+    t0 = time.perf_counter()
+    oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out.to(torch.bfloat16))
+    t = (time.perf_counter() - t0) * (wl_b2.B * wl_b2.H) / 2
+    out["bwd_d128"] = {"value": wl_b2.B * wl_b2.L / t, "unit": "tokens/s", "cores": 2,
+                       "kind": "oracle", "sample": "2 of %d heads, L %d, d 128, one thread per "
+                       "head; time extrapolated by head count" % (wl_b2.B * wl_b2.H, wl_b2.L)}
     # decode: one step over 4 heads of the prefix cache
     nh, n0 = 4, wl_dec.n_prefix
     g = torch.Generator().manual_seed(wl_dec.seed)
