@@ -341,3 +341,39 @@ def test_bwd_d128_workload_sampled_heads(lib, fox):
     ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
                           d_out.reshape(-1, L, 128)[heads], log_f=sel.get("log_f"))
     _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
+
+
+def test_bwd_d128_max_heads(lib):
+    # B * H at the 65535 limit (the grid's second dimension), two blocks per head, head
+    # size 128 (tensor-core query pass)
+    B, L = 65535, 65
+    x = pi.make_fwd_inputs(B, 1, L, d=128, seed=3400, dtype=torch.bfloat16, device="cuda")
+    x, d_out, grads = _case128(lib, B, 1, L, torch.bfloat16, seed=3400, x=x)
+    heads = [0, 1, 32767, B - 1]
+    sel = {k: x[k].reshape(-1, *x[k].shape[2:])[heads] for k in ("q", "k", "v", "w", "beta")}
+    ref = oracle.path_bwd(sel["q"], sel["k"], sel["v"], sel["w"], sel["beta"],
+                          d_out.reshape(-1, L, 128)[heads])
+    _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
+
+
+@pytest.mark.parametrize("dtype,fox", [(torch.bfloat16, False), (torch.bfloat16, True),
+                                       (torch.float32, False)])
+def test_bwd_d128_custom_scale(lib, dtype, fox):
+    # a softmax scale other than 1/sqrt(d): the query pass carries dS unscaled and scales
+    # its products on output
+    x = pi.make_fwd_inputs(1, 2, 150, d=128, seed=3500, dtype=dtype, fox=fox, device="cuda")
+    d_out = torch.randn((1, 2, 150, 128), generator=torch.Generator().manual_seed(3501))
+    d_out = d_out.to(dtype).cuda()
+    if fox:
+        out, lse = lib.path_fox_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"],
+                                    scale=0.3)
+        grads = lib.path_fox_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], out,
+                                 lse, d_out, scale=0.3)
+    else:
+        out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], scale=0.3)
+        grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out,
+                                  scale=0.3)
+    torch.cuda.synchronize()
+    ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out, scale=0.3,
+                          log_f=x["log_f"] if fox else None)
+    _compare(grads, ref, TOL[dtype])
