@@ -73,27 +73,84 @@ struct Frag {
     __device__ __forceinline__ int col(int j, int e) const { return n0 + 8 * j + 2 * t + (e & 1); }
 };
 
+// Fragments of the tf32 m16n8k8 MMA from fp32 tiles. A non-transposed operand (A stored
+// [i][k], B stored [j][k]: the contraction index contiguous) is read with ldmatrix: an 8 x 8
+// matrix of 16-bit elements is 8 rows x 4 fp32, and the element a thread receives (row
+// lane / 4, 16-bit columns 2 (lane % 4) and + 1) is exactly fp32 column lane % 4, the tf32
+// fragment's; one ldmatrix.x4 replaces four scalar loads. Transposed operands keep scalar
+// loads (ldmatrix transposes 16-bit elements, not 32-bit ones).
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// Operand fetchers for one k-step (k0) of a warp's 16 x 32 block.
+template <bool TA, bool NEG>
+struct OpA {
+    const float *A;
+    uint32_t lsm;  // ldmatrix row address of this lane (non-transposed)
+    __device__ OpA(const float *A_, const Frag &f) : A(A_) {
+        const int lane = threadIdx.x & 31;
+        lsm = TA ? 0u : smem_u32(A + (f.m0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * LD + 4 * (lane >> 4));
+    }
+    __device__ __forceinline__ void get(int k0, const Frag &f, uint32_t (&a)[4]) const {
+        if constexpr (!TA) {
+            ldsm4(lsm + 4u * (uint32_t)k0, a);
+        } else {
+            const float av[4] = {A[(k0 + f.t) * LD + f.m0 + f.g], A[(k0 + f.t) * LD + f.m0 + f.g + 8],
+                                 A[(k0 + f.t + 4) * LD + f.m0 + f.g],
+                                 A[(k0 + f.t + 4) * LD + f.m0 + f.g + 8]};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = __float_as_uint(av[e]);
+        }
+        if constexpr (NEG) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] ^= 0x80000000u;
+        }
+    }
+};
+template <bool TB>
+struct OpB {
+    const float *B;
+    uint32_t lsm;  // ldmatrix row address of this lane for n-tiles 0 and 1 (non-transposed)
+    __device__ OpB(const float *B_, const Frag &f) : B(B_) {
+        const int lane = threadIdx.x & 31;
+        lsm = TB ? smem_u32(B + (f.n0 + (lane & 7) + 8 * (lane >> 4)) * LD + 4 * ((lane >> 3) & 1)) : 0u;
+    }
+    // b[j] for the four n-tiles j of the block
+    __device__ __forceinline__ void get(int k0, const Frag &f, uint32_t (&b)[4][2]) const {
+        if constexpr (TB) {
+            uint32_t r[4];
+            ldsm4(lsm + 4u * (uint32_t)k0, r);
+            b[0][0] = r[0]; b[0][1] = r[1]; b[1][0] = r[2]; b[1][1] = r[3];
+            ldsm4(lsm + 4u * (uint32_t)(16 * LD + k0), r);
+            b[2][0] = r[0]; b[2][1] = r[1]; b[3][0] = r[2]; b[3][1] = r[3];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = f.n0 + 8 * j + f.g;
+                b[j][0] = __float_as_uint(B[(k0 + f.t) * LD + n]);
+                b[j][1] = __float_as_uint(B[(k0 + f.t + 4) * LD + n]);
+            }
+        }
+    }
+};
+
 // acc += (NEG ? -1 : 1) * opA x opB over K = 64, with opA(i, k) = TA ? A[k][i] : A[i][k] and
 // opB(k, j) = TB ? B[j][k] : B[k][j] (tiles row-major at stride LD). The operands go to the
 // tf32 MMA as their fp32 bits, which it reads truncated to a 10-bit significand.
 template <bool TA, bool TB, bool NEG = false>
 __device__ __forceinline__ void mm(const float *A, const float *B, const Frag &f, Acc &acc) {
-    auto a_at = [&](int i, int k) { return TA ? A[k * LD + i] : A[i * LD + k]; };
-    auto b_at = [&](int k, int j) { return TB ? B[j * LD + k] : B[k * LD + j]; };
+    const OpA<TA, NEG> oa(A, f);
+    const OpB<TB> ob(B, f);
 #pragma unroll 2
     for (int k0 = 0; k0 < 64; k0 += 8) {
-        float av[4] = {a_at(f.m0 + f.g, k0 + f.t), a_at(f.m0 + f.g + 8, k0 + f.t),
-                       a_at(f.m0 + f.g, k0 + f.t + 4), a_at(f.m0 + f.g + 8, k0 + f.t + 4)};
-        uint32_t a[4];
+        uint32_t a[4], b[4][2];
+        oa.get(k0, f, a);
+        ob.get(k0, f, b);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) a[e] = __float_as_uint(NEG ? -av[e] : av[e]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = f.n0 + 8 * j + f.g;
-            const uint32_t b[2] = {__float_as_uint(b_at(k0 + f.t, n)),
-                                   __float_as_uint(b_at(k0 + f.t + 4, n))};
-            mma_tf32(acc[j], a, b);
-        }
+        for (int j = 0; j < 4; ++j) mma_tf32(acc[j], a, b[j]);
     }
 }
 
@@ -102,26 +159,21 @@ __device__ __forceinline__ void mm(const float *A, const float *B, const Frag &f
 template <bool TA1, bool TB1, bool NEG1, bool TA2, bool TB2, bool NEG2>
 __device__ __forceinline__ void mm2(const float *A1, const float *B1, Acc &acc1,
                                     const float *A2, const float *B2, Acc &acc2, const Frag &f) {
-    auto at = [&](const float *M, bool T, int i, int k) { return T ? M[k * LD + i] : M[i * LD + k]; };
+    const OpA<TA1, NEG1> oa1(A1, f);
+    const OpB<TB1> ob1(B1, f);
+    const OpA<TA2, NEG2> oa2(A2, f);
+    const OpB<TB2> ob2(B2, f);
 #pragma unroll 2
     for (int k0 = 0; k0 < 64; k0 += 8) {
-        uint32_t a1[4], a2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = f.m0 + f.g + 8 * (e & 1), kk = k0 + f.t + 4 * (e >> 1);
-            const float x1 = at(A1, TA1, i, kk), x2 = at(A2, TA2, i, kk);
-            a1[e] = __float_as_uint(NEG1 ? -x1 : x1);
-            a2[e] = __float_as_uint(NEG2 ? -x2 : x2);
-        }
+        uint32_t a1[4], a2[4], b1[4][2], b2[4][2];
+        oa1.get(k0, f, a1);
+        oa2.get(k0, f, a2);
+        ob1.get(k0, f, b1);
+        ob2.get(k0, f, b2);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int n = f.n0 + 8 * j + f.g;
-            const uint32_t b1[2] = {__float_as_uint(at(B1, !TB1, n, k0 + f.t)),
-                                    __float_as_uint(at(B1, !TB1, n, k0 + f.t + 4))};
-            const uint32_t b2[2] = {__float_as_uint(at(B2, !TB2, n, k0 + f.t)),
-                                    __float_as_uint(at(B2, !TB2, n, k0 + f.t + 4))};
-            mma_tf32(acc1[j], a1, b1);
-            mma_tf32(acc2[j], a2, b2);
+            mma_tf32(acc1[j], a1, b1[j]);
+            mma_tf32(acc2[j], a2, b2[j]);
         }
     }
 }
