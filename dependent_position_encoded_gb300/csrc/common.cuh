@@ -485,19 +485,28 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// 3-D bf16 map over (heads, rows, 64 columns) with a (1, box_rows, 64) box and 128-byte
+// 3-D 16-bit (bf16 or fp16) map over (heads, rows, 64 columns) with a (1, box_rows, 64) box and 128-byte
 // swizzle (the layout every tcgen05 operand tile here uses). Rows beyond `rows` read 0.
-inline bool make_map_bf16(CUtensorMap *m, const void *ptr, int rows, int heads, int box_rows) {
+inline bool make_map_16bit(CUtensorMap *m, CUtensorMapDataType type, const void *ptr, int rows,
+                           int heads, int box_rows) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)rows * kD * 2};
     cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return enc(m, type, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool make_map_bf16(CUtensorMap *m, const void *ptr, int rows, int heads, int box_rows) {
+    return make_map_16bit(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rows, heads, box_rows);
+}
+
+inline bool make_map_f16(CUtensorMap *m, const void *ptr, int rows, int heads, int box_rows) {
+    return make_map_16bit(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ptr, rows, heads, box_rows);
 }
 
 }  // namespace path

@@ -46,10 +46,10 @@ constexpr int kThreads = 256;
 constexpr uint32_t kT = 8192;  // one 64 x 64 16-bit tile
 
 // Tile slots (from the 1024-aligned base). Q, W, K adjacent (MMA1 A = [Q; W], B = [W; K]);
-// a zero tile after K (B = [K; 0] in the last group); Lq^T and Rk^T adjacent (A = [Lq; Rk]);
-// AT, A adjacent (MMA3 A). U, KhT, V reuse the slots of AT, A and the solve scratch (KhT and
-// V adjacent: B = [Khat^T | V']).
-constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_Z = 3 * kT, T_LQ = 4 * kT,
+// slot 3 stages P_b for its TMA store; Lq^T and Rk^T adjacent (A = [Lq; Rk]), after the last
+// group the staging of the diagonal table and k~; AT, A adjacent (MMA3 A). U, KhT, V reuse the
+// slots of AT, A and the solve scratch; U's slot stages q~ after G1.
+constexpr uint32_t T_Q = 0 * kT, T_W = 1 * kT, T_K = 2 * kT, T_PB = 3 * kT, T_LQ = 4 * kT,
                    T_RKT = 5 * kT, T_AT = 6 * kT, T_A = 7 * kT, T_U = 6 * kT, T_KHT = 7 * kT,
                    T_V = 8 * kT;
 constexpr uint32_t SCR = 6 * kT;           // solve scratch (E/X fp32 + Y) overlays slots 6-8
@@ -146,10 +146,12 @@ template <bool FOX>
 __global__ void __launch_bounds__(kThreads, 3)
 ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ beta,
+                     const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_qt_out,
+                     const __grid_constant__ CUtensorMap tm_kp_out,
+                     const __grid_constant__ CUtensorMap tm_dg_out, const float *__restrict__ beta,
                      const float *__restrict__ log_f, int L, int Lp, int nblk, float scale_log2,
-                     __nv_bfloat16 *__restrict__ qt, __nv_bfloat16 *__restrict__ kp,
-                     __half *__restrict__ dg, float *__restrict__ qn, float *__restrict__ dmax,
+                     float *__restrict__ qn, float *__restrict__ dmax,
                      float *__restrict__ bkmax, double *__restrict__ btot,
                      double *__restrict__ bmin, uint32_t *status, uint64_t limit_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -208,9 +210,6 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         lc[2 * ln] = run - b + a;
         lc[2 * ln + 1] = run;
     }
-    // the zero tile: the rows of B = [K; 0] that pair with the W rows of A = [Q; W]
-    reinterpret_cast<uint4 *>(sm + T_Z)[r] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4 *>(sm + T_Z)[r + kThreads] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
@@ -372,9 +371,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) ok = wait_all(bar_mma, 0);
 
     const size_t blk_base = (size_t)bh * nblk + blk;
-    __nv_bfloat16 *kp_blk = kp + blk_base * (2 * kC) * kD;
-    // FoX partial sums (row norms, table maxima, key norms) in the U slot, free after G1
-    float *const part = reinterpret_cast<float *>(sm + T_U);
+    float qs = 0.f;  // FoX: this thread's half of |q~_i|^2 (the other half goes through bs)
     if (ok) {
         tc_fence_after();
         float x[32];
@@ -383,7 +380,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_row32(tmem + lane_off + 64 + c0, x);
 #pragma unroll
             for (int c = 0; c < 32; ++c) x[c] = (c0 + c == lr ? 1.f : 0.f) - x[c];
-            store_global_half(kp_blk + (kC + lr) * kD + c0, x);
+            store_half16<false>(sm + T_PB, lr, hf, x);  // written by one TMA store below
         } else {
             // q~_i = q_i - (Lq U)_i
             const int i = lr - kC;
@@ -392,40 +389,51 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_row32(tmem + lane_off + c0, x);
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] -= x[c];
-            store_global_half(qt + ((size_t)bh * Lp + t0 + i) * kD + c0, y);
+            store_half16<false>(sm + T_U, i, hf, y);  // q~, written by one TMA store below
             if (FOX) {
-                float qs = 0.f;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const float r16 = __bfloat162float(__float2bfloat16_rn(y[c]));
                     qs = fmaf(r16, r16, qs);
                 }
-                part[(i * 2 + hf) * 2] = qs;
+                if (hf == 1) bs[i] = qs;  // beta is no longer needed
             }
         }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (r == 0 && ok) {
+        tma_store_3d(&tm_kp_out, base + T_PB, 0, 2 * kC * blk + kC, bh);  // P_b
+        tma_store_3d(&tm_qt_out, base + T_U, 0, t0, bh);                  // q~
+    }
+    if (FOX && ok && hf == 0 && lr >= kC)
+        qn[(size_t)bh * Lp + t0 + lr - kC] = sqrtf(qs + bs[lr - kC]);
 
-    // ---- G2: [Q; W] x [K; 0]^T (bf16) - [Lq; Rk] x [Khat^T | V'] (fp16, MN-major): rows i
-    // (0-63) give Q K^T - Lq Khat^T (columns 0-63), rows 64 + j give -Rk V' (columns 64-127);
-    // W is fp16 by now, so the W rows of the first product are unused, like the off-diagonal
-    // blocks
+    // ---- G2: [Q; W] x K^T (bf16, N = 64) - [Lq; Rk] x Khat^T into columns 0-63 and
+    // -[Lq; Rk] x V' into columns 64-127 (fp16, MN-major, N = 64 each): rows i (0-63) give
+    // Q K^T - Lq Khat^T, rows 64 + j give -Rk V'; W is fp16 by now, so the W rows of the first
+    // product are unused, like the off-diagonal blocks
     if (r == 0 && ok) {
         tc_fence_after();
         const uint64_t aq = sdesc_sw128(base + T_Q, 16, 1024);
         const uint64_t bk = sdesc_sw128(base + T_K, 16, 1024);
-        constexpr uint32_t IDQK = idesc16(128, 128, 1, false, false);
+        constexpr uint32_t IDQK = idesc16(128, 64, 1, false, false);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, aq + 2 * kk, bk + 2 * kk, IDQK, kk > 0);
         const uint64_t a = sdesc_sw128(base + T_LQ, T_RKT - T_LQ, 1024);
-        const uint64_t b = sdesc_sw128(base + T_KHT, T_V - T_KHT, 1024);
-        constexpr uint32_t IDN = idesc16(128, 128, 0, true, true, true);
+        const uint64_t bh_ = sdesc_sw128(base + T_KHT, 16, 1024);
+        const uint64_t bv = sdesc_sw128(base + T_V, 16, 1024);
+        constexpr uint32_t IDN = idesc16(128, 64, 0, true, true, true);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 128 * kk, b + 128 * kk, IDN, 1);
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem, a + 128 * kk, bh_ + 128 * kk, IDN, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + 64, a + 128 * kk, bv + 128 * kk, IDN, kk > 0);
     }
     if (r == 0) umma_commit(bar_mma);
     if (ok) ok = wait_all(bar_mma, 1);
+    // FoX partial maxima and key norms in the Q slot, free once G2 has completed
+    float *const part = reinterpret_cast<float *>(sm + T_Q);
     if (ok) {
         tc_fence_after();
         float x[32];
@@ -441,16 +449,12 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (FOX) v += kLog2e * (lci - lc[jj]);
                 x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
             }
-            uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
-                                   pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+            store_half16<true>(sm + T_LQ, i, hf, x);  // the table, written by one TMA store
             if (FOX) {
                 float dm = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) dm = fmaxf(dm, __half2float(__float2half_rn(x[j])));
-                part[(i * 2 + hf) * 2 + 1] = dm;
+                part[i * 2 + hf] = dm;
             }
         } else {
             // k~_j = k_j - (Rk V')_j
@@ -460,7 +464,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_row32(tmem + lane_off + 64 + c0, x);
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] += x[c];
-            store_global_half(kp_blk + j * kD + c0, y);
+            store_half16<false>(sm + T_RKT, j, hf, y);  // k~, written by one TMA store
             if (FOX) {
                 float ks = 0.f;
 #pragma unroll
@@ -473,13 +477,16 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
         }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (r == 0 && ok) {
+        tma_store_3d(&tm_dg_out, base + T_LQ, 0, kC * blk, bh);          // diagonal table
+        tma_store_3d(&tm_kp_out, base + T_RKT, 0, 2 * kC * blk, bh);     // k~
+    }
     if (FOX && ok && hf == 0 && lr < kC) {
-        // (q~, table) row lr: combine the two half-row partials
-        const size_t row = (size_t)bh * Lp + t0 + lr;
-        qn[row] = sqrtf(part[(lr * 2) * 2] + part[(lr * 2 + 1) * 2]);
-        dmax[row] = fmaxf(part[(lr * 2) * 2 + 1], part[(lr * 2 + 1) * 2 + 1]);
+        // table row lr: combine the two half-row partials
+        dmax[(size_t)bh * Lp + t0 + lr] = fmaxf(part[lr * 2], part[lr * 2 + 1]);
     }
     if (FOX && warp == 1) {
         // for the early-exit bounds, in fp64 (off the block's critical path: fp64 is slow
@@ -509,6 +516,7 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) bkmax[blk_base] = m;
     }
+    if (r == 0) bulk_wait_all();  // the stores have read their tiles and written the outputs
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -1039,16 +1047,18 @@ cudaError_t launch_ut_prepare_tc(const void *q, const void *k, const void *w, co
         !make_input_map(&tw, w, L, BH))
         return cudaErrorInvalidValue;
     const bool fox = log_f != nullptr;
+    CUtensorMap tqto, tkpo, tdgo;  // outputs: q~, [k~; P_b] rows and the fp16 table (64-row boxes)
+    if (!make_map_bf16(&tqto, basep + lay.off_qt, lay.Lp, BH, kC) ||
+        !make_map_bf16(&tkpo, basep + lay.off_kp, lay.nblk * 2 * kC, BH, kC) ||
+        !make_map_f16(&tdgo, basep + lay.off_dg, lay.nblk * kC, BH, kC))
+        return cudaErrorInvalidValue;
     auto kern = fox ? ut_prepare_tc_kernel<true> : ut_prepare_tc_kernel<false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     dim3 grid(lay.nblk, BH);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(
-        tq, tk, tw, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
-        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_qt),
-        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_kp),
-        reinterpret_cast<__half *>(basep + lay.off_dg),
+        tq, tk, tw, tqto, tkpo, tdgo, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
         fox ? reinterpret_cast<float *>(basep + lay.off_qn) : nullptr,
         fox ? reinterpret_cast<float *>(basep + lay.off_dmax) : nullptr,
         fox ? reinterpret_cast<float *>(basep + lay.off_bkmax) : nullptr,
