@@ -125,16 +125,6 @@ __device__ __forceinline__ void tmem_row32(uint32_t taddr, float *x) {
     for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(a[j]);
 }
 
-// 32 fp32 values as 64 contiguous bytes of bf16 in global memory.
-__device__ __forceinline__ void store_global_half(__nv_bfloat16 *dst, const float *y) {
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        d[c] = make_uint4(pack_bf16x2(y[8 * c], y[8 * c + 1]), pack_bf16x2(y[8 * c + 2], y[8 * c + 3]),
-                          pack_bf16x2(y[8 * c + 4], y[8 * c + 5]),
-                          pack_bf16x2(y[8 * c + 6], y[8 * c + 7]));
-}
-
 // Thread layout: warp w reads TMEM lanes 32 (w mod 4) .. +31 (the accumulator rows lr) and
 // handles the 32-column half hf = w / 4 of every 64-column block of its row, so each row's
 // epilogue is split between two warps.
@@ -541,13 +531,18 @@ ut_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 // 8 KB slots: 0 Q0 1 W0 2 K0 3 Q1 4 W1 5 K1 (bf16 inputs, [Q;W;K] per column half so that
 // [Q;W] and [W;K] are contiguous in each half); 6 Wh0 7 Wh1 8 Rk^T (fp16, MMA3's B at an 8 KB
 // stride); 9 Lq; 10-12 the solve scratch, then A^T, A; after MMA3: U0 = 10, U1 = 11,
-// Khat^T = 12, V'0 = 1, V'1 = 4 (W's bf16 halves are dead after MMA1).
+// Khat^T = 12, V'0 = 1, V'1 = 4 (W's bf16 halves are dead after MMA1). The outputs are staged
+// in dead slots and written by TMA stores: after MMA4x q~ in 10, 11 and the table in 9; after
+// MMA4y P_b in 0, 1 (rows 0-63) and 3, 4 (rows 64-127), k~ in 6, 7 (column halves).
 constexpr uint32_t k2Slots = 13;
 constexpr uint32_t P2_Q0 = 0 * kT, P2_W0 = 1 * kT, P2_K0 = 2 * kT, P2_Q1 = 3 * kT, P2_W1 = 4 * kT,
                    P2_K1 = 5 * kT, P2_WH0 = 6 * kT, P2_WH1 = 7 * kT, P2_RKT = 8 * kT,
                    P2_LQ = 9 * kT, P2_SCR = 10 * kT, P2_AT = 10 * kT, P2_A = 11 * kT,
                    P2_U0 = 10 * kT, P2_U1 = 11 * kT, P2_KHT = 12 * kT, P2_V0 = 1 * kT,
                    P2_V1 = 4 * kT;
+constexpr uint32_t P2_OQ0 = 10 * kT, P2_OQ1 = 11 * kT, P2_ODG = 9 * kT, P2_OP00 = 0 * kT,
+                   P2_OP01 = 1 * kT, P2_OP10 = 3 * kT, P2_OP11 = 4 * kT, P2_OK0 = 6 * kT,
+                   P2_OK1 = 7 * kT;
 constexpr uint32_t P2_Y = P2_SCR + 64 * XLD * 4;
 constexpr uint32_t P2_BAR = k2Slots * kT, P2_SLOT = P2_BAR + 16, P2_BETA = P2_SLOT + 16,
                    P2_LC = P2_BETA + 256;
@@ -566,11 +561,12 @@ template <bool FOX>
 __global__ void __launch_bounds__(kThreads, 2)
 ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_w, const float *__restrict__ beta,
+                        const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_qt_out,
+                        const __grid_constant__ CUtensorMap tm_kp_out,
+                        const __grid_constant__ CUtensorMap tm_dg_out, const float *__restrict__ beta,
                         const float *__restrict__ log_f, int L, int Lp, int nblk,
-                        float scale_log2, __nv_bfloat16 *__restrict__ qt,
-                        __nv_bfloat16 *__restrict__ kp, __half *__restrict__ dg,
-                        float *__restrict__ lc2, float *__restrict__ tail2,
+                        float scale_log2, float *__restrict__ lc2, float *__restrict__ tail2,
                         double *__restrict__ tot2, float *__restrict__ qn,
                         float *__restrict__ dmax, float *__restrict__ bkmax,
                         double *__restrict__ btot, double *__restrict__ bmin, uint32_t *status,
@@ -829,7 +825,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) ok = wait_all(bar_mma, 0);
 
     const size_t blk_base = (size_t)bh * nblk + blk;
-    __nv_bfloat16 *kp_blk = kp + blk_base * (kC + 128) * 128;
+    const int kp_row = (kC + 128) * blk;  // first [k~; P_b] row of the block in its head
     if (ok && lr < kC) {
         tc_fence_after();
         const int i = lr;
@@ -843,7 +839,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_row32(tmem + lane_off + 64 * hf + 32 * h2, x);
 #pragma unroll
             for (int c = 0; c < 32; ++c) y[c] -= x[c];
-            store_global_half(qt + ((size_t)bh * Lp + t0 + i) * 128 + 64 * hf + 32 * h2, y);
+            store_half16<false>(sm + (hf ? P2_OQ1 : P2_OQ0), i, h2, y);
             if (FOX) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -863,11 +859,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (FOX) v += kLog2e * (lci - lc[jj]);
             x[j] = (jj <= i && t0 + jj < L) ? v : -INFINITY;
         }
-        uint4 *dd = reinterpret_cast<uint4 *>(dg + (blk_base * kC + i) * kC + c0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            dd[c] = make_uint4(pack_h2(x[8 * c], x[8 * c + 1]), pack_h2(x[8 * c + 2], x[8 * c + 3]),
-                               pack_h2(x[8 * c + 4], x[8 * c + 5]), pack_h2(x[8 * c + 6], x[8 * c + 7]));
+        store_half16<true>(sm + P2_ODG, i, hf, x);
         if (FOX) {
             float dm = -INFINITY;
 #pragma unroll
@@ -875,8 +867,14 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
             part[128 + i * 2 + hf] = dm;
         }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (r == 0 && ok) {
+        tma_store_3d(&tm_qt_out, base + P2_OQ0, 0, t0, bh);
+        tma_store_3d(&tm_qt_out, base + P2_OQ1, 64, t0, bh);
+        tma_store_3d(&tm_dg_out, base + P2_ODG, 0, kC * blk, bh);
+    }
     if (FOX && ok && hf == 0 && lr < kC) {
         // (q~, table) row lr: combine the two half-row partials
         const size_t row = (size_t)bh * Lp + t0 + lr;
@@ -909,7 +907,8 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_row32(tmem + lane_off + cb, x);
 #pragma unroll
             for (int c = 0; c < 32; ++c) x[c] = (cb + c == lr ? 1.f : 0.f) - x[c];
-            store_global_half(kp_blk + (size_t)(kC + lr) * 128 + cb, x);
+            uint8_t *pt = sm + (lr < kC ? (hf ? P2_OP01 : P2_OP00) : (hf ? P2_OP11 : P2_OP10));
+            store_half16<false>(pt, lr & (kC - 1), h2, x);
         }
         if (lr < kC) {
             // k~_j = k_j - (Rk V')_j
@@ -923,7 +922,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tmem_row32(tmem + lane_off + 128 + 64 * hf + 32 * h2, x);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) y[c] -= x[c];
-                store_global_half(kp_blk + (size_t)j * 128 + 64 * hf + 32 * h2, y);
+                store_half16<false>(sm + (hf ? P2_OK1 : P2_OK0), j, h2, y);
                 if (FOX) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -936,8 +935,17 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (FOX) part[256 + j * 2 + hf] = (t0 + j < L) ? ks : 0.f;
         }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (r == 0 && ok) {
+        tma_store_3d(&tm_kp_out, base + P2_OK0, 0, kp_row, bh);
+        tma_store_3d(&tm_kp_out, base + P2_OK1, 64, kp_row, bh);
+        tma_store_3d(&tm_kp_out, base + P2_OP00, 0, kp_row + kC, bh);
+        tma_store_3d(&tm_kp_out, base + P2_OP01, 64, kp_row + kC, bh);
+        tma_store_3d(&tm_kp_out, base + P2_OP10, 0, kp_row + 2 * kC, bh);
+        tma_store_3d(&tm_kp_out, base + P2_OP11, 64, kp_row + 2 * kC, bh);
+    }
     if (FOX && ok && warp == 2) {
         // largest |k~_j| of the block: lane l takes rows l and l + 32
         const float *kpart = part + 256;
@@ -947,6 +955,7 @@ ut_prepare_tc128_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) bkmax[blk_base] = m;
     }
+    if (r == 0) bulk_wait_all();  // the stores have read their tiles and written the outputs
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -988,7 +997,8 @@ bool make_input_map(CUtensorMap *m, const void *ptr, int L, int heads) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// (heads, L rows, 128 columns) bf16 input, (64 columns, 64 rows) boxes, 128-byte swizzle.
+// (heads, L rows, 128 columns) bf16, (64 columns, 64 rows) boxes, 128-byte swizzle (the
+// inputs, and q~ and [k~; P_b] with their row counts in place of L).
 bool make_input_map128(CUtensorMap *m, const void *ptr, int L, int heads) {
     EncodeTiled enc = encode_fn();
     if (!enc) return false;
@@ -1012,19 +1022,19 @@ cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
     const bool fox = log_f != nullptr;
     const D128TcLayout lay = d128_tc_layout(1, BH, L, fox);
     char *basep = static_cast<char *>(ws);
-    CUtensorMap tq, tk, tw;
+    CUtensorMap tq, tk, tw, tqto, tkpo, tdgo;
     if (!make_input_map128(&tq, q, L, BH) || !make_input_map128(&tk, k, L, BH) ||
-        !make_input_map128(&tw, w, L, BH))
+        !make_input_map128(&tw, w, L, BH) ||
+        !make_input_map128(&tqto, basep + lay.off_qt, lay.Lp, BH) ||
+        !make_input_map128(&tkpo, basep + lay.off_kp, lay.nblk * (kC + 128), BH) ||
+        !make_map_f16(&tdgo, basep + lay.off_dg, lay.nblk * kC, BH, kC))
         return cudaErrorInvalidValue;
     auto kern = fox ? ut_prepare_tc128_kernel<true> : ut_prepare_tc128_kernel<false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)k2SmemBytes);
     if (err != cudaSuccess) return err;
     kern<<<dim3(lay.nblk, BH), kThreads, k2SmemBytes, stream>>>(
-        tq, tk, tw, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
-        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_qt),
-        reinterpret_cast<__nv_bfloat16 *>(basep + lay.off_kp),
-        reinterpret_cast<__half *>(basep + lay.off_dg),
+        tq, tk, tw, tqto, tkpo, tdgo, beta, log_f, L, lay.Lp, lay.nblk, scale * kLog2e,
         fox ? reinterpret_cast<float *>(basep + lay.off_lc2) : nullptr,
         fox ? reinterpret_cast<float *>(basep + lay.off_tail2) : nullptr,
         fox ? reinterpret_cast<double *>(basep + lay.off_tot2) : nullptr,
