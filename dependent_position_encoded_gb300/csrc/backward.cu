@@ -373,8 +373,8 @@ __device__ __forceinline__ void dot8(const float (&x)[kNS][NE], const float (&w)
 }
 
 // Workspace inputs (fp32): dqt, dkt (BH, Lp, D), dP (BH, nblk, D, D), dTd (BH, nblk, 64, 64).
-// w and k stay in shared memory in their input type (exact), so that at d = 128 bf16 inputs
-// fit two CTAs per SM.
+// w and k stay in shared memory in their input type (exact). Built for fp32 inputs; bf16
+// inputs take the matrix-form block passes of backward_block_mm.cu.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, (D == 64 || sizeof(T) == 2) ? 2 : 1)
 bwd_block_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ w,
@@ -705,7 +705,7 @@ BwdLayout bwd_layout(int B, int H, int L, bool fox) {
 
 size_t bwd_query_smem() { return (size_t)(5 * BUF + 4 * kC) * sizeof(float); }
 
-// The token-level block pass at head size D (64 or 128): dq, dk, dw (BH, L, D) and dbeta
+// The token-level block pass (fp32 inputs) at head size D (64 or 128): dq, dk, dw (BH, L, D) and dbeta
 // (BH, L) fp32 from dqt, dkt (BH, Lp, D), dP (BH, nblk, D, D) and the diagonal dT
 // (BH, nblk, 64, 64).
 template <typename T>
@@ -799,16 +799,11 @@ cudaError_t launch_bwd_fox_dlogf(const float *rsum, const float *csum, int BH, i
                                             int, float, float *, float *, float *, float *,     \
                                             float *, float *, void *, cudaStream_t);
 PATH_BWD_INST(float)
-PATH_BWD_INST(__nv_bfloat16)
 #undef PATH_BWD_INST
 template cudaError_t launch_bwd_block_sweep<float>(const void *, const void *, const void *,
                                                    const float *, const float *, const float *,
                                                    const float *, const float *, float *, float *,
                                                    float *, float *, int, int, int, int, int,
                                                    cudaStream_t);
-template cudaError_t launch_bwd_block_sweep<__nv_bfloat16>(
-    const void *, const void *, const void *, const float *, const float *, const float *,
-    const float *, const float *, float *, float *, float *, float *, int, int, int, int, int,
-    cudaStream_t);
 
 }  // namespace path

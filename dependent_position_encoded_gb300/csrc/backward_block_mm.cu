@@ -195,52 +195,74 @@ __device__ __forceinline__ void get(const float *tile, const Frag &f, Acc &acc) 
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[j][e] = tile[f.row(e) * LD + f.col(j, e)];
 }
-// rows r < nvalid of a (64-row) global fp32 tensor, row-major at 64 floats per row
-__device__ __forceinline__ void store_rows(float *dst, const Acc &acc, const Frag &f, int nvalid) {
+// rows r < nvalid of a (64-row) global fp32 block, row-major at ld floats per row
+__device__ __forceinline__ void store_rows(float *dst, const Acc &acc, const Frag &f, int nvalid,
+                                           int ld = kD) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {
             const int r = f.row(e);
             if (r < nvalid)
-                *reinterpret_cast<float2 *>(dst + (size_t)r * kD + f.col(j, e)) =
+                *reinterpret_cast<float2 *>(dst + (size_t)r * ld + f.col(j, e)) =
                     make_float2(acc[j][e], acc[j][e + 1]);
         }
 }
+// acc = the same positions read back (zero at rows r >= nvalid)
+__device__ __forceinline__ void load_rows(const float *src, Acc &acc, const Frag &f, int nvalid,
+                                          int ld) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            const int r = f.row(e);
+            const float2 v = r < nvalid
+                                 ? *reinterpret_cast<const float2 *>(src + (size_t)r * ld + f.col(j, e))
+                                 : make_float2(0.f, 0.f);
+            acc[j][e] = v.x;
+            acc[j][e + 1] = v.y;
+        }
+}
 
-// 64 x 64 fp32 tile from 64 rows of global memory at stride 64 floats, zero past nvalid or
+// 64 x 64 fp32 tile from 64 rows of global memory at stride ld floats, zero past nvalid or
 // everywhere if !use: asynchronous 16-byte copies (zero-filled where not used), waited for
 // by cp_async_wait
-__device__ __forceinline__ void load_tile_async(float *tile, const float *src, int nvalid, bool use) {
+__device__ __forceinline__ void load_tile_async(float *tile, const float *src, int nvalid, bool use,
+                                                int ld = kD) {
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int e = threadIdx.x + it * kThreads, r = e >> 4, c = (e & 15) * 4;
         const bool in = use && r < nvalid;
         const uint32_t dst = smem_u32(tile + r * LD + c);
-        const float *g = in ? src + (size_t)r * kD + c : src;
+        const float *g = in ? src + (size_t)r * ld + c : src;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(g),
                      "r"(in ? 16 : 0)
                      : "memory");
     }
 }
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
-// Three bf16 64 x 64 tiles (rows of (.., L, 64) tensors, zero past nvalid) as fp32: every
-// load is issued before the first conversion
-__device__ __forceinline__ void load_bf16_tiles(float *const (&dst)[3],
-                                                const __nv_bfloat16 *const (&src)[3], int nvalid) {
-    uint2 u[3][4];
+// N bf16 64 x 64 tiles (rows of bf16 tensors at ld elements per row, zero past nvalid) as
+// fp32: every load is issued before the first conversion
+template <int N>
+__device__ __forceinline__ void load_bf16_tiles(float *const (&dst)[N],
+                                                const __nv_bfloat16 *const (&src)[N], int nvalid,
+                                                int ld = kD) {
+    uint2 u[N][4];
 #pragma unroll
-    for (int m = 0; m < 3; ++m)
+    for (int m = 0; m < N; ++m)
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
             const int e = threadIdx.x + it * kThreads, r = e >> 4, c = (e & 15) * 4;
-            u[m][it] = r < nvalid ? *reinterpret_cast<const uint2 *>(src[m] + (size_t)r * kD + c)
+            u[m][it] = r < nvalid ? *reinterpret_cast<const uint2 *>(src[m] + (size_t)r * ld + c)
                                   : make_uint2(0u, 0u);
         }
 #pragma unroll
-    for (int m = 0; m < 3; ++m)
+    for (int m = 0; m < N; ++m)
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
             const int e = threadIdx.x + it * kThreads, r = e >> 4, c = (e & 15) * 4;
@@ -442,6 +464,250 @@ bwd_block_mm_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__
     if (tid < nvalid) dbeta[hL + t0 + tid] = dbs[tid];
 }
 
+// Head size 128: the same gradient with every d-side matrix (W, Q, K, dq~, dk~, U, V, dU,
+// dV and the outputs) as two 64-column halves h and dP_b as four 64 x 64 quadrants dP[h'][h]
+// (rows h', columns h). G, Lq, Rk, dLq, dRk and dA sum their contractions over both halves;
+//     dV_h = -Rk^T dk~_h - sum_h' W_h' dP[h'][h],     dw_h' -= V_h dP[h'][h]^T for each h,
+// and every other d-side product is one per half. Twelve fp32 tiles as in head size 64: W's
+// halves, dT, X, A, Lq and Rk stay resident while q, k, dq~, dk~ and the dP quadrants stream
+// through the others; dw's halves accumulate in registers, dq and dk are formed last.
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_block_mm128_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                       const __nv_bfloat16 *__restrict__ w, const float *__restrict__ beta,
+                       const float *__restrict__ dqt, const float *__restrict__ dkt,
+                       const float *__restrict__ dP, const float *__restrict__ dTd,
+                       float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dw,
+                       float *__restrict__ dbeta, int L, int Lp, int nblk) {
+    constexpr int D = 128;
+    extern __shared__ __align__(16) float sm[];
+    float *S[kTiles];
+#pragma unroll
+    for (int i = 0; i < kTiles; ++i) S[i] = sm + i * (kTile / 4);
+    float *const Ys = sm + kYOff / 4;
+    float *const bs = sm + kBetaOff / 4;
+    float *const dbs = bs + 64;
+
+    const int tid = threadIdx.x;
+    const int blk = blockIdx.x, bh = blockIdx.y;
+    const int t0 = blk * kC;
+    const size_t hL = (size_t)bh * L;
+    const int nvalid = min(kC, L - t0);
+    const bool last = blk == nblk - 1;
+    const Frag f;
+    const __nv_bfloat16 *const qr = q + (hL + t0) * D, *const kr = k + (hL + t0) * D,
+                               *const wr = w + (hL + t0) * D;
+    const float *const dqr = dqt + ((size_t)bh * Lp + t0) * D;
+    const float *const dkr = dkt + ((size_t)bh * Lp + t0) * D;
+
+    // tiles: 0, 1 W's halves, 2 dT, 5 E then X, 6 Lq, 7 Rk, 8 A; 3, 4, 9, 10, 11 stream
+    float *const W0 = S[0], *const W1 = S[1], *const dT = S[2];
+    load_tile_async(dT, dTd + ((size_t)bh * nblk + blk) * kC * kC, nvalid, true);
+    {
+        float *const d1[3] = {W0, W1, S[3]};
+        const __nv_bfloat16 *const s1[3] = {wr, wr + 64, qr};
+        load_bf16_tiles(d1, s1, nvalid, D);
+        float *const d2[3] = {S[9], S[4], S[10]};
+        const __nv_bfloat16 *const s2[3] = {qr + 64, kr, kr + 64};
+        load_bf16_tiles(d2, s2, nvalid, D);
+    }
+    cp_async_wait();
+    if (tid < kC) {
+        bs[tid] = tid < nvalid ? beta[hL + t0 + tid] : 0.f;
+        dbs[tid] = 0.f;
+    }
+    __syncthreads();
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        if (c > r) dT[r * LD + c] = 0.f;
+    }
+
+    Acc a0, a1, a2;
+    // ---- G = W W^T, Lq = tril(Q W^T), Rk = striu(K W^T), each over both halves
+    zero(a0);
+    zero(a1);
+    zero(a2);
+    mm2<false, true, false, false, true, false>(W0, W0, a0, S[3], W0, a1, f);
+    mm2<false, true, false, false, true, false>(W1, W1, a0, S[9], W1, a1, f);
+    mm<false, true>(S[4], W0, f, a2);
+    mm<false, true>(S[10], W1, f, a2);
+    put(S[5], a0, f, [](int, int) { return true; });
+    put(S[6], a1, f, [](int r, int c) { return c <= r; });
+    put(S[7], a2, f, [](int r, int c) { return c > r; });
+    __syncthreads();
+    // dq~ and dk~ halves stream in under the inverse (the q and k tiles are dead)
+    load_tile_async(S[3], dqr, nvalid, true, D);
+    load_tile_async(S[9], dqr + 64, nvalid, true, D);
+    load_tile_async(S[4], dkr, nvalid, !last, D);
+    load_tile_async(S[10], dkr + 64, nvalid, !last, D);
+    cp_async_commit();
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        S[5][r * LD + c] = c > r ? bs[r] * S[5][r * LD + c] : 0.f;
+    }
+    __syncthreads();
+    // ---- X = (I + E)^{-1} in place (tile 5), A = X D (tile 8)
+    blocked_unit_upper_inverse(S[5], Ys, tid);
+    float *const X = S[5], *const A = S[8], *const Lq = S[6], *const Rk = S[7];
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        A[r * LD + c] = X[r * LD + c] * bs[c];
+    }
+    cp_async_wait();
+    __syncthreads();
+
+    Acc dLq, dRk, dA, dW0, dW1;
+    zero(dLq);
+    zero(dRk);
+    zero(dA);
+    zero(dW0);
+    zero(dW1);
+    float *const Ut = S[11];  // U_h, dU_h, V_h, dV_h in turn
+    // ---- per half: U_h = A^T W_h; dLq -= dq~_h U_h^T; dU_h = -Lq^T dq~_h;
+    //      dA += W_h dU_h^T; dw_h += A dU_h
+    auto qside = [&](const float *Wh, const float *dqh, Acc &dWh) {
+        zero(a0);
+        mm<true, false>(A, Wh, f, a0);
+        put(Ut, a0, f, [](int, int) { return true; });
+        __syncthreads();
+        zero(a0);
+        mm2<false, true, true, true, false, true>(dqh, Ut, dLq, Lq, dqh, a0, f);
+        __syncthreads();
+        put(Ut, a0, f, [](int, int) { return true; });
+        __syncthreads();
+        mm2<false, true, false, false, false, false>(Wh, Ut, dA, A, Ut, dWh, f);
+        __syncthreads();
+    };
+    qside(W0, S[3], dW0);
+    qside(W1, S[9], dW1);
+    // ---- per half: V_h = A W_h; dRk -= dk~_h V_h^T; dV_h = -Rk^T dk~_h - sum_h' W_h' dP[h'][h];
+    //      dw_h' -= V_h dP[h'][h]^T; dA += dV_h W_h^T; dw_h += A^T dV_h
+    const float *const dPb = dP + ((size_t)bh * nblk + blk) * D * D;
+    const bool useP = blk > 0 && !last;  // P_0 and the last P_b reach no logit
+    auto kside = [&](int h, const float *Wh, const float *dkh, Acc &dWh) {
+        load_tile_async(S[3], dPb + 64 * h, kC, useP, D);           // dP[0][h]
+        load_tile_async(S[9], dPb + 64 * D + 64 * h, kC, useP, D);  // dP[1][h]
+        cp_async_commit();
+        zero(a0);
+        mm<false, false>(A, Wh, f, a0);
+        put(Ut, a0, f, [](int, int) { return true; });
+        cp_async_wait();
+        __syncthreads();
+        zero(a1);
+        mm2<false, true, true, true, false, true>(dkh, Ut, dRk, Rk, dkh, a1, f);
+        mm<false, false, true>(W0, S[3], f, a1);
+        mm<false, false, true>(W1, S[9], f, a1);
+        mm2<false, true, true, false, true, true>(Ut, S[3], dW0, Ut, S[9], dW1, f);
+        __syncthreads();
+        put(Ut, a1, f, [](int, int) { return true; });
+        __syncthreads();
+        mm2<false, true, false, true, false, false>(Ut, Wh, dA, A, Ut, dWh, f);
+        __syncthreads();
+    };
+    kside(0, W0, S[4], dW0);
+    kside(1, W1, S[10], dW1);
+    // ---- with dT: dY = -dT Rk (tile 3), Y = Lq A^T (tile 9); dRk -= dT^T Y; dLq += dY A;
+    //      dA += dY^T Lq
+    zero(a0);
+    zero(a1);
+    mm2<false, false, true, false, true, false>(dT, Rk, a0, Lq, A, a1, f);
+    put(S[3], a0, f, [](int, int) { return true; });
+    put(S[9], a1, f, [](int, int) { return true; });
+    __syncthreads();
+    mm2<true, false, true, false, false, false>(dT, S[9], dRk, S[3], A, dLq, f);
+    mm<true, false>(S[3], Lq, f, dA);
+    __syncthreads();
+    // ---- dLq = tril (tile 3), dRk = striu (tile 9); q and k again (tiles 6, 7, 4, 10: Lq,
+    //      Rk and dk~ are dead); per half dq_h = dq~_h + dT K_h + dLq W_h,
+    //      dk_h = dk~_h + dT^T Q_h + dRk W_h, dw_h += dLq^T Q_h + dRk^T K_h
+    put(S[3], dLq, f, [](int r, int c) { return c <= r; });
+    put(S[9], dRk, f, [](int r, int c) { return c > r; });
+    {
+        float *const d1[2] = {S[6], S[7]};
+        const __nv_bfloat16 *const s1[2] = {qr, kr};
+        load_bf16_tiles(d1, s1, nvalid, D);
+        float *const d2[2] = {S[4], S[10]};
+        const __nv_bfloat16 *const s2[2] = {qr + 64, kr + 64};
+        load_bf16_tiles(d2, s2, nvalid, D);
+    }
+    __syncthreads();
+    auto outs = [&](int h, const float *Wh, const float *Qh, const float *Kh, Acc &dWh) {
+        load_rows(dqr + 64 * h, a0, f, nvalid, D);
+        load_rows(dkr + 64 * h, a1, f, last ? 0 : nvalid, D);
+        mm2<false, false, false, true, false, false>(dT, Kh, a0, dT, Qh, a1, f);
+        mm2<false, false, false, false, false, false>(S[3], Wh, a0, S[9], Wh, a1, f);
+        mm<true, false>(S[3], Qh, f, dWh);
+        mm<true, false>(S[9], Kh, f, dWh);
+        store_rows(dq + (hL + t0) * D + 64 * h, a0, f, nvalid, D);
+        store_rows(dk + (hL + t0) * D + 64 * h, a1, f, nvalid, D);
+    };
+    outs(0, W0, S[6], S[7], dW0);
+    outs(1, W1, S[4], S[10], dW1);
+    // ---- A = X D: dbeta_u += sum_s dA_su X_su, dX = dA D (tile 11)
+    {
+        float cs[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cs[j][0] = cs[j][1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = f.row(e), c = f.col(j, e);
+                cs[j][e & 1] = fmaf(dA[j][e], X[r * LD + c], cs[j][e & 1]);
+                dA[j][e] *= bs[c];
+            }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v = cs[j][h];
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (f.g == 0) atomicAdd(&dbs[f.n0 + 8 * j + 2 * f.t + h], v);
+            }
+    }
+    put(Ut, dA, f, [](int, int) { return true; });
+    __syncthreads();  // also: tiles 3 and 9 (dLq, dRk) are no longer read
+    // ---- dTT = -X^T dX X^T (P1 = X^T dX in tile 3); G again
+    zero(a0);
+    mm<true, false>(X, Ut, f, a0);
+    put(S[3], a0, f, [](int, int) { return true; });
+    __syncthreads();
+    zero(a1);
+    zero(a2);
+    mm2<false, true, true, false, true, false>(S[3], X, a1, W0, W0, a2, f);
+    mm<false, true>(W1, W1, f, a2);
+    // ---- T = I + D strictly-upper(G): dbeta_s += sum_{v>s} dTT_sv G_sv, dG = D su(dTT)
+    {
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = f.row(e), c = f.col(j, e);
+                const bool up = c > r;
+                rs[e >> 1] = fmaf(up ? a1[j][e] : 0.f, a2[j][e], rs[e >> 1]);
+                a1[j][e] = up ? bs[r] * a1[j][e] : 0.f;
+            }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v = rs[h];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (f.t == 0) atomicAdd(&dbs[f.m0 + f.g + 8 * h], v);
+        }
+    }
+    put(S[9], a1, f, [](int, int) { return true; });  // dG
+    __syncthreads();
+    // dw_h += (dG + dG^T) W_h
+    mm<false, false>(S[9], W0, f, dW0);
+    mm<true, false>(S[9], W0, f, dW0);
+    mm<false, false>(S[9], W1, f, dW1);
+    mm<true, false>(S[9], W1, f, dW1);
+    store_rows(dw + (hL + t0) * D, dW0, f, nvalid, D);
+    store_rows(dw + (hL + t0) * D + 64, dW1, f, nvalid, D);
+    if (tid < nvalid) dbeta[hL + t0 + tid] = dbs[tid];
+}
+
 }  // namespace
 
 // The block pass for bf16 inputs: dq, dk, dw (B, H, L, 64) and dbeta (B, H, L), fp32, from
@@ -455,6 +721,24 @@ cudaError_t launch_bwd_block_mm(const void *q, const void *k, const void *w, con
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     bwd_block_mm_kernel<<<dim3(nblk, BH), kThreads, kSmem, stream>>>(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(w), beta, dqt, dkt, dP, dTd, dq, dk, dw, dbeta, L, Lp,
+        nblk);
+    return cudaGetLastError();
+}
+
+// The block pass for bf16 inputs at head size 128: dq, dk, dw (B, H, L, 128) and dbeta
+// (B, H, L), fp32, from dq~, dk~ (BH, Lp, 128), dP (BH, nblk, 128, 128) and the diagonal dT
+// (BH, nblk, 64, 64).
+cudaError_t launch_bwd_block_mm128(const void *q, const void *k, const void *w, const float *beta,
+                                   const float *dqt, const float *dkt, const float *dP,
+                                   const float *dTd, float *dq, float *dk, float *dw,
+                                   float *dbeta, int BH, int L, int Lp, int nblk,
+                                   cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_block_mm128_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    bwd_block_mm128_kernel<<<dim3(nblk, BH), kThreads, kSmem, stream>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
         static_cast<const __nv_bfloat16 *>(w), beta, dqt, dkt, dP, dTd, dq, dk, dw, dbeta, L, Lp,
         nblk);

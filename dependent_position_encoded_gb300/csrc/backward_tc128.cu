@@ -19,9 +19,9 @@
 // Precision follows the d = 64 tensor-core pass: bf16 operands (the bf16 preparation's
 // factors, the carried rows rounded to bf16 at every key block and stashed so, p and dT
 // rounded to bf16), fp32 accumulation, and G kept in fp32 and fed to its recursion as a bf16
-// head and tail (G = G_hi + G_lo, about 16 significant bits). The block pass (the
-// token-level sweep of backward.cu at d = 128) then takes dq~, dk~, dP_b and the diagonal dT
-// to q, k, w and beta.
+// head and tail (G = G_hi + G_lo, about 16 significant bits). The block pass in matrix form
+// (backward_block_mm.cu at d = 128) then takes dq~, dk~, dP_b and the diagonal dT to q, k, w
+// and beta.
 #include "common.cuh"
 
 namespace path {
@@ -30,11 +30,10 @@ cudaError_t launch_ut_prepare_tc128(const void *q, const void *k, const void *w,
                                     const float *beta, const float *log_f, int BH, int L,
                                     float scale, void *ws, uint64_t limit_ns,
                                     cudaStream_t stream);
-template <typename T>
-cudaError_t launch_bwd_block_sweep(const void *q, const void *k, const void *w, const float *beta,
+cudaError_t launch_bwd_block_mm128(const void *q, const void *k, const void *w, const float *beta,
                                    const float *dqt, const float *dkt, const float *dP,
                                    const float *dTd, float *dq, float *dk, float *dw,
-                                   float *dbeta, int BH, int L, int Lp, int nblk, int D,
+                                   float *dbeta, int BH, int L, int Lp, int nblk,
                                    cudaStream_t stream);
 cudaError_t launch_bwd_fox_sums(const float *log_f, int BH, int L, int Lp, int nblk, float *loc,
                                 double *cb, cudaStream_t stream);
@@ -658,8 +657,8 @@ cudaError_t launch_path_bwd128_tc(const void *q, const void *k, const void *v, c
         reinterpret_cast<__nv_bfloat16 *>(base + y.off_stash), dv, L, Lp, nb, y.f.nblk, y.f.Lp,
         scale, scale * kLog2e, loc, cb, rs, cs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_bwd_block_sweep<__nv_bfloat16>(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw,
-                                                   dbeta, BH, L, Lp, nb, kD2, stream)) != cudaSuccess)
+    if ((e = launch_bwd_block_mm128(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, BH, L,
+                                    Lp, nb, stream)) != cudaSuccess)
         return e;
     if (fox) e = launch_bwd_fox_dlogf(rs, cs, BH, L, Lp, dlogf, stream);
     return e;

@@ -140,11 +140,13 @@ def test_fox_bwd_workload_sampled_heads(lib):
     _compare(grads, ref, TOL[torch.bfloat16], heads=heads)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("kind", ["projection", "reflection", "identity"])
-def test_bwd_degenerate_transitions(lib, kind):
-    # beta = 1: every H_s is a projection (singular; the block pass undoes its steps from
-    # the recorded w . x and never inverts H_s); beta = 2: exact reflections; w = 0: H = I
-    x = pi.make_fwd_inputs(1, 2, 200, seed=31, dtype=torch.float32, clip=0.0, device="cuda")
+def test_bwd_degenerate_transitions(lib, kind, dtype):
+    # beta = 1: every H_s is a projection (singular; the fp32 block pass undoes its steps
+    # from the recorded w . x and never inverts H_s, the bf16 one inverts only the unit
+    # triangular I + D strictly-upper(W W^T)); beta = 2: exact reflections; w = 0: H = I
+    x = pi.make_fwd_inputs(1, 2, 200, seed=31, dtype=dtype, clip=0.0, device="cuda")
     if kind == "projection":
         x["beta"] = torch.ones_like(x["beta"])
     elif kind == "reflection":
@@ -152,14 +154,14 @@ def test_bwd_degenerate_transitions(lib, kind):
     else:
         x["w"] = torch.zeros_like(x["w"])
     g = torch.Generator(device="cpu").manual_seed(32)
-    d_out = torch.randn((1, 2, 200, 64), generator=g).cuda()
+    d_out = torch.randn((1, 2, 200, 64), generator=g).to(dtype).cuda()
     out, lse = lib.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"])
     grads = lib.path_attn_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], out, lse, d_out)
     torch.cuda.synchronize()
     if kind == "identity":
         assert torch.count_nonzero(grads["dw"]) == 0 and torch.count_nonzero(grads["dbeta"]) == 0
     ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
-    _compare(grads, ref, 1e-4)
+    _compare(grads, ref, TOL[dtype])
 
 
 def test_bwd_long_head_fp32(lib):
@@ -310,8 +312,9 @@ def test_fox_bwd_d128_matches_oracle(lib, B, H, L, dtype, gate_scale):
     _compare(grads, ref, TOL[dtype])
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("kind", ["projection", "reflection", "identity"])
-def test_bwd_d128_degenerate_transitions(lib, kind):
+def test_bwd_d128_degenerate_transitions(lib, kind, dtype):
     # beta = 1 (singular projections), beta = 2 (reflections), w = 0 (H = I), at d = 128
     def mutate(x):
         if kind == "projection":
@@ -320,13 +323,12 @@ def test_bwd_d128_degenerate_transitions(lib, kind):
             x["beta"] = torch.full_like(x["beta"], 2.0)
         else:
             x["w"] = torch.zeros_like(x["w"])
-    x0 = pi.make_fwd_inputs(1, 2, 200, d=128, seed=3200, dtype=torch.float32, clip=0.0,
-                            device="cuda")
-    x, d_out, grads = _case128(lib, 1, 2, 200, torch.float32, seed=3200, mutate=mutate, x=x0)
+    x0 = pi.make_fwd_inputs(1, 2, 200, d=128, seed=3200, dtype=dtype, clip=0.0, device="cuda")
+    x, d_out, grads = _case128(lib, 1, 2, 200, dtype, seed=3200, mutate=mutate, x=x0)
     if kind == "identity":
         assert torch.count_nonzero(grads["dw"]) == 0 and torch.count_nonzero(grads["dbeta"]) == 0
     ref = oracle.path_bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], d_out)
-    _compare(grads, ref, 1e-4)
+    _compare(grads, ref, TOL[dtype])
 
 
 @pytest.mark.parametrize("fox", [False, True])
