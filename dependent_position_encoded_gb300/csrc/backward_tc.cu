@@ -182,7 +182,7 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     float *__restrict__ dv, const float *__restrict__ loc,
                     const double *__restrict__ cb, float *__restrict__ rsum,
                     float *__restrict__ csum, int L, int Lp, int nblk, int nbe, float scale,
-                    float scale_log2, uint32_t *status, uint64_t limit_ns) {
+                    float scale_log2, uint32_t *status, uint64_t limit_ns, int heads_fast) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -194,8 +194,9 @@ bwd_query_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int npair = nbe >> 1;
-    const int t = npair - 1 - (int)blockIdx.x;  // longest walks first
-    const int bh = blockIdx.y;
+    // longest walks first, heads fastest or head by head (heads_fastest)
+    const int t = npair - 1 - (int)(heads_fast ? blockIdx.y : blockIdx.x);
+    const int bh = heads_fast ? blockIdx.x : blockIdx.y;
     const int steps1 = 2 * t + 2, steps2 = 2 * t + 1;
     const size_t rec0 = (size_t)t * t;  // first stash record of this tile within the head
     const Wait wait{abort_f, status, limit_ns};
@@ -816,13 +817,15 @@ cudaError_t launch_path_bwd_tc(const void *q, const void *k, const void *v, cons
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
         return e;
-    const dim3 grid(y.nbe / 2, y.BH);
+    // shared per token: [K~_b; P_b] (256 B) and v (128 B)
+    const bool hf = heads_fastest((size_t)y.BH, (size_t)L, 384);
+    const dim3 grid = hf ? dim3(y.BH, y.nbe / 2) : dim3(y.nbe / 2, y.BH);
     kern<<<grid, kThr, smem, stream>>>(
         tqt, tkp, tv, tdo, tst, static_cast<const __nv_bfloat16 *>(o),
         static_cast<const __nv_bfloat16 *>(dout), lse,
         reinterpret_cast<const __half *>(base + f.off_dg), stash, dqt, dkt, dPb, dTd, dv, loc, cb,
         rs, cs, L, y.Lp, y.nblk, y.nbe, scale, scale * kLog2e, reinterpret_cast<uint32_t *>(base),
-        limit_ns);
+        limit_ns, hf ? 1 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_bwd_block_mm(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, y.BH, L,
                                  y.Lp, y.nblk, stream)) != cudaSuccess)

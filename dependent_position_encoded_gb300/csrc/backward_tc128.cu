@@ -230,7 +230,7 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
                         __nv_bfloat16 *__restrict__ stash, float *__restrict__ dv, int L, int Lp,
                         int nb, int nblk_p, int Lp_p, float scale, float scale_log2,
                         const float *__restrict__ loc, const double *__restrict__ cb,
-                        float *__restrict__ rsum, float *__restrict__ csum) {
+                        float *__restrict__ rsum, float *__restrict__ csum, int heads_fast) {
     extern __shared__ __align__(128) uint8_t sm[];
     const uint32_t sb = smem_u32(sm);
     auto tile = [&](int t) { return sb + (uint32_t)t * kTile; };
@@ -242,7 +242,11 @@ bwd_query128_mma_kernel(const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 1, wn = warp & 1, g = lane >> 2, t4 = lane & 3;
-    const int a = nb - 1 - (int)blockIdx.x, bh = blockIdx.y;
+    // a one-dimensional grid over (query block, head), longest walks first, heads fastest or
+    // head by head (heads_fastest)
+    const unsigned BH = gridDim.x / (unsigned)nb;
+    const int a = nb - 1 - (int)(heads_fast ? blockIdx.x / BH : blockIdx.x % (unsigned)nb);
+    const int bh = (int)(heads_fast ? blockIdx.x % BH : blockIdx.x / (unsigned)nb);
     const int t0 = a * 64;
     const int nq = min(64, L - t0);  // query rows of this block below L
     const size_t hL = (size_t)bh * L;
@@ -648,14 +652,17 @@ cudaError_t launch_path_bwd128_tc(const void *q, const void *k, const void *v, c
     if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem)) !=
         cudaSuccess)
         return e;
-    kq<<<dim3(nb, BH), kThr, kSmem, stream>>>(
+    if ((size_t)BH * nb > 0x7fffffffu) return cudaErrorInvalidConfiguration;
+    // shared per token: [K~_b; P_b] (768 B) and v (256 B)
+    const bool hf = heads_fastest((size_t)BH, (size_t)L, 1024);
+    kq<<<(unsigned)(BH * nb), kThr, kSmem, stream>>>(
         static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(o),
         static_cast<const __nv_bfloat16 *>(dout), lse,
         reinterpret_cast<const __nv_bfloat16 *>(base + y.f.off_qt),
         reinterpret_cast<const __nv_bfloat16 *>(base + y.f.off_kp),
         reinterpret_cast<const __half *>(base + y.f.off_dg), dqt, dkt, dPb, dTd,
         reinterpret_cast<__nv_bfloat16 *>(base + y.off_stash), dv, L, Lp, nb, y.f.nblk, y.f.Lp,
-        scale, scale * kLog2e, loc, cb, rs, cs);
+        scale, scale * kLog2e, loc, cb, rs, cs, hf ? 1 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_bwd_block_mm128(q, k, w, beta, dqt, dkt, dPb, dTd, dq, dk, dw, dbeta, BH, L,
                                     Lp, nb, stream)) != cudaSuccess)

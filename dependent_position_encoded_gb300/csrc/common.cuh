@@ -42,6 +42,16 @@ struct FwdLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Launch order of the kernels whose CTAs walk key blocks for longer the later their query
+// tile (every such grid lists each head's tiles longest walk first). When the operands that
+// a head's CTAs share (shared_bytes_per_token for every token of every head) fit in about
+// three quarters of L2, heads go fastest, so that the longest walks of all heads start first and
+// the end of the launch is made of short walks. Otherwise CTAs run head by head, so that
+// the CTAs resident together share their key blocks in L2.
+inline bool heads_fastest(size_t BH, size_t L, size_t shared_bytes_per_token) {
+    return BH * L * shared_bytes_per_token <= ((size_t)96 << 20);
+}
+
 // Workspace of the d = 128 forward (defined in fwd_d128.cu).
 struct D128Layout {
     int BH, nblk, Lp;

@@ -145,7 +145,7 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
                     const __grid_constant__ CUtensorMap tm_v128,
                     const __half *__restrict__ dg, __nv_bfloat16 *__restrict__ out,
                     float *__restrict__ lse, int L, int nblk, float scale_log2,
-                    uint32_t *status, uint64_t limit_ns, int force_timeout) {
+                    uint32_t *status, uint64_t limit_ns, int force_timeout, int heads_fast) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -154,8 +154,9 @@ path_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_qt,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntile = nblk >> 1;                   // tiles = key-block pairs
     const int ncta = (ntile + 1) >> 1;
-    const int pair = ncta - 1 - (int)blockIdx.x;   // heaviest tile pairs first
-    const int bh = blockIdx.y;
+    // the heaviest tile pairs first, heads fastest or head by head (heads_fastest)
+    const int pair = ncta - 1 - (int)(heads_fast ? blockIdx.y : blockIdx.x);
+    const int bh = heads_fast ? blockIdx.x : blockIdx.y;
     const bool hasB = 2 * pair + 1 < ntile;
     const int top = hasB ? 2 * pair + 1 : 2 * pair;  // first key-block pair of the stream
     const int nstream = top + 1;
@@ -646,12 +647,14 @@ cudaError_t launch_scan_tc(const void *v, void *out, float *lse, int BH, int L, 
                                (int)kScanSmemBytes);
     if (err != cudaSuccess) return err;
     const int ntile = lay.nblk / 2;
-    dim3 grid((ntile + 1) / 2, BH);
+    // shared per token: [K^; K~; Pi] (192 B) and v (128 B)
+    const bool hf = heads_fastest((size_t)BH, (size_t)L, 320);
+    const dim3 grid = hf ? dim3(BH, (ntile + 1) / 2) : dim3((ntile + 1) / 2, BH);
     kern<<<grid, kScanThreads, kScanSmemBytes, stream>>>(
         tm_qt, tm_kp128, tm_kp64, tm_pr64, tm_v128,
         reinterpret_cast<const __half *>(basep + lay.off_dg), static_cast<__nv_bfloat16 *>(out),
         lse, L, lay.nblk, scale * kLog2e,
-        reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout);
+        reinterpret_cast<uint32_t *>(basep), limit_ns, force_timeout, hf ? 1 : 0);
     return cudaGetLastError();
 }
 

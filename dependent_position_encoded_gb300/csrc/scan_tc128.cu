@@ -120,7 +120,7 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
                   const double *__restrict__ tot2, const int *__restrict__ first_blk,
                   __nv_bfloat16 *__restrict__ out,
                   float *__restrict__ lse, int L, int Lp, int nblk, float scale_log2,
-                  uint32_t *status, uint64_t limit_ns) {
+                  uint32_t *status, uint64_t limit_ns, int heads_fast) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -131,8 +131,9 @@ scan_tc128_kernel(const __grid_constant__ CUtensorMap tm_qt,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int npair = nblk >> 1;
-    const int t = npair - 1 - (int)blockIdx.x;  // longest walks first
-    const int bh = blockIdx.y;
+    // longest walks first, heads fastest or head by head (heads_fastest)
+    const int t = npair - 1 - (int)(heads_fast ? blockIdx.y : blockIdx.x);
+    const int bh = heads_fast ? blockIdx.x : blockIdx.y;
     // key blocks 2t+1 down to 0, or for PaTH-FoX down to the lower early-exit extent of the
     // tile's two query blocks (never above block 2t, its own lower diagonal block)
     int lo = 0;
@@ -433,14 +434,16 @@ cudaError_t launch_scan_tc128(const void *v, void *out, float *lse, bool fox, in
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(y.nblk / 2, BH), kThr, kSmem, stream>>>(
+    // shared per token: [K~_b; P_b] (768 B) and v (256 B)
+    const bool hf = heads_fastest((size_t)BH, (size_t)L, 1024);
+    kern<<<hf ? dim3(BH, y.nblk / 2) : dim3(y.nblk / 2, BH), kThr, kSmem, stream>>>(
         tq, tk, tv, reinterpret_cast<const __half *>(base + y.off_dg),
         fox ? reinterpret_cast<const float *>(base + y.off_lc2) : nullptr,
         fox ? reinterpret_cast<const float *>(base + y.off_tail2) : nullptr,
         fox ? reinterpret_cast<const double *>(base + y.off_tot2) : nullptr,
         fox ? reinterpret_cast<const int *>(base + y.off_first) : nullptr,
         static_cast<__nv_bfloat16 *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e,
-        reinterpret_cast<uint32_t *>(base), limit_ns);
+        reinterpret_cast<uint32_t *>(base), limit_ns, hf ? 1 : 0);
     return cudaGetLastError();
 }
 
