@@ -505,7 +505,7 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
                  const float *__restrict__ tail, const double *__restrict__ tot,
                  const double *__restrict__ cst, const double *__restrict__ mpre,
                  const float *__restrict__ kpre, T *__restrict__ out, float *__restrict__ lse,
-                 int L, int Lp, int nblk, float scale_log2) {
+                 int L, int Lp, int nblk, float scale_log2, int heads_fast) {
     extern __shared__ __align__(16) float sm[];
     float *Xr = sm;                 // X [i][c], 64 x LDB
     float *KB = Xr + kC * LDB;      // K~_b [j][c], 64 x LDB (slot of 128 x LDA)
@@ -517,7 +517,11 @@ scan_d128_kernel(const T *__restrict__ v, const float *__restrict__ qt, const fl
     float *rbias = alpha_s + kC;    // FoX: row terms lc_i + sum of the blocks in between
     float *kbias = rbias + kC;      // FoX: tail sums T_b - lc_j of the keys of block b
 
-    const int tid = threadIdx.x, ib = blockIdx.x, bh = blockIdx.y;
+    // longest walks (the last query blocks) first, heads fastest or head by head
+    // (heads_fastest)
+    const int tid = threadIdx.x;
+    const int ib = nblk - 1 - (int)(heads_fast ? blockIdx.y : blockIdx.x);
+    const int bh = heads_fast ? blockIdx.x : blockIdx.y;
     if (ib * kC >= L) return;
     const int ty = tid / 16, tx = tid % 16, r0 = ty, c0 = 4 * tx;
     const int row = tid >> 2, part = tid & 3;
@@ -773,13 +777,15 @@ cudaError_t launch_scan_d128(const void *v, void *out, float *lse, bool fox, int
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) !=
         cudaSuccess)
         return e;
-    kern<<<dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
+    // shared per token: k~ (512 B), P_b rows (1 KB), v (512 B)
+    const bool hf = heads_fastest((size_t)y.BH, (size_t)L, 2048);
+    kern<<<hf ? dim3(y.BH, y.nblk) : dim3(y.nblk, y.BH), kThreads, sm, stream>>>(
         static_cast<const T *>(v), reinterpret_cast<const float *>(base + y.off_qt),
         reinterpret_cast<const float *>(base + y.off_kp), reinterpret_cast<const float *>(base + y.off_dg),
         reinterpret_cast<const float *>(base + y.off_lc), reinterpret_cast<const float *>(base + y.off_tail),
         reinterpret_cast<const double *>(base + y.off_tot), reinterpret_cast<const double *>(base + y.off_cst),
         reinterpret_cast<const double *>(base + y.off_mpre), reinterpret_cast<const float *>(base + y.off_kpre),
-        static_cast<T *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e);
+        static_cast<T *>(out), lse, L, y.Lp, y.nblk, scale * kLog2e, hf ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -94,7 +94,7 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
                      const float *__restrict__ c2, const float *__restrict__ pbase,
                      const int *__restrict__ first_blk,
                      float *__restrict__ out, float *__restrict__ lse, int L, int Lp, int nblk,
-                     float scale_log2) {
+                     float scale_log2, int heads_fast) {
     extern __shared__ __align__(16) float sm[];
     float *Xr = sm;          // state X[i][c]
     float *KB = Xr + BUF;    // k~_b [j][c]
@@ -106,8 +106,11 @@ path_scan_f32_kernel(const float *__restrict__ v, const float *__restrict__ qt,
     float *c2k = alpha_s + kC;
 
     const int tid = threadIdx.x;
-    const int ib = blockIdx.x;
-    const int bh = blockIdx.y;
+    // longest walks (the last query blocks) first, heads fastest or head by head
+    // (heads_fastest)
+    const int nq = (int)(heads_fast ? gridDim.y : gridDim.x);
+    const int ib = nq - 1 - (int)(heads_fast ? blockIdx.y : blockIdx.x);
+    const int bh = heads_fast ? blockIdx.x : blockIdx.y;
     if (ib * kC >= L) return;
     const size_t head = (size_t)bh;
     const int ty = tid / 16, tx = tid % 16, c0 = 4 * tx;
@@ -234,7 +237,10 @@ cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int 
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid((L + kC - 1) / kC, BH);
+    // shared per token: k~, P_b rows and v (256 B each)
+    const bool hf = heads_fastest((size_t)BH, (size_t)L, 768);
+    const int nq = (L + kC - 1) / kC;
+    const dim3 grid = hf ? dim3(BH, nq) : dim3(nq, BH);
     kern<<<grid, kThreads, smem, stream>>>(
         static_cast<const float *>(v), reinterpret_cast<const float *>(basep + lay.off_qt),
         reinterpret_cast<const float *>(basep + lay.off_kp),
@@ -242,7 +248,7 @@ cudaError_t launch_scan_f32(const void *v, void *out, float *lse, bool fox, int 
         fox ? reinterpret_cast<const float *>(basep + lay.off_c2) : nullptr,
         fox ? reinterpret_cast<const float *>(basep + lay.off_pbase) : nullptr,
         fox ? reinterpret_cast<const int *>(basep + lay.off_fb) : nullptr,
-        static_cast<float *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e);
+        static_cast<float *>(out), lse, L, lay.Lp, lay.nblk, scale * kLog2e, hf ? 1 : 0);
     return cudaGetLastError();
 }
 
