@@ -444,7 +444,7 @@ prep_d128_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__re
 }
 
 // ---------------------------------------------------------------- PaTH-FoX exit bounds
-// One warp per head, 32 blocks per round: C_b = sum of the totals of blocks 0..b-1 (fp64),
+// One warp per head, 32 blocks per iteration: C_b = sum of the totals of blocks 0..b-1 (fp64),
 // Mpre(b) = min over blocks b' <= b of C_b' + (smallest in-block sum of b'), and Kpre(b) =
 // max over blocks b' <= b of the block's largest |k~_j|; all in log2 units.
 __global__ void __launch_bounds__(128)
@@ -461,7 +461,7 @@ fox_bounds_d128_kernel(const double *__restrict__ tot, const double *__restrict_
         const int b = b0 + lane;
         const bool in = b < nblk;
         const double t = in ? tot[h0 + b] : 0.0;
-        double inc = t;  // inclusive prefix of the totals within this round
+        double inc = t;  // inclusive prefix of the totals within these 32 blocks
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const double y = __shfl_up_sync(0xffffffffu, inc, o);
