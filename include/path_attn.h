@@ -145,12 +145,13 @@ path_status path_fwd_prepare(const void *q, const void *k, const void *w, const 
  *   scale      : the forward's softmax scale (finite)
  *   ws         : ws_bytes >= path_workspace_bytes(PATH_OP_BWD, B, H, L, d, dtype), which
  *                grows as B H (L / 64)^2 (the query pass keeps every carried query block
- *                and its logit gradient: about 32 KB per block pair for fp32 inputs at
- *                d = 64, e.g. 1.0 GB at B H = 64, L = 2048, and 48 KB at d = 128)
- * Gradients are fp32 whatever dtype is (bf16 inputs are widened on load). At d = 64, bf16
- * inputs take bf16 tensor-core products with fp32 accumulation in the query pass and tf32
- * products in the block pass; fp32 inputs, and every input at d = 128, take fp32 products
- * throughout. w is used as given (no renormalisation). Gradients of several query blocks meet in dv and in
+ *                and its logit gradient: per block pair 32 KB for fp32 inputs at d = 64,
+ *                e.g. 1.0 GB at B H = 64, L = 2048, and 48 KB at d = 128; half of that for
+ *                bf16 inputs, which keep them in bf16)
+ * Gradients are fp32 whatever dtype is (bf16 inputs are widened on load). bf16 inputs take
+ * bf16 tensor-core products with fp32 accumulation in the query pass (tcgen05 at d = 64,
+ * warp-level MMAs at d = 128) and tf32 tensor-core products in the block pass; fp32 inputs
+ * take fp32 products throughout. w is used as given (no renormalisation). Gradients of several query blocks meet in dv and in
  * internal per-block sums through fp32 atomic adds, so their rounding order (not their
  * value beyond fp32 rounding) varies between runs. Outputs are written from zero: no
  * accumulation into the caller's buffers.
