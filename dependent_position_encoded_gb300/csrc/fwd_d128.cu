@@ -64,12 +64,6 @@ __device__ __forceinline__ void zero(float (&a)[4][4]) {
         for (int j = 0; j < 4; ++j) a[i][j] = 0.f;
 }
 
-__device__ __forceinline__ void store4(float *Z, int ld, int m0, int n0, const float (&a)[4][4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4 *>(Z + (m0 + i) * ld + n0) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
-}
-
 // rows x 128 fp32 tile (row-major, 128 floats per row) into shared memory rows of stride
 // ld; eight 16-byte loads in flight per thread before the first store
 __device__ __forceinline__ void load128(float *dst, int ld, const float *__restrict__ src, int rows) {
@@ -92,23 +86,12 @@ __device__ __forceinline__ void load128(float *dst, int ld, const float *__restr
     }
 }
 
-// four consecutive elements of type T, widened
+// four consecutive elements (the kernels are instantiated for fp32 inputs)
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
-__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(p);
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
 
 template <typename T> __device__ __forceinline__ void put4(T *dst, const float *v);
 template <> __device__ __forceinline__ void put4<float>(float *dst, const float *v) {
     *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-}
-template <> __device__ __forceinline__ void put4<__nv_bfloat16>(__nv_bfloat16 *dst, const float *v) {
-    uint2 u;
-    u.x = pack_bf16x2(v[0], v[1]);
-    u.y = pack_bf16x2(v[2], v[3]);
-    *reinterpret_cast<uint2 *>(dst) = u;
 }
 
 // ---------------------------------------------------------------- register-tiled products
