@@ -121,6 +121,19 @@ def compact(obj, sig=5):
     return obj
 
 
+# Legs that end the JSON line, in this order: a reader that keeps only the line's end (the
+# last 3 KB) still finds them.
+LINE_END = ("fwd_d128", "bwd", "bwd_d128", "decode", "fox", "sweep_L")
+
+
+def order_line(line):
+    """The line's keys in print order: everything else first (insertion order), then the
+    LINE_END legs that are present."""
+    ordered = {k: v for k, v in line.items() if k not in LINE_END}
+    ordered.update({k: line[k] for k in LINE_END if k in line})
+    return ordered
+
+
 def kernel_source_hash(name):
     src = os.path.join(ROOT, "dependent_position_encoded_gb300", "csrc", name)
     with open(src, "rb") as f:
@@ -988,11 +1001,7 @@ def main():
         line = dict(head)
         line.update(legs)
         line.update(tail)
-        # the legs a reader of the line's end should find there come last
-        last = ("fwd_d128", "bwd", "bwd_d128", "decode", "fox", "sweep_L")
-        ordered = {k: v for k, v in line.items() if k not in last}
-        ordered.update({k: line[k] for k in last if k in line})
-        print(json.dumps(compact(ordered)))
+        print(json.dumps(compact(order_line(line))))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -58,3 +58,17 @@ def test_single_rank_is_local():
     assert (t_max, ms_step) == (8.0, 4.0)
     assert value == pytest.approx(32 * 4096 * 2 / 8e-3)
     assert bench.shard_workload(pi.BF16_L4096, 0) is pi.BF16_L4096
+
+
+def test_line_order_ends_with_the_headline_legs():
+    # the legs a reader of the line's last 3 KB needs come last, in LINE_END order; the
+    # contract keys keep their place at the front
+    line = {"metric": "m", "value": 1.0, "sweep_L": {}, "bwd": {}, "producer": {},
+            "fox": {}, "decode": {}, "fwd_f32": {}, "bwd_d128": {}, "fwd_d128": {}}
+    keys = list(bench.order_line(line))
+    assert keys[:2] == ["metric", "value"]
+    assert keys[-6:] == list(bench.LINE_END)
+    assert set(keys) == set(line)
+    # absent legs are skipped, not invented
+    assert list(bench.order_line({"metric": "m", "fox": {}})) == ["metric", "fox"]
+
